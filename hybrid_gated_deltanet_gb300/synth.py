@@ -1,0 +1,198 @@
+"""Seeded synthetic inputs for the Gated DeltaNet layer.
+
+This module only draws random numbers and stores them in the storage dtypes
+the layer reads (bf16 or fp32).  It holds none of the layer's arithmetic: no
+convolution, normalisation, gate or recurrence is computed here.  Both the CUDA
+path (through the Python binding) and the CPU oracle (tests only) receive the
+arrays produced here, so the two sides see bit-identical inputs.
+
+Shapes follow the statement of the layer on the pages:
+
+* "Hybrid transformers under load: where Gated DeltaNet loses to full
+  attention" (braintools.ru), section 4.1: the Qwen3.5-4B state is
+  32 x 128 x 128 fp32 (2,097,152 B) plus a 49,152 B conv part per layer, i.e.
+  16 k-heads, 32 v-heads, d = 128, 8192 conv channels and 3 stored conv rows in
+  bf16.
+* "Chapter 6: engine start-up and memory plan" (Strata), section 6.2,
+  ModelGeometry: 16 k-heads, 48 v-heads, d_state 128, d_conv 4, 10240 conv
+  channels = 2*128*16 + 128*48.
+
+Rounding: values are drawn in fp64 with numpy's PCG64, rounded to fp32 (RNE)
+and, for bf16 storage, rounded again fp32 -> bf16 (RNE on the bit pattern).
+The decoded values (exact in fp64) are what the oracle consumes.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Dict, List, Optional
+
+import numpy as np
+
+BF16 = "bf16"
+F32 = "f32"
+
+
+# ----------------------------------------------------------------------------
+# storage-dtype helpers (pure bit manipulation, no layer arithmetic)
+# ----------------------------------------------------------------------------
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round fp32 values to bf16 (round-to-nearest-even); returns uint16 bits."""
+    f = np.ascontiguousarray(a, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    bias = 0x7FFF + ((u >> 16) & 1)
+    return ((u + bias) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact decode of bf16 bit patterns to fp64."""
+    u = np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32).astype(np.float64)
+
+
+@dataclasses.dataclass
+class Stored:
+    """An array in its storage dtype plus its exact fp64 value.
+
+    ``raw`` is what the GPU receives: uint16 bit patterns for bf16, float32
+    otherwise.  ``f64`` is the same numbers decoded exactly.
+    """
+
+    raw: np.ndarray
+    f64: np.ndarray
+    dtype: str
+
+    @property
+    def shape(self):
+        return self.raw.shape
+
+
+def store(values: np.ndarray, dtype: str) -> Stored:
+    f32 = np.asarray(values, dtype=np.float64).astype(np.float32)
+    if dtype == BF16:
+        bits = f32_to_bf16_bits(f32)
+        return Stored(bits, bf16_bits_to_f64(bits), BF16)
+    if dtype == F32:
+        return Stored(np.ascontiguousarray(f32), f32.astype(np.float64), F32)
+    raise ValueError(f"unknown storage dtype {dtype!r}")
+
+
+# ----------------------------------------------------------------------------
+# geometry
+# ----------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class Geometry:
+    n_k_heads: int
+    n_v_heads: int
+    d_k: int
+    d_v: int
+    d_conv: int = 4
+
+    @property
+    def group(self) -> int:
+        return self.n_v_heads // self.n_k_heads
+
+    @property
+    def conv_channels(self) -> int:
+        # [q | k | v] channel order, head-major
+        return 2 * self.n_k_heads * self.d_k + self.n_v_heads * self.d_v
+
+    @property
+    def value_dim(self) -> int:
+        return self.n_v_heads * self.d_v
+
+    def state_bytes_per_slot(self) -> int:
+        return self.n_v_heads * self.d_v * self.d_k * 4
+
+    def conv_state_bytes_per_slot(self, act_dtype: str) -> int:
+        return (self.d_conv - 1) * self.conv_channels * (2 if act_dtype == BF16 else 4)
+
+
+QWEN35_4B = Geometry(16, 32, 128, 128, 4)   # braintools.ru, section 4.1
+WIDE_GVA = Geometry(16, 48, 128, 128, 4)    # Strata chapter 6, section 6.2
+TINY = Geometry(2, 2, 32, 32, 4)
+
+
+# ----------------------------------------------------------------------------
+# generators
+# ----------------------------------------------------------------------------
+def make_params(geom: Geometry, rng: np.random.Generator, act_dtype: str) -> Dict[str, Stored]:
+    """Per-layer parameters.
+
+    conv_w ~ U(-1/2, 1/2) (= +-1/sqrt(d_conv) for d_conv = 4), A_log ~ U(0, ln 16)
+    per v-head, norm_w = 1 + 0.1 N(0,1).  No conv bias, no dt_bias.
+    """
+    C = geom.conv_channels
+    conv_w = rng.uniform(-0.5, 0.5, size=(C, geom.d_conv))
+    A_log = rng.uniform(0.0, math.log(16.0), size=(geom.n_v_heads,))
+    norm_w = 1.0 + 0.1 * rng.standard_normal(geom.d_v)
+    return {
+        "conv_w": store(conv_w, act_dtype),
+        "A_log": store(A_log, F32),
+        "norm_w": store(norm_w, act_dtype),
+    }
+
+
+def make_tokens(geom: Geometry, n_tok: int, rng: np.random.Generator, act_dtype: str,
+                x_std: float = 1.0) -> Dict[str, Stored]:
+    """Per-token layer inputs: x (pre-conv [q|k|v]), z, a, b, all ~ N(0,1)."""
+    C = geom.conv_channels
+    x = x_std * rng.standard_normal((n_tok, C))
+    z = rng.standard_normal((n_tok, geom.value_dim))
+    a = rng.standard_normal((n_tok, geom.n_v_heads))
+    b = rng.standard_normal((n_tok, geom.n_v_heads))
+    return {"x": store(x, act_dtype), "z": store(z, act_dtype),
+            "a": store(a, act_dtype), "b": store(b, act_dtype)}
+
+
+def make_state(geom: Geometry, n_slots: int, rng: np.random.Generator, std: float = 0.1) -> Stored:
+    """fp32 recurrent states [n_slots, H_v, d_v, d_k] ~ N(0, std^2)."""
+    s = std * rng.standard_normal((n_slots, geom.n_v_heads, geom.d_v, geom.d_k))
+    return store(s, F32)
+
+
+def make_conv_state(geom: Geometry, n_slots: int, rng: np.random.Generator, act_dtype: str,
+                    std: float = 0.1) -> Stored:
+    """Conv states [n_slots, d_conv-1, C_ch] ~ N(0, std^2) in the act dtype."""
+    c = std * rng.standard_normal((n_slots, geom.d_conv - 1, geom.conv_channels))
+    return store(c, act_dtype)
+
+
+def log_uniform_lengths(rng: np.random.Generator, n: int, lo: int, hi: int) -> List[int]:
+    """floor(exp(U(ln lo, ln hi))) sequence lengths."""
+    return [int(math.floor(math.exp(v))) for v in rng.uniform(math.log(lo), math.log(hi), size=n)]
+
+
+def orthonormal_rows(rng: np.random.Generator, n: int, d: int) -> np.ndarray:
+    """n <= d orthonormal rows (from the QR factor of a Gaussian matrix)."""
+    qm, _ = np.linalg.qr(rng.standard_normal((d, d)))
+    return np.ascontiguousarray(qm[:, :n].T)
+
+
+# ----------------------------------------------------------------------------
+# named workloads (shapes and distributions of the pages' models)
+# ----------------------------------------------------------------------------
+@dataclasses.dataclass
+class Workload:
+    name: str
+    geom: Geometry
+    act_dtype: str
+    chunk: int
+    seed: int
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny: 1 seq, T=64, 2/2 heads, d=32, fp32, chunk 16", TINY, F32, 16, 0),
+    "decode4b": Workload("Qwen3.5-4B-like decode: 16/32 heads, d=128, bf16, fp32 state",
+                         QWEN35_4B, BF16, 64, 1),
+    "prefill4b": Workload("chunked prefill: 1 seq, T=8192, 16/32 heads, d=128, bf16, chunk 64",
+                          QWEN35_4B, BF16, 64, 2),
+    "wide": Workload("wide GVA: 16/48 heads, d=128, 10240 conv channels, bf16", WIDE_GVA, BF16, 64, 3),
+    "serving": Workload("serving mix: varlen 20 seqs log-U[500,30000] + decode 256 slots",
+                        QWEN35_4B, BF16, 64, 4),
+}
+
+
+def rng_for(seed: int, stream: int = 0) -> np.random.Generator:
+    """Independent seeded streams: (seed, stream) -> PCG64."""
+    return np.random.Generator(np.random.PCG64([seed, stream]))
