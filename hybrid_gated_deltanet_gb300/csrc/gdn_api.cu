@@ -1,0 +1,291 @@
+// gdn_api.cu -- the exported C ABI of libgdn (see include/gdn.h).
+//
+// Every entry point validates its arguments on the host, then launches on the
+// caller's stream.  Nothing here allocates device memory or synchronises.
+// Error messages follow the Strata convention (chapter 6, sections 6.2 and
+// 6.5): name the argument, the value found and the value required.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+gdn_status fail(gdn_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+gdn_status ok() {
+    g_last_error.clear();
+    return GDN_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define GDN_REQUIRE_PTR(p, name)                                                          \
+    do {                                                                                  \
+        if (!(p)) return fail(GDN_ERR_NULL, "%s: found NULL, required a device pointer", name); \
+        if (!aligned16(p))                                                                \
+            return fail(GDN_ERR_ALIGN, "%s: found address %p, required 16-byte alignment", name, \
+                        (const void*)(p));                                                \
+    } while (0)
+
+#define GDN_OPTIONAL_PTR(p, name)                                                         \
+    do {                                                                                  \
+        if ((p) && !aligned16(p))                                                         \
+            return fail(GDN_ERR_ALIGN, "%s: found address %p, required 16-byte alignment", name, \
+                        (const void*)(p));                                                \
+    } while (0)
+
+gdn_status make_geom(const gdn_config* cfg, bool need_chunk, gdn::Geom* g) {
+    if (!cfg) return fail(GDN_ERR_NULL, "cfg: found NULL, required a gdn_config");
+    if (cfg->act_dtype != GDN_DTYPE_BF16 && cfg->act_dtype != GDN_DTYPE_F32)
+        return fail(GDN_ERR_DTYPE, "cfg.act_dtype: found %d, required GDN_DTYPE_BF16 (0) or GDN_DTYPE_F32 (1)",
+                    cfg->act_dtype);
+    if (cfg->n_k_heads < 1 || cfg->n_v_heads < 1)
+        return fail(GDN_ERR_SHAPE, "cfg.n_k_heads/n_v_heads: found %d/%d, required >= 1", cfg->n_k_heads,
+                    cfg->n_v_heads);
+    if (cfg->n_v_heads % cfg->n_k_heads != 0)
+        return fail(GDN_ERR_SHAPE, "cfg.n_v_heads: found %d, required a multiple of n_k_heads = %d",
+                    cfg->n_v_heads, cfg->n_k_heads);
+    const int G = cfg->n_v_heads / cfg->n_k_heads;
+    if (G > 8) return fail(GDN_ERR_UNSUPPORTED, "cfg.n_v_heads/n_k_heads: found %d, required <= 8", G);
+    if (cfg->d_k != 32 && cfg->d_k != 64 && cfg->d_k != 128)
+        return fail(GDN_ERR_SHAPE, "cfg.d_k: found %d, required 32, 64 or 128", cfg->d_k);
+    if (cfg->d_v != 32 && cfg->d_v != 64 && cfg->d_v != 128)
+        return fail(GDN_ERR_SHAPE, "cfg.d_v: found %d, required 32, 64 or 128", cfg->d_v);
+    if (cfg->d_k != cfg->d_v)
+        return fail(GDN_ERR_UNSUPPORTED, "cfg.d_v: found %d, required d_v == d_k = %d", cfg->d_v, cfg->d_k);
+    if (cfg->d_conv < 2 || cfg->d_conv > 4)
+        return fail(GDN_ERR_SHAPE, "cfg.d_conv: found %d, required 2..4", cfg->d_conv);
+    if (need_chunk && cfg->chunk != 16 && cfg->chunk != 32 && cfg->chunk != 64)
+        return fail(GDN_ERR_SHAPE, "cfg.chunk: found %d, required 16, 32 or 64", cfg->chunk);
+    if (!(cfg->l2_eps >= 0.f) || !(cfg->norm_eps >= 0.f))
+        return fail(GDN_ERR_SHAPE, "cfg.l2_eps/norm_eps: found %g/%g, required >= 0", (double)cfg->l2_eps,
+                    (double)cfg->norm_eps);
+    if (cfg->flags & ~15u) return fail(GDN_ERR_SHAPE, "cfg.flags: found 0x%x, required a subset of 0xf", cfg->flags);
+    g->Hk = cfg->n_k_heads;
+    g->Hv = cfg->n_v_heads;
+    g->D = cfg->d_k;
+    g->K = cfg->d_conv;
+    g->G = G;
+    g->C_ch = 2 * cfg->n_k_heads * cfg->d_k + cfg->n_v_heads * cfg->d_v;
+    g->chunk = cfg->chunk;
+    g->act_bf16 = cfg->act_dtype == GDN_DTYPE_BF16;
+    g->q_scale = cfg->q_scale;
+    g->l2_eps = cfg->l2_eps;
+    g->norm_eps = cfg->norm_eps;
+    g->flags = cfg->flags;
+    return GDN_OK;
+}
+
+gdn_status make_params(const gdn_params* prm, const gdn::Geom& g, bool need_all, gdn::LayerParams* p) {
+    if (!prm) return fail(GDN_ERR_NULL, "prm: found NULL, required a gdn_params");
+    const bool conv = !(g.flags & GDN_FLAG_RAW_QKV);
+    const bool gates = !(g.flags & GDN_FLAG_GATES_DIRECT);
+    const bool norm = !(g.flags & GDN_FLAG_NO_OUTNORM);
+    if (conv || !need_all) GDN_REQUIRE_PTR(prm->conv_w, "prm.conv_w");
+    else GDN_OPTIONAL_PTR(prm->conv_w, "prm.conv_w");
+    GDN_OPTIONAL_PTR(prm->conv_b, "prm.conv_b");
+    if (need_all && gates) GDN_REQUIRE_PTR(prm->A_log, "prm.A_log");
+    else GDN_OPTIONAL_PTR(prm->A_log, "prm.A_log");
+    GDN_OPTIONAL_PTR(prm->dt_bias, "prm.dt_bias");
+    if (need_all && norm) GDN_REQUIRE_PTR(prm->norm_w, "prm.norm_w");
+    else GDN_OPTIONAL_PTR(prm->norm_w, "prm.norm_w");
+    p->conv_w = prm->conv_w;
+    p->conv_b = prm->conv_b;
+    p->A_log = prm->A_log;
+    p->dt_bias = prm->dt_bias;
+    p->norm_w = prm->norm_w;
+    return GDN_OK;
+}
+
+gdn_status cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return ok();
+    return fail(GDN_ERR_CUDA, "%s: CUDA error %d (%s)", what, (int)e, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdn_last_error(void) { return g_last_error.c_str(); }
+
+const char* gdn_version(void) { return "libgdn 0.1 (sm_103a)"; }
+
+size_t gdn_workspace_size(const gdn_config* cfg, int32_t op, int64_t n_tokens, int32_t n_seq) {
+    gdn::Geom g;
+    const bool prefill = op == GDN_OP_CHUNK_PREFILL || op == GDN_OP_VARLEN_PREFILL;
+    if (make_geom(cfg, prefill, &g) != GDN_OK) return 0;
+    if (n_tokens < 0 || n_seq < 0) {
+        fail(GDN_ERR_RANGE, "n_tokens/n_seq: found %lld/%d, required >= 0", (long long)n_tokens, n_seq);
+        return 0;
+    }
+    ok();
+    if (!prefill) return 0;
+    return gdn::prefill_workspace_bytes(g, n_tokens, op == GDN_OP_CHUNK_PREFILL ? 1 : n_seq);
+}
+
+gdn_status gdn_conv_state_update(const gdn_config* cfg, const gdn_params* prm, const void* x, void* conv_pool,
+                                 const int32_t* slot_idx, int32_t n_seq, int32_t n_tok, int32_t n_slots,
+                                 void* u_out, void* stream) {
+    gdn::Geom g;
+    gdn::LayerParams p;
+    gdn_status st = make_geom(cfg, false, &g);
+    if (st) return st;
+    if (n_seq < 0 || n_tok < 0 || n_slots < 1)
+        return fail(GDN_ERR_RANGE, "n_seq/n_tok/n_slots: found %d/%d/%d, required >= 0/>= 0/>= 1", n_seq, n_tok,
+                    n_slots);
+    if (n_seq > 0 && n_tok > 0) {
+        if ((st = make_params(prm, g, false, &p))) return st;
+        GDN_REQUIRE_PTR(x, "x");
+        GDN_REQUIRE_PTR(conv_pool, "conv_pool");
+        GDN_REQUIRE_PTR(slot_idx, "slot_idx");
+        GDN_OPTIONAL_PTR(u_out, "u_out");
+    } else {
+        return ok();
+    }
+    gdn::ConvJob job{x, conv_pool, slot_idx, u_out, n_seq, n_tok, n_slots};
+    return cuda_status(gdn::launch_conv_update(g, p, job, (cudaStream_t)stream), "gdn_conv_state_update");
+}
+
+static gdn_status rows_common(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* z,
+                              const void* a, const void* b, void* conv_pool, float* state_pool,
+                              const int32_t* slot_idx, const int32_t* snap_idx, int32_t B, int32_t r,
+                              int32_t n_slots, void* y, void* stream, const char* who) {
+    gdn::Geom g;
+    gdn::LayerParams p;
+    gdn_status st = make_geom(cfg, false, &g);
+    if (st) return st;
+    if (B < 0 || B > 65535) return fail(GDN_ERR_RANGE, "B: found %d, required 0..65535", B);
+    if (r < 1 || r > 16) return fail(GDN_ERR_RANGE, "r: found %d, required 1..16", r);
+    if (n_slots < 1) return fail(GDN_ERR_RANGE, "n_slots: found %d, required >= 1", n_slots);
+    if (B == 0) return ok();
+    if ((st = make_params(prm, g, true, &p))) return st;
+    GDN_REQUIRE_PTR(x, "x");
+    if (!(g.flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR(z, "z");
+    GDN_REQUIRE_PTR(a, "a");
+    GDN_REQUIRE_PTR(b, "b");
+    GDN_REQUIRE_PTR(conv_pool, "conv_pool");
+    GDN_REQUIRE_PTR(state_pool, "state_pool");
+    GDN_REQUIRE_PTR(slot_idx, "slot_idx");
+    GDN_REQUIRE_PTR(y, "y");
+    gdn::RowsJob job{x, z, a, b, conv_pool, state_pool, slot_idx, snap_idx, y, B, r, n_slots};
+    return cuda_status(gdn::launch_rows(g, p, job, (cudaStream_t)stream), who);
+}
+
+gdn_status gdn_decode_step(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* z, const void* a,
+                           const void* b, void* conv_pool, float* state_pool, const int32_t* slot_idx, int32_t B,
+                           int32_t n_slots, void* y, void* stream) {
+    return rows_common(cfg, prm, x, z, a, b, conv_pool, state_pool, slot_idx, nullptr, B, 1, n_slots, y, stream,
+                       "gdn_decode_step");
+}
+
+gdn_status gdn_verify_rows(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* z, const void* a,
+                           const void* b, void* conv_pool, float* state_pool, const int32_t* slot_idx,
+                           const int32_t* snap_idx, int32_t B, int32_t r, int32_t n_slots, void* y, void* stream) {
+    if (B > 0) GDN_REQUIRE_PTR(snap_idx, "snap_idx");
+    return rows_common(cfg, prm, x, z, a, b, conv_pool, state_pool, slot_idx, snap_idx, B, r, n_slots, y, stream,
+                       "gdn_verify_rows");
+}
+
+gdn_status gdn_commit_rows(const gdn_config* cfg, void* conv_pool, float* state_pool, const int32_t* slot_idx,
+                           const int32_t* snap_idx, const int32_t* accepted, int32_t B, int32_t r, int32_t n_slots,
+                           void* stream) {
+    gdn::Geom g;
+    gdn_status st = make_geom(cfg, false, &g);
+    if (st) return st;
+    if (B < 0 || B > 65535) return fail(GDN_ERR_RANGE, "B: found %d, required 0..65535", B);
+    if (r < 1 || r > 16) return fail(GDN_ERR_RANGE, "r: found %d, required 1..16", r);
+    if (n_slots < 1) return fail(GDN_ERR_RANGE, "n_slots: found %d, required >= 1", n_slots);
+    if (B == 0) return ok();
+    GDN_REQUIRE_PTR(conv_pool, "conv_pool");
+    GDN_REQUIRE_PTR(state_pool, "state_pool");
+    GDN_REQUIRE_PTR(slot_idx, "slot_idx");
+    GDN_REQUIRE_PTR(snap_idx, "snap_idx");
+    GDN_REQUIRE_PTR(accepted, "accepted");
+    gdn::CommitJob job{conv_pool, state_pool, slot_idx, snap_idx, accepted, B, r, n_slots};
+    return cuda_status(gdn::launch_commit(g, job, (cudaStream_t)stream), "gdn_commit_rows");
+}
+
+static gdn_status prefill_common(const gdn_config* cfg, const gdn_params* prm, gdn::PrefillJob& job, void* stream,
+                                 const char* who) {
+    gdn::Geom g;
+    gdn::LayerParams p;
+    gdn_status st = make_geom(cfg, true, &g);
+    if (st) return st;
+    if (job.n_tokens < 0 || job.n_tokens > (int64_t)1 << 31)
+        return fail(GDN_ERR_RANGE, "n_tokens: found %lld, required 0..2^31", (long long)job.n_tokens);
+    if ((st = make_params(prm, g, true, &p))) return st;
+    if (job.n_tokens > 0) {
+        GDN_REQUIRE_PTR(job.x, "x");
+        if (!(g.flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR(job.z, "z");
+        GDN_REQUIRE_PTR(job.a, "a");
+        GDN_REQUIRE_PTR(job.b, "b");
+        GDN_REQUIRE_PTR(job.y, "y");
+    }
+    const size_t need = gdn::prefill_workspace_bytes(g, job.n_tokens, job.cu_seqlens ? job.n_seq : 1);
+    if (need > 0) GDN_REQUIRE_PTR(job.workspace, "workspace");
+    if (job.ws_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace: found %zu bytes, required %zu bytes", job.ws_bytes, need);
+    return cuda_status(gdn::launch_prefill(g, p, job, (cudaStream_t)stream), who);
+}
+
+gdn_status gdn_chunk_prefill(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* z, const void* a,
+                             const void* b, int64_t T, const float* s0, const void* conv0, float* s_final,
+                             void* conv_final, void* y, void* workspace, size_t ws_bytes, void* stream) {
+    GDN_OPTIONAL_PTR(s0, "s0");
+    GDN_OPTIONAL_PTR(conv0, "conv0");
+    GDN_REQUIRE_PTR(s_final, "s_final");
+    GDN_REQUIRE_PTR(conv_final, "conv_final");
+    GDN_OPTIONAL_PTR(workspace, "workspace");
+    gdn::PrefillJob job = {};
+    job.x = x; job.z = z; job.a = a; job.b = b; job.y = y;
+    job.n_tokens = T;
+    job.n_seq = 1;
+    job.s0 = s0; job.s_final = s_final; job.conv0 = conv0; job.conv_final = conv_final;
+    job.workspace = workspace; job.ws_bytes = ws_bytes;
+    return prefill_common(cfg, prm, job, stream, "gdn_chunk_prefill");
+}
+
+gdn_status gdn_varlen_prefill(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* z, const void* a,
+                              const void* b, const int32_t* cu_seqlens, int32_t n_seq, int64_t n_tokens,
+                              const int32_t* slot_idx, const uint8_t* has_init, void* conv_pool, float* state_pool,
+                              int32_t n_slots, void* y, void* workspace, size_t ws_bytes, void* stream) {
+    if (n_seq < 0 || n_seq > 65535) return fail(GDN_ERR_RANGE, "n_seq: found %d, required 0..65535", n_seq);
+    if (n_slots < 1) return fail(GDN_ERR_RANGE, "n_slots: found %d, required >= 1", n_slots);
+    if (n_seq == 0) {
+        if (n_tokens != 0)
+            return fail(GDN_ERR_RANGE, "n_tokens: found %lld with n_seq = 0, required 0", (long long)n_tokens);
+        gdn::Geom g;
+        gdn_status st = make_geom(cfg, true, &g);
+        return st ? st : ok();
+    }
+    GDN_REQUIRE_PTR(cu_seqlens, "cu_seqlens");
+    GDN_REQUIRE_PTR(slot_idx, "slot_idx");
+    GDN_OPTIONAL_PTR(has_init, "has_init");
+    GDN_REQUIRE_PTR(conv_pool, "conv_pool");
+    GDN_REQUIRE_PTR(state_pool, "state_pool");
+    GDN_OPTIONAL_PTR(workspace, "workspace");
+    gdn::PrefillJob job = {};
+    job.x = x; job.z = z; job.a = a; job.b = b; job.y = y;
+    job.n_tokens = n_tokens;
+    job.n_seq = n_seq;
+    job.cu_seqlens = cu_seqlens;
+    job.slot_idx = slot_idx; job.has_init = has_init;
+    job.state_pool = state_pool; job.conv_pool = conv_pool; job.n_slots = n_slots;
+    job.workspace = workspace; job.ws_bytes = ws_bytes;
+    return prefill_common(cfg, prm, job, stream, "gdn_varlen_prefill");
+}
+
+}  // extern "C"

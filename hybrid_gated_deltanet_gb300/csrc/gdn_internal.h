@@ -1,0 +1,83 @@
+// gdn_internal.h -- launcher interface between the C-ABI layer (gdn_api.cu)
+// and the kernel files.  Host-only types; nothing here is exported.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+// Geometry + options after validation (all derived fields filled in).
+struct Geom {
+    int Hk, Hv, D, K, G, C_ch, chunk;
+    int act_bf16;  // 1: bf16 activations, 0: fp32
+    float q_scale, l2_eps, norm_eps;
+    uint32_t flags;
+};
+
+struct LayerParams {
+    const void* conv_w;
+    const void* conv_b;
+    const float* A_log;
+    const float* dt_bias;
+    const void* norm_w;
+};
+
+// decode (r = 1, snap_idx = NULL: in place) and verify (snap_idx [B][r])
+struct RowsJob {
+    const void *x, *z, *a, *b;
+    void* conv_pool;
+    float* state_pool;
+    const int32_t* slot_idx;
+    const int32_t* snap_idx;
+    void* y;
+    int B, r, n_slots;
+};
+cudaError_t launch_rows(const Geom& g, const LayerParams& prm, const RowsJob& job, cudaStream_t st);
+
+// conv + SiLU over all channels, then roll each sequence's conv state
+struct ConvJob {
+    const void* x;
+    void* conv_pool;
+    const int32_t* slot_idx;
+    void* u_out;
+    int n_seq, n_tok, n_slots;
+};
+cudaError_t launch_conv_update(const Geom& g, const LayerParams& prm, const ConvJob& job,
+                               cudaStream_t st);
+
+struct CommitJob {
+    void* conv_pool;
+    float* state_pool;
+    const int32_t *slot_idx, *snap_idx, *accepted;
+    int B, r, n_slots;
+};
+cudaError_t launch_commit(const Geom& g, const CommitJob& job, cudaStream_t st);
+
+// prefill: single sequence (cu_seqlens == NULL) or packed varlen
+struct PrefillJob {
+    const void *x, *z, *a, *b;
+    void* y;
+    int64_t n_tokens;
+    int n_seq;
+    const int32_t* cu_seqlens;  // NULL: one sequence [0, n_tokens)
+    // varlen: pools + slots
+    const int32_t* slot_idx;
+    const uint8_t* has_init;
+    float* state_pool;
+    void* conv_pool;
+    int n_slots;
+    // single sequence: direct pointers
+    const float* s0;
+    float* s_final;
+    const void* conv0;
+    void* conv_final;
+    void* workspace;
+    size_t ws_bytes;
+};
+size_t prefill_workspace_bytes(const Geom& g, int64_t n_tokens, int n_seq);
+cudaError_t launch_prefill(const Geom& g, const LayerParams& prm, const PrefillJob& job,
+                           cudaStream_t st);
+
+}  // namespace gdn

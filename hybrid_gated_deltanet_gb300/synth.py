@@ -25,7 +25,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
-from typing import Dict, List, Optional
+from typing import Dict, List
 
 import numpy as np
 
@@ -50,17 +50,47 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     return u.view(np.float32).astype(np.float64)
 
 
-@dataclasses.dataclass
+class LazyF64:
+    """fp64 view of a stored array, decoded on indexing (only the slice asked for)."""
+
+    def __init__(self, raw: np.ndarray, dtype: str):
+        self._raw = raw
+        self._dtype = dtype
+
+    @property
+    def shape(self):
+        return self._raw.shape
+
+    def _decode(self, part):
+        if self._dtype == BF16:
+            return bf16_bits_to_f64(part)
+        return np.asarray(part, dtype=np.float64)
+
+    def __getitem__(self, idx):
+        return self._decode(self._raw[idx])
+
+    def __array__(self, dtype=None, copy=None):
+        out = self._decode(self._raw)
+        return out if dtype is None else out.astype(dtype)
+
+    def __len__(self):
+        return self._raw.shape[0]
+
+
 class Stored:
     """An array in its storage dtype plus its exact fp64 value.
 
     ``raw`` is what the GPU receives: uint16 bit patterns for bf16, float32
-    otherwise.  ``f64`` is the same numbers decoded exactly.
+    otherwise.  ``f64`` decodes the same numbers exactly (lazily, per slice).
     """
 
-    raw: np.ndarray
-    f64: np.ndarray
-    dtype: str
+    def __init__(self, raw: np.ndarray, dtype: str):
+        self.raw = raw
+        self.dtype = dtype
+
+    @property
+    def f64(self) -> LazyF64:
+        return LazyF64(self.raw, self.dtype)
 
     @property
     def shape(self):
@@ -70,11 +100,18 @@ class Stored:
 def store(values: np.ndarray, dtype: str) -> Stored:
     f32 = np.asarray(values, dtype=np.float64).astype(np.float32)
     if dtype == BF16:
-        bits = f32_to_bf16_bits(f32)
-        return Stored(bits, bf16_bits_to_f64(bits), BF16)
+        return Stored(f32_to_bf16_bits(f32), BF16)
     if dtype == F32:
-        return Stored(np.ascontiguousarray(f32), f32.astype(np.float64), F32)
+        return Stored(np.ascontiguousarray(f32), F32)
     raise ValueError(f"unknown storage dtype {dtype!r}")
+
+
+def _store_rows(draw, n_rows: int, dtype: str, block: int = 4096) -> Stored:
+    """Draw n_rows rows block by block (bounded host memory) and store them."""
+    parts = [store(draw(min(block, n_rows - r0)), dtype).raw for r0 in range(0, n_rows, block)]
+    if not parts:
+        parts = [store(draw(0), dtype).raw]
+    return Stored(np.ascontiguousarray(np.concatenate(parts, axis=0)), dtype)
 
 
 # ----------------------------------------------------------------------------
@@ -134,28 +171,33 @@ def make_params(geom: Geometry, rng: np.random.Generator, act_dtype: str) -> Dic
 
 
 def make_tokens(geom: Geometry, n_tok: int, rng: np.random.Generator, act_dtype: str,
-                x_std: float = 1.0) -> Dict[str, Stored]:
-    """Per-token layer inputs: x (pre-conv [q|k|v]), z, a, b, all ~ N(0,1)."""
+                x_std: float = 1.0, block: int = 4096) -> Dict[str, Stored]:
+    """Per-token layer inputs: x (pre-conv [q|k|v]), z, a, b, all ~ N(0,1).
+
+    Drawn in blocks of ``block`` tokens; within a block the order is x, z, a, b.
+    """
     C = geom.conv_channels
-    x = x_std * rng.standard_normal((n_tok, C))
-    z = rng.standard_normal((n_tok, geom.value_dim))
-    a = rng.standard_normal((n_tok, geom.n_v_heads))
-    b = rng.standard_normal((n_tok, geom.n_v_heads))
-    return {"x": store(x, act_dtype), "z": store(z, act_dtype),
-            "a": store(a, act_dtype), "b": store(b, act_dtype)}
+    raws = {"x": [], "z": [], "a": [], "b": []}
+    for t0 in range(0, max(n_tok, 1), block):
+        n = min(block, n_tok - t0) if n_tok > 0 else 0
+        raws["x"].append(store(x_std * rng.standard_normal((n, C)), act_dtype).raw)
+        raws["z"].append(store(rng.standard_normal((n, geom.value_dim)), act_dtype).raw)
+        raws["a"].append(store(rng.standard_normal((n, geom.n_v_heads)), act_dtype).raw)
+        raws["b"].append(store(rng.standard_normal((n, geom.n_v_heads)), act_dtype).raw)
+    return {k: Stored(np.ascontiguousarray(np.concatenate(v, axis=0)), act_dtype) for k, v in raws.items()}
 
 
 def make_state(geom: Geometry, n_slots: int, rng: np.random.Generator, std: float = 0.1) -> Stored:
     """fp32 recurrent states [n_slots, H_v, d_v, d_k] ~ N(0, std^2)."""
-    s = std * rng.standard_normal((n_slots, geom.n_v_heads, geom.d_v, geom.d_k))
-    return store(s, F32)
+    shape = (geom.n_v_heads, geom.d_v, geom.d_k)
+    return _store_rows(lambda n: std * rng.standard_normal((n,) + shape), n_slots, F32, block=64)
 
 
 def make_conv_state(geom: Geometry, n_slots: int, rng: np.random.Generator, act_dtype: str,
                     std: float = 0.1) -> Stored:
     """Conv states [n_slots, d_conv-1, C_ch] ~ N(0, std^2) in the act dtype."""
-    c = std * rng.standard_normal((n_slots, geom.d_conv - 1, geom.conv_channels))
-    return store(c, act_dtype)
+    shape = (geom.d_conv - 1, geom.conv_channels)
+    return _store_rows(lambda n: std * rng.standard_normal((n,) + shape), n_slots, act_dtype, block=256)
 
 
 def log_uniform_lengths(rng: np.random.Generator, n: int, lo: int, hi: int) -> List[int]:

@@ -1,0 +1,205 @@
+/*
+ * gdn.h -- C ABI of libgdn, a GB300 (sm_103a) implementation of the Gated
+ * DeltaNet linear-attention layer of hybrid Qwen3.5/3.6-style models.
+ *
+ * The layer, per token and per v-head j (k-head h = floor(j / G), G = H_v/H_k):
+ *   u   = silu(causal depthwise conv1d over the [q|k|v] channels)
+ *   q^  = q_scale q / sqrt(|q|^2 + l2_eps),   k^ = k / sqrt(|k|^2 + l2_eps)
+ *   g   = -exp(A_log_j) softplus(a_j + dt_bias_j),  alpha = exp(g),  beta = sigmoid(b_j)
+ *   S   = alpha S (I - beta k^ k^T) + beta v k^T,   o = S q^
+ *   y   = norm_w * o / sqrt(mean(o^2) + norm_eps) * silu(z)
+ * The pages describe this layer in words: a fixed-size state that a gate
+ * partly erases and a delta-rule write corrects ("Hybrid transformers under
+ * load: where Gated DeltaNet loses to full attention", braintools.ru,
+ * section 3), with the per-layer state stated in bytes in its section 4.1
+ * (32 x 128 x 128 fp32 = 2,097,152 B plus a 49,152 B conv part for
+ * Qwen3.5-4B) and the wide geometry in "Chapter 6: engine start-up and memory
+ * plan" (Strata), section 6.2 (16 k-heads, 48 v-heads, d_conv 4, 10240 conv
+ * channels = 2*128*16 + 128*48).
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * - Every array argument is a DEVICE pointer, except the two structs, which
+ *   are read on the host during the call.  The caller owns every buffer,
+ *   including the state pools and the workspace; the library keeps no pointer
+ *   after the call returns and allocates no memory (Strata chapter 6,
+ *   section 6.10: the token path allocates nothing).
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream) and never synchronise.  A failed launch returns
+ *   GDN_ERR_CUDA.
+ * - Arguments are checked on the host before any launch; on failure nothing is
+ *   launched, the status is returned and gdn_last_error() names the argument,
+ *   the value found and the value required (Strata chapter 6, sections 6.2
+ *   and 6.5: report the tensor, the shape found and the shape required;
+ *   refuse with both numbers).
+ * - Every pointer must be 16-byte aligned (GDN_ERR_ALIGN).
+ * - Layouts are row-major and dense.  "act" means the activation dtype of the
+ *   config (bf16 or fp32).  Channel order of x is [q | k | v], head-major:
+ *   q of k-head h at h*d_k, k at H_k*d_k + h*d_k, v of v-head j at
+ *   2*H_k*d_k + j*d_v.  C_ch = 2*H_k*d_k + H_v*d_v.
+ * - State pool: float [n_slots][H_v][d_v][d_k], one fp32 state per slot,
+ *   updated in place.  Conv pool: act [n_slots][d_conv-1][C_ch], the last
+ *   d_conv-1 raw (pre-conv) inputs of the slot, oldest first.
+ * - Slot indices are read on the device.  An index outside [0, n_slots) is
+ *   skipped by the kernels (nothing is read or written for that entry; its y
+ *   rows are left as they were).  Duplicate slots within one call race and
+ *   give undefined results.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_NULL = -1,        /* a required pointer is NULL */
+    GDN_ERR_SHAPE = -2,       /* a size or geometry field is invalid */
+    GDN_ERR_DTYPE = -3,       /* unknown act_dtype */
+    GDN_ERR_ALIGN = -4,       /* a pointer is not 16-byte aligned */
+    GDN_ERR_RANGE = -5,       /* a host-side count or index is out of range */
+    GDN_ERR_WORKSPACE = -6,   /* workspace too small (both sizes in gdn_last_error) */
+    GDN_ERR_UNSUPPORTED = -7, /* valid but not implemented (e.g. d_k != d_v) */
+    GDN_ERR_CUDA = -8         /* a CUDA call failed (message in gdn_last_error) */
+} gdn_status;
+
+/* activation dtype of x, z, a, b, y, conv weights/bias, norm weight, conv states */
+enum { GDN_DTYPE_BF16 = 0, GDN_DTYPE_F32 = 1 };
+
+/* flags: switch steps off so that closed forms can be checked on the GPU */
+enum {
+    GDN_FLAG_RAW_QKV = 1u,      /* x already holds [q|k|v]: no conv, no SiLU */
+    GDN_FLAG_NO_L2NORM = 2u,    /* q^ = q_scale q, k^ = k */
+    GDN_FLAG_GATES_DIRECT = 4u, /* a holds g = log(alpha) <= 0, b holds beta */
+    GDN_FLAG_NO_OUTNORM = 8u    /* y = o */
+};
+
+/* op codes for gdn_workspace_size */
+enum {
+    GDN_OP_CONV_STATE_UPDATE = 0,
+    GDN_OP_DECODE_STEP = 1,
+    GDN_OP_VERIFY_ROWS = 2,
+    GDN_OP_CHUNK_PREFILL = 3,
+    GDN_OP_VARLEN_PREFILL = 4
+};
+
+/* Layer geometry and options.  Requirements (GDN_ERR_SHAPE otherwise):
+ * n_k_heads >= 1, n_v_heads % n_k_heads == 0, G = n_v_heads/n_k_heads <= 8,
+ * d_k = d_v in {32, 64, 128} (d_k != d_v: GDN_ERR_UNSUPPORTED),
+ * 2 <= d_conv <= 4, chunk in {16, 32, 64} (prefill only). */
+typedef struct gdn_config {
+    int32_t n_k_heads, n_v_heads, d_k, d_v, d_conv, chunk;
+    int32_t act_dtype;                 /* GDN_DTYPE_* */
+    float q_scale, l2_eps, norm_eps;   /* 1.0, 1e-6, 1e-6 are the defaults */
+    uint32_t flags;                    /* GDN_FLAG_* */
+} gdn_config;
+
+/* Per-layer parameters (device pointers). */
+typedef struct gdn_params {
+    const void* conv_w;   /* act [C_ch][d_conv]; tap d_conv-1 multiplies the current token */
+    const void* conv_b;   /* act [C_ch] or NULL (no bias) */
+    const float* A_log;   /* [H_v] */
+    const float* dt_bias; /* [H_v] or NULL (zero) */
+    const void* norm_w;   /* act [d_v], shared by all v-heads */
+} gdn_params;
+
+/* Causal conv1d + SiLU over all C_ch channels for n_seq sequences of n_tok
+ * tokens each, continuing from and updating each sequence's conv state.
+ *   x       act [n_seq*n_tok][C_ch]  (sequence-major)
+ *   u_out   act [n_seq*n_tok][C_ch]  silu(conv(x)); may be NULL to only roll the state
+ *   conv_pool act [n_slots][d_conv-1][C_ch], read and written in place
+ *   slot_idx int32 [n_seq]
+ * The conv part of the layer state is "the conv part" of section 4.1 of the
+ * braintools.ru page (3 raw rows of 8192 bf16 channels = 49,152 B). */
+gdn_status gdn_conv_state_update(const gdn_config* cfg, const gdn_params* prm, const void* x,
+                                 void* conv_pool, const int32_t* slot_idx, int32_t n_seq,
+                                 int32_t n_tok, int32_t n_slots, void* u_out, void* stream);
+
+/* One decode step: one token for each of B slots, state read once and written
+ * back in place (one pass over the state: "Forge: how I wrote my own inference
+ * engine", entry of 25-26 August, the single-pass DeltaNet decode kernel).
+ *   x act [B][C_ch], z act [B][H_v*d_v], a, b act [B][H_v], y act [B][H_v*d_v]
+ *   slot_idx int32 [B]; state_pool and conv_pool updated in place. */
+gdn_status gdn_decode_step(const gdn_config* cfg, const gdn_params* prm, const void* x,
+                           const void* z, const void* a, const void* b, void* conv_pool,
+                           float* state_pool, const int32_t* slot_idx, int32_t B,
+                           int32_t n_slots, void* y, void* stream);
+
+/* Speculative-decoding verify: r rows (draft tokens) per slot, processed in
+ * sequence with the state kept on chip; the state and conv state after row i
+ * are written to pool slot snap_idx[b][i] ("Forge ...", entry of 27 August:
+ * verify of k tokens is a k-row chunk, DeltaNet runs through sequential rows,
+ * with shadow snapshots between rows so that rollback is a copy).  The slot
+ * slot_idx[b] itself is read, not written (unless it appears in snap_idx).
+ * Accepting a rows selects snap_idx[b][a-1] (a = 0 keeps slot_idx[b]): remap
+ * the slot table on the host, or copy with gdn_commit_rows.
+ *   x act [B][r][C_ch], z act [B][r][H_v*d_v], a, b act [B][r][H_v],
+ *   y act [B][r][H_v*d_v], slot_idx int32 [B], snap_idx int32 [B][r], 1 <= r <= 16. */
+gdn_status gdn_verify_rows(const gdn_config* cfg, const gdn_params* prm, const void* x,
+                           const void* z, const void* a, const void* b, void* conv_pool,
+                           float* state_pool, const int32_t* slot_idx, const int32_t* snap_idx,
+                           int32_t B, int32_t r, int32_t n_slots, void* y, void* stream);
+
+/* Rollback/commit by copy: for each b with accepted[b] >= 1 copies the state
+ * and conv state of snap_idx[b][accepted[b]-1] into slot_idx[b]; accepted[b]
+ * = 0 leaves slot_idx[b] as it was before the verify.  accepted int32 [B]
+ * (device), values outside [0, r] are treated as 0. */
+gdn_status gdn_commit_rows(const gdn_config* cfg, void* conv_pool, float* state_pool,
+                           const int32_t* slot_idx, const int32_t* snap_idx,
+                           const int32_t* accepted, int32_t B, int32_t r, int32_t n_slots,
+                           void* stream);
+
+/* Chunkwise (WY / UT-transform) prefill of one sequence of T tokens
+ * ("Forge ...", entry of 25-26 August: a chunked DeltaNet prefill kernel with
+ * deterministic reduction).  Results equal the token-by-token evaluation
+ * (Strata chapter 6, section 6.9: prefill is the decode path one token at a
+ * time) up to rounding; the reduction order is fixed, so results are
+ * bitwise reproducible.
+ *   x act [T][C_ch], z act [T][H_v*d_v], a, b act [T][H_v], y act [T][H_v*d_v]
+ *   s0 float [H_v][d_v][d_k] or NULL (zeros); s_final float [H_v][d_v][d_k]
+ *   (may equal s0); conv0 act [d_conv-1][C_ch] or NULL (zeros); conv_final
+ *   act [d_conv-1][C_ch] (may equal conv0).
+ *   workspace: at least gdn_workspace_size(cfg, GDN_OP_CHUNK_PREFILL, T, 1) bytes. */
+gdn_status gdn_chunk_prefill(const gdn_config* cfg, const gdn_params* prm, const void* x,
+                             const void* z, const void* a, const void* b, int64_t T,
+                             const float* s0, const void* conv0, float* s_final, void* conv_final,
+                             void* y, void* workspace, size_t ws_bytes, void* stream);
+
+/* Packed variable-length prefill: n_seq sequences back to back, sequence s
+ * covering tokens [cu_seqlens[s], cu_seqlens[s+1]).  Chunks restart at each
+ * sequence start; sequence s reads its initial state and conv state from pool
+ * slot slot_idx[s] when has_init[s] != 0 (zeros otherwise, or always when
+ * has_init is NULL) and writes its final ones there.
+ *   x act [n_tokens][C_ch], z, y act [n_tokens][H_v*d_v], a, b act [n_tokens][H_v]
+ *   cu_seqlens int32 [n_seq+1] (device; 0 = cu_seqlens[0] <= ... <= cu_seqlens[n_seq]
+ *   = n_tokens; out-of-range entries are clamped into [0, n_tokens])
+ *   slot_idx int32 [n_seq], has_init uint8 [n_seq] or NULL.
+ *   workspace: gdn_workspace_size(cfg, GDN_OP_VARLEN_PREFILL, n_tokens, n_seq) bytes. */
+gdn_status gdn_varlen_prefill(const gdn_config* cfg, const gdn_params* prm, const void* x,
+                              const void* z, const void* a, const void* b,
+                              const int32_t* cu_seqlens, int32_t n_seq, int64_t n_tokens,
+                              const int32_t* slot_idx, const uint8_t* has_init, void* conv_pool,
+                              float* state_pool, int32_t n_slots, void* y, void* workspace,
+                              size_t ws_bytes, void* stream);
+
+/* Workspace bytes an op needs for n_tokens tokens in n_seq sequences (0 for
+ * the ops that need none).  Returns 0 and sets gdn_last_error on an invalid
+ * config. */
+size_t gdn_workspace_size(const gdn_config* cfg, int32_t op, int64_t n_tokens, int32_t n_seq);
+
+/* Message of the last failed call on this host thread ("" if none).  The
+ * string stays valid until the next call on this thread. */
+const char* gdn_last_error(void);
+
+/* Library version string. */
+const char* gdn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,144 @@
+"""The C ABI without a GPU: libgdn loads, exports every entry point that
+include/gdn.h declares, and rejects bad arguments on the host with the status
+and a message naming the argument, the value found and the value required
+(Strata chapter 6, sections 6.2 and 6.5).  No call here reaches a launch."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from hybrid_gated_deltanet_gb300 import binding as gb
+from hybrid_gated_deltanet_gb300 import build as gbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "gdn.h")
+FAKE = 0x100000  # an aligned address that is never dereferenced on the host
+
+
+@pytest.fixture(scope="module")
+def lib():
+    gbuild.build()
+    return gb.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(gdn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for fn in ("gdn_conv_state_update", "gdn_decode_step", "gdn_verify_rows", "gdn_chunk_prefill",
+               "gdn_varlen_prefill", "gdn_workspace_size", "gdn_last_error"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", gb.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (gdn_\w+)", out))
+    assert set(declared_functions()) <= exported
+    assert lib.gdn_version().decode().startswith("libgdn")
+
+
+def _cfg(**kw):
+    c = gb.Config(16, 32, 128, 128, 4, 64, gb.BF16)
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c.c()
+
+
+def _prm():
+    return gb.CParams(FAKE, None, FAKE, None, FAKE)
+
+
+def _decode(lib, cfg, x=FAKE, B=4, n_slots=8, prm=None):
+    prm = prm or _prm()
+    return lib.gdn_decode_step(ctypes.byref(cfg), ctypes.byref(prm), x, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B,
+                               n_slots, FAKE, None)
+
+
+def _err(lib):
+    return lib.gdn_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,status,needle", [
+    (dict(act_dtype=7), -3, "cfg.act_dtype: found 7"),
+    (dict(n_v_heads=30), -2, "cfg.n_v_heads: found 30, required a multiple of n_k_heads = 16"),
+    (dict(n_k_heads=2, n_v_heads=32), -7, "required <= 8"),
+    (dict(d_k=48, d_v=48), -2, "cfg.d_k: found 48"),
+    (dict(d_v=64), -7, "required d_v == d_k = 128"),
+    (dict(d_conv=5), -2, "cfg.d_conv: found 5"),
+    (dict(flags=16), -2, "cfg.flags"),
+])
+def test_config_validation(lib, kw, status, needle):
+    assert _decode(lib, _cfg(**kw)) == status
+    assert needle in _err(lib)
+
+
+def test_null_and_alignment(lib):
+    assert lib.gdn_decode_step(None, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, FAKE, None) == -1
+    assert "cfg: found NULL" in _err(lib)
+    assert _decode(lib, _cfg(), x=0) == -1
+    assert "x: found NULL, required a device pointer" in _err(lib)
+    assert _decode(lib, _cfg(), x=FAKE + 4) == -4
+    assert "x: found address" in _err(lib) and "16-byte alignment" in _err(lib)
+    prm = gb.CParams(FAKE, None, None, None, FAKE)
+    assert _decode(lib, _cfg(), prm=prm) == -1 and "prm.A_log" in _err(lib)
+
+
+def test_counts(lib):
+    assert _decode(lib, _cfg(), B=-1) == -5 and "B: found -1" in _err(lib)
+    assert _decode(lib, _cfg(), n_slots=0) == -5 and "n_slots: found 0" in _err(lib)
+    assert _decode(lib, _cfg(), B=0) == 0 and _err(lib) == ""   # nothing to launch
+    cfg = _cfg()
+    prm = _prm()
+    st = lib.gdn_verify_rows(ctypes.byref(cfg), ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2,
+                             17, 8, FAKE, None)
+    assert st == -5 and "r: found 17, required 1..16" in _err(lib)
+    st = lib.gdn_verify_rows(ctypes.byref(cfg), ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 2,
+                             4, 8, FAKE, None)
+    assert st == -1 and "snap_idx" in _err(lib)
+
+
+def test_workspace_size_and_refusal(lib):
+    cfg = _cfg()
+    need = lib.gdn_workspace_size(ctypes.byref(cfg), gb.OP_CHUNK_PREFILL, 8192, 1)
+    # q^ and k^ (2 x 16 x 128) + v (32 x 128) + g, beta (2 x 32) fp32 per token
+    assert need == 8192 * (2 * 16 * 128 + 32 * 128 + 2 * 32) * 4
+    assert lib.gdn_workspace_size(ctypes.byref(cfg), gb.OP_DECODE_STEP, 64, 1) == 0
+    bad = _cfg(chunk=48)
+    assert lib.gdn_workspace_size(ctypes.byref(bad), gb.OP_CHUNK_PREFILL, 10, 1) == 0
+    assert "cfg.chunk: found 48" in _err(lib)
+    prm = _prm()
+    st = lib.gdn_chunk_prefill(ctypes.byref(cfg), ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, 8192, None, None, FAKE,
+                               FAKE, FAKE, FAKE, need - 1, None)
+    assert st == -6
+    assert f"workspace: found {need - 1} bytes, required {need} bytes" in _err(lib)
+    st = lib.gdn_chunk_prefill(ctypes.byref(cfg), ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, 8192, None, None, FAKE,
+                               FAKE, FAKE, None, 0, None)
+    assert st == -1 and "workspace" in _err(lib)
+
+
+def test_varlen_validation(lib):
+    cfg = _cfg()
+    prm = _prm()
+    st = lib.gdn_varlen_prefill(ctypes.byref(cfg), ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, None, 3, 100, FAKE,
+                                None, FAKE, FAKE, 8, FAKE, FAKE, 1 << 30, None)
+    assert st == -1 and "cu_seqlens" in _err(lib)
+    st = lib.gdn_varlen_prefill(ctypes.byref(cfg), ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, FAKE, 0, 5, FAKE,
+                                None, FAKE, FAKE, 8, FAKE, FAKE, 0, None)
+    assert st == -5 and "n_tokens: found 5 with n_seq = 0" in _err(lib)
+    st = lib.gdn_varlen_prefill(ctypes.byref(cfg), ctypes.byref(prm), None, None, None, None, None, 0, 0, None, None,
+                                None, None, 8, None, None, 0, None)
+    assert st == 0
+
+
+def test_binding_raises_with_message(lib):
+    cfg = gb.Config(16, 30, 128, 128)
+    with pytest.raises(gb.GdnError, match="GDN_ERR_SHAPE: cfg.n_v_heads: found 30"):
+        gb.gdn_workspace_size(cfg, gb.OP_CHUNK_PREFILL, 10)
