@@ -30,22 +30,31 @@ gdn_status ok() {
     return GDN_OK;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1u)) == 0; }
 
-#define GDN_REQUIRE_PTR(p, name)                                                          \
-    do {                                                                                  \
+// State buffers and the workspace are moved with 128-bit accesses (16-byte
+// alignment); activation arrays, parameters and index arrays need their
+// element alignment (`al` below: 2 for bf16, 4 otherwise).
+#define GDN_PTR_ALIGN(p, name, al)                                                           \
+    do {                                                                                     \
+        if (!aligned((p), (al)))                                                             \
+            return fail(GDN_ERR_ALIGN, "%s: found address %p, required %u-byte alignment", name, \
+                        (const void*)(p), (unsigned)(al));                                   \
+    } while (0)
+
+#define GDN_REQUIRE_PTR_A(p, name, al)                                                        \
+    do {                                                                                     \
         if (!(p)) return fail(GDN_ERR_NULL, "%s: found NULL, required a device pointer", name); \
-        if (!aligned16(p))                                                                \
-            return fail(GDN_ERR_ALIGN, "%s: found address %p, required 16-byte alignment", name, \
-                        (const void*)(p));                                                \
+        GDN_PTR_ALIGN(p, name, al);                                                          \
     } while (0)
 
-#define GDN_OPTIONAL_PTR(p, name)                                                         \
-    do {                                                                                  \
-        if ((p) && !aligned16(p))                                                         \
-            return fail(GDN_ERR_ALIGN, "%s: found address %p, required 16-byte alignment", name, \
-                        (const void*)(p));                                                \
+#define GDN_OPTIONAL_PTR_A(p, name, al)                                                       \
+    do {                                                                                     \
+        if (p) GDN_PTR_ALIGN(p, name, al);                                                   \
     } while (0)
+
+#define GDN_REQUIRE_PTR(p, name) GDN_REQUIRE_PTR_A(p, name, 16u)
+#define GDN_OPTIONAL_PTR(p, name) GDN_OPTIONAL_PTR_A(p, name, 16u)
 
 gdn_status make_geom(const gdn_config* cfg, bool need_chunk, gdn::Geom* g) {
     if (!cfg) return fail(GDN_ERR_NULL, "cfg: found NULL, required a gdn_config");
@@ -94,14 +103,15 @@ gdn_status make_params(const gdn_params* prm, const gdn::Geom& g, bool need_all,
     const bool conv = !(g.flags & GDN_FLAG_RAW_QKV);
     const bool gates = !(g.flags & GDN_FLAG_GATES_DIRECT);
     const bool norm = !(g.flags & GDN_FLAG_NO_OUTNORM);
-    if (conv || !need_all) GDN_REQUIRE_PTR(prm->conv_w, "prm.conv_w");
-    else GDN_OPTIONAL_PTR(prm->conv_w, "prm.conv_w");
-    GDN_OPTIONAL_PTR(prm->conv_b, "prm.conv_b");
-    if (need_all && gates) GDN_REQUIRE_PTR(prm->A_log, "prm.A_log");
-    else GDN_OPTIONAL_PTR(prm->A_log, "prm.A_log");
-    GDN_OPTIONAL_PTR(prm->dt_bias, "prm.dt_bias");
-    if (need_all && norm) GDN_REQUIRE_PTR(prm->norm_w, "prm.norm_w");
-    else GDN_OPTIONAL_PTR(prm->norm_w, "prm.norm_w");
+    const unsigned ae = g.act_bf16 ? 2u : 4u;
+    if (conv || !need_all) GDN_REQUIRE_PTR_A(prm->conv_w, "prm.conv_w", ae);
+    else GDN_OPTIONAL_PTR_A(prm->conv_w, "prm.conv_w", ae);
+    GDN_OPTIONAL_PTR_A(prm->conv_b, "prm.conv_b", ae);
+    if (need_all && gates) GDN_REQUIRE_PTR_A(prm->A_log, "prm.A_log", 4u);
+    else GDN_OPTIONAL_PTR_A(prm->A_log, "prm.A_log", 4u);
+    GDN_OPTIONAL_PTR_A(prm->dt_bias, "prm.dt_bias", 4u);
+    if (need_all && norm) GDN_REQUIRE_PTR_A(prm->norm_w, "prm.norm_w", ae);
+    else GDN_OPTIONAL_PTR_A(prm->norm_w, "prm.norm_w", ae);
     p->conv_w = prm->conv_w;
     p->conv_b = prm->conv_b;
     p->A_log = prm->A_log;
@@ -148,10 +158,10 @@ gdn_status gdn_conv_state_update(const gdn_config* cfg, const gdn_params* prm, c
                     n_slots);
     if (n_seq > 0 && n_tok > 0) {
         if ((st = make_params(prm, g, false, &p))) return st;
-        GDN_REQUIRE_PTR(x, "x");
+        GDN_REQUIRE_PTR_A(x, "x", g.act_bf16 ? 2u : 4u);
         GDN_REQUIRE_PTR(conv_pool, "conv_pool");
-        GDN_REQUIRE_PTR(slot_idx, "slot_idx");
-        GDN_OPTIONAL_PTR(u_out, "u_out");
+        GDN_REQUIRE_PTR_A(slot_idx, "slot_idx", 4u);
+        GDN_OPTIONAL_PTR_A(u_out, "u_out", g.act_bf16 ? 2u : 4u);
     } else {
         return ok();
     }
@@ -172,14 +182,14 @@ static gdn_status rows_common(const gdn_config* cfg, const gdn_params* prm, cons
     if (n_slots < 1) return fail(GDN_ERR_RANGE, "n_slots: found %d, required >= 1", n_slots);
     if (B == 0) return ok();
     if ((st = make_params(prm, g, true, &p))) return st;
-    GDN_REQUIRE_PTR(x, "x");
-    if (!(g.flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR(z, "z");
-    GDN_REQUIRE_PTR(a, "a");
-    GDN_REQUIRE_PTR(b, "b");
+    GDN_REQUIRE_PTR_A(x, "x", g.act_bf16 ? 2u : 4u);
+    if (!(g.flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR_A(z, "z", g.act_bf16 ? 2u : 4u);
+    GDN_REQUIRE_PTR_A(a, "a", g.act_bf16 ? 2u : 4u);
+    GDN_REQUIRE_PTR_A(b, "b", g.act_bf16 ? 2u : 4u);
     GDN_REQUIRE_PTR(conv_pool, "conv_pool");
     GDN_REQUIRE_PTR(state_pool, "state_pool");
-    GDN_REQUIRE_PTR(slot_idx, "slot_idx");
-    GDN_REQUIRE_PTR(y, "y");
+    GDN_REQUIRE_PTR_A(slot_idx, "slot_idx", 4u);
+    GDN_REQUIRE_PTR_A(y, "y", g.act_bf16 ? 2u : 4u);
     gdn::RowsJob job{x, z, a, b, conv_pool, state_pool, slot_idx, snap_idx, y, B, r, n_slots};
     return cuda_status(gdn::launch_rows(g, p, job, (cudaStream_t)stream), who);
 }
@@ -194,7 +204,7 @@ gdn_status gdn_decode_step(const gdn_config* cfg, const gdn_params* prm, const v
 gdn_status gdn_verify_rows(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* z, const void* a,
                            const void* b, void* conv_pool, float* state_pool, const int32_t* slot_idx,
                            const int32_t* snap_idx, int32_t B, int32_t r, int32_t n_slots, void* y, void* stream) {
-    if (B > 0) GDN_REQUIRE_PTR(snap_idx, "snap_idx");
+    if (B > 0) GDN_REQUIRE_PTR_A(snap_idx, "snap_idx", 4u);
     return rows_common(cfg, prm, x, z, a, b, conv_pool, state_pool, slot_idx, snap_idx, B, r, n_slots, y, stream,
                        "gdn_verify_rows");
 }
@@ -211,9 +221,9 @@ gdn_status gdn_commit_rows(const gdn_config* cfg, void* conv_pool, float* state_
     if (B == 0) return ok();
     GDN_REQUIRE_PTR(conv_pool, "conv_pool");
     GDN_REQUIRE_PTR(state_pool, "state_pool");
-    GDN_REQUIRE_PTR(slot_idx, "slot_idx");
-    GDN_REQUIRE_PTR(snap_idx, "snap_idx");
-    GDN_REQUIRE_PTR(accepted, "accepted");
+    GDN_REQUIRE_PTR_A(slot_idx, "slot_idx", 4u);
+    GDN_REQUIRE_PTR_A(snap_idx, "snap_idx", 4u);
+    GDN_REQUIRE_PTR_A(accepted, "accepted", 4u);
     gdn::CommitJob job{conv_pool, state_pool, slot_idx, snap_idx, accepted, B, r, n_slots};
     return cuda_status(gdn::launch_commit(g, job, (cudaStream_t)stream), "gdn_commit_rows");
 }
@@ -228,11 +238,11 @@ static gdn_status prefill_common(const gdn_config* cfg, const gdn_params* prm, g
         return fail(GDN_ERR_RANGE, "n_tokens: found %lld, required 0..2^31", (long long)job.n_tokens);
     if ((st = make_params(prm, g, true, &p))) return st;
     if (job.n_tokens > 0) {
-        GDN_REQUIRE_PTR(job.x, "x");
-        if (!(g.flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR(job.z, "z");
-        GDN_REQUIRE_PTR(job.a, "a");
-        GDN_REQUIRE_PTR(job.b, "b");
-        GDN_REQUIRE_PTR(job.y, "y");
+        GDN_REQUIRE_PTR_A(job.x, "x", g.act_bf16 ? 2u : 4u);
+        if (!(g.flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR_A(job.z, "z", g.act_bf16 ? 2u : 4u);
+        GDN_REQUIRE_PTR_A(job.a, "a", g.act_bf16 ? 2u : 4u);
+        GDN_REQUIRE_PTR_A(job.b, "b", g.act_bf16 ? 2u : 4u);
+        GDN_REQUIRE_PTR_A(job.y, "y", g.act_bf16 ? 2u : 4u);
     }
     const size_t need = gdn::prefill_workspace_bytes(g, job.n_tokens, job.cu_seqlens ? job.n_seq : 1);
     if (need > 0) GDN_REQUIRE_PTR(job.workspace, "workspace");
@@ -271,9 +281,9 @@ gdn_status gdn_varlen_prefill(const gdn_config* cfg, const gdn_params* prm, cons
         gdn_status st = make_geom(cfg, true, &g);
         return st ? st : ok();
     }
-    GDN_REQUIRE_PTR(cu_seqlens, "cu_seqlens");
-    GDN_REQUIRE_PTR(slot_idx, "slot_idx");
-    GDN_OPTIONAL_PTR(has_init, "has_init");
+    GDN_REQUIRE_PTR_A(cu_seqlens, "cu_seqlens", 4u);
+    GDN_REQUIRE_PTR_A(slot_idx, "slot_idx", 4u);
+    GDN_OPTIONAL_PTR_A(has_init, "has_init", 1u);
     GDN_REQUIRE_PTR(conv_pool, "conv_pool");
     GDN_REQUIRE_PTR(state_pool, "state_pool");
     GDN_OPTIONAL_PTR(workspace, "workspace");

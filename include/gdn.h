@@ -32,7 +32,10 @@
  *   the value found and the value required (Strata chapter 6, sections 6.2
  *   and 6.5: report the tensor, the shape found and the shape required;
  *   refuse with both numbers).
- * - Every pointer must be 16-byte aligned (GDN_ERR_ALIGN).
+ * - Alignment (GDN_ERR_ALIGN otherwise): state pools, s0, s_final, conv
+ *   pools and the workspace 16 bytes (they are moved with 128-bit accesses);
+ *   activation arrays and parameters their element size (2 for bf16, 4 for
+ *   fp32); int32 arrays 4 bytes.
  * - Layouts are row-major and dense.  "act" means the activation dtype of the
  *   config (bf16 or fp32).  Channel order of x is [q | k | v], head-major:
  *   q of k-head h at h*d_k, k at H_k*d_k + h*d_k, v of v-head j at
@@ -60,7 +63,7 @@ typedef enum gdn_status {
     GDN_ERR_NULL = -1,        /* a required pointer is NULL */
     GDN_ERR_SHAPE = -2,       /* a size or geometry field is invalid */
     GDN_ERR_DTYPE = -3,       /* unknown act_dtype */
-    GDN_ERR_ALIGN = -4,       /* a pointer is not 16-byte aligned */
+    GDN_ERR_ALIGN = -4,       /* a pointer is misaligned for its use */
     GDN_ERR_RANGE = -5,       /* a host-side count or index is out of range */
     GDN_ERR_WORKSPACE = -6,   /* workspace too small (both sizes in gdn_last_error) */
     GDN_ERR_UNSUPPORTED = -7, /* valid but not implemented (e.g. d_k != d_v) */
