@@ -111,6 +111,7 @@ def load() -> ctypes.CDLL:
             "gdn_verify_rows": [cfgp, prmp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp],
             "gdn_commit_rows": [cfgp, vp, vp, vp, vp, vp, i32, i32, i32, vp],
             "gdn_chunk_prefill": [cfgp, prmp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, sz, vp],
+            "gdn_chunk_prefill_noalloc": [cfgp, prmp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp],
             "gdn_varlen_prefill": [cfgp, prmp, vp, vp, vp, vp, vp, i32, i64, vp, vp, vp, vp, i32, vp, vp, sz, vp],
         }
         for name, args in sigs.items():
@@ -192,6 +193,15 @@ def gdn_chunk_prefill(cfg: Config, prm: Params, x, z, a, b, s0, conv0, s_final, 
     _check(load().gdn_chunk_prefill(ctypes.byref(c), ctypes.byref(p), _p(x), _p(z), _p(a), _p(b), x.shape[0], _p(s0),
                                     _p(conv0), _p(s_final), _p(conv_final), _p(y), _p(workspace), ws_bytes,
                                     _stream(stream)))
+
+
+def gdn_chunk_prefill_noalloc(cfg: Config, prm: Params, x, z, a, b, s0, conv0, s_final, conv_final, y, stream=None):
+    """gdn_chunk_prefill without a workspace argument, for callers that cannot
+    allocate: the library's static 64 MiB device scratch is used instead."""
+    c, p = cfg.c(), prm.c()
+    _check(load().gdn_chunk_prefill_noalloc(ctypes.byref(c), ctypes.byref(p), _p(x), _p(z), _p(a), _p(b),
+                                            x.shape[0], _p(s0), _p(conv0), _p(s_final), _p(conv_final), _p(y),
+                                            _stream(stream)))
 
 
 def gdn_varlen_prefill(cfg: Config, prm: Params, x, z, a, b, cu_seqlens, slot_idx, has_init, conv_pool, state_pool, y,

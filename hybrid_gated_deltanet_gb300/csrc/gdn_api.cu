@@ -127,6 +127,15 @@ gdn_status cuda_status(cudaError_t e, const char* what) {
 
 }  // namespace
 
+namespace gdn {
+// Lets another translation unit of the library report a failure through
+// gdn_last_error (same thread-local message as the entry points here).
+int report_error(int status, const char* message) {
+    g_last_error = message;
+    return status;
+}
+}  // namespace gdn
+
 extern "C" {
 
 const char* gdn_last_error(void) { return g_last_error.c_str(); }

@@ -189,6 +189,29 @@ gdn_status gdn_varlen_prefill(const gdn_config* cfg, const gdn_params* prm, cons
                               float* state_pool, int32_t n_slots, void* y, void* workspace,
                               size_t ws_bytes, void* stream);
 
+/* Chunked prefill for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point: it exists for callers that cannot
+ * call cudaMalloc when they run a prefill -- a host runtime that owns the
+ * whole device memory budget through its own allocator, code running while
+ * its stream is captured into a CUDA graph (cudaMalloc/cudaFree are not
+ * allowed there), or a latency-critical path that cannot pay for the
+ * device-wide synchronisation of cudaFree.
+ * Same arguments and results as gdn_chunk_prefill, minus the workspace: the
+ * workspace is a static device array of 64 MiB inside libgdn, which every GPU
+ * that loads the library holds until the process exits.  T is limited to
+ * what fits: gdn_workspace_size(cfg, GDN_OP_CHUNK_PREFILL, T, 1) <= 64 MiB
+ * (about 2000 tokens at the Qwen3.5-4B geometry); larger T returns
+ * GDN_ERR_WORKSPACE with both sizes in gdn_last_error().
+ * The first call on a device looks up the array's address (cudaGetSymbolAddress,
+ * with that device current) and caches it: make that first call before any
+ * stream capture.  All calls share the array and it keeps the previous call's
+ * contents (nothing in it needs to start at zero); calls that overlap on the
+ * GPU race on it.  Nothing here allocates. */
+gdn_status gdn_chunk_prefill_noalloc(const gdn_config* cfg, const gdn_params* prm, const void* x,
+                                     const void* z, const void* a, const void* b, int64_t T,
+                                     const float* s0, const void* conv0, float* s_final,
+                                     void* conv_final, void* y, void* stream);
+
 /* Workspace bytes an op needs for n_tokens tokens in n_seq sequences (0 for
  * the ops that need none).  Returns 0 and sets gdn_last_error on an invalid
  * config. */
