@@ -415,12 +415,17 @@ def profile_case(args):
     gbuild.build()
     device = torch.device("cuda", 0)
     if args.case == "decode-small":
-        global N_LAYERS
+        global N_LAYERS, B, POOL
         N_LAYERS = 2  # 2 x 64 slots x 2 MiB of state: 256 MiB, larger than L2
+        B = args.batch
+        POOL = max(4 * B, 2)
         cfg, host, layers = setup_decode(torch, device, seed=0)
-        t = time_decode(torch, cfg, layers, args.steps, args.warmup, use_graph=False)
-        print(json.dumps({"case": args.case, "launches": (args.steps + args.warmup + 1) * N_LAYERS,
-                          "us_per_launch": round(1e6 * t / (args.steps * N_LAYERS), 3)}))
+        t = time_decode(torch, cfg, layers, args.steps, args.warmup, use_graph=not args.no_graph)
+        us = 1e6 * t / (args.steps * N_LAYERS)
+        print(json.dumps({"case": args.case, "batch": B, "launches": (args.steps + args.warmup + 1) * N_LAYERS,
+                          "us_per_launch": round(us, 3),
+                          "gbs": round((B * SLOT_BYTES + PARAM_BYTES) / us / 1e3, 1),
+                          "slices": os.environ.get("GDN_DECODE_SLICES", "auto")}))
     else:
         t, _ = prefill_measure(torch, device, args.steps, args.warmup, seed=0, check=False)
         print(json.dumps({"case": args.case, "ms_per_call": round(1e3 * t, 4)}))
@@ -547,6 +552,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--batch", type=int, default=64, help="slots of the decode-small case")
     ap.add_argument("--case", default="full", choices=["full", "decode-small", "prefill-small"],
                     help="small cases for ncu captures")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -122,6 +122,8 @@ def load() -> ctypes.CDLL:
         lib.gdn_workspace_size.restype = sz
         lib.gdn_last_error.argtypes = []
         lib.gdn_last_error.restype = ctypes.c_char_p
+        lib.gdn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        lib.gdn_device_status.restype = ctypes.c_int
         lib.gdn_version.argtypes = []
         lib.gdn_version.restype = ctypes.c_char_p
         _lib = lib
@@ -139,6 +141,14 @@ def _stream(stream) -> Optional[int]:
     if isinstance(stream, torch.cuda.Stream):
         return stream.cuda_stream
     return int(stream)
+
+
+def gdn_device_status() -> int:
+    """Reads and clears the device status word (0: no kernel reported a timed-out
+    wait).  Synchronises the current device."""
+    v = ctypes.c_uint32(0)
+    _check(load().gdn_device_status(ctypes.byref(v)))
+    return int(v.value)
 
 
 def gdn_workspace_size(cfg: Config, op: int, n_tokens: int, n_seq: int = 1) -> int:

@@ -104,14 +104,14 @@ gdn_status make_params(const gdn_params* prm, const gdn::Geom& g, bool need_all,
     const bool gates = !(g.flags & GDN_FLAG_GATES_DIRECT);
     const bool norm = !(g.flags & GDN_FLAG_NO_OUTNORM);
     const unsigned ae = g.act_bf16 ? 2u : 4u;
-    if (conv || !need_all) GDN_REQUIRE_PTR_A(prm->conv_w, "prm.conv_w", ae);
-    else GDN_OPTIONAL_PTR_A(prm->conv_w, "prm.conv_w", ae);
+    if (conv || !need_all) GDN_REQUIRE_PTR(prm->conv_w, "prm.conv_w");
+    else GDN_OPTIONAL_PTR(prm->conv_w, "prm.conv_w");
     GDN_OPTIONAL_PTR_A(prm->conv_b, "prm.conv_b", ae);
     if (need_all && gates) GDN_REQUIRE_PTR_A(prm->A_log, "prm.A_log", 4u);
     else GDN_OPTIONAL_PTR_A(prm->A_log, "prm.A_log", 4u);
     GDN_OPTIONAL_PTR_A(prm->dt_bias, "prm.dt_bias", 4u);
-    if (need_all && norm) GDN_REQUIRE_PTR_A(prm->norm_w, "prm.norm_w", ae);
-    else GDN_OPTIONAL_PTR_A(prm->norm_w, "prm.norm_w", ae);
+    if (need_all && norm) GDN_REQUIRE_PTR(prm->norm_w, "prm.norm_w");
+    else GDN_OPTIONAL_PTR(prm->norm_w, "prm.norm_w");
     p->conv_w = prm->conv_w;
     p->conv_b = prm->conv_b;
     p->A_log = prm->A_log;
@@ -141,6 +141,15 @@ extern "C" {
 const char* gdn_last_error(void) { return g_last_error.c_str(); }
 
 const char* gdn_version(void) { return "libgdn 0.1 (sm_103a)"; }
+
+gdn_status gdn_device_status(uint32_t* status) {
+    if (!status) return fail(GDN_ERR_NULL, "status: found NULL, required a host pointer");
+    unsigned a = 0, b = 0;
+    cudaError_t e = gdn::take_device_status_decode(&a);
+    if (e == cudaSuccess) e = gdn::take_device_status_prefill(&b);
+    *status = a | b;
+    return cuda_status(e, "gdn_device_status");
+}
 
 size_t gdn_workspace_size(const gdn_config* cfg, int32_t op, int64_t n_tokens, int32_t n_seq) {
     gdn::Geom g;
@@ -191,8 +200,8 @@ static gdn_status rows_common(const gdn_config* cfg, const gdn_params* prm, cons
     if (n_slots < 1) return fail(GDN_ERR_RANGE, "n_slots: found %d, required >= 1", n_slots);
     if (B == 0) return ok();
     if ((st = make_params(prm, g, true, &p))) return st;
-    GDN_REQUIRE_PTR_A(x, "x", g.act_bf16 ? 2u : 4u);
-    if (!(g.flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR_A(z, "z", g.act_bf16 ? 2u : 4u);
+    GDN_REQUIRE_PTR(x, "x");  // x and z are staged with bulk copies: 16-byte aligned
+    if (!(g.flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR(z, "z");
     GDN_REQUIRE_PTR_A(a, "a", g.act_bf16 ? 2u : 4u);
     GDN_REQUIRE_PTR_A(b, "b", g.act_bf16 ? 2u : 4u);
     GDN_REQUIRE_PTR(conv_pool, "conv_pool");

@@ -53,4 +53,23 @@ __device__ __forceinline__ void gates(float a, float b, float A_log, float dt, b
 
 constexpr uint32_t kFlagRawQKV = 1u, kFlagNoL2 = 2u, kFlagGatesDirect = 4u, kFlagNoOutNorm = 8u;
 
+// ---- device status word ------------------------------------------------------
+// A kernel whose bounded wait gives up ORs a code into this word instead of
+// spinning forever; gdn_device_status() reads and clears it.  The kernels are
+// compiled without relocatable device code, so every translation unit that
+// includes this header has its own word and its own reader below.
+constexpr unsigned kDevWaitTimeout = 1u;
+
+static __device__ unsigned int g_device_status = 0;
+
+__device__ __forceinline__ void report_device_status(unsigned code) { atomicOr(&g_device_status, code); }
+
+static inline cudaError_t take_device_status_tu(unsigned* out) {
+    unsigned v = 0, zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof v);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero);
+    *out = v;
+    return e;
+}
+
 }  // namespace gdn

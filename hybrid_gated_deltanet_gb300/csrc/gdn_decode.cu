@@ -32,13 +32,12 @@
 
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_tma.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace gdn {
 namespace {
-
-constexpr int kMaxRows = 16;
 
 struct RowsArgs {
     Geom g;
@@ -53,84 +52,170 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// silu(conv) (or the raw value) of channel ch for verify row t of batch entry bb
-template <typename TA>
-__device__ __forceinline__ float conv_at(const RowsArgs& A, int ch, int t, int bb, int slot) {
-    using L = Act<TA>;
-    const Geom& g = A.g;
-    const RowsJob& J = A.job;
-    const int C = g.C_ch, K = g.K;
-    if (g.flags & kFlagRawQKV) return L::ld(J.x, ((size_t)bb * J.r + t) * C + ch);
-    float c = A.p.conv_b ? L::ld(A.p.conv_b, ch) : 0.0f;
-    for (int m = 0; m < K; ++m) {
-        const int tau = t - (K - 1) + m;
-        const float xv = tau >= 0 ? L::ld(J.x, ((size_t)bb * J.r + tau) * C + ch)
-                                  : L::ld(J.conv_pool, ((size_t)slot * (K - 1) + (K - 1 + tau)) * C + ch);
-        c = fmaf(L::ld(A.p.conv_w, (size_t)ch * K + m), xv, c);
-    }
-    return siluf_(c);
+// Shared-memory layout of one k_rows CTA (byte offsets, 16-byte aligned runs).
+struct RowsSmem {
+    int bar, S, x, c, w, z, nw, ab, qs, ks, vs, red, obuf, ssp, total;
+};
+
+__host__ __device__ inline RowsSmem rows_smem(int D, int RPC, int r, int K, int E) {
+    auto up = [](int v) { return (v + 15) & ~15; };
+    const int NCH = 2 * D + RPC;
+    RowsSmem s;
+    int o = 0;
+    s.bar = o; o += 16;                   // two mbarriers
+    s.S = o; o += RPC * D * 4;            // the CTA's state rows, fp32
+    s.x = o; o = up(o + r * NCH * E);     // x of the CTA's channels, per row
+    s.c = o; o = up(o + (K - 1) * NCH * E);  // conv state of those channels
+    s.w = o; o = up(o + NCH * K * E);     // conv weights of those channels
+    s.z = o; o = up(o + r * RPC * E);     // z of the CTA's rows
+    s.nw = o; o = up(o + RPC * E);        // norm weight of the CTA's rows
+    s.ab = o; o = up(o + 2 * r * 4);      // a, b per row
+    s.qs = o; o += D * 4;
+    s.ks = o; o += D * 4;
+    s.vs = o; o = up(o + RPC * 4);
+    s.red = o; o += 64 * 4;
+    s.obuf = o; o = up(o + r * RPC * 4);
+    s.ssp = o; o = up(o + r * 4);
+    s.total = o;
+    return s;
 }
 
+constexpr int kRowsThreads = 256;
+
 template <int D, typename TA>
-__global__ void __launch_bounds__(512) k_rows(const __grid_constant__ RowsArgs A) {
+__global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ RowsArgs A) {
     constexpr int LPR = D / 4;     // lanes per state row (4 floats per lane)
     constexpr int RPI = 32 / LPR;  // rows per warp-wide 128-bit access
-    constexpr int NV = D / 16;     // float4 per lane: 8 rows per warp
+    constexpr int E = sizeof(TA);
     using L = Act<TA>;
     cg::cluster_group cluster = cg::this_cluster();
     const Geom& g = A.g;
     const RowsJob& J = A.job;
-    const int NS = A.NS, G = g.G, Hk = g.Hk, Hv = g.Hv, K = g.K, C = g.C_ch;
+    const int NS = A.NS, G = g.G, Hk = g.Hk, Hv = g.Hv, K = g.K, C = g.C_ch, Km1 = g.K - 1;
     const int CS = G * NS;
     const int gi = blockIdx.x / NS, s = blockIdx.x % NS;
     const int h = blockIdx.y, j = h * G + gi, bb = blockIdx.z;
-    const int RPC = D / NS;
+    const int RPC = D / NS, NCH = 2 * D + RPC;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int nthr = blockDim.x, nwarp = nthr >> 5;
+    constexpr int nthr = kRowsThreads, nwarp = kRowsThreads / 32;
     const int r = J.r;
     const int crank = (int)cluster.block_rank();
+    const bool raw = g.flags & kFlagRawQKV;
+    const bool outnorm = !(g.flags & kFlagNoOutNorm);
+    const bool direct = g.flags & kFlagGatesDirect;
+    // One slice per v-head: the output norm is local and the only cluster
+    // barrier orders the conv-state reads of the k-head group before its
+    // writes, so it can arrive early and wait late.  With NS > 1 the slices
+    // also exchange partial sums of o^2 through distributed shared memory.
+    const bool whole_head = NS == 1;
 
-    extern __shared__ float4 smem4[];
-    float* sm = reinterpret_cast<float*>(smem4);
-    float* qs = sm;                    // [D]   conv+SiLU output of q (this row)
-    float* ks = qs + D;                // [D]   ... of k
-    float* vs = ks + D;                // [RPC] ... of this slice's v
-    float* red = vs + D;               // [16 warps][4]
-    float* obuf = red + 64;            // [kMaxRows][RPC] o of every row
-    float* ssp = obuf + kMaxRows * D;  // [kMaxRows] partial sum of o^2
+    extern __shared__ __align__(128) unsigned char smem[];
+    const RowsSmem lay = rows_smem(D, RPC, r, K, E);
+    uint64_t* bar_in = reinterpret_cast<uint64_t*>(smem + lay.bar);  // small inputs
+    uint64_t* bar_s = bar_in + 1;                                     // the state slice
+    float* Sb = reinterpret_cast<float*>(smem + lay.S);
+    TA* xs = reinterpret_cast<TA*>(smem + lay.x);
+    TA* cs = reinterpret_cast<TA*>(smem + lay.c);
+    TA* wsm = reinterpret_cast<TA*>(smem + lay.w);
+    TA* zs = reinterpret_cast<TA*>(smem + lay.z);
+    TA* nw = reinterpret_cast<TA*>(smem + lay.nw);
+    float* ab = reinterpret_cast<float*>(smem + lay.ab);
+    float* qs = reinterpret_cast<float*>(smem + lay.qs);
+    float* ks = reinterpret_cast<float*>(smem + lay.ks);
+    float* vs = reinterpret_cast<float*>(smem + lay.vs);
+    float* red = reinterpret_cast<float*>(smem + lay.red);
+    float* obuf = reinterpret_cast<float*>(smem + lay.obuf);
+    float* ssp = reinterpret_cast<float*>(smem + lay.ssp);
 
     const int slot = J.slot_idx[bb];
     if (slot < 0 || slot >= J.n_slots) return;  // the whole cluster shares bb
 
-    // ---- issue the state loads first: they overlap the prologue --------------
-    const int row0 = s * RPC + warp * 8;
-    const int col4 = lane % LPR, rsub = lane / LPR;
-    float4 sreg[NV];
-    {
-        const float* Sb = J.state_pool + ((size_t)slot * Hv + j) * D * D;
-#pragma unroll
-        for (int i = 0; i < NV; ++i)
-            sreg[i] = *reinterpret_cast<const float4*>(Sb + (size_t)(row0 + i * RPI + rsub) * D + col4 * 4);
-    }
+    // the CTA's channels: q and k of k-head h, the slice of v of v-head j
+    const int ch_q = h * D, ch_k = Hk * D + h * D, ch_v = 2 * Hk * D + j * D + s * RPC;
+    float* Sg = J.state_pool + (((size_t)slot * Hv + j) * D + (size_t)s * RPC) * D;
 
-    const bool direct = g.flags & kFlagGatesDirect;
+    // ---- stage everything with bulk async copies (one thread issues) ----------
+    if (tid == 0) {
+        mbar_init(bar_in, 1);
+        mbar_init(bar_s, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(bar_s, RPC * D * 4);
+        bulk_g2s(Sb, Sg, RPC * D * 4, bar_s);
+        const bool conv_w = !raw && A.p.conv_w;
+        const uint32_t bytes = (r + Km1) * NCH * E + (conv_w ? NCH * K * E : 0) + (outnorm ? (r + 1) * RPC * E : 0);
+        mbar_arrive_expect_tx(bar_in, bytes);
+        const char* cg_ = static_cast<const char*>(J.conv_pool);
+        for (int m = 0; m < Km1; ++m) {
+            const char* row = cg_ + ((size_t)slot * Km1 + m) * C * E;
+            bulk_g2s(cs + m * NCH, row + (size_t)ch_q * E, D * E, bar_in);
+            bulk_g2s(cs + m * NCH + D, row + (size_t)ch_k * E, D * E, bar_in);
+            bulk_g2s(cs + m * NCH + 2 * D, row + (size_t)ch_v * E, RPC * E, bar_in);
+        }
+        const char* xg = static_cast<const char*>(J.x);
+        for (int t = 0; t < r; ++t) {
+            const char* row = xg + ((size_t)bb * r + t) * C * E;
+            bulk_g2s(xs + t * NCH, row + (size_t)ch_q * E, D * E, bar_in);
+            bulk_g2s(xs + t * NCH + D, row + (size_t)ch_k * E, D * E, bar_in);
+            bulk_g2s(xs + t * NCH + 2 * D, row + (size_t)ch_v * E, RPC * E, bar_in);
+        }
+        if (conv_w) {
+            const char* w = static_cast<const char*>(A.p.conv_w);
+            bulk_g2s(wsm, w + (size_t)ch_q * K * E, D * K * E, bar_in);
+            bulk_g2s(wsm + D * K, w + (size_t)ch_k * K * E, D * K * E, bar_in);
+            bulk_g2s(wsm + 2 * D * K, w + (size_t)ch_v * K * E, RPC * K * E, bar_in);
+        }
+        if (outnorm) {
+            const char* zg = static_cast<const char*>(J.z);
+            for (int t = 0; t < r; ++t)
+                bulk_g2s(zs + t * RPC, zg + (((size_t)bb * r + t) * Hv * D + (size_t)j * D + s * RPC) * E, RPC * E,
+                         bar_in);
+            bulk_g2s(nw, static_cast<const char*>(A.p.norm_w) + (size_t)s * RPC * E, RPC * E, bar_in);
+        }
+    }
+    for (int i = tid; i < 2 * r; i += nthr) {
+        const size_t rowx = (size_t)bb * r + (i >> 1);
+        ab[i] = L::ld((i & 1) ? J.b : J.a, rowx * Hv + j);
+    }
     const float A_log_j = direct ? 0.0f : A.p.A_log[j];
     const float dt_j = (!direct && A.p.dt_bias) ? A.p.dt_bias[j] : 0.0f;
+    __syncthreads();  // barriers initialised, a/b staged
+    // one warp polls the barrier, the others sleep in bar.sync
+    bool ok = true;
+    if (warp == 0) {
+        ok = mbar_wait(bar_in, 0);
+        if (!ok) mbar_wait(bar_in, 0);  // bounded again: let the copies in flight land
+    }
+    ok = __syncthreads_and(ok);
+    if (whole_head) cluster_arrive_release();  // this CTA's conv-state reads are done (in shared memory)
 
+    // ---- prologue of every row (conv, norms, gates) from shared memory --------
+    auto conv = [&](int lc, int t) -> float {
+        if (raw) return L::ld(xs, (size_t)t * NCH + lc);
+        const int ch = lc < D ? ch_q + lc : (lc < 2 * D ? ch_k + lc - D : ch_v + lc - 2 * D);
+        float c = A.p.conv_b ? L::ld(A.p.conv_b, ch) : 0.0f;
+        for (int m = 0; m < K; ++m) {
+            const int tau = t - Km1 + m;
+            const float xv = tau >= 0 ? L::ld(xs, (size_t)tau * NCH + lc) : L::ld(cs, (size_t)(Km1 + tau) * NCH + lc);
+            c = fmaf(L::ld(wsm, (size_t)lc * K + m), xv, c);
+        }
+        return siluf_(c);
+    };
+    const int col4 = lane % LPR, rsub = lane / LPR;
+    bool s_ok = true;
     for (int t = 0; t < r; ++t) {
         const size_t rowx = (size_t)bb * r + t;
-        __syncthreads();  // readers of qs/ks/vs/red from the previous row are done
         float sq = 0.f, sk = 0.f, sqk = 0.f;
-        for (int c = tid; c < D; c += nthr) {
-            const float qv = conv_at<TA>(A, h * D + c, t, bb, slot);
-            const float kv = conv_at<TA>(A, Hk * D + h * D + c, t, bb, slot);
-            qs[c] = qv;
-            ks[c] = kv;
-            sq = fmaf(qv, qv, sq);
-            sk = fmaf(kv, kv, sk);
-            sqk = fmaf(qv, kv, sqk);
+        if (ok) {
+            for (int c = tid; c < D; c += nthr) {
+                const float qv = conv(c, t), kv = conv(D + c, t);
+                qs[c] = qv;
+                ks[c] = kv;
+                sq = fmaf(qv, qv, sq);
+                sk = fmaf(kv, kv, sk);
+                sqk = fmaf(qv, kv, sqk);
+            }
+            for (int c = tid; c < RPC; c += nthr) vs[c] = conv(2 * D + c, t);
         }
-        for (int c = tid; c < RPC; c += nthr) vs[c] = conv_at<TA>(A, 2 * Hk * D + j * D + s * RPC + c, t, bb, slot);
         sq = warp_sum(sq);
         sk = warp_sum(sk);
         sqk = warp_sum(sqk);
@@ -139,7 +224,17 @@ __global__ void __launch_bounds__(512) k_rows(const __grid_constant__ RowsArgs A
             red[warp * 4 + 1] = sk;
             red[warp * 4 + 2] = sqk;
         }
-        __syncthreads();
+        if (t == 0) {
+            if (warp == 0) {
+                s_ok = mbar_wait(bar_s, 0);
+                if (!s_ok) mbar_wait(bar_s, 0);  // bounded again: let the state copy land
+            }
+            ok = __syncthreads_and(ok && s_ok);  // one verdict for the whole CTA
+            if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
+        } else {
+            __syncthreads();
+        }
+        if (!ok) break;
         sq = sk = sqk = 0.f;
         for (int w = 0; w < nwarp; ++w) {
             sq += red[w * 4 + 0];
@@ -156,7 +251,7 @@ __global__ void __launch_bounds__(512) k_rows(const __grid_constant__ RowsArgs A
         }
         const float kq = sqk * rq * rk;
         float gl, beta;
-        gates(L::ld(J.a, rowx * Hv + j), L::ld(J.b, rowx * Hv + j), A_log_j, dt_j, direct, gl, beta);
+        gates(ab[2 * t], ab[2 * t + 1], A_log_j, dt_j, direct, gl, beta);
         const float alpha = expf(gl);
         float kr[4], qr[4];
 #pragma unroll
@@ -164,49 +259,93 @@ __global__ void __launch_bounds__(512) k_rows(const __grid_constant__ RowsArgs A
             kr[e] = ks[col4 * 4 + e] * rk;
             qr[e] = qs[col4 * 4 + e] * rq;
         }
+        const int dst = J.snap_idx ? J.snap_idx[rowx] : -1;
+        float* Sd = (dst >= 0 && dst < J.n_slots)
+                        ? J.state_pool + (((size_t)dst * Hv + j) * D + (size_t)s * RPC) * D
+                        : nullptr;
+        if constexpr (D == 128) {
+            // 8 rows per warp group; the 16 partial dot products (S.k, S.q of the
+            // 8 rows) are reduced across the 32 lanes with a transposing butterfly
+            // (16 shuffles instead of 80): lane l ends with the sum of value l >> 1.
+            for (int rb = warp * 8; rb < RPC; rb += nwarp * 8) {
+                float4 sv[8];
+                float v[16];
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-            float dk = sreg[i].x * kr[0];
-            dk = fmaf(sreg[i].y, kr[1], dk);
-            dk = fmaf(sreg[i].z, kr[2], dk);
-            dk = fmaf(sreg[i].w, kr[3], dk);
-            float dq = sreg[i].x * qr[0];
-            dq = fmaf(sreg[i].y, qr[1], dq);
-            dq = fmaf(sreg[i].z, qr[2], dq);
-            dq = fmaf(sreg[i].w, qr[3], dq);
+                for (int i = 0; i < 8; ++i) {
+                    sv[i] = *reinterpret_cast<const float4*>(Sb + (rb + i) * D + lane * 4);
+                    float dk = sv[i].x * kr[0];
+                    dk = fmaf(sv[i].y, kr[1], dk);
+                    dk = fmaf(sv[i].z, kr[2], dk);
+                    v[i] = fmaf(sv[i].w, kr[3], dk);
+                    float dq = sv[i].x * qr[0];
+                    dq = fmaf(sv[i].y, qr[1], dq);
+                    dq = fmaf(sv[i].z, qr[2], dq);
+                    v[8 + i] = fmaf(sv[i].w, qr[3], dq);
+                }
+#pragma unroll
+                for (int n = 8, off = 16; n >= 1; n >>= 1, off >>= 1) {
+                    const bool upper = lane & off;
+#pragma unroll
+                    for (int i = 0; i < n; ++i) {
+                        const float send = upper ? v[i] : v[i + n];
+                        const float keep = upper ? v[i + n] : v[i];
+                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    }
+                }
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+                const int idx = lane >> 1;  // 0..7: S.k of row rb+idx; 8..15: S.q of row rb+idx-8
+                const float e_mine = idx < 8 ? vs[rb + idx] - alpha * v[0] : 0.f;
+                float ei[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ei[i] = __shfl_sync(0xffffffffu, e_mine, 2 * i);
+                const float e_for_q = __shfl_sync(0xffffffffu, e_mine, ((idx - 8) & 7) * 2);
+                if (idx >= 8 && !(lane & 1)) obuf[t * RPC + rb + idx - 8] = fmaf(alpha, v[0], beta * e_for_q * kq);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float be = beta * ei[i];
+                    sv[i].x = fmaf(alpha, sv[i].x, be * kr[0]);
+                    sv[i].y = fmaf(alpha, sv[i].y, be * kr[1]);
+                    sv[i].z = fmaf(alpha, sv[i].z, be * kr[2]);
+                    sv[i].w = fmaf(alpha, sv[i].w, be * kr[3]);
+                    *reinterpret_cast<float4*>(Sb + (rb + i) * D + lane * 4) = sv[i];
+                    if (Sd) *reinterpret_cast<float4*>(Sd + (rb + i) * D + lane * 4) = sv[i];  // verify snapshot
+                }
+            }
+        } else {
+#pragma unroll 4
+        for (int rb = warp * RPI; rb < RPC; rb += nwarp * RPI) {
+            const int rl = rb + rsub;  // row within the slice
+            float4* sp = reinterpret_cast<float4*>(Sb + rl * D + col4 * 4);
+            float4 sv = *sp;
+            float dk = sv.x * kr[0];
+            dk = fmaf(sv.y, kr[1], dk);
+            dk = fmaf(sv.z, kr[2], dk);
+            dk = fmaf(sv.w, kr[3], dk);
+            float dq = sv.x * qr[0];
+            dq = fmaf(sv.y, qr[1], dq);
+            dq = fmaf(sv.z, qr[2], dq);
+            dq = fmaf(sv.w, qr[3], dq);
 #pragma unroll
             for (int off = LPR / 2; off > 0; off >>= 1) {
                 dk += __shfl_xor_sync(0xffffffffu, dk, off);
                 dq += __shfl_xor_sync(0xffffffffu, dq, off);
             }
-            const int rl = warp * 8 + i * RPI + rsub;  // row within the slice
             const float e = vs[rl] - alpha * dk;
             const float be = beta * e;
-            sreg[i].x = fmaf(alpha, sreg[i].x, be * kr[0]);
-            sreg[i].y = fmaf(alpha, sreg[i].y, be * kr[1]);
-            sreg[i].z = fmaf(alpha, sreg[i].z, be * kr[2]);
-            sreg[i].w = fmaf(alpha, sreg[i].w, be * kr[3]);
+            sv.x = fmaf(alpha, sv.x, be * kr[0]);
+            sv.y = fmaf(alpha, sv.y, be * kr[1]);
+            sv.z = fmaf(alpha, sv.z, be * kr[2]);
+            sv.w = fmaf(alpha, sv.w, be * kr[3]);
+            *sp = sv;
+            if (Sd) *reinterpret_cast<float4*>(Sd + rl * D + col4 * 4) = sv;  // verify snapshot
             if (col4 == 0) obuf[t * RPC + rl] = fmaf(alpha, dq, be * kq);
         }
-        if (J.snap_idx) {  // verify: the state after row t goes to its snapshot slot
-            const int dst = J.snap_idx[rowx];
-            if (dst >= 0 && dst < J.n_slots) {
-                float* Sd = J.state_pool + ((size_t)dst * Hv + j) * D * D;
-#pragma unroll
-                for (int i = 0; i < NV; ++i)
-                    *reinterpret_cast<float4*>(Sd + (size_t)(row0 + i * RPI + rsub) * D + col4 * 4) = sreg[i];
-            }
         }
-    }
-    if (!J.snap_idx) {  // decode: in place
-        float* Sd = J.state_pool + ((size_t)slot * Hv + j) * D * D;
-#pragma unroll
-        for (int i = 0; i < NV; ++i)
-            *reinterpret_cast<float4*>(Sd + (size_t)(row0 + i * RPI + rsub) * D + col4 * 4) = sreg[i];
+        __syncthreads();  // qs/ks/vs/red reused by the next row; obuf complete
     }
 
-    // ---- output gated RMSNorm: sum of o^2 over the head's D rows --------------
-    __syncthreads();
+    // ---- state back (decode: in place, one bulk store) and the output ---------
+    fence_proxy_async_smem();
     for (int t = warp; t < r; t += nwarp) {
         float ss = 0.f;
         for (int rr = lane; rr < RPC; rr += 32) {
@@ -216,49 +355,56 @@ __global__ void __launch_bounds__(512) k_rows(const __grid_constant__ RowsArgs A
         ss = warp_sum(ss);
         if (lane == 0) ssp[t] = ss;
     }
-    cluster.sync();  // partials visible; every conv-state read in this cluster is done
-
-    const bool outnorm = !(g.flags & kFlagNoOutNorm);
-    for (int idx = tid; idx < r * RPC; idx += nthr) {
-        const int t = idx / RPC, rr = idx % RPC;
-        const size_t rowx = (size_t)bb * r + t;
-        const int dv = s * RPC + rr;
-        const float o = obuf[idx];
-        float yv = o;
-        if (outnorm) {
-            float tot = 0.f;
-            for (int s2 = 0; s2 < NS; ++s2) tot += *cluster.map_shared_rank(&ssp[t], gi * NS + s2);
-            const float zz = L::ld(J.z, rowx * (size_t)Hv * D + (size_t)j * D + dv);
-            yv = o * rsqrtf(tot / (float)D + g.norm_eps) * L::ld(A.p.norm_w, dv) * siluf_(zz);
-        }
-        L::st(J.y, rowx * (size_t)Hv * D + (size_t)j * D + dv, yv);
+    __syncthreads();
+    if (!whole_head) cluster_arrive_release();  // partial sums and conv-state reads are done
+    if (tid == 0 && ok && !J.snap_idx) {
+        bulk_s2g(Sg, Sb, RPC * D * 4);
+        bulk_commit();
     }
+    if (!whole_head) cluster_wait_acquire();
 
-    // ---- conv state: last K-1 raw inputs, after the barrier --------------------
-    const int Km1 = K - 1;
-    auto roll = [&](int ch) {
-        float old[3];
-#pragma unroll
-        for (int m = 0; m < 3; ++m)
-            old[m] = m < Km1 ? L::ld(J.conv_pool, ((size_t)slot * Km1 + m) * C + ch) : 0.0f;
-        auto val = [&](int p) -> float {
-            return p < Km1 ? old[p] : L::ld(J.x, ((size_t)bb * r + (p - Km1)) * C + ch);
-        };
-        if (!J.snap_idx) {
-            for (int m = 0; m < Km1; ++m) L::st(J.conv_pool, ((size_t)slot * Km1 + m) * C + ch, val(r + m));
-        } else {
-            for (int t = 0; t < r; ++t) {
-                const int dst = J.snap_idx[(size_t)bb * r + t];
-                if (dst < 0 || dst >= J.n_slots) continue;
-                for (int m = 0; m < Km1; ++m)
-                    L::st(J.conv_pool, ((size_t)dst * Km1 + m) * C + ch, val(t + 1 + m));
+    if (ok) {
+        for (int idx = tid; idx < r * RPC; idx += nthr) {
+            const int t = idx / RPC, rr = idx % RPC;
+            const size_t rowx = (size_t)bb * r + t;
+            const int dv = s * RPC + rr;
+            const float o = obuf[idx];
+            float yv = o;
+            if (outnorm) {
+                float tot = ssp[t];
+                if (!whole_head) {
+                    tot = 0.f;
+                    for (int s2 = 0; s2 < NS; ++s2) tot += *cluster.map_shared_rank(&ssp[t], gi * NS + s2);
+                }
+                yv = o * rsqrtf(tot / (float)D + g.norm_eps) * L::ld(nw, rr) * siluf_(L::ld(zs, idx));
             }
+            L::st(J.y, rowx * (size_t)Hv * D + (size_t)j * D + dv, yv);
         }
-    };
-    for (int c = crank + CS * tid; c < 2 * D; c += CS * nthr) roll(c < D ? h * D + c : Hk * D + h * D + (c - D));
-    for (int c = tid; c < RPC; c += nthr) roll(2 * Hk * D + j * D + s * RPC + c);
-
-    cluster.sync();  // peers may still read this CTA's partial sums
+    }
+    if (whole_head) cluster_wait_acquire();  // every CTA of the group has read its conv state
+    if (ok) {
+        // conv state: the last K-1 raw inputs, copied bit for bit
+        TA* cpool = static_cast<TA*>(J.conv_pool);
+        auto roll = [&](int lc, int ch) {
+            auto val = [&](int p) -> TA { return p < Km1 ? cs[p * NCH + lc] : xs[(p - Km1) * NCH + lc]; };
+            if (!J.snap_idx) {
+                for (int m = 0; m < Km1; ++m) cpool[((size_t)slot * Km1 + m) * C + ch] = val(r + m);
+            } else {
+                for (int t = 0; t < r; ++t) {
+                    const int dst = J.snap_idx[(size_t)bb * r + t];
+                    if (dst < 0 || dst >= J.n_slots) continue;
+                    for (int m = 0; m < Km1; ++m) cpool[((size_t)dst * Km1 + m) * C + ch] = val(t + 1 + m);
+                }
+            }
+        };
+        for (int c = crank + CS * tid; c < 2 * D; c += CS * nthr) roll(c, c < D ? ch_q + c : ch_k + c - D);
+        for (int c = tid; c < RPC; c += nthr) roll(2 * D + c, ch_v + c);
+    }
+    if (!whole_head) {
+        cluster_arrive_relaxed();  // peers are done reading this CTA's partial sums
+        cluster_wait_acquire();
+    }
+    if (tid == 0) bulk_wait_read_all();  // the state store has read its shared-memory source
 }
 
 int choose_slices(const Geom& g, int B) {
@@ -267,21 +413,27 @@ int choose_slices(const Geom& g, int B) {
         int v = std::atoi(e);
         if (v >= 1 && v <= max_ns && (v & (v - 1)) == 0) return v;
     }
-    // enough CTAs to cover 152 SMs a few times over, fewest slices otherwise
-    int ns = 1;
-    while (ns < max_ns && (long)B * g.Hv * ns < 4L * 152) ns *= 2;
-    if (g.D == 128 && ns < 2 && max_ns >= 2) ns = 2;  // 256-thread CTAs for the 128x128 state
-    return ns;
+    // One CTA per v-head (whole 128x128 state in shared memory, local output
+    // norm) measured best or equal at every batch from 1 to 256 on GB300;
+    // slicing the rows (NS > 1) stays available for experiments and tests.
+    return 1;
 }
 
 template <int D, typename TA>
 cudaError_t launch_rows_t(const Geom& g, const LayerParams& p, const RowsJob& job, cudaStream_t st) {
     const int NS = choose_slices(g, job.B);
     RowsArgs A{g, p, job, NS};
+    const RowsSmem lay = rows_smem(D, D / NS, job.r, g.K, (int)sizeof(TA));
+    static bool attr_set = false;  // once per instantiation: allow up to 200 KB
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_rows<D, TA>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(g.G * NS, g.Hk, job.B);
-    cfg.blockDim = dim3((D / NS) * 4);  // D/NS rows, 8 rows per warp
-    cfg.dynamicSmemBytes = (size_t)(3 * D + 64 + kMaxRows * D + kMaxRows) * sizeof(float);
+    cfg.blockDim = dim3(kRowsThreads);
+    cfg.dynamicSmemBytes = (size_t)lay.total;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -396,6 +548,8 @@ cudaError_t launch_conv_update(const Geom& g, const LayerParams& p, const ConvJo
     }
     return cudaGetLastError();
 }
+
+cudaError_t take_device_status_decode(unsigned* out) { return take_device_status_tu(out); }
 
 cudaError_t launch_commit(const Geom& g, const CommitJob& job, cudaStream_t st) {
     if (job.B == 0) return cudaSuccess;

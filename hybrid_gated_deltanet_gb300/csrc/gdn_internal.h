@@ -80,4 +80,8 @@ size_t prefill_workspace_bytes(const Geom& g, int64_t n_tokens, int n_seq);
 cudaError_t launch_prefill(const Geom& g, const LayerParams& prm, const PrefillJob& job,
                            cudaStream_t st);
 
+// read and clear the device status word of each kernel file (synchronous)
+cudaError_t take_device_status_decode(unsigned* out);
+cudaError_t take_device_status_prefill(unsigned* out);
+
 }  // namespace gdn

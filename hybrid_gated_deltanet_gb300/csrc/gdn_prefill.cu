@@ -618,6 +618,8 @@ cudaError_t launch_prefill_t(const Geom& g, const LayerParams& p, const PrefillJ
 
 }  // namespace
 
+cudaError_t take_device_status_prefill(unsigned* out) { return take_device_status_tu(out); }
+
 size_t prefill_workspace_bytes(const Geom& g, int64_t n_tokens, int n_seq) {
     (void)n_seq;
     if (n_tokens <= 0) return 0;

@@ -32,10 +32,11 @@
  *   the value found and the value required (Strata chapter 6, sections 6.2
  *   and 6.5: report the tensor, the shape found and the shape required;
  *   refuse with both numbers).
- * - Alignment (GDN_ERR_ALIGN otherwise): state pools, s0, s_final, conv
- *   pools and the workspace 16 bytes (they are moved with 128-bit accesses);
- *   activation arrays and parameters their element size (2 for bf16, 4 for
- *   fp32); int32 arrays 4 bytes.
+ * - Alignment (GDN_ERR_ALIGN otherwise): 16 bytes for the state pools, s0,
+ *   s_final, the conv pools, conv_w, norm_w, the workspace, and x and z of
+ *   the decode and verify calls (these move with bulk or 128-bit copies);
+ *   the element size (2 for bf16, 4 for fp32) for the other activation
+ *   arrays and parameters; 4 bytes for int32 arrays.
  * - Layouts are row-major and dense.  "act" means the activation dtype of the
  *   config (bf16 or fp32).  Channel order of x is [q | k | v], head-major:
  *   q of k-head h at h*d_k, k at H_k*d_k + h*d_k, v of v-head j at
@@ -220,6 +221,15 @@ size_t gdn_workspace_size(const gdn_config* cfg, int32_t op, int64_t n_tokens, i
 /* Message of the last failed call on this host thread ("" if none).  The
  * string stays valid until the next call on this thread. */
 const char* gdn_last_error(void);
+
+/* Device-side status: every wait inside the kernels is bounded (about one
+ * second); a kernel whose wait gives up skips its remaining work, leaves its
+ * outputs incomplete and ORs a code into a status word on the device instead
+ * of hanging.  This call reads and clears that word for the current device
+ * (*status = 0: nothing reported; bit GDN_DEV_WAIT_TIMEOUT: a wait gave up).
+ * It synchronises the current device. */
+enum { GDN_DEV_WAIT_TIMEOUT = 1u };
+gdn_status gdn_device_status(uint32_t* status);
 
 /* Library version string. */
 const char* gdn_version(void);

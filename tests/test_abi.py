@@ -86,7 +86,7 @@ def test_null_and_alignment(lib):
     assert _decode(lib, _cfg(), x=0) == -1
     assert "x: found NULL, required a device pointer" in _err(lib)
     assert _decode(lib, _cfg(), x=FAKE + 1) == -4
-    assert "x: found address" in _err(lib) and "2-byte alignment" in _err(lib)
+    assert "x: found address" in _err(lib) and "16-byte alignment" in _err(lib)
     prm = gb.CParams(FAKE, None, None, None, FAKE)
     assert _decode(lib, _cfg(), prm=prm) == -1 and "prm.A_log" in _err(lib)
 

@@ -53,6 +53,29 @@ def test_decode_step_qwen35_4b(B):
     untouched = np.setdiff1d(np.arange(S.shape[0]), slots)
     np.testing.assert_array_equal(s_got[untouched], S.f64[untouched])
     np.testing.assert_array_equal(c_got[untouched], CS.f64[untouched])
+    assert gb.gdn_device_status() == 0  # no bounded wait gave up
+
+
+@pytest.mark.parametrize("slices", ["1", "2", "4"])
+def test_decode_row_slices(slices, monkeypatch):
+    """The state rows of a v-head split over 1, 2 or 4 CTAs of a cluster (output
+    norm through distributed shared memory) give the same parity."""
+    monkeypatch.setenv("GDN_DECODE_SLICES", slices)
+    geom, act, p, tok, S, CS, slots = _pool_case("decode4b", 8, stream=77)
+    cfg = config(geom, act)
+    sp, cp = dev(S), dev(CS)
+    y = torch.empty((8, geom.value_dim), dtype=cfg.torch_dtype, device="cuda")
+    gb.gdn_decode_step(cfg, params_dev(p), dev(tok["x"]), dev(tok["z"]), dev(tok["a"]), dev(tok["b"]), cp, sp,
+                       torch.from_numpy(slots).cuda(), y)
+    torch.cuda.synchronize()
+    s_got, c_got, y_got = host(sp), host(cp), host(y)
+    ys, yr, ss, sr = [], [], [], []
+    for b in range(8):
+        ref = _oracle_slot(geom, p, tok, S, CS, slots[b], slice(b, b + 1))
+        ys.append(y_got[b]); yr.append(ref["y"][0]); ss.append(s_got[slots[b]]); sr.append(ref["S"])
+        np.testing.assert_array_equal(c_got[slots[b]], ref["conv"])
+    errs = {"y": rel_fro(ys, yr), "S": rel_fro(ss, sr)}
+    assert errs["y"] <= 2e-2 and errs["S"] <= 1e-3, fmt(errs)
 
 
 def test_decode_16_consecutive_steps():
