@@ -38,6 +38,8 @@
 
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_tc.cuh"
+#include "gdn_tma.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -120,81 +122,158 @@ __device__ __forceinline__ const void* seq_conv_in(const PrefillJob& J, const Ge
 // ---------------------------------------------------------------------------
 // 1. prologue
 // ---------------------------------------------------------------------------
-constexpr int kProTok = 4;  // tokens per CTA
+// Thread = VEC consecutive channels (16 bytes of activations) x kProTok
+// consecutive tokens.  The d_conv raw rows of the window stay in registers and
+// slide by one row per token, so every x element is read once; taps that fall
+// before a sequence start come from that sequence's conv state.  The L2 norm
+// of a q/k head is a shuffle reduction over the D/VEC lanes that hold it.
+constexpr int kProTok = 16;      // tokens per CTA
+constexpr int kProThreads = 256;
+
+template <typename TA>
+struct Vec16;  // 16 bytes of activations
+template <>
+struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    static __device__ __forceinline__ void load(const void* p, float* out) {
+        const uint4 u = *static_cast<const uint4*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(h[i]);
+            out[2 * i] = f.x;
+            out[2 * i + 1] = f.y;
+        }
+    }
+};
+template <>
+struct Vec16<float> {
+    static constexpr int N = 4;
+    static __device__ __forceinline__ void load(const void* p, float* out) {
+        const float4 f = *static_cast<const float4*>(p);
+        out[0] = f.x; out[1] = f.y; out[2] = f.z; out[3] = f.w;
+    }
+};
 
 template <int D, typename TA>
-__global__ void __launch_bounds__(256) k_prologue(const __grid_constant__ PrefillArgs A) {
+__global__ void __launch_bounds__(kProThreads) k_prologue(const __grid_constant__ PrefillArgs A) {
     using L = Act<TA>;
-    constexpr int CPL = D / 32;  // channels per lane
+    using V = Vec16<TA>;
+    constexpr int VEC = V::N;
+    constexpr int LPH = D / VEC;  // lanes per head
     const Geom& g = A.g;
     const PrefillJob& J = A.J;
     const int Hk = g.Hk, Hv = g.Hv, K = g.K, C = g.C_ch;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarp = blockDim.x >> 5;
-    const int items = 2 * Hk + Hv;
-    const int64_t tok0 = (int64_t)blockIdx.x * kProTok;
+    const int tid = threadIdx.x;
+    const int64_t t0 = (int64_t)blockIdx.x * kProTok;
     const bool raw = g.flags & kFlagRawQKV;
-    for (int it = warp; it < kProTok * items; it += nwarp) {
-        const int64_t n = tok0 + it / items;
-        if (n >= J.n_tokens) break;
-        const int item = it % items;
-        const int s = find_seq(J, n);
-        int64_t start, end;
-        seq_bounds(J, s, start, end);
-        int slot_ok;
-        const void* cin = seq_conv_in(J, g, s, slot_ok);
-        const int ch0 = item * D;  // [q heads | k heads | v heads] matches the channel order
-        float u[CPL];
-        float ss = 0.f;
-#pragma unroll
-        for (int e = 0; e < CPL; ++e) {
-            const int ch = ch0 + lane + 32 * e;
-            float val;
-            if (raw) {
-                val = L::ld(J.x, (size_t)n * C + ch);
-            } else {
-                float c = A.p.conv_b ? L::ld(A.p.conv_b, ch) : 0.f;
-                for (int m = 0; m < K; ++m) {
-                    const int64_t tau = n - (K - 1) + m;
-                    float xv;
-                    // history before the sequence start comes from its conv state; the
-                    // bounds keep every read in range even for inconsistent cu_seqlens
-                    if (tau >= start && tau <= n) xv = L::ld(J.x, (size_t)tau * C + ch);
-                    else if (cin && tau < start && tau - start >= -(K - 1))
-                        xv = L::ld(cin, (size_t)((K - 1) + (tau - start)) * C + ch);
-                    else xv = 0.f;
-                    c = fmaf(L::ld(A.p.conv_w, (size_t)ch * K + m), xv, c);
-                }
-                val = siluf_(c);
-            }
-            u[e] = val;
-            ss = fmaf(val, val, ss);
-        }
-        if (item < 2 * Hk) {
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            float scale;
-            if (g.flags & kFlagNoL2) scale = item < Hk ? g.q_scale : 1.f;
-            else scale = (item < Hk ? g.q_scale : 1.f) * rsqrtf(ss + g.l2_eps);
-            float* dst = A.qk + ((size_t)n * 2 * Hk + item) * D;
-#pragma unroll
-            for (int e = 0; e < CPL; ++e) dst[lane + 32 * e] = u[e] * scale;
-        } else {
-            float* dst = A.v + ((size_t)n * Hv + (item - 2 * Hk)) * D;
-#pragma unroll
-            for (int e = 0; e < CPL; ++e) dst[lane + 32 * e] = u[e];
+    const bool direct = g.flags & kFlagGatesDirect;
+
+    // gates of this CTA's tokens (first channel block only)
+    if (blockIdx.y == 0) {
+        for (int i = tid; i < kProTok * Hv; i += kProThreads) {
+            const int64_t n = t0 + i / Hv;
+            if (n >= J.n_tokens) break;
+            const int j = i % Hv;
+            float gl, be;
+            gates(L::ld(J.a, (size_t)n * Hv + j), L::ld(J.b, (size_t)n * Hv + j), direct ? 0.f : A.p.A_log[j],
+                  (!direct && A.p.dt_bias) ? A.p.dt_bias[j] : 0.f, direct, gl, be);
+            A.gl[(size_t)n * Hv + j] = gl;
+            A.beta[(size_t)n * Hv + j] = be;
         }
     }
-    // gates
-    const bool direct = g.flags & kFlagGatesDirect;
-    for (int i = threadIdx.x; i < kProTok * Hv; i += blockDim.x) {
-        const int64_t n = tok0 + i / Hv;
-        if (n >= J.n_tokens) break;
-        const int j = i % Hv;
-        float gl, be;
-        gates(L::ld(J.a, (size_t)n * Hv + j), L::ld(J.b, (size_t)n * Hv + j), direct ? 0.f : A.p.A_log[j],
-              (!direct && A.p.dt_bias) ? A.p.dt_bias[j] : 0.f, direct, gl, be);
-        A.gl[(size_t)n * Hv + j] = gl;
-        A.beta[(size_t)n * Hv + j] = be;
+
+    const int grp = blockIdx.y * kProThreads + tid;
+    const int ch0 = grp * VEC;
+    const bool active = ch0 < C;  // C is a multiple of VEC: a group is all in or all out
+    const int ch = active ? ch0 : 0;
+    // w[r][c]: weight of window row r (row n-3+r) for channel c; tap m of the
+    // K taps multiplies row n-(K-1)+m, i.e. window row r = 4-K+m
+    float w[4][VEC];
+    float bias[VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) {
+        bias[c] = (!raw && A.p.conv_b) ? L::ld(A.p.conv_b, ch + c) : 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int m = r - (4 - K);
+            w[r][c] = (!raw && m >= 0) ? L::ld(A.p.conv_w, (size_t)(ch + c) * K + m) : 0.f;
+        }
+    }
+    // win[3] is row n, win[2] row n-1, ... (zeros before token 0); before the
+    // first token win[1..3] hold rows t0-3 .. t0-1, shifted down at each token
+    float win[4][VEC];
+#pragma unroll
+    for (int c = 0; c < VEC; ++c) win[0][c] = 0.f;
+#pragma unroll
+    for (int m = 1; m < 4; ++m) {
+        const int64_t tau = t0 - 4 + m;
+        if (tau >= 0 && active) {
+            V::load(static_cast<const TA*>(J.x) + (size_t)tau * C + ch, win[m]);
+        } else {
+#pragma unroll
+            for (int c = 0; c < VEC; ++c) win[m][c] = 0.f;
+        }
+    }
+    const bool is_q = ch0 < Hk * D, is_qk = ch0 < 2 * Hk * D;
+    for (int tt = 0; tt < kProTok; ++tt) {
+        const int64_t n = t0 + tt;
+        if (n >= J.n_tokens) break;  // uniform over the CTA
+        // slide: win[1..K-1] hold rows n-(K-1)..n-1; load row n into win[K]
+#pragma unroll
+        for (int m = 0; m < 3; ++m)
+#pragma unroll
+            for (int c = 0; c < VEC; ++c) win[m][c] = win[m + 1][c];
+        if (active) V::load(static_cast<const TA*>(J.x) + (size_t)n * C + ch, win[3]);
+        // with K < 4 the window's live rows are win[4-K .. 3]
+        float u[VEC];
+        if (raw) {
+#pragma unroll
+            for (int c = 0; c < VEC; ++c) u[c] = win[3][c];
+        } else {
+            const int s = find_seq(J, n);
+            int64_t start, end;
+            seq_bounds(J, s, start, end);
+            int slot_ok;
+            const void* cin = seq_conv_in(J, g, s, slot_ok);
+#pragma unroll
+            for (int c = 0; c < VEC; ++c) u[c] = bias[c];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if (r < 4 - K) continue;  // not a tap
+                const int64_t tau = n - 3 + r;
+                if (tau >= start) {
+#pragma unroll
+                    for (int c = 0; c < VEC; ++c) u[c] = fmaf(w[r][c], win[r][c], u[c]);
+                } else if (cin && tau - start >= -(K - 1) && active) {
+                    float h[VEC];
+                    V::load(static_cast<const TA*>(cin) + (size_t)((K - 1) + (tau - start)) * C + ch, h);
+#pragma unroll
+                    for (int c = 0; c < VEC; ++c) u[c] = fmaf(w[r][c], h[c], u[c]);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < VEC; ++c) u[c] = siluf_(u[c]);
+        }
+        if (is_qk) {
+            float ss = 0.f;
+#pragma unroll
+            for (int c = 0; c < VEC; ++c) ss = fmaf(u[c], u[c], ss);
+#pragma unroll
+            for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            float scale = is_q ? g.q_scale : 1.f;
+            if (!(g.flags & kFlagNoL2)) scale *= rsqrtf(ss + g.l2_eps);
+            if (active) {
+                float4* dst = reinterpret_cast<float4*>(A.qk + (size_t)n * 2 * Hk * D + ch0);
+#pragma unroll
+                for (int c = 0; c < VEC; c += 4)
+                    dst[c / 4] = make_float4(u[c] * scale, u[c + 1] * scale, u[c + 2] * scale, u[c + 3] * scale);
+            }
+        } else if (active) {
+            float4* dst = reinterpret_cast<float4*>(A.v + (size_t)n * Hv * D + (ch0 - 2 * Hk * D));
+#pragma unroll
+            for (int c = 0; c < VEC; c += 4) dst[c / 4] = make_float4(u[c], u[c + 1], u[c + 2], u[c + 3]);
+        }
     }
 }
 
@@ -560,6 +639,427 @@ __global__ void __launch_bounds__(kChunkThreads, 1) k_chunk(const __grid_constan
     cluster.sync();  // peers may still read this CTA's partial sums
 }
 
+// ---------------------------------------------------------------------------
+// 3b. chunk kernel on the 5th-generation tensor cores (d = 128, C = 64, bf16)
+// ---------------------------------------------------------------------------
+// One CTA per (sequence, v-head j, slice of 32 of the 128 state rows); the 4
+// slices of a v-head form a cluster for the output norm.  The fp32 state
+// slice lives in TMEM as S^T (lane = d_k index, 32 columns = this slice's
+// d_v rows) for the whole sequence.  Per chunk of 64 tokens, four rounds of
+// tcgen05.mma (TF32 operands rounded to nearest, fp32 accumulation in TMEM):
+//   R1  KK^T, QK^T                      (64x64, K = 128)
+//   R2  U~ = (T diag(b)) V, W = (T diag(b e^g)) K, O1 = Q S^T
+//   R3  U = U~ - W S^T                  (negated-A accumulate)
+//   R4  O2 = P U, S^T <- e^gC S^T + K^T (diag(e^(gC - g)) U)
+// with the decay masks, the UT inverse T = (I + A)^-1 (16x16 blocks, fp32)
+// and the moves between TMEM and the 128B-swizzled operand tiles done by all
+// 256 threads in between.  y = gated RMSNorm(diag(e^g) O1 + O2).
+namespace tcp {
+constexpr int C = 64, D = 128, DV = 32, NS = 4, THREADS = 256, LDA = 68;
+constexpr int OFF_Q = 0;                      // Q^   [64][128] tf32 tile
+constexpr int OFF_K = OFF_Q + 32768;          // K^   [64][128], later W [64][128]
+constexpr int OFF_KT = OFF_K + 32768;         // K^T  [128][64]
+constexpr int OFF_VT = OFF_KT + 32768;        // V^T  [32][64], later (diag(e^(gC-g)) U)^T
+constexpr int OFF_S0 = OFF_VT + 8192;         // S    [32][128] (this slice's rows)
+constexpr int OFF_P = OFF_S0 + 16384;         // P    [64][64]
+constexpr int OFF_TB = OFF_P + 16384;         // T diag(b)      [64][64]
+constexpr int OFF_TW = OFF_TB + 16384;        // T diag(b e^g)  [64][64]
+constexpr int OFF_UT = OFF_TW + 16384;        // U^T  [32][64]
+constexpr int OFF_AM = OFF_UT + 8192;         // fp32 A (also the V staging area) [64][68]
+constexpr int OFF_TM = OFF_AM + C * LDA * 4;  // fp32 T [64][68]
+constexpr int OFF_SMALL = OFF_TM + C * LDA * 4;
+constexpr int SMALL_FLOATS = 4 * C + 2 * C + 2 * C;  // gam, bet, eg, erev, ssq[2], ored[2]
+constexpr int SMEM = OFF_SMALL + SMALL_FLOATS * 4 + 64;
+constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024 bytes
+// TMEM columns
+constexpr int cKK = 0, cQK = 64, cW = 128, cU = 256, cO1 = 288, cO2 = 320, cS = 352, TMEM_COLS = 512;
+}  // namespace tcp
+
+__global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_constant__ PrefillArgs A) {
+    using namespace tcp;
+    using L = Act<__nv_bfloat16>;
+    cg::cluster_group cluster = cg::this_cluster();
+    const Geom& g = A.g;
+    const PrefillJob& J = A.J;
+    const int Hk = g.Hk, Hv = g.Hv;
+    const int s_idx = blockIdx.x, j = blockIdx.y, seq = blockIdx.z, h = j / g.G;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int q4 = warp & 3, hf = warp >> 2;  // TMEM lane quadrant, column half
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
+    unsigned char *Qs = sm + OFF_Q, *Ks = sm + OFF_K, *KTs = sm + OFF_KT, *VTs = sm + OFF_VT, *S0s = sm + OFF_S0;
+    unsigned char *Ps = sm + OFF_P, *TBs = sm + OFF_TB, *TWs = sm + OFF_TW, *UTs = sm + OFF_UT;
+    float* Am = reinterpret_cast<float*>(sm + OFF_AM);
+    float* Tm = reinterpret_cast<float*>(sm + OFF_TM);
+    float* gam = reinterpret_cast<float*>(sm + OFF_SMALL);
+    float* bet = gam + C;
+    float* eg = bet + C;
+    float* erev = eg + C;
+    float* ssq = erev + C;   // [2][C]
+    float* ored = ssq + 2 * C;  // [2][C]
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(ored + 2 * C);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+
+    if (warp == 0) tc::alloc(tslot, TMEM_COLS);
+    if (tid == 0) {
+        mbar_init(mbar, 1);
+        fence_mbar_init();
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = *tslot;
+    uint32_t phase = 0;
+    bool ok = true;
+
+    int64_t start, end;
+    seq_bounds(J, seq, start, end);
+    const float* Sin = nullptr;
+    float* Sout = nullptr;
+    if (!J.cu_seqlens) {
+        Sin = J.s0 ? J.s0 + (size_t)j * D * D : nullptr;
+        Sout = J.s_final + (size_t)j * D * D;
+    } else {
+        const int slot = J.slot_idx[seq];
+        if (slot >= 0 && slot < J.n_slots) {
+            Sout = J.state_pool + ((size_t)slot * Hv + j) * D * D;
+            if (J.has_init && J.has_init[seq]) Sin = Sout;
+        }
+    }
+    const int dS = 32 * q4 + lane;  // the d_k index this thread owns in S^T
+    {
+        float v[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const int dv = hf * 16 + c;
+            v[c] = Sin ? Sin[(size_t)(s_idx * DV + dv) * D + dS] : 0.f;
+            tc::st_elem(S0s, DV, dv, dS, v[c]);
+        }
+        tc::st16(tc::taddr(tm, 32 * q4, cS + hf * 16), v);
+    }
+
+    auto mma_round_begin = [&]() {
+        tc::fence_before();
+        fence_proxy_async_smem();
+        __syncthreads();
+    };
+    auto mma_round_end = [&]() {
+        if (tid == 0) tc::commit(mbar);
+        bool w = true;
+        if (ok) {
+            w = mbar_wait(mbar, phase);
+            if (!w) w = mbar_wait(mbar, phase);
+        }
+        phase ^= 1u;
+        ok = __syncthreads_and(ok && w);
+        tc::fence_after();
+    };
+
+    const int64_t T = end - start;
+    const int n_chunks = (int)((T + C - 1) / C);
+    const bool outnorm = !(g.flags & kFlagNoOutNorm);
+    const int trow = 16 * q4 + (lane & 15);  // the chunk row this thread reads from M=64 accumulators
+    const bool rowok = lane < 16;
+    for (int ci = 0; ci < n_chunks; ++ci) {
+        const int64_t t0 = start + (int64_t)ci * C;
+        const int n = (int)((end - t0) < C ? (end - t0) : C);
+        __syncthreads();
+        // ---- (1) load q^, k^, v, g, beta of the chunk (rows >= n are zero) --------
+        for (int f = tid; f < C * 32; f += THREADS) {
+            const int r = f >> 5, c4 = f & 31;
+            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), qv = kv;
+            if (r < n) {
+                const size_t tok = (size_t)(t0 + r);
+                kv = *reinterpret_cast<const float4*>(A.qk + (tok * 2 * Hk + Hk + h) * D + c4 * 4);
+                qv = *reinterpret_cast<const float4*>(A.qk + (tok * 2 * Hk + h) * D + c4 * 4);
+            }
+            tc::st_row4(Ks, C, r, c4 * 4, kv.x, kv.y, kv.z, kv.w);
+            tc::st_row4(Qs, C, r, c4 * 4, qv.x, qv.y, qv.z, qv.w);
+        }
+        float* Vst = Am;  // [64][32] fp32 staging
+        for (int f = tid; f < C * (DV / 4); f += THREADS) {
+            const int r = f >> 3, c4 = f & 7;
+            float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (r < n) vv = *reinterpret_cast<const float4*>(A.v + ((size_t)(t0 + r) * Hv + j) * D + s_idx * DV + c4 * 4);
+            *reinterpret_cast<float4*>(Vst + r * DV + c4 * 4) = vv;
+        }
+        if (tid < C) {
+            gam[tid] = tid < n ? A.gl[(size_t)(t0 + tid) * Hv + j] : 0.f;
+            bet[tid] = tid < n ? A.beta[(size_t)(t0 + tid) * Hv + j] : 0.f;
+        }
+        __syncthreads();
+        // ---- (2) transposes; gamma = cumsum(g) -----------------------------------
+        for (int d = warp * 16; d < warp * 16 + 16; ++d)
+            for (int tb = 0; tb < C; tb += 32) {
+                const int t = tb + lane;
+                *reinterpret_cast<float*>(KTs + tc::sw_off(D, d, t)) =
+                    *reinterpret_cast<const float*>(Ks + tc::sw_off(C, t, d));
+            }
+        for (int dv = warp * 4; dv < warp * 4 + 4; ++dv)
+            for (int tb = 0; tb < C; tb += 32) {
+                const int t = tb + lane;
+                tc::st_elem(VTs, DV, dv, t, Vst[t * DV + dv]);
+            }
+        if (warp == 0) {
+            float run = 0.f;
+            for (int base = 0; base < C; base += 32) {
+                float v = gam[base + lane];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, v, off);
+                    if (lane >= off) v += o;
+                }
+                v += run;
+                gam[base + lane] = v;
+                eg[base + lane] = expf(v);
+                run = __shfl_sync(0xffffffffu, v, 31);
+            }
+            __syncwarp();
+            for (int t = lane; t < C; t += 32) erev[t] = expf(gam[C - 1] - gam[t]);
+        }
+        // ---- R1: KK^T, QK^T ----------------------------------------------------------
+        mma_round_begin();
+        if (tid == 0 && ok) {
+            tc::fence_after();
+            tc::mma_tf32(tm + cKK, Ks, C, Ks, C, D, tc::idesc_tf32(C, C), false);
+            tc::mma_tf32(tm + cQK, Qs, C, Ks, C, D, tc::idesc_tf32(C, C), false);
+        }
+        mma_round_end();
+        // ---- decay masks: A (strictly lower, beta_t), P (lower incl.) ---------------
+        for (int cb = 0; cb < 2; ++cb) {
+            const int i0 = hf * 32 + cb * 16;
+            float kk[16], qk[16];
+            tc::ld16(tc::taddr(tm, 32 * q4, cKK + i0), kk);
+            tc::ld16(tc::taddr(tm, 32 * q4, cQK + i0), qk);
+            if (rowok) {
+                const int t = trow;
+#pragma unroll
+                for (int c = 0; c < 16; c += 4) {
+                    float a4[4], p4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = i0 + c + e;
+                        const float dec = i <= t ? expf(gam[t] - gam[i]) : 0.f;  // exponent <= 0 only
+                        a4[e] = i < t ? bet[t] * dec * kk[c + e] : 0.f;
+                        p4[e] = dec * qk[c + e];
+                    }
+                    *reinterpret_cast<float4*>(Am + t * LDA + i0 + c) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+                    tc::st_row4(Ps, C, t, i0 + c, p4[0], p4[1], p4[2], p4[3]);
+                }
+            }
+        }
+        __syncthreads();
+        // ---- T = (I + A)^-1: 16x16 diagonal blocks, then block merges ------------------
+        if (warp < 4) {
+            const int b0 = warp * 16;
+            for (int i = 0; i < 16; ++i) {
+                float arow[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) arow[k] = Am[(b0 + i) * LDA + b0 + k];
+                __syncwarp();
+                if (lane < 16) {
+                    float x = (lane == i) ? 1.f : 0.f;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k)
+                        if (k >= lane && k < i) x -= arow[k] * Tm[(b0 + k) * LDA + b0 + lane];
+                    Tm[(b0 + i) * LDA + b0 + lane] = (lane <= i) ? x : 0.f;
+                }
+                __syncwarp();
+            }
+        }
+        for (int f = tid; f < C * C; f += THREADS) {
+            const int t = f >> 6, c = f & 63;
+            if ((c >> 4) > (t >> 4)) Tm[t * LDA + c] = 0.f;
+        }
+        __syncthreads();
+        for (int dd = 1; dd < 4; ++dd) {
+            // blocks (a, b) with a - b = dd; 2 warps per block, 4 elements per lane
+            const int nblk = 4 - dd;
+            if (warp < 2 * nblk) {
+                const int bb = warp >> 1, half = warp & 1;
+                const int a0 = (bb + dd) * 16, c0b = bb * 16;
+                float y[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int idx = half * 128 + lane + 32 * e, r = idx >> 4, c = idx & 15;
+                    float acc = 0.f;
+                    for (int k = c0b; k < a0; ++k) acc = fmaf(Am[(a0 + r) * LDA + k], Tm[k * LDA + c0b + c], acc);
+                    y[e] = acc;
+                }
+                // Y into the (unused) target block, then X_ab = -X_aa Y
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int idx = half * 128 + lane + 32 * e, r = idx >> 4, c = idx & 15;
+                    Tm[(a0 + r) * LDA + c0b + c] = y[e];
+                }
+            }
+            __syncthreads();
+            const bool act = warp < 2 * nblk;
+            const int bb = warp >> 1, half = warp & 1;
+            const int a0 = (bb + dd) * 16, c0b = bb * 16;
+            float y[4] = {0.f, 0.f, 0.f, 0.f};
+            if (act) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int idx = half * 128 + lane + 32 * e, r = idx >> 4, c = idx & 15;
+                    float acc = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) acc = fmaf(Tm[(a0 + r) * LDA + a0 + k], Tm[(a0 + k) * LDA + c0b + c], acc);
+                    y[e] = -acc;
+                }
+            }
+            __syncthreads();  // every read of Y done before it is overwritten
+            if (act) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int idx = half * 128 + lane + 32 * e, r = idx >> 4, c = idx & 15;
+                    Tm[(a0 + r) * LDA + c0b + c] = y[e];
+                }
+            }
+            __syncthreads();
+        }
+        // ---- T diag(beta) and T diag(beta e^gamma) as operand tiles ----------------------
+        for (int f = tid; f < C * 16; f += THREADS) {
+            const int t = f >> 4, i = (f & 15) * 4;
+            const float4 tv = *reinterpret_cast<const float4*>(Tm + t * LDA + i);
+            tc::st_row4(TBs, C, t, i, tv.x * bet[i], tv.y * bet[i + 1], tv.z * bet[i + 2], tv.w * bet[i + 3]);
+            tc::st_row4(TWs, C, t, i, tv.x * bet[i] * eg[i], tv.y * bet[i + 1] * eg[i + 1],
+                        tv.z * bet[i + 2] * eg[i + 2], tv.w * bet[i + 3] * eg[i + 3]);
+        }
+        // ---- R2: U~, W, O1 ------------------------------------------------------------------
+        mma_round_begin();
+        if (tid == 0 && ok) {
+            tc::fence_after();
+            tc::mma_tf32(tm + cU, TBs, C, VTs, DV, C, tc::idesc_tf32(C, DV), false);
+            tc::mma_tf32(tm + cW, TWs, C, KTs, D, C, tc::idesc_tf32(C, D), false);
+            tc::mma_tf32(tm + cO1, Qs, C, S0s, DV, D, tc::idesc_tf32(C, DV), false);
+        }
+        mma_round_end();
+        // W -> operand tile over K^ (no longer needed)
+        for (int cb = 0; cb < 4; ++cb) {
+            const int d0 = hf * 64 + cb * 16;
+            float w16[16];
+            tc::ld16(tc::taddr(tm, 32 * q4, cW + d0), w16);
+            if (rowok) {
+#pragma unroll
+                for (int c = 0; c < 16; c += 4)
+                    tc::st_row4(Ks, C, trow, d0 + c, w16[c], w16[c + 1], w16[c + 2], w16[c + 3]);
+            }
+        }
+        // ---- R3: U = U~ - W S^T -------------------------------------------------------------
+        mma_round_begin();
+        if (tid == 0 && ok) {
+            tc::fence_after();
+            tc::mma_tf32(tm + cU, Ks, C, S0s, DV, D, tc::idesc_tf32(C, DV, true), true);
+        }
+        mma_round_end();
+        {
+            // U -> U^T and (diag(e^(gC - g)) U)^T tiles; S^T *= e^gC in TMEM
+            float u16[16];
+            tc::ld16(tc::taddr(tm, 32 * q4, cU + hf * 16), u16);
+            if (rowok) {
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    tc::st_elem(UTs, DV, hf * 16 + c, trow, u16[c]);
+                    tc::st_elem(VTs, DV, hf * 16 + c, trow, u16[c] * erev[trow]);
+                }
+            }
+            float s16[16];
+            tc::ld16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
+            const float egC = eg[C - 1];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) s16[c] *= egC;
+            tc::st16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
+        }
+        // ---- R4: O2 = P U, S^T += K^T U' ---------------------------------------------------
+        mma_round_begin();
+        if (tid == 0 && ok) {
+            tc::fence_after();
+            tc::mma_tf32(tm + cO2, Ps, C, UTs, DV, C, tc::idesc_tf32(C, DV), false);
+            tc::mma_tf32(tm + cS, KTs, D, VTs, DV, C, tc::idesc_tf32(D, DV), true);
+        }
+        mma_round_end();
+        // ---- O = diag(e^g) O1 + O2; S^T -> S operand tile for the next chunk ----------------
+        float o16[16];
+        {
+            float a16[16];
+            tc::ld16(tc::taddr(tm, 32 * q4, cO1 + hf * 16), a16);
+            tc::ld16(tc::taddr(tm, 32 * q4, cO2 + hf * 16), o16);
+            float part = 0.f;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                o16[c] = fmaf(rowok ? eg[trow] : 0.f, a16[c], o16[c]);
+                part = fmaf(o16[c], o16[c], part);
+            }
+            if (rowok) ored[hf * C + trow] = part;
+            float s16[16];
+            tc::ld16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) tc::st_elem(S0s, DV, hf * 16 + c, dS, s16[c]);
+        }
+        __syncthreads();
+        float* ssq_cur = ssq + (ci & 1) * C;
+        if (tid < C) ssq_cur[tid] = ored[tid] + ored[C + tid];
+        cluster.sync();
+        if (rowok && trow < n) {
+            const size_t tok = (size_t)(t0 + trow);
+            float rstd = 1.f;
+            if (outnorm) {
+                float tot = 0.f;
+                for (int s2 = 0; s2 < NS; ++s2) tot += *cluster.map_shared_rank(&ssq_cur[trow], s2);
+                rstd = rsqrtf(tot / (float)D + g.norm_eps);
+            }
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const int dv = s_idx * DV + hf * 16 + c;
+                float yv = o16[c];
+                if (outnorm) {
+                    const float zz = L::ld(J.z, tok * (size_t)Hv * D + (size_t)j * D + dv);
+                    yv = yv * rstd * L::ld(A.p.norm_w, dv) * siluf_(zz);
+                }
+                L::st(J.y, tok * (size_t)Hv * D + (size_t)j * D + dv, yv);
+            }
+        }
+    }
+    // ---- final state ------------------------------------------------------------------------
+    {
+        float s16[16];
+        tc::ld16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
+        if (Sout) {
+#pragma unroll
+            for (int c = 0; c < 16; ++c) Sout[(size_t)(s_idx * DV + hf * 16 + c) * D + dS] = s16[c];
+        }
+    }
+    if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::dealloc(tm, TMEM_COLS);
+    cluster.sync();  // peers may still read this CTA's partial sums
+}
+
+cudaError_t launch_chunk_tc(const PrefillArgs& A, cudaStream_t st) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, tcp::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tcp::NS, A.g.Hv, A.J.n_seq);
+    cfg.blockDim = dim3(tcp::THREADS);
+    cfg.dynamicSmemBytes = tcp::SMEM_ALLOC;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = tcp::NS;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_chunk_tc, A);
+}
+
 int prefill_slices(int D) {
     if (const char* e = std::getenv("GDN_PREFILL_SLICES")) {
         const int v = std::atoi(e);
@@ -582,8 +1082,10 @@ cudaError_t launch_prefill_t(const Geom& g, const LayerParams& p, const PrefillJ
     A.beta = reinterpret_cast<float*>(ws + wl.beta);
     A.NS = prefill_slices(D);
     if (J.n_tokens > 0) {
-        const unsigned blocks = (unsigned)((J.n_tokens + kProTok - 1) / kProTok);
-        k_prologue<D, TA><<<blocks, 256, 0, st>>>(A);
+        constexpr int VEC = 16 / (int)sizeof(TA);
+        const dim3 blocks((unsigned)((J.n_tokens + kProTok - 1) / kProTok),
+                          (unsigned)((g.C_ch / VEC + kProThreads - 1) / kProThreads));
+        k_prologue<D, TA><<<blocks, kProThreads, 0, st>>>(A);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -594,6 +1096,9 @@ cudaError_t launch_prefill_t(const Geom& g, const LayerParams& p, const PrefillJ
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    if (D == 128 && g.chunk == 64 && g.act_bf16 && std::getenv("GDN_PREFILL_PRECISE") == nullptr &&
+        std::getenv("GDN_PREFILL_MMA_SYNC") == nullptr)
+        return launch_chunk_tc(A, st);
     const int DV = D / A.NS;
     const ChunkSmem lay = chunk_smem(g.chunk, D, DV);
     const size_t smem = (size_t)lay.total * sizeof(float);
