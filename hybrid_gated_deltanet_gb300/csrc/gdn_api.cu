@@ -256,11 +256,11 @@ static gdn_status prefill_common(const gdn_config* cfg, const gdn_params* prm, g
         return fail(GDN_ERR_RANGE, "n_tokens: found %lld, required 0..2^31", (long long)job.n_tokens);
     if ((st = make_params(prm, g, true, &p))) return st;
     if (job.n_tokens > 0) {
-        GDN_REQUIRE_PTR_A(job.x, "x", g.act_bf16 ? 2u : 4u);
-        if (!(g.flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR_A(job.z, "z", g.act_bf16 ? 2u : 4u);
+        GDN_REQUIRE_PTR(job.x, "x");  // x, z, y move in 16-byte vectors
+        if (!(g.flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR(job.z, "z");
         GDN_REQUIRE_PTR_A(job.a, "a", g.act_bf16 ? 2u : 4u);
         GDN_REQUIRE_PTR_A(job.b, "b", g.act_bf16 ? 2u : 4u);
-        GDN_REQUIRE_PTR_A(job.y, "y", g.act_bf16 ? 2u : 4u);
+        GDN_REQUIRE_PTR(job.y, "y");
     }
     const size_t need = gdn::prefill_workspace_bytes(g, job.n_tokens, job.cu_seqlens ? job.n_seq : 1);
     if (need > 0) GDN_REQUIRE_PTR(job.workspace, "workspace");

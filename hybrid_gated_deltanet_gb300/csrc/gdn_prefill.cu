@@ -46,6 +46,16 @@ namespace cg = cooperative_groups;
 namespace gdn {
 namespace {
 
+// 16-byte global -> shared copy; src_bytes = 0 fills the 16 bytes with zeros
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst_smem)),
+                 "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit_wait_all() {
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // workspace layout (fp32, each section 256-byte aligned)
 // ---------------------------------------------------------------------------
@@ -728,6 +738,10 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         }
     }
     const int dS = 32 * q4 + lane;  // the d_k index this thread owns in S^T
+    float nw16[16];                 // norm weight of the 16 outputs this thread writes
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+        nw16[c] = (g.flags & kFlagNoOutNorm) ? 1.f : L::ld(A.p.norm_w, s_idx * DV + hf * 16 + c);
     {
         float v[16];
 #pragma unroll
@@ -747,7 +761,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
     auto mma_round_end = [&]() {
         if (tid == 0) tc::commit(mbar);
         bool w = true;
-        if (ok) {
+        if (ok && warp == 0) {  // one warp polls, the others sleep in bar.sync
             w = mbar_wait(mbar, phase);
             if (!w) w = mbar_wait(mbar, phase);
         }
@@ -766,28 +780,53 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         const int n = (int)((end - t0) < C ? (end - t0) : C);
         __syncthreads();
         // ---- (1) load q^, k^, v, g, beta of the chunk (rows >= n are zero) --------
+        // all global reads go out at once (cp.async, 16 B each) into a staging
+        // area over the P/T/U/A tiles, which are dead at this point; then one
+        // shared-to-shared pass rounds to TF32 and swizzles.
+        float* stage = reinterpret_cast<float*>(Ps);  // [64][128] q^ | [64][128] k^ | [64][32] v
+        float* stq = stage;
+        float* stk = stage + C * D;
+        float* stv = stage + 2 * C * D;
         for (int f = tid; f < C * 32; f += THREADS) {
             const int r = f >> 5, c4 = f & 31;
-            float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), qv = kv;
-            if (r < n) {
-                const size_t tok = (size_t)(t0 + r);
-                kv = *reinterpret_cast<const float4*>(A.qk + (tok * 2 * Hk + Hk + h) * D + c4 * 4);
-                qv = *reinterpret_cast<const float4*>(A.qk + (tok * 2 * Hk + h) * D + c4 * 4);
-            }
-            tc::st_row4(Ks, C, r, c4 * 4, kv.x, kv.y, kv.z, kv.w);
-            tc::st_row4(Qs, C, r, c4 * 4, qv.x, qv.y, qv.z, qv.w);
+            const int ok_r = r < n ? 16 : 0;  // src-size 0 zero-fills
+            const size_t tok = (size_t)(t0 + (r < n ? r : 0));
+            cp_async16(stk + r * D + c4 * 4, A.qk + (tok * 2 * Hk + Hk + h) * D + c4 * 4, ok_r);
+            cp_async16(stq + r * D + c4 * 4, A.qk + (tok * 2 * Hk + h) * D + c4 * 4, ok_r);
         }
-        float* Vst = Am;  // [64][32] fp32 staging
         for (int f = tid; f < C * (DV / 4); f += THREADS) {
             const int r = f >> 3, c4 = f & 7;
-            float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (r < n) vv = *reinterpret_cast<const float4*>(A.v + ((size_t)(t0 + r) * Hv + j) * D + s_idx * DV + c4 * 4);
-            *reinterpret_cast<float4*>(Vst + r * DV + c4 * 4) = vv;
+            const size_t tok = (size_t)(t0 + (r < n ? r : 0));
+            cp_async16(stv + r * DV + c4 * 4, A.v + (tok * Hv + j) * D + s_idx * DV + c4 * 4, r < n ? 16 : 0);
+        }
+        cp_async_commit_wait_all();
+        float zpre[16];  // z of this thread's output row, needed at the end of the chunk
+        if (outnorm && rowok && trow < n) {
+            const uint4* zp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(J.z) +
+                                                             (size_t)(t0 + trow) * Hv * D + (size_t)j * D +
+                                                             s_idx * DV + hf * 16);
+            const uint4 z0 = zp[0], z1 = zp[1];
+            const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&z0);
+            const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&z1);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float2 a = __bfloat1622float2(h0[c]), b = __bfloat1622float2(h1[c]);
+                zpre[2 * c] = a.x; zpre[2 * c + 1] = a.y; zpre[8 + 2 * c] = b.x; zpre[8 + 2 * c + 1] = b.y;
+            }
         }
         if (tid < C) {
             gam[tid] = tid < n ? A.gl[(size_t)(t0 + tid) * Hv + j] : 0.f;
             bet[tid] = tid < n ? A.beta[(size_t)(t0 + tid) * Hv + j] : 0.f;
         }
+        __syncthreads();
+        for (int f = tid; f < C * 32; f += THREADS) {
+            const int r = f >> 5, c4 = f & 31;
+            const float4 kv = *reinterpret_cast<const float4*>(stk + r * D + c4 * 4);
+            const float4 qv = *reinterpret_cast<const float4*>(stq + r * D + c4 * 4);
+            tc::st_row4(Ks, C, r, c4 * 4, kv.x, kv.y, kv.z, kv.w);
+            tc::st_row4(Qs, C, r, c4 * 4, qv.x, qv.y, qv.z, qv.w);
+        }
+        float* Vst = stv;  // [64][32] fp32
         __syncthreads();
         // ---- (2) transposes; gamma = cumsum(g) -----------------------------------
         for (int d = warp * 16; d < warp * 16 + 16; ++d)
@@ -851,70 +890,71 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         }
         __syncthreads();
         // ---- T = (I + A)^-1: 16x16 diagonal blocks, then block merges ------------------
-        if (warp < 4) {
-            const int b0 = warp * 16;
+        // diagonal blocks: a lane owns one column of a block in registers and
+        // runs the forward substitution x_i = e_i - sum_{k<i} A_ik x_k
+        if (warp < 2) {
+            const int b0 = (warp * 2 + (lane >> 4)) * 16, jc = lane & 15;
+            float x[16];
+#pragma unroll
             for (int i = 0; i < 16; ++i) {
-                float arow[16];
+                float acc = (i == jc) ? 1.f : 0.f;
 #pragma unroll
-                for (int k = 0; k < 16; ++k) arow[k] = Am[(b0 + i) * LDA + b0 + k];
-                __syncwarp();
-                if (lane < 16) {
-                    float x = (lane == i) ? 1.f : 0.f;
-#pragma unroll
-                    for (int k = 0; k < 16; ++k)
-                        if (k >= lane && k < i) x -= arow[k] * Tm[(b0 + k) * LDA + b0 + lane];
-                    Tm[(b0 + i) * LDA + b0 + lane] = (lane <= i) ? x : 0.f;
-                }
-                __syncwarp();
+                for (int k = 0; k < i; ++k) acc = fmaf(-Am[(b0 + i) * LDA + b0 + k], x[k], acc);
+                x[i] = acc;
             }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) Tm[(b0 + i) * LDA + b0 + jc] = x[i];
         }
         for (int f = tid; f < C * C; f += THREADS) {
             const int t = f >> 6, c = f & 63;
             if ((c >> 4) > (t >> 4)) Tm[t * LDA + c] = 0.f;
         }
         __syncthreads();
+        // off-diagonal blocks by distance: X_ab = -X_aa sum_{c=b}^{a-1} A_ac X_cb,
+        // one output element per thread per block
         for (int dd = 1; dd < 4; ++dd) {
-            // blocks (a, b) with a - b = dd; 2 warps per block, 4 elements per lane
-            const int nblk = 4 - dd;
-            if (warp < 2 * nblk) {
-                const int bb = warp >> 1, half = warp & 1;
-                const int a0 = (bb + dd) * 16, c0b = bb * 16;
-                float y[4];
+            const int nel = (4 - dd) * 256;
+            float y[3];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int idx = half * 128 + lane + 32 * e, r = idx >> 4, c = idx & 15;
+            for (int q = 0; q < 3; ++q) {
+                const int e = tid + q * THREADS;
+                y[q] = 0.f;
+                if (e < nel) {
+                    const int bb = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                    const int a0 = (bb + dd) * 16, c0b = bb * 16;
                     float acc = 0.f;
                     for (int k = c0b; k < a0; ++k) acc = fmaf(Am[(a0 + r) * LDA + k], Tm[k * LDA + c0b + c], acc);
-                    y[e] = acc;
+                    y[q] = acc;
                 }
-                // Y into the (unused) target block, then X_ab = -X_aa Y
+            }
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int idx = half * 128 + lane + 32 * e, r = idx >> 4, c = idx & 15;
-                    Tm[(a0 + r) * LDA + c0b + c] = y[e];
+            for (int q = 0; q < 3; ++q) {  // Y into the (unused) target block
+                const int e = tid + q * THREADS;
+                if (e < nel) {
+                    const int bb = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                    Tm[((bb + dd) * 16 + r) * LDA + bb * 16 + c] = y[q];
                 }
             }
             __syncthreads();
-            const bool act = warp < 2 * nblk;
-            const int bb = warp >> 1, half = warp & 1;
-            const int a0 = (bb + dd) * 16, c0b = bb * 16;
-            float y[4] = {0.f, 0.f, 0.f, 0.f};
-            if (act) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int idx = half * 128 + lane + 32 * e, r = idx >> 4, c = idx & 15;
+            for (int q = 0; q < 3; ++q) {
+                const int e = tid + q * THREADS;
+                if (e < nel) {
+                    const int bb = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                    const int a0 = (bb + dd) * 16, c0b = bb * 16;
                     float acc = 0.f;
 #pragma unroll
                     for (int k = 0; k < 16; ++k) acc = fmaf(Tm[(a0 + r) * LDA + a0 + k], Tm[(a0 + k) * LDA + c0b + c], acc);
-                    y[e] = -acc;
+                    y[q] = -acc;
                 }
             }
             __syncthreads();  // every read of Y done before it is overwritten
-            if (act) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int idx = half * 128 + lane + 32 * e, r = idx >> 4, c = idx & 15;
-                    Tm[(a0 + r) * LDA + c0b + c] = y[e];
+            for (int q = 0; q < 3; ++q) {
+                const int e = tid + q * THREADS;
+                if (e < nel) {
+                    const int bb = e >> 8, r = (e >> 4) & 15, c = e & 15;
+                    Tm[((bb + dd) * 16 + r) * LDA + bb * 16 + c] = y[q];
                 }
             }
             __syncthreads();
@@ -1010,16 +1050,17 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
                 for (int s2 = 0; s2 < NS; ++s2) tot += *cluster.map_shared_rank(&ssq_cur[trow], s2);
                 rstd = rsqrtf(tot / (float)D + g.norm_eps);
             }
+            float yv[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const int dv = s_idx * DV + hf * 16 + c;
-                float yv = o16[c];
-                if (outnorm) {
-                    const float zz = L::ld(J.z, tok * (size_t)Hv * D + (size_t)j * D + dv);
-                    yv = yv * rstd * L::ld(A.p.norm_w, dv) * siluf_(zz);
-                }
-                L::st(J.y, tok * (size_t)Hv * D + (size_t)j * D + dv, yv);
-            }
+            for (int c = 0; c < 16; ++c) yv[c] = outnorm ? o16[c] * rstd * nw16[c] * siluf_(zpre[c]) : o16[c];
+            uint4 pk[2];
+            __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) hp[c] = __floats2bfloat162_rn(yv[2 * c], yv[2 * c + 1]);
+            uint4* yp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(J.y) + tok * (size_t)Hv * D +
+                                                 (size_t)j * D + s_idx * DV + hf * 16);
+            yp[0] = pk[0];
+            yp[1] = pk[1];
         }
     }
     // ---- final state ------------------------------------------------------------------------

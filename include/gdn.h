@@ -33,10 +33,10 @@
  *   and 6.5: report the tensor, the shape found and the shape required;
  *   refuse with both numbers).
  * - Alignment (GDN_ERR_ALIGN otherwise): 16 bytes for the state pools, s0,
- *   s_final, the conv pools, conv_w, norm_w, the workspace, and x and z of
- *   the decode and verify calls (these move with bulk or 128-bit copies);
- *   the element size (2 for bf16, 4 for fp32) for the other activation
- *   arrays and parameters; 4 bytes for int32 arrays.
+ *   s_final, the conv pools, conv_w, norm_w, the workspace, x and z, and
+ *   the y of the prefill calls (these move with bulk or 128-bit copies);
+ *   the element size (2 for bf16, 4 for fp32) for a, b, conv_b, dt_bias,
+ *   A_log and the y of decode/verify; 4 bytes for int32 arrays.
  * - Layouts are row-major and dense.  "act" means the activation dtype of the
  *   config (bf16 or fp32).  Channel order of x is [q | k | v], head-major:
  *   q of k-head h at h*d_k, k at H_k*d_k + h*d_k, v of v-head j at
