@@ -50,6 +50,19 @@ FLOP_VHEAD = C_REF * C_REF / 3 + 2 * C_REF * 256 + 6 * 128 * 128 + 2 * C_REF * 1
 FLOP_PER_TOKEN = 16 * FLOP_KHEAD + 32 * FLOP_VHEAD
 
 
+METRIC = "GDN decode state GB/s (% of HBM peak); chunked-prefill tokens/s/layer (% TC peak)"
+
+
+def decode_config(world: int) -> dict:
+    return {"workload": "Qwen3.5-4B-like GDN decode step: 24 layers x 64 slots, 1 token per slot, "
+                        "16 k-heads / 32 v-heads, d_k = d_v = 128, bf16 q/k/v/z, fp32 state (2 MiB per "
+                        "slot and layer), pool of 256 slots per layer",
+            "layers": N_LAYERS, "slots": B, "pool_slots_per_layer": POOL,
+            "working_set_bytes_per_step": N_LAYERS * (B * SLOT_BYTES + PARAM_BYTES),
+            "l2": "inputs larger than L2 (6.6 GB touched per step vs 129 MB L2); no flush",
+            "parallelism": f"replicas x{world}"}
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -448,15 +461,13 @@ def reference_arm(args):
         busy += dt
     total = time.perf_counter() - t0
     value = args.steps * n_slots * SLOT_BYTES / busy / 1e9
-    line = {"impl": "reference", "metric": "GDN decode state GB/s", "value": round(value, 4), "unit": "GB/s",
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1e3 * total / max(args.steps, 1), 3), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "Qwen3.5-4B-like GDN decode step (16 k-heads, 32 v-heads, d=128, bf16 inputs, "
-                                   "fp32 state): each step a bounded sample of 16 slots of one layer",
-                       "layers": 1, "slots_per_step": n_slots},
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": decode_config(1),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": f"{n_slots} slots x 1 layer per step, fp64 token loop, {threads} threads"},
+                             "sample": f"each step: {n_slots} slots x 1 layer of the decode step (a bounded sample "
+                                       f"of its 24 x 64 slot-layers), fp64 token loop, {threads} threads"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -510,17 +521,11 @@ def gpu_arm(args):
     traffic = measured_traffic("k_rows", "gdn_decode.cu")
     clocks = clk.summary()
     line = {
-        "metric": "GDN decode state GB/s (% of HBM peak); chunked-prefill tokens/s/layer (% TC peak)",
+        "metric": METRIC,
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * t_dec / args.steps, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "Qwen3.5-4B-like GDN decode step: 24 layers x 64 slots, 1 token per slot, "
-                               "16 k-heads / 32 v-heads, d_k = d_v = 128, bf16 q/k/v/z, fp32 state (2 MiB per "
-                               "slot and layer), pool of 256 slots per layer",
-                   "layers": N_LAYERS, "slots": B, "pool_slots_per_layer": POOL,
-                   "working_set_bytes_per_step": step_bytes,
-                   "l2": "inputs larger than L2 (6.9 GB touched per step vs 129 MB L2); no flush",
-                   "graph": not args.no_graph, "parallelism": f"replicas x{world}"},
+        "config": dict(decode_config(world), graph=not args.no_graph),
         "parity": {"decode_rel_fro": parity, "prefill_rel_fro": pf_err,
                    "tolerance": {"y": 2e-2, "S": 1e-3}},
         "roofline": {"bound": "hbm", "kernel": "k_rows (gdn_decode_step)", "achieved": round(achieved, 1),
