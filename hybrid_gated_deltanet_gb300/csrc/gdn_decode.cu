@@ -46,6 +46,21 @@ struct RowsArgs {
     int NS;
 };
 
+// barrier over the 256 consumer threads only (named barrier 1), AND of a predicate
+__device__ __forceinline__ bool __syncthreads_and_consumers(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.and.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
@@ -407,6 +422,294 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
     if (tid == 0) bulk_wait_read_all();  // the state store has read its shared-memory source
 }
 
+// ---- persistent, pipelined decode (d = 128, one token per slot) ---------------
+// One CTA per SM walks a strided list of (slot, v-head) items.  Warp 8 is the
+// producer: it reads the item's slot index and gates, issues the bulk copies
+// of the item's 64 KB state tile and small inputs into one of 3 shared-memory
+// stages (up to 3 items ahead), and once the consumers are done with an item
+// writes its state back with one bulk store.  Warps 0..7 consume: conv +
+// SiLU + L2 norm + gates from shared memory, the row update with the
+// transposing butterfly, the gated RMSNorm and y.  The conv state is rolled
+// by a second, tiny launch after this one (stream order keeps every read of
+// it before the write), so CTAs never wait on each other.
+namespace pd {
+constexpr int D = 128, NCH = 3 * D, STAGES = 3, CONSUMERS = 256, THREADS = CONSUMERS + 32;
+template <typename TA>
+struct Stage {
+    static constexpr int E = sizeof(TA);
+    static constexpr int S = 0;                                // fp32 [128][128]
+    static constexpr int X = S + D * D * 4;                    // act [NCH]
+    static constexpr int CV = X + NCH * E;                     // act [3][NCH] (d_conv - 1 <= 3)
+    static constexpr int W = CV + 3 * NCH * E;                 // act [NCH][4]
+    static constexpr int Z = W + NCH * 4 * E;                  // act [D]
+    static constexpr int NW = Z + D * E;                       // act [D]
+    static constexpr int HDR = NW + D * E;                     // a, b, slot, flags
+    static constexpr int BYTES = ((HDR + 16) + 127) & ~127;
+};
+template <typename TA>
+constexpr int smem_bytes() {
+    return STAGES * Stage<TA>::BYTES + 4 * STAGES * 8 /*mbarriers*/ + (3 * D + 64 + D + 16) * 4 + 128;
+}
+}  // namespace pd
+
+template <typename TA>
+__global__ void __launch_bounds__(pd::THREADS, 1) k_decode_persist(const __grid_constant__ RowsArgs A) {
+    using namespace pd;
+    using L = Act<TA>;
+    using St = Stage<TA>;
+    constexpr int E = sizeof(TA);
+    const Geom& g = A.g;
+    const RowsJob& J = A.job;
+    const int Hk = g.Hk, Hv = g.Hv, G = g.G, K = g.K, Km1 = g.K - 1, C = g.C_ch;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool raw = g.flags & kFlagRawQKV;
+    const bool outnorm = !(g.flags & kFlagNoOutNorm);
+    const bool direct = g.flags & kFlagGatesDirect;
+    const int n_items = J.B * Hv;
+
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * St::BYTES);
+    uint64_t* fullS = full + STAGES;     // the state tile of the stage
+    uint64_t* done = fullS + STAGES;     // consumers finished the stage's item
+    float* qs = reinterpret_cast<float*>(done + STAGES + STAGES);
+    float* ks = qs + D;
+    float* vs = ks + D;
+    float* red = vs + D;
+    float* obuf = red + 64;
+    float* ssp = obuf + D;
+
+    if (tid == 0) {
+        for (int st = 0; st < STAGES; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&fullS[st], 1);
+            mbar_init(&done[st], 1);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == CONSUMERS / 32) {
+        // ---------------- producer ----------------
+        if (lane == 0) {
+            int k = 0;
+            for (int item = blockIdx.x; item < n_items + (int)gridDim.x * STAGES; item += gridDim.x, ++k) {
+                const int st = k % STAGES;
+                const int pitem = item - (int)gridDim.x * STAGES;  // the item that used this stage before
+                if (k >= STAGES && pitem < n_items) {               // retire it
+                    if (!mbar_wait(&done[st], ((k / STAGES) - 1) & 1)) report_device_status(kDevWaitTimeout);
+                    unsigned char* sb = smem + st * St::BYTES;
+                    const int* hdr = reinterpret_cast<const int*>(sb + St::HDR);
+                    if (hdr[2] >= 0) {  // state back in place
+                        const int pj = pitem % Hv;
+                        bulk_s2g(J.state_pool + ((size_t)hdr[2] * Hv + pj) * D * D, sb + St::S, D * D * 4);
+                        bulk_commit();
+                    }
+                    bulk_wait_read_all();  // the stage may be refilled
+                }
+                if (item >= n_items) continue;
+                unsigned char* sb = smem + st * St::BYTES;
+                const int bb = item / Hv, j = item % Hv, h = j / G;
+                const int slot = J.slot_idx[bb];
+                const bool valid = slot >= 0 && slot < J.n_slots;
+                int* hdr = reinterpret_cast<int*>(sb + St::HDR);
+                float* hf = reinterpret_cast<float*>(sb + St::HDR);
+                hf[0] = L::ld(J.a, (size_t)bb * Hv + j);
+                hf[1] = L::ld(J.b, (size_t)bb * Hv + j);
+                hdr[2] = valid ? slot : -1;
+                if (!valid) {
+                    mbar_arrive_expect_tx(&fullS[st], 0);
+                    mbar_arrive_expect_tx(&full[st], 0);
+                    continue;
+                }
+                const int ch_q = h * D, ch_k = Hk * D + h * D, ch_v = 2 * Hk * D + j * D;
+                mbar_arrive_expect_tx(&fullS[st], D * D * 4);
+                bulk_g2s(sb + St::S, J.state_pool + ((size_t)slot * Hv + j) * D * D, D * D * 4, &fullS[st]);
+                const bool conv_w = !raw && A.p.conv_w;
+                const uint32_t bytes =
+                    NCH * E + Km1 * NCH * E + (conv_w ? NCH * K * E : 0) + (outnorm ? 2 * D * E : 0);
+                mbar_arrive_expect_tx(&full[st], bytes);  // releases the header writes too
+                const char* xrow = static_cast<const char*>(J.x) + (size_t)bb * C * E;
+                bulk_g2s(sb + St::X, xrow + (size_t)ch_q * E, D * E, &full[st]);
+                bulk_g2s(sb + St::X + D * E, xrow + (size_t)ch_k * E, D * E, &full[st]);
+                bulk_g2s(sb + St::X + 2 * D * E, xrow + (size_t)ch_v * E, D * E, &full[st]);
+                const char* cg_ = static_cast<const char*>(J.conv_pool);
+                for (int m = 0; m < Km1; ++m) {
+                    const char* row = cg_ + ((size_t)slot * Km1 + m) * C * E;
+                    bulk_g2s(sb + St::CV + m * NCH * E, row + (size_t)ch_q * E, D * E, &full[st]);
+                    bulk_g2s(sb + St::CV + (m * NCH + D) * E, row + (size_t)ch_k * E, D * E, &full[st]);
+                    bulk_g2s(sb + St::CV + (m * NCH + 2 * D) * E, row + (size_t)ch_v * E, D * E, &full[st]);
+                }
+                if (conv_w) {
+                    const char* w = static_cast<const char*>(A.p.conv_w);
+                    bulk_g2s(sb + St::W, w + (size_t)ch_q * K * E, D * K * E, &full[st]);
+                    bulk_g2s(sb + St::W + D * K * E, w + (size_t)ch_k * K * E, D * K * E, &full[st]);
+                    bulk_g2s(sb + St::W + 2 * D * K * E, w + (size_t)ch_v * K * E, D * K * E, &full[st]);
+                }
+                if (outnorm) {
+                    bulk_g2s(sb + St::Z, static_cast<const char*>(J.z) + ((size_t)bb * Hv + j) * D * E, D * E,
+                             &full[st]);
+                    bulk_g2s(sb + St::NW, A.p.norm_w, D * E, &full[st]);
+                }
+            }
+            bulk_wait_read_all();
+        }
+        return;
+    }
+
+    // ---------------- consumers (warps 0..7) ----------------
+    const int col4 = lane;  // D = 128: a warp covers one row, 4 floats per lane
+    int k = 0;
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
+        const int st = k % STAGES;
+        const uint32_t par = (k / STAGES) & 1;
+        unsigned char* sb = smem + st * St::BYTES;
+        const TA* xs = reinterpret_cast<const TA*>(sb + St::X);
+        const TA* cs = reinterpret_cast<const TA*>(sb + St::CV);
+        const TA* wsm = reinterpret_cast<const TA*>(sb + St::W);
+        const TA* zs = reinterpret_cast<const TA*>(sb + St::Z);
+        const TA* nw = reinterpret_cast<const TA*>(sb + St::NW);
+        float* Sb = reinterpret_cast<float*>(sb + St::S);
+        const int bb = item / Hv, j = item % Hv, h = j / G;
+        bool ok = true;
+        if (warp == 0) {
+            ok = mbar_wait(&full[st], par);
+            if (!ok) mbar_wait(&full[st], par);
+        }
+        ok = __syncthreads_and_consumers(ok);
+        const int* hdr = reinterpret_cast<const int*>(sb + St::HDR);
+        const float* hfl = reinterpret_cast<const float*>(sb + St::HDR);
+        const bool valid = hdr[2] >= 0;
+        const int ch_q = h * D, ch_k = Hk * D + h * D, ch_v = 2 * Hk * D + j * D;
+        auto conv = [&](int lc) -> float {
+            if (raw) return L::ld(xs, lc);
+            const int ch = lc < D ? ch_q + lc : (lc < 2 * D ? ch_k + lc - D : ch_v + lc - 2 * D);
+            float c = A.p.conv_b ? L::ld(A.p.conv_b, ch) : 0.0f;
+            for (int m = 0; m < K; ++m) {
+                const int tau = m - Km1;  // taps before the current token come from the conv state
+                const float xv = tau >= 0 ? L::ld(xs, lc) : L::ld(cs, (size_t)(Km1 + tau) * NCH + lc);
+                c = fmaf(L::ld(wsm, (size_t)lc * K + m), xv, c);
+            }
+            return siluf_(c);
+        };
+        float sq = 0.f, sk = 0.f, sqk = 0.f;
+        if (ok && valid) {
+            for (int c = tid; c < D; c += CONSUMERS) {
+                const float qv = conv(c), kv = conv(D + c);
+                qs[c] = qv;
+                ks[c] = kv;
+                sq = fmaf(qv, qv, sq);
+                sk = fmaf(kv, kv, sk);
+                sqk = fmaf(qv, kv, sqk);
+            }
+            for (int c = tid; c < D; c += CONSUMERS) vs[c] = conv(2 * D + c);
+        }
+        sq = warp_sum(sq);
+        sk = warp_sum(sk);
+        sqk = warp_sum(sqk);
+        if (lane == 0) {
+            red[warp * 4 + 0] = sq;
+            red[warp * 4 + 1] = sk;
+            red[warp * 4 + 2] = sqk;
+        }
+        bool s_ok = true;
+        if (warp == 0 && ok) {
+            s_ok = mbar_wait(&fullS[st], par);
+            if (!s_ok) mbar_wait(&fullS[st], par);
+        }
+        ok = __syncthreads_and_consumers(ok && s_ok);
+        if (ok && valid) {
+            sq = sk = sqk = 0.f;
+            for (int w = 0; w < CONSUMERS / 32; ++w) {
+                sq += red[w * 4 + 0];
+                sk += red[w * 4 + 1];
+                sqk += red[w * 4 + 2];
+            }
+            float rq, rk;
+            if (g.flags & kFlagNoL2) {
+                rq = g.q_scale;
+                rk = 1.0f;
+            } else {
+                rq = g.q_scale * rsqrtf(sq + g.l2_eps);
+                rk = rsqrtf(sk + g.l2_eps);
+            }
+            const float kq = sqk * rq * rk;
+            float gl, beta;
+            gates(hfl[0], hfl[1], direct ? 0.f : A.p.A_log[j], (!direct && A.p.dt_bias) ? A.p.dt_bias[j] : 0.f,
+                  direct, gl, beta);
+            const float alpha = expf(gl);
+            float kr[4], qr[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                kr[e] = ks[col4 * 4 + e] * rk;
+                qr[e] = qs[col4 * 4 + e] * rq;
+            }
+            for (int rb = warp * 8; rb < D; rb += 8 * (CONSUMERS / 32)) {
+                float4 sv[8];
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    sv[i] = *reinterpret_cast<const float4*>(Sb + (rb + i) * D + lane * 4);
+                    float dk = sv[i].x * kr[0];
+                    dk = fmaf(sv[i].y, kr[1], dk);
+                    dk = fmaf(sv[i].z, kr[2], dk);
+                    v[i] = fmaf(sv[i].w, kr[3], dk);
+                    float dq = sv[i].x * qr[0];
+                    dq = fmaf(sv[i].y, qr[1], dq);
+                    dq = fmaf(sv[i].z, qr[2], dq);
+                    v[8 + i] = fmaf(sv[i].w, qr[3], dq);
+                }
+#pragma unroll
+                for (int n = 8, off = 16; n >= 1; n >>= 1, off >>= 1) {
+                    const bool upper = lane & off;
+#pragma unroll
+                    for (int i = 0; i < n; ++i) {
+                        const float send = upper ? v[i] : v[i + n];
+                        const float keep = upper ? v[i + n] : v[i];
+                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    }
+                }
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+                const int idx = lane >> 1;
+                const float e_mine = idx < 8 ? vs[rb + idx] - alpha * v[0] : 0.f;
+                float ei[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) ei[i] = __shfl_sync(0xffffffffu, e_mine, 2 * i);
+                const float e_for_q = __shfl_sync(0xffffffffu, e_mine, ((idx - 8) & 7) * 2);
+                if (idx >= 8 && !(lane & 1)) obuf[rb + idx - 8] = fmaf(alpha, v[0], beta * e_for_q * kq);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float be = beta * ei[i];
+                    sv[i].x = fmaf(alpha, sv[i].x, be * kr[0]);
+                    sv[i].y = fmaf(alpha, sv[i].y, be * kr[1]);
+                    sv[i].z = fmaf(alpha, sv[i].z, be * kr[2]);
+                    sv[i].w = fmaf(alpha, sv[i].w, be * kr[3]);
+                    *reinterpret_cast<float4*>(Sb + (rb + i) * D + lane * 4) = sv[i];
+                }
+            }
+        }
+        fence_proxy_async_smem();  // the state tile goes out through the async proxy
+        __syncthreads_and_consumers(true);
+        if (ok && valid) {
+            // output gated RMSNorm over the whole v-head
+            if (warp == 0) {
+                float ss = 0.f;
+                for (int rr = lane; rr < D; rr += 32) ss = fmaf(obuf[rr], obuf[rr], ss);
+                ss = warp_sum(ss);
+                if (lane == 0) ssp[0] = ss;
+            }
+            __syncthreads_and_consumers(true);
+            for (int rr = tid; rr < D; rr += CONSUMERS) {
+                float yv = obuf[rr];
+                if (outnorm) yv = yv * rsqrtf(ssp[0] / (float)D + g.norm_eps) * L::ld(nw, rr) * siluf_(L::ld(zs, rr));
+                L::st(J.y, ((size_t)bb * Hv + j) * D + rr, yv);
+            }
+        }
+        if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
+        __syncthreads_and_consumers(true);  // qs/ks/vs/obuf/red reused by the next item; stage fully read
+        if (tid == 0) mbar_arrive(&done[st]);  // the producer may store and refill the stage
+    }
+}
+
 int choose_slices(const Geom& g, int B) {
     const int max_ns = std::min(8 / g.G, g.D / 8);
     if (const char* e = std::getenv("GDN_DECODE_SLICES")) {
@@ -511,8 +814,46 @@ __global__ void k_commit(const Geom g, const CommitJob J, int elt_bytes) {
 
 }  // namespace
 
+template <typename TA>
+cudaError_t launch_decode_persist(const Geom& g, const LayerParams& p, const RowsJob& job, cudaStream_t st) {
+    constexpr int smem = pd::smem_bytes<TA>();
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_decode_persist<TA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    int sms = 152;
+    {
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    }
+    const int items = job.B * g.Hv;
+    RowsArgs A{g, p, job, 1};
+    k_decode_persist<TA><<<std::min(items, sms), pd::THREADS, smem, st>>>(A);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // roll the conv state (raw inputs) after every read of it above
+    ConvJob cj{job.x, job.conv_pool, job.slot_idx, nullptr, job.B, 1, job.n_slots};
+    const size_t total = (size_t)job.B * g.C_ch;
+    const int blocks = (int)std::min<size_t>((total + 255) / 256, (size_t)sms * 8);
+    k_conv_roll<TA><<<blocks, 256, 0, st>>>(g, cj);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_rows(const Geom& g, const LayerParams& p, const RowsJob& job, cudaStream_t st) {
     if (job.B == 0) return cudaSuccess;
+    // the persistent pipelined kernel pays off once every SM has several
+    // (slot, v-head) items to overlap (measured: B = 64 and 256 at the 4B
+    // geometry gain 18% / 26%; B <= 16 is faster with one CTA per item)
+    if (g.D == 128 && job.r == 1 && !job.snap_idx && std::getenv("GDN_DECODE_CLUSTERED") == nullptr &&
+        std::getenv("GDN_DECODE_SLICES") == nullptr) {
+        int sms = 152, dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if ((long)job.B * g.Hv >= 4L * sms)
+            return g.act_bf16 ? launch_decode_persist<__nv_bfloat16>(g, p, job, st)
+                              : launch_decode_persist<float>(g, p, job, st);
+    }
     if (g.act_bf16) {
         switch (g.D) {
             case 32: return launch_rows_t<32, __nv_bfloat16>(g, p, job, st);

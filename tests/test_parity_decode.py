@@ -78,6 +78,38 @@ def test_decode_row_slices(slices, monkeypatch):
     assert errs["y"] <= 2e-2 and errs["S"] <= 1e-3, fmt(errs)
 
 
+@pytest.mark.parametrize("wl_name,B", [("decode4b", 64), ("wide", 32)])
+def test_decode_persistent_path_with_invalid_slots(wl_name, B):
+    """Batches large enough for the persistent pipelined kernel (>= 4 items per
+    SM), with a few out-of-range slot indices that must be skipped, on the
+    2- and 3-v-heads-per-k-head geometries."""
+    geom, act, p, tok, S, CS, slots = _pool_case(wl_name, B, stream=400 + B, pool_factor=2)
+    bad = np.array([1, B // 2, B - 1])
+    slots = slots.copy()
+    slots[bad] = [-3, S.shape[0], 10 ** 6]
+    cfg = config(geom, act)
+    sp, cp = dev(S), dev(CS)
+    y = torch.zeros((B, geom.value_dim), dtype=cfg.torch_dtype, device="cuda")
+    gb.gdn_decode_step(cfg, params_dev(p), dev(tok["x"]), dev(tok["z"]), dev(tok["a"]), dev(tok["b"]), cp, sp,
+                       torch.from_numpy(slots).cuda(), y)
+    torch.cuda.synchronize()
+    s_got, c_got, y_got = host(sp), host(cp), host(y)
+    good = [b for b in range(B) if b not in set(bad.tolist())]
+    ys, yr, ss, sr = [], [], [], []
+    for b in good[:12]:
+        ref = _oracle_slot(geom, p, tok, S, CS, slots[b], slice(b, b + 1))
+        ys.append(y_got[b]); yr.append(ref["y"][0]); ss.append(s_got[slots[b]]); sr.append(ref["S"])
+        np.testing.assert_array_equal(c_got[slots[b]], ref["conv"])
+    errs = {"y": rel_fro(ys, yr), "S": rel_fro(ss, sr)}
+    assert errs["y"] <= 2e-2 and errs["S"] <= 1e-3, fmt(errs)
+    assert np.all(y_got[bad] == 0)  # skipped entries leave y untouched
+    used = set(slots[good].tolist())
+    untouched = np.array([i for i in range(S.shape[0]) if i not in used])
+    np.testing.assert_array_equal(s_got[untouched], S.f64[untouched])
+    np.testing.assert_array_equal(c_got[untouched], CS.f64[untouched])
+    assert gb.gdn_device_status() == 0
+
+
 def test_decode_16_consecutive_steps():
     """16 decode steps on 4 slots == the oracle over the 16 tokens of each slot."""
     B, T = 4, 16
