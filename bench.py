@@ -518,7 +518,7 @@ def gpu_arm(args):
         pf_cpu = {"value": round(pf_cpu_rate, 3), "unit": "tokens/s/layer", "cores": cpu_thr, "kind": "oracle",
                   "sample": f"{args.cpu_prefill_tokens} tokens x {pf_heads} of 32 v-heads ({pf_cpu_dt:.1f} s), "
                             "scaled to 32 heads"}
-    traffic = measured_traffic("k_rows", "gdn_decode.cu")
+    traffic = measured_traffic("k_decode_persist", "gdn_decode.cu")
     clocks = clk.summary()
     line = {
         "metric": METRIC,
@@ -528,10 +528,12 @@ def gpu_arm(args):
         "config": dict(decode_config(world), graph=not args.no_graph),
         "parity": {"decode_rel_fro": parity, "prefill_rel_fro": pf_err,
                    "tolerance": {"y": 2e-2, "S": 1e-3}},
-        "roofline": {"bound": "hbm", "kernel": "k_rows (gdn_decode_step)", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm",
+                     "kernel": "gdn_decode_step = k_decode_persist (state, 97% of the bytes) + k_conv_roll",
+                     "achieved": round(achieved, 1),
                      "peak": peaks["hbm_gbs"], "peak_src": peaks["src"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": traffic, "launch_us": round(launch_s * 1e6, 3),
+                     "traffic": traffic, "call_us": round(launch_s * 1e6, 3),
                      "algorithmic_bytes_per_launch": B * SLOT_BYTES + PARAM_BYTES},
         "prefill": {"workload": "chunked prefill, 1 sequence, T = 8192, 16/32 heads, d = 128, bf16 in, fp32 state, "
                                 "chunk 64 (3 launches: prologue, conv state, chunk kernel)",
@@ -543,7 +545,7 @@ def gpu_arm(args):
         "e2e": {"value": round(world * step_bytes * e2e_steps / e2e_t / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(1e3 * e2e_t / e2e_steps, 4)},
-        "gpu_launches": args.steps * N_LAYERS,
+        "gpu_launches": args.steps * N_LAYERS * 2,  # per layer: the decode kernel and the conv-state roll
         "clocks": clocks,
     }
     print(json.dumps(line))
