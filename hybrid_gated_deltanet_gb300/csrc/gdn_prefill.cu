@@ -80,6 +80,36 @@ WsLayout ws_layout(const Geom& g, int64_t N) {
     return L;
 }
 
+// Workspace of the tcgen05 chunk kernel (d = 128, chunk 64, 4 slices of 32
+// state rows): ready-to-copy operand tiles, TF32-rounded and 128B-swizzled,
+// one set per chunk slot.  Sequence s's chunk c sits in slot
+// floor(start_s / 64) + s + c, which never collides with another sequence's.
+//   per (slot, k-head): Q^ [64][128] | K^ [64][128] | K^T [128][64]   (3 x 32 KB)
+//   per (slot, v-head, slice): V^T [32][64]                           (8 KB)
+//   per (slot, v-head): g [64], beta [64]                              (512 B)
+constexpr size_t kTileQK = 3 * 32768, kTileV = 4 * 8192, kTileGB = 2 * 64 * 4;
+
+struct TileWs {
+    size_t qk, v, gb, total;
+    int64_t ncs;
+};
+
+size_t align1024(size_t x) { return (x + 1023) & ~(size_t)1023; }
+
+TileWs tile_ws(const Geom& g, int64_t N, int n_seq) {
+    TileWs L;
+    L.ncs = N / 64 + n_seq + 1;
+    size_t off = 0;
+    L.qk = off;
+    off = align1024(off + (size_t)L.ncs * g.Hk * kTileQK);
+    L.v = off;
+    off = align1024(off + (size_t)L.ncs * g.Hv * kTileV);
+    L.gb = off;
+    off = align1024(off + (size_t)L.ncs * g.Hv * kTileGB);
+    L.total = off;
+    return L;
+}
+
 struct PrefillArgs {
     Geom g;
     LayerParams p;
@@ -88,8 +118,19 @@ struct PrefillArgs {
     float* v;     // [N][Hv][D]
     float* gl;    // [N][Hv]       g = log(alpha)
     float* beta;  // [N][Hv]
+    unsigned char* tqk;  // tile workspace (tcgen05 path), see TileWs
+    unsigned char* tv;
+    float* tgb;
+    int tiles;           // 1: the prologue writes the tile workspace
     int NS;
 };
+
+// chunk slot and row of token n of sequence s (start = its first token)
+__device__ __forceinline__ void chunk_slot(int64_t n, int64_t start, int s, int64_t& cs, int& r) {
+    const int64_t rel = n - start;
+    cs = start / 64 + s + rel / 64;
+    r = (int)(rel % 64);
+}
 
 // sequence bounds, clamped into [0, N]
 __device__ __forceinline__ void seq_bounds(const PrefillJob& J, int s, int64_t& start, int64_t& end) {
@@ -166,7 +207,7 @@ struct Vec16<float> {
 };
 
 template <int D, typename TA>
-__global__ void __launch_bounds__(kProThreads) k_prologue(const __grid_constant__ PrefillArgs A) {
+__global__ void __launch_bounds__(kProThreads, 2) k_prologue(const __grid_constant__ PrefillArgs A) {
     using L = Act<TA>;
     using V = Vec16<TA>;
     constexpr int VEC = V::N;
@@ -188,8 +229,19 @@ __global__ void __launch_bounds__(kProThreads) k_prologue(const __grid_constant_
             float gl, be;
             gates(L::ld(J.a, (size_t)n * Hv + j), L::ld(J.b, (size_t)n * Hv + j), direct ? 0.f : A.p.A_log[j],
                   (!direct && A.p.dt_bias) ? A.p.dt_bias[j] : 0.f, direct, gl, be);
-            A.gl[(size_t)n * Hv + j] = gl;
-            A.beta[(size_t)n * Hv + j] = be;
+            if (A.tiles) {
+                const int sq = find_seq(J, n);
+                int64_t st_, en_, cs;
+                int r;
+                seq_bounds(J, sq, st_, en_);
+                chunk_slot(n, st_, sq, cs, r);
+                float* gb = A.tgb + ((size_t)cs * Hv + j) * 128;
+                gb[r] = gl;
+                gb[64 + r] = be;
+            } else {
+                A.gl[(size_t)n * Hv + j] = gl;
+                A.beta[(size_t)n * Hv + j] = be;
+            }
         }
     }
 
@@ -226,6 +278,31 @@ __global__ void __launch_bounds__(kProThreads) k_prologue(const __grid_constant_
         }
     }
     const bool is_q = ch0 < Hk * D, is_qk = ch0 < 2 * Hk * D;
+    // tile mode: K^T and V^T tile rows are t-contiguous; 4 consecutive tokens of
+    // the same chunk slot go out as one 16-byte store per channel
+    float tb[VEC][4];
+    int64_t tb_cs = -1;
+    int tb_r0 = 0, tb_n = 0;
+    unsigned char* tb_base = nullptr;
+    int tb_rows = 0, tb_row0 = 0;  // tile rows (128 for K^T, 32 for V^T) and this thread's first row
+    auto tb_flush = [&]() {
+        if (tb_n == 0) return;
+        if (tb_n == 4 && (tb_r0 & 3) == 0) {
+#pragma unroll
+            for (int c = 0; c < VEC; ++c)
+                *reinterpret_cast<float4*>(tb_base + tc::sw_off(tb_rows, tb_row0 + c, tb_r0)) =
+                    make_float4(tb[c][0], tb[c][1], tb[c][2], tb[c][3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (e < tb_n) {
+#pragma unroll
+                    for (int c = 0; c < VEC; ++c)
+                        *reinterpret_cast<float*>(tb_base + tc::sw_off(tb_rows, tb_row0 + c, tb_r0 + e)) = tb[c][e];
+                }
+        }
+        tb_n = 0;
+    };
     for (int tt = 0; tt < kProTok; ++tt) {
         const int64_t n = t0 + tt;
         if (n >= J.n_tokens) break;  // uniform over the CTA
@@ -237,13 +314,13 @@ __global__ void __launch_bounds__(kProThreads) k_prologue(const __grid_constant_
         if (active) V::load(static_cast<const TA*>(J.x) + (size_t)n * C + ch, win[3]);
         // with K < 4 the window's live rows are win[4-K .. 3]
         float u[VEC];
+        const int s = find_seq(J, n);
+        int64_t start, end;
+        seq_bounds(J, s, start, end);
         if (raw) {
 #pragma unroll
             for (int c = 0; c < VEC; ++c) u[c] = win[3][c];
         } else {
-            const int s = find_seq(J, n);
-            int64_t start, end;
-            seq_bounds(J, s, start, end);
             int slot_ok;
             const void* cin = seq_conv_in(J, g, s, slot_ok);
 #pragma unroll
@@ -273,18 +350,70 @@ __global__ void __launch_bounds__(kProThreads) k_prologue(const __grid_constant_
             for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
             float scale = is_q ? g.q_scale : 1.f;
             if (!(g.flags & kFlagNoL2)) scale *= rsqrtf(ss + g.l2_eps);
-            if (active) {
+            if (A.tiles && D == 128) {
+                if (active) {
+                    int64_t cs;
+                    int r;
+                    chunk_slot(n, start, s, cs, r);
+                    const int hq = ch0 / D, d0 = ch0 % D;
+                    const int hh = hq < Hk ? hq : hq - Hk;
+                    unsigned char* tile = A.tqk + ((size_t)cs * Hk + hh) * kTileQK + (hq < Hk ? 0 : 32768);
+#pragma unroll
+                    for (int c = 0; c < VEC; c += 4)
+                        *reinterpret_cast<float4*>(tile + tc::sw_off(64, r, d0 + c)) =
+                            make_float4(tc::to_tf32_rn(u[c] * scale), tc::to_tf32_rn(u[c + 1] * scale),
+                                        tc::to_tf32_rn(u[c + 2] * scale), tc::to_tf32_rn(u[c + 3] * scale));
+                    if (hq >= Hk) {  // K^T tile: element (d, t), buffered over 4 tokens
+                        if (tb_n > 0 && (cs != tb_cs || r != tb_r0 + tb_n || tb_n == 4)) tb_flush();
+                        if (tb_n == 0) {
+                            tb_cs = cs;
+                            tb_r0 = r;
+                            tb_base = A.tqk + ((size_t)cs * Hk + hh) * kTileQK + 65536;
+                            tb_rows = 128;
+                            tb_row0 = d0;
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            if (e == tb_n) {
+#pragma unroll
+                                for (int c = 0; c < VEC; ++c) tb[c][e] = tc::to_tf32_rn(u[c] * scale);
+                            }
+                        ++tb_n;
+                    }
+                }
+            } else if (active) {
                 float4* dst = reinterpret_cast<float4*>(A.qk + (size_t)n * 2 * Hk * D + ch0);
 #pragma unroll
                 for (int c = 0; c < VEC; c += 4)
                     dst[c / 4] = make_float4(u[c] * scale, u[c + 1] * scale, u[c + 2] * scale, u[c + 3] * scale);
             }
+        } else if (active && A.tiles && D == 128) {
+            int64_t cs;
+            int r;
+            chunk_slot(n, start, s, cs, r);
+            const int c0 = ch0 - 2 * Hk * D, jj = c0 / D, dv0 = c0 % D, sl = dv0 / 32;
+            if (tb_n > 0 && (cs != tb_cs || r != tb_r0 + tb_n || tb_n == 4)) tb_flush();
+            if (tb_n == 0) {
+                tb_cs = cs;
+                tb_r0 = r;
+                tb_base = A.tv + (((size_t)cs * Hv + jj) * 4 + sl) * 8192;
+                tb_rows = 32;
+                tb_row0 = dv0 % 32;
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (e == tb_n) {
+#pragma unroll
+                    for (int c = 0; c < VEC; ++c) tb[c][e] = tc::to_tf32_rn(u[c]);
+                }
+            ++tb_n;
         } else if (active) {
             float4* dst = reinterpret_cast<float4*>(A.v + (size_t)n * Hv * D + (ch0 - 2 * Hk * D));
 #pragma unroll
             for (int c = 0; c < VEC; c += 4) dst[c / 4] = make_float4(u[c], u[c + 1], u[c + 2], u[c + 3]);
         }
     }
+    if (A.tiles && D == 128) tb_flush();
 }
 
 // ---------------------------------------------------------------------------
@@ -664,6 +793,35 @@ __global__ void __launch_bounds__(kChunkThreads, 1) k_chunk(const __grid_constan
 // with the decay masks, the UT inverse T = (I + A)^-1 (16x16 blocks, fp32)
 // and the moves between TMEM and the 128B-swizzled operand tiles done by all
 // 256 threads in between.  y = gated RMSNorm(diag(e^g) O1 + O2).
+// One warp: the 16x8 tile C = A(16 x K) B(K x 8) with A(m,k) = Ap[m*lda + k] and
+// B(k,n) = Bp[k*ldb + n], K a multiple of 8, fp32-accurate through the 3xTF32
+// split (hi*hi + hi*lo + lo*hi).  Lane layout of c: (g, 2t), (g, 2t+1),
+// (g+8, 2t), (g+8, 2t+1) with g = lane / 4, t = lane % 4.
+__device__ __forceinline__ void warp_tile16x8_precise(const float* Ap, int lda, const float* Bp, int ldb, int K,
+                                                      int lane, float c[4]) {
+    const int gq = lane >> 2, t4 = lane & 3;
+    c[0] = c[1] = c[2] = c[3] = 0.f;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        const float fa[4] = {Ap[gq * lda + k0 + t4], Ap[(gq + 8) * lda + k0 + t4], Ap[gq * lda + k0 + t4 + 4],
+                             Ap[(gq + 8) * lda + k0 + t4 + 4]};
+        const float fb[2] = {Bp[(k0 + t4) * ldb + gq], Bp[(k0 + t4 + 4) * ldb + gq]};
+        uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            ah[e] = to_tf32(fa[e]);
+            al[e] = to_tf32(fa[e] - __uint_as_float(ah[e]));
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            bh[e] = to_tf32(fb[e]);
+            bl[e] = to_tf32(fb[e] - __uint_as_float(bh[e]));
+        }
+        mma_tf32(c, al, bh);
+        mma_tf32(c, ah, bl);
+        mma_tf32(c, ah, bh);
+    }
+}
+
 namespace tcp {
 constexpr int C = 64, D = 128, DV = 32, NS = 4, THREADS = 256, LDA = 68;
 constexpr int OFF_Q = 0;                      // Q^   [64][128] tf32 tile
@@ -678,8 +836,8 @@ constexpr int OFF_UT = OFF_TW + 16384;        // U^T  [32][64]
 constexpr int OFF_AM = OFF_UT + 8192;         // fp32 A (also the V staging area) [64][68]
 constexpr int OFF_TM = OFF_AM + C * LDA * 4;  // fp32 T [64][68]
 constexpr int OFF_SMALL = OFF_TM + C * LDA * 4;
-constexpr int SMALL_FLOATS = 4 * C + 2 * C + 2 * C;  // gam, bet, eg, erev, ssq[2], ored[2]
-constexpr int SMEM = OFF_SMALL + SMALL_FLOATS * 4 + 64;
+constexpr int SMALL_FLOATS = 4 * C + 2 * C + 2 * C + DV;  // gam, bet, eg, erev, ssq[2], ored[2], norm_w slice
+constexpr int SMEM = OFF_SMALL + SMALL_FLOATS * 4 + 64;  // + 4 mbarriers and the TMEM address
 constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024 bytes
 // TMEM columns
 constexpr int cKK = 0, cQK = 64, cW = 128, cU = 256, cO1 = 288, cO2 = 320, cS = 352, TMEM_COLS = 512;
@@ -708,12 +866,19 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
     float* erev = eg + C;
     float* ssq = erev + C;   // [2][C]
     float* ored = ssq + 2 * C;  // [2][C]
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(ored + 2 * C);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    float* nwsl = ored + 2 * C;  // norm_w of this slice
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(nwsl + DV);  // MMA rounds
+    uint64_t* barQ = mbar + 1;   // Q^ tile of the chunk
+    uint64_t* barK = mbar + 2;   // K^ tile
+    uint64_t* barKV = mbar + 3;  // K^T and V^T tiles
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 4);
 
     if (warp == 0) tc::alloc(tslot, TMEM_COLS);
     if (tid == 0) {
         mbar_init(mbar, 1);
+        mbar_init(barQ, 1);
+        mbar_init(barK, 1);
+        mbar_init(barKV, 1);
         fence_mbar_init();
     }
     tc::fence_before();
@@ -738,10 +903,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         }
     }
     const int dS = 32 * q4 + lane;  // the d_k index this thread owns in S^T
-    float nw16[16];                 // norm weight of the 16 outputs this thread writes
-#pragma unroll
-    for (int c = 0; c < 16; ++c)
-        nw16[c] = (g.flags & kFlagNoOutNorm) ? 1.f : L::ld(A.p.norm_w, s_idx * DV + hf * 16 + c);
+    if (tid < DV) nwsl[tid] = (g.flags & kFlagNoOutNorm) ? 1.f : L::ld(A.p.norm_w, s_idx * DV + tid);
     {
         float v[16];
 #pragma unroll
@@ -775,71 +937,67 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
     const bool outnorm = !(g.flags & kFlagNoOutNorm);
     const int trow = 16 * q4 + (lane & 15);  // the chunk row this thread reads from M=64 accumulators
     const bool rowok = lane < 16;
+    // operand tiles come ready-made from the prologue: one bulk copy each,
+    // issued for chunk c+1 as soon as chunk c's last use of the buffer is done
+    auto cslot = [&](int c) -> size_t { return (size_t)(start / C + seq + c); };
+    auto issue_q = [&](int c) {
+        mbar_arrive_expect_tx(barQ, 32768);
+        bulk_g2s(Qs, A.tqk + (cslot(c) * Hk + h) * kTileQK, 32768, barQ);
+    };
+    auto issue_k = [&](int c) {
+        mbar_arrive_expect_tx(barK, 32768);
+        bulk_g2s(Ks, A.tqk + (cslot(c) * Hk + h) * kTileQK + 32768, 32768, barK);
+    };
+    auto issue_kv = [&](int c) {
+        mbar_arrive_expect_tx(barKV, 32768 + 8192);
+        bulk_g2s(KTs, A.tqk + (cslot(c) * Hk + h) * kTileQK + 65536, 32768, barKV);
+        bulk_g2s(VTs, A.tv + ((cslot(c) * Hv + j) * 4 + s_idx) * 8192, 8192, barKV);
+    };
+    auto wait_bar = [&](uint64_t* b, uint32_t par) {  // one warp polls, then everyone
+        bool w = true;
+        if (ok && warp == 0) {
+            w = mbar_wait(b, par);
+            if (!w) w = mbar_wait(b, par);
+        }
+        ok = __syncthreads_and(ok && w);
+    };
+    if (tid == 0 && n_chunks > 0) {
+        issue_q(0);
+        issue_k(0);
+        issue_kv(0);
+    }
+    float g_next = 0.f, b_next = 0.f;  // gates of the next chunk (threads < 64)
+    if (tid < C && n_chunks > 0) {
+        const float* gb = A.tgb + (cslot(0) * Hv + j) * 128;
+        g_next = gb[tid];
+        b_next = gb[C + tid];
+    }
     for (int ci = 0; ci < n_chunks; ++ci) {
         const int64_t t0 = start + (int64_t)ci * C;
         const int n = (int)((end - t0) < C ? (end - t0) : C);
         __syncthreads();
-        // ---- (1) load q^, k^, v, g, beta of the chunk (rows >= n are zero) --------
-        // all global reads go out at once (cp.async, 16 B each) into a staging
-        // area over the P/T/U/A tiles, which are dead at this point; then one
-        // shared-to-shared pass rounds to TF32 and swizzles.
-        float* stage = reinterpret_cast<float*>(Ps);  // [64][128] q^ | [64][128] k^ | [64][32] v
-        float* stq = stage;
-        float* stk = stage + C * D;
-        float* stv = stage + 2 * C * D;
-        for (int f = tid; f < C * 32; f += THREADS) {
-            const int r = f >> 5, c4 = f & 31;
-            const int ok_r = r < n ? 16 : 0;  // src-size 0 zero-fills
-            const size_t tok = (size_t)(t0 + (r < n ? r : 0));
-            cp_async16(stk + r * D + c4 * 4, A.qk + (tok * 2 * Hk + Hk + h) * D + c4 * 4, ok_r);
-            cp_async16(stq + r * D + c4 * 4, A.qk + (tok * 2 * Hk + h) * D + c4 * 4, ok_r);
-        }
-        for (int f = tid; f < C * (DV / 4); f += THREADS) {
-            const int r = f >> 3, c4 = f & 7;
-            const size_t tok = (size_t)(t0 + (r < n ? r : 0));
-            cp_async16(stv + r * DV + c4 * 4, A.v + (tok * Hv + j) * D + s_idx * DV + c4 * 4, r < n ? 16 : 0);
-        }
-        cp_async_commit_wait_all();
-        float zpre[16];  // z of this thread's output row, needed at the end of the chunk
-        if (outnorm && rowok && trow < n) {
-            const uint4* zp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(J.z) +
-                                                             (size_t)(t0 + trow) * Hv * D + (size_t)j * D +
-                                                             s_idx * DV + hf * 16);
-            const uint4 z0 = zp[0], z1 = zp[1];
-            const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&z0);
-            const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&z1);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float2 a = __bfloat1622float2(h0[c]), b = __bfloat1622float2(h1[c]);
-                zpre[2 * c] = a.x; zpre[2 * c + 1] = a.y; zpre[8 + 2 * c] = b.x; zpre[8 + 2 * c + 1] = b.y;
-            }
-        }
+        // ---- (1) the chunk's tiles (prefetched) and gates; zero the tail rows ------
         if (tid < C) {
-            gam[tid] = tid < n ? A.gl[(size_t)(t0 + tid) * Hv + j] : 0.f;
-            bet[tid] = tid < n ? A.beta[(size_t)(t0 + tid) * Hv + j] : 0.f;
+            gam[tid] = tid < n ? g_next : 0.f;
+            bet[tid] = tid < n ? b_next : 0.f;
+            if (ci + 1 < n_chunks) {  // gates of the next chunk, in flight during this one
+                const float* gb = A.tgb + (cslot(ci + 1) * Hv + j) * 128;
+                g_next = gb[tid];
+                b_next = gb[C + tid];
+            }
+        }
+        const uint32_t par = (uint32_t)(ci & 1);
+        wait_bar(barQ, par);
+        wait_bar(barK, par);
+        if (n < C) {  // rows of the last chunk past the sequence end were never written: zero them
+            for (int f = tid; f < (C - n) * 32; f += THREADS) {
+                const int r = n + (f >> 5), c4 = (f & 31) * 4;
+                *reinterpret_cast<float4*>(Qs + tc::sw_off(C, r, c4)) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4*>(Ks + tc::sw_off(C, r, c4)) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
         __syncthreads();
-        for (int f = tid; f < C * 32; f += THREADS) {
-            const int r = f >> 5, c4 = f & 31;
-            const float4 kv = *reinterpret_cast<const float4*>(stk + r * D + c4 * 4);
-            const float4 qv = *reinterpret_cast<const float4*>(stq + r * D + c4 * 4);
-            tc::st_row4(Ks, C, r, c4 * 4, kv.x, kv.y, kv.z, kv.w);
-            tc::st_row4(Qs, C, r, c4 * 4, qv.x, qv.y, qv.z, qv.w);
-        }
-        float* Vst = stv;  // [64][32] fp32
-        __syncthreads();
-        // ---- (2) transposes; gamma = cumsum(g) -----------------------------------
-        for (int d = warp * 16; d < warp * 16 + 16; ++d)
-            for (int tb = 0; tb < C; tb += 32) {
-                const int t = tb + lane;
-                *reinterpret_cast<float*>(KTs + tc::sw_off(D, d, t)) =
-                    *reinterpret_cast<const float*>(Ks + tc::sw_off(C, t, d));
-            }
-        for (int dv = warp * 4; dv < warp * 4 + 4; ++dv)
-            for (int tb = 0; tb < C; tb += 32) {
-                const int t = tb + lane;
-                tc::st_elem(VTs, DV, dv, t, Vst[t * DV + dv]);
-            }
+        // ---- (2) gamma = cumsum(g) ---------------------------------------------------
         if (warp == 0) {
             float run = 0.f;
             for (int base = 0; base < C; base += 32) {
@@ -869,8 +1027,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         for (int cb = 0; cb < 2; ++cb) {
             const int i0 = hf * 32 + cb * 16;
             float kk[16], qk[16];
-            tc::ld16(tc::taddr(tm, 32 * q4, cKK + i0), kk);
-            tc::ld16(tc::taddr(tm, 32 * q4, cQK + i0), qk);
+            tc::ld16x2(tc::taddr(tm, 32 * q4, cKK + i0), kk, tc::taddr(tm, 32 * q4, cQK + i0), qk);
             if (rowok) {
                 const int t = trow;
 #pragma unroll
@@ -879,7 +1036,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int i = i0 + c + e;
-                        const float dec = i <= t ? expf(gam[t] - gam[i]) : 0.f;  // exponent <= 0 only
+                        const float dec = i <= t ? __expf(gam[t] - gam[i]) : 0.f;  // exponent <= 0 only
                         a4[e] = i < t ? bet[t] * dec * kk[c + e] : 0.f;
                         p4[e] = dec * qk[c + e];
                     }
@@ -890,17 +1047,22 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         }
         __syncthreads();
         // ---- T = (I + A)^-1: 16x16 diagonal blocks, then block merges ------------------
-        // diagonal blocks: a lane owns one column of a block in registers and
-        // runs the forward substitution x_i = e_i - sum_{k<i} A_ik x_k
+        // diagonal blocks: a lane owns column j of a block (x[i] = X_ij) and
+        // column j of A; right-looking substitution: once x_k is final, every
+        // later row takes -A_ik x_k (A_ik from lane k by shuffle), so the
+        // dependent chain is 16 FMAs long
         if (warp < 2) {
-            const int b0 = (warp * 2 + (lane >> 4)) * 16, jc = lane & 15;
+            const int b0 = (warp * 2 + (lane >> 4)) * 16, jc = lane & 15, lb = lane & 16;
+            float acol[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acol[i] = Am[(b0 + i) * LDA + b0 + jc];
             float x[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                float acc = (i == jc) ? 1.f : 0.f;
+            for (int i = 0; i < 16; ++i) x[i] = (i == jc) ? 1.f : 0.f;
 #pragma unroll
-                for (int k = 0; k < i; ++k) acc = fmaf(-Am[(b0 + i) * LDA + b0 + k], x[k], acc);
-                x[i] = acc;
+            for (int k = 0; k < 15; ++k) {
+#pragma unroll
+                for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-__shfl_sync(0xffffffffu, acol[i], lb + k), x[k], x[i]);
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) Tm[(b0 + i) * LDA + b0 + jc] = x[i];
@@ -910,52 +1072,36 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
             if ((c >> 4) > (t >> 4)) Tm[t * LDA + c] = 0.f;
         }
         __syncthreads();
-        // off-diagonal blocks by distance: X_ab = -X_aa sum_{c=b}^{a-1} A_ac X_cb,
-        // one output element per thread per block
+        // off-diagonal blocks by distance: X_ab = -X_aa sum_{c=b}^{a-1} A_ac X_cb;
+        // the 16x16 block products run on warp-level mma.sync (3xTF32), one
+        // 16x8 half block per warp
         for (int dd = 1; dd < 4; ++dd) {
-            const int nel = (4 - dd) * 256;
-            float y[3];
-#pragma unroll
-            for (int q = 0; q < 3; ++q) {
-                const int e = tid + q * THREADS;
-                y[q] = 0.f;
-                if (e < nel) {
-                    const int bb = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                    const int a0 = (bb + dd) * 16, c0b = bb * 16;
-                    float acc = 0.f;
-                    for (int k = c0b; k < a0; ++k) acc = fmaf(Am[(a0 + r) * LDA + k], Tm[k * LDA + c0b + c], acc);
-                    y[q] = acc;
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < 3; ++q) {  // Y into the (unused) target block
-                const int e = tid + q * THREADS;
-                if (e < nel) {
-                    const int bb = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                    Tm[((bb + dd) * 16 + r) * LDA + bb * 16 + c] = y[q];
-                }
+            const int ntile = (4 - dd) * 2;
+            for (int tl = warp; tl < ntile; tl += THREADS / 32) {  // Y = A_a[b..a) X_[b..a)b
+                const int bb = tl >> 1, nt = tl & 1;
+                const int a0 = (bb + dd) * 16, c0b = bb * 16;
+                float cc[4];
+                warp_tile16x8_precise(Am + a0 * LDA + c0b, LDA, Tm + c0b * LDA + c0b + 8 * nt, LDA, a0 - c0b, lane,
+                                      cc);
+                const int gq = lane >> 2, t4 = lane & 3;
+                float* y0 = Tm + a0 * LDA + c0b + 8 * nt;
+                y0[gq * LDA + 2 * t4] = cc[0];
+                y0[gq * LDA + 2 * t4 + 1] = cc[1];
+                y0[(gq + 8) * LDA + 2 * t4] = cc[2];
+                y0[(gq + 8) * LDA + 2 * t4 + 1] = cc[3];
             }
             __syncthreads();
-#pragma unroll
-            for (int q = 0; q < 3; ++q) {
-                const int e = tid + q * THREADS;
-                if (e < nel) {
-                    const int bb = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                    const int a0 = (bb + dd) * 16, c0b = bb * 16;
-                    float acc = 0.f;
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) acc = fmaf(Tm[(a0 + r) * LDA + a0 + k], Tm[(a0 + k) * LDA + c0b + c], acc);
-                    y[q] = -acc;
-                }
-            }
-            __syncthreads();  // every read of Y done before it is overwritten
-#pragma unroll
-            for (int q = 0; q < 3; ++q) {
-                const int e = tid + q * THREADS;
-                if (e < nel) {
-                    const int bb = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                    Tm[((bb + dd) * 16 + r) * LDA + bb * 16 + c] = y[q];
-                }
+            for (int tl = warp; tl < ntile; tl += THREADS / 32) {  // X_ab = -X_aa Y
+                const int bb = tl >> 1, nt = tl & 1;
+                const int a0 = (bb + dd) * 16, c0b = bb * 16;
+                float cc[4];
+                warp_tile16x8_precise(Tm + a0 * LDA + a0, LDA, Tm + a0 * LDA + c0b + 8 * nt, LDA, 16, lane, cc);
+                const int gq = lane >> 2, t4 = lane & 3;
+                float* x0 = Tm + a0 * LDA + c0b + 8 * nt;
+                x0[gq * LDA + 2 * t4] = -cc[0];
+                x0[gq * LDA + 2 * t4 + 1] = -cc[1];
+                x0[(gq + 8) * LDA + 2 * t4] = -cc[2];
+                x0[(gq + 8) * LDA + 2 * t4 + 1] = -cc[3];
             }
             __syncthreads();
         }
@@ -967,6 +1113,14 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
             tc::st_row4(TWs, C, t, i, tv.x * bet[i] * eg[i], tv.y * bet[i + 1] * eg[i + 1],
                         tv.z * bet[i + 2] * eg[i + 2], tv.w * bet[i + 3] * eg[i + 3]);
         }
+        wait_bar(barKV, par);
+        if (n < C) {  // tail columns (t >= n) of K^T and V^T
+            for (int f = tid; f < (D + DV) * (C - n); f += THREADS) {
+                const int row = f / (C - n), t = n + f % (C - n);
+                if (row < D) *reinterpret_cast<float*>(KTs + tc::sw_off(D, row, t)) = 0.f;
+                else *reinterpret_cast<float*>(VTs + tc::sw_off(DV, row - D, t)) = 0.f;
+            }
+        }
         // ---- R2: U~, W, O1 ------------------------------------------------------------------
         mma_round_begin();
         if (tid == 0 && ok) {
@@ -976,6 +1130,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
             tc::mma_tf32(tm + cO1, Qs, C, S0s, DV, D, tc::idesc_tf32(C, DV), false);
         }
         mma_round_end();
+        if (tid == 0 && ci + 1 < n_chunks) issue_q(ci + 1);  // Q^ of this chunk is no longer read
         // W -> operand tile over K^ (no longer needed)
         for (int cb = 0; cb < 4; ++cb) {
             const int d0 = hf * 64 + cb * 16;
@@ -994,6 +1149,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
             tc::mma_tf32(tm + cU, Ks, C, S0s, DV, D, tc::idesc_tf32(C, DV, true), true);
         }
         mma_round_end();
+        if (tid == 0 && ci + 1 < n_chunks) issue_k(ci + 1);  // W (over K^) has been read
         {
             // U -> U^T and (diag(e^(gC - g)) U)^T tiles; S^T *= e^gC in TMEM
             float u16[16];
@@ -1019,13 +1175,27 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
             tc::mma_tf32(tm + cO2, Ps, C, UTs, DV, C, tc::idesc_tf32(C, DV), false);
             tc::mma_tf32(tm + cS, KTs, D, VTs, DV, C, tc::idesc_tf32(D, DV), true);
         }
+        float zpre[16];  // z of this thread's output row (loaded while R4 runs)
+        if (outnorm && rowok && trow < n) {
+            const uint4* zp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(J.z) +
+                                                             (size_t)(t0 + trow) * Hv * D + (size_t)j * D +
+                                                             s_idx * DV + hf * 16);
+            const uint4 z0 = zp[0], z1 = zp[1];
+            const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&z0);
+            const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&z1);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float2 a = __bfloat1622float2(h0[c]), b = __bfloat1622float2(h1[c]);
+                zpre[2 * c] = a.x; zpre[2 * c + 1] = a.y; zpre[8 + 2 * c] = b.x; zpre[8 + 2 * c + 1] = b.y;
+            }
+        }
         mma_round_end();
+        if (tid == 0 && ci + 1 < n_chunks) issue_kv(ci + 1);  // K^T and (the U' over) V^T are read
         // ---- O = diag(e^g) O1 + O2; S^T -> S operand tile for the next chunk ----------------
         float o16[16];
         {
             float a16[16];
-            tc::ld16(tc::taddr(tm, 32 * q4, cO1 + hf * 16), a16);
-            tc::ld16(tc::taddr(tm, 32 * q4, cO2 + hf * 16), o16);
+            tc::ld16x2(tc::taddr(tm, 32 * q4, cO1 + hf * 16), a16, tc::taddr(tm, 32 * q4, cO2 + hf * 16), o16);
             float part = 0.f;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
@@ -1052,7 +1222,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
             }
             float yv[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) yv[c] = outnorm ? o16[c] * rstd * nw16[c] * siluf_(zpre[c]) : o16[c];
+            for (int c = 0; c < 16; ++c) yv[c] = outnorm ? o16[c] * rstd * nwsl[hf * 16 + c] * siluf_(zpre[c]) : o16[c];
             uint4 pk[2];
             __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll
@@ -1122,6 +1292,16 @@ cudaError_t launch_prefill_t(const Geom& g, const LayerParams& p, const PrefillJ
     A.gl = reinterpret_cast<float*>(ws + wl.g);
     A.beta = reinterpret_cast<float*>(ws + wl.beta);
     A.NS = prefill_slices(D);
+    A.tiles = (D == 128 && g.chunk == 64 && g.act_bf16 && std::getenv("GDN_PREFILL_PRECISE") == nullptr &&
+               std::getenv("GDN_PREFILL_MMA_SYNC") == nullptr)
+                  ? 1
+                  : 0;
+    if (A.tiles) {
+        const TileWs tl = tile_ws(g, J.n_tokens, J.n_seq);
+        A.tqk = reinterpret_cast<unsigned char*>(ws + tl.qk);
+        A.tv = reinterpret_cast<unsigned char*>(ws + tl.v);
+        A.tgb = reinterpret_cast<float*>(ws + tl.gb);
+    }
     if (J.n_tokens > 0) {
         constexpr int VEC = 16 / (int)sizeof(TA);
         const dim3 blocks((unsigned)((J.n_tokens + kProTok - 1) / kProTok),
@@ -1137,9 +1317,7 @@ cudaError_t launch_prefill_t(const Geom& g, const LayerParams& p, const PrefillJ
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (D == 128 && g.chunk == 64 && g.act_bf16 && std::getenv("GDN_PREFILL_PRECISE") == nullptr &&
-        std::getenv("GDN_PREFILL_MMA_SYNC") == nullptr)
-        return launch_chunk_tc(A, st);
+    if (A.tiles) return launch_chunk_tc(A, st);
     const int DV = D / A.NS;
     const ChunkSmem lay = chunk_smem(g.chunk, D, DV);
     const size_t smem = (size_t)lay.total * sizeof(float);
@@ -1167,9 +1345,10 @@ cudaError_t launch_prefill_t(const Geom& g, const LayerParams& p, const PrefillJ
 cudaError_t take_device_status_prefill(unsigned* out) { return take_device_status_tu(out); }
 
 size_t prefill_workspace_bytes(const Geom& g, int64_t n_tokens, int n_seq) {
-    (void)n_seq;
     if (n_tokens <= 0) return 0;
-    return ws_layout(g, n_tokens).total;
+    size_t bytes = ws_layout(g, n_tokens).total;
+    if (g.D == 128 && g.chunk == 64 && g.act_bf16) bytes = std::max(bytes, tile_ws(g, n_tokens, n_seq).total);
+    return bytes;
 }
 
 cudaError_t launch_prefill(const Geom& g, const LayerParams& p, const PrefillJob& J, cudaStream_t st) {
