@@ -87,10 +87,13 @@ WsLayout ws_layout(const Geom& g, int64_t N) {
 //   per (slot, k-head): Q^ [64][128] | K^ [64][128] | K^T [128][64]   (3 x 32 KB)
 //   per (slot, v-head, slice): V^T [32][64]                           (8 KB)
 //   per (slot, v-head): g [64], beta [64]                              (512 B)
+//   per (slot, v-head): chain record written by the prep kernel       (65 KB)
+//     W [64][128] | T diag(beta) [64][64] | P [64][64] | e^gamma [64], e^(gamma_C - gamma) [64]
 constexpr size_t kTileQK = 3 * 32768, kTileV = 4 * 8192, kTileGB = 2 * 64 * 4;
+constexpr size_t kRecW = 0, kRecTB = 32768, kRecP = 49152, kRecG = 65536, kTileRec = 66560;
 
 struct TileWs {
-    size_t qk, v, gb, total;
+    size_t qk, v, gb, rec, total;
     int64_t ncs;
 };
 
@@ -106,6 +109,8 @@ TileWs tile_ws(const Geom& g, int64_t N, int n_seq) {
     off = align1024(off + (size_t)L.ncs * g.Hv * kTileV);
     L.gb = off;
     off = align1024(off + (size_t)L.ncs * g.Hv * kTileGB);
+    L.rec = off;
+    off = align1024(off + (size_t)L.ncs * g.Hv * kTileRec);
     L.total = off;
     return L;
 }
@@ -121,6 +126,8 @@ struct PrefillArgs {
     unsigned char* tqk;  // tile workspace (tcgen05 path), see TileWs
     unsigned char* tv;
     float* tgb;
+    unsigned char* trec;  // chain records (prep kernel -> chain kernel)
+    int64_t ncs;          // chunk slots of the tile workspace
     int tiles;           // 1: the prologue writes the tile workspace
     int NS;
 };
@@ -779,20 +786,28 @@ __global__ void __launch_bounds__(kChunkThreads, 1) k_chunk(const __grid_constan
 }
 
 // ---------------------------------------------------------------------------
-// 3b. chunk kernel on the 5th-generation tensor cores (d = 128, C = 64, bf16)
+// 3b. tcgen05 path (d = 128, C = 64, bf16): prep kernel + chain kernel
 // ---------------------------------------------------------------------------
-// One CTA per (sequence, v-head j, slice of 32 of the 128 state rows); the 4
-// slices of a v-head form a cluster for the output norm.  The fp32 state
-// slice lives in TMEM as S^T (lane = d_k index, 32 columns = this slice's
-// d_v rows) for the whole sequence.  Per chunk of 64 tokens, four rounds of
-// tcgen05.mma (TF32 operands rounded to nearest, fp32 accumulation in TMEM):
-//   R1  KK^T, QK^T                      (64x64, K = 128)
-//   R2  U~ = (T diag(b)) V, W = (T diag(b e^g)) K, O1 = Q S^T
-//   R3  U = U~ - W S^T                  (negated-A accumulate)
-//   R4  O2 = P U, S^T <- e^gC S^T + K^T (diag(e^(gC - g)) U)
-// with the decay masks, the UT inverse T = (I + A)^-1 (16x16 blocks, fp32)
-// and the moves between TMEM and the 128B-swizzled operand tiles done by all
-// 256 threads in between.  y = gated RMSNorm(diag(e^g) O1 + O2).
+// The chunk form splits into work that does not depend on the state and the
+// short sequential chain that does.
+//
+// k_chunk_prep, one CTA per (chunk slot, v-head j), all chunks in parallel:
+//   gamma = cumsum(g), KK^T and QK^T (tcgen05), the decay masks
+//   A = strict-lower(beta_t e^(gamma_t - gamma_i) KK^T) and
+//   P = lower-incl(e^(gamma_t - gamma_i) QK^T), T = (I + A)^-1 (16x16 blocks,
+//   fp32), T diag(beta), and W = T diag(beta e^gamma) K (tcgen05); W, T
+//   diag(beta), P as TF32 operand tiles and e^gamma, e^(gamma_C - gamma) go
+//   to the chain record of the chunk.
+// k_chunk_tc, one CTA per (sequence, v-head j, slice of 32 of the 128 state
+// rows), the 4 slices of a v-head a cluster: the fp32 state slice lives in
+// TMEM as S^T (lane = d_k index, 32 columns = this slice's d_v rows) for the
+// whole sequence, and per chunk two rounds of tcgen05.mma
+//   Ra  U = T diag(beta) V - W S^T,  O1 = Q S^T
+//   Rb  O2 = P U,  S^T <- e^gamma_C S^T + K^T (diag(e^(gamma_C - gamma)) U)
+// with y = gated RMSNorm(diag(e^gamma) O1 + O2) of chunk c written while Ra
+// of chunk c+1 runs.  TF32 operands are rounded to nearest; accumulation is
+// fp32 in TMEM.
+
 // One warp: the 16x8 tile C = A(16 x K) B(K x 8) with A(m,k) = Ap[m*lda + k] and
 // B(k,n) = Bp[k*ldb + n], K a multiple of 8, fp32-accurate through the 3xTF32
 // split (hi*hi + hi*lo + lo*hi).  Lane layout of c: (g, 2t), (g, 2t+1),
@@ -822,30 +837,306 @@ __device__ __forceinline__ void warp_tile16x8_precise(const float* Ap, int lda, 
     }
 }
 
+// sequence owning chunk slot cs: the largest s with floor(start_s / 64) + s <= cs
+__device__ __forceinline__ int slot_seq(const PrefillJob& J, int64_t cs) {
+    if (!J.cu_seqlens) return 0;
+    int lo = 0, hi = J.n_seq - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        int64_t st, en;
+        seq_bounds(J, mid, st, en);
+        if (st / 64 + mid <= cs) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
 namespace tcp {
 constexpr int C = 64, D = 128, DV = 32, NS = 4, THREADS = 256, LDA = 68;
-constexpr int OFF_Q = 0;                      // Q^   [64][128] tf32 tile
-constexpr int OFF_K = OFF_Q + 32768;          // K^   [64][128], later W [64][128]
-constexpr int OFF_KT = OFF_K + 32768;         // K^T  [128][64]
-constexpr int OFF_VT = OFF_KT + 32768;        // V^T  [32][64], later (diag(e^(gC-g)) U)^T
-constexpr int OFF_S0 = OFF_VT + 8192;         // S    [32][128] (this slice's rows)
-constexpr int OFF_P = OFF_S0 + 16384;         // P    [64][64]
-constexpr int OFF_TB = OFF_P + 16384;         // T diag(b)      [64][64]
-constexpr int OFF_TW = OFF_TB + 16384;        // T diag(b e^g)  [64][64]
-constexpr int OFF_UT = OFF_TW + 16384;        // U^T  [32][64]
-constexpr int OFF_AM = OFF_UT + 8192;         // fp32 A (also the V staging area) [64][68]
-constexpr int OFF_TM = OFF_AM + C * LDA * 4;  // fp32 T [64][68]
-constexpr int OFF_SMALL = OFF_TM + C * LDA * 4;
-constexpr int SMALL_FLOATS = 4 * C + 2 * C + 2 * C + DV;  // gam, bet, eg, erev, ssq[2], ored[2], norm_w slice
-constexpr int SMEM = OFF_SMALL + SMALL_FLOATS * 4 + 64;  // + 4 mbarriers and the TMEM address
-constexpr int SMEM_ALLOC = SMEM + 1024;  // room to align the base to 1024 bytes
-// TMEM columns
-constexpr int cKK = 0, cQK = 64, cW = 128, cU = 256, cO1 = 288, cO2 = 320, cS = 352, TMEM_COLS = 512;
+// prep kernel shared memory
+constexpr int PR_R0 = 0;                       // Q^, then K^T, then W staging   (32 KB)
+constexpr int PR_R1 = 32768;                   // K^, then P | T diag(b) staging (32 KB)
+constexpr int PR_AM = 65536;                   // fp32 A [64][68], then the T diag(b e^g) tile
+constexpr int PR_TM = PR_AM + C * LDA * 4;     // fp32 T [64][68]
+constexpr int PR_SMALL = PR_TM + C * LDA * 4;  // gam, bet, e^g, e^(gC-g)
+constexpr int PR_SMEM = PR_SMALL + 4 * C * 4 + 64;
+constexpr int PR_SMEM_ALLOC = PR_SMEM + 1024;
+constexpr int pKK = 0, pQK = 64, pW = 128, PR_TMEM_COLS = 256;
+// chain kernel shared memory
+constexpr int OFF_Q = 0;                   // Q^  [64][128]
+constexpr int OFF_W = OFF_Q + 32768;       // W   [64][128]
+constexpr int OFF_KT = OFF_W + 32768;      // K^T [128][64]
+constexpr int OFF_TB = OFF_KT + 32768;     // T diag(b) [64][64]
+constexpr int OFF_P = OFF_TB + 16384;      // P   [64][64]
+constexpr int OFF_VT = OFF_P + 16384;      // V^T of this slice [32][64]
+constexpr int OFF_UP = OFF_VT + 8192;      // (diag(e^(gC-g)) U)^T [32][64]
+constexpr int OFF_UT = OFF_UP + 8192;      // U^T [32][64]
+constexpr int OFF_S0 = OFF_UT + 8192;      // S   [32][128] (this slice's rows)
+constexpr int OFF_G = OFF_S0 + 16384;      // e^g [64] | e^(gC-g) [64]
+constexpr int OFF_SMALL = OFF_G + 512;     // ssq [2][64], ored [2][64], norm_w slice [32]
+constexpr int SMALL_FLOATS = 4 * C + DV;
+constexpr int SMEM = OFF_SMALL + SMALL_FLOATS * 4 + 64;  // + 3 mbarriers and the TMEM address
+constexpr int SMEM_ALLOC = SMEM + 1024;                  // room to align the base to 1024 bytes
+constexpr int cU = 0, cO1 = 32, cO2 = 64, cS = 96, TMEM_COLS = 128;
 }  // namespace tcp
+
+__global__ void __launch_bounds__(tcp::THREADS, 2) k_chunk_prep(const __grid_constant__ PrefillArgs A) {
+    using namespace tcp;
+    const Geom& g = A.g;
+    const PrefillJob& J = A.J;
+    const int Hk = g.Hk, Hv = g.Hv;
+    const int j = blockIdx.x, h = j / g.G;
+    const int64_t cs = (int64_t)blockIdx.z * gridDim.y + blockIdx.y;
+    if (cs >= A.ncs) return;
+    const int sq = slot_seq(J, cs);
+    int64_t start, end;
+    seq_bounds(J, sq, start, end);
+    const int64_t t0 = (cs - (start / C + sq)) * C + start;
+    if (t0 < start || t0 >= end) return;  // a slot between two sequences' chunks
+    const int n = (int)((end - t0) < C ? (end - t0) : C);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int q4 = warp & 3, hf = warp >> 2;
+    const int trow = 16 * q4 + (lane & 15);  // the chunk row this thread reads from M=64 accumulators
+    const bool rowok = lane < 16;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
+    unsigned char *R0 = sm + PR_R0, *R1 = sm + PR_R1;
+    unsigned char *Ps = R1, *TBs = R1 + 16384, *TWs = sm + PR_AM;
+    float* Am = reinterpret_cast<float*>(sm + PR_AM);
+    float* Tm = reinterpret_cast<float*>(sm + PR_TM);
+    float* gam = reinterpret_cast<float*>(sm + PR_SMALL);
+    float* bet = gam + C;
+    float* eg = bet + C;
+    float* erev = eg + C;  // e^g and e^(gC-g) contiguous: one bulk store
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(erev + C);
+    uint64_t* barQK = mbar + 1;
+    uint64_t* barKT = mbar + 2;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 3);
+    const unsigned char* tile = A.tqk + ((size_t)cs * Hk + h) * kTileQK;
+    unsigned char* rec = A.trec + ((size_t)cs * Hv + j) * kTileRec;
+
+    if (warp == 0) tc::alloc(tslot, PR_TMEM_COLS);
+    if (tid == 0) {
+        mbar_init(mbar, 1);
+        mbar_init(barQK, 1);
+        mbar_init(barKT, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(barQK, 65536);
+        bulk_g2s(R0, tile, 32768, barQK);
+        bulk_g2s(R1, tile + 32768, 32768, barQK);
+    }
+    if (tid < C) {
+        const float* gb = A.tgb + ((size_t)cs * Hv + j) * 128;
+        gam[tid] = tid < n ? gb[tid] : 0.f;
+        bet[tid] = tid < n ? gb[C + tid] : 0.f;
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = *tslot;
+    uint32_t phase = 0;
+    bool ok = true;
+    auto wait_bar = [&](uint64_t* b, uint32_t par) {  // one warp polls, then everyone
+        bool w = true;
+        if (ok && warp == 0) {
+            w = mbar_wait(b, par);
+            if (!w) w = mbar_wait(b, par);
+        }
+        ok = __syncthreads_and(ok && w);
+    };
+    auto mma_round_begin = [&]() {
+        tc::fence_before();
+        fence_proxy_async_smem();
+        __syncthreads();
+    };
+    auto mma_round_end = [&]() {
+        if (tid == 0) tc::commit(mbar);
+        bool w = true;
+        if (ok && warp == 0) {
+            w = mbar_wait(mbar, phase);
+            if (!w) w = mbar_wait(mbar, phase);
+        }
+        phase ^= 1u;
+        ok = __syncthreads_and(ok && w);
+        tc::fence_after();
+    };
+
+    // ---- gamma = cumsum(g), e^gamma, e^(gamma_C - gamma) ----------------------------
+    if (warp == 0) {
+        float run = 0.f;
+        for (int base = 0; base < C; base += 32) {
+            float v = gam[base + lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float o = __shfl_up_sync(0xffffffffu, v, off);
+                if (lane >= off) v += o;
+            }
+            v += run;
+            gam[base + lane] = v;
+            eg[base + lane] = expf(v);
+            run = __shfl_sync(0xffffffffu, v, 31);
+        }
+        __syncwarp();
+        for (int t = lane; t < C; t += 32) erev[t] = expf(gam[C - 1] - gam[t]);
+    }
+    wait_bar(barQK, 0);
+    if (n < C) {  // rows past the sequence end were never written: zero them
+        for (int f = tid; f < (C - n) * 32; f += THREADS) {
+            const int r = n + (f >> 5), c4 = (f & 31) * 4;
+            *reinterpret_cast<float4*>(R0 + tc::sw_off(C, r, c4)) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(R1 + tc::sw_off(C, r, c4)) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    // ---- KK^T, QK^T ----------------------------------------------------------------------
+    mma_round_begin();
+    if (tid == 0 && ok) {
+        tc::fence_after();
+        tc::mma_tf32(tm + pKK, R1, C, R1, C, D, tc::idesc_tf32(C, C), false);
+        tc::mma_tf32(tm + pQK, R0, C, R1, C, D, tc::idesc_tf32(C, C), false);
+    }
+    mma_round_end();
+    if (tid == 0) {  // Q^ is no longer read: K^T into its place
+        mbar_arrive_expect_tx(barKT, 32768);
+        bulk_g2s(R0, tile + 65536, 32768, barKT);
+    }
+    // ---- decay masks: A (strictly lower, beta_t), P (lower incl.) -----------------------
+    for (int cb = 0; cb < 2; ++cb) {
+        const int i0 = hf * 32 + cb * 16;
+        float kk[16], qk[16];
+        tc::ld16x2(tc::taddr(tm, 32 * q4, pKK + i0), kk, tc::taddr(tm, 32 * q4, pQK + i0), qk);
+        if (rowok) {
+            const int t = trow;
+#pragma unroll
+            for (int c = 0; c < 16; c += 4) {
+                float a4[4], p4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = i0 + c + e;
+                    const float dec = i <= t ? __expf(gam[t] - gam[i]) : 0.f;  // exponent <= 0 only
+                    a4[e] = i < t ? bet[t] * dec * kk[c + e] : 0.f;
+                    p4[e] = dec * qk[c + e];
+                }
+                *reinterpret_cast<float4*>(Am + t * LDA + i0 + c) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+                tc::st_row4(Ps, C, t, i0 + c, p4[0], p4[1], p4[2], p4[3]);
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_s2g(rec + kRecP, Ps, 16384);
+        bulk_s2g(rec + kRecG, eg, 2 * C * 4);
+        bulk_commit();
+    }
+    // ---- T = (I + A)^-1: 16x16 diagonal blocks, then block merges ------------------
+    // diagonal blocks: a lane owns column j of a block (x[i] = X_ij) and
+    // column j of A; right-looking substitution: once x_k is final, every
+    // later row takes -A_ik x_k (A_ik from lane k by shuffle), so the
+    // dependent chain is 16 FMAs long
+    if (warp < 2) {
+        const int b0 = (warp * 2 + (lane >> 4)) * 16, jc = lane & 15, lb = lane & 16;
+        float acol[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acol[i] = Am[(b0 + i) * LDA + b0 + jc];
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) x[i] = (i == jc) ? 1.f : 0.f;
+#pragma unroll
+        for (int k = 0; k < 15; ++k) {
+#pragma unroll
+            for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-__shfl_sync(0xffffffffu, acol[i], lb + k), x[k], x[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) Tm[(b0 + i) * LDA + b0 + jc] = x[i];
+    }
+    for (int f = tid; f < C * C; f += THREADS) {
+        const int t = f >> 6, c = f & 63;
+        if ((c >> 4) > (t >> 4)) Tm[t * LDA + c] = 0.f;
+    }
+    __syncthreads();
+    // off-diagonal blocks by distance: X_ab = -X_aa sum_{c=b}^{a-1} A_ac X_cb;
+    // the 16x16 block products run on warp-level mma.sync (3xTF32), one
+    // 16x8 half block per warp
+    for (int dd = 1; dd < 4; ++dd) {
+        const int ntile = (4 - dd) * 2;
+        for (int tl = warp; tl < ntile; tl += THREADS / 32) {  // Y = A_a[b..a) X_[b..a)b
+            const int bb = tl >> 1, nt = tl & 1;
+            const int a0 = (bb + dd) * 16, c0b = bb * 16;
+            float cc[4];
+            warp_tile16x8_precise(Am + a0 * LDA + c0b, LDA, Tm + c0b * LDA + c0b + 8 * nt, LDA, a0 - c0b, lane, cc);
+            const int gq = lane >> 2, t4 = lane & 3;
+            float* y0 = Tm + a0 * LDA + c0b + 8 * nt;
+            y0[gq * LDA + 2 * t4] = cc[0];
+            y0[gq * LDA + 2 * t4 + 1] = cc[1];
+            y0[(gq + 8) * LDA + 2 * t4] = cc[2];
+            y0[(gq + 8) * LDA + 2 * t4 + 1] = cc[3];
+        }
+        __syncthreads();
+        for (int tl = warp; tl < ntile; tl += THREADS / 32) {  // X_ab = -X_aa Y
+            const int bb = tl >> 1, nt = tl & 1;
+            const int a0 = (bb + dd) * 16, c0b = bb * 16;
+            float cc[4];
+            warp_tile16x8_precise(Tm + a0 * LDA + a0, LDA, Tm + a0 * LDA + c0b + 8 * nt, LDA, 16, lane, cc);
+            const int gq = lane >> 2, t4 = lane & 3;
+            float* x0 = Tm + a0 * LDA + c0b + 8 * nt;
+            x0[gq * LDA + 2 * t4] = -cc[0];
+            x0[gq * LDA + 2 * t4 + 1] = -cc[1];
+            x0[(gq + 8) * LDA + 2 * t4] = -cc[2];
+            x0[(gq + 8) * LDA + 2 * t4 + 1] = -cc[3];
+        }
+        __syncthreads();
+    }
+    // ---- T diag(beta) (to the record) and T diag(beta e^gamma) (over A) -------------------
+    for (int f = tid; f < C * 16; f += THREADS) {
+        const int t = f >> 4, i = (f & 15) * 4;
+        const float4 tv = *reinterpret_cast<const float4*>(Tm + t * LDA + i);
+        tc::st_row4(TBs, C, t, i, tv.x * bet[i], tv.y * bet[i + 1], tv.z * bet[i + 2], tv.w * bet[i + 3]);
+        tc::st_row4(TWs, C, t, i, tv.x * bet[i] * eg[i], tv.y * bet[i + 1] * eg[i + 1],
+                    tv.z * bet[i + 2] * eg[i + 2], tv.w * bet[i + 3] * eg[i + 3]);
+    }
+    fence_proxy_async_smem();
+    wait_bar(barKT, 0);
+    if (tid == 0) {
+        bulk_s2g(rec + kRecTB, TBs, 16384);
+        bulk_commit();
+    }
+    if (n < C) {  // tail columns (t >= n) of K^T
+        for (int f = tid; f < D * (C - n); f += THREADS) {
+            const int row = f / (C - n), t = n + f % (C - n);
+            *reinterpret_cast<float*>(R0 + tc::sw_off(D, row, t)) = 0.f;
+        }
+    }
+    // ---- W = T diag(beta e^gamma) K --------------------------------------------------------
+    mma_round_begin();
+    if (tid == 0 && ok) {
+        tc::fence_after();
+        tc::mma_tf32(tm + pW, TWs, C, R0, D, C, tc::idesc_tf32(C, D), false);
+    }
+    mma_round_end();
+    for (int cb = 0; cb < 4; ++cb) {  // W -> operand tile over K^T (no longer read)
+        const int d0 = hf * 64 + cb * 16;
+        float w16[16];
+        tc::ld16(tc::taddr(tm, 32 * q4, pW + d0), w16);
+        if (rowok) {
+#pragma unroll
+            for (int c = 0; c < 16; c += 4) tc::st_row4(R0, C, trow, d0 + c, w16[c], w16[c + 1], w16[c + 2], w16[c + 3]);
+        }
+    }
+    fence_proxy_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_s2g(rec + kRecW, R0, 32768);
+        bulk_commit();
+        bulk_wait_all();  // shared memory stays valid until the stores have completed
+    }
+    if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
+    if (warp == 0) tc::dealloc(tm, PR_TMEM_COLS);
+}
 
 __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_constant__ PrefillArgs A) {
     using namespace tcp;
-    using L = Act<__nv_bfloat16>;
     cg::cluster_group cluster = cg::this_cluster();
     const Geom& g = A.g;
     const PrefillJob& J = A.J;
@@ -856,29 +1147,22 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
-    unsigned char *Qs = sm + OFF_Q, *Ks = sm + OFF_K, *KTs = sm + OFF_KT, *VTs = sm + OFF_VT, *S0s = sm + OFF_S0;
-    unsigned char *Ps = sm + OFF_P, *TBs = sm + OFF_TB, *TWs = sm + OFF_TW, *UTs = sm + OFF_UT;
-    float* Am = reinterpret_cast<float*>(sm + OFF_AM);
-    float* Tm = reinterpret_cast<float*>(sm + OFF_TM);
-    float* gam = reinterpret_cast<float*>(sm + OFF_SMALL);
-    float* bet = gam + C;
-    float* eg = bet + C;
-    float* erev = eg + C;
-    float* ssq = erev + C;   // [2][C]
-    float* ored = ssq + 2 * C;  // [2][C]
-    float* nwsl = ored + 2 * C;  // norm_w of this slice
+    unsigned char *Qs = sm + OFF_Q, *Ws = sm + OFF_W, *KTs = sm + OFF_KT, *TBs = sm + OFF_TB, *Ps = sm + OFF_P;
+    unsigned char *VTs = sm + OFF_VT, *UPs = sm + OFF_UP, *UTs = sm + OFF_UT, *S0s = sm + OFF_S0;
+    float* Gs = reinterpret_cast<float*>(sm + OFF_G);  // e^g [64] | e^(gC-g) [64]
+    float* ssq = reinterpret_cast<float*>(sm + OFF_SMALL);  // [2][C]
+    float* ored = ssq + 2 * C;                               // [2][C]
+    float* nwsl = ored + 2 * C;                              // norm_w of this slice
     uint64_t* mbar = reinterpret_cast<uint64_t*>(nwsl + DV);  // MMA rounds
-    uint64_t* barQ = mbar + 1;   // Q^ tile of the chunk
-    uint64_t* barK = mbar + 2;   // K^ tile
-    uint64_t* barKV = mbar + 3;  // K^T and V^T tiles
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 4);
+    uint64_t* barA = mbar + 1;  // Q^, W, T diag(b), V^T of a chunk
+    uint64_t* barB = mbar + 2;  // K^T, P, gates of a chunk
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 3);
 
     if (warp == 0) tc::alloc(tslot, TMEM_COLS);
     if (tid == 0) {
         mbar_init(mbar, 1);
-        mbar_init(barQ, 1);
-        mbar_init(barK, 1);
-        mbar_init(barKV, 1);
+        mbar_init(barA, 1);
+        mbar_init(barB, 1);
         fence_mbar_init();
     }
     tc::fence_before();
@@ -903,7 +1187,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         }
     }
     const int dS = 32 * q4 + lane;  // the d_k index this thread owns in S^T
-    if (tid < DV) nwsl[tid] = (g.flags & kFlagNoOutNorm) ? 1.f : L::ld(A.p.norm_w, s_idx * DV + tid);
+    if (tid < DV) nwsl[tid] = (g.flags & kFlagNoOutNorm) ? 1.f : Act<__nv_bfloat16>::ld(A.p.norm_w, s_idx * DV + tid);
     {
         float v[16];
 #pragma unroll
@@ -920,8 +1204,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         fence_proxy_async_smem();
         __syncthreads();
     };
-    auto mma_round_end = [&]() {
-        if (tid == 0) tc::commit(mbar);
+    auto wait_mma = [&]() {
         bool w = true;
         if (ok && warp == 0) {  // one warp polls, the others sleep in bar.sync
             w = mbar_wait(mbar, phase);
@@ -931,29 +1214,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         ok = __syncthreads_and(ok && w);
         tc::fence_after();
     };
-
-    const int64_t T = end - start;
-    const int n_chunks = (int)((T + C - 1) / C);
-    const bool outnorm = !(g.flags & kFlagNoOutNorm);
-    const int trow = 16 * q4 + (lane & 15);  // the chunk row this thread reads from M=64 accumulators
-    const bool rowok = lane < 16;
-    // operand tiles come ready-made from the prologue: one bulk copy each,
-    // issued for chunk c+1 as soon as chunk c's last use of the buffer is done
-    auto cslot = [&](int c) -> size_t { return (size_t)(start / C + seq + c); };
-    auto issue_q = [&](int c) {
-        mbar_arrive_expect_tx(barQ, 32768);
-        bulk_g2s(Qs, A.tqk + (cslot(c) * Hk + h) * kTileQK, 32768, barQ);
-    };
-    auto issue_k = [&](int c) {
-        mbar_arrive_expect_tx(barK, 32768);
-        bulk_g2s(Ks, A.tqk + (cslot(c) * Hk + h) * kTileQK + 32768, 32768, barK);
-    };
-    auto issue_kv = [&](int c) {
-        mbar_arrive_expect_tx(barKV, 32768 + 8192);
-        bulk_g2s(KTs, A.tqk + (cslot(c) * Hk + h) * kTileQK + 65536, 32768, barKV);
-        bulk_g2s(VTs, A.tv + ((cslot(c) * Hv + j) * 4 + s_idx) * 8192, 8192, barKV);
-    };
-    auto wait_bar = [&](uint64_t* b, uint32_t par) {  // one warp polls, then everyone
+    auto wait_bar = [&](uint64_t* b, uint32_t par) {
         bool w = true;
         if (ok && warp == 0) {
             w = mbar_wait(b, par);
@@ -961,221 +1222,113 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         }
         ok = __syncthreads_and(ok && w);
     };
+
+    const int64_t T = end - start;
+    const int n_chunks = (int)((T + C - 1) / C);
+    const bool outnorm = !(g.flags & kFlagNoOutNorm);
+    const int trow = 16 * q4 + (lane & 15);  // the chunk row this thread reads from M=64 accumulators
+    const bool rowok = lane < 16;
+    auto rows_of = [&](int c) -> int {
+        const int64_t left = end - (start + (int64_t)c * C);
+        return (int)(left < C ? left : C);
+    };
+    // operand tiles come ready-made (prologue and prep kernel): bulk copies
+    // issued for chunk c+1 as soon as chunk c's last use of the buffer is done
+    auto cslot = [&](int c) -> size_t { return (size_t)(start / C + seq + c); };
+    auto issue_a = [&](int c) {
+        const unsigned char* tq = A.tqk + (cslot(c) * Hk + h) * kTileQK;
+        const unsigned char* rc = A.trec + (cslot(c) * Hv + j) * kTileRec;
+        mbar_arrive_expect_tx(barA, 32768 + 32768 + 16384 + 8192);
+        bulk_g2s(Qs, tq, 32768, barA);
+        bulk_g2s(Ws, rc + kRecW, 32768, barA);
+        bulk_g2s(TBs, rc + kRecTB, 16384, barA);
+        bulk_g2s(VTs, A.tv + ((cslot(c) * Hv + j) * 4 + s_idx) * 8192, 8192, barA);
+    };
+    auto issue_b = [&](int c) {
+        const unsigned char* tq = A.tqk + (cslot(c) * Hk + h) * kTileQK;
+        const unsigned char* rc = A.trec + (cslot(c) * Hv + j) * kTileRec;
+        mbar_arrive_expect_tx(barB, 32768 + 16384 + 2 * C * 4);
+        bulk_g2s(KTs, tq + 65536, 32768, barB);
+        bulk_g2s(Ps, rc + kRecP, 16384, barB);
+        bulk_g2s(Gs, rc + kRecG, 2 * C * 4, barB);
+    };
+    // Ra of chunk c: U = T diag(b) V - W S^T, O1 = Q S^T (S0s holds the state
+    // entering chunk c); committed, not waited for
+    auto issue_ra = [&](int c) {
+        wait_bar(barA, (uint32_t)(c & 1));
+        const int nc = rows_of(c);
+        if (nc < C) {  // tokens past the sequence end were never written: zero Q^ rows, V^T columns
+            for (int f = tid; f < (C - nc) * 32; f += THREADS) {
+                const int r = nc + (f >> 5), c4 = (f & 31) * 4;
+                *reinterpret_cast<float4*>(Qs + tc::sw_off(C, r, c4)) = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            for (int f = tid; f < DV * (C - nc); f += THREADS) {
+                const int row = f / (C - nc), t = nc + f % (C - nc);
+                *reinterpret_cast<float*>(VTs + tc::sw_off(DV, row, t)) = 0.f;
+            }
+        }
+        mma_round_begin();
+        if (tid == 0) {
+            if (ok) {
+                tc::fence_after();
+                tc::mma_tf32(tm + cU, TBs, C, VTs, DV, C, tc::idesc_tf32(C, DV), false);
+                tc::mma_tf32(tm + cU, Ws, C, S0s, DV, D, tc::idesc_tf32(C, DV, true), true);
+                tc::mma_tf32(tm + cO1, Qs, C, S0s, DV, D, tc::idesc_tf32(C, DV), false);
+            }
+            tc::commit(mbar);
+        }
+    };
+
     if (tid == 0 && n_chunks > 0) {
-        issue_q(0);
-        issue_k(0);
-        issue_kv(0);
+        issue_a(0);
+        issue_b(0);
     }
-    float g_next = 0.f, b_next = 0.f;  // gates of the next chunk (threads < 64)
-    if (tid < C && n_chunks > 0) {
-        const float* gb = A.tgb + (cslot(0) * Hv + j) * 128;
-        g_next = gb[tid];
-        b_next = gb[C + tid];
-    }
+    if (n_chunks > 0) issue_ra(0);
     for (int ci = 0; ci < n_chunks; ++ci) {
         const int64_t t0 = start + (int64_t)ci * C;
-        const int n = (int)((end - t0) < C ? (end - t0) : C);
-        __syncthreads();
-        // ---- (1) the chunk's tiles (prefetched) and gates; zero the tail rows ------
-        if (tid < C) {
-            gam[tid] = tid < n ? g_next : 0.f;
-            bet[tid] = tid < n ? b_next : 0.f;
-            if (ci + 1 < n_chunks) {  // gates of the next chunk, in flight during this one
-                const float* gb = A.tgb + (cslot(ci + 1) * Hv + j) * 128;
-                g_next = gb[tid];
-                b_next = gb[C + tid];
-            }
-        }
+        const int n = rows_of(ci);
         const uint32_t par = (uint32_t)(ci & 1);
-        wait_bar(barQ, par);
-        wait_bar(barK, par);
-        if (n < C) {  // rows of the last chunk past the sequence end were never written: zero them
-            for (int f = tid; f < (C - n) * 32; f += THREADS) {
-                const int r = n + (f >> 5), c4 = (f & 31) * 4;
-                *reinterpret_cast<float4*>(Qs + tc::sw_off(C, r, c4)) = make_float4(0.f, 0.f, 0.f, 0.f);
-                *reinterpret_cast<float4*>(Ks + tc::sw_off(C, r, c4)) = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        __syncthreads();
-        // ---- (2) gamma = cumsum(g) ---------------------------------------------------
-        if (warp == 0) {
-            float run = 0.f;
-            for (int base = 0; base < C; base += 32) {
-                float v = gam[base + lane];
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float o = __shfl_up_sync(0xffffffffu, v, off);
-                    if (lane >= off) v += o;
-                }
-                v += run;
-                gam[base + lane] = v;
-                eg[base + lane] = expf(v);
-                run = __shfl_sync(0xffffffffu, v, 31);
-            }
-            __syncwarp();
-            for (int t = lane; t < C; t += 32) erev[t] = expf(gam[C - 1] - gam[t]);
-        }
-        // ---- R1: KK^T, QK^T ----------------------------------------------------------
-        mma_round_begin();
-        if (tid == 0 && ok) {
-            tc::fence_after();
-            tc::mma_tf32(tm + cKK, Ks, C, Ks, C, D, tc::idesc_tf32(C, C), false);
-            tc::mma_tf32(tm + cQK, Qs, C, Ks, C, D, tc::idesc_tf32(C, C), false);
-        }
-        mma_round_end();
-        // ---- decay masks: A (strictly lower, beta_t), P (lower incl.) ---------------
-        for (int cb = 0; cb < 2; ++cb) {
-            const int i0 = hf * 32 + cb * 16;
-            float kk[16], qk[16];
-            tc::ld16x2(tc::taddr(tm, 32 * q4, cKK + i0), kk, tc::taddr(tm, 32 * q4, cQK + i0), qk);
-            if (rowok) {
-                const int t = trow;
-#pragma unroll
-                for (int c = 0; c < 16; c += 4) {
-                    float a4[4], p4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = i0 + c + e;
-                        const float dec = i <= t ? __expf(gam[t] - gam[i]) : 0.f;  // exponent <= 0 only
-                        a4[e] = i < t ? bet[t] * dec * kk[c + e] : 0.f;
-                        p4[e] = dec * qk[c + e];
-                    }
-                    *reinterpret_cast<float4*>(Am + t * LDA + i0 + c) = make_float4(a4[0], a4[1], a4[2], a4[3]);
-                    tc::st_row4(Ps, C, t, i0 + c, p4[0], p4[1], p4[2], p4[3]);
-                }
-            }
-        }
-        __syncthreads();
-        // ---- T = (I + A)^-1: 16x16 diagonal blocks, then block merges ------------------
-        // diagonal blocks: a lane owns column j of a block (x[i] = X_ij) and
-        // column j of A; right-looking substitution: once x_k is final, every
-        // later row takes -A_ik x_k (A_ik from lane k by shuffle), so the
-        // dependent chain is 16 FMAs long
-        if (warp < 2) {
-            const int b0 = (warp * 2 + (lane >> 4)) * 16, jc = lane & 15, lb = lane & 16;
-            float acol[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acol[i] = Am[(b0 + i) * LDA + b0 + jc];
-            float x[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) x[i] = (i == jc) ? 1.f : 0.f;
-#pragma unroll
-            for (int k = 0; k < 15; ++k) {
-#pragma unroll
-                for (int i = k + 1; i < 16; ++i) x[i] = fmaf(-__shfl_sync(0xffffffffu, acol[i], lb + k), x[k], x[i]);
-            }
-#pragma unroll
-            for (int i = 0; i < 16; ++i) Tm[(b0 + i) * LDA + b0 + jc] = x[i];
-        }
-        for (int f = tid; f < C * C; f += THREADS) {
-            const int t = f >> 6, c = f & 63;
-            if ((c >> 4) > (t >> 4)) Tm[t * LDA + c] = 0.f;
-        }
-        __syncthreads();
-        // off-diagonal blocks by distance: X_ab = -X_aa sum_{c=b}^{a-1} A_ac X_cb;
-        // the 16x16 block products run on warp-level mma.sync (3xTF32), one
-        // 16x8 half block per warp
-        for (int dd = 1; dd < 4; ++dd) {
-            const int ntile = (4 - dd) * 2;
-            for (int tl = warp; tl < ntile; tl += THREADS / 32) {  // Y = A_a[b..a) X_[b..a)b
-                const int bb = tl >> 1, nt = tl & 1;
-                const int a0 = (bb + dd) * 16, c0b = bb * 16;
-                float cc[4];
-                warp_tile16x8_precise(Am + a0 * LDA + c0b, LDA, Tm + c0b * LDA + c0b + 8 * nt, LDA, a0 - c0b, lane,
-                                      cc);
-                const int gq = lane >> 2, t4 = lane & 3;
-                float* y0 = Tm + a0 * LDA + c0b + 8 * nt;
-                y0[gq * LDA + 2 * t4] = cc[0];
-                y0[gq * LDA + 2 * t4 + 1] = cc[1];
-                y0[(gq + 8) * LDA + 2 * t4] = cc[2];
-                y0[(gq + 8) * LDA + 2 * t4 + 1] = cc[3];
-            }
-            __syncthreads();
-            for (int tl = warp; tl < ntile; tl += THREADS / 32) {  // X_ab = -X_aa Y
-                const int bb = tl >> 1, nt = tl & 1;
-                const int a0 = (bb + dd) * 16, c0b = bb * 16;
-                float cc[4];
-                warp_tile16x8_precise(Tm + a0 * LDA + a0, LDA, Tm + a0 * LDA + c0b + 8 * nt, LDA, 16, lane, cc);
-                const int gq = lane >> 2, t4 = lane & 3;
-                float* x0 = Tm + a0 * LDA + c0b + 8 * nt;
-                x0[gq * LDA + 2 * t4] = -cc[0];
-                x0[gq * LDA + 2 * t4 + 1] = -cc[1];
-                x0[(gq + 8) * LDA + 2 * t4] = -cc[2];
-                x0[(gq + 8) * LDA + 2 * t4 + 1] = -cc[3];
-            }
-            __syncthreads();
-        }
-        // ---- T diag(beta) and T diag(beta e^gamma) as operand tiles ----------------------
-        for (int f = tid; f < C * 16; f += THREADS) {
-            const int t = f >> 4, i = (f & 15) * 4;
-            const float4 tv = *reinterpret_cast<const float4*>(Tm + t * LDA + i);
-            tc::st_row4(TBs, C, t, i, tv.x * bet[i], tv.y * bet[i + 1], tv.z * bet[i + 2], tv.w * bet[i + 3]);
-            tc::st_row4(TWs, C, t, i, tv.x * bet[i] * eg[i], tv.y * bet[i + 1] * eg[i + 1],
-                        tv.z * bet[i + 2] * eg[i + 2], tv.w * bet[i + 3] * eg[i + 3]);
-        }
-        wait_bar(barKV, par);
-        if (n < C) {  // tail columns (t >= n) of K^T and V^T
-            for (int f = tid; f < (D + DV) * (C - n); f += THREADS) {
+        wait_mma();                                          // Ra of this chunk
+        if (tid == 0 && ci + 1 < n_chunks) issue_a(ci + 1);  // Q^, W, T diag(b), V^T are free
+        wait_bar(barB, par);
+        if (n < C) {  // tail columns (t >= n) of K^T
+            for (int f = tid; f < D * (C - n); f += THREADS) {
                 const int row = f / (C - n), t = n + f % (C - n);
-                if (row < D) *reinterpret_cast<float*>(KTs + tc::sw_off(D, row, t)) = 0.f;
-                else *reinterpret_cast<float*>(VTs + tc::sw_off(DV, row - D, t)) = 0.f;
+                *reinterpret_cast<float*>(KTs + tc::sw_off(D, row, t)) = 0.f;
             }
         }
-        // ---- R2: U~, W, O1 ------------------------------------------------------------------
-        mma_round_begin();
-        if (tid == 0 && ok) {
-            tc::fence_after();
-            tc::mma_tf32(tm + cU, TBs, C, VTs, DV, C, tc::idesc_tf32(C, DV), false);
-            tc::mma_tf32(tm + cW, TWs, C, KTs, D, C, tc::idesc_tf32(C, D), false);
-            tc::mma_tf32(tm + cO1, Qs, C, S0s, DV, D, tc::idesc_tf32(C, DV), false);
-        }
-        mma_round_end();
-        if (tid == 0 && ci + 1 < n_chunks) issue_q(ci + 1);  // Q^ of this chunk is no longer read
-        // W -> operand tile over K^ (no longer needed)
-        for (int cb = 0; cb < 4; ++cb) {
-            const int d0 = hf * 64 + cb * 16;
-            float w16[16];
-            tc::ld16(tc::taddr(tm, 32 * q4, cW + d0), w16);
-            if (rowok) {
-#pragma unroll
-                for (int c = 0; c < 16; c += 4)
-                    tc::st_row4(Ks, C, trow, d0 + c, w16[c], w16[c + 1], w16[c + 2], w16[c + 3]);
-            }
-        }
-        // ---- R3: U = U~ - W S^T -------------------------------------------------------------
-        mma_round_begin();
-        if (tid == 0 && ok) {
-            tc::fence_after();
-            tc::mma_tf32(tm + cU, Ks, C, S0s, DV, D, tc::idesc_tf32(C, DV, true), true);
-        }
-        mma_round_end();
-        if (tid == 0 && ci + 1 < n_chunks) issue_k(ci + 1);  // W (over K^) has been read
+        // ---- U -> U^T and (diag(e^(gC - g)) U)^T tiles; S^T *= e^gC in TMEM -----------------
+        float egt = 0.f;  // e^gamma of this thread's output row
         {
-            // U -> U^T and (diag(e^(gC - g)) U)^T tiles; S^T *= e^gC in TMEM
             float u16[16];
             tc::ld16(tc::taddr(tm, 32 * q4, cU + hf * 16), u16);
             if (rowok) {
+                const float er = Gs[C + trow];
+                egt = Gs[trow];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     tc::st_elem(UTs, DV, hf * 16 + c, trow, u16[c]);
-                    tc::st_elem(VTs, DV, hf * 16 + c, trow, u16[c] * erev[trow]);
+                    tc::st_elem(UPs, DV, hf * 16 + c, trow, u16[c] * er);
                 }
             }
             float s16[16];
             tc::ld16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
-            const float egC = eg[C - 1];
+            const float egC = Gs[C - 1];
 #pragma unroll
             for (int c = 0; c < 16; ++c) s16[c] *= egC;
             tc::st16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
         }
-        // ---- R4: O2 = P U, S^T += K^T U' ---------------------------------------------------
+        // ---- Rb: O2 = P U, S^T += K^T U' ---------------------------------------------------
         mma_round_begin();
-        if (tid == 0 && ok) {
-            tc::fence_after();
-            tc::mma_tf32(tm + cO2, Ps, C, UTs, DV, C, tc::idesc_tf32(C, DV), false);
-            tc::mma_tf32(tm + cS, KTs, D, VTs, DV, C, tc::idesc_tf32(D, DV), true);
+        if (tid == 0) {
+            if (ok) {
+                tc::fence_after();
+                tc::mma_tf32(tm + cO2, Ps, C, UTs, DV, C, tc::idesc_tf32(C, DV), false);
+                tc::mma_tf32(tm + cS, KTs, D, UPs, DV, C, tc::idesc_tf32(D, DV), true);
+            }
+            tc::commit(mbar);
         }
-        float zpre[16];  // z of this thread's output row (loaded while R4 runs)
+        float zpre[16];  // z of this thread's output row (loaded while Rb runs)
         if (outnorm && rowok && trow < n) {
             const uint4* zp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(J.z) +
                                                              (size_t)(t0 + trow) * Hv * D + (size_t)j * D +
@@ -1189,8 +1342,8 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
                 zpre[2 * c] = a.x; zpre[2 * c + 1] = a.y; zpre[8 + 2 * c] = b.x; zpre[8 + 2 * c + 1] = b.y;
             }
         }
-        mma_round_end();
-        if (tid == 0 && ci + 1 < n_chunks) issue_kv(ci + 1);  // K^T and (the U' over) V^T are read
+        wait_mma();
+        if (tid == 0 && ci + 1 < n_chunks) issue_b(ci + 1);  // K^T, P, gates are read
         // ---- O = diag(e^g) O1 + O2; S^T -> S operand tile for the next chunk ----------------
         float o16[16];
         {
@@ -1199,7 +1352,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
             float part = 0.f;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-                o16[c] = fmaf(rowok ? eg[trow] : 0.f, a16[c], o16[c]);
+                o16[c] = fmaf(egt, a16[c], o16[c]);
                 part = fmaf(o16[c], o16[c], part);
             }
             if (rowok) ored[hf * C + trow] = part;
@@ -1211,7 +1364,9 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         __syncthreads();
         float* ssq_cur = ssq + (ci & 1) * C;
         if (tid < C) ssq_cur[tid] = ored[tid] + ored[C + tid];
-        cluster.sync();
+        cluster_arrive_release();
+        if (ci + 1 < n_chunks) issue_ra(ci + 1);  // runs while this chunk's output is normalised
+        cluster_wait_acquire();
         if (rowok && trow < n) {
             const size_t tok = (size_t)(t0 + trow);
             float rstd = 1.f;
@@ -1249,12 +1404,22 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
     cluster.sync();  // peers may still read this CTA's partial sums
 }
 
-cudaError_t launch_chunk_tc(const PrefillArgs& A, cudaStream_t st) {
+cudaError_t launch_chunk_tc(const PrefillArgs& A, int64_t n_slots, cudaStream_t st) {
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, tcp::SMEM_ALLOC);
+        cudaError_t e = cudaFuncSetAttribute(k_chunk_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             tcp::PR_SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, tcp::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         attr_set = true;
+    }
+    if (n_slots > 0) {
+        const int64_t ny = n_slots < 32768 ? n_slots : 32768;
+        const dim3 grid((unsigned)A.g.Hv, (unsigned)ny, (unsigned)((n_slots + ny - 1) / ny));
+        k_chunk_prep<<<grid, tcp::THREADS, tcp::PR_SMEM_ALLOC, st>>>(A);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tcp::NS, A.g.Hv, A.J.n_seq);
@@ -1301,6 +1466,8 @@ cudaError_t launch_prefill_t(const Geom& g, const LayerParams& p, const PrefillJ
         A.tqk = reinterpret_cast<unsigned char*>(ws + tl.qk);
         A.tv = reinterpret_cast<unsigned char*>(ws + tl.v);
         A.tgb = reinterpret_cast<float*>(ws + tl.gb);
+        A.trec = reinterpret_cast<unsigned char*>(ws + tl.rec);
+        A.ncs = tl.ncs;
     }
     if (J.n_tokens > 0) {
         constexpr int VEC = 16 / (int)sizeof(TA);
@@ -1317,7 +1484,7 @@ cudaError_t launch_prefill_t(const Geom& g, const LayerParams& p, const PrefillJ
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (A.tiles) return launch_chunk_tc(A, st);
+    if (A.tiles) return launch_chunk_tc(A, A.ncs, st);
     const int DV = D / A.NS;
     const ChunkSmem lay = chunk_smem(g.chunk, D, DV);
     const size_t smem = (size_t)lay.total * sizeof(float);

@@ -72,6 +72,9 @@ __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// every committed bulk store of this thread has completed
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // make this thread's generic-proxy writes to shared memory visible to the
 // async proxy (bulk stores read shared memory through it)
 __device__ __forceinline__ void fence_proxy_async_smem() {
