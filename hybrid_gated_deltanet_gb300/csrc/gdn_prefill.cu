@@ -46,16 +46,6 @@ namespace cg = cooperative_groups;
 namespace gdn {
 namespace {
 
-// 16-byte global -> shared copy; src_bytes = 0 fills the 16 bytes with zeros
-__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src, int src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"((uint32_t)__cvta_generic_to_shared(dst_smem)),
-                 "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit_wait_all() {
-    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-}
-
 // ---------------------------------------------------------------------------
 // workspace layout (fp32, each section 256-byte aligned)
 // ---------------------------------------------------------------------------
@@ -84,13 +74,14 @@ WsLayout ws_layout(const Geom& g, int64_t N) {
 // state rows): ready-to-copy operand tiles, TF32-rounded and 128B-swizzled,
 // one set per chunk slot.  Sequence s's chunk c sits in slot
 // floor(start_s / 64) + s + c, which never collides with another sequence's.
-//   per (slot, k-head): Q^ [64][128] | K^ [64][128] | K^T [128][64]   (3 x 32 KB)
-//   per (slot, v-head, slice): V^T [32][64]                           (8 KB)
+//   per (slot, k-head): [K^; Q^] [128][128] | K^T [128][64]           (96 KB)
+//   per (slot, v-head): V^T [128][64]                                  (32 KB)
 //   per (slot, v-head): g [64], beta [64]                              (512 B)
-//   per (slot, v-head): chain record written by the prep kernel       (65 KB)
-//     W [64][128] | T diag(beta) [64][64] | P [64][64] | e^gamma [64], e^(gamma_C - gamma) [64]
-constexpr size_t kTileQK = 3 * 32768, kTileV = 4 * 8192, kTileGB = 2 * 64 * 4;
-constexpr size_t kRecW = 0, kRecTB = 32768, kRecP = 49152, kRecG = 65536, kTileRec = 66560;
+//   per (slot, v-head): record written by the prep kernels             (161 KB)
+//     [-W; Q'] [128][128] | per slice s of 32 state rows: U~_s, X_s fp32 [64][32] |
+//     T diag(beta) [64][64] | P [64][64] | e^gamma [64], e^(gamma_C - gamma) [64]
+constexpr size_t kTileQK = 3 * 32768, kTileV = 32768, kTileGB = 2 * 64 * 4;
+constexpr size_t kRecA = 0, kRecUX = 65536, kRecTB = 131072, kRecP = 147456, kRecG = 163840, kTileRec = 164864;
 
 struct TileWs {
     size_t qk, v, gb, rec, total;
@@ -132,13 +123,6 @@ struct PrefillArgs {
     int NS;
 };
 
-// chunk slot and row of token n of sequence s (start = its first token)
-__device__ __forceinline__ void chunk_slot(int64_t n, int64_t start, int s, int64_t& cs, int& r) {
-    const int64_t rel = n - start;
-    cs = start / 64 + s + rel / 64;
-    r = (int)(rel % 64);
-}
-
 // sequence bounds, clamped into [0, N]
 __device__ __forceinline__ void seq_bounds(const PrefillJob& J, int s, int64_t& start, int64_t& end) {
     if (!J.cu_seqlens) {
@@ -163,6 +147,32 @@ __device__ __forceinline__ int find_seq(const PrefillJob& J, int64_t n) {
         else hi = mid - 1;
     }
     return lo;
+}
+
+// sequence owning chunk slot cs: the largest s with floor(start_s / 64) + s <= cs
+__device__ __forceinline__ int slot_seq(const PrefillJob& J, int64_t cs) {
+    if (!J.cu_seqlens) return 0;
+    int lo = 0, hi = J.n_seq - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        int64_t st, en;
+        seq_bounds(J, mid, st, en);
+        if (st / 64 + mid <= cs) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// chunk of slot cs: its first token t0 and row count n; false for a slot
+// between two sequences' chunks
+__device__ __forceinline__ bool slot_chunk(const PrefillJob& J, int64_t cs, int64_t& t0, int& n) {
+    const int sq = slot_seq(J, cs);
+    int64_t start, end;
+    seq_bounds(J, sq, start, end);
+    t0 = (cs - (start / 64 + sq)) * 64 + start;
+    if (t0 < start || t0 >= end) return false;
+    n = (int)((end - t0) < 64 ? (end - t0) : 64);
+    return true;
 }
 
 __device__ __forceinline__ const void* seq_conv_in(const PrefillJob& J, const Geom& g, int s, int& slot_ok) {
@@ -236,19 +246,8 @@ __global__ void __launch_bounds__(kProThreads, 2) k_prologue(const __grid_consta
             float gl, be;
             gates(L::ld(J.a, (size_t)n * Hv + j), L::ld(J.b, (size_t)n * Hv + j), direct ? 0.f : A.p.A_log[j],
                   (!direct && A.p.dt_bias) ? A.p.dt_bias[j] : 0.f, direct, gl, be);
-            if (A.tiles) {
-                const int sq = find_seq(J, n);
-                int64_t st_, en_, cs;
-                int r;
-                seq_bounds(J, sq, st_, en_);
-                chunk_slot(n, st_, sq, cs, r);
-                float* gb = A.tgb + ((size_t)cs * Hv + j) * 128;
-                gb[r] = gl;
-                gb[64 + r] = be;
-            } else {
-                A.gl[(size_t)n * Hv + j] = gl;
-                A.beta[(size_t)n * Hv + j] = be;
-            }
+            A.gl[(size_t)n * Hv + j] = gl;
+            A.beta[(size_t)n * Hv + j] = be;
         }
     }
 
@@ -285,31 +284,6 @@ __global__ void __launch_bounds__(kProThreads, 2) k_prologue(const __grid_consta
         }
     }
     const bool is_q = ch0 < Hk * D, is_qk = ch0 < 2 * Hk * D;
-    // tile mode: K^T and V^T tile rows are t-contiguous; 4 consecutive tokens of
-    // the same chunk slot go out as one 16-byte store per channel
-    float tb[VEC][4];
-    int64_t tb_cs = -1;
-    int tb_r0 = 0, tb_n = 0;
-    unsigned char* tb_base = nullptr;
-    int tb_rows = 0, tb_row0 = 0;  // tile rows (128 for K^T, 32 for V^T) and this thread's first row
-    auto tb_flush = [&]() {
-        if (tb_n == 0) return;
-        if (tb_n == 4 && (tb_r0 & 3) == 0) {
-#pragma unroll
-            for (int c = 0; c < VEC; ++c)
-                *reinterpret_cast<float4*>(tb_base + tc::sw_off(tb_rows, tb_row0 + c, tb_r0)) =
-                    make_float4(tb[c][0], tb[c][1], tb[c][2], tb[c][3]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (e < tb_n) {
-#pragma unroll
-                    for (int c = 0; c < VEC; ++c)
-                        *reinterpret_cast<float*>(tb_base + tc::sw_off(tb_rows, tb_row0 + c, tb_r0 + e)) = tb[c][e];
-                }
-        }
-        tb_n = 0;
-    };
     for (int tt = 0; tt < kProTok; ++tt) {
         const int64_t n = t0 + tt;
         if (n >= J.n_tokens) break;  // uniform over the CTA
@@ -357,70 +331,232 @@ __global__ void __launch_bounds__(kProThreads, 2) k_prologue(const __grid_consta
             for (int off = LPH / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
             float scale = is_q ? g.q_scale : 1.f;
             if (!(g.flags & kFlagNoL2)) scale *= rsqrtf(ss + g.l2_eps);
-            if (A.tiles && D == 128) {
-                if (active) {
-                    int64_t cs;
-                    int r;
-                    chunk_slot(n, start, s, cs, r);
-                    const int hq = ch0 / D, d0 = ch0 % D;
-                    const int hh = hq < Hk ? hq : hq - Hk;
-                    unsigned char* tile = A.tqk + ((size_t)cs * Hk + hh) * kTileQK + (hq < Hk ? 0 : 32768);
-#pragma unroll
-                    for (int c = 0; c < VEC; c += 4)
-                        *reinterpret_cast<float4*>(tile + tc::sw_off(64, r, d0 + c)) =
-                            make_float4(tc::to_tf32_rn(u[c] * scale), tc::to_tf32_rn(u[c + 1] * scale),
-                                        tc::to_tf32_rn(u[c + 2] * scale), tc::to_tf32_rn(u[c + 3] * scale));
-                    if (hq >= Hk) {  // K^T tile: element (d, t), buffered over 4 tokens
-                        if (tb_n > 0 && (cs != tb_cs || r != tb_r0 + tb_n || tb_n == 4)) tb_flush();
-                        if (tb_n == 0) {
-                            tb_cs = cs;
-                            tb_r0 = r;
-                            tb_base = A.tqk + ((size_t)cs * Hk + hh) * kTileQK + 65536;
-                            tb_rows = 128;
-                            tb_row0 = d0;
-                        }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (e == tb_n) {
-#pragma unroll
-                                for (int c = 0; c < VEC; ++c) tb[c][e] = tc::to_tf32_rn(u[c] * scale);
-                            }
-                        ++tb_n;
-                    }
-                }
-            } else if (active) {
+            if (active) {
                 float4* dst = reinterpret_cast<float4*>(A.qk + (size_t)n * 2 * Hk * D + ch0);
 #pragma unroll
                 for (int c = 0; c < VEC; c += 4)
                     dst[c / 4] = make_float4(u[c] * scale, u[c + 1] * scale, u[c + 2] * scale, u[c + 3] * scale);
             }
-        } else if (active && A.tiles && D == 128) {
-            int64_t cs;
-            int r;
-            chunk_slot(n, start, s, cs, r);
-            const int c0 = ch0 - 2 * Hk * D, jj = c0 / D, dv0 = c0 % D, sl = dv0 / 32;
-            if (tb_n > 0 && (cs != tb_cs || r != tb_r0 + tb_n || tb_n == 4)) tb_flush();
-            if (tb_n == 0) {
-                tb_cs = cs;
-                tb_r0 = r;
-                tb_base = A.tv + (((size_t)cs * Hv + jj) * 4 + sl) * 8192;
-                tb_rows = 32;
-                tb_row0 = dv0 % 32;
-            }
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (e == tb_n) {
-#pragma unroll
-                    for (int c = 0; c < VEC; ++c) tb[c][e] = tc::to_tf32_rn(u[c]);
-                }
-            ++tb_n;
         } else if (active) {
             float4* dst = reinterpret_cast<float4*>(A.v + (size_t)n * Hv * D + (ch0 - 2 * Hk * D));
 #pragma unroll
             for (int c = 0; c < VEC; c += 4) dst[c / 4] = make_float4(u[c], u[c + 1], u[c + 2], u[c + 3]);
         }
     }
-    if (A.tiles && D == 128) tb_flush();
+}
+
+// ---------------------------------------------------------------------------
+// 1b. tile prologue (tcgen05 path: d = 128, C = 64, bf16)
+// ---------------------------------------------------------------------------
+// One CTA per (chunk slot, unit): unit h < Hk builds k-head h's tiles -- the
+// stacked [K^; Q^] (rows 0..63 k, 64..127 q of the chunk's tokens) and K^T --
+// and unit Hk + j builds v-head j's V^T tile and gates.  A thread owns 8
+// consecutive channels (one 16-byte load per row) of 8 (q/k) or 4 (v)
+// consecutive tokens and loads all rows it needs (3 more for the conv
+// window) before any arithmetic.  Rows are staged in shared memory, the
+// transposed tile is built from them there, and every tile leaves with bulk
+// stores.  Tokens past the sequence end give zero rows and columns, and zero
+// gates, so no consumer has to mask the last chunk.
+constexpr int kPtThreads = 256;
+constexpr int kPtSmemAlloc = 98304 + 1024;
+
+// conv window of one thread: rows tau0-3 .. tau0+NT-1 of its 8 channels
+// (taps before the sequence start from its conv state), packed bf16
+template <int NT>
+__device__ __forceinline__ void load_window(const PrefillJob& J, int Cch, int K, int ch, int64_t tau0, int64_t start,
+                                            int64_t end, const void* cin, uint4 rows[NT + 3]) {
+#pragma unroll
+    for (int r = 0; r < NT + 3; ++r) {
+        const int64_t tau = tau0 - 3 + r;
+        rows[r] = make_uint4(0, 0, 0, 0);
+        if (tau >= start && tau < end) {
+            rows[r] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(J.x) + (size_t)tau * Cch + ch);
+        } else if (tau < start && cin && tau - start >= -(K - 1)) {
+            rows[r] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(cin) +
+                                                      (size_t)((K - 1) + (tau - start)) * Cch + ch);
+        }
+    }
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float f[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 v = __bfloat1622float2(h[i]);
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
+    }
+}
+
+// SiLU with the fast exponential and division (bf16 activations only: the
+// difference to the exact form is far below their rounding)
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
+
+// conv + SiLU of the NT tokens of one thread's window (rows i .. i+3 are the
+// taps of token i), through a sliding window of 4 unpacked rows; emit(i, u)
+// receives token i's 8 channels
+template <int NT, typename Emit>
+__device__ __forceinline__ void conv_tokens(const uint4 rows[NT + 3], const float w[4][8], const float bias[8],
+                                            int K, bool raw, Emit emit) {
+    float win[4][8];
+#pragma unroll
+    for (int r = 1; r < 4; ++r) unpack8(rows[r - 1], win[r]);
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+#pragma unroll
+        for (int r = 0; r < 3; ++r)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) win[r][c] = win[r + 1][c];
+        unpack8(rows[i + 3], win[3]);
+        float u[8];
+        if (raw) {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) u[c] = win[3][c];
+        } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c) u[c] = bias[c];
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                if (r < 4 - K) continue;  // not a tap
+#pragma unroll
+                for (int c = 0; c < 8; ++c) u[c] = fmaf(w[r][c], win[r][c], u[c]);
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c) u[c] = silu_fast(u[c]);
+        }
+        emit(i, u);
+    }
+}
+
+__global__ void __launch_bounds__(kPtThreads, 2) k_prologue_tc(const __grid_constant__ PrefillArgs A) {
+    using L = Act<__nv_bfloat16>;
+    constexpr int D = 128, C = 64;
+    const Geom& g = A.g;
+    const PrefillJob& J = A.J;
+    const int Hk = g.Hk, Hv = g.Hv, K = g.K, Cch = g.C_ch;
+    const int unit = blockIdx.x;
+    const int64_t cs = (int64_t)blockIdx.z * gridDim.y + blockIdx.y;
+    if (cs >= A.ncs) return;
+    const int sq = slot_seq(J, cs);
+    int64_t start, end;
+    seq_bounds(J, sq, start, end);
+    const int64_t t0 = (cs - (start / C + sq)) * C + start;
+    if (t0 < start || t0 >= end) return;  // a slot between two sequences' chunks
+    const int n = (int)((end - t0) < C ? (end - t0) : C);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool raw = g.flags & kFlagRawQKV;
+    int slot_ok;
+    const void* cin = seq_conv_in(J, g, sq, slot_ok);
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
+    const bool qk = unit < Hk;
+    const int cg = qk ? lane : (lane & 15);  // 8-channel group inside the unit's channels
+    int ch;
+    if (qk) ch = (cg < 16 ? unit * D : (Hk + unit) * D) + (cg & 15) * 8;
+    else ch = 2 * Hk * D + (unit - Hk) * D + cg * 8;
+    // w[r][c]: weight of window row r (row tau-3+r) for channel c; tap m of the
+    // K taps multiplies row tau-(K-1)+m, i.e. window row r = 4-K+m
+    float w[4][8], bias[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        bias[c] = (!raw && A.p.conv_b) ? L::ld(A.p.conv_b, ch + c) : 0.f;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int m = r - (4 - K);
+            w[r][c] = (!raw && m >= 0) ? L::ld(A.p.conv_w, (size_t)(ch + c) * K + m) : 0.f;
+        }
+    }
+    if (qk) {
+        // staging: [K^; Q^] [128][128] at 0, K^T [128][64] at 64 KB
+        unsigned char* st = sm;
+        unsigned char* kt = sm + 65536;
+        const int tt0 = warp * 8;
+        uint4 rows[11];
+        load_window<8>(J, Cch, K, ch, t0 + tt0, start, end, cin, rows);
+        const bool is_q = cg < 16;
+        const int d0 = (cg & 15) * 8;
+        conv_tokens<8>(rows, w, bias, K, raw, [&](int i, float u[8]) {
+            const int t = tt0 + i;
+            float ss = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) ss = fmaf(u[c], u[c], ss);
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            float scale = is_q ? g.q_scale : 1.f;
+            if (!(g.flags & kFlagNoL2)) scale *= rsqrtf(ss + g.l2_eps);
+            if (t >= n) scale = 0.f;  // past the sequence end
+            const int r = is_q ? C + t : t;
+#pragma unroll
+            for (int c = 0; c < 8; c += 4)
+                tc::st_row4(st, D, r, d0 + c, u[c] * scale, u[c + 1] * scale, u[c + 2] * scale, u[c + 3] * scale);
+        });
+        __syncthreads();
+        {  // K^T from the K^ rows: thread = (d, half of the tokens)
+            const int d = tid & 127, th = (tid >> 7) * 32;
+#pragma unroll
+            for (int t4 = 0; t4 < 32; t4 += 4) {
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] = *reinterpret_cast<const float*>(st + tc::sw_off(D, th + t4 + e, d));
+                *reinterpret_cast<float4*>(kt + tc::sw_off(D, d, th + t4)) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            unsigned char* dst = A.tqk + ((size_t)cs * Hk + unit) * kTileQK;
+            for (int p = 0; p < 3; ++p) bulk_s2g(dst + p * 32768, sm + p * 32768, 32768);
+            bulk_commit();
+            bulk_wait_read_all();
+        }
+    } else {
+        // staging: V rows [64][128] at 0, V^T [128][64] at 32 KB
+        const int j = unit - Hk;
+        unsigned char* vs = sm;
+        unsigned char* vt = sm + 32768;
+        const int tt0 = (warp * 2 + (lane >> 4)) * 4;
+        uint4 rows[7];
+        load_window<4>(J, Cch, K, ch, t0 + tt0, start, end, cin, rows);
+        const int d0 = cg * 8;
+        conv_tokens<4>(rows, w, bias, K, raw, [&](int i, float u[8]) {
+            const int t = tt0 + i;
+            const float keep = t < n ? 1.f : 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; c += 4)
+                tc::st_row4(vs, C, t, d0 + c, u[c] * keep, u[c + 1] * keep, u[c + 2] * keep, u[c + 3] * keep);
+        });
+        if (tid < C) {  // gates of token t
+            const bool direct = g.flags & kFlagGatesDirect;
+            float gl = 0.f, be = 0.f;
+            if (tid < n) {
+                const size_t tok = (size_t)(t0 + tid);
+                gates(L::ld(J.a, tok * Hv + j), L::ld(J.b, tok * Hv + j), direct ? 0.f : A.p.A_log[j],
+                      (!direct && A.p.dt_bias) ? A.p.dt_bias[j] : 0.f, direct, gl, be);
+            }
+            float* gb = A.tgb + ((size_t)cs * Hv + j) * 128;
+            gb[tid] = gl;
+            gb[C + tid] = be;
+        }
+        __syncthreads();
+        {  // V^T from the V rows: thread = (dv, half of the tokens)
+            const int d = tid & 127, th = (tid >> 7) * 32;
+#pragma unroll
+            for (int t4 = 0; t4 < 32; t4 += 4) {
+                float v[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] = *reinterpret_cast<const float*>(vs + tc::sw_off(C, th + t4 + e, d));
+                *reinterpret_cast<float4*>(vt + tc::sw_off(D, d, th + t4)) = make_float4(v[0], v[1], v[2], v[3]);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_s2g(A.tv + ((size_t)cs * Hv + j) * kTileV, vt, 32768);
+            bulk_commit();
+            bulk_wait_read_all();
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -786,27 +922,35 @@ __global__ void __launch_bounds__(kChunkThreads, 1) k_chunk(const __grid_constan
 }
 
 // ---------------------------------------------------------------------------
-// 3b. tcgen05 path (d = 128, C = 64, bf16): prep kernel + chain kernel
+// 3b. tcgen05 path (d = 128, C = 64, bf16): two prep kernels + chain kernel
 // ---------------------------------------------------------------------------
-// The chunk form splits into work that does not depend on the state and the
-// short sequential chain that does.
+// The chunk form splits into work that does not depend on the state and a
+// short sequential chain that does.  With U~ = T diag(beta) V,
+// W = T diag(beta e^gamma) K and P = (QK^T o decay, lower incl.),
+//   U = U~ - W S^T,  O = diag(e^gamma) Q S^T + P U = Q' S^T + X,
+//   Q' = diag(e^gamma) Q - P W,  X = P U~,
+//   S^T <- e^gamma_C S^T + K^T diag(e^(gamma_C - gamma)) U,
+// so only one product with the state gives both U and O, and the second
+// updates the state.
 //
-// k_chunk_prep, one CTA per (chunk slot, v-head j), all chunks in parallel:
-//   gamma = cumsum(g), KK^T and QK^T (tcgen05), the decay masks
-//   A = strict-lower(beta_t e^(gamma_t - gamma_i) KK^T) and
-//   P = lower-incl(e^(gamma_t - gamma_i) QK^T), T = (I + A)^-1 (16x16 blocks,
-//   fp32), T diag(beta), and W = T diag(beta e^gamma) K (tcgen05); W, T
-//   diag(beta), P as TF32 operand tiles and e^gamma, e^(gamma_C - gamma) go
-//   to the chain record of the chunk.
-// k_chunk_tc, one CTA per (sequence, v-head j, slice of 32 of the 128 state
-// rows), the 4 slices of a v-head a cluster: the fp32 state slice lives in
-// TMEM as S^T (lane = d_k index, 32 columns = this slice's d_v rows) for the
-// whole sequence, and per chunk two rounds of tcgen05.mma
-//   Ra  U = T diag(beta) V - W S^T,  O1 = Q S^T
-//   Rb  O2 = P U,  S^T <- e^gamma_C S^T + K^T (diag(e^(gamma_C - gamma)) U)
-// with y = gated RMSNorm(diag(e^gamma) O1 + O2) of chunk c written while Ra
-// of chunk c+1 runs.  TF32 operands are rounded to nearest; accumulation is
-// fp32 in TMEM.
+// k_chunk_prep (per chunk slot, v-head; all chunks in parallel): gamma =
+//   cumsum(g), KK^T and QK^T (tcgen05), A = strict-lower(beta_t
+//   e^(gamma_t - gamma_i) KK^T), P, T = (I + A)^-1 (16x16 blocks, fp32) and
+//   T diag(beta) -> record.
+// k_chunk_prep2 (same grid): W^T = (K^T diag(e^gamma)) (T diag(beta))^T and
+//   U~^T = V^T (T diag(beta))^T, then (P W)^T = W^T P^T and X^T = U~^T P^T
+//   (tcgen05, M = 128) -> record: the stacked operand [-W; Q'] and, per slice
+//   of 32 state rows, U~ and X in fp32.
+// k_chunk_tc (per sequence, v-head, slice; the 4 slices a cluster): the fp32
+//   state slice lives in TMEM as S^T (lane = d_k index, 32 columns = the
+//   slice's d_v rows); per chunk
+//     Ra  D = [-W; Q'] S^T                    (M = 128, K = 128)
+//         U = U~ + D[0:64],  O = X + D[64:128]
+//     Rb  S^T <- e^gamma_C S^T + K^T (diag(e^(gamma_C - gamma)) U)
+//   and y = gated RMSNorm(O) of chunk c is written while Ra of chunk c+1 runs.
+//   Both products deal their K-steps to four TMEM accumulators (summed by the
+//   epilogues): with N = 32 a single accumulation chain is latency-bound.
+// TF32 operands are rounded to nearest; accumulation is fp32 in TMEM.
 
 // One warp: the 16x8 tile C = A(16 x K) B(K x 8) with A(m,k) = Ap[m*lda + k] and
 // B(k,n) = Bp[k*ldb + n], K a multiple of 8, fp32-accurate through the 3xTF32
@@ -837,47 +981,46 @@ __device__ __forceinline__ void warp_tile16x8_precise(const float* Ap, int lda, 
     }
 }
 
-// sequence owning chunk slot cs: the largest s with floor(start_s / 64) + s <= cs
-__device__ __forceinline__ int slot_seq(const PrefillJob& J, int64_t cs) {
-    if (!J.cu_seqlens) return 0;
-    int lo = 0, hi = J.n_seq - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        int64_t st, en;
-        seq_bounds(J, mid, st, en);
-        if (st / 64 + mid <= cs) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
+// byte offset of (t, v) in a [64][32] fp32 block of U~ or X: 16-byte chunks
+// XOR-swizzled by t % 8, so that a warp reading one row per lane is
+// conflict-free
+__device__ __forceinline__ uint32_t ux_off(int t, int v) {
+    return (uint32_t)(t * 128 + ((((v >> 2) ^ (t & 7))) << 4) + ((v & 3) << 2));
 }
 
 namespace tcp {
 constexpr int C = 64, D = 128, DV = 32, NS = 4, THREADS = 256, LDA = 68;
-// prep kernel shared memory
-constexpr int PR_R0 = 0;                       // Q^, then K^T, then W staging   (32 KB)
-constexpr int PR_R1 = 32768;                   // K^, then P | T diag(b) staging (32 KB)
-constexpr int PR_AM = 65536;                   // fp32 A [64][68], then the T diag(b e^g) tile
+// k_chunk_prep shared memory
+constexpr int PR_R0 = 0;                       // [K^; Q^] tile (64 KB), then P | T diag(b) staging at 32 KB
+constexpr int PR_R1 = 32768;
+constexpr int PR_AM = 65536;                   // fp32 A [64][68]
 constexpr int PR_TM = PR_AM + C * LDA * 4;     // fp32 T [64][68]
 constexpr int PR_SMALL = PR_TM + C * LDA * 4;  // gam, bet, e^g, e^(gC-g)
 constexpr int PR_SMEM = PR_SMALL + 4 * C * 4 + 64;
 constexpr int PR_SMEM_ALLOC = PR_SMEM + 1024;
-constexpr int pKK = 0, pQK = 64, pW = 128, PR_TMEM_COLS = 256;
-// chain kernel shared memory
-constexpr int OFF_Q = 0;                   // Q^  [64][128]
-constexpr int OFF_W = OFF_Q + 32768;       // W   [64][128]
-constexpr int OFF_KT = OFF_W + 32768;      // K^T [128][64]
-constexpr int OFF_TB = OFF_KT + 32768;     // T diag(b) [64][64]
-constexpr int OFF_P = OFF_TB + 16384;      // P   [64][64]
-constexpr int OFF_VT = OFF_P + 16384;      // V^T of this slice [32][64]
-constexpr int OFF_UP = OFF_VT + 8192;      // (diag(e^(gC-g)) U)^T [32][64]
-constexpr int OFF_UT = OFF_UP + 8192;      // U^T [32][64]
-constexpr int OFF_S0 = OFF_UT + 8192;      // S   [32][128] (this slice's rows)
-constexpr int OFF_G = OFF_S0 + 16384;      // e^g [64] | e^(gC-g) [64]
-constexpr int OFF_SMALL = OFF_G + 512;     // ssq [2][64], ored [2][64], norm_w slice [32]
+constexpr int PR_TMEM_COLS = 64;  // [KK^T; QK^T] (M = 128, N = 64)
+// k_chunk_prep2 shared memory
+constexpr int P2_KT = 0;           // K^T tile, then W^T  [128][64]
+constexpr int P2_VT = 32768;       // V^T tile, then U~^T [128][64]
+constexpr int P2_TB = 65536;       // T diag(b) [64][64]
+constexpr int P2_P = 81920;        // P         [64][64]
+constexpr int P2_G = 98304;        // e^g [64]
+constexpr int P2_SMEM = P2_G + C * 4 + 64;
+constexpr int P2_SMEM_ALLOC = P2_SMEM + 1024;
+constexpr int P2_TMEM_COLS = 128;  // two M=128 x N=64 accumulators
+// k_chunk_tc shared memory
+constexpr int OFF_A = 0;               // [-W; Q']   [128][128]
+constexpr int OFF_KT = OFF_A + 65536;  // K^T        [128][64]
+constexpr int OFF_UX = OFF_KT + 32768; // U~ | X of this slice, fp32 [64][32] each
+constexpr int OFF_UP = OFF_UX + 16384; // (diag(e^(gC-g)) U)^T [32][64]
+constexpr int OFF_S0 = OFF_UP + 8192;  // S   [32][128] (this slice's rows)
+constexpr int OFF_G = OFF_S0 + 16384;  // e^g [64] | e^(gC-g) [64]
+constexpr int OFF_SMALL = OFF_G + 512; // ssq [2][64], ored [2][64], norm_w slice [32]
 constexpr int SMALL_FLOATS = 4 * C + DV;
-constexpr int SMEM = OFF_SMALL + SMALL_FLOATS * 4 + 64;  // + 3 mbarriers and the TMEM address
+constexpr int SMEM = OFF_SMALL + SMALL_FLOATS * 4 + 64;  // + 4 mbarriers and the TMEM address
 constexpr int SMEM_ALLOC = SMEM + 1024;                  // room to align the base to 1024 bytes
-constexpr int cU = 0, cO1 = 32, cO2 = 64, cS = 96, TMEM_COLS = 128;
+// Ra: four partial accumulators of D at cD + 32 a; Rb: S^T at cS plus three partials
+constexpr int cD = 0, cS = 128, TMEM_COLS = 256;
 }  // namespace tcp
 
 __global__ void __launch_bounds__(tcp::THREADS, 2) k_chunk_prep(const __grid_constant__ PrefillArgs A) {
@@ -888,21 +1031,16 @@ __global__ void __launch_bounds__(tcp::THREADS, 2) k_chunk_prep(const __grid_con
     const int j = blockIdx.x, h = j / g.G;
     const int64_t cs = (int64_t)blockIdx.z * gridDim.y + blockIdx.y;
     if (cs >= A.ncs) return;
-    const int sq = slot_seq(J, cs);
-    int64_t start, end;
-    seq_bounds(J, sq, start, end);
-    const int64_t t0 = (cs - (start / C + sq)) * C + start;
-    if (t0 < start || t0 >= end) return;  // a slot between two sequences' chunks
-    const int n = (int)((end - t0) < C ? (end - t0) : C);
+    int64_t t0;
+    int n;
+    if (!slot_chunk(J, cs, t0, n)) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int q4 = warp & 3, hf = warp >> 2;
-    const int trow = 16 * q4 + (lane & 15);  // the chunk row this thread reads from M=64 accumulators
-    const bool rowok = lane < 16;
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
     unsigned char *R0 = sm + PR_R0, *R1 = sm + PR_R1;
-    unsigned char *Ps = R1, *TBs = R1 + 16384, *TWs = sm + PR_AM;
+    unsigned char *Ps = R1, *TBs = R1 + 16384;
     float* Am = reinterpret_cast<float*>(sm + PR_AM);
     float* Tm = reinterpret_cast<float*>(sm + PR_TM);
     float* gam = reinterpret_cast<float*>(sm + PR_SMALL);
@@ -911,8 +1049,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 2) k_chunk_prep(const __grid_con
     float* erev = eg + C;  // e^g and e^(gC-g) contiguous: one bulk store
     uint64_t* mbar = reinterpret_cast<uint64_t*>(erev + C);
     uint64_t* barQK = mbar + 1;
-    uint64_t* barKT = mbar + 2;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 3);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 2);
     const unsigned char* tile = A.tqk + ((size_t)cs * Hk + h) * kTileQK;
     unsigned char* rec = A.trec + ((size_t)cs * Hv + j) * kTileRec;
 
@@ -920,47 +1057,21 @@ __global__ void __launch_bounds__(tcp::THREADS, 2) k_chunk_prep(const __grid_con
     if (tid == 0) {
         mbar_init(mbar, 1);
         mbar_init(barQK, 1);
-        mbar_init(barKT, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(barQK, 65536);
         bulk_g2s(R0, tile, 32768, barQK);
         bulk_g2s(R1, tile + 32768, 32768, barQK);
     }
-    if (tid < C) {
+    if (tid < C) {  // (zero past the sequence end)
         const float* gb = A.tgb + ((size_t)cs * Hv + j) * 128;
-        gam[tid] = tid < n ? gb[tid] : 0.f;
-        bet[tid] = tid < n ? gb[C + tid] : 0.f;
+        gam[tid] = gb[tid];
+        bet[tid] = gb[C + tid];
     }
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tm = *tslot;
-    uint32_t phase = 0;
     bool ok = true;
-    auto wait_bar = [&](uint64_t* b, uint32_t par) {  // one warp polls, then everyone
-        bool w = true;
-        if (ok && warp == 0) {
-            w = mbar_wait(b, par);
-            if (!w) w = mbar_wait(b, par);
-        }
-        ok = __syncthreads_and(ok && w);
-    };
-    auto mma_round_begin = [&]() {
-        tc::fence_before();
-        fence_proxy_async_smem();
-        __syncthreads();
-    };
-    auto mma_round_end = [&]() {
-        if (tid == 0) tc::commit(mbar);
-        bool w = true;
-        if (ok && warp == 0) {
-            w = mbar_wait(mbar, phase);
-            if (!w) w = mbar_wait(mbar, phase);
-        }
-        phase ^= 1u;
-        ok = __syncthreads_and(ok && w);
-        tc::fence_after();
-    };
 
     // ---- gamma = cumsum(g), e^gamma, e^(gamma_C - gamma) ----------------------------
     if (warp == 0) {
@@ -980,46 +1091,53 @@ __global__ void __launch_bounds__(tcp::THREADS, 2) k_chunk_prep(const __grid_con
         __syncwarp();
         for (int t = lane; t < C; t += 32) erev[t] = expf(gam[C - 1] - gam[t]);
     }
-    wait_bar(barQK, 0);
-    if (n < C) {  // rows past the sequence end were never written: zero them
-        for (int f = tid; f < (C - n) * 32; f += THREADS) {
-            const int r = n + (f >> 5), c4 = (f & 31) * 4;
-            *reinterpret_cast<float4*>(R0 + tc::sw_off(C, r, c4)) = make_float4(0.f, 0.f, 0.f, 0.f);
-            *reinterpret_cast<float4*>(R1 + tc::sw_off(C, r, c4)) = make_float4(0.f, 0.f, 0.f, 0.f);
+    {
+        bool w = true;
+        if (warp == 0) {
+            w = mbar_wait(barQK, 0);
+            if (!w) w = mbar_wait(barQK, 0);
         }
+        ok = __syncthreads_and(w);
     }
-    // ---- KK^T, QK^T ----------------------------------------------------------------------
-    mma_round_begin();
-    if (tid == 0 && ok) {
+    // ---- [KK^T; QK^T] = [K^; Q^] K^T: one M = 128 product (B = the K^ rows of
+    // the stacked tile, whose atoms are 128 rows apart) --------------------------------
+    tc::fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        if (ok) {
+            tc::fence_after();
+            tc::mma_tf32(tm, R0, 2 * C, R0, 2 * C, D, tc::idesc_tf32(2 * C, C), false);
+        }
+        tc::commit(mbar);
+    }
+    {
+        bool w = true;
+        if (ok && warp == 0) {
+            w = mbar_wait(mbar, 0);
+            if (!w) w = mbar_wait(mbar, 0);
+        }
+        ok = __syncthreads_and(ok && w);
         tc::fence_after();
-        tc::mma_tf32(tm + pKK, R1, C, R1, C, D, tc::idesc_tf32(C, C), false);
-        tc::mma_tf32(tm + pQK, R0, C, R1, C, D, tc::idesc_tf32(C, C), false);
     }
-    mma_round_end();
-    if (tid == 0) {  // Q^ is no longer read: K^T into its place
-        mbar_arrive_expect_tx(barKT, 32768);
-        bulk_g2s(R0, tile + 65536, 32768, barKT);
-    }
-    // ---- decay masks: A (strictly lower, beta_t), P (lower incl.) -----------------------
-    for (int cb = 0; cb < 2; ++cb) {
-        const int i0 = hf * 32 + cb * 16;
-        float kk[16], qk[16];
-        tc::ld16x2(tc::taddr(tm, 32 * q4, pKK + i0), kk, tc::taddr(tm, 32 * q4, pQK + i0), qk);
-        if (rowok) {
-            const int t = trow;
+    // ---- decay masks: A (strictly lower, beta_t) from the KK^T rows (lanes 0..63),
+    // P (lower incl.) from the QK^T rows (lanes 64..127), over the stacked tile -----------
+    {
+        const bool arow = q4 < 2;
+        const int t = 32 * (q4 & 1) + lane;
+        const float gt = gam[t], bt = bet[t];
+        float v[32];
+        tc::ld16x2(tc::taddr(tm, 32 * q4, hf * 32), v, tc::taddr(tm, 32 * q4, hf * 32 + 16), v + 16);
 #pragma unroll
-            for (int c = 0; c < 16; c += 4) {
-                float a4[4], p4[4];
+        for (int c = 0; c < 32; c += 4) {
+            float o4[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int i = i0 + c + e;
-                    const float dec = i <= t ? __expf(gam[t] - gam[i]) : 0.f;  // exponent <= 0 only
-                    a4[e] = i < t ? bet[t] * dec * kk[c + e] : 0.f;
-                    p4[e] = dec * qk[c + e];
-                }
-                *reinterpret_cast<float4*>(Am + t * LDA + i0 + c) = make_float4(a4[0], a4[1], a4[2], a4[3]);
-                tc::st_row4(Ps, C, t, i0 + c, p4[0], p4[1], p4[2], p4[3]);
+            for (int e = 0; e < 4; ++e) {
+                const int i = hf * 32 + c + e;
+                const float dec = i <= t ? __expf(gt - gam[i]) : 0.f;  // exponent <= 0 only
+                o4[e] = arow ? (i < t ? bt * dec * v[c + e] : 0.f) : dec * v[c + e];
             }
+            if (arow) *reinterpret_cast<float4*>(Am + t * LDA + hf * 32 + c) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+            else tc::st_row4(Ps, C, t, hf * 32 + c, o4[0], o4[1], o4[2], o4[3]);
         }
     }
     fence_proxy_async_smem();
@@ -1087,52 +1205,161 @@ __global__ void __launch_bounds__(tcp::THREADS, 2) k_chunk_prep(const __grid_con
         }
         __syncthreads();
     }
-    // ---- T diag(beta) (to the record) and T diag(beta e^gamma) (over A) -------------------
+    // ---- T diag(beta) -> record -----------------------------------------------------------
     for (int f = tid; f < C * 16; f += THREADS) {
         const int t = f >> 4, i = (f & 15) * 4;
         const float4 tv = *reinterpret_cast<const float4*>(Tm + t * LDA + i);
         tc::st_row4(TBs, C, t, i, tv.x * bet[i], tv.y * bet[i + 1], tv.z * bet[i + 2], tv.w * bet[i + 3]);
-        tc::st_row4(TWs, C, t, i, tv.x * bet[i] * eg[i], tv.y * bet[i + 1] * eg[i + 1],
-                    tv.z * bet[i + 2] * eg[i + 2], tv.w * bet[i + 3] * eg[i + 3]);
-    }
-    fence_proxy_async_smem();
-    wait_bar(barKT, 0);
-    if (tid == 0) {
-        bulk_s2g(rec + kRecTB, TBs, 16384);
-        bulk_commit();
-    }
-    if (n < C) {  // tail columns (t >= n) of K^T
-        for (int f = tid; f < D * (C - n); f += THREADS) {
-            const int row = f / (C - n), t = n + f % (C - n);
-            *reinterpret_cast<float*>(R0 + tc::sw_off(D, row, t)) = 0.f;
-        }
-    }
-    // ---- W = T diag(beta e^gamma) K --------------------------------------------------------
-    mma_round_begin();
-    if (tid == 0 && ok) {
-        tc::fence_after();
-        tc::mma_tf32(tm + pW, TWs, C, R0, D, C, tc::idesc_tf32(C, D), false);
-    }
-    mma_round_end();
-    for (int cb = 0; cb < 4; ++cb) {  // W -> operand tile over K^T (no longer read)
-        const int d0 = hf * 64 + cb * 16;
-        float w16[16];
-        tc::ld16(tc::taddr(tm, 32 * q4, pW + d0), w16);
-        if (rowok) {
-#pragma unroll
-            for (int c = 0; c < 16; c += 4) tc::st_row4(R0, C, trow, d0 + c, w16[c], w16[c + 1], w16[c + 2], w16[c + 3]);
-        }
     }
     fence_proxy_async_smem();
     tc::fence_before();
     __syncthreads();
     if (tid == 0) {
-        bulk_s2g(rec + kRecW, R0, 32768);
+        bulk_s2g(rec + kRecTB, TBs, 16384);
         bulk_commit();
-        bulk_wait_all();  // shared memory stays valid until the stores have completed
+        bulk_wait_read_all();  // shared memory stays valid until the stores have read it
     }
     if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
     if (warp == 0) tc::dealloc(tm, PR_TMEM_COLS);
+}
+
+__global__ void __launch_bounds__(tcp::THREADS, 2) k_chunk_prep2(const __grid_constant__ PrefillArgs A) {
+    using namespace tcp;
+    const Geom& g = A.g;
+    const PrefillJob& J = A.J;
+    const int Hk = g.Hk, Hv = g.Hv;
+    const int j = blockIdx.x, h = j / g.G;
+    const int64_t cs = (int64_t)blockIdx.z * gridDim.y + blockIdx.y;
+    if (cs >= A.ncs) return;
+    int64_t t0;
+    int n;
+    if (!slot_chunk(J, cs, t0, n)) return;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int q4 = warp & 3, hf = warp >> 2;
+    const int row = 32 * q4 + lane;  // the accumulator row (M = 128) this thread reads
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
+    unsigned char *KTs = sm + P2_KT, *VTs = sm + P2_VT, *TBs = sm + P2_TB, *Ps = sm + P2_P;
+    float* eg = reinterpret_cast<float*>(sm + P2_G);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(eg + C);
+    uint64_t* barIn = mbar + 1;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 2);
+    const unsigned char* tile = A.tqk + ((size_t)cs * Hk + h) * kTileQK;
+    unsigned char* rec = A.trec + ((size_t)cs * Hv + j) * kTileRec;
+
+    if (warp == 0) tc::alloc(tslot, P2_TMEM_COLS);
+    if (tid == 0) {
+        mbar_init(mbar, 1);
+        mbar_init(barIn, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(barIn, 32768 + 32768 + 16384 + 16384 + C * 4);
+        bulk_g2s(KTs, tile + 65536, 32768, barIn);
+        bulk_g2s(VTs, A.tv + ((size_t)cs * Hv + j) * kTileV, 32768, barIn);
+        bulk_g2s(TBs, rec + kRecTB, 16384, barIn);
+        bulk_g2s(Ps, rec + kRecP, 16384, barIn);
+        bulk_g2s(eg, rec + kRecG, C * 4, barIn);
+    }
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = *tslot;
+    bool ok = true;
+    uint32_t phase = 0;
+    auto wait_mma = [&]() {
+        bool w = true;
+        if (ok && warp == 0) {
+            w = mbar_wait(mbar, phase);
+            if (!w) w = mbar_wait(mbar, phase);
+        }
+        phase ^= 1u;
+        ok = __syncthreads_and(ok && w);
+        tc::fence_after();
+    };
+    {
+        bool w = true;
+        if (warp == 0) {
+            w = mbar_wait(barIn, 0);
+            if (!w) w = mbar_wait(barIn, 0);
+        }
+        ok = __syncthreads_and(w);
+    }
+    // K^T <- K^T diag(e^gamma), so that (K^T diag(e^gamma)) (T diag(beta))^T = W^T
+    for (int f = tid; f < D * 16; f += THREADS) {
+        const int d = f >> 4, t = (f & 15) * 4;
+        float4* kp = reinterpret_cast<float4*>(KTs + tc::sw_off(D, d, t));
+        const float4 kv = *kp;
+        *kp = make_float4(tc::to_tf32_rn(kv.x * eg[t]), tc::to_tf32_rn(kv.y * eg[t + 1]),
+                          tc::to_tf32_rn(kv.z * eg[t + 2]), tc::to_tf32_rn(kv.w * eg[t + 3]));
+    }
+    // ---- W^T = K'^T TB^T, U~^T = V^T TB^T (M = 128, N = 64, K = 64) ------------------------
+    tc::fence_before();
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        if (ok) {
+            tc::fence_after();
+            tc::mma_tf32(tm + 0, KTs, D, TBs, C, C, tc::idesc_tf32(D, C), false);
+            tc::mma_tf32(tm + 64, VTs, D, TBs, C, C, tc::idesc_tf32(D, C), false);
+        }
+        tc::commit(mbar);
+    }
+    wait_mma();
+    // -W -> rows 0..63 of the stacked operand; W^T and U~^T -> operand tiles
+    // over K^T and V^T; U~ -> the slice blocks of the record
+    unsigned char* ra = rec + kRecA;
+    unsigned char* ux = rec + kRecUX + (size_t)q4 * 16384;  // slice q4 holds v = 32 q4 .. 32 q4 + 31
+    for (int cb = 0; cb < 2; ++cb) {
+        const int i0 = hf * 32 + cb * 16;
+        float w16[16], u16[16];
+        tc::ld16x2(tc::taddr(tm, 32 * q4, i0), w16, tc::taddr(tm, 32 * q4, 64 + i0), u16);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            *reinterpret_cast<float*>(ra + tc::sw_off(D, i0 + c, row)) = -tc::to_tf32_rn(w16[c]);
+            *reinterpret_cast<float*>(ux + ux_off(i0 + c, lane)) = u16[c];
+        }
+#pragma unroll
+        for (int c = 0; c < 16; c += 4) {
+            tc::st_row4(KTs, D, row, i0 + c, w16[c], w16[c + 1], w16[c + 2], w16[c + 3]);
+            tc::st_row4(VTs, D, row, i0 + c, u16[c], u16[c + 1], u16[c + 2], u16[c + 3]);
+        }
+    }
+    // Q^ values of this thread's d (its column of Q) for the Q' epilogue, loaded
+    // while the next products run
+    const float* qtile = reinterpret_cast<const float*>(tile);  // [K^; Q^] tile (TF32 values)
+    float qv[32];
+#pragma unroll
+    for (int c = 0; c < 32; ++c) qv[c] = qtile[tc::sw_off(2 * C, C + hf * 32 + c, row) >> 2];
+    // ---- (P W)^T = W^T P^T, X^T = U~^T P^T -------------------------------------------------
+    tc::fence_before();
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        if (ok) {
+            tc::fence_after();
+            tc::mma_tf32(tm + 0, KTs, D, Ps, C, C, tc::idesc_tf32(D, C), false);
+            tc::mma_tf32(tm + 64, VTs, D, Ps, C, C, tc::idesc_tf32(D, C), false);
+        }
+        tc::commit(mbar);
+    }
+    wait_mma();
+    // Q' = diag(e^gamma) Q - P W -> rows 64..127 of the stacked operand; X -> record
+    for (int cb = 0; cb < 2; ++cb) {
+        const int t0c = hf * 32 + cb * 16;
+        float pw[16], x16[16];
+        tc::ld16x2(tc::taddr(tm, 32 * q4, t0c), pw, tc::taddr(tm, 32 * q4, 64 + t0c), x16);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const int t = t0c + c;
+            const float qp = t < n ? fmaf(eg[t], qv[cb * 16 + c], -pw[c]) : 0.f;
+            *reinterpret_cast<float*>(ra + tc::sw_off(D, C + t, row)) = tc::to_tf32_rn(qp);
+            *reinterpret_cast<float*>(ux + 8192 + ux_off(t, lane)) = x16[c];
+        }
+    }
+    if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::dealloc(tm, P2_TMEM_COLS);
 }
 
 __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_constant__ PrefillArgs A) {
@@ -1147,22 +1374,23 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
-    unsigned char *Qs = sm + OFF_Q, *Ws = sm + OFF_W, *KTs = sm + OFF_KT, *TBs = sm + OFF_TB, *Ps = sm + OFF_P;
-    unsigned char *VTs = sm + OFF_VT, *UPs = sm + OFF_UP, *UTs = sm + OFF_UT, *S0s = sm + OFF_S0;
+    unsigned char *As = sm + OFF_A, *KTs = sm + OFF_KT, *UXs = sm + OFF_UX, *UPs = sm + OFF_UP, *S0s = sm + OFF_S0;
     float* Gs = reinterpret_cast<float*>(sm + OFF_G);  // e^g [64] | e^(gC-g) [64]
     float* ssq = reinterpret_cast<float*>(sm + OFF_SMALL);  // [2][C]
-    float* ored = ssq + 2 * C;                               // [2][C]
+    float* ored = ssq + 2 * C;                               // [2][C] half-row sums of squares
     float* nwsl = ored + 2 * C;                              // norm_w of this slice
     uint64_t* mbar = reinterpret_cast<uint64_t*>(nwsl + DV);  // MMA rounds
-    uint64_t* barA = mbar + 1;  // Q^, W, T diag(b), V^T of a chunk
-    uint64_t* barB = mbar + 2;  // K^T, P, gates of a chunk
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 3);
+    uint64_t* barA = mbar + 1;  // [-W; Q'] of a chunk
+    uint64_t* barB = mbar + 2;  // K^T of a chunk
+    uint64_t* barC = mbar + 3;  // U~, X, gates of a chunk
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 4);
 
     if (warp == 0) tc::alloc(tslot, TMEM_COLS);
     if (tid == 0) {
         mbar_init(mbar, 1);
         mbar_init(barA, 1);
         mbar_init(barB, 1);
+        mbar_init(barC, 1);
         fence_mbar_init();
     }
     tc::fence_before();
@@ -1187,23 +1415,9 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         }
     }
     const int dS = 32 * q4 + lane;  // the d_k index this thread owns in S^T
-    if (tid < DV) nwsl[tid] = (g.flags & kFlagNoOutNorm) ? 1.f : Act<__nv_bfloat16>::ld(A.p.norm_w, s_idx * DV + tid);
-    {
-        float v[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const int dv = hf * 16 + c;
-            v[c] = Sin ? Sin[(size_t)(s_idx * DV + dv) * D + dS] : 0.f;
-            tc::st_elem(S0s, DV, dv, dS, v[c]);
-        }
-        tc::st16(tc::taddr(tm, 32 * q4, cS + hf * 16), v);
-    }
+    const bool outnorm = !(g.flags & kFlagNoOutNorm);
+    if (tid < DV) nwsl[tid] = outnorm ? Act<__nv_bfloat16>::ld(A.p.norm_w, s_idx * DV + tid) : 1.f;
 
-    auto mma_round_begin = [&]() {
-        tc::fence_before();
-        fence_proxy_async_smem();
-        __syncthreads();
-    };
     auto wait_mma = [&]() {
         bool w = true;
         if (ok && warp == 0) {  // one warp polls, the others sleep in bar.sync
@@ -1225,177 +1439,192 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
 
     const int64_t T = end - start;
     const int n_chunks = (int)((T + C - 1) / C);
-    const bool outnorm = !(g.flags & kFlagNoOutNorm);
-    const int trow = 16 * q4 + (lane & 15);  // the chunk row this thread reads from M=64 accumulators
-    const bool rowok = lane < 16;
+    const bool urow = q4 < 2;                  // rows 0..63 of D: U; rows 64..127: O
+    const int trow = 32 * (q4 & 1) + lane;     // the chunk row of this thread's D row
     auto rows_of = [&](int c) -> int {
         const int64_t left = end - (start + (int64_t)c * C);
         return (int)(left < C ? left : C);
     };
-    // operand tiles come ready-made (prologue and prep kernel): bulk copies
+    // operand tiles come ready-made (prologue and prep kernels): bulk copies
     // issued for chunk c+1 as soon as chunk c's last use of the buffer is done
     auto cslot = [&](int c) -> size_t { return (size_t)(start / C + seq + c); };
     auto issue_a = [&](int c) {
-        const unsigned char* tq = A.tqk + (cslot(c) * Hk + h) * kTileQK;
-        const unsigned char* rc = A.trec + (cslot(c) * Hv + j) * kTileRec;
-        mbar_arrive_expect_tx(barA, 32768 + 32768 + 16384 + 8192);
-        bulk_g2s(Qs, tq, 32768, barA);
-        bulk_g2s(Ws, rc + kRecW, 32768, barA);
-        bulk_g2s(TBs, rc + kRecTB, 16384, barA);
-        bulk_g2s(VTs, A.tv + ((cslot(c) * Hv + j) * 4 + s_idx) * 8192, 8192, barA);
+        mbar_arrive_expect_tx(barA, 65536);
+        bulk_g2s(As, A.trec + (cslot(c) * Hv + j) * kTileRec + kRecA, 65536, barA);
     };
     auto issue_b = [&](int c) {
-        const unsigned char* tq = A.tqk + (cslot(c) * Hk + h) * kTileQK;
-        const unsigned char* rc = A.trec + (cslot(c) * Hv + j) * kTileRec;
-        mbar_arrive_expect_tx(barB, 32768 + 16384 + 2 * C * 4);
-        bulk_g2s(KTs, tq + 65536, 32768, barB);
-        bulk_g2s(Ps, rc + kRecP, 16384, barB);
-        bulk_g2s(Gs, rc + kRecG, 2 * C * 4, barB);
+        mbar_arrive_expect_tx(barB, 32768);
+        bulk_g2s(KTs, A.tqk + (cslot(c) * Hk + h) * kTileQK + 65536, 32768, barB);
     };
-    // Ra of chunk c: U = T diag(b) V - W S^T, O1 = Q S^T (S0s holds the state
-    // entering chunk c); committed, not waited for
+    auto issue_c = [&](int c) {
+        const unsigned char* rc = A.trec + (cslot(c) * Hv + j) * kTileRec;
+        mbar_arrive_expect_tx(barC, 16384 + 2 * C * 4);
+        bulk_g2s(UXs, rc + kRecUX + (size_t)s_idx * 16384, 16384, barC);
+        bulk_g2s(Gs, rc + kRecG, 2 * C * 4, barC);
+    };
+    // Ra of chunk c: D = [-W; Q'] S^T with S0s holding the state entering c
     auto issue_ra = [&](int c) {
         wait_bar(barA, (uint32_t)(c & 1));
-        const int nc = rows_of(c);
-        if (nc < C) {  // tokens past the sequence end were never written: zero Q^ rows, V^T columns
-            for (int f = tid; f < (C - nc) * 32; f += THREADS) {
-                const int r = nc + (f >> 5), c4 = (f & 31) * 4;
-                *reinterpret_cast<float4*>(Qs + tc::sw_off(C, r, c4)) = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            for (int f = tid; f < DV * (C - nc); f += THREADS) {
-                const int row = f / (C - nc), t = nc + f % (C - nc);
-                *reinterpret_cast<float*>(VTs + tc::sw_off(DV, row, t)) = 0.f;
-            }
-        }
-        mma_round_begin();
+        tc::fence_before();
+        fence_proxy_async_smem();
+        __syncthreads();
         if (tid == 0) {
             if (ok) {
                 tc::fence_after();
-                tc::mma_tf32(tm + cU, TBs, C, VTs, DV, C, tc::idesc_tf32(C, DV), false);
-                tc::mma_tf32(tm + cU, Ws, C, S0s, DV, D, tc::idesc_tf32(C, DV, true), true);
-                tc::mma_tf32(tm + cO1, Qs, C, S0s, DV, D, tc::idesc_tf32(C, DV), false);
+                tc::mma_tf32_split(tm + cD, 4, 32, As, D, S0s, DV, D, tc::idesc_tf32(D, DV), false);
             }
             tc::commit(mbar);
         }
     };
 
-    if (tid == 0 && n_chunks > 0) {
-        issue_a(0);
-        issue_b(0);
+    // initial state: S0s <- S (TF32), TMEM S^T <- e^gamma_C S for the first chunk
+    float s16[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        const int dv = hf * 16 + c;
+        s16[c] = Sin ? Sin[(size_t)(s_idx * DV + dv) * D + dS] : 0.f;
+        tc::st_elem(S0s, DV, dv, dS, s16[c]);
     }
-    if (n_chunks > 0) issue_ra(0);
+    if (n_chunks > 0) {
+        if (tid == 0) {
+            issue_a(0);
+            issue_b(0);
+            issue_c(0);
+        }
+        wait_bar(barC, 0);
+        const float egC = Gs[C - 1];
+        float v[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) v[c] = s16[c] * egC;
+        tc::st16(tc::taddr(tm, 32 * q4, cS + hf * 16), v);
+        issue_ra(0);
+    }
+    uint4 ypk[2];  // y of the previous chunk (output-row threads), not yet stored
+    bool yprev_ok = false;
+    size_t yprev_tok = 0;
     for (int ci = 0; ci < n_chunks; ++ci) {
         const int64_t t0 = start + (int64_t)ci * C;
         const int n = rows_of(ci);
         const uint32_t par = (uint32_t)(ci & 1);
         wait_mma();                                          // Ra of this chunk
-        if (tid == 0 && ci + 1 < n_chunks) issue_a(ci + 1);  // Q^, W, T diag(b), V^T are free
-        wait_bar(barB, par);
-        if (n < C) {  // tail columns (t >= n) of K^T
-            for (int f = tid; f < D * (C - n); f += THREADS) {
-                const int row = f / (C - n), t = n + f % (C - n);
-                *reinterpret_cast<float*>(KTs + tc::sw_off(D, row, t)) = 0.f;
-            }
-        }
-        // ---- U -> U^T and (diag(e^(gC - g)) U)^T tiles; S^T *= e^gC in TMEM -----------------
-        float egt = 0.f;  // e^gamma of this thread's output row
+        if (tid == 0 && ci + 1 < n_chunks) issue_a(ci + 1);  // [-W; Q'] is free
+        // ---- U = U~ + D[0:64] -> (diag(e^(gC - g)) U)^T tile (warps 0,1,4,5); O = X +
+        // D[64:128] and its sums of squares (warps 2,3,6,7); 16 columns per thread -----
+        float* ssq_cur = ssq + (ci & 1) * C;
+        float o16[16];
         {
-            float u16[16];
-            tc::ld16(tc::taddr(tm, 32 * q4, cU + hf * 16), u16);
-            if (rowok) {
+            float d16[16];
+            tc::ld16_sum4(tc::taddr(tm, 32 * q4, cD + hf * 16), 32, d16);
+            if (urow) {
                 const float er = Gs[C + trow];
-                egt = Gs[trow];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    tc::st_elem(UTs, DV, hf * 16 + c, trow, u16[c]);
-                    tc::st_elem(UPs, DV, hf * 16 + c, trow, u16[c] * er);
+                for (int c4 = 0; c4 < 16; c4 += 4) {
+                    const float4 a = *reinterpret_cast<const float4*>(UXs + ux_off(trow, hf * 16 + c4));
+                    tc::st_elem(UPs, DV, hf * 16 + c4, trow, (a.x + d16[c4]) * er);
+                    tc::st_elem(UPs, DV, hf * 16 + c4 + 1, trow, (a.y + d16[c4 + 1]) * er);
+                    tc::st_elem(UPs, DV, hf * 16 + c4 + 2, trow, (a.z + d16[c4 + 2]) * er);
+                    tc::st_elem(UPs, DV, hf * 16 + c4 + 3, trow, (a.w + d16[c4 + 3]) * er);
                 }
-            }
-            float s16[16];
-            tc::ld16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
-            const float egC = Gs[C - 1];
+            } else {
+                float part = 0.f;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) s16[c] *= egC;
-            tc::st16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
-        }
-        // ---- Rb: O2 = P U, S^T += K^T U' ---------------------------------------------------
-        mma_round_begin();
-        if (tid == 0) {
-            if (ok) {
-                tc::fence_after();
-                tc::mma_tf32(tm + cO2, Ps, C, UTs, DV, C, tc::idesc_tf32(C, DV), false);
-                tc::mma_tf32(tm + cS, KTs, D, UPs, DV, C, tc::idesc_tf32(D, DV), true);
+                for (int c4 = 0; c4 < 16; c4 += 4) {
+                    const float4 a = *reinterpret_cast<const float4*>(UXs + 8192 + ux_off(trow, hf * 16 + c4));
+                    o16[c4] = a.x + d16[c4];
+                    o16[c4 + 1] = a.y + d16[c4 + 1];
+                    o16[c4 + 2] = a.z + d16[c4 + 2];
+                    o16[c4 + 3] = a.w + d16[c4 + 3];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) part = fmaf(o16[c4 + e], o16[c4 + e], part);
+                }
+                ored[hf * C + trow] = part;
+                named_bar_sync(1, 128);  // warps 2,3,6,7
+                if (hf == 0) ssq_cur[trow] = ored[trow] + ored[C + trow];
             }
-            tc::commit(mbar);
         }
-        float zpre[16];  // z of this thread's output row (loaded while Rb runs)
-        if (outnorm && rowok && trow < n) {
+        // warps 2 and 3 wrote the sums of squares the peers read: they release (their
+        // earlier global stores were issued a chunk ago); the other warps -- among them
+        // the one with bulk copies in flight -- arrive relaxed
+        if (!urow && hf == 0) cluster_arrive_release();
+        else cluster_arrive_relaxed();
+        if (!urow && ci > 0 && yprev_ok) {  // y of the previous chunk, held back until now
+            uint4* yp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(J.y) + yprev_tok * (size_t)Hv * D +
+                                                 (size_t)j * D + s_idx * DV + hf * 16);
+            yp[0] = ypk[0];
+            yp[1] = ypk[1];
+        }
+        uint4 zr[2];  // z of this thread's output row
+        if (!urow && outnorm && trow < n) {
             const uint4* zp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(J.z) +
                                                              (size_t)(t0 + trow) * Hv * D + (size_t)j * D +
                                                              s_idx * DV + hf * 16);
-            const uint4 z0 = zp[0], z1 = zp[1];
-            const __nv_bfloat162* h0 = reinterpret_cast<const __nv_bfloat162*>(&z0);
-            const __nv_bfloat162* h1 = reinterpret_cast<const __nv_bfloat162*>(&z1);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const float2 a = __bfloat1622float2(h0[c]), b = __bfloat1622float2(h1[c]);
-                zpre[2 * c] = a.x; zpre[2 * c + 1] = a.y; zpre[8 + 2 * c] = b.x; zpre[8 + 2 * c + 1] = b.y;
-            }
+            zr[0] = zp[0];
+            zr[1] = zp[1];
         }
-        wait_mma();
-        if (tid == 0 && ci + 1 < n_chunks) issue_b(ci + 1);  // K^T, P, gates are read
-        // ---- O = diag(e^g) O1 + O2; S^T -> S operand tile for the next chunk ----------------
-        float o16[16];
-        {
-            float a16[16];
-            tc::ld16x2(tc::taddr(tm, 32 * q4, cO1 + hf * 16), a16, tc::taddr(tm, 32 * q4, cO2 + hf * 16), o16);
-            float part = 0.f;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                o16[c] = fmaf(egt, a16[c], o16[c]);
-                part = fmaf(o16[c], o16[c], part);
-            }
-            if (rowok) ored[hf * C + trow] = part;
-            float s16[16];
-            tc::ld16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) tc::st_elem(S0s, DV, hf * 16 + c, dS, s16[c]);
-        }
+        wait_bar(barB, par);
+        // ---- Rb: S^T += K^T U' -------------------------------------------------------------
+        tc::fence_before();
+        fence_proxy_async_smem();
         __syncthreads();
-        float* ssq_cur = ssq + (ci & 1) * C;
-        if (tid < C) ssq_cur[tid] = ored[tid] + ored[C + tid];
-        cluster_arrive_release();
-        if (ci + 1 < n_chunks) issue_ra(ci + 1);  // runs while this chunk's output is normalised
+        if (tid == 0) {
+            if (ok) {
+                tc::fence_after();
+                tc::mma_tf32_split(tm + cS, 4, 32, KTs, D, UPs, DV, C, tc::idesc_tf32(D, DV), true);
+            }
+            tc::commit(mbar);
+            if (ci + 1 < n_chunks) issue_c(ci + 1);  // U~, X and the gates have been read
+        }
+        wait_mma();                                          // Rb
+        if (tid == 0 && ci + 1 < n_chunks) issue_b(ci + 1);  // K^T is free
+        // ---- S^T -> S operand tile for the next chunk ----------------------------------------
+        tc::ld16_sum4(tc::taddr(tm, 32 * q4, cS + hf * 16), 32, s16);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) tc::st_elem(S0s, DV, hf * 16 + c, dS, s16[c]);
+        if (ci + 1 < n_chunks) {
+            issue_ra(ci + 1);
+            wait_bar(barC, par ^ 1u);  // gates of the next chunk: S^T *= e^gamma_C in TMEM
+            const float egC = Gs[C - 1];
+            float v[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = s16[c] * egC;
+            tc::st16(tc::taddr(tm, 32 * q4, cS + hf * 16), v);
+        }
         cluster_wait_acquire();
-        if (rowok && trow < n) {
-            const size_t tok = (size_t)(t0 + trow);
+        // ---- y = gated RMSNorm(O) of this chunk, stored after the next chunk's arrive -------
+        yprev_ok = !urow && trow < n;
+        yprev_tok = (size_t)(t0 + trow);
+        if (yprev_ok) {
             float rstd = 1.f;
             if (outnorm) {
-                float tot = 0.f;
-                for (int s2 = 0; s2 < NS; ++s2) tot += *cluster.map_shared_rank(&ssq_cur[trow], s2);
-                rstd = rsqrtf(tot / (float)D + g.norm_eps);
+                float sq[NS];
+#pragma unroll
+                for (int s2 = 0; s2 < NS; ++s2) sq[s2] = *cluster.map_shared_rank(&ssq_cur[trow], s2);
+                rstd = rsqrtf(((sq[0] + sq[1]) + (sq[2] + sq[3])) / (float)D + g.norm_eps);
             }
-            float yv[16];
+            const __nv_bfloat162* zh = reinterpret_cast<const __nv_bfloat162*>(zr);
+            __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(ypk);
 #pragma unroll
-            for (int c = 0; c < 16; ++c) yv[c] = outnorm ? o16[c] * rstd * nwsl[hf * 16 + c] * siluf_(zpre[c]) : o16[c];
-            uint4 pk[2];
-            __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(pk);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) hp[c] = __floats2bfloat162_rn(yv[2 * c], yv[2 * c + 1]);
-            uint4* yp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(J.y) + tok * (size_t)Hv * D +
-                                                 (size_t)j * D + s_idx * DV + hf * 16);
-            yp[0] = pk[0];
-            yp[1] = pk[1];
+            for (int c = 0; c < 8; ++c) {
+                float y0 = o16[2 * c], y1 = o16[2 * c + 1];
+                if (outnorm) {
+                    const float2 zz = __bfloat1622float2(zh[c]);
+                    y0 = y0 * rstd * nwsl[hf * 16 + 2 * c] * silu_fast(zz.x);
+                    y1 = y1 * rstd * nwsl[hf * 16 + 2 * c + 1] * silu_fast(zz.y);
+                }
+                hp[c] = __floats2bfloat162_rn(y0, y1);
+            }
         }
     }
-    // ---- final state ------------------------------------------------------------------------
-    {
-        float s16[16];
-        tc::ld16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
-        if (Sout) {
+    if (n_chunks > 0 && yprev_ok) {  // y of the last chunk
+        uint4* yp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(J.y) + yprev_tok * (size_t)Hv * D +
+                                             (size_t)j * D + s_idx * DV + hf * 16);
+        yp[0] = ypk[0];
+        yp[1] = ypk[1];
+    }
+    // ---- final state (the S operand registers hold the state after the last chunk) ---------
+    if (Sout) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) Sout[(size_t)(s_idx * DV + hf * 16 + c) * D + dS] = s16[c];
-        }
+        for (int c = 0; c < 16; ++c) Sout[(size_t)(s_idx * DV + hf * 16 + c) * D + dS] = s16[c];
     }
     if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
     tc::fence_before();
@@ -1410,6 +1639,8 @@ cudaError_t launch_chunk_tc(const PrefillArgs& A, int64_t n_slots, cudaStream_t 
         cudaError_t e = cudaFuncSetAttribute(k_chunk_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              tcp::PR_SMEM_ALLOC);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(k_chunk_prep2, cudaFuncAttributeMaxDynamicSharedMemorySize, tcp::P2_SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(k_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, tcp::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -1419,6 +1650,9 @@ cudaError_t launch_chunk_tc(const PrefillArgs& A, int64_t n_slots, cudaStream_t 
         const dim3 grid((unsigned)A.g.Hv, (unsigned)ny, (unsigned)((n_slots + ny - 1) / ny));
         k_chunk_prep<<<grid, tcp::THREADS, tcp::PR_SMEM_ALLOC, st>>>(A);
         cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        k_chunk_prep2<<<grid, tcp::THREADS, tcp::P2_SMEM_ALLOC, st>>>(A);
+        e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
@@ -1469,7 +1703,20 @@ cudaError_t launch_prefill_t(const Geom& g, const LayerParams& p, const PrefillJ
         A.trec = reinterpret_cast<unsigned char*>(ws + tl.rec);
         A.ncs = tl.ncs;
     }
-    if (J.n_tokens > 0) {
+    if (A.tiles) {
+        static bool attr_set = false;
+        if (!attr_set) {
+            cudaError_t e = cudaFuncSetAttribute(k_prologue_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kPtSmemAlloc);
+            if (e != cudaSuccess) return e;
+            attr_set = true;
+        }
+        const int64_t ny = A.ncs < 32768 ? A.ncs : 32768;
+        const dim3 grid((unsigned)(g.Hk + g.Hv), (unsigned)ny, (unsigned)((A.ncs + ny - 1) / ny));
+        k_prologue_tc<<<grid, kPtThreads, kPtSmemAlloc, st>>>(A);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    } else if (J.n_tokens > 0) {
         constexpr int VEC = 16 / (int)sizeof(TA);
         const dim3 blocks((unsigned)((J.n_tokens + kProTok - 1) / kProTok),
                           (unsigned)((g.C_ch / VEC + kProThreads - 1) / kProThreads));

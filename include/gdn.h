@@ -201,7 +201,7 @@ gdn_status gdn_varlen_prefill(const gdn_config* cfg, const gdn_params* prm, cons
  * workspace is a static device array of 64 MiB inside libgdn, which every GPU
  * that loads the library holds until the process exits.  T is limited to
  * what fits: gdn_workspace_size(cfg, GDN_OP_CHUNK_PREFILL, T, 1) <= 64 MiB
- * (about 800 tokens at the Qwen3.5-4B geometry); larger T returns
+ * (about 440 tokens at the Qwen3.5-4B geometry); larger T returns
  * GDN_ERR_WORKSPACE with both sizes in gdn_last_error().
  * The first call on a device looks up the array's address (cudaGetSymbolAddress,
  * with that device current) and caches it: make that first call before any

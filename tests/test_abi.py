@@ -112,7 +112,7 @@ def test_workspace_size_and_refusal(lib):
     # g and beta 2 x 32), or operand tiles per 64-token chunk slot (8192/64 + 1 sequence + 1 slots;
     # per k-head Q^, K^, K^T tiles of 32 KB, per v-head 4 V^T tiles of 8 KB and 512 B of gates)
     per_token = 8192 * (2 * 16 * 128 + 32 * 128 + 2 * 32) * 4
-    tiles = (8192 // 64 + 2) * (16 * 3 * 32768 + 32 * 4 * 8192 + 32 * 512 + 32 * 66560)
+    tiles = (8192 // 64 + 2) * (16 * 3 * 32768 + 32 * 4 * 8192 + 32 * 512 + 32 * 164864)
     assert need == max(per_token, tiles)
     assert lib.gdn_workspace_size(ctypes.byref(cfg), gb.OP_DECODE_STEP, 64, 1) == 0
     bad = _cfg(chunk=48)

@@ -47,7 +47,7 @@ def _call_noalloc_c_abi(cfg, prm, x, z, a, b, s0, c0, s, c, y):
 
 
 def test_noalloc_prefill_matches_workspace_prefill_two_calls():
-    for stream, T in ((501, 800), (502, 450)):
+    for stream, T in ((501, 440), (502, 300)):
         geom, act, p, tok, S0, C0 = _inputs(stream, T)
         cfg = config(geom, act)
         prm = params_dev(p)
