@@ -947,9 +947,11 @@ __global__ void __launch_bounds__(kChunkThreads, 1) k_chunk(const __grid_constan
 //     Ra  D = [-W; Q'] S^T                    (M = 128, K = 128)
 //         U = U~ + D[0:64],  O = X + D[64:128]
 //     Rb  S^T <- e^gamma_C S^T + K^T (diag(e^(gamma_C - gamma)) U)
-//   and y = gated RMSNorm(O) of chunk c is written while Ra of chunk c+1 runs.
-//   Both products deal their K-steps to four TMEM accumulators (summed by the
-//   epilogues): with N = 32 a single accumulation chain is latency-bound.
+//   and y = gated RMSNorm(O) of chunk c is computed while Ra of chunk c+1 runs.
+//   The tensor core takes about one MMA instruction per 140 cycles whatever
+//   its M and N, so the chain's cost is its 24 instructions per chunk (16 for
+//   Ra with K = 128, 8 for Rb with K = 64); everything else is arranged around
+//   them.
 // TF32 operands are rounded to nearest; accumulation is fp32 in TMEM.
 
 // One warp: the 16x8 tile C = A(16 x K) B(K x 8) with A(m,k) = Ap[m*lda + k] and
@@ -1015,12 +1017,12 @@ constexpr int OFF_UX = OFF_KT + 32768; // U~ | X of this slice, fp32 [64][32] ea
 constexpr int OFF_UP = OFF_UX + 16384; // (diag(e^(gC-g)) U)^T [32][64]
 constexpr int OFF_S0 = OFF_UP + 8192;  // S   [32][128] (this slice's rows)
 constexpr int OFF_G = OFF_S0 + 16384;  // e^g [64] | e^(gC-g) [64]
-constexpr int OFF_SMALL = OFF_G + 512; // ssq [2][64], ored [2][64], norm_w slice [32]
-constexpr int SMALL_FLOATS = 4 * C + DV;
-constexpr int SMEM = OFF_SMALL + SMALL_FLOATS * 4 + 64;  // + 4 mbarriers and the TMEM address
+constexpr int OFF_SMALL = OFF_G + 512; // ssq [2][NS][64], ored [2][64], norm_w slice [32]
+constexpr int SMALL_FLOATS = 2 * NS * C + 2 * C + DV;
+constexpr int SMEM = OFF_SMALL + SMALL_FLOATS * 4 + 64;  // + 6 mbarriers and the TMEM address
 constexpr int SMEM_ALLOC = SMEM + 1024;                  // room to align the base to 1024 bytes
-// Ra: four partial accumulators of D at cD + 32 a; Rb: S^T at cS plus three partials
-constexpr int cD = 0, cS = 128, TMEM_COLS = 256;
+constexpr int cD = 0, cS = 32, TMEM_COLS = 64;
+static_assert(NS == 4, "the output norm adds the 4 slices' row sums explicitly");
 }  // namespace tcp
 
 __global__ void __launch_bounds__(tcp::THREADS, 2) k_chunk_prep(const __grid_constant__ PrefillArgs A) {
@@ -1376,29 +1378,39 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
     unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
     unsigned char *As = sm + OFF_A, *KTs = sm + OFF_KT, *UXs = sm + OFF_UX, *UPs = sm + OFF_UP, *S0s = sm + OFF_S0;
     float* Gs = reinterpret_cast<float*>(sm + OFF_G);  // e^g [64] | e^(gC-g) [64]
-    float* ssq = reinterpret_cast<float*>(sm + OFF_SMALL);  // [2][C]
-    float* ored = ssq + 2 * C;                               // [2][C] half-row sums of squares
+    float* ssq = reinterpret_cast<float*>(sm + OFF_SMALL);  // [2][NS][C] row sums of squares per slice
+    float* ored = ssq + 2 * NS * C;                          // [2][C] half-row sums of squares
     float* nwsl = ored + 2 * C;                              // norm_w of this slice
     uint64_t* mbar = reinterpret_cast<uint64_t*>(nwsl + DV);  // MMA rounds
-    uint64_t* barA = mbar + 1;  // [-W; Q'] of a chunk
-    uint64_t* barB = mbar + 2;  // K^T of a chunk
-    uint64_t* barC = mbar + 3;  // U~, X, gates of a chunk
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 4);
+    uint64_t* barA = mbar + 1;    // [-W; Q'] of a chunk
+    uint64_t* barB = mbar + 2;    // K^T of a chunk
+    uint64_t* barC = mbar + 3;    // U~, X, gates of a chunk
+    uint64_t* barSq = mbar + 4;   // [2]: the peers' sums of squares of a chunk (by parity)
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 6);
 
     if (warp == 0) tc::alloc(tslot, TMEM_COLS);
+    const bool outnorm = !(g.flags & kFlagNoOutNorm);
+    constexpr uint32_t kSqBytes = (NS - 1) * C * 4;  // the peers' row sums of one chunk
     if (tid == 0) {
         mbar_init(mbar, 1);
         mbar_init(barA, 1);
         mbar_init(barB, 1);
         mbar_init(barC, 1);
+        mbar_init(barSq, 1);
+        mbar_init(barSq + 1, 1);
         fence_mbar_init();
+        if (outnorm) {  // chunks 0 and 1
+            mbar_arrive_expect_tx(barSq, kSqBytes);
+            mbar_arrive_expect_tx(barSq + 1, kSqBytes);
+        }
     }
     tc::fence_before();
-    __syncthreads();
+    cluster.sync();  // every CTA's barriers are initialised before a peer stores into them
     tc::fence_after();
     const uint32_t tm = *tslot;
     uint32_t phase = 0;
     bool ok = true;
+    const uint32_t my_rank = cluster.block_rank();
 
     int64_t start, end;
     seq_bounds(J, seq, start, end);
@@ -1415,7 +1427,6 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         }
     }
     const int dS = 32 * q4 + lane;  // the d_k index this thread owns in S^T
-    const bool outnorm = !(g.flags & kFlagNoOutNorm);
     if (tid < DV) nwsl[tid] = outnorm ? Act<__nv_bfloat16>::ld(A.p.norm_w, s_idx * DV + tid) : 1.f;
 
     auto wait_mma = [&]() {
@@ -1471,7 +1482,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         if (tid == 0) {
             if (ok) {
                 tc::fence_after();
-                tc::mma_tf32_split(tm + cD, 4, 32, As, D, S0s, DV, D, tc::idesc_tf32(D, DV), false);
+                tc::mma_tf32(tm + cD, As, D, S0s, DV, D, tc::idesc_tf32(D, DV), false);
             }
             tc::commit(mbar);
         }
@@ -1499,9 +1510,6 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         tc::st16(tc::taddr(tm, 32 * q4, cS + hf * 16), v);
         issue_ra(0);
     }
-    uint4 ypk[2];  // y of the previous chunk (output-row threads), not yet stored
-    bool yprev_ok = false;
-    size_t yprev_tok = 0;
     for (int ci = 0; ci < n_chunks; ++ci) {
         const int64_t t0 = start + (int64_t)ci * C;
         const int n = rows_of(ci);
@@ -1510,11 +1518,12 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         if (tid == 0 && ci + 1 < n_chunks) issue_a(ci + 1);  // [-W; Q'] is free
         // ---- U = U~ + D[0:64] -> (diag(e^(gC - g)) U)^T tile (warps 0,1,4,5); O = X +
         // D[64:128] and its sums of squares (warps 2,3,6,7); 16 columns per thread -----
-        float* ssq_cur = ssq + (ci & 1) * C;
+        float* ssq_cur = ssq + (ci & 1) * NS * C;  // [NS][C]
+        uint64_t* bar_sq = barSq + (ci & 1);
         float o16[16];
         {
             float d16[16];
-            tc::ld16_sum4(tc::taddr(tm, 32 * q4, cD + hf * 16), 32, d16);
+            tc::ld16(tc::taddr(tm, 32 * q4, cD + hf * 16), d16);
             if (urow) {
                 const float er = Gs[C + trow];
 #pragma unroll
@@ -1539,19 +1548,17 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
                 }
                 ored[hf * C + trow] = part;
                 named_bar_sync(1, 128);  // warps 2,3,6,7
-                if (hf == 0) ssq_cur[trow] = ored[trow] + ored[C + trow];
+                if (hf == 0 && outnorm) {  // this slice's row sum -> every CTA of the cluster
+                    const float sq = ored[trow] + ored[C + trow];
+                    float* mine = ssq_cur + my_rank * C + trow;
+                    *mine = sq;
+#pragma unroll
+                    for (int r = 0; r < NS; ++r)
+                        if (r != (int)my_rank)
+                            st_async_f32(mapa_shared(tc::smem_addr(mine), r), sq,
+                                         mapa_shared(tc::smem_addr(bar_sq), r));
+                }
             }
-        }
-        // warps 2 and 3 wrote the sums of squares the peers read: they release (their
-        // earlier global stores were issued a chunk ago); the other warps -- among them
-        // the one with bulk copies in flight -- arrive relaxed
-        if (!urow && hf == 0) cluster_arrive_release();
-        else cluster_arrive_relaxed();
-        if (!urow && ci > 0 && yprev_ok) {  // y of the previous chunk, held back until now
-            uint4* yp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(J.y) + yprev_tok * (size_t)Hv * D +
-                                                 (size_t)j * D + s_idx * DV + hf * 16);
-            yp[0] = ypk[0];
-            yp[1] = ypk[1];
         }
         uint4 zr[2];  // z of this thread's output row
         if (!urow && outnorm && trow < n) {
@@ -1569,7 +1576,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         if (tid == 0) {
             if (ok) {
                 tc::fence_after();
-                tc::mma_tf32_split(tm + cS, 4, 32, KTs, D, UPs, DV, C, tc::idesc_tf32(D, DV), true);
+                tc::mma_tf32(tm + cS, KTs, D, UPs, DV, C, tc::idesc_tf32(D, DV), true);
             }
             tc::commit(mbar);
             if (ci + 1 < n_chunks) issue_c(ci + 1);  // U~, X and the gates have been read
@@ -1577,7 +1584,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         wait_mma();                                          // Rb
         if (tid == 0 && ci + 1 < n_chunks) issue_b(ci + 1);  // K^T is free
         // ---- S^T -> S operand tile for the next chunk ----------------------------------------
-        tc::ld16_sum4(tc::taddr(tm, 32 * q4, cS + hf * 16), 32, s16);
+        tc::ld16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
 #pragma unroll
         for (int c = 0; c < 16; ++c) tc::st_elem(S0s, DV, hf * 16 + c, dS, s16[c]);
         if (ci + 1 < n_chunks) {
@@ -1589,48 +1596,49 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
             for (int c = 0; c < 16; ++c) v[c] = s16[c] * egC;
             tc::st16(tc::taddr(tm, 32 * q4, cS + hf * 16), v);
         }
-        cluster_wait_acquire();
-        // ---- y = gated RMSNorm(O) of this chunk, stored after the next chunk's arrive -------
-        yprev_ok = !urow && trow < n;
-        yprev_tok = (size_t)(t0 + trow);
-        if (yprev_ok) {
+        // ---- y = gated RMSNorm(O) of this chunk (while Ra of the next chunk runs) ---------
+        if (!urow) {
             float rstd = 1.f;
-            if (outnorm) {
-                float sq[NS];
-#pragma unroll
-                for (int s2 = 0; s2 < NS; ++s2) sq[s2] = *cluster.map_shared_rank(&ssq_cur[trow], s2);
-                rstd = rsqrtf(((sq[0] + sq[1]) + (sq[2] + sq[3])) / (float)D + g.norm_eps);
+            if (outnorm) {  // the peers' row sums of this chunk have landed
+                const uint32_t sq_par = (uint32_t)((ci >> 1) & 1);
+                bool w = mbar_wait(bar_sq, sq_par);
+                if (!w) w = mbar_wait(bar_sq, sq_par);
+                ok = ok && w;
+                if (tid == 64) mbar_arrive_expect_tx(bar_sq, kSqBytes);  // for chunk ci + 2
+                const float* sq = ssq_cur + trow;
+                rstd = rsqrtf(((sq[0] + sq[C]) + (sq[2 * C] + sq[3 * C])) / (float)D + g.norm_eps);
             }
-            const __nv_bfloat162* zh = reinterpret_cast<const __nv_bfloat162*>(zr);
-            __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(ypk);
+            if (trow < n) {
+                const __nv_bfloat162* zh = reinterpret_cast<const __nv_bfloat162*>(zr);
+                uint4 pk[2];
+                __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float y0 = o16[2 * c], y1 = o16[2 * c + 1];
-                if (outnorm) {
-                    const float2 zz = __bfloat1622float2(zh[c]);
-                    y0 = y0 * rstd * nwsl[hf * 16 + 2 * c] * silu_fast(zz.x);
-                    y1 = y1 * rstd * nwsl[hf * 16 + 2 * c + 1] * silu_fast(zz.y);
+                for (int c = 0; c < 8; ++c) {
+                    float y0 = o16[2 * c], y1 = o16[2 * c + 1];
+                    if (outnorm) {
+                        const float2 zz = __bfloat1622float2(zh[c]);
+                        y0 = y0 * rstd * nwsl[hf * 16 + 2 * c] * silu_fast(zz.x);
+                        y1 = y1 * rstd * nwsl[hf * 16 + 2 * c + 1] * silu_fast(zz.y);
+                    }
+                    hp[c] = __floats2bfloat162_rn(y0, y1);
                 }
-                hp[c] = __floats2bfloat162_rn(y0, y1);
+                uint4* yp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(J.y) + (size_t)(t0 + trow) * Hv * D +
+                                                     (size_t)j * D + s_idx * DV + hf * 16);
+                yp[0] = pk[0];
+                yp[1] = pk[1];
             }
         }
-    }
-    if (n_chunks > 0 && yprev_ok) {  // y of the last chunk
-        uint4* yp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(J.y) + yprev_tok * (size_t)Hv * D +
-                                             (size_t)j * D + s_idx * DV + hf * 16);
-        yp[0] = ypk[0];
-        yp[1] = ypk[1];
     }
     // ---- final state (the S operand registers hold the state after the last chunk) ---------
     if (Sout) {
 #pragma unroll
         for (int c = 0; c < 16; ++c) Sout[(size_t)(s_idx * DV + hf * 16 + c) * D + dS] = s16[c];
     }
-    if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
     tc::fence_before();
-    __syncthreads();
+    ok = __syncthreads_and(ok);
+    if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
     if (warp == 0) tc::dealloc(tm, TMEM_COLS);
-    cluster.sync();  // peers may still read this CTA's partial sums
+    cluster.sync();  // every st.async into this CTA's shared memory has landed
 }
 
 cudaError_t launch_chunk_tc(const PrefillArgs& A, int64_t n_slots, cudaStream_t st) {
