@@ -536,7 +536,7 @@ def gpu_arm(args):
                      "traffic": traffic, "call_us": round(launch_s * 1e6, 3),
                      "algorithmic_bytes_per_launch": B * SLOT_BYTES + PARAM_BYTES},
         "prefill": {"workload": "chunked prefill, 1 sequence, T = 8192, 16/32 heads, d = 128, bf16 in, fp32 state, "
-                                "chunk 64 (3 launches: prologue, conv state, chunk kernel)",
+                                "chunk 64 (5 launches: tile prologue, conv state, two prep kernels, chain kernel)",
                     "tokens_per_s_per_layer": round(PREFILL_T / t_pf, 1), "ms_per_call": round(t_pf * 1e3, 4),
                     "tflops": round(pf_tflops, 3), "flop_per_token": FLOP_PER_TOKEN,
                     "peak_tflops": peaks["bf16_tflops"], "frac_tc": round(pf_tflops / peaks["bf16_tflops"], 4),
