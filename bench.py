@@ -439,10 +439,145 @@ def profile_case(args):
                           "us_per_launch": round(us, 3),
                           "gbs": round((B * SLOT_BYTES + PARAM_BYTES) / us / 1e3, 1),
                           "slices": os.environ.get("GDN_DECODE_SLICES", "auto")}))
+    elif args.case == "serving":
+        print(json.dumps(serving_measure(torch, device, args.steps, args.warmup)))
+    elif args.case == "verify":
+        for nb in (4, 64):
+            print(json.dumps(verify_measure(torch, device, args.steps, args.warmup, batch=nb)))
     else:
         t, _ = prefill_measure(torch, device, args.steps, args.warmup, seed=0, check=False)
         print(json.dumps({"case": args.case, "ms_per_call": round(1e3 * t, 4)}))
     return 0
+
+
+def verify_measure(torch, device, steps, warmup, batch=4, r=4):
+    """Speculative verify on the wide-GVA geometry (16/48 heads, d = 128, 10240
+    conv channels): `batch` slots, r rows each, the state after every row
+    written to a snapshot slot, then a commit of a random accepted count.
+    Timing only: N(0, 1) inputs drawn on the device from a fixed seed."""
+    from hybrid_gated_deltanet_gb300 import binding as gb
+    from hybrid_gated_deltanet_gb300 import synth
+    geom = synth.WIDE_GVA
+    hv, dd, cch = geom.n_v_heads, geom.d_k, geom.conv_channels
+    cfg = gb.Config(geom.n_k_heads, hv, dd, dd, geom.d_conv, chunk=64, act_dtype=gb.BF16)
+    r_ = synth.rng_for(3, 7)
+    p = synth.make_params(geom, r_, synth.BF16)
+    prm = gb.Params(conv_w=_dev(p["conv_w"], torch, device), A_log=_dev(p["A_log"], torch, device),
+                    norm_w=_dev(p["norm_w"], torch, device))
+    n_slots = 2 * batch * (1 + r)
+    perm = r_.permutation(n_slots).astype(np.int32)
+    slots = torch.from_numpy(perm[:batch].copy()).to(device)
+    snaps = torch.from_numpy(perm[batch:batch * (1 + r)].reshape(batch, r).copy()).to(device)
+    accept = torch.from_numpy(r_.integers(0, r + 1, size=batch).astype(np.int32)).to(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(3)
+    bf = torch.bfloat16
+    S = 0.1 * torch.randn((n_slots, hv, dd, dd), generator=g, device=device)
+    Cp = (0.1 * torch.randn((n_slots, geom.d_conv - 1, cch), generator=g, device=device)).to(bf)
+    x = torch.randn((batch, r, cch), generator=g, device=device).to(bf)
+    z = torch.randn((batch, r, hv * dd), generator=g, device=device).to(bf)
+    a = torch.randn((batch, r, hv), generator=g, device=device).to(bf)
+    b = torch.randn((batch, r, hv), generator=g, device=device).to(bf)
+    y = torch.empty((batch, r, hv * dd), dtype=bf, device=device)
+    stream = torch.cuda.Stream()
+
+    def verify():
+        gb.gdn_verify_rows(cfg, prm, x, z, a, b, Cp, S, slots, snaps, y, stream=stream)
+
+    def commit():
+        gb.gdn_commit_rows(cfg, Cp, S, slots, snaps, accept, stream=stream)
+
+    def timed(fn, n):
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    n = max(20, steps)
+    t_v = timed(verify, n)
+    t_c = timed(commit, n)
+    state, conv = hv * dd * dd * 4, (geom.d_conv - 1) * cch * 2
+    row_io = cch * 2 + 2 * hv * dd * 2 + 2 * hv * 2  # x, z, y, a, b of one row
+    v_bytes = batch * ((1 + r) * (state + conv) + r * row_io)
+    return {"case": "verify", "geometry": "16/48 heads, d = 128, 10240 conv channels, bf16, fp32 state",
+            "batch": batch, "rows": r, "verify_us": round(1e6 * t_v, 2),
+            "verify_gbs": round(v_bytes / t_v / 1e9, 1), "verify_bytes": v_bytes,
+            "commit_us": round(1e6 * t_c, 2)}
+
+
+def serving_measure(torch, device, steps, warmup, n_seq=20, pool=512, batch=256):
+    """The serving mix: one varlen prefill of n_seq sequences with lengths
+    log-uniform in [500, 30000] into a pool of fp32 states, then decode steps of
+    `batch` slots drawn at random from the same pool.  Timing only: inputs are
+    N(0, 1) drawn on the device from a fixed seed (the parity of both paths is
+    covered by the tests)."""
+    from hybrid_gated_deltanet_gb300 import binding as gb
+    from hybrid_gated_deltanet_gb300 import synth
+    r = synth.rng_for(4, 0)
+    lengths = synth.log_uniform_lengths(r, n_seq, 500, 30000)
+    n_tok = int(sum(lengths))
+    cfg = gb.Config(*GEOM_ARGS, chunk=64, act_dtype=gb.BF16)
+    p = synth.make_params(synth.QWEN35_4B, r, synth.BF16)
+    prm = gb.Params(conv_w=_dev(p["conv_w"], torch, device), A_log=_dev(p["A_log"], torch, device),
+                    norm_w=_dev(p["norm_w"], torch, device))
+    g = torch.Generator(device=device)
+    g.manual_seed(4)
+    bf = torch.bfloat16
+    x = torch.randn((n_tok, 8192), generator=g, device=device).to(bf)
+    z = torch.randn((n_tok, 4096), generator=g, device=device).to(bf)
+    a = torch.randn((n_tok, 32), generator=g, device=device).to(bf)
+    b = torch.randn((n_tok, 32), generator=g, device=device).to(bf)
+    y = torch.empty((n_tok, 4096), dtype=bf, device=device)
+    S = torch.zeros((pool, 32, 128, 128), device=device)
+    Cp = torch.zeros((pool, 3, 8192), dtype=bf, device=device)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32, device=device)
+    pf_slots = torch.from_numpy(r.permutation(pool)[:n_seq].astype(np.int32)).to(device)
+    ws = torch.empty(gb.gdn_workspace_size(cfg, gb.OP_VARLEN_PREFILL, n_tok, n_seq), dtype=torch.uint8, device=device)
+    dec_slots = torch.from_numpy(r.permutation(pool)[:batch].astype(np.int32)).to(device)
+    dx = torch.randn((batch, 8192), generator=g, device=device).to(bf)
+    dz = torch.randn((batch, 4096), generator=g, device=device).to(bf)
+    da = torch.randn((batch, 32), generator=g, device=device).to(bf)
+    db = torch.randn((batch, 32), generator=g, device=device).to(bf)
+    dy = torch.empty((batch, 4096), dtype=bf, device=device)
+    stream = torch.cuda.Stream()
+
+    def prefill():
+        gb.gdn_varlen_prefill(cfg, prm, x, z, a, b, cu, pf_slots, None, Cp, S, y, ws, stream=stream)
+
+    def decode():
+        gb.gdn_decode_step(cfg, prm, dx, dz, da, db, Cp, S, dec_slots, dy, stream=stream)
+
+    def timed(fn, n):
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    t_pf = timed(prefill, max(1, steps))
+    t_dec = timed(decode, max(1, steps) * 20)
+    dec_bytes = batch * SLOT_BYTES + PARAM_BYTES
+    return {"case": "serving", "n_seq": n_seq, "lengths": lengths, "tokens": n_tok,
+            "prefill_ms": round(1e3 * t_pf, 3), "prefill_tokens_per_s_per_layer": round(n_tok / t_pf, 1),
+            "prefill_tflops": round(FLOP_PER_TOKEN * n_tok / t_pf / 1e12, 2),
+            "longest_seq_chunks": int(max(lengths) + 63) // 64,
+            "decode_batch": batch, "decode_us": round(1e6 * t_dec, 2),
+            "decode_gbs": round(dec_bytes / t_dec / 1e9, 1)}
 
 
 def reference_arm(args):
@@ -560,7 +695,7 @@ def main():
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--batch", type=int, default=64, help="slots of the decode-small case")
-    ap.add_argument("--case", default="full", choices=["full", "decode-small", "prefill-small"],
+    ap.add_argument("--case", default="full", choices=["full", "decode-small", "prefill-small", "serving", "verify"],
                     help="small cases for ncu captures")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-prefill-tokens", type=int, default=8192)
