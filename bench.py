@@ -441,6 +441,8 @@ def profile_case(args):
                           "slices": os.environ.get("GDN_DECODE_SLICES", "auto")}))
     elif args.case == "serving":
         print(json.dumps(serving_measure(torch, device, args.steps, args.warmup)))
+    elif args.case == "ckpt":
+        print(json.dumps(ckpt_measure(torch, device, args.steps, args.warmup)))
     elif args.case == "verify":
         for nb in (4, 64):
             print(json.dumps(verify_measure(torch, device, args.steps, args.warmup, batch=nb)))
@@ -448,6 +450,62 @@ def profile_case(args):
         t, _ = prefill_measure(torch, device, args.steps, args.warmup, seed=0, check=False)
         print(json.dumps({"case": args.case, "ms_per_call": round(1e3 * t, 4)}))
     return 0
+
+
+def ckpt_measure(torch, device, steps, warmup, every=1024):
+    """The T = 8192 prefill with a prefix snapshot every `every` tokens (into pool
+    slots) against the same prefill without snapshots (timing only)."""
+    from hybrid_gated_deltanet_gb300 import binding as gb
+    from hybrid_gated_deltanet_gb300 import synth
+    r = synth.rng_for(2, 5)
+    cfg = gb.Config(*GEOM_ARGS, chunk=64, act_dtype=gb.BF16)
+    p = synth.make_params(synth.QWEN35_4B, r, synth.BF16)
+    prm = gb.Params(conv_w=_dev(p["conv_w"], torch, device), A_log=_dev(p["A_log"], torch, device),
+                    norm_w=_dev(p["norm_w"], torch, device))
+    g = torch.Generator(device=device)
+    g.manual_seed(5)
+    bf, T = torch.bfloat16, PREFILL_T
+    x = torch.randn((T, 8192), generator=g, device=device).to(bf)
+    z = torch.randn((T, 4096), generator=g, device=device).to(bf)
+    a = torch.randn((T, 32), generator=g, device=device).to(bf)
+    b = torch.randn((T, 32), generator=g, device=device).to(bf)
+    y = torch.empty((T, 4096), dtype=bf, device=device)
+    n_ck = T // every
+    S = torch.zeros((1 + n_ck, 32, 128, 128), device=device)
+    Cp = torch.zeros((1 + n_ck, 3, 8192), dtype=bf, device=device)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=device)
+    sl = torch.zeros(1, dtype=torch.int32, device=device)
+    off = torch.tensor([0, n_ck], dtype=torch.int32, device=device)
+    ck = torch.arange(1, 1 + n_ck, dtype=torch.int32, device=device)
+    ws = torch.empty(gb.gdn_workspace_size(cfg, gb.OP_VARLEN_PREFILL, T, 1), dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream()
+
+    def plain():
+        gb.gdn_varlen_prefill(cfg, prm, x, z, a, b, cu, sl, None, Cp, S, y, ws, stream=stream)
+
+    def snap():
+        gb.gdn_varlen_prefill_ckpt(cfg, prm, x, z, a, b, cu, sl, None, Cp, S, y, every, off, ck, ws, stream=stream)
+
+    def timed(fn, n):
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    n = max(10, steps)
+    t0, t1 = timed(plain, n), timed(snap, n)
+    return {"case": "ckpt", "tokens": T, "every": every, "snapshots": n_ck,
+            "snapshot_bytes": n_ck * (32 * 128 * 128 * 4 + 3 * 8192 * 2),
+            "ms_plain": round(1e3 * t0, 4), "ms_with_snapshots": round(1e3 * t1, 4),
+            "overhead_pct": round(100 * (t1 / t0 - 1), 2)}
 
 
 def verify_measure(torch, device, steps, warmup, batch=4, r=4):
@@ -695,7 +753,7 @@ def main():
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--batch", type=int, default=64, help="slots of the decode-small case")
-    ap.add_argument("--case", default="full", choices=["full", "decode-small", "prefill-small", "serving", "verify"],
+    ap.add_argument("--case", default="full", choices=["full", "decode-small", "prefill-small", "serving", "verify", "ckpt"],
                     help="small cases for ncu captures")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-prefill-tokens", type=int, default=8192)

@@ -113,6 +113,8 @@ def load() -> ctypes.CDLL:
             "gdn_chunk_prefill": [cfgp, prmp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, sz, vp],
             "gdn_chunk_prefill_noalloc": [cfgp, prmp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp],
             "gdn_varlen_prefill": [cfgp, prmp, vp, vp, vp, vp, vp, i32, i64, vp, vp, vp, vp, i32, vp, vp, sz, vp],
+            "gdn_varlen_prefill_ckpt": [cfgp, prmp, vp, vp, vp, vp, vp, i32, i64, vp, vp, vp, vp, i32, vp, i32, vp,
+                                        vp, vp, sz, vp],
         }
         for name, args in sigs.items():
             fn = getattr(lib, name)
@@ -223,3 +225,16 @@ def gdn_varlen_prefill(cfg: Config, prm: Params, x, z, a, b, cu_seqlens, slot_id
                                      slot_idx.numel(), x.shape[0], _p(slot_idx), _p(has_init), _p(conv_pool),
                                      _p(state_pool), state_pool.shape[0], _p(y), _p(workspace), ws_bytes,
                                      _stream(stream)))
+
+
+def gdn_varlen_prefill_ckpt(cfg: Config, prm: Params, x, z, a, b, cu_seqlens, slot_idx, has_init, conv_pool,
+                            state_pool, y, ckpt_every: int, ckpt_offset, ckpt_slots, workspace, stream=None):
+    """gdn_varlen_prefill plus prefix snapshots: the state after (k+1)*ckpt_every
+    tokens of sequence s goes to pool slot ckpt_slots[ckpt_offset[s] + k]."""
+    c, p = cfg.c(), prm.c()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().gdn_varlen_prefill_ckpt(ctypes.byref(c), ctypes.byref(p), _p(x), _p(z), _p(a), _p(b),
+                                          _p(cu_seqlens), slot_idx.numel(), x.shape[0], _p(slot_idx), _p(has_init),
+                                          _p(conv_pool), _p(state_pool), state_pool.shape[0], _p(y), int(ckpt_every),
+                                          _p(ckpt_offset), _p(ckpt_slots), _p(workspace), ws_bytes,
+                                          _stream(stream)))

@@ -316,4 +316,45 @@ gdn_status gdn_varlen_prefill(const gdn_config* cfg, const gdn_params* prm, cons
     return prefill_common(cfg, prm, job, stream, "gdn_varlen_prefill");
 }
 
+gdn_status gdn_varlen_prefill_ckpt(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* z,
+                                   const void* a, const void* b, const int32_t* cu_seqlens, int32_t n_seq,
+                                   int64_t n_tokens, const int32_t* slot_idx, const uint8_t* has_init,
+                                   void* conv_pool, float* state_pool, int32_t n_slots, void* y, int32_t ckpt_every,
+                                   const int32_t* ckpt_offset, const int32_t* ckpt_slots, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+    if (n_seq < 0 || n_seq > 65535) return fail(GDN_ERR_RANGE, "n_seq: found %d, required 0..65535", n_seq);
+    if (n_slots < 1) return fail(GDN_ERR_RANGE, "n_slots: found %d, required >= 1", n_slots);
+    {
+        gdn::Geom g;
+        gdn_status st = make_geom(cfg, true, &g);
+        if (st) return st;
+        if (ckpt_every <= 0 || ckpt_every % cfg->chunk != 0)
+            return fail(GDN_ERR_RANGE, "ckpt_every: found %d, required a positive multiple of chunk = %d", ckpt_every,
+                        cfg->chunk);
+    }
+    if (n_seq == 0) {
+        if (n_tokens != 0)
+            return fail(GDN_ERR_RANGE, "n_tokens: found %lld with n_seq = 0, required 0", (long long)n_tokens);
+        return ok();
+    }
+    GDN_REQUIRE_PTR_A(cu_seqlens, "cu_seqlens", 4u);
+    GDN_REQUIRE_PTR_A(slot_idx, "slot_idx", 4u);
+    GDN_OPTIONAL_PTR_A(has_init, "has_init", 1u);
+    GDN_REQUIRE_PTR(conv_pool, "conv_pool");
+    GDN_REQUIRE_PTR(state_pool, "state_pool");
+    GDN_REQUIRE_PTR_A(ckpt_offset, "ckpt_offset", 4u);
+    GDN_REQUIRE_PTR_A(ckpt_slots, "ckpt_slots", 4u);
+    GDN_OPTIONAL_PTR(workspace, "workspace");
+    gdn::PrefillJob job = {};
+    job.x = x; job.z = z; job.a = a; job.b = b; job.y = y;
+    job.n_tokens = n_tokens;
+    job.n_seq = n_seq;
+    job.cu_seqlens = cu_seqlens;
+    job.slot_idx = slot_idx; job.has_init = has_init;
+    job.state_pool = state_pool; job.conv_pool = conv_pool; job.n_slots = n_slots;
+    job.ckpt_every = ckpt_every; job.ckpt_offset = ckpt_offset; job.ckpt_slots = ckpt_slots;
+    job.workspace = workspace; job.ws_bytes = ws_bytes;
+    return prefill_common(cfg, prm, job, stream, "gdn_varlen_prefill_ckpt");
+}
+
 }  // extern "C"

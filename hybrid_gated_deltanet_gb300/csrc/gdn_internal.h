@@ -75,6 +75,11 @@ struct PrefillJob {
     void* conv_final;
     void* workspace;
     size_t ws_bytes;
+    // varlen snapshots every ckpt_every tokens (0: none) into pool slots
+    // ckpt_slots[ckpt_offset[s] + k]
+    int32_t ckpt_every;
+    const int32_t* ckpt_offset;
+    const int32_t* ckpt_slots;
 };
 size_t prefill_workspace_bytes(const Geom& g, int64_t n_tokens, int n_seq);
 cudaError_t launch_prefill(const Geom& g, const LayerParams& prm, const PrefillJob& job,

@@ -175,6 +175,23 @@ __device__ __forceinline__ bool slot_chunk(const PrefillJob& J, int64_t cs, int6
     return true;
 }
 
+// pool slot of snapshot k of sequence s (the state after its first
+// (k+1)*ckpt_every tokens), or -1 when none is to be written there
+__device__ __forceinline__ int ckpt_slot(const PrefillJob& J, int s, int64_t k) {
+    if (J.ckpt_every <= 0 || !J.ckpt_offset) return -1;
+    const int64_t o0 = J.ckpt_offset[s], o1 = J.ckpt_offset[s + 1];
+    if (k < 0 || k >= o1 - o0) return -1;
+    const int slot = J.ckpt_slots[o0 + k];
+    return (slot >= 0 && slot < J.n_slots) ? slot : -1;
+}
+
+// snapshot due after tokens [start, start + done) of a sequence of T tokens: its
+// pool slot, or -1
+__device__ __forceinline__ int ckpt_after(const PrefillJob& J, int s, int64_t done, int64_t T) {
+    if (J.ckpt_every <= 0 || done > T || done % J.ckpt_every != 0) return -1;
+    return ckpt_slot(J, s, done / J.ckpt_every - 1);
+}
+
 __device__ __forceinline__ const void* seq_conv_in(const PrefillJob& J, const Geom& g, int s, int& slot_ok) {
     if (!J.cu_seqlens) {
         slot_ok = 1;
@@ -595,6 +612,30 @@ __global__ void k_conv_final(const __grid_constant__ PrefillArgs A) {
     }
 }
 
+// conv states of the prefix snapshots: the d_conv-1 raw inputs before each
+// snapshot boundary (thread = channel; grid z strides over the snapshots)
+template <typename TA>
+__global__ void k_conv_ckpt(const __grid_constant__ PrefillArgs A) {
+    using L = Act<TA>;
+    const Geom& g = A.g;
+    const PrefillJob& J = A.J;
+    const int Cch = g.C_ch, Km1 = g.K - 1;
+    const int ch = blockIdx.x * blockDim.x + threadIdx.x, s = blockIdx.y;
+    if (ch >= Cch) return;
+    int64_t start, end;
+    seq_bounds(J, s, start, end);
+    const size_t elt = g.act_bf16 ? 2 : 4;
+    for (int64_t done = (int64_t)(blockIdx.z + 1) * J.ckpt_every; done <= end - start;
+         done += (int64_t)gridDim.z * J.ckpt_every) {
+        const int ck = ckpt_slot(J, s, done / J.ckpt_every - 1);
+        if (ck < 0) continue;
+        void* dst = static_cast<char*>(J.conv_pool) + (size_t)ck * Km1 * Cch * elt;
+        for (int m = 0; m < Km1; ++m)  // (done >= chunk > d_conv - 1: all rows inside the sequence)
+            L::st(dst, (size_t)m * Cch + ch, L::ld(J.x, (size_t)(start + done - Km1 + m) * Cch + ch));
+    }
+}
+
+
 // ---------------------------------------------------------------------------
 // 3. chunk kernel
 // ---------------------------------------------------------------------------
@@ -909,6 +950,15 @@ __global__ void __launch_bounds__(kChunkThreads, 1) k_chunk(const __grid_constan
                 yv = yv * rsqrtf(tot / (float)D + g.norm_eps) * L::ld(A.p.norm_w, dv) * siluf_(zz);
             }
             L::st(J.y, tok * (size_t)Hv * D + (size_t)j * D + dv, yv);
+        }
+        const int ck = ckpt_after(J, seq, (int64_t)(ci + 1) * C, T);  // (uniform over the CTA)
+        if (ck >= 0) {
+            __syncthreads();  // the state update is complete
+            float* dst = J.state_pool + ((size_t)ck * Hv + j) * D * D;
+            for (int i = tid; i < DV * D; i += kChunkThreads) {
+                const int r = i / D, c = i % D;
+                dst[(size_t)(s_idx * DV + r) * D + c] = Ss[r * ldk + c];
+            }
         }
     }
     __syncthreads();
@@ -1587,6 +1637,12 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         tc::ld16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
 #pragma unroll
         for (int c = 0; c < 16; ++c) tc::st_elem(S0s, DV, hf * 16 + c, dS, s16[c]);
+        const int ck = ckpt_after(J, seq, (int64_t)(ci + 1) * C, T);
+        if (ck >= 0) {  // a prefix snapshot ends with this chunk
+            float* dst = J.state_pool + ((size_t)ck * Hv + j) * D * D;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) dst[(size_t)(s_idx * DV + hf * 16 + c) * D + dS] = s16[c];
+        }
         if (ci + 1 < n_chunks) {
             issue_ra(ci + 1);
             wait_bar(barC, par ^ 1u);  // gates of the next chunk: S^T *= e^gamma_C in TMEM
@@ -1736,6 +1792,11 @@ cudaError_t launch_prefill_t(const Geom& g, const LayerParams& p, const PrefillJ
         const size_t total = (size_t)J.n_seq * g.C_ch;
         const int blocks = (int)std::min<size_t>((total + 255) / 256, 152 * 8);
         k_conv_final<TA><<<blocks, 256, 0, st>>>(A);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (J.ckpt_every > 0 && J.n_tokens > 0) {
+        k_conv_ckpt<TA><<<dim3((unsigned)((g.C_ch + 255) / 256), (unsigned)J.n_seq, 16u), 256, 0, st>>>(A);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

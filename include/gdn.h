@@ -190,6 +190,35 @@ gdn_status gdn_varlen_prefill(const gdn_config* cfg, const gdn_params* prm, cons
                               float* state_pool, int32_t n_slots, void* y, void* workspace,
                               size_t ws_bytes, void* stream);
 
+/* gdn_varlen_prefill that also leaves snapshots of the recurrent state every
+ * ckpt_every tokens of each sequence, for prefix reuse ("Hybrid transformers
+ * under load ...", braintools.ru, section 3: a request that shares a prefix
+ * with an earlier one resumes from a copy of the state saved at the prefix
+ * end, since the live state has moved on; section 4.2: a snapshot at every
+ * block boundary, state and conv state of every layer).
+ *   Snapshot k (k = 0, 1, ...) of sequence s is the state after its first
+ *   (k+1)*ckpt_every tokens (an initial state read from the pool counts as the
+ *   state before token 0).  It goes to pool slot ckpt_slots[ckpt_offset[s] + k]
+ *   for k < ckpt_offset[s+1] - ckpt_offset[s] and k < floor(L_s / ckpt_every);
+ *   later boundaries are not written.  The slot receives what a slot holds
+ *   after a prefill ending there -- the fp32 state of every v-head and the conv
+ *   state (the d_conv-1 raw inputs before the boundary) -- so a decode, verify
+ *   or prefill can resume from it.
+ *   ckpt_every: a positive multiple of cfg->chunk, else GDN_ERR_RANGE.
+ *   ckpt_offset int32 [n_seq+1] (device, non-decreasing), ckpt_slots int32
+ *   [ckpt_offset[n_seq]] (device).  Snapshot slots must differ from one another
+ *   and from every slot_idx[s] (the sequences' own slots are read while the
+ *   snapshots are written); indices outside [0, n_slots) are skipped.
+ *   All other arguments, the workspace and the errors are gdn_varlen_prefill's. */
+gdn_status gdn_varlen_prefill_ckpt(const gdn_config* cfg, const gdn_params* prm, const void* x,
+                                   const void* z, const void* a, const void* b,
+                                   const int32_t* cu_seqlens, int32_t n_seq, int64_t n_tokens,
+                                   const int32_t* slot_idx, const uint8_t* has_init,
+                                   void* conv_pool, float* state_pool, int32_t n_slots, void* y,
+                                   int32_t ckpt_every, const int32_t* ckpt_offset,
+                                   const int32_t* ckpt_slots, void* workspace, size_t ws_bytes,
+                                   void* stream);
+
 /* Chunked prefill for callers that cannot allocate device memory.  The pages
  * have no counterpart to this entry point: it exists for callers that cannot
  * call cudaMalloc when they run a prefill -- a host runtime that owns the

@@ -142,6 +142,23 @@ def test_varlen_validation(lib):
     assert st == 0
 
 
+def test_varlen_ckpt_validation(lib):
+    """gdn_varlen_prefill_ckpt: snapshot spacing must be a positive multiple of the
+    chunk; the offset and slot arrays are required."""
+    cfg = _cfg()
+    prm = _prm()
+
+    def call(every, off=FAKE, slots=FAKE):
+        return lib.gdn_varlen_prefill_ckpt(ctypes.byref(cfg), ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, FAKE, 2, 100,
+                                           FAKE, None, FAKE, FAKE, 8, FAKE, every, off, slots, FAKE, 1 << 30, None)
+
+    assert call(0) == -5 and "ckpt_every: found 0, required a positive multiple of chunk = 64" in _err(lib)
+    assert call(96) == -5 and "found 96" in _err(lib)
+    assert call(128, off=None) == -1 and "ckpt_offset" in _err(lib)
+    assert call(128, slots=None) == -1 and "ckpt_slots" in _err(lib)
+    assert call(128, off=FAKE + 2) == -4 and "ckpt_offset" in _err(lib)
+
+
 def test_binding_raises_with_message(lib):
     cfg = gb.Config(16, 30, 128, 128)
     with pytest.raises(gb.GdnError, match="GDN_ERR_SHAPE: cfg.n_v_heads: found 30"):
