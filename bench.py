@@ -559,16 +559,27 @@ def verify_measure(torch, device, steps, warmup, batch=4, r=4):
         e1.synchronize()
         return e0.elapsed_time(e1) / 1e3 / n
 
+    def verify_nosnap():
+        gb.gdn_verify_rows_nosnap(cfg, prm, x, z, a, b, Cp, S, slots, y, stream=stream)
+
+    def commit_recompute():
+        gb.gdn_commit_rows_recompute(cfg, prm, x, a, b, Cp, S, slots, accept, stream=stream)
+
     n = max(20, steps)
     t_v = timed(verify, n)
     t_c = timed(commit, n)
+    t_vn = timed(verify_nosnap, n)
+    t_cr = timed(commit_recompute, n)
     state, conv = hv * dd * dd * 4, (geom.d_conv - 1) * cch * 2
     row_io = cch * 2 + 2 * hv * dd * 2 + 2 * hv * 2  # x, z, y, a, b of one row
     v_bytes = batch * ((1 + r) * (state + conv) + r * row_io)
     return {"case": "verify", "geometry": "16/48 heads, d = 128, 10240 conv channels, bf16, fp32 state",
             "batch": batch, "rows": r, "verify_us": round(1e6 * t_v, 2),
             "verify_gbs": round(v_bytes / t_v / 1e9, 1), "verify_bytes": v_bytes,
-            "commit_us": round(1e6 * t_c, 2)}
+            "commit_us": round(1e6 * t_c, 2),
+            "recompute_variant": {"verify_us": round(1e6 * t_vn, 2), "commit_us": round(1e6 * t_cr, 2),
+                                  "verify_plus_commit_us": round(1e6 * (t_vn + t_cr), 2),
+                                  "snapshot_verify_plus_commit_us": round(1e6 * (t_v + t_c), 2)}}
 
 
 def serving_measure(torch, device, steps, warmup, n_seq=20, pool=512, batch=256):

@@ -113,6 +113,8 @@ def load() -> ctypes.CDLL:
             "gdn_chunk_prefill": [cfgp, prmp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp, sz, vp],
             "gdn_chunk_prefill_noalloc": [cfgp, prmp, vp, vp, vp, vp, i64, vp, vp, vp, vp, vp, vp],
             "gdn_varlen_prefill": [cfgp, prmp, vp, vp, vp, vp, vp, i32, i64, vp, vp, vp, vp, i32, vp, vp, sz, vp],
+            "gdn_verify_rows_nosnap": [cfgp, prmp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp, vp],
+            "gdn_commit_rows_recompute": [cfgp, prmp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, vp],
             "gdn_varlen_prefill_ckpt": [cfgp, prmp, vp, vp, vp, vp, vp, i32, i64, vp, vp, vp, vp, i32, vp, i32, vp,
                                         vp, vp, sz, vp],
         }
@@ -238,3 +240,22 @@ def gdn_varlen_prefill_ckpt(cfg: Config, prm: Params, x, z, a, b, cu_seqlens, sl
                                           _p(conv_pool), _p(state_pool), state_pool.shape[0], _p(y), int(ckpt_every),
                                           _p(ckpt_offset), _p(ckpt_slots), _p(workspace), ws_bytes,
                                           _stream(stream)))
+
+
+def gdn_verify_rows_nosnap(cfg: Config, prm: Params, x, z, a, b, conv_pool, state_pool, slot_idx, y, stream=None):
+    """x [B, r, C_ch] ...: y of every row; the pools are not written."""
+    c, p = cfg.c(), prm.c()
+    B, r = x.shape[0], x.shape[1]
+    _check(load().gdn_verify_rows_nosnap(ctypes.byref(c), ctypes.byref(p), _p(x), _p(z), _p(a), _p(b),
+                                         _p(conv_pool), _p(state_pool), _p(slot_idx), B, r, state_pool.shape[0],
+                                         _p(y), _stream(stream)))
+
+
+def gdn_commit_rows_recompute(cfg: Config, prm: Params, x, a, b, conv_pool, state_pool, slot_idx, accepted,
+                              stream=None):
+    """Applies the first accepted[b] rows of x/a/b [B, r, ...] to slot_idx[b] in place."""
+    c, p = cfg.c(), prm.c()
+    B, r = x.shape[0], x.shape[1]
+    _check(load().gdn_commit_rows_recompute(ctypes.byref(c), ctypes.byref(p), _p(x), _p(a), _p(b), _p(conv_pool),
+                                            _p(state_pool), _p(slot_idx), _p(accepted), B, r, state_pool.shape[0],
+                                            _stream(stream)))

@@ -190,7 +190,8 @@ gdn_status gdn_conv_state_update(const gdn_config* cfg, const gdn_params* prm, c
 static gdn_status rows_common(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* z,
                               const void* a, const void* b, void* conv_pool, float* state_pool,
                               const int32_t* slot_idx, const int32_t* snap_idx, int32_t B, int32_t r,
-                              int32_t n_slots, void* y, void* stream, const char* who) {
+                              int32_t n_slots, void* y, void* stream, const char* who, int mode = 0,
+                              const int32_t* accepted = nullptr) {
     gdn::Geom g;
     gdn::LayerParams p;
     gdn_status st = make_geom(cfg, false, &g);
@@ -201,14 +202,17 @@ static gdn_status rows_common(const gdn_config* cfg, const gdn_params* prm, cons
     if (B == 0) return ok();
     if ((st = make_params(prm, g, true, &p))) return st;
     GDN_REQUIRE_PTR(x, "x");  // x and z are staged with bulk copies: 16-byte aligned
-    if (!(g.flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR(z, "z");
+    if (!(g.flags & GDN_FLAG_NO_OUTNORM) && mode != 2) GDN_REQUIRE_PTR(z, "z");
     GDN_REQUIRE_PTR_A(a, "a", g.act_bf16 ? 2u : 4u);
     GDN_REQUIRE_PTR_A(b, "b", g.act_bf16 ? 2u : 4u);
     GDN_REQUIRE_PTR(conv_pool, "conv_pool");
     GDN_REQUIRE_PTR(state_pool, "state_pool");
     GDN_REQUIRE_PTR_A(slot_idx, "slot_idx", 4u);
-    GDN_REQUIRE_PTR_A(y, "y", g.act_bf16 ? 2u : 4u);
+    if (mode != 2) GDN_REQUIRE_PTR_A(y, "y", g.act_bf16 ? 2u : 4u);
+    else GDN_REQUIRE_PTR_A(accepted, "accepted", 4u);
     gdn::RowsJob job{x, z, a, b, conv_pool, state_pool, slot_idx, snap_idx, y, B, r, n_slots};
+    job.mode = mode;
+    job.accepted = accepted;
     return cuda_status(gdn::launch_rows(g, p, job, (cudaStream_t)stream), who);
 }
 
@@ -225,6 +229,21 @@ gdn_status gdn_verify_rows(const gdn_config* cfg, const gdn_params* prm, const v
     if (B > 0) GDN_REQUIRE_PTR_A(snap_idx, "snap_idx", 4u);
     return rows_common(cfg, prm, x, z, a, b, conv_pool, state_pool, slot_idx, snap_idx, B, r, n_slots, y, stream,
                        "gdn_verify_rows");
+}
+
+gdn_status gdn_verify_rows_nosnap(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* z,
+                                  const void* a, const void* b, void* conv_pool, float* state_pool,
+                                  const int32_t* slot_idx, int32_t B, int32_t r, int32_t n_slots, void* y,
+                                  void* stream) {
+    return rows_common(cfg, prm, x, z, a, b, conv_pool, state_pool, slot_idx, nullptr, B, r, n_slots, y, stream,
+                       "gdn_verify_rows_nosnap", 1);
+}
+
+gdn_status gdn_commit_rows_recompute(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* a,
+                                     const void* b, void* conv_pool, float* state_pool, const int32_t* slot_idx,
+                                     const int32_t* accepted, int32_t B, int32_t r, int32_t n_slots, void* stream) {
+    return rows_common(cfg, prm, x, nullptr, a, b, conv_pool, state_pool, slot_idx, nullptr, B, r, n_slots, nullptr,
+                       stream, "gdn_commit_rows_recompute", 2, accepted);
 }
 
 gdn_status gdn_commit_rows(const gdn_config* cfg, void* conv_pool, float* state_pool, const int32_t* slot_idx,

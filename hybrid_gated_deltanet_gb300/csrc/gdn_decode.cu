@@ -116,7 +116,8 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
     const int r = J.r;
     const int crank = (int)cluster.block_rank();
     const bool raw = g.flags & kFlagRawQKV;
-    const bool outnorm = !(g.flags & kFlagNoOutNorm);
+    const int mode = J.mode;
+    const bool outnorm = !(g.flags & kFlagNoOutNorm) && mode != 2;  // (a commit writes no y)
     const bool direct = g.flags & kFlagGatesDirect;
     // One slice per v-head: the output norm is local and the only cluster
     // barrier orders the conv-state reads of the k-head group before its
@@ -144,6 +145,13 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
 
     const int slot = J.slot_idx[bb];
     if (slot < 0 || slot >= J.n_slots) return;  // the whole cluster shares bb
+    // rows to run: all r, or for a commit by recompute the accepted ones
+    int nr = r;
+    if (mode == 2) {
+        const int acc = J.accepted[bb];
+        nr = acc < 0 ? 0 : (acc > r ? r : acc);
+        if (nr == 0) return;  // nothing accepted: the slot keeps its state (whole cluster)
+    }
 
     // the CTA's channels: q and k of k-head h, the slice of v of v-head j
     const int ch_q = h * D, ch_k = Hk * D + h * D, ch_v = 2 * Hk * D + j * D + s * RPC;
@@ -217,7 +225,7 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
     };
     const int col4 = lane % LPR, rsub = lane / LPR;
     bool s_ok = true;
-    for (int t = 0; t < r; ++t) {
+    for (int t = 0; t < nr; ++t) {
         const size_t rowx = (size_t)bb * r + t;
         float sq = 0.f, sk = 0.f, sqk = 0.f;
         if (ok) {
@@ -361,7 +369,7 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
 
     // ---- state back (decode: in place, one bulk store) and the output ---------
     fence_proxy_async_smem();
-    for (int t = warp; t < r; t += nwarp) {
+    for (int t = warp; t < nr; t += nwarp) {
         float ss = 0.f;
         for (int rr = lane; rr < RPC; rr += 32) {
             const float o = obuf[t * RPC + rr];
@@ -372,13 +380,13 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
     }
     __syncthreads();
     if (!whole_head) cluster_arrive_release();  // partial sums and conv-state reads are done
-    if (tid == 0 && ok && !J.snap_idx) {
+    if (tid == 0 && ok && !J.snap_idx && mode != 1) {  // decode, commit: the state in place
         bulk_s2g(Sg, Sb, RPC * D * 4);
         bulk_commit();
     }
     if (!whole_head) cluster_wait_acquire();
 
-    if (ok) {
+    if (ok && mode != 2) {
         for (int idx = tid; idx < r * RPC; idx += nthr) {
             const int t = idx / RPC, rr = idx % RPC;
             const size_t rowx = (size_t)bb * r + t;
@@ -397,13 +405,13 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
         }
     }
     if (whole_head) cluster_wait_acquire();  // every CTA of the group has read its conv state
-    if (ok) {
+    if (ok && mode != 1) {
         // conv state: the last K-1 raw inputs, copied bit for bit
         TA* cpool = static_cast<TA*>(J.conv_pool);
         auto roll = [&](int lc, int ch) {
             auto val = [&](int p) -> TA { return p < Km1 ? cs[p * NCH + lc] : xs[(p - Km1) * NCH + lc]; };
             if (!J.snap_idx) {
-                for (int m = 0; m < Km1; ++m) cpool[((size_t)slot * Km1 + m) * C + ch] = val(r + m);
+                for (int m = 0; m < Km1; ++m) cpool[((size_t)slot * Km1 + m) * C + ch] = val(nr + m);
             } else {
                 for (int t = 0; t < r; ++t) {
                     const int dst = J.snap_idx[(size_t)bb * r + t];
@@ -846,7 +854,7 @@ cudaError_t launch_rows(const Geom& g, const LayerParams& p, const RowsJob& job,
     // the persistent pipelined kernel pays off once every SM has several
     // (slot, v-head) items to overlap (measured: B = 64 and 256 at the 4B
     // geometry gain 18% / 26%; B <= 16 is faster with one CTA per item)
-    if (g.D == 128 && job.r == 1 && !job.snap_idx && std::getenv("GDN_DECODE_CLUSTERED") == nullptr &&
+    if (g.D == 128 && job.r == 1 && !job.snap_idx && job.mode == 0 && std::getenv("GDN_DECODE_CLUSTERED") == nullptr &&
         std::getenv("GDN_DECODE_SLICES") == nullptr) {
         int sms = 152, dev = 0;
         if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

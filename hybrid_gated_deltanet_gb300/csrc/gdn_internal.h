@@ -33,6 +33,11 @@ struct RowsJob {
     const int32_t* snap_idx;
     void* y;
     int B, r, n_slots;
+    // 0: decode (state in place) or verify with snapshots; 1: verify that
+    // writes y only; 2: commit by recompute -- the first accepted[b] rows
+    // applied in place, no y
+    int mode = 0;
+    const int32_t* accepted = nullptr;
 };
 cudaError_t launch_rows(const Geom& g, const LayerParams& prm, const RowsJob& job, cudaStream_t st);
 

@@ -157,6 +157,32 @@ gdn_status gdn_commit_rows(const gdn_config* cfg, void* conv_pool, float* state_
                            const int32_t* accepted, int32_t B, int32_t r, int32_t n_slots,
                            void* stream);
 
+/* Verify without snapshots: the same r rows per slot as gdn_verify_rows and
+ * the same y, but no state is written anywhere -- the slot keeps its
+ * pre-verify state and conv state.  Paired with gdn_commit_rows_recompute it
+ * replaces the r snapshot writes of gdn_verify_rows + gdn_commit_rows by one
+ * more read and write of the state: 3 state volumes per slot and verify
+ * instead of 1 + r (+2 for the commit copy).  "Forge: how I wrote my own
+ * inference engine", 27 August, verifies rows in sequence and rolls back by
+ * copying a snapshot; this is the variant that recomputes instead.
+ * Arguments as gdn_verify_rows without snap_idx. */
+gdn_status gdn_verify_rows_nosnap(const gdn_config* cfg, const gdn_params* prm, const void* x,
+                                  const void* z, const void* a, const void* b, void* conv_pool,
+                                  float* state_pool, const int32_t* slot_idx, int32_t B, int32_t r,
+                                  int32_t n_slots, void* y, void* stream);
+
+/* Commit by recompute: applies the first accepted[b] of the r verified rows
+ * of entry b (x, a, b: the inputs given to gdn_verify_rows_nosnap, [B][r]...)
+ * to the state and conv state of slot_idx[b], in place; accepted[b] = 0 (or
+ * outside [0, r]: clamped) leaves the slot as it is.  The arithmetic and its
+ * order are those of the verify, so the committed state equals bit for bit
+ * the snapshot gdn_verify_rows would have written after row accepted[b].
+ * No y is produced; z is not read.  accepted int32 [B] (device). */
+gdn_status gdn_commit_rows_recompute(const gdn_config* cfg, const gdn_params* prm, const void* x,
+                                     const void* a, const void* b, void* conv_pool, float* state_pool,
+                                     const int32_t* slot_idx, const int32_t* accepted, int32_t B,
+                                     int32_t r, int32_t n_slots, void* stream);
+
 /* Chunkwise (WY / UT-transform) prefill of one sequence of T tokens
  * ("Forge ...", entry of 25-26 August: a chunked DeltaNet prefill kernel with
  * deterministic reduction).  Results equal the token-by-token evaluation

@@ -159,6 +159,20 @@ def test_varlen_ckpt_validation(lib):
     assert call(128, off=FAKE + 2) == -4 and "ckpt_offset" in _err(lib)
 
 
+def test_recompute_commit_validation(lib):
+    cfg = _cfg()
+    prm = _prm()
+    st = lib.gdn_commit_rows_recompute(ctypes.byref(cfg), ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None,
+                                       4, 4, 16, None)
+    assert st == -1 and "accepted" in _err(lib)
+    st = lib.gdn_commit_rows_recompute(ctypes.byref(cfg), ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                       4, 17, 16, None)
+    assert st == -5 and "r: found 17" in _err(lib)
+    st = lib.gdn_verify_rows_nosnap(ctypes.byref(cfg), ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                    4, 4, 16, None, None)
+    assert st == -1 and "y" in _err(lib)
+
+
 def test_binding_raises_with_message(lib):
     cfg = gb.Config(16, 30, 128, 128)
     with pytest.raises(gb.GdnError, match="GDN_ERR_SHAPE: cfg.n_v_heads: found 30"):
