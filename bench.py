@@ -257,32 +257,67 @@ def time_decode(torch, cfg, layers, steps, warmup, use_graph=True):
 
 def time_decode_e2e(torch, cfg, layers, steps, warmup):
     """Same step through the public API, with each step's inputs copied in from
-    pinned host memory and its outputs copied back, inside the timed region."""
+    pinned host memory and its outputs copied back, inside the timed region.
+    Three streams pipeline it: layer l's inputs are copied in on a copy stream
+    once the previous step's kernel for layer l has read its buffers, layer l
+    runs on the compute stream once its inputs have landed and its previous y
+    has been read out, and y goes back on a third stream.  The timed region
+    ends after the last read-back."""
     from hybrid_gated_deltanet_gb300 import binding as gb
     stream = torch.cuda.Stream()
-    hin = [{k: L[k].cpu().pin_memory() for k in ("x", "z", "a", "b")} for L in layers]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    # each layer's x, z, a, b packed into one pinned host buffer and one device
+    # buffer (16-byte aligned views): one copy in per layer
+    keys = ("x", "z", "a", "b")
+    packs = []
+    for L in layers:
+        sizes = [L[k].numel() for k in keys]
+        dbuf = torch.empty(sum(sizes), dtype=L["x"].dtype, device=L["x"].device)
+        views, o = {}, 0
+        for k, n_el in zip(keys, sizes):
+            views[k] = dbuf[o:o + n_el].view(L[k].shape)
+            views[k].copy_(L[k])
+            o += n_el
+        packs.append((dbuf, views, dbuf.cpu().pin_memory()))
     hout = [torch.empty(L["y"].shape, dtype=L["y"].dtype, pin_memory=True) for L in layers]
-    h2d = sum(t.numel() * t.element_size() for d in hin for t in d.values())
+    h2d = sum(hb.numel() * hb.element_size() for _, _, hb in packs)
     d2h = sum(t.numel() * t.element_size() for t in hout)
+    n = len(layers)
+    e_in = [torch.cuda.Event() for _ in range(n)]    # inputs of layer l landed
+    e_k = [torch.cuda.Event() for _ in range(n)]     # kernel of layer l done
+    e_out = [torch.cuda.Event() for _ in range(n)]   # y of layer l copied out
+    for l in range(n):  # start state: nothing outstanding
+        e_k[l].record(stream)
+        e_out[l].record(s_out)
 
     def step():
-        for L, hi, ho in zip(layers, hin, hout):
-            for k in ("x", "z", "a", "b"):
-                L[k].copy_(hi[k], non_blocking=True)
-            gb.gdn_decode_step(cfg, L["prm"], L["x"], L["z"], L["a"], L["b"], L["C"], L["S"], L["slots"], L["y"],
+        for l, (L, (dbuf, v, hbuf), ho) in enumerate(zip(layers, packs, hout)):
+            s_in.wait_event(e_k[l])
+            with torch.cuda.stream(s_in):
+                dbuf.copy_(hbuf, non_blocking=True)
+            e_in[l].record(s_in)
+            stream.wait_event(e_in[l])
+            stream.wait_event(e_out[l])
+            gb.gdn_decode_step(cfg, L["prm"], v["x"], v["z"], v["a"], v["b"], L["C"], L["S"], L["slots"], L["y"],
                                stream=stream)
-            ho.copy_(L["y"], non_blocking=True)
+            e_k[l].record(stream)
+            s_out.wait_event(e_k[l])
+            with torch.cuda.stream(s_out):
+                ho.copy_(L["y"], non_blocking=True)
+            e_out[l].record(s_out)
 
-    with torch.cuda.stream(stream):
-        for _ in range(warmup):
-            step()
+    for _ in range(warmup):
+        step()
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(steps):
-            step()
-        ev1.record(stream)
+    ev0.record(stream)
+    s_in.wait_event(ev0)
+    for _ in range(steps):
+        step()
+    stream.wait_event(e_out[n - 1])  # every read-back of the last step precedes the end mark
+    for l in range(n):
+        stream.wait_event(e_out[l])
+    ev1.record(stream)
     ev1.synchronize()
     return ev0.elapsed_time(ev1) / 1e3, h2d, d2h
 

@@ -59,6 +59,17 @@ def _compare(wl, stream, B, r, geom=None, act=None, oracle_heads=None):
     others = np.setdiff1d(np.arange(S.raw.shape[0]), slots)
     np.testing.assert_array_equal(sB[others], S.f64[others])  # the recompute path touches no other slot
     if oracle_heads is not None:
+        # y of every verified row against the oracle on all r rows
+        cols = np.concatenate([np.arange(jh * geom.d_v, (jh + 1) * geom.d_v) for jh in oracle_heads])
+        yg, ys, yr = host(yb), [], []
+        for i in range(B):
+            rows = np.arange(i * r, (i + 1) * r)
+            ref = oracle.run_sequence(geom, tok["x"].f64[rows], tok["z"].f64[rows], tok["a"].f64[rows],
+                                      tok["b"].f64[rows], s0=S.f64[slots[i]], conv0=CS.f64[slots[i]],
+                                      heads=oracle_heads, **oracle_kwargs(p))
+            ys.append(yg[i][:, cols].ravel()); yr.append(ref["y"][:, cols].ravel())
+        err = rel_fro(np.concatenate(ys), np.concatenate(yr))
+        assert err <= tol_for(act)["y"], fmt({"y": err})
         ss, sr = [], []
         for i in range(B):
             n = int(accept[i])
@@ -86,3 +97,13 @@ def test_recompute_equals_snapshot_path_wide_gva_and_oracle():
 
 def test_recompute_tiny_fp32():
     _compare("tiny", 51, 6, 5, oracle_heads=[0, 1])
+
+
+# larger batches (B x H_v above the SM count) and r up to 16
+@pytest.mark.parametrize("B,r", [(24, 4), (20, 16), (40, 1)])
+def test_recompute_equals_snapshot_path_large_batch_4b(B, r):
+    _compare("decode4b", 61 + r, B, r, oracle_heads=sample_heads(32, 2, seed=B))
+
+
+def test_recompute_equals_snapshot_path_large_batch_wide():
+    _compare("wide", 71, 16, 4, oracle_heads=sample_heads(48, 2, seed=4))
