@@ -1071,7 +1071,8 @@ constexpr int OFF_SMALL = OFF_G + 512; // ssq [2][NS][64], ored [2][64], norm_w 
 constexpr int SMALL_FLOATS = 2 * NS * C + 2 * C + DV;
 constexpr int SMEM = OFF_SMALL + SMALL_FLOATS * 4 + 64;  // + 6 mbarriers and the TMEM address
 constexpr int SMEM_ALLOC = SMEM + 1024;                  // room to align the base to 1024 bytes
-constexpr int cD = 0, cS = 32, TMEM_COLS = 64;
+constexpr int kIssuers = 4;  // warps issuing the K-steps of a state product (one accumulator each)
+constexpr int cD = 0, cS = 32 * kIssuers, TMEM_COLS = 64 * kIssuers;
 static_assert(NS == 4, "the output norm adds the 4 slices' row sums explicitly");
 }  // namespace tcp
 
@@ -1442,7 +1443,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
     const bool outnorm = !(g.flags & kFlagNoOutNorm);
     constexpr uint32_t kSqBytes = (NS - 1) * C * 4;  // the peers' row sums of one chunk
     if (tid == 0) {
-        mbar_init(mbar, 1);
+        mbar_init(mbar, kIssuers);  // one commit per issuing warp
         mbar_init(barA, 1);
         mbar_init(barB, 1);
         mbar_init(barC, 1);
@@ -1479,24 +1480,22 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
     const int dS = 32 * q4 + lane;  // the d_k index this thread owns in S^T
     if (tid < DV) nwsl[tid] = outnorm ? Act<__nv_bfloat16>::ld(A.p.norm_w, s_idx * DV + tid) : 1.f;
 
+    // every thread polls a barrier itself (no CTA-wide barrier needed to learn
+    // that an MMA round or a copy has completed)
+    auto poll = [&](uint64_t* b, uint32_t par) {
+        bool w = mbar_wait(b, par);
+        if (!w) w = mbar_wait(b, par);
+        ok = ok && w;
+    };
     auto wait_mma = [&]() {
-        bool w = true;
-        if (ok && warp == 0) {  // one warp polls, the others sleep in bar.sync
-            w = mbar_wait(mbar, phase);
-            if (!w) w = mbar_wait(mbar, phase);
-        }
+        poll(mbar, phase);
         phase ^= 1u;
-        ok = __syncthreads_and(ok && w);
         tc::fence_after();
     };
-    auto wait_bar = [&](uint64_t* b, uint32_t par) {
-        bool w = true;
-        if (ok && warp == 0) {
-            w = mbar_wait(b, par);
-            if (!w) w = mbar_wait(b, par);
-        }
-        ok = __syncthreads_and(ok && w);
-    };
+    // the K-steps of each state product are issued by lane 0 of warps 0..3 into
+    // 4 accumulators (parts) 32 columns apart: the tensor core accepts
+    // instructions from several warps faster than from one
+    const bool issuer = lane == 0 && warp < kIssuers;
 
     const int64_t T = end - start;
     const int n_chunks = (int)((T + C - 1) / C);
@@ -1525,14 +1524,14 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
     };
     // Ra of chunk c: D = [-W; Q'] S^T with S0s holding the state entering c
     auto issue_ra = [&](int c) {
-        wait_bar(barA, (uint32_t)(c & 1));
         tc::fence_before();
         fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
+        ok = __syncthreads_and(ok);  // S0s complete
+        if (issuer) {
+            poll(barA, (uint32_t)(c & 1));
             if (ok) {
                 tc::fence_after();
-                tc::mma_tf32(tm + cD, As, D, S0s, DV, D, tc::idesc_tf32(D, DV), false);
+                tc::mma_tf32_part(tm + cD, As, D, S0s, DV, D, tc::idesc_tf32(D, DV), warp, kIssuers, 32, false);
             }
             tc::commit(mbar);
         }
@@ -1552,7 +1551,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
             issue_b(0);
             issue_c(0);
         }
-        wait_bar(barC, 0);
+        poll(barC, 0);
         const float egC = Gs[C - 1];
         float v[16];
 #pragma unroll
@@ -1573,7 +1572,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         float o16[16];
         {
             float d16[16];
-            tc::ld16(tc::taddr(tm, 32 * q4, cD + hf * 16), d16);
+            tc::ld16_sum4(tc::taddr(tm, 32 * q4, cD + hf * 16), 32, d16);
             if (urow) {
                 const float er = Gs[C + trow];
 #pragma unroll
@@ -1584,6 +1583,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
                     tc::st_elem(UPs, DV, hf * 16 + c4 + 2, trow, (a.z + d16[c4 + 2]) * er);
                     tc::st_elem(UPs, DV, hf * 16 + c4 + 3, trow, (a.w + d16[c4 + 3]) * er);
                 }
+                fence_proxy_async_smem();  // U' is read by the tensor core
             } else {
                 float part = 0.f;
 #pragma unroll
@@ -1610,6 +1610,22 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
                 }
             }
         }
+        // ---- Rb: S^T += K^T U' --------------------------------------------------------------
+        // warps 0..5: the U' writers (0, 1, 4, 5) and the issuers (0..3); the O warps 6, 7
+        // have passed barrier 1 with warps 2, 3, so every read of U~, X and the gates is done
+        if (warp < 6) {
+            tc::fence_before();
+            named_bar_sync(2, 192);
+        }
+        if (issuer) {
+            poll(barB, par);
+            if (ok) {
+                tc::fence_after();
+                tc::mma_tf32_part(tm + cS, KTs, D, UPs, DV, C, tc::idesc_tf32(D, DV), warp, kIssuers, 32, true);
+            }
+            tc::commit(mbar);
+        }
+        if (tid == 0 && ci + 1 < n_chunks) issue_c(ci + 1);  // U~, X and the gates have been read
         uint4 zr[2];  // z of this thread's output row
         if (!urow && outnorm && trow < n) {
             const uint4* zp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(J.z) +
@@ -1618,23 +1634,10 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
             zr[0] = zp[0];
             zr[1] = zp[1];
         }
-        wait_bar(barB, par);
-        // ---- Rb: S^T += K^T U' -------------------------------------------------------------
-        tc::fence_before();
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            if (ok) {
-                tc::fence_after();
-                tc::mma_tf32(tm + cS, KTs, D, UPs, DV, C, tc::idesc_tf32(D, DV), true);
-            }
-            tc::commit(mbar);
-            if (ci + 1 < n_chunks) issue_c(ci + 1);  // U~, X and the gates have been read
-        }
         wait_mma();                                          // Rb
         if (tid == 0 && ci + 1 < n_chunks) issue_b(ci + 1);  // K^T is free
         // ---- S^T -> S operand tile for the next chunk ----------------------------------------
-        tc::ld16(tc::taddr(tm, 32 * q4, cS + hf * 16), s16);
+        tc::ld16_sum4(tc::taddr(tm, 32 * q4, cS + hf * 16), 32, s16);
 #pragma unroll
         for (int c = 0; c < 16; ++c) tc::st_elem(S0s, DV, hf * 16 + c, dS, s16[c]);
         const int ck = ckpt_after(J, seq, (int64_t)(ci + 1) * C, T);
@@ -1645,7 +1648,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         }
         if (ci + 1 < n_chunks) {
             issue_ra(ci + 1);
-            wait_bar(barC, par ^ 1u);  // gates of the next chunk: S^T *= e^gamma_C in TMEM
+            poll(barC, par ^ 1u);  // gates of the next chunk: S^T <- e^gamma_C S^T (the sum) in TMEM
             const float egC = Gs[C - 1];
             float v[16];
 #pragma unroll

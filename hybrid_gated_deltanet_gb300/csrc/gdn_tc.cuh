@@ -82,6 +82,29 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, const void* a_tile, in
     }
 }
 
+// The K-steps s = part, part + nparts, ... of that product, into accumulator
+// d_tmem + part * acc_cols: nparts threads (in different warps) issue the
+// parts of one product side by side and the caller adds the nparts partial
+// results.  accumulate_first: part 0 adds onto the accumulator's contents,
+// the other parts start from zero.
+__device__ __forceinline__ void mma_tf32_part(uint32_t d_tmem, const void* a_tile, int a_rows, const void* b_tile,
+                                              int b_rows, int K, uint32_t idesc, int part, int nparts, int acc_cols,
+                                              bool accumulate_first) {
+    const uint32_t a0 = smem_addr(a_tile), b0 = smem_addr(b_tile);
+    const uint32_t d = d_tmem + (uint32_t)(part * acc_cols);
+    for (int s = part, k0 = part * 8; k0 < K; s += nparts, k0 += 8 * nparts) {
+        const uint32_t koff = (uint32_t)((k0 & 31) * 4);
+        const uint64_t ad = sdesc(a0 + (uint32_t)((k0 >> 5) * a_rows * 128) + koff);
+        const uint64_t bd = sdesc(b0 + (uint32_t)((k0 >> 5) * b_rows * 128) + koff);
+        const uint32_t acc = (s >= nparts || (part == 0 && accumulate_first)) ? 1u : 0u;
+        asm volatile(
+            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+            " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+            "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+            : "memory");
+    }
+}
+
 __device__ __forceinline__ void commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                  : "memory");
@@ -133,6 +156,25 @@ __device__ __forceinline__ void ld16x2(uint32_t ta, float va[16], uint32_t tb, f
         va[i] = __uint_as_float(r[i]);
         vb[i] = __uint_as_float(r[16 + i]);
     }
+}
+
+// sum of 16 consecutive columns over four accumulators `stride` columns apart
+__device__ __forceinline__ void ld16_sum4(uint32_t ta, uint32_t stride, float v[16]) {
+    uint32_t r[64];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(r[16 * q + 0]), "=r"(r[16 * q + 1]), "=r"(r[16 * q + 2]), "=r"(r[16 * q + 3]),
+              "=r"(r[16 * q + 4]), "=r"(r[16 * q + 5]), "=r"(r[16 * q + 6]), "=r"(r[16 * q + 7]),
+              "=r"(r[16 * q + 8]), "=r"(r[16 * q + 9]), "=r"(r[16 * q + 10]), "=r"(r[16 * q + 11]),
+              "=r"(r[16 * q + 12]), "=r"(r[16 * q + 13]), "=r"(r[16 * q + 14]), "=r"(r[16 * q + 15])
+            : "r"(ta + q * stride));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        v[i] = (__uint_as_float(r[i]) + __uint_as_float(r[16 + i])) +
+               (__uint_as_float(r[32 + i]) + __uint_as_float(r[48 + i]));
 }
 
 __device__ __forceinline__ void st16(uint32_t taddr, const float v[16]) {
