@@ -801,6 +801,35 @@ __global__ void k_conv_roll(const Geom g, const ConvJob J) {
     }
 }
 
+// The same roll 16 bytes of channels per thread (x and the conv pool 16-byte
+// aligned, as the decode step requires): raw inputs move bit for bit.
+template <typename TA>
+__global__ void k_conv_roll_v(const Geom g, const ConvJob J) {
+    constexpr int VEC = 16 / (int)sizeof(TA);
+    const int C = g.C_ch, Km1 = g.K - 1, CV = C / VEC;
+    const size_t total = (size_t)J.n_seq * CV;
+    const TA* x = static_cast<const TA*>(J.x);
+    TA* cp = static_cast<TA*>(J.conv_pool);
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
+         idx += (size_t)gridDim.x * blockDim.x) {
+        const int ch = (int)(idx % CV) * VEC, sq = (int)(idx / CV);
+        const int slot = J.slot_idx[sq];
+        if (slot < 0 || slot >= J.n_slots) continue;
+        uint4 old[3];
+#pragma unroll
+        for (int m = 0; m < 3; ++m)
+            if (m < Km1) old[m] = *reinterpret_cast<const uint4*>(cp + ((size_t)slot * Km1 + m) * C + ch);
+#pragma unroll
+        for (int m = 0; m < 3; ++m) {
+            if (m >= Km1) break;
+            const int pidx = J.n_tok + m;
+            const uint4 v = pidx < Km1 ? old[pidx < 3 ? pidx : 0]
+                                       : *reinterpret_cast<const uint4*>(x + ((size_t)sq * J.n_tok + (pidx - Km1)) * C + ch);
+            *reinterpret_cast<uint4*>(cp + ((size_t)slot * Km1 + m) * C + ch) = v;
+        }
+    }
+}
+
 // ---- commit by copy -----------------------------------------------------------
 __global__ void k_commit(const Geom g, const CommitJob J, int elt_bytes) {
     const int b = blockIdx.y;
@@ -843,9 +872,9 @@ cudaError_t launch_decode_persist(const Geom& g, const LayerParams& p, const Row
     if (e != cudaSuccess) return e;
     // roll the conv state (raw inputs) after every read of it above
     ConvJob cj{job.x, job.conv_pool, job.slot_idx, nullptr, job.B, 1, job.n_slots};
-    const size_t total = (size_t)job.B * g.C_ch;
+    const size_t total = (size_t)job.B * g.C_ch / (16 / sizeof(TA));
     const int blocks = (int)std::min<size_t>((total + 255) / 256, (size_t)sms * 8);
-    k_conv_roll<TA><<<blocks, 256, 0, st>>>(g, cj);
+    k_conv_roll_v<TA><<<blocks, 256, 0, st>>>(g, cj);
     return cudaGetLastError();
 }
 
