@@ -69,7 +69,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // Shared-memory layout of one k_rows CTA (byte offsets, 16-byte aligned runs).
 struct RowsSmem {
-    int bar, S, x, c, w, z, nw, ab, qs, ks, vs, red, obuf, ssp, total;
+    int bar, S, x, c, w, z, nw, ab, qs, ks, vs, red, tsc, obuf, ssp, total;
 };
 
 __host__ __device__ inline RowsSmem rows_smem(int D, int RPC, int r, int K, int E) {
@@ -85,10 +85,11 @@ __host__ __device__ inline RowsSmem rows_smem(int D, int RPC, int r, int K, int 
     s.z = o; o = up(o + r * RPC * E);     // z of the CTA's rows
     s.nw = o; o = up(o + RPC * E);        // norm weight of the CTA's rows
     s.ab = o; o = up(o + 2 * r * 4);      // a, b per row
-    s.qs = o; o += D * 4;
-    s.ks = o; o += D * 4;
-    s.vs = o; o = up(o + RPC * 4);
-    s.red = o; o += 64 * 4;
+    s.qs = o; o += r * D * 4;             // q of every token (before the norm)
+    s.ks = o; o += r * D * 4;             // k of every token
+    s.vs = o; o = up(o + r * RPC * 4);    // v of every token (the CTA's rows)
+    s.red = o; o += r * 32 * 4;           // per-warp partial sums, per token
+    s.tsc = o; o += r * 8 * 4;            // per-token alpha, beta, scales, q^.k^
     s.obuf = o; o = up(o + r * RPC * 4);
     s.ssp = o; o = up(o + r * 4);
     s.total = o;
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
     float* ks = reinterpret_cast<float*>(smem + lay.ks);
     float* vs = reinterpret_cast<float*>(smem + lay.vs);
     float* red = reinterpret_cast<float*>(smem + lay.red);
+    float* tsc = reinterpret_cast<float*>(smem + lay.tsc);
     float* obuf = reinterpret_cast<float*>(smem + lay.obuf);
     float* ssp = reinterpret_cast<float*>(smem + lay.ssp);
 
@@ -212,6 +214,10 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
     if (whole_head) cluster_arrive_release();  // this CTA's conv-state reads are done (in shared memory)
 
     // ---- prologue of every row (conv, norms, gates) from shared memory --------
+    // A state row's update over the r tokens involves no other state row, so
+    // the q, k, v and gates of all r tokens are prepared first (in parallel
+    // over tokens and channels) and each warp then carries its state rows
+    // through all tokens without a CTA barrier between tokens.
     auto conv = [&](int lc, int t) -> float {
         if (raw) return L::ld(xs, (size_t)t * NCH + lc);
         const int ch = lc < D ? ch_q + lc : (lc < 2 * D ? ch_k + lc - D : ch_v + lc - 2 * D);
@@ -224,45 +230,48 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
         return siluf_(c);
     };
     const int col4 = lane % LPR, rsub = lane / LPR;
-    bool s_ok = true;
-    for (int t = 0; t < nr; ++t) {
-        const size_t rowx = (size_t)bb * r + t;
+    if (ok) {
+        for (int t = 0; t < nr; ++t) {
+            float sq = 0.f, sk = 0.f, sqk = 0.f;
+            // work item w < D: channel w of q and k; D <= w < D + RPC: channel w - D of v
+            for (int w = tid; w < D + RPC; w += nthr) {
+                if (w < D) {
+                    const float qv = conv(w, t), kv = conv(D + w, t);
+                    qs[t * D + w] = qv;
+                    ks[t * D + w] = kv;
+                    sq = fmaf(qv, qv, sq);
+                    sk = fmaf(kv, kv, sk);
+                    sqk = fmaf(qv, kv, sqk);
+                } else {
+                    vs[t * RPC + (w - D)] = conv(2 * D + (w - D), t);
+                }
+            }
+            sq = warp_sum(sq);
+            sk = warp_sum(sk);
+            sqk = warp_sum(sqk);
+            if (lane == 0) {
+                red[(t * nwarp + warp) * 4 + 0] = sq;
+                red[(t * nwarp + warp) * 4 + 1] = sk;
+                red[(t * nwarp + warp) * 4 + 2] = sqk;
+            }
+        }
+    }
+    {
+        bool s_ok = true;
+        if (warp == 0) {
+            s_ok = mbar_wait(bar_s, 0);
+            if (!s_ok) mbar_wait(bar_s, 0);  // bounded again: let the state copy land
+        }
+        ok = __syncthreads_and(ok && s_ok);  // one verdict for the whole CTA; red complete
+        if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
+    }
+    // per-token scalars: alpha, beta, the q and k scales, q^.k^
+    for (int t = tid; t < nr; t += nthr) {
         float sq = 0.f, sk = 0.f, sqk = 0.f;
-        if (ok) {
-            for (int c = tid; c < D; c += nthr) {
-                const float qv = conv(c, t), kv = conv(D + c, t);
-                qs[c] = qv;
-                ks[c] = kv;
-                sq = fmaf(qv, qv, sq);
-                sk = fmaf(kv, kv, sk);
-                sqk = fmaf(qv, kv, sqk);
-            }
-            for (int c = tid; c < RPC; c += nthr) vs[c] = conv(2 * D + c, t);
-        }
-        sq = warp_sum(sq);
-        sk = warp_sum(sk);
-        sqk = warp_sum(sqk);
-        if (lane == 0) {
-            red[warp * 4 + 0] = sq;
-            red[warp * 4 + 1] = sk;
-            red[warp * 4 + 2] = sqk;
-        }
-        if (t == 0) {
-            if (warp == 0) {
-                s_ok = mbar_wait(bar_s, 0);
-                if (!s_ok) mbar_wait(bar_s, 0);  // bounded again: let the state copy land
-            }
-            ok = __syncthreads_and(ok && s_ok);  // one verdict for the whole CTA
-            if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
-        } else {
-            __syncthreads();
-        }
-        if (!ok) break;
-        sq = sk = sqk = 0.f;
         for (int w = 0; w < nwarp; ++w) {
-            sq += red[w * 4 + 0];
-            sk += red[w * 4 + 1];
-            sqk += red[w * 4 + 2];
+            sq += red[(t * nwarp + w) * 4 + 0];
+            sk += red[(t * nwarp + w) * 4 + 1];
+            sqk += red[(t * nwarp + w) * 4 + 2];
         }
         float rq, rk;
         if (g.flags & kFlagNoL2) {
@@ -272,100 +281,125 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
             rq = g.q_scale * rsqrtf(sq + g.l2_eps);
             rk = rsqrtf(sk + g.l2_eps);
         }
-        const float kq = sqk * rq * rk;
         float gl, beta;
         gates(ab[2 * t], ab[2 * t + 1], A_log_j, dt_j, direct, gl, beta);
-        const float alpha = expf(gl);
-        float kr[4], qr[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            kr[e] = ks[col4 * 4 + e] * rk;
-            qr[e] = qs[col4 * 4 + e] * rq;
-        }
-        const int dst = J.snap_idx ? J.snap_idx[rowx] : -1;
-        float* Sd = (dst >= 0 && dst < J.n_slots)
-                        ? J.state_pool + (((size_t)dst * Hv + j) * D + (size_t)s * RPC) * D
-                        : nullptr;
+        tsc[t * 8 + 0] = expf(gl);
+        tsc[t * 8 + 1] = beta;
+        tsc[t * 8 + 2] = rq;
+        tsc[t * 8 + 3] = rk;
+        tsc[t * 8 + 4] = sqk * rq * rk;
+    }
+    __syncthreads();
+    if (ok) {
+        auto snap_rows = [&](int t) -> float* {  // verify snapshot of token t, or nullptr
+            const int dst = (mode == 0 && J.snap_idx) ? J.snap_idx[(size_t)bb * r + t] : -1;
+            return (dst >= 0 && dst < J.n_slots) ? J.state_pool + (((size_t)dst * Hv + j) * D + (size_t)s * RPC) * D
+                                                 : nullptr;
+        };
         if constexpr (D == 128) {
             // 8 rows per warp group; the 16 partial dot products (S.k, S.q of the
             // 8 rows) are reduced across the 32 lanes with a transposing butterfly
             // (16 shuffles instead of 80): lane l ends with the sum of value l >> 1.
             for (int rb = warp * 8; rb < RPC; rb += nwarp * 8) {
                 float4 sv[8];
-                float v[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    sv[i] = *reinterpret_cast<const float4*>(Sb + (rb + i) * D + lane * 4);
-                    float dk = sv[i].x * kr[0];
-                    dk = fmaf(sv[i].y, kr[1], dk);
-                    dk = fmaf(sv[i].z, kr[2], dk);
-                    v[i] = fmaf(sv[i].w, kr[3], dk);
-                    float dq = sv[i].x * qr[0];
-                    dq = fmaf(sv[i].y, qr[1], dq);
-                    dq = fmaf(sv[i].z, qr[2], dq);
-                    v[8 + i] = fmaf(sv[i].w, qr[3], dq);
-                }
+                for (int i = 0; i < 8; ++i) sv[i] = *reinterpret_cast<const float4*>(Sb + (rb + i) * D + lane * 4);
+                for (int t = 0; t < nr; ++t) {
+                    const float alpha = tsc[t * 8 + 0], beta = tsc[t * 8 + 1], rq = tsc[t * 8 + 2],
+                                rk = tsc[t * 8 + 3], kq = tsc[t * 8 + 4];
+                    float kr[4], qr[4];
 #pragma unroll
-                for (int n = 8, off = 16; n >= 1; n >>= 1, off >>= 1) {
-                    const bool upper = lane & off;
+                    for (int e = 0; e < 4; ++e) {
+                        kr[e] = ks[t * D + col4 * 4 + e] * rk;
+                        qr[e] = qs[t * D + col4 * 4 + e] * rq;
+                    }
+                    float v[16];
 #pragma unroll
-                    for (int i = 0; i < n; ++i) {
-                        const float send = upper ? v[i] : v[i + n];
-                        const float keep = upper ? v[i + n] : v[i];
-                        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                    for (int i = 0; i < 8; ++i) {
+                        float dk = sv[i].x * kr[0];
+                        dk = fmaf(sv[i].y, kr[1], dk);
+                        dk = fmaf(sv[i].z, kr[2], dk);
+                        v[i] = fmaf(sv[i].w, kr[3], dk);
+                        float dq = sv[i].x * qr[0];
+                        dq = fmaf(sv[i].y, qr[1], dq);
+                        dq = fmaf(sv[i].z, qr[2], dq);
+                        v[8 + i] = fmaf(sv[i].w, qr[3], dq);
+                    }
+#pragma unroll
+                    for (int n = 8, off = 16; n >= 1; n >>= 1, off >>= 1) {
+                        const bool upper = lane & off;
+#pragma unroll
+                        for (int i = 0; i < n; ++i) {
+                            const float send = upper ? v[i] : v[i + n];
+                            const float keep = upper ? v[i + n] : v[i];
+                            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+                        }
+                    }
+                    v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+                    const int idx = lane >> 1;  // 0..7: S.k of row rb+idx; 8..15: S.q of row rb+idx-8
+                    const float e_mine = idx < 8 ? vs[t * RPC + rb + idx] - alpha * v[0] : 0.f;
+                    float ei[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) ei[i] = __shfl_sync(0xffffffffu, e_mine, 2 * i);
+                    const float e_for_q = __shfl_sync(0xffffffffu, e_mine, ((idx - 8) & 7) * 2);
+                    if (idx >= 8 && !(lane & 1)) obuf[t * RPC + rb + idx - 8] = fmaf(alpha, v[0], beta * e_for_q * kq);
+                    float* Sd = snap_rows(t);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float be = beta * ei[i];
+                        sv[i].x = fmaf(alpha, sv[i].x, be * kr[0]);
+                        sv[i].y = fmaf(alpha, sv[i].y, be * kr[1]);
+                        sv[i].z = fmaf(alpha, sv[i].z, be * kr[2]);
+                        sv[i].w = fmaf(alpha, sv[i].w, be * kr[3]);
+                        if (Sd) *reinterpret_cast<float4*>(Sd + (rb + i) * D + lane * 4) = sv[i];  // verify snapshot
                     }
                 }
-                v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-                const int idx = lane >> 1;  // 0..7: S.k of row rb+idx; 8..15: S.q of row rb+idx-8
-                const float e_mine = idx < 8 ? vs[rb + idx] - alpha * v[0] : 0.f;
-                float ei[8];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) ei[i] = __shfl_sync(0xffffffffu, e_mine, 2 * i);
-                const float e_for_q = __shfl_sync(0xffffffffu, e_mine, ((idx - 8) & 7) * 2);
-                if (idx >= 8 && !(lane & 1)) obuf[t * RPC + rb + idx - 8] = fmaf(alpha, v[0], beta * e_for_q * kq);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float be = beta * ei[i];
-                    sv[i].x = fmaf(alpha, sv[i].x, be * kr[0]);
-                    sv[i].y = fmaf(alpha, sv[i].y, be * kr[1]);
-                    sv[i].z = fmaf(alpha, sv[i].z, be * kr[2]);
-                    sv[i].w = fmaf(alpha, sv[i].w, be * kr[3]);
-                    *reinterpret_cast<float4*>(Sb + (rb + i) * D + lane * 4) = sv[i];
-                    if (Sd) *reinterpret_cast<float4*>(Sd + (rb + i) * D + lane * 4) = sv[i];  // verify snapshot
-                }
+                for (int i = 0; i < 8; ++i) *reinterpret_cast<float4*>(Sb + (rb + i) * D + lane * 4) = sv[i];
             }
         } else {
 #pragma unroll 4
-        for (int rb = warp * RPI; rb < RPC; rb += nwarp * RPI) {
-            const int rl = rb + rsub;  // row within the slice
-            float4* sp = reinterpret_cast<float4*>(Sb + rl * D + col4 * 4);
-            float4 sv = *sp;
-            float dk = sv.x * kr[0];
-            dk = fmaf(sv.y, kr[1], dk);
-            dk = fmaf(sv.z, kr[2], dk);
-            dk = fmaf(sv.w, kr[3], dk);
-            float dq = sv.x * qr[0];
-            dq = fmaf(sv.y, qr[1], dq);
-            dq = fmaf(sv.z, qr[2], dq);
-            dq = fmaf(sv.w, qr[3], dq);
+            for (int rb = warp * RPI; rb < RPC; rb += nwarp * RPI) {
+                const int rl = rb + rsub;  // row within the slice
+                float4* sp = reinterpret_cast<float4*>(Sb + rl * D + col4 * 4);
+                float4 sv = *sp;
+                for (int t = 0; t < nr; ++t) {
+                    const float alpha = tsc[t * 8 + 0], beta = tsc[t * 8 + 1], rq = tsc[t * 8 + 2],
+                                rk = tsc[t * 8 + 3], kq = tsc[t * 8 + 4];
+                    float kr[4], qr[4];
 #pragma unroll
-            for (int off = LPR / 2; off > 0; off >>= 1) {
-                dk += __shfl_xor_sync(0xffffffffu, dk, off);
-                dq += __shfl_xor_sync(0xffffffffu, dq, off);
+                    for (int e = 0; e < 4; ++e) {
+                        kr[e] = ks[t * D + col4 * 4 + e] * rk;
+                        qr[e] = qs[t * D + col4 * 4 + e] * rq;
+                    }
+                    float dk = sv.x * kr[0];
+                    dk = fmaf(sv.y, kr[1], dk);
+                    dk = fmaf(sv.z, kr[2], dk);
+                    dk = fmaf(sv.w, kr[3], dk);
+                    float dq = sv.x * qr[0];
+                    dq = fmaf(sv.y, qr[1], dq);
+                    dq = fmaf(sv.z, qr[2], dq);
+                    dq = fmaf(sv.w, qr[3], dq);
+#pragma unroll
+                    for (int off = LPR / 2; off > 0; off >>= 1) {
+                        dk += __shfl_xor_sync(0xffffffffu, dk, off);
+                        dq += __shfl_xor_sync(0xffffffffu, dq, off);
+                    }
+                    const float e = vs[t * RPC + rl] - alpha * dk;
+                    const float be = beta * e;
+                    sv.x = fmaf(alpha, sv.x, be * kr[0]);
+                    sv.y = fmaf(alpha, sv.y, be * kr[1]);
+                    sv.z = fmaf(alpha, sv.z, be * kr[2]);
+                    sv.w = fmaf(alpha, sv.w, be * kr[3]);
+                    float* Sd = snap_rows(t);
+                    if (Sd) *reinterpret_cast<float4*>(Sd + rl * D + col4 * 4) = sv;  // verify snapshot
+                    if (col4 == 0) obuf[t * RPC + rl] = fmaf(alpha, dq, be * kq);
+                }
+                *sp = sv;
             }
-            const float e = vs[rl] - alpha * dk;
-            const float be = beta * e;
-            sv.x = fmaf(alpha, sv.x, be * kr[0]);
-            sv.y = fmaf(alpha, sv.y, be * kr[1]);
-            sv.z = fmaf(alpha, sv.z, be * kr[2]);
-            sv.w = fmaf(alpha, sv.w, be * kr[3]);
-            *sp = sv;
-            if (Sd) *reinterpret_cast<float4*>(Sd + rl * D + col4 * 4) = sv;  // verify snapshot
-            if (col4 == 0) obuf[t * RPC + rl] = fmaf(alpha, dq, be * kq);
         }
-        }
-        __syncthreads();  // qs/ks/vs/red reused by the next row; obuf complete
     }
+    __syncthreads();  // obuf complete, the state rows back in shared memory
 
     // ---- state back (decode: in place, one bulk store) and the output ---------
     fence_proxy_async_smem();
