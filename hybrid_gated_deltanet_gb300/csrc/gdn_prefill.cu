@@ -991,9 +991,9 @@ __global__ void __launch_bounds__(kChunkThreads, 1) k_chunk(const __grid_constan
 //   U~^T = V^T (T diag(beta))^T, then (P W)^T = W^T P^T and X^T = U~^T P^T
 //   (tcgen05, M = 128) -> record: the stacked operand [-W; Q'] and, per slice
 //   of 32 state rows, U~ and X in fp32.
-// k_chunk_tc (per sequence, v-head, slice; the 4 slices a cluster): the fp32
-//   state slice lives in TMEM as S^T (lane = d_k index, 32 columns = the
-//   slice's d_v rows); per chunk
+// k_chunk_tc<NSL> (per sequence, v-head, slice; the NSL = 4 or 2 slices a
+//   cluster): the fp32 state slice lives in TMEM as S^T (lane = d_k index,
+//   128 / NSL columns = the slice's d_v rows); per chunk
 //     Ra  D = [-W; Q'] S^T                    (M = 128, K = 128)
 //         U = U~ + D[0:64],  O = X + D[64:128]
 //     Rb  S^T <- e^gamma_C S^T + K^T (diag(e^(gamma_C - gamma)) U)
@@ -1041,7 +1041,7 @@ __device__ __forceinline__ uint32_t ux_off(int t, int v) {
 }
 
 namespace tcp {
-constexpr int C = 64, D = 128, DV = 32, NS = 4, THREADS = 256, LDA = 68;
+constexpr int C = 64, D = 128, THREADS = 256, LDA = 68;
 // k_chunk_prep shared memory
 constexpr int PR_R0 = 0;                       // [K^; Q^] tile (64 KB), then P | T diag(b) staging at 32 KB
 constexpr int PR_R1 = 32768;
@@ -1060,20 +1060,7 @@ constexpr int P2_G = 98304;        // e^g [64]
 constexpr int P2_SMEM = P2_G + C * 4 + 64;
 constexpr int P2_SMEM_ALLOC = P2_SMEM + 1024;
 constexpr int P2_TMEM_COLS = 128;  // two M=128 x N=64 accumulators
-// k_chunk_tc shared memory
-constexpr int OFF_A = 0;               // [-W; Q']   [128][128]
-constexpr int OFF_KT = OFF_A + 65536;  // K^T        [128][64]
-constexpr int OFF_UX = OFF_KT + 32768; // U~ | X of this slice, fp32 [64][32] each
-constexpr int OFF_UP = OFF_UX + 16384; // (diag(e^(gC-g)) U)^T [32][64]
-constexpr int OFF_S0 = OFF_UP + 8192;  // S   [32][128] (this slice's rows)
-constexpr int OFF_G = OFF_S0 + 16384;  // e^g [64] | e^(gC-g) [64]
-constexpr int OFF_SMALL = OFF_G + 512; // ssq [2][NS][64], ored [2][64], norm_w slice [32]
-constexpr int SMALL_FLOATS = 2 * NS * C + 2 * C + DV;
-constexpr int SMEM = OFF_SMALL + SMALL_FLOATS * 4 + 64;  // + 6 mbarriers and the TMEM address
-constexpr int SMEM_ALLOC = SMEM + 1024;                  // room to align the base to 1024 bytes
-constexpr int kIssuers = 4;  // warps issuing the K-steps of a state product (one accumulator each)
-constexpr int cD = 0, cS = 32 * kIssuers, TMEM_COLS = 64 * kIssuers;
-static_assert(NS == 4, "the output norm adds the 4 slices' row sums explicitly");
+constexpr int kIssuers = 4;  // warps issuing the K-steps of a chain state product (one accumulator each)
 }  // namespace tcp
 
 __global__ void __launch_bounds__(tcp::THREADS, 2) k_chunk_prep(const __grid_constant__ PrefillArgs A) {
@@ -1415,8 +1402,32 @@ __global__ void __launch_bounds__(tcp::THREADS, 2) k_chunk_prep2(const __grid_co
     if (warp == 0) tc::dealloc(tm, P2_TMEM_COLS);
 }
 
+// chain kernel shared memory and TMEM for NSL slices of DV = 128 / NSL state rows
+template <int NSL>
+struct ChainLay {
+    static constexpr int DV = tcp::D / NSL;
+    static constexpr int OFF_A = 0;                             // [-W; Q']   [128][128]
+    static constexpr int OFF_KT = OFF_A + 65536;                // K^T        [128][64]
+    static constexpr int OFF_UX = OFF_KT + 32768;               // U~ | X of the CTA's 32-row slices, 16 KB each
+    static constexpr int OFF_UP = OFF_UX + (DV / 32) * 16384;   // (diag(e^(gC-g)) U)^T [DV][64]
+    static constexpr int OFF_S0 = OFF_UP + DV * 64 * 4;         // S   [DV][128] (this CTA's rows)
+    static constexpr int OFF_G = OFF_S0 + DV * 128 * 4;         // e^g [64] | e^(gC-g) [64]
+    static constexpr int OFF_SMALL = OFF_G + 512;               // ssq [2][NSL][64], ored [2][64], norm_w [DV]
+    static constexpr int SMALL_FLOATS = 2 * NSL * tcp::C + 2 * tcp::C + DV;
+    static constexpr int SMEM = OFF_SMALL + SMALL_FLOATS * 4 + 64;  // + 6 mbarriers and the TMEM address
+    static constexpr int SMEM_ALLOC = SMEM + 1024;                  // room to align the base to 1024 bytes
+    // Ra: kIssuers partial accumulators of D, DV columns apart; Rb: S^T and kIssuers - 1 partials
+    static constexpr int cD = 0, cS = DV * tcp::kIssuers, TMEM_COLS = 2 * DV * tcp::kIssuers;
+};
+
+template <int NSL>
 __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_constant__ PrefillArgs A) {
     using namespace tcp;
+    using Lay = ChainLay<NSL>;
+    constexpr int DV = Lay::DV;
+    constexpr int HC = DV / 2;   // columns of a thread (its half of the slice)
+    constexpr int NB = HC / 16;  // 16-column blocks of a thread
+    constexpr int cD = Lay::cD, cS = Lay::cS;
     cg::cluster_group cluster = cg::this_cluster();
     const Geom& g = A.g;
     const PrefillJob& J = A.J;
@@ -1427,11 +1438,12 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
-    unsigned char *As = sm + OFF_A, *KTs = sm + OFF_KT, *UXs = sm + OFF_UX, *UPs = sm + OFF_UP, *S0s = sm + OFF_S0;
-    float* Gs = reinterpret_cast<float*>(sm + OFF_G);  // e^g [64] | e^(gC-g) [64]
-    float* ssq = reinterpret_cast<float*>(sm + OFF_SMALL);  // [2][NS][C] row sums of squares per slice
-    float* ored = ssq + 2 * NS * C;                          // [2][C] half-row sums of squares
-    float* nwsl = ored + 2 * C;                              // norm_w of this slice
+    unsigned char *As = sm + Lay::OFF_A, *KTs = sm + Lay::OFF_KT, *UXs = sm + Lay::OFF_UX;
+    unsigned char *UPs = sm + Lay::OFF_UP, *S0s = sm + Lay::OFF_S0;
+    float* Gs = reinterpret_cast<float*>(sm + Lay::OFF_G);     // e^g [64] | e^(gC-g) [64]
+    float* ssq = reinterpret_cast<float*>(sm + Lay::OFF_SMALL);  // [2][NSL][C] row sums of squares per slice
+    float* ored = ssq + 2 * NSL * C;                             // [2][C] half-row sums of squares
+    float* nwsl = ored + 2 * C;                                  // norm_w of this slice
     uint64_t* mbar = reinterpret_cast<uint64_t*>(nwsl + DV);  // MMA rounds
     uint64_t* barA = mbar + 1;    // [-W; Q'] of a chunk
     uint64_t* barB = mbar + 2;    // K^T of a chunk
@@ -1439,9 +1451,9 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
     uint64_t* barSq = mbar + 4;   // [2]: the peers' sums of squares of a chunk (by parity)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 6);
 
-    if (warp == 0) tc::alloc(tslot, TMEM_COLS);
+    if (warp == 0) tc::alloc(tslot, Lay::TMEM_COLS);
     const bool outnorm = !(g.flags & kFlagNoOutNorm);
-    constexpr uint32_t kSqBytes = (NS - 1) * C * 4;  // the peers' row sums of one chunk
+    constexpr uint32_t kSqBytes = (NSL - 1) * C * 4;  // the peers' row sums of one chunk
     if (tid == 0) {
         mbar_init(mbar, kIssuers);  // one commit per issuing warp
         mbar_init(barA, 1);
@@ -1478,6 +1490,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         }
     }
     const int dS = 32 * q4 + lane;  // the d_k index this thread owns in S^T
+    const int col0 = hf * HC;       // this thread's first column (state row) inside the slice
     if (tid < DV) nwsl[tid] = outnorm ? Act<__nv_bfloat16>::ld(A.p.norm_w, s_idx * DV + tid) : 1.f;
 
     // every thread polls a barrier itself (no CTA-wide barrier needed to learn
@@ -1493,7 +1506,7 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         tc::fence_after();
     };
     // the K-steps of each state product are issued by lane 0 of warps 0..3 into
-    // 4 accumulators (parts) 32 columns apart: the tensor core accepts
+    // 4 accumulators (parts) DV columns apart: the tensor core accepts
     // instructions from several warps faster than from one
     const bool issuer = lane == 0 && warp < kIssuers;
 
@@ -1505,6 +1518,8 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         const int64_t left = end - (start + (int64_t)c * C);
         return (int)(left < C ? left : C);
     };
+    // U~ (or X, +8 KB) of column c of the CTA: 32-row slice c / 32 of the record, 16 KB each
+    auto ux = [&](int c, int t) -> const unsigned char* { return UXs + (c >> 5) * 16384 + ux_off(t, c & 31); };
     // operand tiles come ready-made (prologue and prep kernels): bulk copies
     // issued for chunk c+1 as soon as chunk c's last use of the buffer is done
     auto cslot = [&](int c) -> size_t { return (size_t)(start / C + seq + c); };
@@ -1518,8 +1533,8 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
     };
     auto issue_c = [&](int c) {
         const unsigned char* rc = A.trec + (cslot(c) * Hv + j) * kTileRec;
-        mbar_arrive_expect_tx(barC, 16384 + 2 * C * 4);
-        bulk_g2s(UXs, rc + kRecUX + (size_t)s_idx * 16384, 16384, barC);
+        mbar_arrive_expect_tx(barC, (DV / 32) * 16384 + 2 * C * 4);
+        bulk_g2s(UXs, rc + kRecUX + (size_t)s_idx * (DV / 32) * 16384, (DV / 32) * 16384, barC);
         bulk_g2s(Gs, rc + kRecG, 2 * C * 4, barC);
     };
     // Ra of chunk c: D = [-W; Q'] S^T with S0s holding the state entering c
@@ -1531,19 +1546,18 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
             poll(barA, (uint32_t)(c & 1));
             if (ok) {
                 tc::fence_after();
-                tc::mma_tf32_part(tm + cD, As, D, S0s, DV, D, tc::idesc_tf32(D, DV), warp, kIssuers, 32, false);
+                tc::mma_tf32_part(tm + cD, As, D, S0s, DV, D, tc::idesc_tf32(D, DV), warp, kIssuers, DV, false);
             }
             tc::commit(mbar);
         }
     };
 
     // initial state: S0s <- S (TF32), TMEM S^T <- e^gamma_C S for the first chunk
-    float s16[16];
+    float sv[HC];  // this thread's part of the state (d_k = dS, columns col0 ..)
 #pragma unroll
-    for (int c = 0; c < 16; ++c) {
-        const int dv = hf * 16 + c;
-        s16[c] = Sin ? Sin[(size_t)(s_idx * DV + dv) * D + dS] : 0.f;
-        tc::st_elem(S0s, DV, dv, dS, s16[c]);
+    for (int c = 0; c < HC; ++c) {
+        sv[c] = Sin ? Sin[(size_t)(s_idx * DV + col0 + c) * D + dS] : 0.f;
+        tc::st_elem(S0s, DV, col0 + c, dS, sv[c]);
     }
     if (n_chunks > 0) {
         if (tid == 0) {
@@ -1553,10 +1567,13 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         }
         poll(barC, 0);
         const float egC = Gs[C - 1];
-        float v[16];
 #pragma unroll
-        for (int c = 0; c < 16; ++c) v[c] = s16[c] * egC;
-        tc::st16(tc::taddr(tm, 32 * q4, cS + hf * 16), v);
+        for (int b = 0; b < NB; ++b) {
+            float v[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) v[c] = sv[b * 16 + c] * egC;
+            tc::st16(tc::taddr(tm, 32 * q4, cS + col0 + b * 16), v);
+        }
         issue_ra(0);
     }
     for (int ci = 0; ci < n_chunks; ++ci) {
@@ -1566,48 +1583,55 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
         wait_mma();                                          // Ra of this chunk
         if (tid == 0 && ci + 1 < n_chunks) issue_a(ci + 1);  // [-W; Q'] is free
         // ---- U = U~ + D[0:64] -> (diag(e^(gC - g)) U)^T tile (warps 0,1,4,5); O = X +
-        // D[64:128] and its sums of squares (warps 2,3,6,7); 16 columns per thread -----
-        float* ssq_cur = ssq + (ci & 1) * NS * C;  // [NS][C]
+        // D[64:128] and its sums of squares (warps 2,3,6,7); HC columns per thread -------
+        float* ssq_cur = ssq + (ci & 1) * NSL * C;  // [NSL][C]
         uint64_t* bar_sq = barSq + (ci & 1);
-        float o16[16];
-        {
-            float d16[16];
-            tc::ld16_sum4(tc::taddr(tm, 32 * q4, cD + hf * 16), 32, d16);
-            if (urow) {
-                const float er = Gs[C + trow];
+        float ov[HC];
+        if (urow) {
+            const float er = Gs[C + trow];
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                float d16[16];
+                tc::ld16_sum4(tc::taddr(tm, 32 * q4, cD + col0 + b * 16), DV, d16);
 #pragma unroll
                 for (int c4 = 0; c4 < 16; c4 += 4) {
-                    const float4 a = *reinterpret_cast<const float4*>(UXs + ux_off(trow, hf * 16 + c4));
-                    tc::st_elem(UPs, DV, hf * 16 + c4, trow, (a.x + d16[c4]) * er);
-                    tc::st_elem(UPs, DV, hf * 16 + c4 + 1, trow, (a.y + d16[c4 + 1]) * er);
-                    tc::st_elem(UPs, DV, hf * 16 + c4 + 2, trow, (a.z + d16[c4 + 2]) * er);
-                    tc::st_elem(UPs, DV, hf * 16 + c4 + 3, trow, (a.w + d16[c4 + 3]) * er);
+                    const int c = col0 + b * 16 + c4;
+                    const float4 a = *reinterpret_cast<const float4*>(ux(c, trow));
+                    tc::st_elem(UPs, DV, c, trow, (a.x + d16[c4]) * er);
+                    tc::st_elem(UPs, DV, c + 1, trow, (a.y + d16[c4 + 1]) * er);
+                    tc::st_elem(UPs, DV, c + 2, trow, (a.z + d16[c4 + 2]) * er);
+                    tc::st_elem(UPs, DV, c + 3, trow, (a.w + d16[c4 + 3]) * er);
                 }
-                fence_proxy_async_smem();  // U' is read by the tensor core
-            } else {
-                float part = 0.f;
+            }
+            fence_proxy_async_smem();  // U' is read by the tensor core
+        } else {
+            float part = 0.f;
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                float d16[16];
+                tc::ld16_sum4(tc::taddr(tm, 32 * q4, cD + col0 + b * 16), DV, d16);
 #pragma unroll
                 for (int c4 = 0; c4 < 16; c4 += 4) {
-                    const float4 a = *reinterpret_cast<const float4*>(UXs + 8192 + ux_off(trow, hf * 16 + c4));
-                    o16[c4] = a.x + d16[c4];
-                    o16[c4 + 1] = a.y + d16[c4 + 1];
-                    o16[c4 + 2] = a.z + d16[c4 + 2];
-                    o16[c4 + 3] = a.w + d16[c4 + 3];
+                    const float4 a = *reinterpret_cast<const float4*>(ux(col0 + b * 16 + c4, trow) + 8192);
+                    float* o = ov + b * 16 + c4;
+                    o[0] = a.x + d16[c4];
+                    o[1] = a.y + d16[c4 + 1];
+                    o[2] = a.z + d16[c4 + 2];
+                    o[3] = a.w + d16[c4 + 3];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) part = fmaf(o16[c4 + e], o16[c4 + e], part);
+                    for (int e = 0; e < 4; ++e) part = fmaf(o[e], o[e], part);
                 }
-                ored[hf * C + trow] = part;
-                named_bar_sync(1, 128);  // warps 2,3,6,7
-                if (hf == 0 && outnorm) {  // this slice's row sum -> every CTA of the cluster
-                    const float sq = ored[trow] + ored[C + trow];
-                    float* mine = ssq_cur + my_rank * C + trow;
-                    *mine = sq;
+            }
+            ored[hf * C + trow] = part;
+            named_bar_sync(1, 128);  // warps 2,3,6,7
+            if (hf == 0 && outnorm) {  // this slice's row sum -> every CTA of the cluster
+                const float sq = ored[trow] + ored[C + trow];
+                float* mine = ssq_cur + my_rank * C + trow;
+                *mine = sq;
 #pragma unroll
-                    for (int r = 0; r < NS; ++r)
-                        if (r != (int)my_rank)
-                            st_async_f32(mapa_shared(tc::smem_addr(mine), r), sq,
-                                         mapa_shared(tc::smem_addr(bar_sq), r));
-                }
+                for (int r = 0; r < NSL; ++r)
+                    if (r != (int)my_rank)
+                        st_async_f32(mapa_shared(tc::smem_addr(mine), r), sq, mapa_shared(tc::smem_addr(bar_sq), r));
             }
         }
         // ---- Rb: S^T += K^T U' --------------------------------------------------------------
@@ -1621,39 +1645,43 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
             poll(barB, par);
             if (ok) {
                 tc::fence_after();
-                tc::mma_tf32_part(tm + cS, KTs, D, UPs, DV, C, tc::idesc_tf32(D, DV), warp, kIssuers, 32, true);
+                tc::mma_tf32_part(tm + cS, KTs, D, UPs, DV, C, tc::idesc_tf32(D, DV), warp, kIssuers, DV, true);
             }
             tc::commit(mbar);
         }
         if (tid == 0 && ci + 1 < n_chunks) issue_c(ci + 1);  // U~, X and the gates have been read
-        uint4 zr[2];  // z of this thread's output row
+        uint4 zr[HC / 8];  // z of this thread's output row
         if (!urow && outnorm && trow < n) {
             const uint4* zp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(J.z) +
                                                              (size_t)(t0 + trow) * Hv * D + (size_t)j * D +
-                                                             s_idx * DV + hf * 16);
-            zr[0] = zp[0];
-            zr[1] = zp[1];
+                                                             s_idx * DV + col0);
+#pragma unroll
+            for (int q = 0; q < HC / 8; ++q) zr[q] = zp[q];
         }
         wait_mma();                                          // Rb
         if (tid == 0 && ci + 1 < n_chunks) issue_b(ci + 1);  // K^T is free
         // ---- S^T -> S operand tile for the next chunk ----------------------------------------
-        tc::ld16_sum4(tc::taddr(tm, 32 * q4, cS + hf * 16), 32, s16);
 #pragma unroll
-        for (int c = 0; c < 16; ++c) tc::st_elem(S0s, DV, hf * 16 + c, dS, s16[c]);
+        for (int b = 0; b < NB; ++b) tc::ld16_sum4(tc::taddr(tm, 32 * q4, cS + col0 + b * 16), DV, sv + b * 16);
+#pragma unroll
+        for (int c = 0; c < HC; ++c) tc::st_elem(S0s, DV, col0 + c, dS, sv[c]);
         const int ck = ckpt_after(J, seq, (int64_t)(ci + 1) * C, T);
         if (ck >= 0) {  // a prefix snapshot ends with this chunk
             float* dst = J.state_pool + ((size_t)ck * Hv + j) * D * D;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) dst[(size_t)(s_idx * DV + hf * 16 + c) * D + dS] = s16[c];
+            for (int c = 0; c < HC; ++c) dst[(size_t)(s_idx * DV + col0 + c) * D + dS] = sv[c];
         }
         if (ci + 1 < n_chunks) {
             issue_ra(ci + 1);
             poll(barC, par ^ 1u);  // gates of the next chunk: S^T <- e^gamma_C S^T (the sum) in TMEM
             const float egC = Gs[C - 1];
-            float v[16];
 #pragma unroll
-            for (int c = 0; c < 16; ++c) v[c] = s16[c] * egC;
-            tc::st16(tc::taddr(tm, 32 * q4, cS + hf * 16), v);
+            for (int b = 0; b < NB; ++b) {
+                float v[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) v[c] = sv[b * 16 + c] * egC;
+                tc::st16(tc::taddr(tm, 32 * q4, cS + col0 + b * 16), v);
+            }
         }
         // ---- y = gated RMSNorm(O) of this chunk (while Ra of the next chunk runs) ---------
         if (!urow) {
@@ -1664,40 +1692,85 @@ __global__ void __launch_bounds__(tcp::THREADS, 1) k_chunk_tc(const __grid_const
                 if (!w) w = mbar_wait(bar_sq, sq_par);
                 ok = ok && w;
                 if (tid == 64) mbar_arrive_expect_tx(bar_sq, kSqBytes);  // for chunk ci + 2
-                const float* sq = ssq_cur + trow;
-                rstd = rsqrtf(((sq[0] + sq[C]) + (sq[2 * C] + sq[3 * C])) / (float)D + g.norm_eps);
+                float tot = 0.f;
+#pragma unroll
+                for (int r = 0; r < NSL; ++r) tot += ssq_cur[r * C + trow];
+                rstd = rsqrtf(tot / (float)D + g.norm_eps);
             }
             if (trow < n) {
                 const __nv_bfloat162* zh = reinterpret_cast<const __nv_bfloat162*>(zr);
-                uint4 pk[2];
+                uint4 pk[HC / 8];
                 __nv_bfloat162* hp = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    float y0 = o16[2 * c], y1 = o16[2 * c + 1];
+                for (int c = 0; c < HC / 2; ++c) {
+                    float y0 = ov[2 * c], y1 = ov[2 * c + 1];
                     if (outnorm) {
                         const float2 zz = __bfloat1622float2(zh[c]);
-                        y0 = y0 * rstd * nwsl[hf * 16 + 2 * c] * silu_fast(zz.x);
-                        y1 = y1 * rstd * nwsl[hf * 16 + 2 * c + 1] * silu_fast(zz.y);
+                        y0 = y0 * rstd * nwsl[col0 + 2 * c] * silu_fast(zz.x);
+                        y1 = y1 * rstd * nwsl[col0 + 2 * c + 1] * silu_fast(zz.y);
                     }
                     hp[c] = __floats2bfloat162_rn(y0, y1);
                 }
                 uint4* yp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(J.y) + (size_t)(t0 + trow) * Hv * D +
-                                                     (size_t)j * D + s_idx * DV + hf * 16);
-                yp[0] = pk[0];
-                yp[1] = pk[1];
+                                                     (size_t)j * D + s_idx * DV + col0);
+#pragma unroll
+                for (int q = 0; q < HC / 8; ++q) yp[q] = pk[q];
             }
         }
     }
     // ---- final state (the S operand registers hold the state after the last chunk) ---------
     if (Sout) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) Sout[(size_t)(s_idx * DV + hf * 16 + c) * D + dS] = s16[c];
+        for (int c = 0; c < HC; ++c) Sout[(size_t)(s_idx * DV + col0 + c) * D + dS] = sv[c];
     }
     tc::fence_before();
     ok = __syncthreads_and(ok);
     if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
-    if (warp == 0) tc::dealloc(tm, TMEM_COLS);
+    if (warp == 0) tc::dealloc(tm, Lay::TMEM_COLS);
     cluster.sync();  // every st.async into this CTA's shared memory has landed
+}
+
+// Slices of the chain per (sequence, v-head): 4 CTAs of 32 state rows finish a
+// long sequence soonest; when the chain CTAs fill the GPU more than once over,
+// 2 CTAs of 64 rows do the same work in half the instructions (an MMA costs
+// about the same at N = 64 as at N = 32), so the waves drain sooner.
+int chain_slices(const PrefillArgs& A) {
+    if (const char* e = std::getenv("GDN_CHAIN_SLICES")) {
+        const int v = std::atoi(e);
+        if (v == 2 || v == 4) return v;
+    }
+    static int n_sm = 0;
+    if (n_sm == 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            n_sm = 1;
+    }
+    return (int64_t)A.J.n_seq * A.g.Hv * 4 > (int64_t)n_sm ? 2 : 4;
+}
+
+template <int NSL>
+cudaError_t launch_chain(const PrefillArgs& A, cudaStream_t st) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_chunk_tc<NSL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             ChainLay<NSL>::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(NSL, A.g.Hv, A.J.n_seq);
+    cfg.blockDim = dim3(tcp::THREADS);
+    cfg.dynamicSmemBytes = ChainLay<NSL>::SMEM_ALLOC;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = NSL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_chunk_tc<NSL>, A);
 }
 
 cudaError_t launch_chunk_tc(const PrefillArgs& A, int64_t n_slots, cudaStream_t st) {
@@ -1707,8 +1780,6 @@ cudaError_t launch_chunk_tc(const PrefillArgs& A, int64_t n_slots, cudaStream_t 
                                              tcp::PR_SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(k_chunk_prep2, cudaFuncAttributeMaxDynamicSharedMemorySize, tcp::P2_SMEM_ALLOC);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k_chunk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, tcp::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -1722,19 +1793,7 @@ cudaError_t launch_chunk_tc(const PrefillArgs& A, int64_t n_slots, cudaStream_t 
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(tcp::NS, A.g.Hv, A.J.n_seq);
-    cfg.blockDim = dim3(tcp::THREADS);
-    cfg.dynamicSmemBytes = tcp::SMEM_ALLOC;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = tcp::NS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_chunk_tc, A);
+    return chain_slices(A) == 2 ? launch_chain<2>(A, st) : launch_chain<4>(A, st);
 }
 
 int prefill_slices(int D) {

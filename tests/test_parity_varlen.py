@@ -67,6 +67,21 @@ def test_varlen_small_mixed_init():
     np.testing.assert_array_equal(c_got[rest], CS.f64[rest])
 
 
+@pytest.mark.parametrize("slices", ["2", "4"])
+def test_varlen_chain_slices(monkeypatch, slices):
+    """The state chain split in 2 slices of 64 state rows or 4 of 32 (chosen by
+    how many chain CTAs the batch makes; forced here) gives the same results."""
+    monkeypatch.setenv("GDN_CHAIN_SLICES", slices)
+    lens = [200, 1, 64, 130, 63]
+    geom, act, r, p, tok = make_case("serving", 4, sum(lens))
+    cfg = config(geom, act)
+    S = synth.make_state(geom, 8, r, std=0.1)
+    CS = synth.make_conv_state(geom, 8, r, act, std=0.1)
+    slots, has_init = [6, 1, 0, 3, 4], [1, 0, 1, 0, 1]
+    cu, y, s_got, c_got = run_varlen(cfg, p, tok, lens, slots, has_init, S, CS)
+    check_seqs(geom, act, p, tok, cu, y, s_got, c_got, slots, has_init, S, CS, range(len(lens)))
+
+
 def test_varlen_tiny_fp32_equals_single_prefill():
     lens = [64, 45, 16, 3]
     geom, act, r, p, tok = make_case("tiny", 2, sum(lens))
