@@ -478,6 +478,11 @@ def profile_case(args):
         print(json.dumps(serving_measure(torch, device, args.steps, args.warmup)))
     elif args.case == "ckpt":
         print(json.dumps(ckpt_measure(torch, device, args.steps, args.warmup)))
+    elif args.case == "proj-decode":
+        print(json.dumps(proj_decode_case(torch, device, args.steps, args.warmup, args.batch)))
+    elif args.case == "layer":
+        for rec in layer_measure(torch, device, args.steps, args.warmup):
+            print(json.dumps(rec))
     elif args.case == "verify":
         for nb in (4, 64):
             print(json.dumps(verify_measure(torch, device, args.steps, args.warmup, batch=nb)))
@@ -485,6 +490,145 @@ def profile_case(args):
         t, _ = prefill_measure(torch, device, args.steps, args.warmup, seed=0, check=False)
         print(json.dumps({"case": args.case, "ms_per_call": round(1e3 * t, 4)}))
     return 0
+
+
+def proj_decode_case(torch, device, steps, warmup, batch):
+    """The two projections of a decode step alone (`batch` tokens, model width
+    2560, one layer's weights: 84 MB), for ncu captures: in-projection then
+    out-projection, warmup + steps times."""
+    from hybrid_gated_deltanet_gb300 import binding as gb
+    from hybrid_gated_deltanet_gb300 import synth
+    geom = synth.QWEN35_4B
+    hid, vd = synth.HIDDEN, geom.value_dim
+    n_in = geom.conv_channels + vd + 2 * geom.n_v_heads
+    g = torch.Generator(device=device)
+    g.manual_seed(9)
+    bf = torch.bfloat16
+    w_in = (torch.randn((n_in, hid), generator=g, device=device) / hid ** 0.5).to(bf)
+    w_out = (torch.randn((hid, vd), generator=g, device=device) / vd ** 0.5).to(bf)
+    h = torch.randn((batch, hid), generator=g, device=device).to(bf)
+    u = torch.empty((batch, n_in), dtype=bf, device=device)
+    y = torch.randn((batch, vd), generator=g, device=device).to(bf)
+    o = torch.empty((batch, hid), dtype=bf, device=device)
+    nb = max(gb.gdn_proj_workspace_size(batch, n_in, hid), gb.gdn_proj_workspace_size(batch, hid, vd))
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device=device)
+    for _ in range(warmup + steps):
+        gb.gdn_proj_gemm(h, w_in, u, ws)
+        gb.gdn_proj_gemm(y, w_out, o, ws)
+    torch.cuda.synchronize()
+    return {"case": "proj-decode", "batch": batch, "launches": 2 * (warmup + steps)}
+
+
+def layer_measure(torch, device, steps, warmup, n_layers=4, batch=64):
+    """The layer between its projections (model width 2560, Qwen3.5-4B-like
+    geometry; timing only, N(0, 1) inputs and N(0, 1/k) weights drawn on the
+    device from a fixed seed):
+    * the two projection GEMMs of a T = 8192 prefill (tensor-core TFLOP/s);
+    * gdn_layer_varlen_prefill of one T = 8192 sequence (tokens/s);
+    * gdn_layer_decode of `batch` slots, round-robin over `n_layers` layers
+      with their own weights and pools (more than L2 in total), and its
+      in-projection alone (weight GB/s)."""
+    from hybrid_gated_deltanet_gb300 import binding as gb
+    from hybrid_gated_deltanet_gb300 import synth
+    geom = synth.QWEN35_4B
+    hid = synth.HIDDEN
+    cfg = gb.Config(*GEOM_ARGS, chunk=64, act_dtype=gb.BF16)
+    r = synth.rng_for(6, 0)
+    p = synth.make_params(geom, r, synth.BF16)
+    prm = gb.Params(conv_w=_dev(p["conv_w"], torch, device), A_log=_dev(p["A_log"], torch, device),
+                    norm_w=_dev(p["norm_w"], torch, device))
+    g = torch.Generator(device=device)
+    g.manual_seed(6)
+    bf = torch.bfloat16
+    n_in = geom.conv_channels + geom.value_dim + 2 * geom.n_v_heads
+    vd = geom.value_dim
+    projs = [gb.Proj((torch.randn((n_in, hid), generator=g, device=device) / hid ** 0.5).to(bf),
+                     (torch.randn((hid, vd), generator=g, device=device) / vd ** 0.5).to(bf)) for _ in range(n_layers)]
+    stream = torch.cuda.Stream()
+
+    def timed(fn, n):
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                fn()
+            e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    out = []
+    T = PREFILL_T
+    h = torch.randn((T, hid), generator=g, device=device).to(bf)
+    u = torch.empty((T, n_in), dtype=bf, device=device)
+    yv = torch.randn((T, vd), generator=g, device=device).to(bf)
+    o = torch.empty((T, hid), dtype=bf, device=device)
+    n = max(10, steps)
+    t_in = timed(lambda: gb.gdn_proj_gemm(h, projs[0].w_in, u, stream=stream), n)
+    t_out = timed(lambda: gb.gdn_proj_gemm(yv, projs[0].w_out, o, stream=stream), n)  # T tokens: no split, no workspace
+    for name, t, nn_, kk in (("in", t_in, n_in, hid), ("out", t_out, hid, vd)):
+        fl = 2.0 * T * nn_ * kk
+        out.append({"case": "layer", "what": f"{name}-projection GEMM", "tokens": T, "n_out": nn_, "k": kk,
+                    "us": round(1e6 * t, 2), "tflops": round(fl / t / 1e12, 1)})
+    # whole layer, one T = 8192 sequence
+    S = torch.zeros((1, 32, 128, 128), device=device)
+    Cp = torch.zeros((1, 3, 8192), dtype=bf, device=device)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=device)
+    sl = torch.zeros(1, dtype=torch.int32, device=device)
+    ws = torch.empty(gb.gdn_layer_workspace_size(cfg, gb.OP_LAYER_VARLEN_PREFILL, T, 1, hid), dtype=torch.uint8,
+                     device=device)
+    t_pf = timed(lambda: gb.gdn_layer_varlen_prefill(cfg, prm, projs[0], h, cu, sl, None, Cp, S, o, ws,
+                                                      stream=stream), n)
+    fl_layer = FLOP_PER_TOKEN * T + 2.0 * T * (n_in * hid + hid * vd)
+    out.append({"case": "layer", "what": "gdn_layer_varlen_prefill", "tokens": T, "ms": round(1e3 * t_pf, 4),
+                "tokens_per_s": round(T / t_pf, 1), "tflops": round(fl_layer / t_pf / 1e12, 1)})
+    del h, u, yv, o, ws
+    # decode: batch slots per layer, n_layers layers round-robin
+    pools = []
+    for _ in range(n_layers):
+        pools.append((torch.randn((batch, 32, 128, 128), generator=g, device=device) * 0.1,
+                      (torch.randn((batch, 3, 8192), generator=g, device=device) * 0.1).to(bf)))
+    hd = torch.randn((batch, hid), generator=g, device=device).to(bf)
+    od = torch.empty((batch, hid), dtype=bf, device=device)
+    si = torch.arange(batch, dtype=torch.int32, device=device)
+    wsd = torch.empty(gb.gdn_layer_workspace_size(cfg, gb.OP_LAYER_DECODE, batch, 1, hid), dtype=torch.uint8,
+                      device=device)
+    wsp = torch.empty(max(16, gb.gdn_proj_workspace_size(batch, n_in, hid), gb.gdn_proj_workspace_size(batch, hid, vd)),
+                      dtype=torch.uint8, device=device)
+    ud = torch.empty((batch, n_in), dtype=bf, device=device)
+
+    def dec_all():
+        for li in range(n_layers):
+            gb.gdn_layer_decode(cfg, prm, projs[li], hd, pools[li][1], pools[li][0], si, od, wsd, stream=stream)
+
+    def inproj_all():
+        for li in range(n_layers):
+            gb.gdn_proj_gemm(hd, projs[li].w_in, ud, wsp, stream=stream)
+
+    yd = torch.randn((batch, vd), generator=g, device=device).to(bf)
+
+    def outproj_all():
+        for li in range(n_layers):
+            gb.gdn_proj_gemm(yd, projs[li].w_out, od, wsp, stream=stream)
+
+    nd = max(20, steps)
+    t_dec = timed(dec_all, nd) / n_layers
+    t_ip = timed(inproj_all, nd) / n_layers
+    t_op = timed(outproj_all, nd) / n_layers
+    wbytes = 2 * (n_in * hid + hid * vd)
+    dec_bytes = batch * SLOT_BYTES + PARAM_BYTES + wbytes + 2 * batch * hid * 2 - batch * (8192 + 4096 + 64) * 2 \
+        - batch * 4096 * 2
+    out.append({"case": "layer", "what": "gdn_layer_decode", "batch": batch, "layers": n_layers,
+                "us_per_layer": round(1e6 * t_dec, 2), "algorithmic_bytes": dec_bytes,
+                "gbs": round(dec_bytes / t_dec / 1e9, 1)})
+    out.append({"case": "layer", "what": "decode in-projection GEMM", "batch": batch,
+                "us": round(1e6 * t_ip, 2), "weight_gbs": round(2 * n_in * hid / t_ip / 1e9, 1)})
+    out.append({"case": "layer", "what": "decode out-projection GEMM", "batch": batch,
+                "us": round(1e6 * t_op, 2), "weight_gbs": round(2 * hid * vd / t_op / 1e9, 1)})
+    return out
 
 
 def ckpt_measure(torch, device, steps, warmup, every=1024):
@@ -799,7 +943,8 @@ def main():
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--batch", type=int, default=64, help="slots of the decode-small case")
-    ap.add_argument("--case", default="full", choices=["full", "decode-small", "prefill-small", "serving", "verify", "ckpt"],
+    ap.add_argument("--case", default="full", choices=["full", "decode-small", "prefill-small", "serving", "verify", "ckpt", "layer",
+                             "proj-decode"],
                     help="small cases for ncu captures")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-prefill-tokens", type=int, default=8192)

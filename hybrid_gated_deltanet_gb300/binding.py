@@ -21,7 +21,8 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 
 BF16, F32 = 0, 1
 RAW_QKV, NO_L2NORM, GATES_DIRECT, NO_OUTNORM = 1, 2, 4, 8
-OP_CONV_STATE_UPDATE, OP_DECODE_STEP, OP_VERIFY_ROWS, OP_CHUNK_PREFILL, OP_VARLEN_PREFILL = range(5)
+(OP_CONV_STATE_UPDATE, OP_DECODE_STEP, OP_VERIFY_ROWS, OP_CHUNK_PREFILL, OP_VARLEN_PREFILL, OP_LAYER_DECODE,
+ OP_LAYER_VARLEN_PREFILL) = range(7)
 
 STATUS = {0: "GDN_OK", -1: "GDN_ERR_NULL", -2: "GDN_ERR_SHAPE", -3: "GDN_ERR_DTYPE", -4: "GDN_ERR_ALIGN",
           -5: "GDN_ERR_RANGE", -6: "GDN_ERR_WORKSPACE", -7: "GDN_ERR_UNSUPPORTED", -8: "GDN_ERR_CUDA"}
@@ -84,6 +85,21 @@ class Params:
         return CParams(_p(self.conv_w), _p(self.conv_b), _p(self.A_log), _p(self.dt_bias), _p(self.norm_w))
 
 
+class CProj(ctypes.Structure):
+    _fields_ = [("w_in", ctypes.c_void_p), ("w_out", ctypes.c_void_p), ("hidden", ctypes.c_int32)]
+
+
+@dataclasses.dataclass
+class Proj:
+    """Projection weights of a layer: w_in bf16 [C_ch + H_v*d_v + 2*H_v, hidden] (rows of
+    x, z, a, b), w_out bf16 [hidden, H_v*d_v]."""
+    w_in: torch.Tensor
+    w_out: torch.Tensor
+
+    def c(self) -> CProj:
+        return CProj(_p(self.w_in), _p(self.w_out), self.w_in.shape[1])
+
+
 def _p(t: Optional[torch.Tensor]):
     if t is None:
         return None
@@ -118,12 +134,20 @@ def load() -> ctypes.CDLL:
             "gdn_varlen_prefill_ckpt": [cfgp, prmp, vp, vp, vp, vp, vp, i32, i64, vp, vp, vp, vp, i32, vp, i32, vp,
                                         vp, vp, sz, vp],
         }
+        projp = ctypes.POINTER(CProj)
+        sigs["gdn_proj_gemm"] = [vp, vp, vp, i64, i32, i32, i64, vp, sz, vp]
+        sigs["gdn_layer_decode"] = [cfgp, prmp, projp, vp, vp, vp, vp, i32, i32, vp, vp, sz, vp]
+        sigs["gdn_layer_varlen_prefill"] = [cfgp, prmp, projp, vp, vp, i32, i64, vp, vp, vp, vp, i32, vp, vp, sz, vp]
         for name, args in sigs.items():
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
         lib.gdn_workspace_size.argtypes = [cfgp, i32, i64, i32]
         lib.gdn_workspace_size.restype = sz
+        lib.gdn_proj_workspace_size.argtypes = [i64, i32, i32]
+        lib.gdn_proj_workspace_size.restype = sz
+        lib.gdn_layer_workspace_size.argtypes = [cfgp, i32, i64, i32, i32]
+        lib.gdn_layer_workspace_size.restype = sz
         lib.gdn_last_error.argtypes = []
         lib.gdn_last_error.restype = ctypes.c_char_p
         lib.gdn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -259,3 +283,48 @@ def gdn_commit_rows_recompute(cfg: Config, prm: Params, x, a, b, conv_pool, stat
     _check(load().gdn_commit_rows_recompute(ctypes.byref(c), ctypes.byref(p), _p(x), _p(a), _p(b), _p(conv_pool),
                                             _p(state_pool), _p(slot_idx), _p(accepted), B, r, state_pool.shape[0],
                                             _stream(stream)))
+
+
+def gdn_proj_workspace_size(n_tok: int, n_out: int, k: int) -> int:
+    return load().gdn_proj_workspace_size(n_tok, n_out, k)
+
+
+def gdn_layer_workspace_size(cfg: Config, op: int, n_tokens: int, n_seq: int, hidden: int) -> int:
+    c = cfg.c()
+    n = load().gdn_layer_workspace_size(ctypes.byref(c), op, n_tokens, n_seq, hidden)
+    msg = load().gdn_last_error().decode()
+    if msg:
+        raise GdnError(-2, msg)
+    return n
+
+
+def gdn_proj_gemm(act, w, out, workspace=None, stream=None):
+    """out[t, n] = sum_k act[t, k] w[n, k]: act bf16 [n_tok, k], w bf16 [n_out, k],
+    out bf16 [n_tok, >= n_out] (row stride out.shape[1]); workspace of
+    gdn_proj_workspace_size bytes (or None when that is 0)."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().gdn_proj_gemm(_p(act), _p(w), _p(out), act.shape[0], w.shape[0], act.shape[1], out.shape[1],
+                                _p(workspace), ws_bytes, _stream(stream)))
+
+
+def gdn_layer_decode(cfg: Config, prm: Params, proj: Proj, h, conv_pool, state_pool, slot_idx, out, workspace,
+                     stream=None):
+    """One token for each of B = h.shape[0] slots through in-projection, decode step and
+    out-projection; h, out bf16 [B, hidden]."""
+    c, p, j = cfg.c(), prm.c(), proj.c()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().gdn_layer_decode(ctypes.byref(c), ctypes.byref(p), ctypes.byref(j), _p(h), _p(conv_pool),
+                                   _p(state_pool), _p(slot_idx), h.shape[0], state_pool.shape[0], _p(out),
+                                   _p(workspace), ws_bytes, _stream(stream)))
+
+
+def gdn_layer_varlen_prefill(cfg: Config, prm: Params, proj: Proj, h, cu_seqlens, slot_idx, has_init, conv_pool,
+                             state_pool, out, workspace, stream=None):
+    """Packed sequences of h bf16 [n_tokens, hidden] through in-projection, varlen prefill
+    and out-projection into out bf16 [n_tokens, hidden]."""
+    c, p, j = cfg.c(), prm.c(), proj.c()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().gdn_layer_varlen_prefill(ctypes.byref(c), ctypes.byref(p), ctypes.byref(j), _p(h),
+                                           _p(cu_seqlens), slot_idx.numel(), h.shape[0], _p(slot_idx),
+                                           _p(has_init), _p(conv_pool), _p(state_pool), state_pool.shape[0], _p(out),
+                                           _p(workspace), ws_bytes, _stream(stream)))

@@ -145,10 +145,59 @@ const char* gdn_version(void) { return "libgdn 0.1 (sm_103a)"; }
 gdn_status gdn_device_status(uint32_t* status) {
     if (!status) return fail(GDN_ERR_NULL, "status: found NULL, required a host pointer");
     unsigned a = 0, b = 0;
+    unsigned c = 0;
     cudaError_t e = gdn::take_device_status_decode(&a);
     if (e == cudaSuccess) e = gdn::take_device_status_prefill(&b);
-    *status = a | b;
+    if (e == cudaSuccess) e = gdn::take_device_status_proj(&c);
+    *status = a | b | c;
     return cuda_status(e, "gdn_device_status");
+}
+
+// the in-projection's outputs and y of n tokens (bf16) and the projections'
+// split-K partial sums, each on a 256-byte boundary; a layer prefill's own
+// workspace follows at `rest`
+struct LayerWs {
+    size_t x, z, a, b, y, part, rest;
+};
+static LayerWs layer_ws(const gdn::Geom& g, int64_t n, int32_t hidden) {
+    auto al = [](size_t v) { return (v + 255) & ~(size_t)255; };
+    const size_t t = (size_t)(n > 0 ? n : 0);
+    LayerWs L;
+    size_t o = 0;
+    L.x = o; o += al(t * g.C_ch * 2);
+    L.z = o; o += al(t * g.Hv * g.D * 2);
+    L.a = o; o += al(t * g.Hv * 2);
+    L.b = o; o += al(t * g.Hv * 2);
+    L.y = o; o += al(t * g.Hv * g.D * 2);
+    // split-K partial sums of either projection (they run one after the other)
+    const size_t p_in = gdn::proj_plan(g.C_ch + g.Hv * g.D + 2 * g.Hv, hidden, n).ws_bytes;
+    const size_t p_out = gdn::proj_plan(hidden, g.Hv * g.D, n).ws_bytes;
+    L.part = o; o += al(p_in > p_out ? p_in : p_out);
+    L.rest = o;
+    return L;
+}
+
+size_t gdn_proj_workspace_size(int64_t n_tok, int32_t n_out, int32_t k) {
+    if (n_tok < 0 || n_out < 1 || k < 1) return 0;
+    return gdn::proj_plan(n_out, k, n_tok).ws_bytes;
+}
+
+size_t gdn_layer_workspace_size(const gdn_config* cfg, int32_t op, int64_t n_tokens, int32_t n_seq, int32_t hidden) {
+    gdn::Geom g;
+    const bool prefill = op == GDN_OP_LAYER_VARLEN_PREFILL;
+    if (op != GDN_OP_LAYER_DECODE && !prefill) {
+        fail(GDN_ERR_RANGE, "op: found %d, required GDN_OP_LAYER_DECODE (5) or GDN_OP_LAYER_VARLEN_PREFILL (6)", op);
+        return 0;
+    }
+    if (make_geom(cfg, prefill, &g) != GDN_OK) return 0;
+    if (n_tokens < 0 || n_seq < 0 || hidden < 8 || hidden % 8 != 0) {
+        fail(GDN_ERR_RANGE, "n_tokens/n_seq/hidden: found %lld/%d/%d, required >= 0/>= 0/a positive multiple of 8",
+             (long long)n_tokens, n_seq, hidden);
+        return 0;
+    }
+    ok();
+    const size_t base = layer_ws(g, n_tokens, hidden).rest;
+    return prefill ? base + gdn::prefill_workspace_bytes(g, n_tokens, n_seq) : base;
 }
 
 size_t gdn_workspace_size(const gdn_config* cfg, int32_t op, int64_t n_tokens, int32_t n_seq) {
@@ -187,6 +236,29 @@ gdn_status gdn_conv_state_update(const gdn_config* cfg, const gdn_params* prm, c
     return cuda_status(gdn::launch_conv_update(g, p, job, (cudaStream_t)stream), "gdn_conv_state_update");
 }
 
+static gdn_status rows_check(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* z,
+                             const void* a, const void* b, void* conv_pool, float* state_pool,
+                             const int32_t* slot_idx, int32_t B, int32_t r, int32_t n_slots, void* y, int mode,
+                             const int32_t* accepted, gdn::Geom* g, gdn::LayerParams* p) {
+    gdn_status st = make_geom(cfg, false, g);
+    if (st) return st;
+    if (B < 0 || B > 65535) return fail(GDN_ERR_RANGE, "B: found %d, required 0..65535", B);
+    if (r < 1 || r > 16) return fail(GDN_ERR_RANGE, "r: found %d, required 1..16", r);
+    if (n_slots < 1) return fail(GDN_ERR_RANGE, "n_slots: found %d, required >= 1", n_slots);
+    if (B == 0) return GDN_OK;
+    if ((st = make_params(prm, *g, true, p))) return st;
+    GDN_REQUIRE_PTR(x, "x");  // x and z are staged with bulk copies: 16-byte aligned
+    if (!(g->flags & GDN_FLAG_NO_OUTNORM) && mode != 2) GDN_REQUIRE_PTR(z, "z");
+    GDN_REQUIRE_PTR_A(a, "a", g->act_bf16 ? 2u : 4u);
+    GDN_REQUIRE_PTR_A(b, "b", g->act_bf16 ? 2u : 4u);
+    GDN_REQUIRE_PTR(conv_pool, "conv_pool");
+    GDN_REQUIRE_PTR(state_pool, "state_pool");
+    GDN_REQUIRE_PTR_A(slot_idx, "slot_idx", 4u);
+    if (mode != 2) GDN_REQUIRE_PTR_A(y, "y", g->act_bf16 ? 2u : 4u);
+    else GDN_REQUIRE_PTR_A(accepted, "accepted", 4u);
+    return GDN_OK;
+}
+
 static gdn_status rows_common(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* z,
                               const void* a, const void* b, void* conv_pool, float* state_pool,
                               const int32_t* slot_idx, const int32_t* snap_idx, int32_t B, int32_t r,
@@ -194,22 +266,10 @@ static gdn_status rows_common(const gdn_config* cfg, const gdn_params* prm, cons
                               const int32_t* accepted = nullptr) {
     gdn::Geom g;
     gdn::LayerParams p;
-    gdn_status st = make_geom(cfg, false, &g);
+    gdn_status st = rows_check(cfg, prm, x, z, a, b, conv_pool, state_pool, slot_idx, B, r, n_slots, y, mode,
+                               accepted, &g, &p);
     if (st) return st;
-    if (B < 0 || B > 65535) return fail(GDN_ERR_RANGE, "B: found %d, required 0..65535", B);
-    if (r < 1 || r > 16) return fail(GDN_ERR_RANGE, "r: found %d, required 1..16", r);
-    if (n_slots < 1) return fail(GDN_ERR_RANGE, "n_slots: found %d, required >= 1", n_slots);
     if (B == 0) return ok();
-    if ((st = make_params(prm, g, true, &p))) return st;
-    GDN_REQUIRE_PTR(x, "x");  // x and z are staged with bulk copies: 16-byte aligned
-    if (!(g.flags & GDN_FLAG_NO_OUTNORM) && mode != 2) GDN_REQUIRE_PTR(z, "z");
-    GDN_REQUIRE_PTR_A(a, "a", g.act_bf16 ? 2u : 4u);
-    GDN_REQUIRE_PTR_A(b, "b", g.act_bf16 ? 2u : 4u);
-    GDN_REQUIRE_PTR(conv_pool, "conv_pool");
-    GDN_REQUIRE_PTR(state_pool, "state_pool");
-    GDN_REQUIRE_PTR_A(slot_idx, "slot_idx", 4u);
-    if (mode != 2) GDN_REQUIRE_PTR_A(y, "y", g.act_bf16 ? 2u : 4u);
-    else GDN_REQUIRE_PTR_A(accepted, "accepted", 4u);
     gdn::RowsJob job{x, z, a, b, conv_pool, state_pool, slot_idx, snap_idx, y, B, r, n_slots};
     job.mode = mode;
     job.accepted = accepted;
@@ -265,26 +325,33 @@ gdn_status gdn_commit_rows(const gdn_config* cfg, void* conv_pool, float* state_
     return cuda_status(gdn::launch_commit(g, job, (cudaStream_t)stream), "gdn_commit_rows");
 }
 
+static gdn_status prefill_check(const gdn_config* cfg, const gdn_params* prm, const gdn::PrefillJob& job,
+                                gdn::Geom* g, gdn::LayerParams* p) {
+    gdn_status st = make_geom(cfg, true, g);
+    if (st) return st;
+    if (job.n_tokens < 0 || job.n_tokens > (int64_t)1 << 31)
+        return fail(GDN_ERR_RANGE, "n_tokens: found %lld, required 0..2^31", (long long)job.n_tokens);
+    if ((st = make_params(prm, *g, true, p))) return st;
+    if (job.n_tokens > 0) {
+        GDN_REQUIRE_PTR(job.x, "x");  // x, z, y move in 16-byte vectors
+        if (!(g->flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR(job.z, "z");
+        GDN_REQUIRE_PTR_A(job.a, "a", g->act_bf16 ? 2u : 4u);
+        GDN_REQUIRE_PTR_A(job.b, "b", g->act_bf16 ? 2u : 4u);
+        GDN_REQUIRE_PTR(job.y, "y");
+    }
+    const size_t need = gdn::prefill_workspace_bytes(*g, job.n_tokens, job.cu_seqlens ? job.n_seq : 1);
+    if (need > 0) GDN_REQUIRE_PTR(job.workspace, "workspace");
+    if (job.ws_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace: found %zu bytes, required %zu bytes", job.ws_bytes, need);
+    return GDN_OK;
+}
+
 static gdn_status prefill_common(const gdn_config* cfg, const gdn_params* prm, gdn::PrefillJob& job, void* stream,
                                  const char* who) {
     gdn::Geom g;
     gdn::LayerParams p;
-    gdn_status st = make_geom(cfg, true, &g);
+    gdn_status st = prefill_check(cfg, prm, job, &g, &p);
     if (st) return st;
-    if (job.n_tokens < 0 || job.n_tokens > (int64_t)1 << 31)
-        return fail(GDN_ERR_RANGE, "n_tokens: found %lld, required 0..2^31", (long long)job.n_tokens);
-    if ((st = make_params(prm, g, true, &p))) return st;
-    if (job.n_tokens > 0) {
-        GDN_REQUIRE_PTR(job.x, "x");  // x, z, y move in 16-byte vectors
-        if (!(g.flags & GDN_FLAG_NO_OUTNORM)) GDN_REQUIRE_PTR(job.z, "z");
-        GDN_REQUIRE_PTR_A(job.a, "a", g.act_bf16 ? 2u : 4u);
-        GDN_REQUIRE_PTR_A(job.b, "b", g.act_bf16 ? 2u : 4u);
-        GDN_REQUIRE_PTR(job.y, "y");
-    }
-    const size_t need = gdn::prefill_workspace_bytes(g, job.n_tokens, job.cu_seqlens ? job.n_seq : 1);
-    if (need > 0) GDN_REQUIRE_PTR(job.workspace, "workspace");
-    if (job.ws_bytes < need)
-        return fail(GDN_ERR_WORKSPACE, "workspace: found %zu bytes, required %zu bytes", job.ws_bytes, need);
     return cuda_status(gdn::launch_prefill(g, p, job, (cudaStream_t)stream), who);
 }
 
@@ -374,6 +441,155 @@ gdn_status gdn_varlen_prefill_ckpt(const gdn_config* cfg, const gdn_params* prm,
     job.ckpt_every = ckpt_every; job.ckpt_offset = ckpt_offset; job.ckpt_slots = ckpt_slots;
     job.workspace = workspace; job.ws_bytes = ws_bytes;
     return prefill_common(cfg, prm, job, stream, "gdn_varlen_prefill_ckpt");
+}
+
+gdn_status gdn_proj_gemm(const void* act, const void* w, void* out, int64_t n_tok, int32_t n_out, int32_t k,
+                         int64_t ld_out, void* workspace, size_t ws_bytes, void* stream) {
+    if (n_tok < 0 || n_tok >= ((int64_t)1 << 31))
+        return fail(GDN_ERR_RANGE, "n_tok: found %lld, required 0..2^31-1", (long long)n_tok);
+    if (n_out < 1) return fail(GDN_ERR_SHAPE, "n_out: found %d, required >= 1", n_out);
+    if (k < 8 || k % 8 != 0) return fail(GDN_ERR_SHAPE, "k: found %d, required a positive multiple of 8", k);
+    if (ld_out < n_out)
+        return fail(GDN_ERR_SHAPE, "ld_out: found %lld, required >= n_out = %d", (long long)ld_out, n_out);
+    if (n_tok == 0) return ok();
+    GDN_REQUIRE_PTR(act, "act");
+    GDN_REQUIRE_PTR(w, "w");
+    GDN_REQUIRE_PTR_A(out, "out", 2u);
+    const size_t need = gdn::proj_plan(n_out, k, n_tok).ws_bytes;
+    if (need > 0) GDN_REQUIRE_PTR(workspace, "workspace");
+    if (ws_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace: found %zu bytes, required %zu bytes", ws_bytes, need);
+    gdn::ProjJob job = {};
+    job.w = w; job.act = act; job.n_out = n_out; job.k = k; job.n_tok = n_tok;
+    job.ws = workspace; job.ws_bytes = ws_bytes;
+    job.nseg = 1;
+    job.seg[0] = gdn::ProjOut{out, ld_out, 0, n_out};
+    return cuda_status(gdn::launch_proj(job, (cudaStream_t)stream), "gdn_proj_gemm");
+}
+
+static gdn_status proj_check(const gdn::Geom& g, const gdn_proj* proj) {
+    if (!g.act_bf16)
+        return fail(GDN_ERR_UNSUPPORTED, "cfg.act_dtype: found 1 (GDN_DTYPE_F32), required GDN_DTYPE_BF16 (0) "
+                                         "with the projections");
+    if (!proj) return fail(GDN_ERR_NULL, "proj: found NULL, required a gdn_proj");
+    if (proj->hidden < 8 || proj->hidden % 8 != 0)
+        return fail(GDN_ERR_SHAPE, "proj.hidden: found %d, required a positive multiple of 8", proj->hidden);
+    GDN_REQUIRE_PTR(proj->w_in, "proj.w_in");
+    GDN_REQUIRE_PTR(proj->w_out, "proj.w_out");
+    return GDN_OK;
+}
+
+// [x | z | a | b] = h w_in^T into the workspace
+static cudaError_t launch_in_proj(const gdn::Geom& g, const gdn_proj* proj, const void* h, int64_t n,
+                                  unsigned char* ws, const LayerWs& L, cudaStream_t st) {
+    const int32_t vd = g.Hv * g.D;
+    gdn::ProjJob j = {};
+    j.w = proj->w_in; j.act = h; j.k = proj->hidden; j.n_tok = n;
+    j.n_out = g.C_ch + vd + 2 * g.Hv;
+    j.nseg = 4;
+    j.seg[0] = gdn::ProjOut{ws + L.x, g.C_ch, 0, g.C_ch};
+    j.seg[1] = gdn::ProjOut{ws + L.z, vd, g.C_ch, g.C_ch + vd};
+    j.seg[2] = gdn::ProjOut{ws + L.a, g.Hv, g.C_ch + vd, g.C_ch + vd + g.Hv};
+    j.seg[3] = gdn::ProjOut{ws + L.b, g.Hv, g.C_ch + vd + g.Hv, g.C_ch + vd + 2 * g.Hv};
+    j.ws = ws + L.part;
+    j.ws_bytes = L.rest - L.part;
+    return gdn::launch_proj(j, st);
+}
+
+// out = y w_out^T
+static cudaError_t launch_out_proj(const gdn::Geom& g, const gdn_proj* proj, const void* y, int64_t n, void* out,
+                                   unsigned char* ws, const LayerWs& L, cudaStream_t st) {
+    gdn::ProjJob j = {};
+    j.w = proj->w_out; j.act = y; j.k = g.Hv * g.D; j.n_tok = n;
+    j.n_out = proj->hidden;
+    j.nseg = 1;
+    j.seg[0] = gdn::ProjOut{out, proj->hidden, 0, proj->hidden};
+    j.ws = ws + L.part;
+    j.ws_bytes = L.rest - L.part;
+    return gdn::launch_proj(j, st);
+}
+
+gdn_status gdn_layer_decode(const gdn_config* cfg, const gdn_params* prm, const gdn_proj* proj, const void* h,
+                            void* conv_pool, float* state_pool, const int32_t* slot_idx, int32_t B, int32_t n_slots,
+                            void* out, void* workspace, size_t ws_bytes, void* stream) {
+    gdn::Geom g;
+    gdn::LayerParams p;
+    gdn_status st = make_geom(cfg, false, &g);
+    if (st) return st;
+    if ((st = proj_check(g, proj))) return st;
+    if (B < 0 || B > 65535) return fail(GDN_ERR_RANGE, "B: found %d, required 0..65535", B);
+    if (B == 0) return n_slots < 1 ? fail(GDN_ERR_RANGE, "n_slots: found %d, required >= 1", n_slots) : ok();
+    GDN_REQUIRE_PTR(h, "h");
+    GDN_REQUIRE_PTR_A(out, "out", 2u);
+    const LayerWs L = layer_ws(g, B, proj->hidden);
+    GDN_REQUIRE_PTR(workspace, "workspace");
+    if (ws_bytes < L.rest)
+        return fail(GDN_ERR_WORKSPACE, "workspace: found %zu bytes, required %zu bytes", ws_bytes, L.rest);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    // every check of the decode step before the first launch
+    if ((st = rows_check(cfg, prm, ws + L.x, ws + L.z, ws + L.a, ws + L.b, conv_pool, state_pool, slot_idx, B, 1,
+                         n_slots, ws + L.y, 0, nullptr, &g, &p)))
+        return st;
+    const cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_in_proj(g, proj, h, B, ws, L, s);
+    if (e != cudaSuccess) return cuda_status(e, "gdn_layer_decode (in-projection)");
+    gdn::RowsJob job{ws + L.x, ws + L.z, ws + L.a, ws + L.b, conv_pool, state_pool, slot_idx, nullptr, ws + L.y,
+                     B, 1, n_slots};
+    e = gdn::launch_rows(g, p, job, s);
+    if (e != cudaSuccess) return cuda_status(e, "gdn_layer_decode (decode step)");
+    return cuda_status(launch_out_proj(g, proj, ws + L.y, B, out, ws, L, s), "gdn_layer_decode (out-projection)");
+}
+
+gdn_status gdn_layer_varlen_prefill(const gdn_config* cfg, const gdn_params* prm, const gdn_proj* proj, const void* h,
+                                    const int32_t* cu_seqlens, int32_t n_seq, int64_t n_tokens,
+                                    const int32_t* slot_idx, const uint8_t* has_init, void* conv_pool,
+                                    float* state_pool, int32_t n_slots, void* out, void* workspace, size_t ws_bytes,
+                                    void* stream) {
+    gdn::Geom g;
+    gdn::LayerParams p;
+    gdn_status st = make_geom(cfg, true, &g);
+    if (st) return st;
+    if ((st = proj_check(g, proj))) return st;
+    if (n_seq < 0 || n_seq > 65535) return fail(GDN_ERR_RANGE, "n_seq: found %d, required 0..65535", n_seq);
+    if (n_slots < 1) return fail(GDN_ERR_RANGE, "n_slots: found %d, required >= 1", n_slots);
+    if (n_seq == 0) {
+        if (n_tokens != 0)
+            return fail(GDN_ERR_RANGE, "n_tokens: found %lld with n_seq = 0, required 0", (long long)n_tokens);
+        return ok();
+    }
+    if (n_tokens < 0 || n_tokens > (int64_t)1 << 31)
+        return fail(GDN_ERR_RANGE, "n_tokens: found %lld, required 0..2^31", (long long)n_tokens);
+    GDN_REQUIRE_PTR_A(cu_seqlens, "cu_seqlens", 4u);
+    GDN_REQUIRE_PTR_A(slot_idx, "slot_idx", 4u);
+    GDN_OPTIONAL_PTR_A(has_init, "has_init", 1u);
+    GDN_REQUIRE_PTR(conv_pool, "conv_pool");
+    GDN_REQUIRE_PTR(state_pool, "state_pool");
+    if (n_tokens > 0) {
+        GDN_REQUIRE_PTR(h, "h");
+        GDN_REQUIRE_PTR_A(out, "out", 2u);
+    }
+    const LayerWs L = layer_ws(g, n_tokens, proj->hidden);
+    const size_t need = L.rest + gdn::prefill_workspace_bytes(g, n_tokens, n_seq);
+    GDN_REQUIRE_PTR(workspace, "workspace");
+    if (ws_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace: found %zu bytes, required %zu bytes", ws_bytes, need);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    gdn::PrefillJob job = {};
+    job.x = ws + L.x; job.z = ws + L.z; job.a = ws + L.a; job.b = ws + L.b; job.y = ws + L.y;
+    job.n_tokens = n_tokens;
+    job.n_seq = n_seq;
+    job.cu_seqlens = cu_seqlens;
+    job.slot_idx = slot_idx; job.has_init = has_init;
+    job.state_pool = state_pool; job.conv_pool = conv_pool; job.n_slots = n_slots;
+    job.workspace = ws + L.rest; job.ws_bytes = ws_bytes - L.rest;
+    if ((st = prefill_check(cfg, prm, job, &g, &p))) return st;
+    const cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = launch_in_proj(g, proj, h, n_tokens, ws, L, s);
+    if (e != cudaSuccess) return cuda_status(e, "gdn_layer_varlen_prefill (in-projection)");
+    e = gdn::launch_prefill(g, p, job, s);
+    if (e != cudaSuccess) return cuda_status(e, "gdn_layer_varlen_prefill (prefill)");
+    return cuda_status(launch_out_proj(g, proj, ws + L.y, n_tokens, out, ws, L, s),
+                       "gdn_layer_varlen_prefill (out-projection)");
 }
 
 }  // extern "C"

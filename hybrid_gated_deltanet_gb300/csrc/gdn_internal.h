@@ -90,8 +90,35 @@ size_t prefill_workspace_bytes(const Geom& g, int64_t n_tokens, int n_seq);
 cudaError_t launch_prefill(const Geom& g, const LayerParams& prm, const PrefillJob& job,
                            cudaStream_t st);
 
+// out[t][n] = sum_k act[t][k] w[n][k] (bf16, fp32 accumulation); weight rows
+// [seg.n0, seg.n1) land in columns [0, n1 - n0) of seg.out (row stride seg.ld)
+struct ProjOut {
+    void* out;
+    int64_t ld;
+    int32_t n0, n1;
+};
+struct ProjJob {
+    const void* w;    // bf16 [n_out][k]
+    const void* act;  // bf16 [n_tok][k]
+    int32_t n_out, k;
+    int64_t n_tok;
+    int nseg;
+    ProjOut seg[4];
+    void* ws;  // fp32 partial sums when K is split (proj_plan().ws_bytes)
+    size_t ws_bytes;
+};
+struct ProjPlan {
+    int bt;           // tokens per tile
+    int64_t n_tiles;  // (128-row weight block, token block) tiles
+    int ks;           // CTAs per tile splitting K (1: none)
+    size_t ws_bytes;  // workspace for the split's partial sums
+};
+ProjPlan proj_plan(int32_t n_out, int32_t k, int64_t n_tok);
+cudaError_t launch_proj(const ProjJob& job, cudaStream_t st);
+
 // read and clear the device status word of each kernel file (synchronous)
 cudaError_t take_device_status_decode(unsigned* out);
 cudaError_t take_device_status_prefill(unsigned* out);
+cudaError_t take_device_status_proj(unsigned* out);
 
 }  // namespace gdn

@@ -200,6 +200,27 @@ def make_conv_state(geom: Geometry, n_slots: int, rng: np.random.Generator, act_
     return _store_rows(lambda n: std * rng.standard_normal((n,) + shape), n_slots, act_dtype, block=256)
 
 
+# model width around the layer: n_embd = 2560 in Strata chapter 6, section 6.2
+# (ModelGeometry); the Qwen3.5-4B-like geometry uses the same width
+HIDDEN = 2560
+
+
+def make_proj(geom: Geometry, hidden: int, rng: np.random.Generator) -> Dict[str, Stored]:
+    """Projection weights, bf16: w_in [C_ch + H_v*d_v + 2*H_v, hidden] ~ N(0, 1/hidden)
+    (rows of x, z, a, b; with h ~ N(0, 1) their outputs are ~ N(0, 1) like the layer
+    inputs of the other workloads) and w_out [hidden, H_v*d_v] ~ N(0, 1/(H_v*d_v))."""
+    n_in = geom.conv_channels + geom.value_dim + 2 * geom.n_v_heads
+    w_in = _store_rows(lambda n: rng.standard_normal((n, hidden)) / math.sqrt(hidden), n_in, BF16, block=2048)
+    w_out = _store_rows(lambda n: rng.standard_normal((n, geom.value_dim)) / math.sqrt(geom.value_dim), hidden, BF16,
+                        block=2048)
+    return {"w_in": w_in, "w_out": w_out}
+
+
+def make_hidden(n_tok: int, hidden: int, rng: np.random.Generator) -> Stored:
+    """Hidden states h [n_tok, hidden] ~ N(0, 1), bf16."""
+    return _store_rows(lambda n: rng.standard_normal((n, hidden)), n_tok, BF16, block=2048)
+
+
 def log_uniform_lengths(rng: np.random.Generator, n: int, lo: int, hi: int) -> List[int]:
     """floor(exp(U(ln lo, ln hi))) sequence lengths."""
     return [int(math.floor(math.exp(v))) for v in rng.uniform(math.log(lo), math.log(hi), size=n)]

@@ -88,7 +88,9 @@ enum {
     GDN_OP_DECODE_STEP = 1,
     GDN_OP_VERIFY_ROWS = 2,
     GDN_OP_CHUNK_PREFILL = 3,
-    GDN_OP_VARLEN_PREFILL = 4
+    GDN_OP_VARLEN_PREFILL = 4,
+    GDN_OP_LAYER_DECODE = 5,         /* gdn_layer_workspace_size only: gdn_layer_decode, n_tokens = B */
+    GDN_OP_LAYER_VARLEN_PREFILL = 6  /* gdn_layer_workspace_size only: gdn_layer_varlen_prefill */
 };
 
 /* Layer geometry and options.  Requirements (GDN_ERR_SHAPE otherwise):
@@ -268,10 +270,78 @@ gdn_status gdn_chunk_prefill_noalloc(const gdn_config* cfg, const gdn_params* pr
                                      const float* s0, const void* conv0, float* s_final,
                                      void* conv_final, void* y, void* stream);
 
+/* ---- The projections either side of the layer -------------------------------
+ * The layer's inputs [x | z | a | b] come from one in-projection of the
+ * model's hidden states h, and its output y goes back to the model width
+ * through one out-projection.  "Forge: how I wrote my own inference engine and
+ * overtook llama.cpp" (24 August) measures the matrix projections at 59% of its
+ * hybrid prefill, and its opening formulas bound decode by the weight bytes
+ * read per token over the memory bandwidth.  These calls run them on the
+ * tensor cores (tcgen05, bf16 operands, fp32 accumulation, the bf16 result
+ * rounded to nearest even) and chain them with the layer. */
+
+/* out[t][n] = sum_k act[t][k] * w[n][k] for t < n_tok, n < n_out (w in the
+ * nn.Linear layout [n_out][k]).
+ *   act bf16 [n_tok][k] and w bf16 [n_out][k], dense, 16-byte aligned;
+ *   out bf16 with rows of ld_out >= n_out elements, 2-byte aligned.
+ *   k: a positive multiple of 8 (rows start on 16-byte boundaries);
+ *   n_out >= 1; 0 <= n_tok < 2^31 (0: nothing to do).
+ *   workspace: gdn_proj_workspace_size(n_tok, n_out, k) bytes, 16-byte
+ *   aligned (NULL when that is 0).  With few tokens (up to 256) and few
+ *   128-row blocks of w, K is split over several CTAs per block whose fp32
+ *   partial sums meet in the workspace; the sums are added in a fixed order,
+ *   so results do not change from call to call. */
+gdn_status gdn_proj_gemm(const void* act, const void* w, void* out, int64_t n_tok, int32_t n_out,
+                         int32_t k, int64_t ld_out, void* workspace, size_t ws_bytes, void* stream);
+
+/* Workspace bytes of gdn_proj_gemm for these sizes (0: none needed or invalid
+ * sizes).  Depends on the sizes only. */
+size_t gdn_proj_workspace_size(int64_t n_tok, int32_t n_out, int32_t k);
+
+/* Projection weights of one layer (device pointers, bf16, row-major). */
+typedef struct gdn_proj {
+    const void* w_in;   /* [C_ch + 2*H_v + H_v*d_v][hidden]: the rows of x (C_ch), then
+                           z (H_v*d_v), then a (H_v), then b (H_v) */
+    const void* w_out;  /* [hidden][H_v*d_v] */
+    int32_t hidden;     /* model width: a positive multiple of 8 */
+} gdn_proj;
+
+/* One decode step of the whole layer for B slots: [x|z|a|b] = h w_in^T, the
+ * step of gdn_decode_step on them, out = y w_out^T.
+ *   h, out bf16 [B][hidden]; conv_pool, state_pool, slot_idx, B, n_slots as in
+ *   gdn_decode_step.  act_dtype must be GDN_DTYPE_BF16 (else
+ *   GDN_ERR_UNSUPPORTED).
+ *   workspace: gdn_layer_workspace_size(cfg, GDN_OP_LAYER_DECODE, B, 1,
+ *   proj->hidden) bytes; it holds x, z, a, b and y of the B tokens (bf16)
+ *   between the three steps and the projections' partial sums. */
+gdn_status gdn_layer_decode(const gdn_config* cfg, const gdn_params* prm, const gdn_proj* proj,
+                            const void* h, void* conv_pool, float* state_pool,
+                            const int32_t* slot_idx, int32_t B, int32_t n_slots, void* out,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/* The whole layer over packed sequences: in-projection, gdn_varlen_prefill,
+ * out-projection.  h, out bf16 [n_tokens][hidden]; the other arguments as in
+ * gdn_varlen_prefill; act_dtype must be GDN_DTYPE_BF16.
+ *   workspace: gdn_layer_workspace_size(cfg, GDN_OP_LAYER_VARLEN_PREFILL,
+ *   n_tokens, n_seq, proj->hidden) bytes: x, z, a, b, y of the tokens, the
+ *   projections' partial sums and the prefill's own workspace. */
+gdn_status gdn_layer_varlen_prefill(const gdn_config* cfg, const gdn_params* prm,
+                                    const gdn_proj* proj, const void* h,
+                                    const int32_t* cu_seqlens, int32_t n_seq, int64_t n_tokens,
+                                    const int32_t* slot_idx, const uint8_t* has_init,
+                                    void* conv_pool, float* state_pool, int32_t n_slots, void* out,
+                                    void* workspace, size_t ws_bytes, void* stream);
+
 /* Workspace bytes an op needs for n_tokens tokens in n_seq sequences (0 for
  * the ops that need none).  Returns 0 and sets gdn_last_error on an invalid
  * config. */
 size_t gdn_workspace_size(const gdn_config* cfg, int32_t op, int64_t n_tokens, int32_t n_seq);
+
+/* Workspace bytes of gdn_layer_decode (op GDN_OP_LAYER_DECODE, n_tokens = B)
+ * or gdn_layer_varlen_prefill (op GDN_OP_LAYER_VARLEN_PREFILL) for a model
+ * width `hidden`.  Returns 0 and sets gdn_last_error on invalid arguments. */
+size_t gdn_layer_workspace_size(const gdn_config* cfg, int32_t op, int64_t n_tokens, int32_t n_seq,
+                                int32_t hidden);
 
 /* Message of the last failed call on this host thread ("" if none).  The
  * string stays valid until the next call on this thread. */

@@ -32,7 +32,8 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for fn in ("gdn_conv_state_update", "gdn_decode_step", "gdn_verify_rows", "gdn_chunk_prefill",
-               "gdn_varlen_prefill", "gdn_workspace_size", "gdn_last_error"):
+               "gdn_varlen_prefill", "gdn_workspace_size", "gdn_last_error", "gdn_proj_gemm", "gdn_layer_decode",
+               "gdn_layer_varlen_prefill"):
         assert fn in names
 
 
@@ -171,6 +172,72 @@ def test_recompute_commit_validation(lib):
     st = lib.gdn_verify_rows_nosnap(ctypes.byref(cfg), ctypes.byref(prm), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                                     4, 4, 16, None, None)
     assert st == -1 and "y" in _err(lib)
+
+
+def test_projection_and_layer_validation(lib):
+    cfg = _cfg()
+    prm = _prm()
+    st = lib.gdn_proj_gemm(FAKE, FAKE, FAKE, 4, 16, 60, 16, None, 0, None)
+    assert st == -2 and "k: found 60, required a positive multiple of 8" in _err(lib)
+    st = lib.gdn_proj_gemm(FAKE, FAKE, FAKE, 4, 16, 64, 8, None, 0, None)
+    assert st == -2 and "ld_out: found 8, required >= n_out = 16" in _err(lib)
+    assert lib.gdn_proj_gemm(None, None, None, 0, 16, 64, 16, None, 0, None) == 0
+    need = lib.gdn_proj_workspace_size(4, 2560, 4096)
+    st = lib.gdn_proj_gemm(FAKE, FAKE, FAKE, 4, 2560, 4096, 2560, FAKE, need - 16, None)
+    assert st == -6 and f"required {need} bytes" in _err(lib)
+
+    def dec(cfg_=cfg, proj=gb.CProj(FAKE, FAKE, 2560), ws_bytes=1 << 30):
+        return lib.gdn_layer_decode(ctypes.byref(cfg_), ctypes.byref(prm), ctypes.byref(proj) if proj else None,
+                                    FAKE, FAKE, FAKE, FAKE, 4, 8, FAKE, FAKE, ws_bytes, None)
+
+    assert dec(proj=None) == -1 and "proj: found NULL" in _err(lib)
+    assert dec(proj=gb.CProj(FAKE, FAKE, 2561)) == -2 and "proj.hidden: found 2561" in _err(lib)
+    assert dec(proj=gb.CProj(FAKE, None, 2560)) == -1 and "proj.w_out" in _err(lib)
+    assert dec(cfg_=_cfg(act_dtype=1)) == -7 and "GDN_DTYPE_BF16" in _err(lib)
+    need = lib.gdn_layer_workspace_size(ctypes.byref(cfg), gb.OP_LAYER_DECODE, 4, 1, 2560)
+    assert dec(ws_bytes=need - 1) == -6 and f"required {need} bytes" in _err(lib)
+    st = lib.gdn_layer_varlen_prefill(ctypes.byref(cfg), ctypes.byref(prm), ctypes.byref(gb.CProj(FAKE, FAKE, 2560)),
+                                      FAKE, None, 2, 100, FAKE, None, FAKE, FAKE, 8, FAKE, FAKE, 1 << 30, None)
+    assert st == -1 and "cu_seqlens" in _err(lib)
+
+
+def test_projection_workspace_sizes(lib):
+    """Split-K partials: up to 64 tokens in 64-token tiles, more in 256-token tiles;
+    when the 128-row tiles number at most 74, K (in 64-wide blocks) is split over
+    ks = min(16, 148 // tiles) CTAs, fewer if a CTA would get under 2 blocks; each
+    split tile needs ks x tile-width x 128 fp32."""
+    def want(n_tok, n_out, k):
+        bt = 64 if n_tok <= 64 else 256
+        tiles = -(-n_out // 128) * -(-n_tok // bt)
+        if tiles * 2 > 148:
+            return 0
+        ks, kb = min(16, 148 // tiles), -(-k // 64)
+        while ks > 1 and kb // ks < 2:
+            ks -= 1
+        return tiles * ks * bt * 128 * 4 if ks > 1 else 0
+
+    for n_tok, n_out, k in [(1, 12352, 2560), (64, 12352, 2560), (64, 2560, 4096), (4, 100, 64), (300, 2560, 4096),
+                            (200, 1, 8), (256, 4096, 2560), (8192, 12352, 2560), (100, 256, 1024)]:
+        assert lib.gdn_proj_workspace_size(n_tok, n_out, k) == want(n_tok, n_out, k), (n_tok, n_out, k)
+    assert lib.gdn_proj_workspace_size(64, 12352, 2560) == 0
+    assert lib.gdn_proj_workspace_size(64, 2560, 4096) == 20 * 7 * 64 * 128 * 4
+    assert lib.gdn_proj_workspace_size(256, 2560, 4096) == 20 * 7 * 256 * 128 * 4
+
+
+def test_layer_workspace_sizes(lib):
+    """x [n][8192], z [n][4096], a, b [n][32], y [n][4096] in bf16, then the larger of
+    the two projections' partial sums, each region rounded up to 256 bytes; a layer
+    prefill adds the prefill's own workspace."""
+    cfg = _cfg()
+    up = lambda v: (v + 255) // 256 * 256
+    for n in (1, 4, 64, 300):
+        part = max(lib.gdn_proj_workspace_size(n, 8192 + 4096 + 64, 2560), lib.gdn_proj_workspace_size(n, 2560, 4096))
+        want = up(n * 8192 * 2) + up(n * 4096 * 2) + 2 * up(n * 32 * 2) + up(n * 4096 * 2) + up(part)
+        assert lib.gdn_layer_workspace_size(ctypes.byref(cfg), gb.OP_LAYER_DECODE, n, 1, 2560) == want
+        pf = lib.gdn_workspace_size(ctypes.byref(cfg), gb.OP_VARLEN_PREFILL, n, 3)
+        assert lib.gdn_layer_workspace_size(ctypes.byref(cfg), gb.OP_LAYER_VARLEN_PREFILL, n, 3, 2560) == want + pf
+    assert lib.gdn_layer_workspace_size(ctypes.byref(cfg), gb.OP_LAYER_DECODE, 4, 1, 2561) == 0
+    assert "hidden" in _err(lib)
 
 
 def test_binding_raises_with_message(lib):
