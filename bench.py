@@ -157,6 +157,14 @@ def max_over_ranks(value: float, world: int) -> float:
 # -----------------------------------------------------------------------------
 # the GPU arm
 # -----------------------------------------------------------------------------
+def _side_stream(torch):
+    """A new stream for timed work, after the device has finished everything the
+    default stream was given (input initialisation runs there; a side stream
+    does not wait for it)."""
+    torch.cuda.synchronize()
+    return torch.cuda.Stream()
+
+
 def _dev(stored, torch, device):
     from hybrid_gated_deltanet_gb300 import synth
     if stored.dtype == synth.BF16:
@@ -223,7 +231,7 @@ def decode_parity(torch, cfg, host, layers, n_check=8):
 
 def time_decode(torch, cfg, layers, steps, warmup, use_graph=True):
     from hybrid_gated_deltanet_gb300 import binding as gb
-    stream = torch.cuda.Stream()
+    stream = _side_stream(torch)
 
     def step():
         for L in layers:
@@ -264,7 +272,7 @@ def time_decode_e2e(torch, cfg, layers, steps, warmup):
     has been read out, and y goes back on a third stream.  The timed region
     ends after the last read-back."""
     from hybrid_gated_deltanet_gb300 import binding as gb
-    stream = torch.cuda.Stream()
+    stream = _side_stream(torch)
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
     # each layer's x, z, a, b packed into one pinned host buffer and one device
     # buffer (16-byte aligned views): one copy in per layer
@@ -339,7 +347,7 @@ def prefill_measure(torch, device, steps, warmup, seed, check=True):
     c_fin = torch.empty((3, 8192), dtype=torch.bfloat16, device=device)
     y = torch.empty((PREFILL_T, 4096), dtype=torch.bfloat16, device=device)
     ws = torch.empty(gb.gdn_workspace_size(cfg, gb.OP_CHUNK_PREFILL, PREFILL_T), dtype=torch.uint8, device=device)
-    stream = torch.cuda.Stream()
+    stream = _side_stream(torch)
 
     def call():
         gb.gdn_chunk_prefill(cfg, prm, x, z, a, b, None, None, s_fin, c_fin, y, ws, stream=stream)
@@ -478,6 +486,9 @@ def profile_case(args):
         print(json.dumps(serving_measure(torch, device, args.steps, args.warmup)))
     elif args.case == "ckpt":
         print(json.dumps(ckpt_measure(torch, device, args.steps, args.warmup)))
+    elif args.case == "attn":
+        for rec in attn_measure(torch, device, args.steps, args.warmup):
+            print(json.dumps(rec))
     elif args.case == "proj-decode":
         print(json.dumps(proj_decode_case(torch, device, args.steps, args.warmup, args.batch)))
     elif args.case == "layer":
@@ -490,6 +501,58 @@ def profile_case(args):
         t, _ = prefill_measure(torch, device, args.steps, args.warmup, seed=0, check=False)
         print(json.dumps({"case": args.case, "ms_per_call": round(1e3 * t, 4)}))
     return 0
+
+
+def attn_measure(torch, device, steps, warmup):
+    """Decode attention over a paged KV cache (timing only, N(0, 1) bf16 q, K, V
+    drawn on the device): 16 query / 4 kv-heads of 256 with pages of 16 tokens at
+    B = 1, 16, 64 sequences of 8192 cached tokens, and 24 / 2 heads with pages of
+    528 tokens at B = 4 sequences of 32768.  Bytes: K and V of every cached
+    token read once, the new token's K and V written, q and o."""
+    from hybrid_gated_deltanet_gb300 import binding as gb
+    out = []
+    g = torch.Generator(device=device)
+    g.manual_seed(11)
+    bf = torch.bfloat16
+    for Hq, Hkv, D, page, B, L in ((16, 4, 256, 16, 1, 8192), (16, 4, 256, 16, 16, 8192), (16, 4, 256, 16, 64, 8192),
+                                   (24, 2, 256, 528, 4, 32768)):
+        cfg = gb.AttnConfig(Hq, Hkv, D, page)
+        per = (L + 1 + page - 1) // page
+        n_pages = B * per
+        kp = torch.randn((n_pages, Hkv, page, D), generator=g, device=device).to(bf)
+        vp = torch.randn((n_pages, Hkv, page, D), generator=g, device=device).to(bf)
+        table = torch.randperm(n_pages, generator=g, device=device).to(torch.int32).view(B, per)
+        lens = torch.full((B,), L, dtype=torch.int32, device=device)
+        q = torch.randn((B, Hq, D), generator=g, device=device).to(bf)
+        kn = torch.randn((B, Hkv, D), generator=g, device=device).to(bf)
+        vn = torch.randn((B, Hkv, D), generator=g, device=device).to(bf)
+        o = torch.empty((B, Hq, D), dtype=bf, device=device)
+        nws = gb.gdn_attn_workspace_size(cfg, B, L + 1)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=device)
+        stream = _side_stream(torch)
+
+        def step():
+            gb.gdn_attn_decode(cfg, q, kn, vn, kp, vp, table, lens, L + 1, o, ws, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                step()
+        torch.cuda.synchronize()
+        n = max(20, steps)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                step()
+            e1.record(stream)
+        e1.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / n
+        nbytes = B * (L * Hkv * D * 2 * 2 + Hkv * D * 2 * 2 * 2 + 2 * Hq * D * 2)
+        out.append({"case": "attn", "heads": f"{Hq}/{Hkv}x{D}", "page": page, "batch": B, "context": L,
+                    "splits": None if nws == 0 else nws // (B * Hq * (D + 2) * 4),
+                    "us": round(1e6 * t, 2), "gbs": round(nbytes / t / 1e9, 1)})
+        del kp, vp
+    return out
 
 
 def proj_decode_case(torch, device, steps, warmup, batch):
@@ -544,9 +607,10 @@ def layer_measure(torch, device, steps, warmup, n_layers=4, batch=64):
     vd = geom.value_dim
     projs = [gb.Proj((torch.randn((n_in, hid), generator=g, device=device) / hid ** 0.5).to(bf),
                      (torch.randn((hid, vd), generator=g, device=device) / vd ** 0.5).to(bf)) for _ in range(n_layers)]
-    stream = torch.cuda.Stream()
+    stream = _side_stream(torch)
 
     def timed(fn, n):
+        torch.cuda.synchronize()  # inputs made on the default stream are complete
         with torch.cuda.stream(stream):
             for _ in range(warmup):
                 fn()
@@ -657,7 +721,7 @@ def ckpt_measure(torch, device, steps, warmup, every=1024):
     off = torch.tensor([0, n_ck], dtype=torch.int32, device=device)
     ck = torch.arange(1, 1 + n_ck, dtype=torch.int32, device=device)
     ws = torch.empty(gb.gdn_workspace_size(cfg, gb.OP_VARLEN_PREFILL, T, 1), dtype=torch.uint8, device=device)
-    stream = torch.cuda.Stream()
+    stream = _side_stream(torch)
 
     def plain():
         gb.gdn_varlen_prefill(cfg, prm, x, z, a, b, cu, sl, None, Cp, S, y, ws, stream=stream)
@@ -666,6 +730,7 @@ def ckpt_measure(torch, device, steps, warmup, every=1024):
         gb.gdn_varlen_prefill_ckpt(cfg, prm, x, z, a, b, cu, sl, None, Cp, S, y, every, off, ck, ws, stream=stream)
 
     def timed(fn, n):
+        torch.cuda.synchronize()  # inputs made on the default stream are complete
         with torch.cuda.stream(stream):
             for _ in range(warmup):
                 fn()
@@ -716,7 +781,7 @@ def verify_measure(torch, device, steps, warmup, batch=4, r=4):
     a = torch.randn((batch, r, hv), generator=g, device=device).to(bf)
     b = torch.randn((batch, r, hv), generator=g, device=device).to(bf)
     y = torch.empty((batch, r, hv * dd), dtype=bf, device=device)
-    stream = torch.cuda.Stream()
+    stream = _side_stream(torch)
 
     def verify():
         gb.gdn_verify_rows(cfg, prm, x, z, a, b, Cp, S, slots, snaps, y, stream=stream)
@@ -725,6 +790,7 @@ def verify_measure(torch, device, steps, warmup, batch=4, r=4):
         gb.gdn_commit_rows(cfg, Cp, S, slots, snaps, accept, stream=stream)
 
     def timed(fn, n):
+        torch.cuda.synchronize()  # inputs made on the default stream are complete
         with torch.cuda.stream(stream):
             for _ in range(warmup):
                 fn()
@@ -795,7 +861,7 @@ def serving_measure(torch, device, steps, warmup, n_seq=20, pool=512, batch=256)
     da = torch.randn((batch, 32), generator=g, device=device).to(bf)
     db = torch.randn((batch, 32), generator=g, device=device).to(bf)
     dy = torch.empty((batch, 4096), dtype=bf, device=device)
-    stream = torch.cuda.Stream()
+    stream = _side_stream(torch)
 
     def prefill():
         gb.gdn_varlen_prefill(cfg, prm, x, z, a, b, cu, pf_slots, None, Cp, S, y, ws, stream=stream)
@@ -804,6 +870,7 @@ def serving_measure(torch, device, steps, warmup, n_seq=20, pool=512, batch=256)
         gb.gdn_decode_step(cfg, prm, dx, dz, da, db, Cp, S, dec_slots, dy, stream=stream)
 
     def timed(fn, n):
+        torch.cuda.synchronize()  # inputs made on the default stream are complete
         with torch.cuda.stream(stream):
             for _ in range(warmup):
                 fn()
@@ -944,7 +1011,7 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--batch", type=int, default=64, help="slots of the decode-small case")
     ap.add_argument("--case", default="full", choices=["full", "decode-small", "prefill-small", "serving", "verify", "ckpt", "layer",
-                             "proj-decode"],
+                             "proj-decode", "attn"],
                     help="small cases for ncu captures")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-prefill-tokens", type=int, default=8192)

@@ -100,6 +100,23 @@ class Proj:
         return CProj(_p(self.w_in), _p(self.w_out), self.w_in.shape[1])
 
 
+class CAttnConfig(ctypes.Structure):
+    _fields_ = [("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("scale", ctypes.c_float)]
+
+
+@dataclasses.dataclass
+class AttnConfig:
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int = 256
+    page_size: int = 16
+    scale: float = 0.0
+
+    def c(self) -> CAttnConfig:
+        return CAttnConfig(self.n_q_heads, self.n_kv_heads, self.head_dim, self.page_size, self.scale)
+
+
 def _p(t: Optional[torch.Tensor]):
     if t is None:
         return None
@@ -138,6 +155,8 @@ def load() -> ctypes.CDLL:
         sigs["gdn_proj_gemm"] = [vp, vp, vp, i64, i32, i32, i64, vp, sz, vp]
         sigs["gdn_layer_decode"] = [cfgp, prmp, projp, vp, vp, vp, vp, i32, i32, vp, vp, sz, vp]
         sigs["gdn_layer_varlen_prefill"] = [cfgp, prmp, projp, vp, vp, i32, i64, vp, vp, vp, vp, i32, vp, vp, sz, vp]
+        acfgp = ctypes.POINTER(CAttnConfig)
+        sigs["gdn_attn_decode"] = [acfgp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, sz, vp]
         for name, args in sigs.items():
             fn = getattr(lib, name)
             fn.argtypes = args
@@ -148,6 +167,8 @@ def load() -> ctypes.CDLL:
         lib.gdn_proj_workspace_size.restype = sz
         lib.gdn_layer_workspace_size.argtypes = [cfgp, i32, i64, i32, i32]
         lib.gdn_layer_workspace_size.restype = sz
+        lib.gdn_attn_workspace_size.argtypes = [acfgp, i32, i32]
+        lib.gdn_attn_workspace_size.restype = sz
         lib.gdn_last_error.argtypes = []
         lib.gdn_last_error.restype = ctypes.c_char_p
         lib.gdn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -328,3 +349,23 @@ def gdn_layer_varlen_prefill(cfg: Config, prm: Params, proj: Proj, h, cu_seqlens
                                            _p(cu_seqlens), slot_idx.numel(), h.shape[0], _p(slot_idx),
                                            _p(has_init), _p(conv_pool), _p(state_pool), state_pool.shape[0], _p(out),
                                            _p(workspace), ws_bytes, _stream(stream)))
+
+
+def gdn_attn_workspace_size(cfg: AttnConfig, B: int, max_seq_len: int) -> int:
+    c = cfg.c()
+    n = load().gdn_attn_workspace_size(ctypes.byref(c), B, max_seq_len)
+    msg = load().gdn_last_error().decode()
+    if msg:
+        raise GdnError(-2, msg)
+    return n
+
+
+def gdn_attn_decode(cfg: AttnConfig, q, k_new, v_new, k_pool, v_pool, block_table, seq_lens, max_seq_len: int, o,
+                    workspace=None, stream=None):
+    """q, o [B, Hq, D]; k_new, v_new [B, Hkv, D]; pools [n_pages, Hkv, page, D];
+    block_table int32 [B, max_pages]; seq_lens int32 [B] (tokens before the new one)."""
+    c = cfg.c()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().gdn_attn_decode(ctypes.byref(c), _p(q), _p(k_new), _p(v_new), _p(k_pool), _p(v_pool),
+                                  _p(block_table), _p(seq_lens), q.shape[0], block_table.shape[1], k_pool.shape[0],
+                                  int(max_seq_len), _p(o), _p(workspace), ws_bytes, _stream(stream)))

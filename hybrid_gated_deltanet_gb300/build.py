@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["gdn_api.cu", "gdn_decode.cu", "gdn_prefill.cu", "gdn_noalloc.cu", "gdn_proj.cu"]
+SOURCES = ["gdn_api.cu", "gdn_decode.cu", "gdn_prefill.cu", "gdn_noalloc.cu", "gdn_proj.cu", "gdn_attn.cu"]
 HEADERS = ["gdn_common.cuh", "gdn_internal.h", "gdn_tc.cuh", "gdn_tma.cuh"]
 
 

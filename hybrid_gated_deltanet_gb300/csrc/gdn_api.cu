@@ -592,4 +592,63 @@ gdn_status gdn_layer_varlen_prefill(const gdn_config* cfg, const gdn_params* prm
                        "gdn_layer_varlen_prefill (out-projection)");
 }
 
+static gdn_status attn_check(const gdn_attn_config* cfg) {
+    if (!cfg) return fail(GDN_ERR_NULL, "cfg: found NULL, required a gdn_attn_config");
+    if (cfg->n_kv_heads < 1 || cfg->n_q_heads < 1 || cfg->n_q_heads % cfg->n_kv_heads != 0)
+        return fail(GDN_ERR_SHAPE, "cfg.n_q_heads/n_kv_heads: found %d/%d, required a positive multiple",
+                    cfg->n_q_heads, cfg->n_kv_heads);
+    const int G = cfg->n_q_heads / cfg->n_kv_heads;
+    if (!(G == 1 || G == 2 || (G % 4 == 0 && G <= 32)))
+        return fail(GDN_ERR_UNSUPPORTED, "cfg: G = n_q_heads / n_kv_heads = %d, required 1, 2 or a multiple of 4 "
+                                         "up to 32", G);
+    if (cfg->head_dim != 128 && cfg->head_dim != 256)
+        return fail(GDN_ERR_SHAPE, "cfg.head_dim: found %d, required 128 or 256", cfg->head_dim);
+    if (cfg->page_size < 8 || cfg->page_size > 4096 || cfg->page_size % 8 != 0)
+        return fail(GDN_ERR_SHAPE, "cfg.page_size: found %d, required a multiple of 8 in 8..4096", cfg->page_size);
+    if (!(cfg->scale >= 0.f)) return fail(GDN_ERR_SHAPE, "cfg.scale: found %g, required >= 0", (double)cfg->scale);
+    return GDN_OK;
+}
+
+size_t gdn_attn_workspace_size(const gdn_attn_config* cfg, int32_t B, int32_t max_seq_len) {
+    if (attn_check(cfg) != GDN_OK) return 0;
+    if (B < 0 || max_seq_len < 1) {
+        fail(GDN_ERR_RANGE, "B/max_seq_len: found %d/%d, required >= 0/>= 1", B, max_seq_len);
+        return 0;
+    }
+    ok();
+    return gdn::attn_workspace_bytes(B, cfg->n_q_heads, cfg->n_kv_heads, cfg->head_dim, max_seq_len);
+}
+
+gdn_status gdn_attn_decode(const gdn_attn_config* cfg, const void* q, const void* k_new, const void* v_new,
+                           void* k_pool, void* v_pool, const int32_t* block_table, const int32_t* seq_lens, int32_t B,
+                           int32_t max_pages, int32_t n_pages, int32_t max_seq_len, void* o, void* workspace,
+                           size_t ws_bytes, void* stream) {
+    gdn_status st = attn_check(cfg);
+    if (st) return st;
+    if (B < 0 || B > 65535) return fail(GDN_ERR_RANGE, "B: found %d, required 0..65535", B);
+    if (max_pages < 1 || n_pages < 1 || max_seq_len < 1)
+        return fail(GDN_ERR_RANGE, "max_pages/n_pages/max_seq_len: found %d/%d/%d, required >= 1", max_pages, n_pages,
+                    max_seq_len);
+    if (B == 0) return ok();
+    GDN_REQUIRE_PTR(q, "q");
+    GDN_REQUIRE_PTR(k_new, "k_new");
+    GDN_REQUIRE_PTR(v_new, "v_new");
+    GDN_REQUIRE_PTR(k_pool, "k_pool");
+    GDN_REQUIRE_PTR(v_pool, "v_pool");
+    GDN_REQUIRE_PTR_A(block_table, "block_table", 4u);
+    GDN_REQUIRE_PTR_A(seq_lens, "seq_lens", 4u);
+    GDN_REQUIRE_PTR(o, "o");
+    const size_t need = gdn::attn_workspace_bytes(B, cfg->n_q_heads, cfg->n_kv_heads, cfg->head_dim, max_seq_len);
+    if (need > 0) GDN_REQUIRE_PTR(workspace, "workspace");
+    if (ws_bytes < need)
+        return fail(GDN_ERR_WORKSPACE, "workspace: found %zu bytes, required %zu bytes", ws_bytes, need);
+    gdn::AttnJob j;
+    j.q = q; j.k_new = k_new; j.v_new = v_new; j.k_pool = k_pool; j.v_pool = v_pool;
+    j.block_table = block_table; j.seq_lens = seq_lens; j.o = o; j.ws = workspace;
+    j.B = B; j.Hq = cfg->n_q_heads; j.Hkv = cfg->n_kv_heads; j.D = cfg->head_dim; j.page = cfg->page_size;
+    j.max_pages = max_pages; j.n_pages = n_pages; j.max_seq_len = max_seq_len;
+    j.scale = cfg->scale > 0.f ? cfg->scale : 1.0f / sqrtf((float)cfg->head_dim);
+    return cuda_status(gdn::launch_attn_decode(j, (cudaStream_t)stream), "gdn_attn_decode");
+}
+
 }  // extern "C"

@@ -116,6 +116,25 @@ struct ProjPlan {
 ProjPlan proj_plan(int32_t n_out, int32_t k, int64_t n_tok);
 cudaError_t launch_proj(const ProjJob& job, cudaStream_t st);
 
+// decode attention over a paged KV cache (bf16), GQA with G = Hq / Hkv in
+// {1, 2, 4, 8, 12, 16}; D in {128, 256}
+struct AttnJob {
+    const void *q, *k_new, *v_new;
+    void *k_pool, *v_pool;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    void* o;
+    void* ws;
+    int B, Hq, Hkv, D, page, max_pages, n_pages, max_seq_len;
+    float scale;
+};
+struct AttnPlan {
+    int n_split, span;
+};
+AttnPlan attn_plan(int B, int Hq, int Hkv, int max_seq_len);
+size_t attn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_seq_len);
+cudaError_t launch_attn_decode(const AttnJob& job, cudaStream_t st);
+
 // read and clear the device status word of each kernel file (synchronous)
 cudaError_t take_device_status_decode(unsigned* out);
 cudaError_t take_device_status_prefill(unsigned* out);

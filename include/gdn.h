@@ -337,6 +337,51 @@ gdn_status gdn_layer_varlen_prefill(const gdn_config* cfg, const gdn_params* prm
  * config. */
 size_t gdn_workspace_size(const gdn_config* cfg, int32_t op, int64_t n_tokens, int32_t n_seq);
 
+/* ---- Decode attention of the hybrid's full-attention layers ------------------
+ * The hybrid's other layers are ordinary grouped-query attention over a KV
+ * cache ("Forge: how I wrote my own inference engine and overtook llama.cpp",
+ * its architecture section: 16 of 64 layers GQA attention, 4 kv-heads of 256
+ * dims; its 25-26 August entry: split-KV decode, the query heads of a kv-head
+ * packed together so that each kv-head is read once).  The cache is paged: a
+ * page holds the K and V of page_size tokens of one layer ("Hybrid
+ * transformers under load ...", braintools.ru, section 4.1: 4 kv-heads x 256
+ * bf16 values per token for Qwen3.5-4B).  Query head h reads kv-head
+ * floor(h / G), G = n_q_heads / n_kv_heads. */
+typedef struct gdn_attn_config {
+    int32_t n_q_heads, n_kv_heads; /* G = n_q_heads / n_kv_heads in {1, 2} or a multiple of 4 up to 32 */
+    int32_t head_dim;              /* 128 or 256 */
+    int32_t page_size;             /* tokens per page: a multiple of 8, 8 .. 4096 */
+    float scale;                   /* softmax scale; 0 means 1 / sqrt(head_dim) */
+} gdn_attn_config;
+
+/* One decode step for B sequences: sequence b holds seq_lens[b] tokens in the
+ * cache; its new token (q, k_new, v_new) is appended at position seq_lens[b]
+ * and attends to all seq_lens[b] + 1 tokens:
+ *   o[b][h] = softmax_t(scale q[b][h] . K[b][t][kvh]) V[b][t][kvh], kvh = floor(h / G).
+ *   q, o bf16 [B][n_q_heads][head_dim]; k_new, v_new bf16 [B][n_kv_heads][head_dim]
+ *   k_pool, v_pool bf16 [n_pages][n_kv_heads][page_size][head_dim]: token t of
+ *   sequence b sits on page block_table[b][t / page_size] at row t % page_size.
+ *   block_table int32 [B][max_pages]; seq_lens int32 [B] (device).
+ *   max_seq_len: host bound on every seq_lens[b] + 1 (tokens past it are left out).
+ *   A token whose page index is outside [0, n_pages) is left out of the
+ *   softmax; a sequence with seq_lens[b] < 0 or seq_lens[b] >= max_pages *
+ *   page_size is skipped (nothing read or written, its o rows left as they
+ *   were).  The page receiving a new token must belong to that sequence alone
+ *   (pages shared between sequences are read only).
+ *   workspace: gdn_attn_workspace_size(cfg, B, max_seq_len) bytes (the
+ *   partial results of the context splits; NULL when 0).
+ *   All pointers 16-byte aligned.  bf16 in, fp32 softmax and accumulation,
+ *   bf16 out. */
+gdn_status gdn_attn_decode(const gdn_attn_config* cfg, const void* q, const void* k_new,
+                           const void* v_new, void* k_pool, void* v_pool,
+                           const int32_t* block_table, const int32_t* seq_lens, int32_t B,
+                           int32_t max_pages, int32_t n_pages, int32_t max_seq_len, void* o,
+                           void* workspace, size_t ws_bytes, void* stream);
+
+/* Workspace bytes of gdn_attn_decode (depends on the sizes only; 0 on invalid
+ * arguments, with gdn_last_error set). */
+size_t gdn_attn_workspace_size(const gdn_attn_config* cfg, int32_t B, int32_t max_seq_len);
+
 /* Workspace bytes of gdn_layer_decode (op GDN_OP_LAYER_DECODE, n_tokens = B)
  * or gdn_layer_varlen_prefill (op GDN_OP_LAYER_VARLEN_PREFILL) for a model
  * width `hidden`.  Returns 0 and sets gdn_last_error on invalid arguments. */

@@ -244,3 +244,26 @@ def test_binding_raises_with_message(lib):
     cfg = gb.Config(16, 30, 128, 128)
     with pytest.raises(gb.GdnError, match="GDN_ERR_SHAPE: cfg.n_v_heads: found 30"):
         gb.gdn_workspace_size(cfg, gb.OP_CHUNK_PREFILL, 10)
+
+
+def test_attention_validation(lib):
+    def cfg(**kw):
+        c = gb.AttnConfig(16, 4, 256, 16)
+        for k, v in kw.items():
+            setattr(c, k, v)
+        return c.c()
+
+    def call(c, B=2, ws=None, ws_bytes=0, max_seq=100):
+        return lib.gdn_attn_decode(ctypes.byref(c), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, B, 8, 64, max_seq, FAKE,
+                                   ws, ws_bytes, None)
+
+    assert call(cfg(n_q_heads=12, n_kv_heads=8)) == -2 and "n_q_heads/n_kv_heads: found 12/8" in _err(lib)
+    assert call(cfg(n_q_heads=24, n_kv_heads=4)) == -7 and "G = n_q_heads / n_kv_heads = 6" in _err(lib)
+    assert call(cfg(head_dim=64)) == -2 and "head_dim: found 64" in _err(lib)
+    assert call(cfg(page_size=12)) == -2 and "page_size: found 12" in _err(lib)
+    assert call(cfg(), B=0) == 0
+    need = lib.gdn_attn_workspace_size(ctypes.byref(cfg()), 2, 5000)
+    assert need > 0
+    assert call(cfg(), max_seq=5000) == -1 and "workspace" in _err(lib)
+    assert call(cfg(), max_seq=5000, ws=FAKE, ws_bytes=need - 1) == -6 and f"required {need} bytes" in _err(lib)
+    assert call(cfg(), max_seq=5000, ws=FAKE + 8, ws_bytes=need) == -4
