@@ -552,6 +552,51 @@ def attn_measure(torch, device, steps, warmup):
                     "splits": None if nws == 0 else nws // (B * Hq * (D + 2) * 4),
                     "us": round(1e6 * t, 2), "gbs": round(nbytes / t / 1e9, 1)})
         del kp, vp
+    # prefill: (cached, new) tokens per sequence; flops 4 d Hq per (query, visible key) pair
+    for Hq, Hkv, D, page, seqs in ((16, 4, 256, 16, [(0, 8192)]), (16, 4, 256, 16, [(8192, 512)] * 4),
+                                   (24, 2, 256, 528, [(0, 32768)])):
+        cfg = gb.AttnConfig(Hq, Hkv, D, page)
+        per = [(c + n + page - 1) // page for c, n in seqs]
+        n_pages, max_pages = sum(per), max(per)
+        N = sum(n for _, n in seqs)
+        kp = torch.randn((n_pages, Hkv, page, D), generator=g, device=device).to(bf)
+        vp = torch.randn((n_pages, Hkv, page, D), generator=g, device=device).to(bf)
+        perm = torch.randperm(n_pages, generator=g, device=device).to(torch.int32)
+        table = torch.full((len(seqs), max_pages), -1, dtype=torch.int32, device=device)
+        o0 = 0
+        for i, pcount in enumerate(per):
+            table[i, :pcount] = perm[o0:o0 + pcount]
+            o0 += pcount
+        cu = torch.tensor([0] + list(np.cumsum([n for _, n in seqs])), dtype=torch.int32, device=device)
+        ctx = torch.tensor([c for c, _ in seqs], dtype=torch.int32, device=device)
+        q = torch.randn((N, Hq, D), generator=g, device=device).to(bf)
+        kn = torch.randn((N, Hkv, D), generator=g, device=device).to(bf)
+        vn = torch.randn((N, Hkv, D), generator=g, device=device).to(bf)
+        o = torch.empty((N, Hq, D), dtype=bf, device=device)
+        stream = _side_stream(torch)
+
+        def pstep():
+            gb.gdn_attn_prefill(cfg, q, kn, vn, kp, vp, table, cu, ctx, o, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                pstep()
+        torch.cuda.synchronize()
+        n = max(5, steps // 4)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(n):
+                pstep()
+            e1.record(stream)
+        e1.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / n
+        pairs = sum(nn * c + nn * (nn + 1) // 2 for c, nn in seqs)
+        fl = 4.0 * D * Hq * pairs
+        out.append({"case": "attn-prefill", "heads": f"{Hq}/{Hkv}x{D}", "page": page, "seqs": seqs[:1],
+                    "n_seq": len(seqs), "ms": round(1e3 * t, 3), "tflops": round(fl / t / 1e12, 1),
+                    "tokens_per_s": round(N / t, 1)})
+        del kp, vp
     return out
 
 

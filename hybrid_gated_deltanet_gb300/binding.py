@@ -157,6 +157,7 @@ def load() -> ctypes.CDLL:
         sigs["gdn_layer_varlen_prefill"] = [cfgp, prmp, projp, vp, vp, i32, i64, vp, vp, vp, vp, i32, vp, vp, sz, vp]
         acfgp = ctypes.POINTER(CAttnConfig)
         sigs["gdn_attn_decode"] = [acfgp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, sz, vp]
+        sigs["gdn_attn_prefill"] = [acfgp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, vp, vp]
         for name, args in sigs.items():
             fn = getattr(lib, name)
             fn.argtypes = args
@@ -369,3 +370,13 @@ def gdn_attn_decode(cfg: AttnConfig, q, k_new, v_new, k_pool, v_pool, block_tabl
     _check(load().gdn_attn_decode(ctypes.byref(c), _p(q), _p(k_new), _p(v_new), _p(k_pool), _p(v_pool),
                                   _p(block_table), _p(seq_lens), q.shape[0], block_table.shape[1], k_pool.shape[0],
                                   int(max_seq_len), _p(o), _p(workspace), ws_bytes, _stream(stream)))
+
+
+def gdn_attn_prefill(cfg: AttnConfig, q, k_new, v_new, k_pool, v_pool, block_table, cu_seqlens, ctx_lens, o,
+                     stream=None):
+    """q, o [N, Hq, D]; k_new, v_new [N, Hkv, D]; new tokens of sequence s are rows
+    cu_seqlens[s] .. cu_seqlens[s+1] at positions ctx_lens[s] + i."""
+    c = cfg.c()
+    _check(load().gdn_attn_prefill(ctypes.byref(c), _p(q), _p(k_new), _p(v_new), _p(k_pool), _p(v_pool),
+                                   _p(block_table), _p(cu_seqlens), _p(ctx_lens), ctx_lens.numel(), q.shape[0],
+                                   block_table.shape[1], k_pool.shape[0], _p(o), _stream(stream)))

@@ -651,4 +651,34 @@ gdn_status gdn_attn_decode(const gdn_attn_config* cfg, const void* q, const void
     return cuda_status(gdn::launch_attn_decode(j, (cudaStream_t)stream), "gdn_attn_decode");
 }
 
+gdn_status gdn_attn_prefill(const gdn_attn_config* cfg, const void* q, const void* k_new, const void* v_new,
+                            void* k_pool, void* v_pool, const int32_t* block_table, const int32_t* cu_seqlens,
+                            const int32_t* ctx_lens, int32_t n_seq, int64_t n_tokens, int32_t max_pages,
+                            int32_t n_pages, void* o, void* stream) {
+    gdn_status st = attn_check(cfg);
+    if (st) return st;
+    if (n_seq < 0 || n_seq > 65535) return fail(GDN_ERR_RANGE, "n_seq: found %d, required 0..65535", n_seq);
+    if (n_tokens < 0 || n_tokens > (int64_t)1 << 30)
+        return fail(GDN_ERR_RANGE, "n_tokens: found %lld, required 0..2^30", (long long)n_tokens);
+    if (max_pages < 1 || n_pages < 1)
+        return fail(GDN_ERR_RANGE, "max_pages/n_pages: found %d/%d, required >= 1", max_pages, n_pages);
+    if (n_seq == 0 || n_tokens == 0) return ok();
+    GDN_REQUIRE_PTR(q, "q");
+    GDN_REQUIRE_PTR(k_new, "k_new");
+    GDN_REQUIRE_PTR(v_new, "v_new");
+    GDN_REQUIRE_PTR(k_pool, "k_pool");
+    GDN_REQUIRE_PTR(v_pool, "v_pool");
+    GDN_REQUIRE_PTR_A(block_table, "block_table", 4u);
+    GDN_REQUIRE_PTR_A(cu_seqlens, "cu_seqlens", 4u);
+    GDN_REQUIRE_PTR_A(ctx_lens, "ctx_lens", 4u);
+    GDN_REQUIRE_PTR(o, "o");
+    gdn::AttnPfJob j;
+    j.q = q; j.k_new = k_new; j.v_new = v_new; j.k_pool = k_pool; j.v_pool = v_pool;
+    j.block_table = block_table; j.cu_seqlens = cu_seqlens; j.ctx_lens = ctx_lens; j.o = o;
+    j.n_seq = n_seq; j.Hq = cfg->n_q_heads; j.Hkv = cfg->n_kv_heads; j.D = cfg->head_dim; j.page = cfg->page_size;
+    j.max_pages = max_pages; j.n_pages = n_pages; j.n_tokens = n_tokens;
+    j.scale = cfg->scale > 0.f ? cfg->scale : 1.0f / sqrtf((float)cfg->head_dim);
+    return cuda_status(gdn::launch_attn_prefill(j, (cudaStream_t)stream), "gdn_attn_prefill");
+}
+
 }  // extern "C"

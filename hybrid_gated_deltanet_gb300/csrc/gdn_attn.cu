@@ -22,8 +22,12 @@
 
 #include <cstdlib>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "gdn_common.cuh"
 #include "gdn_internal.h"
+#include "gdn_tc.cuh"
 #include "gdn_tma.cuh"
 
 namespace gdn {
@@ -352,6 +356,465 @@ cudaError_t launch_decode_d(const AttnArgs& A, int G, cudaStream_t st) {
     return cudaErrorInvalidValue;
 }
 
+// ---------------------------------------------------------------------------
+// Prefill (chunk) attention: n_s new tokens of sequence s at positions
+// P_s .. P_s + n_s - 1 attend causally to the sequence's tokens 0 .. own position
+// (the bottom-right aligned mask of forge's 27 August entry: row i sees
+// 0 .. kv0 + i).  The new K and V are first appended to their pages
+// (k_attn_append), then every key comes from the pool.
+//
+// k_attn_prefill: one CTA per (tile of TQ = 128 / G new tokens of one sequence,
+// kv-head); the tile's 128 MMA rows are (token, query head) pairs of that kv-head,
+// so K and V of a kv-head are read once for its G heads.  Per tile of 128 keys:
+//   S = Q K^T   (tcgen05, M = 128, N = 128, K = d: d/16 instructions, S in TMEM)
+//   softmax rows on 4 warps (thread = row), P in bf16 -> shared memory
+//   O += P V    (M = 128, N = d, K = 128: 8 instructions, V read MN-major)
+// with an online softmax whose reference maximum moves only when a row's
+// maximum grows by more than 8 / scale (O is then rescaled in TMEM), so the
+// common step never touches O.  Warp 0 drives the TMA loads (Q once; K and V
+// per key tile, a box per run of page rows), warp 1 issues the MMAs.
+// ---------------------------------------------------------------------------
+struct AttnPfArgs {
+    const int32_t* block_table;  // [n_seq][max_pages]
+    const int32_t* cu_seqlens;   // [n_seq + 1] new tokens
+    const int32_t* ctx_lens;     // [n_seq] cached tokens before the new ones
+    __nv_bfloat16* o;            // [N][Hq][D]
+    int n_seq, Hq, Hkv, G, TQ, page, R, max_pages, n_pages;
+    int64_t n_slots;  // q tiles: N / TQ + n_seq + 1 slots (slot of tile c of sequence s: cu[s] / TQ + s + c)
+    float scale_log2;  // scale * log2(e)
+};
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// all `count` threads of named barrier `id` agree on `pred` (logical and)
+__device__ __forceinline__ bool named_bar_and(int id, int count, bool pred) {
+    int r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n barrier.red.and.pred q, %2, %3, p;\n selp.s32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((int)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr, uint32_t lbo) {
+    // 128-byte swizzled MN-major operand: atoms of 64 (MN) x 8 (K) elements; lbo =
+    // byte stride between atoms along MN, 1024 = stride between 8-row groups along K
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d),
+        "l"(ad), "l"(bd), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+template <int D>
+struct PfLay {
+    static constexpr int ATOM = 128 * 128;  // 128 rows x 128 bytes
+    static constexpr int Q = 0;             // [128 rows][D] K-major: D / 64 atoms
+    static constexpr int K = Q + (D / 64) * ATOM;
+    static constexpr int V = K + (D / 64) * ATOM;  // [128 keys][D] MN-major: D / 64 atoms of 128 keys
+    static constexpr int P = V + (D / 64) * ATOM;  // [128 rows][128 keys] K-major: 2 atoms
+    static constexpr int BAR = P + 2 * ATOM;
+    static constexpr int SMEM = BAR + 16 * 8;
+    static constexpr int SMEM_ALLOC = SMEM + 1024;
+    static constexpr int TMEM_COLS = D == 256 ? 512 : 256;  // S [0, 128), O [TMEM_COLS - D, TMEM_COLS)
+    static constexpr int O_COL = TMEM_COLS - D;
+};
+
+__device__ __forceinline__ int pf_slot_seq(const AttnPfArgs& A, int64_t slot) {
+    int lo = 0, hi = A.n_seq - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)A.cu_seqlens[mid] / A.TQ + mid <= slot) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    k_attn_prefill(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ AttnPfArgs A) {
+    using Ly = PfLay<D>;
+    constexpr int NA = D / 64;  // 64-wide atoms along d
+    const int64_t slot = A.n_slots - 1 - blockIdx.x;  // late (long) tiles first
+    const int kvh = blockIdx.y;
+    const int s = pf_slot_seq(A, slot);
+    const int cu0 = A.cu_seqlens[s], n_s = A.cu_seqlens[s + 1] - cu0;
+    const int P = A.ctx_lens[s];
+    const int t0 = (int)(slot - ((int64_t)cu0 / A.TQ + s)) * A.TQ;  // first new token of the tile
+    if (t0 < 0 || t0 >= n_s || P < 0) return;
+    const int nq = min(A.TQ, n_s - t0);
+    const int L = P + n_s;                                // keys of the sequence
+    const int n_kv = (P + t0 + nq + 127) / 128;           // key tiles the tile's last row needs
+    if ((int64_t)(L + A.page - 1) / A.page > A.max_pages) return;  // pages past the block table
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::BAR);
+    uint64_t *full_q = bars, *full_k = bars + 1, *full_v = bars + 2, *s_done = bars + 3, *s_read = bars + 4,
+             *p_ready = bars + 5, *pv_done = bars + 6;
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
+    if (tid == 0) {
+        mbar_init(full_q, 1);
+        mbar_init(full_k, 1);
+        mbar_init(full_v, 1);
+        mbar_init(s_done, 1);
+        mbar_init(s_read, 4);   // one arrival per softmax warp
+        mbar_init(p_ready, 1);
+        mbar_init(pv_done, 1);
+        fence_mbar_init();
+    }
+    if (warp == 1) tc::alloc(tslot, Ly::TMEM_COLS);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = *tslot;
+    bool ok = true;
+
+    // rows [k0, k0 + 128) of the sequence: bytes the pool can deliver for them
+    auto seg_page = [&](int pos) -> int {
+        const int pid = A.block_table[(size_t)s * A.max_pages + pos / A.page];
+        return (pid >= 0 && pid < A.n_pages) ? pid : -1;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // Q of the tile: tokens cu0 + t0 .., heads kvh G ..; rows past the tile are other
+            // tokens or zeros (never stored)
+            mbar_arrive_expect_tx(full_q, (uint32_t)(NA * A.TQ * A.G * 128));
+            for (int a = 0; a < NA; ++a) tma_load_3d(sm + Ly::Q + a * Ly::ATOM, &tq, a * 64, kvh * A.G, cu0 + t0, full_q);
+            int last_k = -1, last_v = -1;
+            for (int j = 0; j < n_kv && ok; ++j) {
+                const int k0 = j * 128;
+                // K_j once S_{j-1} has read K_{j-1}
+                if (j > 0 && !mbar_wait(s_done, (uint32_t)((j - 1) & 1))) { ok = false; break; }
+                uint32_t bytes = 0;
+                for (int r0 = 0; r0 < 128; r0 += A.R)
+                    if (k0 + r0 < L && seg_page(k0 + r0) >= 0) bytes += NA * A.R * 128;
+                mbar_arrive_expect_tx(full_k, bytes);
+                for (int r0 = 0; r0 < 128; r0 += A.R) {
+                    const int pos = k0 + r0;
+                    const int pid = pos < L ? seg_page(pos) : -1;
+                    if (pid < 0) continue;
+                    for (int a = 0; a < NA; ++a)
+                        tma_load_4d(sm + Ly::K + a * Ly::ATOM + r0 * 128, &tk, a * 64, pos % A.page, kvh, pid, full_k);
+                }
+                last_k = j;
+                // V_j once PV_{j-1} has read V_{j-1}
+                if (j > 0 && !mbar_wait(pv_done, (uint32_t)((j - 1) & 1))) { ok = false; break; }
+                mbar_arrive_expect_tx(full_v, bytes);
+                for (int r0 = 0; r0 < 128; r0 += A.R) {
+                    const int pos = k0 + r0;
+                    const int pid = pos < L ? seg_page(pos) : -1;
+                    if (pid < 0) continue;
+                    for (int a = 0; a < NA; ++a)
+                        tma_load_4d(sm + Ly::V + a * Ly::ATOM + r0 * 128, &tv, a * 64, pos % A.page, kvh, pid, full_v);
+                }
+                last_v = j;
+            }
+            // copies still in flight land before the CTA leaves
+            if (last_k >= 0) mbar_wait(full_k, (uint32_t)(last_k & 1));
+            if (last_v >= 0) mbar_wait(full_v, (uint32_t)(last_v & 1));
+            if (!mbar_wait(full_q, 0)) ok = false;
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
+                                         ((uint32_t)(128 >> 4) << 24);
+            constexpr uint32_t idesc_o = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) |
+                                         ((uint32_t)(D >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+            const uint32_t q0 = tc::smem_addr(sm + Ly::Q), kk0 = tc::smem_addr(sm + Ly::K);
+            const uint32_t v0 = tc::smem_addr(sm + Ly::V), p0 = tc::smem_addr(sm + Ly::P);
+            ok = mbar_wait(full_q, 0);
+            for (int j = 0; j < n_kv && ok; ++j) {
+                // S_j = Q K_j^T once K_j has landed and the softmax has read S_{j-1}
+                if (!mbar_wait(full_k, (uint32_t)(j & 1))) { ok = false; break; }
+                if (j > 0 && !mbar_wait(s_read, (uint32_t)((j - 1) & 1))) { ok = false; break; }
+                tc::fence_after();
+                for (int kd = 0; kd < D / 16; ++kd) {
+                    const uint32_t off = (uint32_t)((kd >> 2) * Ly::ATOM + (kd & 3) * 32);
+                    mma_f16(tm, tc::sdesc(q0 + off), tc::sdesc(kk0 + off), idesc_s, kd > 0 ? 1u : 0u);
+                }
+                tc::commit(s_done);
+                // O += P_j V_j once P_j is written and V_j has landed
+                if (!mbar_wait(p_ready, (uint32_t)(j & 1))) { ok = false; break; }
+                if (!mbar_wait(full_v, (uint32_t)(j & 1))) { ok = false; break; }
+                tc::fence_after();
+                for (int kk = 0; kk < 8; ++kk) {  // 16 keys per instruction
+                    const uint32_t pa = p0 + (uint32_t)((kk >> 2) * Ly::ATOM + (kk & 3) * 32);
+                    const uint32_t vb = v0 + (uint32_t)(kk * 16 * 128);
+                    mma_f16(tm + Ly::O_COL, tc::sdesc(pa), sdesc_mn(vb, Ly::ATOM), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc::commit(pv_done);
+            }
+        }
+    } else {
+        // ---- softmax and epilogue: thread = row r of the tile (TMEM lane r) ----------------
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const int tl = r / A.G, g = r % A.G;      // token in the tile, head in the group
+        const bool row_ok = tl < nq;              // rows past the tile's tokens are never stored
+        const int qpos = P + t0 + tl;             // the row's position in the sequence
+        float m_ref = -INFINITY, l = 0.f;
+        unsigned char* prow = sm + Ly::P + r * 128;
+        for (int j = 0; j < n_kv; ++j) {
+            const int k0 = j * 128;
+            bool w = mbar_wait(s_done, (uint32_t)(j & 1));
+            if (!named_bar_and(1, 128, w)) { ok = false; break; }
+            tc::fence_after();
+            float sv[128];
+#pragma unroll
+            for (int c0 = 0; c0 < 128; c0 += 16) tc::ld16(tc::taddr(tm, 32 * q4, c0), sv + c0);
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(s_read)) : "memory");
+            // keys on pages outside the pool, per run of R page rows (bit c of dead[c / 32])
+            uint32_t dead[4] = {0u, 0u, 0u, 0u};
+            for (int r0 = 0; r0 < 128; r0 += A.R) {
+                const int pos = k0 + r0;
+                if (pos < L && seg_page(pos) < 0)
+                    for (int c = r0; c < r0 + A.R; c += 32) {
+                        const int n = min(32, r0 + A.R - c);
+                        dead[c >> 5] |= (n == 32 ? 0xffffffffu : ((1u << n) - 1u)) << (c & 31);
+                    }
+            }
+            // mask: causal (which also keeps the key inside the sequence) and on a page of the pool
+            float mt = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; ++c) {
+                const int pos = k0 + c;
+                const bool v = row_ok && pos <= qpos && !((dead[c >> 5] >> (c & 31)) & 1u);
+                sv[c] = v ? sv[c] : -INFINITY;
+                mt = fmaxf(mt, sv[c]);
+            }
+            // P_j may replace P_{j-1} (and O be rescaled) once PV_{j-1} is done
+            w = (j == 0) || mbar_wait(pv_done, (uint32_t)((j - 1) & 1));
+            if (!named_bar_and(1, 128, w)) { ok = false; break; }
+            tc::fence_after();
+            // move a row's reference maximum when its maximum grew by more than 2^8 in the
+            // exponent: rescale its O and l.  TMEM loads and stores are warp-collective, so
+            // the warp rescales together when any of its rows needs it (the others by 1).
+            float f = 1.f;
+            if (mt > -INFINITY && (m_ref == -INFINITY || (mt - m_ref) * A.scale_log2 > 8.f)) {
+                if (j > 0 && m_ref > -INFINITY) {
+                    f = exp2f((m_ref - mt) * A.scale_log2);
+                    l *= f;
+                }
+                m_ref = mt;
+            }
+            if (__any_sync(0xffffffffu, f != 1.f)) {
+#pragma unroll 1
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    float ov[16];
+                    tc::ld16(tc::taddr(tm, 32 * q4, Ly::O_COL + c0), ov);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) ov[c] *= f;
+                    tc::st16(tc::taddr(tm, 32 * q4, Ly::O_COL + c0), ov);
+                }
+                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            }
+            // p = 2^((s - m_ref) scale log2 e) in bf16 -> P row (128-byte swizzle, K-major)
+#pragma unroll
+            for (int c8 = 0; c8 < 16; ++c8) {
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a0 = sv[c8 * 8 + 2 * e], a1 = sv[c8 * 8 + 2 * e + 1];
+                    const float p0 = a0 == -INFINITY ? 0.f : exp2f((a0 - m_ref) * A.scale_log2);
+                    const float p1 = a1 == -INFINITY ? 0.f : exp2f((a1 - m_ref) * A.scale_log2);
+                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                    // the sum takes the rounded values, like the product
+                    const float2 back = __bfloat1622float2(h2);
+                    l += back.x + back.y;
+                    pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+                }
+                const int atom = c8 >> 3, ch = c8 & 7;
+                *reinterpret_cast<uint4*>(prow + atom * Ly::ATOM + ((ch ^ (r & 7)) << 4)) =
+                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            // V rows with no key behind them (past the sequence or on a missing page) -> 0,
+            // so that 0 x garbage never reaches O
+            w = mbar_wait(full_v, (uint32_t)(j & 1));
+            if (!named_bar_and(1, 128, w)) { ok = false; break; }
+            {
+                const int key = r;  // thread r clears V row r when needed
+                const int pos = k0 + key;
+                const bool dead = pos >= L || seg_page(pos - (pos % A.R)) < 0;
+                if (dead) {
+#pragma unroll
+                    for (int a = 0; a < NA; ++a) {
+                        uint4* vr = reinterpret_cast<uint4*>(sm + Ly::V + a * Ly::ATOM + key * 128);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) vr[c] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc::fence_before();
+            named_bar_sync(1, 128);
+            if (tid == 64) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(p_ready)) : "memory");
+        }
+        // ---- epilogue: o = O / l (TMEM loads by the whole warp, stores by rows in the tile)
+        bool w = ok && mbar_wait(pv_done, (uint32_t)((n_kv - 1) & 1));
+        w = named_bar_and(1, 128, w);
+        if (!w) ok = false;
+        tc::fence_after();
+        if (w) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            __nv_bfloat16* dst = A.o + ((size_t)(cu0 + t0 + tl) * A.Hq + kvh * A.G + g) * D;
+#pragma unroll 1
+            for (int c0 = 0; c0 < D; c0 += 16) {
+                float ov[16];
+                tc::ld16(tc::taddr(tm, 32 * q4, Ly::O_COL + c0), ov);
+                uint4 pk[2];
+                __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) h[c] = __floats2bfloat162_rn(ov[2 * c] * inv, ov[2 * c + 1] * inv);
+                if (row_ok) {
+                    reinterpret_cast<uint4*>(dst + c0)[0] = pk[0];
+                    reinterpret_cast<uint4*>(dst + c0)[1] = pk[1];
+                }
+            }
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (!ok && lane == 0) report_device_status(kDevWaitTimeout);
+    if (warp == 1) tc::dealloc(tm, Ly::TMEM_COLS);
+}
+
+// new K and V rows of every token into their pages: thread = 16 bytes of a row
+__global__ void k_attn_append(const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
+                              __nv_bfloat16* k_pool, __nv_bfloat16* v_pool, const int32_t* block_table,
+                              const int32_t* cu_seqlens, const int32_t* ctx_lens, int n_seq, int64_t n_tokens,
+                              int Hkv, int D, int page, int max_pages, int n_pages) {
+    const int64_t tok = blockIdx.x;
+    if (tok >= n_tokens) return;
+    int lo = 0, hi = n_seq - 1;  // the sequence holding token tok
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cu_seqlens[mid] <= tok) lo = mid;
+        else hi = mid - 1;
+    }
+    const int P = ctx_lens[lo];
+    if (P < 0) return;
+    const int64_t pos = P + (tok - cu_seqlens[lo]);
+    if (pos / page >= max_pages) return;
+    const int pid = block_table[(size_t)lo * max_pages + pos / page];
+    if (pid < 0 || pid >= n_pages) return;
+    const int per_row = D / 8;
+    for (int i = threadIdx.x; i < Hkv * per_row; i += blockDim.x) {
+        const int h = i / per_row, c = i % per_row;
+        const size_t src = ((size_t)tok * Hkv + h) * D + c * 8;
+        const size_t dst = (((size_t)pid * Hkv + h) * page + pos % page) * D + c * 8;
+        *reinterpret_cast<uint4*>(k_pool + dst) = *reinterpret_cast<const uint4*>(k_new + src);
+        *reinterpret_cast<uint4*>(v_pool + dst) = *reinterpret_cast<const uint4*>(v_new + src);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+template <int D>
+cudaError_t launch_prefill_attn(const AttnPfJob& j, cudaStream_t st) {
+    using Ly = PfLay<D>;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(k_attn_prefill<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Ly::SMEM_ALLOC);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    PFN_cuTensorMapEncodeTiled_v12000 enc = at_encode_fn();
+    if (!enc) return cudaErrorInvalidValue;
+    const int G = j.Hq / j.Hkv;
+    AttnPfArgs A;
+    A.block_table = j.block_table;
+    A.cu_seqlens = j.cu_seqlens;
+    A.ctx_lens = j.ctx_lens;
+    A.o = static_cast<__nv_bfloat16*>(j.o);
+    A.n_seq = j.n_seq;
+    A.Hq = j.Hq;
+    A.Hkv = j.Hkv;
+    A.G = G;
+    A.TQ = 128 / G;
+    A.page = j.page;
+    int R = 128;
+    while (j.page % R) R >>= 1;  // rows per K/V box: gcd(page, 128)
+    A.R = R;
+    A.max_pages = j.max_pages;
+    A.n_pages = j.n_pages;
+    A.n_slots = j.n_tokens / A.TQ + j.n_seq + 1;
+    A.scale_log2 = j.scale * 1.4426950408889634f;
+    CUtensorMap mq, mk, mv;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)j.Hq, (cuuint64_t)j.n_tokens};
+        const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)j.Hq * D * 2};
+        const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)A.TQ};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(j.q), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    for (int w = 0; w < 2; ++w) {
+        const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)j.page, (cuuint64_t)j.Hkv, (cuuint64_t)j.n_pages};
+        const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)j.page * D * 2,
+                                       (cuuint64_t)j.Hkv * j.page * D * 2};
+        const cuuint32_t box[4] = {64, (cuuint32_t)R, 1, 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(w == 0 ? &mk : &mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, w == 0 ? j.k_pool : j.v_pool, dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    k_attn_append<<<(unsigned)j.n_tokens, 128, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(j.k_new), static_cast<const __nv_bfloat16*>(j.v_new),
+        static_cast<__nv_bfloat16*>(j.k_pool), static_cast<__nv_bfloat16*>(j.v_pool), j.block_table, j.cu_seqlens,
+        j.ctx_lens, j.n_seq, j.n_tokens, j.Hkv, D, j.page, j.max_pages, j.n_pages);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    k_attn_prefill<D><<<dim3((unsigned)A.n_slots, (unsigned)j.Hkv), 192, Ly::SMEM_ALLOC, st>>>(mq, mk, mv, A);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 // Splits of the context: about kAttnCtas CTAs over all (sequence, kv-head,
@@ -384,6 +847,13 @@ AttnPlan attn_plan(int B, int Hq, int Hkv, int max_seq_len) {
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_seq_len) {
     const AttnPlan p = attn_plan(B, Hq, Hkv, max_seq_len);
     return p.n_split > 1 ? (size_t)B * Hq * p.n_split * (D + 2) * 4 : 0;
+}
+
+cudaError_t launch_attn_prefill(const AttnPfJob& j, cudaStream_t st) {
+    if (j.n_tokens == 0 || j.n_seq == 0) return cudaSuccess;
+    if (j.D == 256) return launch_prefill_attn<256>(j, st);
+    if (j.D == 128) return launch_prefill_attn<128>(j, st);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_attn_decode(const AttnJob& j, cudaStream_t st) {

@@ -135,6 +135,21 @@ AttnPlan attn_plan(int B, int Hq, int Hkv, int max_seq_len);
 size_t attn_workspace_bytes(int B, int Hq, int Hkv, int D, int max_seq_len);
 cudaError_t launch_attn_decode(const AttnJob& job, cudaStream_t st);
 
+// prefill attention: new tokens cu_seqlens[s] .. cu_seqlens[s+1] of sequence s at
+// positions ctx_lens[s] + i, appended to the pages, then causal attention
+struct AttnPfJob {
+    const void *q, *k_new, *v_new;
+    void *k_pool, *v_pool;
+    const int32_t* block_table;
+    const int32_t* cu_seqlens;
+    const int32_t* ctx_lens;
+    void* o;
+    int n_seq, Hq, Hkv, D, page, max_pages, n_pages;
+    int64_t n_tokens;
+    float scale;
+};
+cudaError_t launch_attn_prefill(const AttnPfJob& job, cudaStream_t st);
+
 // read and clear the device status word of each kernel file (synchronous)
 cudaError_t take_device_status_decode(unsigned* out);
 cudaError_t take_device_status_prefill(unsigned* out);

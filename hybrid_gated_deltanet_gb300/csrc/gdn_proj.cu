@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kPjThreads, 2)
         }
     }
 
-    if (split && warp >= 2 && ok) {
+    if (split && warp >= 2 && __all_sync(0xffffffffu, ok)) {  // TMEM loads are warp-collective
         // this CTA's partial block -> workspace, column-major (a warp stores 32
         // consecutive rows of one column: 128 contiguous bytes); columns past the
         // last token are skipped

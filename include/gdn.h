@@ -378,6 +378,27 @@ gdn_status gdn_attn_decode(const gdn_attn_config* cfg, const void* q, const void
                            int32_t max_pages, int32_t n_pages, int32_t max_seq_len, void* o,
                            void* workspace, size_t ws_bytes, void* stream);
 
+/* Prefill (chunk) attention: sequence s brings n_s = cu_seqlens[s+1] -
+ * cu_seqlens[s] new tokens at positions ctx_lens[s] .. ctx_lens[s] + n_s - 1.
+ * Their K and V are appended to the pages, and new token i attends causally to
+ * the sequence's positions 0 .. ctx_lens[s] + i (forge, 27 August: a chunk of k
+ * tokens is a prefill with the mask aligned at the bottom right, row i sees
+ * 0 .. kv0 + i).
+ *   q, o bf16 [n_tokens][n_q_heads][head_dim]; k_new, v_new bf16
+ *   [n_tokens][n_kv_heads][head_dim]; pools and block_table as in
+ *   gdn_attn_decode (block_table [n_seq][max_pages]); cu_seqlens int32
+ *   [n_seq+1] (device; 0 = cu_seqlens[0] <= ... = n_tokens); ctx_lens int32
+ *   [n_seq] (device).  A sequence whose pages would run past max_pages, or
+ *   with ctx_lens[s] < 0, is skipped; tokens on pages outside [0, n_pages) are
+ *   left out of the softmax.  Same alignment and precision as gdn_attn_decode;
+ *   S = Q K^T and O = P V run on the tensor cores (bf16 operands, fp32
+ *   accumulation), P is rounded to bf16.  No workspace. */
+gdn_status gdn_attn_prefill(const gdn_attn_config* cfg, const void* q, const void* k_new,
+                            const void* v_new, void* k_pool, void* v_pool,
+                            const int32_t* block_table, const int32_t* cu_seqlens,
+                            const int32_t* ctx_lens, int32_t n_seq, int64_t n_tokens,
+                            int32_t max_pages, int32_t n_pages, void* o, void* stream);
+
 /* Workspace bytes of gdn_attn_decode (depends on the sizes only; 0 on invalid
  * arguments, with gdn_last_error set). */
 size_t gdn_attn_workspace_size(const gdn_attn_config* cfg, int32_t B, int32_t max_seq_len);

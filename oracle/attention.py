@@ -33,3 +33,12 @@ def decode_attention(q, K, V, scale: float) -> np.ndarray:
         p = np.exp(s - s.max())
         o[h] = (p @ V[:, kvh, :]) / p.sum()
     return o
+
+
+def prefill_attention(q, K, V, ctx_len: int, scale: float) -> np.ndarray:
+    """Chunk of n new tokens after ctx_len cached ones: q [n, Hq, D]; K, V [ctx_len + n,
+    Hkv, D] (all tokens of the sequence in order).  New token i sits at position
+    ctx_len + i and attends to positions 0 .. ctx_len + i.  Returns o [n, Hq, D]."""
+    q = np.asarray(q, dtype=np.float64)
+    return np.stack([decode_attention(q[i], K[:ctx_len + i + 1], V[:ctx_len + i + 1], scale)
+                     for i in range(q.shape[0])])

@@ -67,3 +67,20 @@ def test_group_mapping_is_contiguous():
     np.testing.assert_allclose(o[2], o[3])
     assert not np.allclose(o[1], o[2])
     np.testing.assert_allclose(o[1], at.decode_attention(qh[None], K[:, :1], V[:, :1], 1.0)[0])
+
+
+def test_prefill_matches_torch_sdpa_with_bottom_right_mask():
+    """The chunk form against torch SDPA with an explicit mask: new token i (after
+    ctx cached tokens) sees keys 0 .. ctx + i."""
+    r = _rng(5)
+    Hq, Hkv, D, ctx, n = 8, 2, 16, 7, 5
+    q = r.standard_normal((n, Hq, D))
+    K, V = r.standard_normal((ctx + n, Hkv, D)), r.standard_normal((ctx + n, Hkv, D))
+    got = at.prefill_attention(q, K, V, ctx, 0.25)
+    G = Hq // Hkv
+    kq = torch.from_numpy(np.repeat(K.transpose(1, 0, 2), G, axis=0))
+    vq = torch.from_numpy(np.repeat(V.transpose(1, 0, 2), G, axis=0))
+    mask = torch.from_numpy(np.arange(ctx + n)[None, :] <= ctx + np.arange(n)[:, None])
+    ref = torch.nn.functional.scaled_dot_product_attention(torch.from_numpy(q.transpose(1, 0, 2)), kq, vq,
+                                                           attn_mask=mask, scale=0.25)
+    np.testing.assert_allclose(got, ref.numpy().transpose(1, 0, 2), rtol=1e-12, atol=1e-12)
