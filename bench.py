@@ -486,6 +486,10 @@ def profile_case(args):
         print(json.dumps(serving_measure(torch, device, args.steps, args.warmup)))
     elif args.case == "ckpt":
         print(json.dumps(ckpt_measure(torch, device, args.steps, args.warmup)))
+    elif args.case == "proj-prefill":
+        print(json.dumps(proj_prefill_case(torch, device, args.steps, args.warmup)))
+    elif args.case == "attn-small":
+        print(json.dumps(attn_small_case(torch, device, args.steps, args.warmup)))
     elif args.case == "attn":
         for rec in attn_measure(torch, device, args.steps, args.warmup):
             print(json.dumps(rec))
@@ -501,6 +505,56 @@ def profile_case(args):
         t, _ = prefill_measure(torch, device, args.steps, args.warmup, seed=0, check=False)
         print(json.dumps({"case": args.case, "ms_per_call": round(1e3 * t, 4)}))
     return 0
+
+
+def proj_prefill_case(torch, device, steps, warmup, T=8192):
+    """The in-projection GEMM of a T-token prefill alone (12352 x 2560 bf16 weights),
+    warmup + steps launches, for ncu captures."""
+    from hybrid_gated_deltanet_gb300 import binding as gb
+    g = torch.Generator(device=device)
+    g.manual_seed(12)
+    bf = torch.bfloat16
+    w = (torch.randn((12352, 2560), generator=g, device=device) / 50).to(bf)
+    h = torch.randn((T, 2560), generator=g, device=device).to(bf)
+    u = torch.empty((T, 12352), dtype=bf, device=device)
+    for _ in range(warmup + steps):
+        gb.gdn_proj_gemm(h, w, u)
+    torch.cuda.synchronize()
+    return {"case": "proj-prefill", "tokens": T, "launches": warmup + steps}
+
+
+def attn_small_case(torch, device, steps, warmup):
+    """Decode attention (16 sequences x 8192 cached tokens) and prefill attention (one
+    2048-token prompt), 16 query / 4 kv-heads of 256, pages of 16; warmup + steps of
+    each, for ncu captures (about 1.2 GB on the device)."""
+    from hybrid_gated_deltanet_gb300 import binding as gb
+    g = torch.Generator(device=device)
+    g.manual_seed(13)
+    bf = torch.bfloat16
+    cfg = gb.AttnConfig(16, 4, 256, 16)
+    B, L = 16, 8192
+    per = (L + 1 + 15) // 16
+    kp = torch.randn((B * per, 4, 16, 256), generator=g, device=device).to(bf)
+    vp = torch.randn((B * per, 4, 16, 256), generator=g, device=device).to(bf)
+    table = torch.randperm(B * per, generator=g, device=device).to(torch.int32).view(B, per)
+    lens = torch.full((B,), L, dtype=torch.int32, device=device)
+    q = torch.randn((B, 16, 256), generator=g, device=device).to(bf)
+    kn = torch.randn((B, 4, 256), generator=g, device=device).to(bf)
+    o = torch.empty((B, 16, 256), dtype=bf, device=device)
+    ws = torch.empty(max(16, gb.gdn_attn_workspace_size(cfg, B, L + 1)), dtype=torch.uint8, device=device)
+    T = 2048
+    tab2 = torch.arange(T // 16, dtype=torch.int32, device=device).view(1, -1)
+    cu = torch.tensor([0, T], dtype=torch.int32, device=device)
+    ctx = torch.zeros(1, dtype=torch.int32, device=device)
+    q2 = torch.randn((T, 16, 256), generator=g, device=device).to(bf)
+    k2 = torch.randn((T, 4, 256), generator=g, device=device).to(bf)
+    o2 = torch.empty((T, 16, 256), dtype=bf, device=device)
+    torch.cuda.synchronize()
+    for _ in range(warmup + steps):
+        gb.gdn_attn_decode(cfg, q, kn, kn, kp, vp, table, lens, L + 1, o, ws)
+        gb.gdn_attn_prefill(cfg, q2, k2, k2, kp, vp, tab2, cu, ctx, o2)
+    torch.cuda.synchronize()
+    return {"case": "attn-small", "launches": 4 * (warmup + steps)}
 
 
 def attn_measure(torch, device, steps, warmup):
@@ -1056,7 +1110,7 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--batch", type=int, default=64, help="slots of the decode-small case")
     ap.add_argument("--case", default="full", choices=["full", "decode-small", "prefill-small", "serving", "verify", "ckpt", "layer",
-                             "proj-decode", "attn"],
+                             "proj-decode", "attn", "proj-prefill", "attn-small"],
                     help="small cases for ncu captures")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-prefill-tokens", type=int, default=8192)

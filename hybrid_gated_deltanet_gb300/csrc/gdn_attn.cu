@@ -140,24 +140,39 @@ __global__ void __launch_bounds__(32 * kAtWarps) k_attn_decode(const __grid_cons
     const int first = t_begin + warp * kTJ;
     const int step = kAtWarps * kTJ;
     const int n_groups = (first < t_end) ? (t_end - first + step - 1) / step : 0;
-    auto group_mask = [&](int t0, bool& pool_rows) -> unsigned {
+    // page of group gi (-1: past the cache or outside the pool).  Lane i of the warp
+    // holds the page of group base + i of a 32-group window: one coalesced lookup per
+    // 32 groups, read out with a shuffle (warp-collective).  Two windows: the groups
+    // being issued run kStages ahead of the groups being scored.
+    auto lookup = [&](int gi) -> int {
+        const int t0 = first + gi * step;
+        if (gi >= n_groups || t0 >= L) return -1;
         const int pg = t0 / A.page;
-        const int page_id = (pg < A.max_pages) ? A.block_table[(size_t)b * A.max_pages + pg] : -1;
-        pool_rows = page_id >= 0 && page_id < A.n_pages;
+        const int pid = (pg < A.max_pages) ? __ldg(A.block_table + (size_t)b * A.max_pages + pg) : -1;
+        return (pid >= 0 && pid < A.n_pages) ? pid : -1;
+    };
+    int win_issue = -1, pid_issue = -1, win_score = -1, pid_score = -1;
+    auto page_of = [&](int gi, int& win, int& held) -> int {
+        const int base = gi & ~31;
+        if (base != win) {
+            win = base;
+            held = lookup(base + lane);
+        }
+        return __shfl_sync(0xffffffffu, held, gi & 31);
+    };
+    auto group_mask = [&](int t0, int page_id) -> unsigned {
         unsigned m = 0;
 #pragma unroll
         for (int j = 0; j < kTJ; ++j) {
             const int t = t0 + j;
-            if ((t < L && pool_rows) || t == L) m |= 1u << j;
+            if ((t < L && page_id >= 0) || t == L) m |= 1u << j;
         }
         return m;
     };
-    auto issue = [&](int gi) {  // lane 0: the pool rows of group gi into stage gi % kStages
+    auto issue = [&](int gi, int page_id) {  // lane 0: the pool rows of group gi into stage gi % kStages
         const int t0 = first + gi * step;
-        const int pg = t0 / A.page;
-        const int page_id = (pg < A.max_pages) ? A.block_table[(size_t)b * A.max_pages + pg] : -1;
         uint64_t* bar = full + gi % kStages;
-        if (page_id >= 0 && page_id < A.n_pages && t0 < L) {
+        if (page_id >= 0) {
             const size_t off = (((size_t)page_id * A.Hkv + kvh) * A.page + t0 % A.page) * D;
             unsigned char* st = ring + (gi % kStages) * Lay::STAGE;
             mbar_arrive_expect_tx(bar, 2 * Lay::ROWS);
@@ -170,7 +185,10 @@ __global__ void __launch_bounds__(32 * kAtWarps) k_attn_decode(const __grid_cons
     if (lane == 0) {
         for (int s = 0; s < kStages; ++s) mbar_init(full + s, 1);
         fence_mbar_init();
-        for (int gi = 0; gi < kStages && gi < n_groups; ++gi) issue(gi);
+    }
+    for (int gi = 0; gi < kStages && gi < n_groups; ++gi) {
+        const int pid = page_of(gi, win_issue, pid_issue);
+        if (lane == 0) issue(gi, pid);
     }
     if (lane < GC) {
         s_m[warp][lane] = -INFINITY;
@@ -196,8 +214,7 @@ __global__ void __launch_bounds__(32 * kAtWarps) k_attn_decode(const __grid_cons
 
     for (int gi = 0; gi < n_groups; ++gi) {
         const int t0 = first + gi * step;
-        bool pool_rows;
-        const unsigned vmask = group_mask(t0, pool_rows);
+        const unsigned vmask = group_mask(t0, page_of(gi, win_score, pid_score));
         const int ls = gi % kStages;
         const unsigned char* st = ring + ls * Lay::STAGE;
         const bool w = mbar_wait(full + ls, (uint32_t)((gi / kStages) & 1));
@@ -266,10 +283,13 @@ __global__ void __launch_bounds__(32 * kAtWarps) k_attn_decode(const __grid_cons
             }
         }
         // the stage is read: refill it with group gi + kStages
-        __syncwarp();
-        if (lane == 0 && gi + kStages < n_groups) {
-            fence_proxy_async_smem();
-            issue(gi + kStages);
+        if (gi + kStages < n_groups) {
+            const int pid = page_of(gi + kStages, win_issue, pid_issue);
+            __syncwarp();
+            if (lane == 0) {
+                fence_proxy_async_smem();
+                issue(gi + kStages, pid);
+            }
         }
     }
     if (!ok && lane == 0) report_device_status(kDevWaitTimeout);
@@ -498,52 +518,57 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t tm = *tslot;
     bool ok = true;
 
-    // rows [k0, k0 + 128) of the sequence: bytes the pool can deliver for them
-    auto seg_page = [&](int pos) -> int {
-        const int pid = A.block_table[(size_t)s * A.max_pages + pos / A.page];
+    // key tile j: lane i (< 128 / R) looks up the page of its run of R rows, all lanes
+    // at once (one load latency per tile, issued a tile ahead); -1: past the
+    // sequence or a page outside the pool
+    const int nseg = 128 / A.R;
+    auto lane_page = [&](int j) -> int {
+        const int pos = j * 128 + lane * A.R;
+        if (lane >= nseg || j >= n_kv || pos >= L) return -1;
+        const int pid = __ldg(A.block_table + (size_t)s * A.max_pages + pos / A.page);
         return (pid >= 0 && pid < A.n_pages) ? pid : -1;
     };
 
     if (warp == 0) {
+        // Q of the tile: tokens cu0 + t0 .., heads kvh G ..; rows past the tile are other
+        // tokens or zeros (never stored)
         if (lane == 0) {
-            // Q of the tile: tokens cu0 + t0 .., heads kvh G ..; rows past the tile are other
-            // tokens or zeros (never stored)
             mbar_arrive_expect_tx(full_q, (uint32_t)(NA * A.TQ * A.G * 128));
             for (int a = 0; a < NA; ++a) tma_load_3d(sm + Ly::Q + a * Ly::ATOM, &tq, a * 64, kvh * A.G, cu0 + t0, full_q);
-            int last_k = -1, last_v = -1;
-            for (int j = 0; j < n_kv && ok; ++j) {
-                const int k0 = j * 128;
-                // K_j once S_{j-1} has read K_{j-1}
-                if (j > 0 && !mbar_wait(s_done, (uint32_t)((j - 1) & 1))) { ok = false; break; }
-                uint32_t bytes = 0;
-                for (int r0 = 0; r0 < 128; r0 += A.R)
-                    if (k0 + r0 < L && seg_page(k0 + r0) >= 0) bytes += NA * A.R * 128;
-                mbar_arrive_expect_tx(full_k, bytes);
-                for (int r0 = 0; r0 < 128; r0 += A.R) {
-                    const int pos = k0 + r0;
-                    const int pid = pos < L ? seg_page(pos) : -1;
-                    if (pid < 0) continue;
-                    for (int a = 0; a < NA; ++a)
-                        tma_load_4d(sm + Ly::K + a * Ly::ATOM + r0 * 128, &tk, a * 64, pos % A.page, kvh, pid, full_k);
-                }
-                last_k = j;
-                // V_j once PV_{j-1} has read V_{j-1}
-                if (j > 0 && !mbar_wait(pv_done, (uint32_t)((j - 1) & 1))) { ok = false; break; }
-                mbar_arrive_expect_tx(full_v, bytes);
-                for (int r0 = 0; r0 < 128; r0 += A.R) {
-                    const int pos = k0 + r0;
-                    const int pid = pos < L ? seg_page(pos) : -1;
-                    if (pid < 0) continue;
-                    for (int a = 0; a < NA; ++a)
-                        tma_load_4d(sm + Ly::V + a * Ly::ATOM + r0 * 128, &tv, a * 64, pos % A.page, kvh, pid, full_v);
-                }
-                last_v = j;
-            }
-            // copies still in flight land before the CTA leaves
-            if (last_k >= 0) mbar_wait(full_k, (uint32_t)(last_k & 1));
-            if (last_v >= 0) mbar_wait(full_v, (uint32_t)(last_v & 1));
-            if (!mbar_wait(full_q, 0)) ok = false;
         }
+        int last_k = -1, last_v = -1;
+        int pid_next = lane_page(0);
+        for (int j = 0; j < n_kv && ok; ++j) {
+            const int k0 = j * 128;
+            const int pid = pid_next;
+            pid_next = lane_page(j + 1);
+            const unsigned have = __ballot_sync(0xffffffffu, pid >= 0);
+            const uint32_t bytes = (uint32_t)__popc(have) * NA * A.R * 128;
+            // K_j once S_{j-1} has read K_{j-1}
+            if (j > 0 && !mbar_wait(s_done, (uint32_t)((j - 1) & 1))) ok = false;
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (lane == 0) mbar_arrive_expect_tx(full_k, bytes);
+            __syncwarp();
+            if (pid >= 0)  // lane i issues its run's boxes
+                for (int a = 0; a < NA; ++a)
+                    tma_load_4d(sm + Ly::K + a * Ly::ATOM + lane * A.R * 128, &tk, a * 64, (k0 + lane * A.R) % A.page,
+                                kvh, pid, full_k);
+            last_k = j;
+            // V_j once PV_{j-1} has read V_{j-1}
+            if (j > 0 && !mbar_wait(pv_done, (uint32_t)((j - 1) & 1))) ok = false;
+            if (!__all_sync(0xffffffffu, ok)) break;
+            if (lane == 0) mbar_arrive_expect_tx(full_v, bytes);
+            __syncwarp();
+            if (pid >= 0)
+                for (int a = 0; a < NA; ++a)
+                    tma_load_4d(sm + Ly::V + a * Ly::ATOM + lane * A.R * 128, &tv, a * 64, (k0 + lane * A.R) % A.page,
+                                kvh, pid, full_v);
+            last_v = j;
+        }
+        // copies still in flight land before the CTA leaves
+        if (last_k >= 0) mbar_wait(full_k, (uint32_t)(last_k & 1));
+        if (last_v >= 0) mbar_wait(full_v, (uint32_t)(last_v & 1));
+        if (!mbar_wait(full_q, 0)) ok = false;
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc_s = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
@@ -584,6 +609,7 @@ __global__ void __launch_bounds__(192, 1)
         const int qpos = P + t0 + tl;             // the row's position in the sequence
         float m_ref = -INFINITY, l = 0.f;
         unsigned char* prow = sm + Ly::P + r * 128;
+        int pid_next = lane_page(0);
         for (int j = 0; j < n_kv; ++j) {
             const int k0 = j * 128;
             bool w = mbar_wait(s_done, (uint32_t)(j & 1));
@@ -595,15 +621,22 @@ __global__ void __launch_bounds__(192, 1)
             tc::fence_before();
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(s_read)) : "memory");
-            // keys on pages outside the pool, per run of R page rows (bit c of dead[c / 32])
+            // keys on pages outside the pool, per run of R page rows (bit c of dead[c / 32]);
+            // runs with no key (past the sequence) are bit seg of gone
+            const int pid = pid_next;
+            pid_next = lane_page(j + 1);
+            const unsigned hole = __ballot_sync(0xffffffffu, lane < nseg && k0 + lane * A.R < L && pid < 0);
+            const unsigned gone = __ballot_sync(0xffffffffu, lane < nseg && pid < 0);
             uint32_t dead[4] = {0u, 0u, 0u, 0u};
-            for (int r0 = 0; r0 < 128; r0 += A.R) {
-                const int pos = k0 + r0;
-                if (pos < L && seg_page(pos) < 0)
+            if (hole) {
+                for (int sg = 0; sg < nseg; ++sg) {
+                    if (!((hole >> sg) & 1u)) continue;
+                    const int r0 = sg * A.R;
                     for (int c = r0; c < r0 + A.R; c += 32) {
                         const int n = min(32, r0 + A.R - c);
                         dead[c >> 5] |= (n == 32 ? 0xffffffffu : ((1u << n) - 1u)) << (c & 31);
                     }
+                }
             }
             // mask: causal (which also keeps the key inside the sequence) and on a page of the pool
             float mt = -INFINITY;
@@ -664,10 +697,8 @@ __global__ void __launch_bounds__(192, 1)
             w = mbar_wait(full_v, (uint32_t)(j & 1));
             if (!named_bar_and(1, 128, w)) { ok = false; break; }
             {
-                const int key = r;  // thread r clears V row r when needed
-                const int pos = k0 + key;
-                const bool dead = pos >= L || seg_page(pos - (pos % A.R)) < 0;
-                if (dead) {
+                const int key = r;  // thread r clears V row r when its run has no key
+                if ((gone >> (key / A.R)) & 1u) {
 #pragma unroll
                     for (int a = 0; a < NA; ++a) {
                         uint4* vr = reinterpret_cast<uint4*>(sm + Ly::V + a * Ly::ATOM + key * 128);
