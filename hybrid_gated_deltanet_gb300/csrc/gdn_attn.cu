@@ -432,6 +432,30 @@ __device__ __forceinline__ bool named_bar_and(int id, int count, bool pred) {
     return r != 0;
 }
 
+// 2^x on the SFU (the PTX ex2 instruction; 2^-inf = 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// 128 consecutive TMEM columns of this warp's lanes: 8 loads, one wait
+__device__ __forceinline__ void ld_row128(uint32_t ta, float v[128]) {
+    uint32_t r[128];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(r[16 * q + 0]), "=r"(r[16 * q + 1]), "=r"(r[16 * q + 2]), "=r"(r[16 * q + 3]),
+              "=r"(r[16 * q + 4]), "=r"(r[16 * q + 5]), "=r"(r[16 * q + 6]), "=r"(r[16 * q + 7]),
+              "=r"(r[16 * q + 8]), "=r"(r[16 * q + 9]), "=r"(r[16 * q + 10]), "=r"(r[16 * q + 11]),
+              "=r"(r[16 * q + 12]), "=r"(r[16 * q + 13]), "=r"(r[16 * q + 14]), "=r"(r[16 * q + 15])
+            : "r"(ta + 16 * q));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+
 __device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr, uint32_t lbo) {
     // 128-byte swizzled MN-major operand: atoms of 64 (MN) x 8 (K) elements; lbo =
     // byte stride between atoms along MN, 1024 = stride between 8-row groups along K
@@ -616,8 +640,7 @@ __global__ void __launch_bounds__(192, 1)
             if (!named_bar_and(1, 128, w)) { ok = false; break; }
             tc::fence_after();
             float sv[128];
-#pragma unroll
-            for (int c0 = 0; c0 < 128; c0 += 16) tc::ld16(tc::taddr(tm, 32 * q4, c0), sv + c0);
+            ld_row128(tc::taddr(tm, 32 * q4, 0), sv);
             tc::fence_before();
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(s_read)) : "memory");
@@ -638,22 +661,24 @@ __global__ void __launch_bounds__(192, 1)
                     }
                 }
             }
-            // mask: causal (which also keeps the key inside the sequence) and on a page of the pool
+            // mask: causal (which also keeps the key inside the sequence) and on a page of the
+            // pool; a tile below the diagonal of every row of the warp, with no hole, needs none
             float mt = -INFINITY;
+            const bool full_tile = __all_sync(0xffffffffu, row_ok && k0 + 127 <= qpos) && !hole;
+            if (full_tile) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const int pos = k0 + c;
-                const bool v = row_ok && pos <= qpos && !((dead[c >> 5] >> (c & 31)) & 1u);
-                sv[c] = v ? sv[c] : -INFINITY;
-                mt = fmaxf(mt, sv[c]);
+                for (int c = 0; c < 128; ++c) mt = fmaxf(mt, sv[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int pos = k0 + c;
+                    const bool v = row_ok && pos <= qpos && !((dead[c >> 5] >> (c & 31)) & 1u);
+                    sv[c] = v ? sv[c] : -INFINITY;
+                    mt = fmaxf(mt, sv[c]);
+                }
             }
-            // P_j may replace P_{j-1} (and O be rescaled) once PV_{j-1} is done
-            w = (j == 0) || mbar_wait(pv_done, (uint32_t)((j - 1) & 1));
-            if (!named_bar_and(1, 128, w)) { ok = false; break; }
-            tc::fence_after();
             // move a row's reference maximum when its maximum grew by more than 2^8 in the
-            // exponent: rescale its O and l.  TMEM loads and stores are warp-collective, so
-            // the warp rescales together when any of its rows needs it (the others by 1).
+            // exponent (its O and l are then rescaled by f)
             float f = 1.f;
             if (mt > -INFINITY && (m_ref == -INFINITY || (mt - m_ref) * A.scale_log2 > 8.f)) {
                 if (j > 0 && m_ref > -INFINITY) {
@@ -662,6 +687,25 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 m_ref = mt;
             }
+            // p = 2^((s - m_ref) scale log2 e) in bf16, packed in registers while PV_{j-1}
+            // still runs; the sum takes the rounded values, like the product
+            uint32_t pk[64];
+            const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref * A.scale_log2;  // a masked s gives 2^-inf = 0
+#pragma unroll
+            for (int e = 0; e < 64; ++e) {
+                const float p0 = ex2_approx(fmaf(sv[2 * e], A.scale_log2, neg_m));
+                const float p1 = ex2_approx(fmaf(sv[2 * e + 1], A.scale_log2, neg_m));
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                const float2 back = __bfloat1622float2(h2);
+                l += back.x + back.y;
+                pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
+            }
+            // P_j may replace P_{j-1}, and O be rescaled, once PV_{j-1} is done
+            w = (j == 0) || mbar_wait(pv_done, (uint32_t)((j - 1) & 1));
+            if (!named_bar_and(1, 128, w)) { ok = false; break; }
+            tc::fence_after();
+            // TMEM loads and stores are warp-collective: the warp rescales together when any
+            // of its rows needs it (the others by 1)
             if (__any_sync(0xffffffffu, f != 1.f)) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < D; c0 += 16) {
@@ -673,24 +717,12 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             }
-            // p = 2^((s - m_ref) scale log2 e) in bf16 -> P row (128-byte swizzle, K-major)
+            // P row (128-byte swizzle, K-major)
 #pragma unroll
             for (int c8 = 0; c8 < 16; ++c8) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float a0 = sv[c8 * 8 + 2 * e], a1 = sv[c8 * 8 + 2 * e + 1];
-                    const float p0 = a0 == -INFINITY ? 0.f : exp2f((a0 - m_ref) * A.scale_log2);
-                    const float p1 = a1 == -INFINITY ? 0.f : exp2f((a1 - m_ref) * A.scale_log2);
-                    const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                    // the sum takes the rounded values, like the product
-                    const float2 back = __bfloat1622float2(h2);
-                    l += back.x + back.y;
-                    pk[e] = *reinterpret_cast<const uint32_t*>(&h2);
-                }
                 const int atom = c8 >> 3, ch = c8 & 7;
                 *reinterpret_cast<uint4*>(prow + atom * Ly::ATOM + ((ch ^ (r & 7)) << 4)) =
-                    make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    make_uint4(pk[4 * c8], pk[4 * c8 + 1], pk[4 * c8 + 2], pk[4 * c8 + 3]);
             }
             // V rows with no key behind them (past the sequence or on a missing page) -> 0,
             // so that 0 x garbage never reaches O
