@@ -501,7 +501,7 @@ __device__ __forceinline__ int pf_slot_seq(const AttnPfArgs& A, int64_t slot) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     k_attn_prefill(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ AttnPfArgs A) {
     using Ly = PfLay<D>;
@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(192, 1)
             mbar_arrive_expect_tx(full_q, (uint32_t)(NA * A.TQ * A.G * 128));
             for (int a = 0; a < NA; ++a) tma_load_3d(sm + Ly::Q + a * Ly::ATOM, &tq, a * 64, kvh * A.G, cu0 + t0, full_q);
         }
-        int last_k = -1, last_v = -1;
+        int last_k = -1;
         int pid_next = lane_page(0);
         for (int j = 0; j < n_kv && ok; ++j) {
             const int k0 = j * 128;
@@ -578,7 +578,21 @@ __global__ void __launch_bounds__(192, 1)
                     tma_load_4d(sm + Ly::K + a * Ly::ATOM + lane * A.R * 128, &tk, a * 64, (k0 + lane * A.R) % A.page,
                                 kvh, pid, full_k);
             last_k = j;
-            // V_j once PV_{j-1} has read V_{j-1}
+        }
+        // copies still in flight land before the CTA leaves
+        if (last_k >= 0) mbar_wait(full_k, (uint32_t)(last_k & 1));
+        if (!mbar_wait(full_q, 0)) ok = false;
+    } else if (warp == 6) {
+        // ---- V producer: V_j once PV_{j-1} has read V_{j-1} (its own warp, so that the
+        // K loads of the next tile never queue behind a V load that waits for PV) ------
+        int last_v = -1;
+        int pid_next = lane_page(0);
+        for (int j = 0; j < n_kv && ok; ++j) {
+            const int k0 = j * 128;
+            const int pid = pid_next;
+            pid_next = lane_page(j + 1);
+            const unsigned have = __ballot_sync(0xffffffffu, pid >= 0);
+            const uint32_t bytes = (uint32_t)__popc(have) * NA * A.R * 128;
             if (j > 0 && !mbar_wait(pv_done, (uint32_t)((j - 1) & 1))) ok = false;
             if (!__all_sync(0xffffffffu, ok)) break;
             if (lane == 0) mbar_arrive_expect_tx(full_v, bytes);
@@ -589,10 +603,7 @@ __global__ void __launch_bounds__(192, 1)
                                 kvh, pid, full_v);
             last_v = j;
         }
-        // copies still in flight land before the CTA leaves
-        if (last_k >= 0) mbar_wait(full_k, (uint32_t)(last_k & 1));
         if (last_v >= 0) mbar_wait(full_v, (uint32_t)(last_v & 1));
-        if (!mbar_wait(full_q, 0)) ok = false;
     } else if (warp == 1) {
         if (lane == 0) {
             constexpr uint32_t idesc_s = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
@@ -624,7 +635,7 @@ __global__ void __launch_bounds__(192, 1)
                 tc::commit(pv_done);
             }
         }
-    } else {
+    } else if (warp < 6) {
         // ---- softmax and epilogue: thread = row r of the tile (TMEM lane r) ----------------
         const int q4 = warp & 3;
         const int r = 32 * q4 + lane;
@@ -874,7 +885,7 @@ cudaError_t launch_prefill_attn(const AttnPfJob& j, cudaStream_t st) {
         j.ctx_lens, j.n_seq, j.n_tokens, j.Hkv, D, j.page, j.max_pages, j.n_pages);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    k_attn_prefill<D><<<dim3((unsigned)A.n_slots, (unsigned)j.Hkv), 192, Ly::SMEM_ALLOC, st>>>(mq, mk, mv, A);
+    k_attn_prefill<D><<<dim3((unsigned)A.n_slots, (unsigned)j.Hkv), 224, Ly::SMEM_ALLOC, st>>>(mq, mk, mv, A);
     return cudaGetLastError();
 }
 
