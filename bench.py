@@ -607,8 +607,8 @@ def attn_measure(torch, device, steps, warmup):
                     "us": round(1e6 * t, 2), "gbs": round(nbytes / t / 1e9, 1)})
         del kp, vp
     # prefill: (cached, new) tokens per sequence; flops 4 d Hq per (query, visible key) pair
-    for Hq, Hkv, D, page, seqs in ((16, 4, 256, 16, [(0, 8192)]), (16, 4, 256, 16, [(8192, 512)] * 4),
-                                   (24, 2, 256, 528, [(0, 32768)])):
+    for Hq, Hkv, D, page, seqs in ((16, 4, 256, 16, [(0, 8192)]), (16, 4, 256, 128, [(0, 8192)]),
+                                   (16, 4, 256, 16, [(8192, 512)] * 4), (24, 2, 256, 528, [(0, 32768)])):
         cfg = gb.AttnConfig(Hq, Hkv, D, page)
         per = [(c + n + page - 1) // page for c, n in seqs]
         n_pages, max_pages = sum(per), max(per)
