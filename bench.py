@@ -689,7 +689,8 @@ def layer_measure(torch, device, steps, warmup, n_layers=4, batch=64):
     * gdn_layer_varlen_prefill of one T = 8192 sequence (tokens/s);
     * gdn_layer_decode of `batch` slots, round-robin over `n_layers` layers
       with their own weights and pools (more than L2 in total), and its
-      in-projection alone (weight GB/s)."""
+      in-projection alone (weight GB/s).
+    Every case is replayed from a CUDA graph (device time)."""
     from hybrid_gated_deltanet_gb300 import binding as gb
     from hybrid_gated_deltanet_gb300 import synth
     geom = synth.QWEN35_4B
@@ -709,16 +710,26 @@ def layer_measure(torch, device, steps, warmup, n_layers=4, batch=64):
     stream = _side_stream(torch)
 
     def timed(fn, n):
+        """Device time per fn() call: fn is captured once in a CUDA graph and replayed,
+        so host launch costs (tensor-map encoding, ctypes) do not count."""
         torch.cuda.synchronize()  # inputs made on the default stream are complete
         with torch.cuda.stream(stream):
             for _ in range(warmup):
                 fn()
         torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            fn()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(warmup):
+                graph.replay()
+        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(n):
-                fn()
+                graph.replay()
             e1.record(stream)
         e1.synchronize()
         return e0.elapsed_time(e1) / 1e3 / n

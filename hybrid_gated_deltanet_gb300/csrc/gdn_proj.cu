@@ -42,10 +42,13 @@ constexpr int kPjThreads = 192;
 constexpr int kBM = 128;  // weight rows per tile: MMA M, TMEM lanes
 constexpr int kBK = 64;   // K per stage: one 128-byte swizzle atom of bf16
 
-template <int BT, int STAGES>
+// a stage holds KBOX consecutive 64-wide K blocks (each a 128-byte swizzle atom) of W and act
+template <int BT, int STAGES, int KBOX>
 struct PjLay {
-    static constexpr int A_BYTES = kBM * kBK * 2;
-    static constexpr int B_BYTES = BT * kBK * 2;
+    static constexpr int A_ATOM = kBM * kBK * 2;
+    static constexpr int B_ATOM = BT * kBK * 2;
+    static constexpr int A_BYTES = KBOX * A_ATOM;
+    static constexpr int B_BYTES = KBOX * B_ATOM;
     static constexpr int STAGE = A_BYTES + B_BYTES;
     static constexpr int BAR_OFF = STAGES * STAGE;  // full[S], empty[S], acc_full[2], acc_empty[2], TMEM address
     static constexpr int SMEM = BAR_OFF + (2 * STAGES + 4) * 8 + 16;
@@ -94,11 +97,11 @@ struct ProjArgs {
     ProjSeg seg[4];
 };
 
-template <int BT, int STAGES>
+template <int BT, int STAGES, int KBOX>
 __global__ void __launch_bounds__(kPjThreads, 2)
     k_proj(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ta,
            const __grid_constant__ ProjArgs P) {
-    using L = PjLay<BT, STAGES>;
+    using L = PjLay<BT, STAGES, KBOX>;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
@@ -142,16 +145,19 @@ __global__ void __launch_bounds__(kPjThreads, 2)
             for (int64_t tile = tile0; tile < P.n_tiles && ok; tile += tstep) {
                 const int wn = (int)(tile % P.tiles_n);
                 const int tt = (int)(tile / P.tiles_n);
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; kb += KBOX, ++it) {
                     const int s = (int)(it % STAGES);
                     if (!mbar_wait(empty + s, ((it / STAGES) & 1u) ^ 1u)) {
                         ok = false;
                         break;
                     }
                     unsigned char* st = sm + s * L::STAGE;
-                    mbar_arrive_expect_tx(full + s, L::STAGE);
-                    tma_load_2d(st, &tw, kb * kBK, wn * kBM, full + s);
-                    tma_load_2d(st + L::A_BYTES, &ta, kb * kBK, tt * BT, full + s);
+                    const int nbox = (kb1 - kb < KBOX) ? kb1 - kb : KBOX;
+                    mbar_arrive_expect_tx(full + s, (uint32_t)(nbox * (L::A_ATOM + L::B_ATOM)));
+                    for (int a = 0; a < nbox; ++a)
+                        tma_load_2d(st + a * L::A_ATOM, &tw, (kb + a) * kBK, wn * kBM, full + s);
+                    for (int a = 0; a < nbox; ++a)
+                        tma_load_2d(st + L::A_BYTES + a * L::B_ATOM, &ta, (kb + a) * kBK, tt * BT, full + s);
                 }
             }
         }
@@ -168,7 +174,7 @@ __global__ void __launch_bounds__(kPjThreads, 2)
                 }
                 tc::fence_after();
                 const uint32_t d = tm + buf * BT;
-                for (int kb = kb0; kb < kb1; ++kb, ++it) {
+                for (int kb = kb0; kb < kb1; kb += KBOX, ++it) {
                     const int s = (int)(it % STAGES);
                     if (!mbar_wait(full + s, (it / STAGES) & 1u)) {
                         ok = false;
@@ -177,10 +183,13 @@ __global__ void __launch_bounds__(kPjThreads, 2)
                     tc::fence_after();
                     const uint32_t a0 = tc::smem_addr(sm + s * L::STAGE);
                     const uint32_t b0 = a0 + L::A_BYTES;
+                    const int nbox = (kb1 - kb < KBOX) ? kb1 - kb : KBOX;
+                    for (int a = 0; a < nbox; ++a)
 #pragma unroll
-                    for (int k16 = 0; k16 < kBK / 16; ++k16)
-                        mma_bf16(d, tc::sdesc(a0 + k16 * 32), tc::sdesc(b0 + k16 * 32), idesc,
-                                 (kb > kb0 || k16 > 0) ? 1u : 0u);
+                        for (int k16 = 0; k16 < kBK / 16; ++k16)
+                            mma_bf16(d, tc::sdesc(a0 + a * L::A_ATOM + k16 * 32),
+                                     tc::sdesc(b0 + a * L::B_ATOM + k16 * 32), idesc,
+                                     (kb > kb0 || a > 0 || k16 > 0) ? 1u : 0u);
                     tc::commit(empty + s);  // the stage is free once these MMAs have read it
                 }
                 if (!ok) break;
@@ -349,20 +358,20 @@ __global__ void __launch_bounds__(32 * kRedWarps) k_proj_reduce(const __grid_con
     }
 }
 
-template <int BT, int STAGES>
+template <int BT, int STAGES, int KBOX>
 cudaError_t launch_tiles(const CUtensorMap& mw, const CUtensorMap& ma, const ProjArgs& P, int ctas_per_sm,
                          cudaStream_t st) {
-    using L = PjLay<BT, STAGES>;
+    using L = PjLay<BT, STAGES, KBOX>;
     static bool attr = false;
     if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_proj<BT, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(k_proj<BT, STAGES, KBOX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              L::SMEM_ALLOC);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     const int64_t slots = (int64_t)sm_count() * ctas_per_sm;
     const int64_t grid = P.ks > 1 ? P.n_tiles * P.ks : (P.n_tiles < slots ? P.n_tiles : slots);
-    k_proj<BT, STAGES><<<(unsigned)grid, kPjThreads, L::SMEM_ALLOC, st>>>(mw, ma, P);
+    k_proj<BT, STAGES, KBOX><<<(unsigned)grid, kPjThreads, L::SMEM_ALLOC, st>>>(mw, ma, P);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || P.ks == 1) return e;
     const int64_t items = P.n_tiles * BT;
@@ -375,7 +384,7 @@ cudaError_t launch_tiles(const CUtensorMap& mw, const CUtensorMap& ma, const Pro
 cudaError_t take_device_status_proj(unsigned* out) { return take_device_status_tu(out); }
 
 // The launch shape depends on the shapes only (so the workspace a call needs is
-// known without a device): up to 64 tokens use 64-token tiles (2 CTAs per SM),
+// known without a device): up to 64 tokens use 64-token tiles (1 CTA per SM),
 // more use 256-token tiles (1 CTA per SM, persistent).  When the tiles would
 // leave most of the GPU idle, K is split over ks CTAs per tile so that about
 // kSplitCtas CTAs run, each with at least 2 K blocks; their fp32 partials take
@@ -427,8 +436,11 @@ cudaError_t launch_proj(const ProjJob& job, cudaStream_t st) {
     CUtensorMap mw, ma;
     if (!make_map(&mw, job.w, job.n_out, job.k, kBM) || !make_map(&ma, job.act, job.n_tok, job.k, plan.bt))
         return cudaErrorInvalidValue;
-    if (plan.bt == 64) return launch_tiles<64, 4>(mw, ma, P, 2, st);
-    return launch_tiles<256, 4>(mw, ma, P, 1, st);
+    // few tokens: 3 stages of 2 K blocks (48 KB), one CTA per SM; under graph replay this
+    // measured 16.1 us for the 64-token in-projection against 18.4 us for 4 stages of one
+    // K block at two CTAs per SM (4 K blocks per stage: 17.0 us)
+    if (plan.bt == 64) return launch_tiles<64, 3, 2>(mw, ma, P, 1, st);
+    return launch_tiles<256, 4, 1>(mw, ma, P, 1, st);
 }
 
 }  // namespace gdn
