@@ -509,6 +509,11 @@ __global__ void __launch_bounds__(pd::THREADS, 1) k_decode_persist(const __grid_
     const bool direct = g.flags & kFlagGatesDirect;
     const int n_items = J.B * Hv;
 
+    // programmatic dependent launch: this grid may be resident before the previous
+    // kernel of the stream ends; every read below waits for it (and its memory)
+    griddep_wait();
+    griddep_launch_dependents();
+
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * St::BYTES);
     uint64_t* fullS = full + STAGES;     // the state tile of the stage
@@ -839,6 +844,8 @@ __global__ void k_conv_roll(const Geom g, const ConvJob J) {
 // aligned, as the decode step requires): raw inputs move bit for bit.
 template <typename TA>
 __global__ void k_conv_roll_v(const Geom g, const ConvJob J) {
+    griddep_wait();  // the decode kernel before it has read every old conv row
+    griddep_launch_dependents();
     constexpr int VEC = 16 / (int)sizeof(TA);
     const int C = g.C_ch, Km1 = g.K - 1, CV = C / VEC;
     const size_t total = (size_t)J.n_seq * CV;
@@ -901,15 +908,29 @@ cudaError_t launch_decode_persist(const Geom& g, const LayerParams& p, const Row
     }
     const int items = job.B * g.Hv;
     RowsArgs A{g, p, job, 1};
-    k_decode_persist<TA><<<std::min(items, sms), pd::THREADS, smem, st>>>(A);
-    cudaError_t e = cudaGetLastError();
+    // both kernels go out with programmatic stream serialization: each may be
+    // scheduled while its predecessor finishes and waits for it (griddep_wait)
+    // before its first access to memory, which hides the launch gaps
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::min(items, sms));
+    cfg.blockDim = dim3(pd::THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_decode_persist<TA>, A);
     if (e != cudaSuccess) return e;
     // roll the conv state (raw inputs) after every read of it above
     ConvJob cj{job.x, job.conv_pool, job.slot_idx, nullptr, job.B, 1, job.n_slots};
     const size_t total = (size_t)job.B * g.C_ch / (16 / sizeof(TA));
     const int blocks = (int)std::min<size_t>((total + 255) / 256, (size_t)sms * 8);
-    k_conv_roll_v<TA><<<blocks, 256, 0, st>>>(g, cj);
-    return cudaGetLastError();
+    cfg.gridDim = dim3((unsigned)blocks);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    return cudaLaunchKernelEx(&cfg, k_conv_roll_v<TA>, g, cj);
 }
 
 cudaError_t launch_rows(const Geom& g, const LayerParams& p, const RowsJob& job, cudaStream_t st) {
