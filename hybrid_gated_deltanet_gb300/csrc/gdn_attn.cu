@@ -107,6 +107,8 @@ __global__ void __launch_bounds__(32 * kAtWarps) k_attn_decode(const __grid_cons
     constexpr int DPL = D / 32;
     using RowT = typename Row<DPL>::T;
     using Lay = AtLay<D>;
+    griddep_wait();  // launched with programmatic serialization
+    griddep_launch_dependents();
     const int G = A.Hq / A.Hkv, hg = G / GC;
     const int split = blockIdx.x, kvh = blockIdx.y / hg, h0 = kvh * G + (blockIdx.y % hg) * GC, b = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -331,6 +333,8 @@ __global__ void __launch_bounds__(32 * kAtWarps) k_attn_decode(const __grid_cons
 // the splits of one (sequence, query head): o = sum_i e^(m_i - M) o_i / sum_i e^(m_i - M) l_i
 template <int D>
 __global__ void __launch_bounds__(D) k_attn_combine(const __grid_constant__ AttnArgs A) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
     const int L = A.seq_lens[b];
     if (L < 0 || L >= A.max_pages * A.page) return;
@@ -358,11 +362,9 @@ cudaError_t launch_decode(const AttnArgs& A, cudaStream_t st) {
     }
     const int hg = (A.Hq / A.Hkv) / GC;
     const dim3 grid((unsigned)A.n_split, (unsigned)(A.Hkv * hg), (unsigned)A.B);
-    k_attn_decode<D, GC><<<grid, 32 * kAtWarps, AtLay<D>::SMEM, st>>>(A);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_attn_decode<D, GC>, grid, dim3(32 * kAtWarps), AtLay<D>::SMEM, st, A);
     if (e != cudaSuccess || A.n_split == 1) return e;
-    k_attn_combine<D><<<dim3((unsigned)A.Hq, (unsigned)A.B), D, 0, st>>>(A);
-    return cudaGetLastError();
+    return launch_pdl(k_attn_combine<D>, dim3((unsigned)A.Hq, (unsigned)A.B), dim3(D), 0, st, A);
 }
 
 // query heads per kv-head G: 1 or 2 in one CTA, multiples of 4 in CTAs of 4
@@ -506,6 +508,8 @@ __global__ void __launch_bounds__(224, 1)
                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ AttnPfArgs A) {
     using Ly = PfLay<D>;
     constexpr int NA = D / 64;  // 64-wide atoms along d
+    griddep_wait();  // launched with programmatic serialization: the appended rows are visible
+    griddep_launch_dependents();
     const int64_t slot = A.n_slots - 1 - blockIdx.x;  // late (long) tiles first
     const int kvh = blockIdx.y;
     const int s = pf_slot_seq(A, slot);
@@ -789,6 +793,8 @@ __global__ void k_attn_append(const __nv_bfloat16* __restrict__ k_new, const __n
                               __nv_bfloat16* k_pool, __nv_bfloat16* v_pool, const int32_t* block_table,
                               const int32_t* cu_seqlens, const int32_t* ctx_lens, int n_seq, int64_t n_tokens,
                               int Hkv, int D, int page, int max_pages, int n_pages) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int64_t tok = blockIdx.x;
     if (tok >= n_tokens) return;
     int lo = 0, hi = n_seq - 1;  // the sequence holding token tok
@@ -879,14 +885,14 @@ cudaError_t launch_prefill_attn(const AttnPfJob& j, cudaStream_t st) {
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    k_attn_append<<<(unsigned)j.n_tokens, 128, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(j.k_new), static_cast<const __nv_bfloat16*>(j.v_new),
-        static_cast<__nv_bfloat16*>(j.k_pool), static_cast<__nv_bfloat16*>(j.v_pool), j.block_table, j.cu_seqlens,
-        j.ctx_lens, j.n_seq, j.n_tokens, j.Hkv, D, j.page, j.max_pages, j.n_pages);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_attn_append, dim3((unsigned)j.n_tokens), dim3(128), 0, st,
+                               static_cast<const __nv_bfloat16*>(j.k_new), static_cast<const __nv_bfloat16*>(j.v_new),
+                               static_cast<__nv_bfloat16*>(j.k_pool), static_cast<__nv_bfloat16*>(j.v_pool),
+                               j.block_table, j.cu_seqlens, j.ctx_lens, j.n_seq, j.n_tokens, j.Hkv, D, j.page,
+                               j.max_pages, j.n_pages);
     if (e != cudaSuccess) return e;
-    k_attn_prefill<D><<<dim3((unsigned)A.n_slots, (unsigned)j.Hkv), 224, Ly::SMEM_ALLOC, st>>>(mq, mk, mv, A);
-    return cudaGetLastError();
+    return launch_pdl(k_attn_prefill<D>, dim3((unsigned)A.n_slots, (unsigned)j.Hkv), dim3(224), Ly::SMEM_ALLOC, st,
+                      mq, mk, mv, A);
 }
 
 }  // namespace

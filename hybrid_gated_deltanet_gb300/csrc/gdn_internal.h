@@ -8,6 +8,25 @@
 
 namespace gdn {
 
+// Launch with programmatic stream serialization: the kernel may become resident
+// while the previous kernel of the stream finishes; it calls griddep_wait()
+// before touching memory, so the stream order of memory effects is unchanged.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Geometry + options after validation (all derived fields filled in).
 struct Geom {
     int Hk, Hv, D, K, G, C_ch, chunk;

@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(kPjThreads, 2)
     k_proj(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap ta,
            const __grid_constant__ ProjArgs P) {
     using L = PjLay<BT, STAGES, KBOX>;
+    griddep_wait();  // launched with programmatic serialization: the previous kernel's results are visible
+    griddep_launch_dependents();
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + L::BAR_OFF);
@@ -314,6 +316,8 @@ int sm_count() {
 // bf16 results, which sit side by side in the output row of that token.
 constexpr int kRedWarps = 8;
 __global__ void __launch_bounds__(32 * kRedWarps) k_proj_reduce(const __grid_constant__ ProjArgs P) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int BT = P.bt;
     const int lane = threadIdx.x & 31;
     const int64_t item = (int64_t)blockIdx.x * kRedWarps + (threadIdx.x >> 5);  // tile * BT + column
@@ -371,12 +375,12 @@ cudaError_t launch_tiles(const CUtensorMap& mw, const CUtensorMap& ma, const Pro
     }
     const int64_t slots = (int64_t)sm_count() * ctas_per_sm;
     const int64_t grid = P.ks > 1 ? P.n_tiles * P.ks : (P.n_tiles < slots ? P.n_tiles : slots);
-    k_proj<BT, STAGES, KBOX><<<(unsigned)grid, kPjThreads, L::SMEM_ALLOC, st>>>(mw, ma, P);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_proj<BT, STAGES, KBOX>, dim3((unsigned)grid), dim3(kPjThreads), L::SMEM_ALLOC, st,
+                               mw, ma, P);
     if (e != cudaSuccess || P.ks == 1) return e;
     const int64_t items = P.n_tiles * BT;
-    k_proj_reduce<<<(unsigned)((items + kRedWarps - 1) / kRedWarps), 32 * kRedWarps, 0, st>>>(P);
-    return cudaGetLastError();
+    return launch_pdl(k_proj_reduce, dim3((unsigned)((items + kRedWarps - 1) / kRedWarps)), dim3(32 * kRedWarps), 0,
+                      st, P);
 }
 
 }  // namespace

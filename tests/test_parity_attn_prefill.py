@@ -108,3 +108,36 @@ def test_attn_prefill_long_prompt():
 
 def test_attn_prefill_page_outside_pool_is_left_out():
     run_case(16, 4, 256, 16, [(64, 40), (16, 100)], 5, holes=[(0, 1), (1, 0)])
+
+
+def test_prefill_then_decode_continue_the_cache():
+    """A 300-token prompt through gdn_attn_prefill, then 3 decode steps through
+    gdn_attn_decode on the same pages: every step against the oracle over all tokens
+    so far (the cache written by one call is what the next one reads)."""
+    Hq, Hkv, D, page = 16, 4, 256, 16
+    r = synth.rng_for(62, 0)
+    cfg = gb.AttnConfig(Hq, Hkv, D, page)
+    T, steps = 300, 3
+    n_pages = math.ceil((T + steps) / page) + 1
+    table = torch.from_numpy(r.permutation(n_pages)[:n_pages - 1].astype(np.int32)).view(1, -1).cuda()
+    kp = torch.zeros((n_pages, Hkv, page, D), dtype=torch.bfloat16, device="cuda")
+    vp = torch.zeros_like(kp)
+    q, k, v = (_bf16(r, (T + steps, H, D)) for H in (Hq, Hkv, Hkv))
+    q64, k64, v64 = q.f64[:], k.f64[:], v.f64[:]
+    qd, kd, vd = dev(q), dev(k), dev(v)
+    o = torch.empty((T, Hq, D), dtype=torch.bfloat16, device="cuda")
+    gb.gdn_attn_prefill(cfg, qd[:T], kd[:T], vd[:T], kp, vp, table, torch.tensor([0, T], dtype=torch.int32).cuda(),
+                        torch.zeros(1, dtype=torch.int32).cuda(), o)
+    torch.cuda.synchronize()
+    ref = at.prefill_attention(q64[:T], k64[:T], v64[:T], 0, 1 / math.sqrt(D))
+    assert rel_fro(host(o), ref) <= 8e-3
+    for s in range(steps):
+        t = T + s
+        od = torch.empty((1, Hq, D), dtype=torch.bfloat16, device="cuda")
+        nws = gb.gdn_attn_workspace_size(cfg, 1, t + 1)
+        ws = torch.empty(nws, dtype=torch.uint8, device="cuda") if nws else None
+        gb.gdn_attn_decode(cfg, qd[t:t + 1], kd[t:t + 1], vd[t:t + 1], kp, vp, table,
+                           torch.tensor([t], dtype=torch.int32).cuda(), t + 1, od, ws)
+        torch.cuda.synchronize()
+        refd = at.decode_attention(q64[t], k64[:t + 1], v64[:t + 1], 1 / math.sqrt(D))
+        assert rel_fro(host(od)[0], refd) <= 4e-3, s

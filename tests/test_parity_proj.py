@@ -209,3 +209,34 @@ def test_layer_varlen_prefill():
     e_out = rel_fro(np.concatenate(outs), np.concatenate(outr))
     e_s = rel_fro(np.concatenate(ss), np.concatenate(sr))
     assert e_out <= tol["y"] and e_s <= tol["S"], (e_out, e_s)
+
+
+def test_layer_prefill_then_decode_steps():
+    """gdn_layer_varlen_prefill of a 150-token prompt into a pool slot, then 2
+    gdn_layer_decode steps from that slot: out of every token and the final state
+    against the oracle layer run over the whole sequence."""
+    T, steps = 150, 2
+    geom, r, p, pw, h = _layer_case(11, T + steps)
+    cfg = config(geom, synth.BF16)
+    n_slots = 3
+    sp = torch.zeros((n_slots, geom.n_v_heads, geom.d_v, geom.d_k), device="cuda")
+    cp = torch.zeros((n_slots, geom.d_conv - 1, geom.conv_channels), dtype=torch.bfloat16, device="cuda")
+    slot = 1
+    proj = gb.Proj(dev(pw["w_in"]), dev(pw["w_out"]))
+    prm = params_dev(p)
+    hd = dev(h)
+    outs = torch.empty((T + steps, synth.HIDDEN), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(gb.gdn_layer_workspace_size(cfg, gb.OP_LAYER_VARLEN_PREFILL, T, 1, synth.HIDDEN),
+                     dtype=torch.uint8, device="cuda")
+    gb.gdn_layer_varlen_prefill(cfg, prm, proj, hd[:T], torch.tensor([0, T], dtype=torch.int32).cuda(),
+                                torch.tensor([slot], dtype=torch.int32).cuda(), None, cp, sp, outs[:T], ws)
+    wsd = torch.empty(gb.gdn_layer_workspace_size(cfg, gb.OP_LAYER_DECODE, 1, 1, synth.HIDDEN), dtype=torch.uint8,
+                      device="cuda")
+    si = torch.tensor([slot], dtype=torch.int32).cuda()
+    for s in range(steps):
+        gb.gdn_layer_decode(cfg, prm, proj, hd[T + s:T + s + 1], cp, sp, si, outs[T + s:T + s + 1], wsd)
+    torch.cuda.synchronize()
+    ref = pj.layer_sequence(geom, h.f64[:], pw["w_in"].f64[:], pw["w_out"].f64[:], **_okw(p))
+    tol = tol_for(synth.BF16)
+    assert rel_fro(host(outs), ref["out"]) <= tol["y"]
+    assert rel_fro(host(sp)[slot], ref["S"]) <= tol["S"]
