@@ -499,6 +499,7 @@ def profile_case(args):
         for rec in layer_measure(torch, device, args.steps, args.warmup):
             print(json.dumps(rec))
     elif args.case == "verify":
+        print(json.dumps(wide_prefill_measure(torch, device, args.steps, args.warmup)))
         for nb in (4, 64):
             print(json.dumps(verify_measure(torch, device, args.steps, args.warmup, batch=nb)))
     else:
@@ -860,6 +861,58 @@ def ckpt_measure(torch, device, steps, warmup, every=1024):
             "snapshot_bytes": n_ck * (32 * 128 * 128 * 4 + 3 * 8192 * 2),
             "ms_plain": round(1e3 * t0, 4), "ms_with_snapshots": round(1e3 * t1, 4),
             "overhead_pct": round(100 * (t1 / t0 - 1), 2)}
+
+
+def wide_prefill_measure(torch, device, steps, warmup, n_seq=4, T=32768):
+    """The wide-GVA prefill (16/48 heads, d = 128, 10240 conv channels): n_seq
+    sequences of T tokens packed into one gdn_varlen_prefill call, each into its
+    own pool slot (the prefill that precedes the verify steps of that workload).
+    Timing only: N(0, 1) inputs drawn on the device from a fixed seed."""
+    from hybrid_gated_deltanet_gb300 import binding as gb
+    from hybrid_gated_deltanet_gb300 import synth
+    geom = synth.WIDE_GVA
+    hv, dd, cch = geom.n_v_heads, geom.d_k, geom.conv_channels
+    cfg = gb.Config(geom.n_k_heads, hv, dd, dd, geom.d_conv, chunk=64, act_dtype=gb.BF16)
+    r_ = synth.rng_for(3, 8)
+    p = synth.make_params(geom, r_, synth.BF16)
+    prm = gb.Params(conv_w=_dev(p["conv_w"], torch, device), A_log=_dev(p["A_log"], torch, device),
+                    norm_w=_dev(p["norm_w"], torch, device))
+    g = torch.Generator(device=device)
+    g.manual_seed(8)
+    bf = torch.bfloat16
+    N = n_seq * T
+    x = torch.randn((N, cch), generator=g, device=device).to(bf)
+    z = torch.randn((N, hv * dd), generator=g, device=device).to(bf)
+    a = torch.randn((N, hv), generator=g, device=device).to(bf)
+    b = torch.randn((N, hv), generator=g, device=device).to(bf)
+    y = torch.empty((N, hv * dd), dtype=bf, device=device)
+    S = torch.zeros((n_seq, hv, dd, dd), device=device)
+    Cp = torch.zeros((n_seq, geom.d_conv - 1, cch), dtype=bf, device=device)
+    cu = torch.arange(0, N + 1, T, dtype=torch.int32, device=device)
+    sl = torch.arange(n_seq, dtype=torch.int32, device=device)
+    ws = torch.empty(gb.gdn_workspace_size(cfg, gb.OP_VARLEN_PREFILL, N, n_seq), dtype=torch.uint8, device=device)
+    stream = _side_stream(torch)
+
+    def call():
+        gb.gdn_varlen_prefill(cfg, prm, x, z, a, b, cu, sl, None, Cp, S, y, ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            call()
+    torch.cuda.synchronize()
+    n = max(3, steps // 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n):
+            call()
+        e1.record(stream)
+    e1.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / n
+    flop_tok = 16 * FLOP_KHEAD + hv * FLOP_VHEAD
+    return {"case": "wide-prefill", "n_seq": n_seq, "tokens_each": T, "ms": round(1e3 * t, 3),
+            "tokens_per_s_per_layer": round(N / t, 1), "tflops": round(flop_tok * N / t / 1e12, 2),
+            "workspace_gb": round(ws.numel() / 1e9, 2)}
 
 
 def verify_measure(torch, device, steps, warmup, batch=4, r=4):
