@@ -267,3 +267,23 @@ def test_attention_validation(lib):
     assert call(cfg(), max_seq=5000) == -1 and "workspace" in _err(lib)
     assert call(cfg(), max_seq=5000, ws=FAKE, ws_bytes=need - 1) == -6 and f"required {need} bytes" in _err(lib)
     assert call(cfg(), max_seq=5000, ws=FAKE + 8, ws_bytes=need) == -4
+
+
+def test_attention_workspace_sizes(lib):
+    """Context splits of gdn_attn_decode: about 1216 CTAs over (sequence, kv-head, group of
+    up to 4 query heads), each split at least 128 tokens, a multiple of 8; the workspace
+    holds B x Hq x splits x (d + 2) fp32 (unnormalised o, maximum, sum) when splitting."""
+    def want(Hq, Hkv, D, B, max_seq):
+        G = Hq // Hkv
+        pairs = B * Hkv * (G // 4 if G >= 4 else 1)
+        ns = min(-(-1216 // pairs), -(-max_seq // 128))
+        ns = max(ns, 1)
+        span = -(-max_seq // ns)
+        span = -(-span // 8) * 8
+        ns = -(-max_seq // span)
+        return B * Hq * ns * (D + 2) * 4 if ns > 1 else 0
+
+    for Hq, Hkv, D, B, L in [(16, 4, 256, 1, 8193), (16, 4, 256, 64, 8193), (24, 2, 256, 4, 32769),
+                             (8, 8, 128, 200, 60), (4, 2, 128, 3, 129), (32, 4, 128, 16, 4000)]:
+        c = gb.AttnConfig(Hq, Hkv, D, 16).c()
+        assert lib.gdn_attn_workspace_size(ctypes.byref(c), B, L) == want(Hq, Hkv, D, B, L), (Hq, Hkv, D, B, L)
