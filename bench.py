@@ -229,7 +229,10 @@ def decode_parity(torch, cfg, host, layers, n_check=8):
     return {"y": _rel(ys, yr), "S": _rel(ss, sr), "slots_checked": n_check}
 
 
-def time_decode(torch, cfg, layers, steps, warmup, use_graph=True):
+def time_decode(torch, cfg, layers, steps, warmup, use_graph=True, per_step=None):
+    """Seconds for `steps` replays of the decode step, timed with CUDA events on the
+    launching stream.  If `per_step` is a list, each replay's own duration (an event
+    after every replay) is appended to it."""
     from hybrid_gated_deltanet_gb300 import binding as gb
     stream = _side_stream(torch)
 
@@ -253,14 +256,16 @@ def time_decode(torch, cfg, layers, steps, warmup, use_graph=True):
         for _ in range(warmup):
             run()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(steps):
+        evs[0].record(stream)
+        for i in range(steps):
             run()
-        ev1.record(stream)
-    ev1.synchronize()
-    return ev0.elapsed_time(ev1) / 1e3  # seconds
+            evs[i + 1].record(stream)
+    evs[-1].synchronize()
+    if per_step is not None:
+        per_step.extend(evs[i].elapsed_time(evs[i + 1]) / 1e3 for i in range(steps))
+    return evs[0].elapsed_time(evs[-1]) / 1e3  # seconds
 
 
 def time_decode_e2e(torch, cfg, layers, steps, warmup):
@@ -1103,7 +1108,9 @@ def gpu_arm(args):
     with ClockSampler(local) as clk:
         barrier(world)
         torch.cuda.synchronize()
-        t_dec = time_decode(torch, cfg, layers, args.steps, args.warmup, use_graph=not args.no_graph)
+        step_s = []
+        t_dec = time_decode(torch, cfg, layers, args.steps, args.warmup, use_graph=not args.no_graph,
+                            per_step=step_s)
         torch.cuda.synchronize()
         barrier(world)
         t_pf, pf_err = prefill_measure(torch, device, pf_steps, max(3, args.warmup // 4), seed=rank,
@@ -1137,6 +1144,8 @@ def gpu_arm(args):
         "metric": METRIC,
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * t_dec / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "step_ms": {"min": round(1e3 * min(step_s), 4), "median": round(1e3 * float(np.median(step_s)), 4),
+                    "max": round(1e3 * max(step_s), 4)},
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": dict(decode_config(world), graph=not args.no_graph),
         "parity": {"decode_rel_fro": parity, "prefill_rel_fro": pf_err,
