@@ -134,6 +134,19 @@ int report_error(int status, const char* message) {
     g_last_error = message;
     return status;
 }
+
+int sm_count() {
+    static std::atomic<int> cache[64];  // static storage: zero, i.e. not yet queried
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::atomic<int>& c = cache[dev & 63];
+    int n = c.load(std::memory_order_relaxed);
+    if (n <= 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+        c.store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
 }  // namespace gdn
 
 extern "C" {

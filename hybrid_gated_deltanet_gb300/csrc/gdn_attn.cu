@@ -353,16 +353,12 @@ __global__ void __launch_bounds__(D) k_attn_combine(const __grid_constant__ Attn
 
 template <int D, int GC>
 cudaError_t launch_decode(const AttnArgs& A, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_attn_decode<D, GC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             AtLay<D>::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = raise_smem_limit(k_attn_decode<D, GC>, AtLay<D>::SMEM, smem_set);
+    if (e != cudaSuccess) return e;
     const int hg = (A.Hq / A.Hkv) / GC;
     const dim3 grid((unsigned)A.n_split, (unsigned)(A.Hkv * hg), (unsigned)A.B);
-    cudaError_t e = launch_pdl(k_attn_decode<D, GC>, grid, dim3(32 * kAtWarps), AtLay<D>::SMEM, st, A);
+    e = launch_pdl(k_attn_decode<D, GC>, grid, dim3(32 * kAtWarps), AtLay<D>::SMEM, st, A);
     if (e != cudaSuccess || A.n_split == 1) return e;
     return launch_pdl(k_attn_combine<D>, dim3((unsigned)A.Hq, (unsigned)A.B), dim3(D), 0, st, A);
 }
@@ -835,12 +831,10 @@ PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn() {
 template <int D>
 cudaError_t launch_prefill_attn(const AttnPfJob& j, cudaStream_t st) {
     using Ly = PfLay<D>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_attn_prefill<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Ly::SMEM_ALLOC);
+    static std::atomic<uint64_t> smem_set{0};
+    {
+        const cudaError_t e = raise_smem_limit(k_attn_prefill<D>, Ly::SMEM_ALLOC, smem_set);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     PFN_cuTensorMapEncodeTiled_v12000 enc = at_encode_fn();
     if (!enc) return cudaErrorInvalidValue;

@@ -774,11 +774,10 @@ cudaError_t launch_rows_t(const Geom& g, const LayerParams& p, const RowsJob& jo
     const int NS = choose_slices(g, job.B);
     RowsArgs A{g, p, job, NS};
     const RowsSmem lay = rows_smem(D, D / NS, job.r, g.K, (int)sizeof(TA));
-    static bool attr_set = false;  // once per instantiation: allow up to 200 KB
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_rows<D, TA>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    static std::atomic<uint64_t> smem_set{0};  // allow up to 200 KB
+    {
+        const cudaError_t e = raise_smem_limit(k_rows<D, TA>, 200 * 1024, smem_set);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(g.G * NS, g.Hk, job.B);
@@ -895,17 +894,12 @@ __global__ void k_commit(const Geom g, const CommitJob J, int elt_bytes) {
 template <typename TA>
 cudaError_t launch_decode_persist(const Geom& g, const LayerParams& p, const RowsJob& job, cudaStream_t st) {
     constexpr int smem = pd::smem_bytes<TA>();
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_decode_persist<TA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    int sms = 152;
+    static std::atomic<uint64_t> smem_set{0};
     {
-        int dev = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const cudaError_t e = raise_smem_limit(k_decode_persist<TA>, smem, smem_set);
+        if (e != cudaSuccess) return e;
     }
+    const int sms = sm_count();
     const int items = job.B * g.Hv;
     RowsArgs A{g, p, job, 1};
     // both kernels go out with programmatic stream serialization: each may be
@@ -940,9 +934,7 @@ cudaError_t launch_rows(const Geom& g, const LayerParams& p, const RowsJob& job,
     // geometry gain 18% / 26%; B <= 16 is faster with one CTA per item)
     if (g.D == 128 && job.r == 1 && !job.snap_idx && job.mode == 0 && std::getenv("GDN_DECODE_CLUSTERED") == nullptr &&
         std::getenv("GDN_DECODE_SLICES") == nullptr) {
-        int sms = 152, dev = 0;
-        if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if ((long)job.B * g.Hv >= 4L * sms)
+        if ((long)job.B * g.Hv >= 4L * sm_count())
             return g.act_bf16 ? launch_decode_persist<__nv_bfloat16>(g, p, job, st)
                               : launch_decode_persist<float>(g, p, job, st);
     }

@@ -6,7 +6,28 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace gdn {
+
+// A kernel's dynamic shared-memory limit belongs to its instance on one device,
+// so it is raised once per device: bit d of `done` records device d (devices
+// 0..63).  Two threads racing through the first call both raise it, which is
+// harmless.
+template <typename... KArgs>
+cudaError_t raise_smem_limit(void (*kernel)(KArgs...), int bytes, std::atomic<uint64_t>& done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = 1ull << (dev & 63);
+    if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
+
+// SMs of the current device, queried once per device (1 if the query fails).
+int sm_count();
 
 // Launch with programmatic stream serialization: the kernel may become resident
 // while the previous kernel of the stream finishes; it calls griddep_wait()

@@ -1739,24 +1739,15 @@ int chain_slices(const PrefillArgs& A) {
         const int v = std::atoi(e);
         if (v == 2 || v == 4) return v;
     }
-    static int n_sm = 0;
-    if (n_sm == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            n_sm = 1;
-    }
-    return (int64_t)A.J.n_seq * A.g.Hv * 4 > (int64_t)n_sm ? 2 : 4;
+    return (int64_t)A.J.n_seq * A.g.Hv * 4 > (int64_t)sm_count() ? 2 : 4;
 }
 
 template <int NSL>
 cudaError_t launch_chain(const PrefillArgs& A, cudaStream_t st) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_chunk_tc<NSL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             ChainLay<NSL>::SMEM_ALLOC);
+    static std::atomic<uint64_t> smem_set{0};
+    {
+        const cudaError_t e = raise_smem_limit(k_chunk_tc<NSL>, ChainLay<NSL>::SMEM_ALLOC, smem_set);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(NSL, A.g.Hv, A.J.n_seq);
@@ -1774,14 +1765,12 @@ cudaError_t launch_chain(const PrefillArgs& A, cudaStream_t st) {
 }
 
 cudaError_t launch_chunk_tc(const PrefillArgs& A, int64_t n_slots, cudaStream_t st) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_chunk_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             tcp::PR_SMEM_ALLOC);
+    static std::atomic<uint64_t> attr1{0}, attr2{0};
+    {
+        cudaError_t e = raise_smem_limit(k_chunk_prep, tcp::PR_SMEM_ALLOC, attr1);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(k_chunk_prep2, cudaFuncAttributeMaxDynamicSharedMemorySize, tcp::P2_SMEM_ALLOC);
+        e = raise_smem_limit(k_chunk_prep2, tcp::P2_SMEM_ALLOC, attr2);
         if (e != cudaSuccess) return e;
-        attr_set = true;
     }
     if (n_slots > 0) {
         const int64_t ny = n_slots < 32768 ? n_slots : 32768;
@@ -1830,12 +1819,10 @@ cudaError_t launch_prefill_t(const Geom& g, const LayerParams& p, const PrefillJ
         A.ncs = tl.ncs;
     }
     if (A.tiles) {
-        static bool attr_set = false;
-        if (!attr_set) {
-            cudaError_t e = cudaFuncSetAttribute(k_prologue_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kPtSmemAlloc);
+        static std::atomic<uint64_t> smem_set{0};
+        {
+            const cudaError_t e = raise_smem_limit(k_prologue_tc, kPtSmemAlloc, smem_set);
             if (e != cudaSuccess) return e;
-            attr_set = true;
         }
         const int64_t ny = A.ncs < 32768 ? A.ncs : 32768;
         const dim3 grid((unsigned)(g.Hk + g.Hv), (unsigned)ny, (unsigned)((A.ncs + ny - 1) / ny));

@@ -299,16 +299,7 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int k, int box_row
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int sm_count() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
-                                                      cudaSuccess)
-            n = 1;
-    }
-    return n;
-}
+
 
 // fp32 partial blocks of a split tile -> bf16 outputs.  One warp per (tile,
 // column = token): lane l adds rows 4l .. 4l+3 of the ks partial blocks (16-byte
@@ -366,12 +357,10 @@ template <int BT, int STAGES, int KBOX>
 cudaError_t launch_tiles(const CUtensorMap& mw, const CUtensorMap& ma, const ProjArgs& P, int ctas_per_sm,
                          cudaStream_t st) {
     using L = PjLay<BT, STAGES, KBOX>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(k_proj<BT, STAGES, KBOX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             L::SMEM_ALLOC);
+    static std::atomic<uint64_t> smem_set{0};
+    {
+        const cudaError_t e = raise_smem_limit(k_proj<BT, STAGES, KBOX>, L::SMEM_ALLOC, smem_set);
         if (e != cudaSuccess) return e;
-        attr = true;
     }
     const int64_t slots = (int64_t)sm_count() * ctas_per_sm;
     const int64_t grid = P.ks > 1 ? P.n_tiles * P.ks : (P.n_tiles < slots ? P.n_tiles : slots);
