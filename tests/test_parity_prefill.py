@@ -58,6 +58,28 @@ def test_prefill_qwen35_4b_all_heads(T):
     np.testing.assert_array_equal(c, ref["conv"])
 
 
+def test_prefill_long_memory_gates():
+    """Gates that keep a long memory.  The workloads' A_log ~ U(0, ln 16) gives a mean
+    alpha of about 0.2 to 0.5, so the state forgets within a few tokens and rounding in
+    the state products cannot build up.  Here A_log runs from -6 to 0 over the v-heads
+    (mean alpha from about 0.998 down to 0.5, i.e. memories of up to ~500 tokens), over
+    2000 tokens, on the tcgen05 path."""
+    T = 2000
+    geom, act, r, p, tok = make_case("prefill4b", 60, T)
+    p = dict(p, A_log=synth.store(np.linspace(-6.0, 0.0, geom.n_v_heads), synth.F32))
+    cfg = config(geom, act)
+    y, s, c = run_prefill(cfg, p, tok)
+    ref = oracle.run_sequence(geom, tok["x"].f64, tok["z"].f64, tok["a"].f64, tok["b"].f64, **oracle_kwargs(p))
+    errs = {"y": rel_fro(y, ref["y"]), "S": rel_fro(s, ref["S"])}
+    tol = tol_for(act)
+    assert errs["y"] <= tol["y"] and errs["S"] <= tol["S"], fmt(errs)
+    # the longest memories on their own, where any build-up would show first
+    long = list(range(4))
+    errs_long = {"S": rel_fro(s[long], ref["S"][long])}
+    assert errs_long["S"] <= tol["S"], fmt(errs_long)
+    np.testing.assert_array_equal(c, ref["conv"])
+
+
 def test_prefill_qwen35_4b_full_size_sampled_heads():
     """T = 8192 (the benchmarked prefill), final state and outputs of 6 v-heads."""
     T = 8192
