@@ -67,6 +67,8 @@ gdn_status make_geom(const gdn_config* cfg, bool need_chunk, gdn::Geom* g) {
     if (cfg->n_v_heads % cfg->n_k_heads != 0)
         return fail(GDN_ERR_SHAPE, "cfg.n_v_heads: found %d, required a multiple of n_k_heads = %d",
                     cfg->n_v_heads, cfg->n_k_heads);
+    if (cfg->n_v_heads > 4096)
+        return fail(GDN_ERR_UNSUPPORTED, "cfg.n_v_heads: found %d, required <= 4096", cfg->n_v_heads);
     const int G = cfg->n_v_heads / cfg->n_k_heads;
     if (G > 8) return fail(GDN_ERR_UNSUPPORTED, "cfg.n_v_heads/n_k_heads: found %d, required <= 8", G);
     if (cfg->d_k != 32 && cfg->d_k != 64 && cfg->d_k != 128)

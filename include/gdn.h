@@ -94,7 +94,9 @@ enum {
 };
 
 /* Layer geometry and options.  Requirements (GDN_ERR_SHAPE otherwise):
- * n_k_heads >= 1, n_v_heads % n_k_heads == 0, G = n_v_heads/n_k_heads <= 8,
+ * n_k_heads >= 1, n_v_heads % n_k_heads == 0, G = n_v_heads/n_k_heads <= 8
+ * (G > 8: GDN_ERR_UNSUPPORTED), n_v_heads <= 4096 (GDN_ERR_UNSUPPORTED otherwise:
+ * it keeps every channel count and grid dimension in range),
  * d_k = d_v in {32, 64, 128} (d_k != d_v: GDN_ERR_UNSUPPORTED),
  * 2 <= d_conv <= 4, chunk in {16, 32, 64} (prefill only). */
 typedef struct gdn_config {

@@ -71,6 +71,7 @@ def _err(lib):
     (dict(act_dtype=7), -3, "cfg.act_dtype: found 7"),
     (dict(n_v_heads=30), -2, "cfg.n_v_heads: found 30, required a multiple of n_k_heads = 16"),
     (dict(n_k_heads=2, n_v_heads=32), -7, "required <= 8"),
+    (dict(n_k_heads=4096, n_v_heads=8192), -7, "cfg.n_v_heads: found 8192, required <= 4096"),
     (dict(d_k=48, d_v=48), -2, "cfg.d_k: found 48"),
     (dict(d_v=64), -7, "required d_v == d_k = 128"),
     (dict(d_conv=5), -2, "cfg.d_conv: found 5"),
