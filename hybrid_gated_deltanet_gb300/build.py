@@ -18,8 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgdn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["gdn_api.cu", "gdn_decode.cu", "gdn_prefill.cu", "gdn_noalloc.cu", "gdn_proj.cu", "gdn_attn.cu"]
-HEADERS = ["gdn_common.cuh", "gdn_internal.h", "gdn_tc.cuh", "gdn_tma.cuh"]
+SOURCES = ["gdn_api.cu", "gdn_decode.cu", "gdn_prefill.cu", "gdn_chunk16.cu", "gdn_noalloc.cu", "gdn_proj.cu",
+           "gdn_attn.cu"]
+HEADERS = ["gdn_common.cuh", "gdn_internal.h", "gdn_prefill_common.cuh", "gdn_tc.cuh", "gdn_tma.cuh"]
 
 
 def _nvcc() -> str:

@@ -160,11 +160,12 @@ const char* gdn_version(void) { return "libgdn 0.1 (sm_103a)"; }
 gdn_status gdn_device_status(uint32_t* status) {
     if (!status) return fail(GDN_ERR_NULL, "status: found NULL, required a host pointer");
     unsigned a = 0, b = 0;
-    unsigned c = 0;
+    unsigned c = 0, d = 0;
     cudaError_t e = gdn::take_device_status_decode(&a);
     if (e == cudaSuccess) e = gdn::take_device_status_prefill(&b);
     if (e == cudaSuccess) e = gdn::take_device_status_proj(&c);
-    *status = a | b | c;
+    if (e == cudaSuccess) e = gdn::take_device_status_chunk16(&d);
+    *status = a | b | c | d;
     return cuda_status(e, "gdn_device_status");
 }
 

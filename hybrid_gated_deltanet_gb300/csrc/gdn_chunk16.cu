@@ -1,0 +1,902 @@
+// gdn_chunk16.cu -- chunkwise (WY / UT-transform) prefill for d_k = d_v = 128,
+// chunk 64 and bf16 activations, on tcgen05 tensor cores with fp16 operands
+// and fp32 accumulation.
+//
+// The layer is the gated delta rule of "Hybrid transformers under load: where
+// Gated DeltaNet loses to full attention" (braintools.ru, section 3): per
+// v-head S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T and
+// o_t = S_t q_t.  Over a chunk of C = 64 tokens with gamma = cumsum(log alpha)
+// and the state S entering the chunk, the token loop is exactly
+//     A   = strict-lower(diag(beta) (K K^T o Gamma)),  T = (I + A)^-1,
+//     P   = lower-incl(Q K^T o Gamma),                 T' = T diag(beta),
+//     W   = T' diag(e^gamma) K,   U~ = T' V,   U = U~ - W S^T,
+//     O   = diag(e^gamma) Q S^T + P U = Q' S^T + X,  Q' = diag(e^gamma) Q - P W,
+//                                                     X  = P U~,
+//     S  <- e^gamma_C S + U^T diag(e^(gamma_C - gamma)) K,
+// with Gamma_ti = e^(gamma_t - gamma_i).  Only the two products with S depend
+// on the previous chunk; everything else is per chunk.
+//
+// Cost model (measured on GB300 with a probe): a tcgen05.mma instruction
+// costs about 108 SM cycles to issue whatever its kind (f16, bf16, tf32), M
+// (64 or 128) and N (up to 128); N = 256 costs about 155.  kind::f16 covers
+// K = 16 per instruction where kind::tf32 covers 8, so fp16 operands halve the
+// instruction count at TF32's precision (11-bit significands, rounded to
+// nearest; fp32 accumulation).  A rounding emulation of this chain gives a
+// relative state error of 3-5e-4 at T = 8192 for mean alpha 0.5 to 0.998,
+// the same as TF32.  fp16 holds magnitudes below 65504: far above the
+// activations and states of the layer (|S| stays near the scale of v).
+//
+// Two launches (the conv-state tail of gdn_prefill.cu follows):
+//  1. k_prep16, one CTA per (chunk slot, k-head), all chunks at once:
+//     conv + SiLU + L2 norm of the k-head's q and k -> [K^; Q^] (fp16) and the
+//     Gram [K^ K^T; Q^ K^T] (one M = 128 product); K^ is stored for the chain.
+//     Per v-head of the k-head's group: gates, gamma, the masks A and P,
+//     T = (I + A)^-1 (fp32), T' = T diag(beta), [T'; PT'] = [I; P] T' and
+//     [W; PW] = [T'; PT'] diag(e^gamma) K^ (M = 128 products), the A operand
+//     [-W; Q'] of the chain with Q' = e^gamma Q^ - PW, and V = silu(conv(x)) of
+//     the v-head's channels -> stored fp16 with e^gamma and e^(gamma_C - gamma).
+//  2. k_chain16, one CTA per (sequence, v-head), chunks in order; the fp32
+//     state S^T lives in tensor memory for the whole sequence.  Per chunk:
+//       PRE  [U~; X] = [T'; PT'] V                                   (4 MMAs)
+//       RA   [U; O]  = [U~; X] + [-W; Q'] S^T                        (8 MMAs)
+//       RB   S^T    <- e^gamma_C S^T + K^T (diag(e^(gamma_C - gamma)) U)  (4 MMAs)
+//     RA accumulates onto the U~ / X columns that PRE wrote, so U and O come
+//     out of tensor memory directly.  Warp roles: a producer lane (bulk
+//     copies, every operand double-buffered and requested as soon as its
+//     buffer is free), an MMA issuer lane, 8 warps for U' (lanes 0..63) and
+//     the S operand after each state update (the chain's critical path), and
+//     4 warps for the gated RMSNorm of O -> y.  They hand over through
+//     mbarriers, one pair per hand-over (indexed by chunk parity), so that no
+//     waiter can see a phase two chunks ahead.
+// Every wait is bounded: a wait that gives up sets an abort flag, after which
+// the CTA runs to its end without waiting (its results are then undefined)
+// and reports kDevWaitTimeout in the device status word.  Reductions have a
+// fixed order, so results are bitwise reproducible ("Forge: how I wrote my
+// own inference engine", 25-26 August: chunked DeltaNet prefill with
+// deterministic reduction).
+#include <algorithm>
+
+#include "gdn_common.cuh"
+#include "gdn_internal.h"
+#include "gdn_prefill_common.cuh"
+#include "gdn_tc.cuh"
+#include "gdn_tma.cuh"
+
+namespace gdn {
+namespace {
+
+namespace c16 {
+constexpr int C = 64, D = 128;
+constexpr uint32_t kK = 16384;            // K^ fp16 [64 t][128 d_k]: 2 atoms of [64][64]
+constexpr uint32_t kAop = 32768;          // [-W; Q'] fp16 [128][128] K-major SW128: 2 atoms of 128 rows
+constexpr uint32_t kTP = 16384;           // [T'; PT'] fp16 [128][64] K-major SW128: 1 atom
+constexpr uint32_t kV = 16384;            // V = silu(conv(x)) fp16, MN-major [64 tokens][128]: 2 atoms
+constexpr uint32_t kGates = 512;          // e^gamma [64] | e^(gamma_C - gamma) [64], fp32
+constexpr uint32_t kRecTP = kAop, kRecV = kAop + kTP, kRecG = kAop + kTP + kV;
+constexpr uint32_t kRec = kAop + kTP + kV + kGates;  // per (chunk slot, v-head)
+
+struct Args {
+    Geom g;
+    LayerParams p;
+    PrefillJob J;
+    unsigned char* kk;   // [ncs][Hk] kK
+    unsigned char* rec;  // [ncs][Hv] kRec
+    int64_t ncs;         // chunk slots
+};
+
+size_t align1024(size_t x) { return (x + 1023) & ~(size_t)1023; }
+
+struct Ws {
+    size_t kk, rec, total;
+    int64_t ncs;
+};
+
+Ws ws_layout(const Geom& g, int64_t N, int n_seq) {
+    Ws L;
+    L.ncs = N / C + n_seq + 1;
+    L.kk = 0;
+    L.rec = align1024((size_t)L.ncs * g.Hk * kK);
+    L.total = align1024(L.rec + (size_t)L.ncs * g.Hv * kRec);
+    return L;
+}
+
+// 8 floats -> 8 fp16 in one 16-byte chunk
+__device__ __forceinline__ uint4 pack8(const float* v) {
+    return make_uint4(tc::pack_h2(v[0], v[1]), tc::pack_h2(v[2], v[3]), tc::pack_h2(v[4], v[5]),
+                      tc::pack_h2(v[6], v[7]));
+}
+
+__device__ __forceinline__ void unpack_h8(const uint4& u, float* f) {
+    float2 a = tc::unpack_h2(u.x), b = tc::unpack_h2(u.y), c = tc::unpack_h2(u.z), d = tc::unpack_h2(u.w);
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+// ---------------------------------------------------------------------------
+// 1. per-chunk preparation
+// ---------------------------------------------------------------------------
+constexpr int P_THREADS = 256;
+constexpr uint32_t P_KQ = 0;                          // [K^; Q^] fp16 [128][128] (atoms of 128 rows)
+constexpr uint32_t P_IP = 32768;                      // [I; P] (A of the T' product), then e^gamma K^, then V
+constexpr uint32_t P_TB = 49152;                      // T' fp16 MN-major [64 (j)][64 (i)]
+constexpr uint32_t P_OUT = 57344;                     // [T'; PT'] tile, then the gates (512 B)
+constexpr uint32_t P_AM = P_OUT + kTP + kGates;       // A fp32 [64][kUtLd]; then [-W; Q'] (with Tm)
+constexpr uint32_t P_TM = P_AM + 64 * kUtLd * 4;      // T fp32 [64][kUtLd]
+constexpr uint32_t P_SMALL = P_TM + 64 * kUtLd * 4;   // gamma [64], beta [64], mbarrier, TMEM slot
+constexpr uint32_t P_SMEM = P_SMALL + 2 * C * 4 + 16;
+constexpr uint32_t P_SMEM_ALLOC = P_SMEM + 1024;
+constexpr uint32_t P_TMEM_COLS = 256;                 // Gram (64) | [T'; PT'] (64) | [W; PW] (128)
+static_assert(P_TM + 64 * kUtLd * 4 - P_AM >= kAop, "[-W; Q'] staging");
+
+__global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__ Args A) {
+    using L = Act<__nv_bfloat16>;
+    const Geom& g = A.g;
+    const PrefillJob& J = A.J;
+    const int Hk = g.Hk, Hv = g.Hv, G = g.G, K = g.K, Cch = g.C_ch;
+    const int h = blockIdx.x;
+    const int64_t cs = (int64_t)blockIdx.z * gridDim.y + blockIdx.y;
+    if (cs >= A.ncs) return;
+    int sq, n;
+    int64_t start, end, t0;
+    if (!slot_chunk(J, cs, sq, start, end, t0, n)) return;  // a slot between two sequences' chunks
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int q4 = warp & 3, hf = warp >> 2;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
+    unsigned char *sKQ = sm + P_KQ, *sIP = sm + P_IP, *sTB = sm + P_TB, *sOUT = sm + P_OUT;
+    unsigned char* sAop = sm + P_AM;
+    float* eg = reinterpret_cast<float*>(sOUT + kTP);  // the record's gate block
+    float* erev = eg + C;
+    float* Am = reinterpret_cast<float*>(sm + P_AM);
+    float* Tm = reinterpret_cast<float*>(sm + P_TM);
+    float* gam = reinterpret_cast<float*>(sm + P_SMALL);
+    float* bet = gam + C;
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(bet + C);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
+    const bool raw = g.flags & kFlagRawQKV;
+    int slot_ok;
+    const void* cin = seq_conv_in(J, g, sq, slot_ok);
+
+    if (warp == 0) tc::alloc(tslot, P_TMEM_COLS);
+    if (tid == 0) {
+        mbar_init(mbar, 1);
+        fence_mbar_init();
+    }
+
+    // ---- conv + SiLU + L2 norm of q and k: thread = 8 channels (lanes 0..15 q,
+    // 16..31 k) x 8 tokens (one warp's) -> rows 0..63 K^, 64..127 Q^ -------------
+    {
+        const bool is_q = lane < 16;
+        const int d0 = (lane & 15) * 8;
+        const int ch = (is_q ? h : Hk + h) * D + d0;
+        float w[4][8], bias[8];
+        conv_weights8(A.p, K, raw, ch, w, bias);
+        const int tt0 = warp * 8;
+        uint4 rows[11];
+        load_window<8>(J, Cch, K, ch, t0 + tt0, start, end, cin, rows);
+        unsigned char* atom = sKQ + (d0 >> 6) * 16384;
+        const int cc = (d0 & 63) >> 3;
+        const float qs = is_q ? g.q_scale : 1.f;
+        const bool l2 = !(g.flags & kFlagNoL2);
+        conv_tokens<8>(rows, w, bias, K, raw, [&](int i, float u[8]) {
+            const int t = tt0 + i;
+            float ss = 0.f;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) ss = fmaf(u[c], u[c], ss);
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+            const float scale = l2 ? qs * rsqrtf(ss + g.l2_eps) : qs;
+            float v[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) v[c] = t < n ? u[c] * scale : 0.f;  // zero past the sequence end
+            *reinterpret_cast<uint4*>(atom + tc::h_off(is_q ? C + t : t, cc)) = pack8(v);
+        });
+    }
+    fence_proxy_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = *tslot;
+    if (tid == 0) {
+        // K^ for the chain: the first 64 rows of each atom
+        unsigned char* dst = A.kk + ((size_t)cs * Hk + h) * kK;
+        bulk_s2g(dst, sKQ, 8192);
+        bulk_s2g(dst + 8192, sKQ + 16384, 8192);
+        bulk_commit();
+        // [K^ K^T; Q^ K^T] = [K^; Q^] K^T: B = the K^ rows of the same tile (N = 64)
+        const uint32_t a0 = tc::smem_addr(sKQ);
+        for (int s = 0; s < D / 16; ++s) {
+            const uint64_t d = tc::sdesc_lbo(a0 + (uint32_t)((s >> 2) * 16384 + (s & 3) * 32), 16);
+            tc::mma_f16(tm, d, d, tc::idesc_f16(128, 64, false, false), s > 0 ? 1u : 0u);
+        }
+        tc::commit(mbar);
+    }
+    uint32_t phase = 0;
+    bool ok = true;
+    auto wait_mma = [&]() {
+        bool w = true;
+        if (warp == 0) {
+            w = mbar_wait(mbar, phase);
+            if (!w) w = mbar_wait(mbar, phase);
+        }
+        phase ^= 1u;
+        ok = __syncthreads_and(ok && w);
+        tc::fence_after();
+    };
+    wait_mma();
+
+    const bool direct = g.flags & kFlagGatesDirect;
+    for (int jj = 0; jj < G; ++jj) {
+        const int j = h * G + jj;
+        if (tid == 0) bulk_wait_read_all();  // the previous record's stores have read shared memory
+        __syncthreads();
+        if (tid < C) {  // gates of token t = tid (zero past the sequence end)
+            float gl = 0.f, be = 0.f;
+            if (tid < n) {
+                const size_t tok = (size_t)(t0 + tid);
+                gates(L::ld(J.a, tok * Hv + j), L::ld(J.b, tok * Hv + j), direct ? 0.f : A.p.A_log[j],
+                      (!direct && A.p.dt_bias) ? A.p.dt_bias[j] : 0.f, direct, gl, be);
+            }
+            gam[tid] = gl;
+            bet[tid] = be;
+        }
+        // identity rows of [I; P] (the region served as e^gamma K^ and V before)
+        for (int f = tid; f < C * 8; f += P_THREADS) {
+            const int r = f >> 3, cc = f & 7;
+            uint32_t wd[4] = {0u, 0u, 0u, 0u};
+            if ((r >> 3) == cc) wd[(r & 7) >> 1] = (r & 1) ? 0x3C000000u : 0x00003C00u;  // fp16 1.0 at column r
+            *reinterpret_cast<uint4*>(sIP + tc::h_off(r, cc)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        }
+        __syncthreads();
+        if (warp == 0) {  // gamma = cumsum(g), e^gamma, e^(gamma_C - gamma)
+            float run = 0.f;
+            for (int base = 0; base < C; base += 32) {
+                float v = gam[base + lane];
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float o = __shfl_up_sync(0xffffffffu, v, off);
+                    if (lane >= off) v += o;
+                }
+                v += run;
+                gam[base + lane] = v;
+                eg[base + lane] = expf(v);
+                run = __shfl_sync(0xffffffffu, v, 31);
+            }
+            __syncwarp();
+            for (int t = lane; t < C; t += 32) erev[t] = expf(gam[C - 1] - gam[t]);
+        }
+        __syncthreads();
+        // decay masks from the Gram: A (strictly lower, beta_t) from the K^K^T rows
+        // (lanes 0..63), P (lower incl.) from the Q^K^T rows (lanes 64..127)
+        {
+            const int t = 32 * (q4 & 1) + lane;
+            const float gt = gam[t], bt = bet[t];
+            float v[32];
+            tc::ld32(tc::taddr(tm, 32 * q4, hf * 32), v);
+            if (q4 < 2) {
+#pragma unroll
+                for (int c = 0; c < 32; c += 4) {
+                    float o4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = hf * 32 + c + e;
+                        o4[e] = i < t ? bt * __expf(gt - gam[i]) * v[c + e] : 0.f;  // exponent <= 0 only
+                    }
+                    *reinterpret_cast<float4*>(Am + t * kUtLd + hf * 32 + c) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float p8[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int i = hf * 32 + 8 * k + e;
+                        p8[e] = i <= t ? __expf(gt - gam[i]) * v[8 * k + e] : 0.f;
+                    }
+                    *reinterpret_cast<uint4*>(sIP + tc::h_off(C + t, hf * 4 + k)) = pack8(p8);
+                }
+            }
+        }
+        __syncthreads();
+        ut_inverse64(Am, Tm, tid, P_THREADS);
+        // T' = T diag(beta) as the B operand of [I; P] T': MN-major, row j holds T'[j][0..63]
+        for (int f = tid; f < C * 8; f += P_THREADS) {
+            const int r = f >> 3, cc = f & 7;
+            float v[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = Tm[r * kUtLd + cc * 8 + e] * bet[cc * 8 + e];
+            *reinterpret_cast<uint4*>(sTB + tc::h_off(r, cc)) = pack8(v);
+        }
+        fence_proxy_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after();
+            if (ok) {
+                const uint32_t a0 = tc::smem_addr(sIP), b0 = tc::smem_addr(sTB);
+                for (int s = 0; s < C / 16; ++s)
+                    tc::mma_f16(tm + 64, tc::sdesc_lbo(a0 + (uint32_t)(s * 32), 16),
+                                tc::sdesc_lbo(b0 + (uint32_t)(s * 2048), 8192), tc::idesc_f16(128, 64, false, true),
+                                s > 0 ? 1u : 0u);
+            }
+            tc::commit(mbar);
+        }
+        wait_mma();
+        {  // [T'; PT'] -> the record tile, K-major [128][64]
+            const int r = 32 * q4 + lane;
+            float v[32];
+            tc::ld32(tc::taddr(tm, 32 * q4, 64 + hf * 32), v);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(sOUT + tc::h_off(r, hf * 4 + k)) = pack8(v + 8 * k);
+        }
+        // e^gamma K^ -> B operand of [W; PW] (MN-major [64 tokens][128 d_k], over [I; P])
+        for (int f = tid; f < C * 16; f += P_THREADS) {
+            const int t = f >> 4, a = (f >> 3) & 1, cc = f & 7;
+            float v[8];
+            unpack_h8(*reinterpret_cast<const uint4*>(sKQ + a * 16384 + tc::h_off(t, cc)), v);
+            const float e = eg[t];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] *= e;
+            *reinterpret_cast<uint4*>(sIP + a * 8192 + tc::h_off(t, cc)) = pack8(v);
+        }
+        fence_proxy_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after();
+            if (ok) {  // [W; PW] = [T'; PT'] (e^gamma K^) (M = 128, N = 128, K = 64)
+                const uint32_t a0 = tc::smem_addr(sOUT), b0 = tc::smem_addr(sIP);
+                for (int s = 0; s < C / 16; ++s)
+                    tc::mma_f16(tm + 128, tc::sdesc_lbo(a0 + (uint32_t)(s * 32), 16),
+                                tc::sdesc_lbo(b0 + (uint32_t)(s * 2048), 8192), tc::idesc_f16(128, 128, false, true),
+                                s > 0 ? 1u : 0u);
+            }
+            tc::commit(mbar);
+        }
+        // V = silu(conv(x)) of the v-head's channels (thread = 8 channels x 4 tokens), into
+        // registers while the product runs
+        uint4 vpk[4];
+        const int cgp = tid & 15, tg = tid >> 4;
+        {
+            const int ch = 2 * Hk * D + j * D + cgp * 8;
+            float w[4][8], bias[8];
+            conv_weights8(A.p, K, raw, ch, w, bias);
+            uint4 rows[7];
+            load_window<4>(J, Cch, K, ch, t0 + 4 * tg, start, end, cin, rows);
+            conv_tokens<4>(rows, w, bias, K, raw, [&](int i, float u[8]) {
+                const int t = 4 * tg + i;
+                float v[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) v[e] = t < n ? u[e] : 0.f;  // zero past the sequence end
+                vpk[i] = pack8(v);
+            });
+        }
+        wait_mma();
+        {  // [-W; Q'] -> staging over A and T (K-major [128][128], atoms of 128 rows)
+            const int r = 32 * q4 + lane;
+            const float e = r < C ? 0.f : eg[r - C];
+#pragma unroll 1
+            for (int b = 0; b < 2; ++b) {
+                float v[32];
+                tc::ld32(tc::taddr(tm, 32 * q4, 128 + hf * 64 + 32 * b), v);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int cc = 4 * b + k;
+                    if (r < C) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) v[8 * k + i] = -v[8 * k + i];
+                    } else {
+                        float qv[8];
+                        unpack_h8(*reinterpret_cast<const uint4*>(sKQ + hf * 16384 + tc::h_off(r, cc)), qv);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) v[8 * k + i] = fmaf(e, qv[i], -v[8 * k + i]);
+                    }
+                    *reinterpret_cast<uint4*>(sAop + hf * 16384 + tc::h_off(r, cc)) = pack8(v + 8 * k);
+                }
+            }
+        }
+        {  // V -> MN-major [64 tokens][128] over e^gamma K^ (read by the finished product)
+            unsigned char* vat = sIP + (cgp >> 3) * 8192;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(vat + tc::h_off(4 * tg + i, cgp & 7)) = vpk[i];
+        }
+        fence_proxy_async_smem();
+        tc::fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            unsigned char* rec = A.rec + ((size_t)cs * Hv + j) * kRec;
+            bulk_s2g(rec, sAop, kAop);
+            bulk_s2g(rec + kRecTP, sOUT, kTP);
+            bulk_s2g(rec + kRecV, sIP, kV);
+            bulk_s2g(rec + kRecG, sOUT + kTP, kGates);
+            bulk_commit();
+        }
+    }
+    if (tid == 0) bulk_wait_read_all();
+    if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 0) tc::dealloc(tm, P_TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// 2. the state chain
+// ---------------------------------------------------------------------------
+constexpr int CH_THREADS = 512;  // 16 warps
+// warps 0..7: critical group (TMEM quadrant warp % 4, column half warp / 4);
+// 8: producer; 9: MMA issuer; 10, 11, 14, 15: y (quadrants 2, 3); 12, 13: idle
+constexpr int W_PROD = 8, W_MMA = 9;
+constexpr uint32_t S_K = 0;                         // 2 stages of K^ (16 KB)
+constexpr uint32_t S_AS = 32768;                    // 2 stages of [-W; Q'] (32 KB): A of RA
+constexpr uint32_t S_TP = S_AS + 2 * kAop;          // 2 stages of [T'; PT'] (16 KB): A of PRE
+constexpr uint32_t S_V = S_TP + 2 * kTP;            // 2 stages of V (16 KB): B of PRE
+constexpr uint32_t S_SOP = S_V + 2 * kV;            // B of RA: S fp16, MN-major [128 d_k][128 d_v] (32 KB)
+constexpr uint32_t S_UP = S_SOP + 32768;            // B of RB: U' fp16, MN-major [64 t][128 d_v] (16 KB)
+constexpr uint32_t S_GATES = S_UP + 16384;          // 2 stages of the gate block (512 B each)
+constexpr uint32_t S_ORED = S_GATES + 2 * kGates;   // [2][2][64] fp32 half-row sums of squares of O
+constexpr uint32_t S_NW = S_ORED + 1024;            // norm_w [128] bf16
+constexpr uint32_t S_BAR = S_NW + 256;              // mbarriers
+constexpr int NBAR = 24;
+constexpr uint32_t S_SMEM = S_BAR + NBAR * 8 + 16;  // + TMEM slot and abort flag
+constexpr uint32_t S_SMEM_ALLOC = S_SMEM + 1024;
+static_assert(S_SMEM_ALLOC <= 232448, "chain shared memory");
+// tensor memory columns: R0 / R1 ([U~; X], then [U; O], of even / odd chunks), S^T (the
+// fp32 state, d_k lanes x d_v columns)
+constexpr uint32_t T_R0 = 0, T_R1 = 128, T_S = 256, T_COLS = 512;
+// barrier pairs (index + chunk parity)
+enum {
+    B_FULL_K = 0,    // K^ and the gates of a chunk landed (producer, tx)
+    B_FULL_A = 2,    // [-W; Q'] landed
+    B_FULL_TP = 4,   // [T'; PT'] landed
+    B_FULL_V = 6,    // V landed
+    B_EMPTY_K = 8,   // K^ and gate stage free (the commit after RB)
+    B_PRE = 10,      // PRE complete (commit): [T'; PT'] and V stages free
+    B_RA = 12,       // RA complete (commit): [-W; Q'] stage free, [U; O] ready
+    B_UP = 14,       // U' written and S^T rescaled in tensor memory (critical group, 256)
+    B_RB = 16,       // RB complete (commit)
+    B_SOP = 18,      // S operand written (critical group, 256)
+    B_OE = 20,       // O rows read from tensor memory (the 4 y warps, 128)
+};
+
+__global__ void __launch_bounds__(CH_THREADS, 1) k_chain16(const __grid_constant__ Args A) {
+    const Geom& g = A.g;
+    const PrefillJob& J = A.J;
+    const int Hk = g.Hk, Hv = g.Hv;
+    const int j = blockIdx.x, seq = blockIdx.y, h = j / g.G;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
+    unsigned char *sK = sm + S_K, *sAS = sm + S_AS, *sTP = sm + S_TP, *sV = sm + S_V;
+    unsigned char *sSOP = sm + S_SOP, *sUP = sm + S_UP;
+    float* sG = reinterpret_cast<float*>(sm + S_GATES);  // [2][128]: e^gamma [64] | e^(gamma_C - gamma) [64]
+    float* ored = reinterpret_cast<float*>(sm + S_ORED);
+    __nv_bfloat16* sNW = reinterpret_cast<__nv_bfloat16*>(sm + S_NW);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + S_BAR);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + NBAR);
+    volatile int* abortp = reinterpret_cast<volatile int*>(tslot + 1);
+
+    int64_t start, end;
+    seq_bounds(J, seq, start, end);
+    const int64_t T = end - start;
+    const int nch = (int)((T + C - 1) / C);
+    const bool outnorm = !(g.flags & kFlagNoOutNorm);
+    const float* Sin = nullptr;
+    float* Sout = nullptr;
+    if (!J.cu_seqlens) {
+        Sin = J.s0 ? J.s0 + (size_t)j * D * D : nullptr;
+        Sout = J.s_final + (size_t)j * D * D;
+    } else {
+        const int slot = J.slot_idx[seq];
+        if (slot >= 0 && slot < J.n_slots) {
+            Sout = J.state_pool + ((size_t)slot * Hv + j) * D * D;
+            if (J.has_init && J.has_init[seq]) Sin = Sout;
+        }
+    }
+
+    // ---- set-up: barriers, tensor memory, norm weights -------------------------------
+    if (warp == 0) tc::alloc(tslot, T_COLS);
+    if (tid == 0) {
+        for (int p = 0; p < 2; ++p) {
+            mbar_init(bar + B_FULL_K + p, 1);
+            mbar_init(bar + B_FULL_A + p, 1);
+            mbar_init(bar + B_FULL_TP + p, 1);
+            mbar_init(bar + B_FULL_V + p, 1);
+            mbar_init(bar + B_EMPTY_K + p, 1);
+            mbar_init(bar + B_PRE + p, 1);
+            mbar_init(bar + B_RA + p, 1);
+            mbar_init(bar + B_UP + p, 256);
+            mbar_init(bar + B_RB + p, 1);
+            mbar_init(bar + B_SOP + p, 256);
+            mbar_init(bar + B_OE + p, 128);
+        }
+        *abortp = 0;
+        fence_mbar_init();
+    }
+    for (int i = tid; i < D; i += CH_THREADS)
+        sNW[i] = outnorm ? static_cast<const __nv_bfloat16*>(A.p.norm_w)[i] : __float2bfloat16(1.f);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = *tslot;
+
+    auto chunk_t0 = [&](int c) -> int64_t { return start + (int64_t)c * C; };
+    auto chunk_n = [&](int c) -> int {
+        const int64_t left = end - chunk_t0(c);
+        return (int)(left < C ? left : C);
+    };
+    auto chunk_slot = [&](int c) -> size_t { return (size_t)(start / C + seq + c); };
+    // bounded wait; after an abort every wait returns at once
+    auto wait = [&](int b, int c) {
+        if (*abortp) return;
+        if (!mbar_wait(bar + b + (c & 1), (uint32_t)((c >> 1) & 1))) *abortp = 1;
+    };
+    auto test = [&](int b, int c) -> bool { return mbar_test(bar + b + (c & 1), (uint32_t)((c >> 1) & 1)); };
+
+    if (warp == W_PROD) {
+        // =============================== producer ===============================
+        // four streams, each issued as soon as its stage is free, in chunk order
+        if (lane == 0 && nch > 0) {
+            int nk = 0, na = 0, ntp = 0, nv = 0;
+            auto src_rec = [&](int c) { return A.rec + (chunk_slot(c) * Hv + j) * kRec; };
+            long long t_start = clock64();
+            while ((nk < nch || na < nch || ntp < nch || nv < nch) && !*abortp) {
+                bool progress = false;
+                if (nk < nch && (nk < 2 || test(B_EMPTY_K, nk - 2))) {
+                    const int c = nk, s = c & 1;
+                    mbar_arrive_expect_tx(bar + B_FULL_K + s, kK + kGates);
+                    bulk_g2s(sK + s * kK, A.kk + (chunk_slot(c) * Hk + h) * kK, kK, bar + B_FULL_K + s);
+                    bulk_g2s(sG + s * 128, src_rec(c) + kRecG, kGates, bar + B_FULL_K + s);
+                    ++nk;
+                    progress = true;
+                }
+                if (na < nch && (na < 2 || test(B_RA, na - 2))) {
+                    const int c = na, s = c & 1;
+                    mbar_arrive_expect_tx(bar + B_FULL_A + s, kAop);
+                    bulk_g2s(sAS + s * kAop, src_rec(c), kAop, bar + B_FULL_A + s);
+                    ++na;
+                    progress = true;
+                }
+                if (ntp < nch && (ntp < 2 || test(B_PRE, ntp - 2))) {
+                    const int c = ntp, s = c & 1;
+                    mbar_arrive_expect_tx(bar + B_FULL_TP + s, kTP);
+                    bulk_g2s(sTP + s * kTP, src_rec(c) + kRecTP, kTP, bar + B_FULL_TP + s);
+                    ++ntp;
+                    progress = true;
+                }
+                if (nv < nch && (nv < 2 || test(B_PRE, nv - 2))) {
+                    const int c = nv, s = c & 1;
+                    mbar_arrive_expect_tx(bar + B_FULL_V + s, kV);
+                    bulk_g2s(sV + s * kV, src_rec(c) + kRecV, kV, bar + B_FULL_V + s);
+                    ++nv;
+                    progress = true;
+                }
+                if (progress) t_start = clock64();
+                else if (clock64() - t_start > kWaitLimitCycles) *abortp = 1;
+            }
+            // no copy may land after the CTA has gone: wait for the last ones (bounded, even after an abort)
+            auto drain = [&](int b, int n) {
+                for (int c = n - 2 < 0 ? 0 : n - 2; c < n; ++c) mbar_wait(bar + b + (c & 1), (uint32_t)((c >> 1) & 1));
+            };
+            drain(B_FULL_K, nk);
+            drain(B_FULL_A, na);
+            drain(B_FULL_TP, ntp);
+            drain(B_FULL_V, nv);
+        }
+    } else if (warp == W_MMA) {
+        // =============================== MMA issuer ===============================
+        if (lane == 0 && nch > 0) {
+            const uint32_t aTP = tc::smem_addr(sTP), aV = tc::smem_addr(sV), aAS = tc::smem_addr(sAS);
+            const uint32_t aSOP = tc::smem_addr(sSOP), aUP = tc::smem_addr(sUP), aK = tc::smem_addr(sK);
+            constexpr uint32_t idPre = tc::idesc_f16(128, 128, false, true);
+            constexpr uint32_t idRa = tc::idesc_f16(128, 128, false, true);
+            constexpr uint32_t idRb = tc::idesc_f16(128, 128, true, true);
+            uint64_t* last = nullptr;  // barrier of the last commit and its parity
+            uint32_t last_par = 0;
+            auto commit = [&](int b, int c) {
+                tc::commit(bar + b + (c & 1));
+                last = bar + b + (c & 1);
+                last_par = (uint32_t)((c >> 1) & 1);
+            };
+            // PRE needs its operands and the [U; O] columns of chunk c-2 read by the y warps
+            // (the U' warps read them before RB(c-2), issued earlier)
+            auto pre_ready = [&](int c) -> bool {
+                return test(B_FULL_TP, c) && test(B_FULL_V, c) && (c < 2 || test(B_OE, c - 2));
+            };
+            auto issue_pre = [&](int c) {  // [U~; X] = [T'; PT'] V into R(c)
+                tc::fence_after();
+                if (!*abortp) {
+                    const uint32_t a0 = aTP + (uint32_t)((c & 1) * kTP), b0 = aV + (uint32_t)((c & 1) * kV);
+                    const uint32_t dcol = (c & 1) ? T_R1 : T_R0;
+                    for (int s = 0; s < C / 16; ++s)
+                        tc::mma_f16(tm + dcol, tc::sdesc_lbo(a0 + (uint32_t)(s * 32), 16),
+                                    tc::sdesc_lbo(b0 + (uint32_t)(s * 2048), 8192), idPre, s > 0 ? 1u : 0u);
+                }
+                commit(B_PRE, c);
+            };
+            auto issue_rb = [&](int c) {  // S^T += K^T U'
+                tc::fence_after();
+                if (!*abortp) {
+                    const uint32_t k0 = aK + (uint32_t)((c & 1) * kK);
+                    for (int s = 0; s < C / 16; ++s)
+                        tc::mma_f16(tm + T_S, tc::sdesc_lbo(k0 + (uint32_t)(s * 2048), 8192),
+                                    tc::sdesc_lbo(aUP + (uint32_t)(s * 2048), 8192), idRb, 1u);
+                }
+                commit(B_RB, c);
+                tc::commit(bar + B_EMPTY_K + (c & 1));
+            };
+            int npre = 0;  // pre-products issued
+            for (int c = 0; c < nch; ++c) {
+                if (npre == c) {  // the pre-product of this chunk was not ready earlier
+                    wait(B_FULL_TP, c);
+                    wait(B_FULL_V, c);
+                    if (c >= 2) wait(B_OE, c - 2);
+                    issue_pre(c);
+                    ++npre;
+                }
+                wait(B_FULL_A, c);
+                wait(B_SOP, c);
+                wait(B_FULL_K, c);
+                tc::fence_after();
+                if (!*abortp) {  // RA: [U; O] = [U~; X] + [-W; Q'] S^T
+                    const uint32_t a0 = aAS + (uint32_t)((c & 1) * kAop);
+                    const uint32_t dcol = (c & 1) ? T_R1 : T_R0;
+                    for (int s = 0; s < D / 16; ++s)
+                        tc::mma_f16(tm + dcol, tc::sdesc_lbo(a0 + (uint32_t)((s >> 2) * 16384 + (s & 3) * 32), 16),
+                                    tc::sdesc_lbo(aSOP + (uint32_t)(s * 2048), 16384), idRa, 1u);
+                }
+                commit(B_RA, c);
+                // RB of this chunk and PRE of the next, in the order their inputs arrive (RB first)
+                bool rb_todo = true;
+                const long long t_start = clock64();
+                while (rb_todo || (npre == c + 1 && npre < nch)) {
+                    if (*abortp) {  // keep every barrier's count: commit without MMAs
+                        if (rb_todo) issue_rb(c);
+                        break;
+                    }
+                    if (rb_todo && test(B_UP, c)) {
+                        issue_rb(c);
+                        rb_todo = false;
+                    } else if (npre == c + 1 && npre < nch && pre_ready(npre)) {
+                        issue_pre(npre);
+                        ++npre;
+                    } else if (clock64() - t_start > kWaitLimitCycles) {
+                        *abortp = 1;
+                    } else if (!rb_todo) {
+                        break;  // the next chunk's pre-product waits at the top of the loop
+                    }
+                }
+            }
+            if (last) mbar_wait(last, last_par);  // every MMA has completed before the TMEM is freed
+        }
+    } else if (warp < 8) {
+        // =============================== critical group ===============================
+        // lanes 0..63 (quadrants 0, 1): U' after RA; all 128 lanes: the S epilogue
+        // after RB.  The S epilogue writes the S operand first (what RA waits for),
+        // then rescales S^T in tensor memory for RB and writes snapshots / the final
+        // state from a re-read.
+        const int q = warp & 3, half = warp >> 2;
+        const int r = 32 * q + lane;  // the tensor-memory lane: d_k of S^T, row of R
+        const bool lo = q < 2;
+        const uint32_t t_s = tc::taddr(tm, 32 * q, T_S + half * 64);
+        // state rows half*64 + 32 b .. + 32 at column r of a [d_v][d_k] fp32 matrix
+        auto store_rows = [&](float* dst, int b, const float* v) {
+            float* d = dst + (size_t)(half * 64 + 32 * b) * D + r;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) d[(size_t)i * D] = v[i];
+        };
+        // S^T <- e S^T in tensor memory for 32 columns from 32 b (RB accumulates onto it)
+        auto rescale = [&](int b, const float* v, float e) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                float w16[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w16[i] = v[16 * k + i] * e;
+                tc::st16_nowait(t_s + 32 * b + 16 * k, w16);
+            }
+        };
+        // S operand rows (fp16, MN-major [d_k][d_v]) for 32 columns from 32 b
+        auto put_sop = [&](int b, const float* v) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint4*>(sSOP + half * 16384 + tc::h_off(r, 4 * b + k)) = pack8(v + 8 * k);
+        };
+        auto s_epilogue = [&](int c) {
+            const bool more = c + 1 < nch;
+            tc::fence_after();
+            if (more) {
+                uint32_t u[64];
+                tc::ld32_nowait(t_s, u);
+                tc::ld32_nowait(t_s + 32, u + 32);
+                tc::ld_wait();
+                put_sop(0, reinterpret_cast<const float*>(u));
+                put_sop(1, reinterpret_cast<const float*>(u) + 32);
+                fence_proxy_async_smem();
+                mbar_arrive(bar + B_SOP + ((c + 1) & 1));
+                wait(B_FULL_K, c + 1);
+            }
+            const float egC = more ? sG[((c + 1) & 1) * 128 + C - 1] : 0.f;
+            const int ck = ckpt_after(J, seq, (int64_t)(c + 1) * C, T);
+            float* snap = ck >= 0 ? J.state_pool + ((size_t)ck * Hv + j) * D * D : nullptr;
+#pragma unroll 1
+            for (int b = 0; b < 2; ++b) {
+                float v[32];
+                tc::ld32(t_s + 32 * b, v);
+                if (more) rescale(b, v, egC);
+                if (snap) store_rows(snap, b, v);           // a prefix snapshot ends with this chunk
+                if (!more && Sout) store_rows(Sout, b, v);  // the final state
+            }
+            if (more) {
+                tc::st_wait();
+                tc::fence_before();
+            }
+        };
+        if (nch > 0) {  // the initial state: S operand of RA(0) and S^T for RB(0)
+            wait(B_FULL_K, 0);
+            const float egC = sG[C - 1];
+            const float* sp = Sin ? Sin + (size_t)(half * 64) * D + r : nullptr;
+#pragma unroll 1
+            for (int b = 0; b < 2; ++b) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = sp ? sp[(size_t)(32 * b + i) * D] : 0.f;
+                put_sop(b, v);
+                rescale(b, v, egC);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar + B_SOP);
+            tc::st_wait();
+            tc::fence_before();
+            if (!lo) mbar_arrive(bar + B_UP);  // S^T of chunk 0 is in place
+        } else if (Sout && Sout != Sin) {  // an empty sequence keeps its state
+#pragma unroll 1
+            for (int b = 0; b < 2; ++b) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = Sin ? Sin[(size_t)(half * 64 + 32 * b + i) * D + r] : 0.f;
+                store_rows(Sout, b, v);
+            }
+        }
+        for (int c = 0; c < nch; ++c) {
+            const int s = c & 1;
+            if (lo) {  // U' = diag(e^(gamma_C - gamma)) U -> B operand of RB
+                wait(B_RA, c);
+                tc::fence_after();
+                const float er = sG[s * 128 + C + r];
+                uint32_t u[64];
+                tc::ld32_nowait(tc::taddr(tm, 32 * q, (s ? T_R1 : T_R0) + half * 64), u);
+                tc::ld32_nowait(tc::taddr(tm, 32 * q, (s ? T_R1 : T_R0) + half * 64 + 32), u + 32);
+                tc::ld_wait();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    float v[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(u[8 * k + i]) * er;
+                    *reinterpret_cast<uint4*>(sUP + half * 8192 + tc::h_off(r, k)) = pack8(v);
+                }
+                fence_proxy_async_smem();
+                tc::fence_before();
+                mbar_arrive(bar + B_UP + s);
+            }
+            wait(B_RB, c);
+            s_epilogue(c);
+            if (!lo && c + 1 < nch) mbar_arrive(bar + B_UP + ((c + 1) & 1));  // S^T rescaled for RB(c+1)
+        }
+    } else if (warp == 10 || warp == 11 || warp == 14 || warp == 15) {
+        // =============================== y warps ===============================
+        const int q = warp & 3, half = (warp - 10) >> 2;
+        const int r = 32 * q + lane;  // tensor-memory lane: a row of O
+        for (int c = 0; c < nch; ++c) {
+            const int s = c & 1;
+            const int t = r - C, n = chunk_n(c);
+            // z of this lane's output row, requested before any wait
+            uint4 zr[8];
+            const size_t row = (size_t)(chunk_t0(c) + (t < n ? t : 0)) * Hv * D + (size_t)j * D + half * 64;
+            if (outnorm && t < n) {
+                const uint4* zp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(J.z) + row);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) zr[k] = zp[k];
+            }
+            wait(B_RA, c);
+            tc::fence_after();
+            const uint32_t t_o = tc::taddr(tm, 32 * q, (s ? T_R1 : T_R0) + half * 64);
+            float part = 0.f;
+#pragma unroll 1
+            for (int b = 0; b < 2; ++b) {
+                float o[32];
+                tc::ld32(t_o + 32 * b, o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) part = fmaf(o[i], o[i], part);
+            }
+            float* ob = ored + s * 128;  // [2][64] per chunk parity
+            ob[half * C + t] = part;
+            named_bar_sync(2, 128);
+            const float rstd = outnorm ? rsqrtf((ob[t] + ob[C + t]) / (float)D + g.norm_eps) : 1.f;
+            uint4* yp = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(J.y) + row);
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                float o[32];
+                tc::ld32(t_o + 32 * b, o);  // warp-collective: every lane loads
+                if (b == 1) {               // the O rows of this chunk have been read
+                    tc::fence_before();
+                    mbar_arrive(bar + B_OE + s);
+                }
+                if (t < n) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint4 pk;
+                        uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+                        const __nv_bfloat162* zh = reinterpret_cast<const __nv_bfloat162*>(&zr[4 * b + k]);
+                        const __nv_bfloat162* wh = reinterpret_cast<const __nv_bfloat162*>(sNW + half * 64 + 32 * b + 8 * k);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = 8 * k + 2 * e;
+                            float y0 = o[i] * rstd, y1 = o[i + 1] * rstd;
+                            if (outnorm) {  // g = w silu(z) in bf16x2: silu(z) = h + h tanh(h), h = z/2
+                                const __nv_bfloat162 hz = __hmul2(zh[e], __float2bfloat162_rn(0.5f));
+                                __nv_bfloat162 th;
+                                {
+                                    uint32_t hi, ho;
+                                    memcpy(&hi, &hz, 4);
+                                    asm("tanh.approx.bf16x2 %0, %1;" : "=r"(ho) : "r"(hi));
+                                    memcpy(&th, &ho, 4);
+                                }
+                                const float2 gf = __bfloat1622float2(__hmul2(__hfma2(hz, th, hz), wh[e]));
+                                y0 *= gf.x;
+                                y1 *= gf.y;
+                            }
+                            const __nv_bfloat162 yb = __floats2bfloat162_rn(y0, y1);
+                            pw[e] = *reinterpret_cast<const uint32_t*>(&yb);
+                        }
+                        yp[4 * b + k] = pk;
+                    }
+                }
+            }
+        }
+    }
+    // ---- tear-down -----------------------------------------------------------------
+    tc::fence_before();
+    __syncthreads();
+    if (*abortp && tid == 0) report_device_status(kDevWaitTimeout);
+    if (warp == 0) tc::dealloc(tm, T_COLS);
+}
+
+}  // namespace c16
+}  // namespace
+
+bool chunk16_applies(const Geom& g) { return g.D == 128 && g.chunk == 64 && g.act_bf16; }
+
+size_t chunk16_workspace_bytes(const Geom& g, int64_t n_tokens, int n_seq) {
+    return n_tokens > 0 ? c16::ws_layout(g, n_tokens, n_seq).total : 0;
+}
+
+cudaError_t chunk16_launch(const Geom& g, const LayerParams& p, const PrefillJob& J, cudaStream_t st) {
+    using namespace c16;
+    static std::atomic<uint64_t> smem_prep{0}, smem_chain{0};
+    cudaError_t e = raise_smem_limit(k_prep16, (int)P_SMEM_ALLOC, smem_prep);
+    if (e != cudaSuccess) return e;
+    e = raise_smem_limit(k_chain16, (int)S_SMEM_ALLOC, smem_chain);
+    if (e != cudaSuccess) return e;
+    Args A;
+    A.g = g;
+    A.p = p;
+    A.J = J;
+    const Ws L = ws_layout(g, J.n_tokens, J.n_seq);
+    unsigned char* ws = static_cast<unsigned char*>(J.workspace);
+    A.kk = ws + L.kk;
+    A.rec = ws + L.rec;
+    A.ncs = L.ncs;
+    if (J.n_tokens > 0) {
+        const int64_t ny = L.ncs < 32768 ? L.ncs : 32768;
+        const dim3 grid((unsigned)g.Hk, (unsigned)ny, (unsigned)((L.ncs + ny - 1) / ny));
+        k_prep16<<<grid, P_THREADS, P_SMEM_ALLOC, st>>>(A);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    k_chain16<<<dim3((unsigned)g.Hv, (unsigned)J.n_seq), CH_THREADS, S_SMEM_ALLOC, st>>>(A);
+    return cudaGetLastError();
+}
+
+cudaError_t take_device_status_chunk16(unsigned* out) { return take_device_status_tu(out); }
+
+}  // namespace gdn

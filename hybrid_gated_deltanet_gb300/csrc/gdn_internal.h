@@ -127,6 +127,11 @@ struct PrefillJob {
     const int32_t* ckpt_slots;
 };
 size_t prefill_workspace_bytes(const Geom& g, int64_t n_tokens, int n_seq);
+// the tcgen05 path for d = 128, chunk 64, bf16 activations (gdn_chunk16.cu):
+// the state chain only; the caller launches the conv-state tail after it
+bool chunk16_applies(const Geom& g);
+size_t chunk16_workspace_bytes(const Geom& g, int64_t n_tokens, int n_seq);
+cudaError_t chunk16_launch(const Geom& g, const LayerParams& prm, const PrefillJob& job, cudaStream_t st);
 cudaError_t launch_prefill(const Geom& g, const LayerParams& prm, const PrefillJob& job,
                            cudaStream_t st);
 
@@ -193,6 +198,7 @@ cudaError_t launch_attn_prefill(const AttnPfJob& job, cudaStream_t st);
 // read and clear the device status word of each kernel file (synchronous)
 cudaError_t take_device_status_decode(unsigned* out);
 cudaError_t take_device_status_prefill(unsigned* out);
+cudaError_t take_device_status_chunk16(unsigned* out);
 cudaError_t take_device_status_proj(unsigned* out);
 
 }  // namespace gdn

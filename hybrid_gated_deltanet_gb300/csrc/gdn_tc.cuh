@@ -16,7 +16,9 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
+#include <string.h>
 
 namespace gdn {
 namespace tc {
@@ -189,6 +191,105 @@ __device__ __forceinline__ void st16(uint32_t taddr, const float v[16]) {
         "r"(__float_as_uint(v[15]))
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// ---- fp16 operands (kind::f16) -------------------------------------------------
+// fp16 tiles use the same 128-byte swizzle: a row of an atom holds 64 fp16
+// values (8 chunks of 16 bytes, chunk index XOR row % 8).  One MMA consumes
+// K = 16.  K-major operands step K inside an atom by 32 bytes; MN-major
+// operands ([K rows][MN], 64 MN values per atom row) step K by 16 rows (2048
+// bytes), and the leading byte offset is the stride between 64-wide MN atoms.
+
+// byte offset of the 16-byte chunk cc (elements 8 cc .. 8 cc + 7) of row r of
+// an fp16 SW128 atom
+__device__ __forceinline__ uint32_t h_off(int r, int cc) {
+    return (uint32_t)(r * 128 + ((cc ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint64_t sdesc_lbo(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;  // stride between MN atoms (MN-major operands)
+    d |= (uint64_t)(1024 >> 4) << 32;            // next 8-row group
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// instruction descriptor: D f32, A/B fp16, A/B K-major unless *_mn, M x N
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+    return (1u << 4) | (a_mn ? (1u << 15) : 0u) | (b_mn ? (1u << 16) : 0u) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// two floats -> fp16x2 (round to nearest), as a 32-bit word (low half = a)
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ float2 unpack_h2(uint32_t u) {
+    __half2 h;
+    memcpy(&h, &u, 4);
+    return __half22float2(h);
+}
+
+// 32 consecutive columns of this warp's 32 lanes, no wait
+__device__ __forceinline__ void ld32_nowait(uint32_t taddr, uint32_t r[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 64 consecutive columns (two loads, one wait)
+__device__ __forceinline__ void ld64(uint32_t taddr, float v[64]) {
+    uint32_t r[64];
+    ld32_nowait(taddr, r);
+    ld32_nowait(taddr + 32, r + 32);
+    ld_wait();
+#pragma unroll
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 consecutive columns
+__device__ __forceinline__ void ld32(uint32_t taddr, float v[32]) {
+    uint32_t r[32];
+    ld32_nowait(taddr, r);
+    ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// store 16 consecutive columns, no wait
+__device__ __forceinline__ void st16_nowait(uint32_t taddr, const float v[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
 }
 
 // TMEM address of (lane, column) relative to an allocation base

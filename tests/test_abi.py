@@ -110,12 +110,17 @@ def test_counts(lib):
 def test_workspace_size_and_refusal(lib):
     cfg = _cfg()
     need = lib.gdn_workspace_size(ctypes.byref(cfg), gb.OP_CHUNK_PREFILL, 8192, 1)
-    # the larger of the two prefill workspaces: fp32 per token (q^ and k^ 2 x 16 x 128, v 32 x 128,
-    # g and beta 2 x 32), or operand tiles per 64-token chunk slot (8192/64 + 1 sequence + 1 slots;
-    # per k-head Q^, K^, K^T tiles of 32 KB, per v-head 4 V^T tiles of 8 KB and 512 B of gates)
-    per_token = 8192 * (2 * 16 * 128 + 32 * 128 + 2 * 32) * 4
-    tiles = (8192 // 64 + 2) * (16 * 3 * 32768 + 32 * 4 * 8192 + 32 * 512 + 32 * 164864)
-    assert need == max(per_token, tiles)
+    # d = 128, chunk 64, bf16: per 64-token chunk slot (8192/64 + 1 sequence + 1 slots), per k-head the
+    # fp16 K^ tile (16 KB), per v-head the fp16 [-W; Q'] (32 KB), [T'; PT'] (16 KB) and V (16 KB)
+    # tiles and 512 B of gates; the two sections start on 1024-byte boundaries
+    slots = 8192 // 64 + 2
+    kk = slots * 16 * 16384
+    rec = slots * 32 * (32768 + 16384 + 16384 + 512)
+    assert need == kk + (rec + 1023) // 1024 * 1024
+    # every other geometry: fp32 per token (q^ and k^ 2 x 16 x 128, v 32 x 128, g and beta 2 x 32)
+    f32 = _cfg(act_dtype=gb.F32)
+    assert lib.gdn_workspace_size(ctypes.byref(f32), gb.OP_CHUNK_PREFILL, 8192, 1) == \
+        8192 * (2 * 16 * 128 + 32 * 128 + 2 * 32) * 4
     assert lib.gdn_workspace_size(ctypes.byref(cfg), gb.OP_DECODE_STEP, 64, 1) == 0
     bad = _cfg(chunk=48)
     assert lib.gdn_workspace_size(ctypes.byref(bad), gb.OP_CHUNK_PREFILL, 10, 1) == 0

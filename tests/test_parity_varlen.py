@@ -67,11 +67,10 @@ def test_varlen_small_mixed_init():
     np.testing.assert_array_equal(c_got[rest], CS.f64[rest])
 
 
-@pytest.mark.parametrize("slices", ["2", "4"])
-def test_varlen_chain_slices(monkeypatch, slices):
-    """The state chain split in 2 slices of 64 state rows or 4 of 32 (chosen by
-    how many chain CTAs the batch makes; forced here) gives the same results."""
-    monkeypatch.setenv("GDN_CHAIN_SLICES", slices)
+def test_varlen_mixed_lengths_and_init():
+    """Sequences of 200, 1, 64, 130 and 63 tokens (full chunks, a one-token
+    sequence, exact and ragged tails) with mixed initial states, through one
+    varlen call."""
     lens = [200, 1, 64, 130, 63]
     geom, act, r, p, tok = make_case("serving", 4, sum(lens))
     cfg = config(geom, act)
