@@ -116,16 +116,22 @@ __device__ __forceinline__ void unpack_h8(const uint4& u, float* f) {
 // ---------------------------------------------------------------------------
 constexpr int P_THREADS = 256;
 constexpr uint32_t P_KQ = 0;                          // [K^; Q^] fp16 [128][128] (atoms of 128 rows)
-constexpr uint32_t P_IP = 32768;                      // [I; P] (A of the T' product), then e^gamma K^, then V
+constexpr uint32_t P_IP = 32768;                      // [I; P] (A of the T' product), then e^gamma K^
 constexpr uint32_t P_TB = 49152;                      // T' fp16 MN-major [64 (j)][64 (i)]
 constexpr uint32_t P_OUT = 57344;                     // [T'; PT'] tile, then the gates (512 B)
-constexpr uint32_t P_AM = P_OUT + kTP + kGates;       // A fp32 [64][kUtLd]; then [-W; Q'] (with Tm)
+constexpr uint32_t P_AM = P_OUT + kTP + kGates;       // A fp32 [64][kUtLd]
 constexpr uint32_t P_TM = P_AM + 64 * kUtLd * 4;      // T fp32 [64][kUtLd]
 constexpr uint32_t P_SMALL = P_TM + 64 * kUtLd * 4;   // gamma [64], beta [64], mbarrier, TMEM slot
 constexpr uint32_t P_SMEM = P_SMALL + 2 * C * 4 + 16;
 constexpr uint32_t P_SMEM_ALLOC = P_SMEM + 1024;
 constexpr uint32_t P_TMEM_COLS = 256;                 // Gram (64) | [T'; PT'] (64) | [W; PW] (128)
-static_assert(P_TM + 64 * kUtLd * 4 - P_AM >= kAop, "[-W; Q'] staging");
+// staging of raw x rows (token t0-3+r in row r), requested before any arithmetic:
+// the k-head's q and k channels over [I; P] .. the gates (67 rows of 512 B), and the
+// channels of 2 v-heads over A and T (67 rows of 256 B each)
+constexpr uint32_t P_XQK = P_IP, P_XV = P_AM;
+constexpr int kXRows = C + 3;
+static_assert(P_XQK + kXRows * 512 <= P_AM, "q/k staging");
+static_assert(P_XV + 2 * kXRows * 256 <= P_SMALL, "v staging");
 
 __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__ Args A) {
     using L = Act<__nv_bfloat16>;
@@ -144,7 +150,7 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
     unsigned char *sKQ = sm + P_KQ, *sIP = sm + P_IP, *sTB = sm + P_TB, *sOUT = sm + P_OUT;
-    unsigned char* sAop = sm + P_AM;
+    unsigned char *sXQK = sm + P_XQK, *sXV = sm + P_XV;
     float* eg = reinterpret_cast<float*>(sOUT + kTP);  // the record's gate block
     float* erev = eg + C;
     float* Am = reinterpret_cast<float*>(sm + P_AM);
@@ -154,31 +160,72 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
     uint64_t* mbar = reinterpret_cast<uint64_t*>(bet + C);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
     const bool raw = g.flags & kFlagRawQKV;
+    const bool direct = g.flags & kFlagGatesDirect;
     int slot_ok;
-    const void* cin = seq_conv_in(J, g, sq, slot_ok);
+    const __nv_bfloat16* cin = static_cast<const __nv_bfloat16*>(seq_conv_in(J, g, sq, slot_ok));
+    const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(J.x);
+
+    // stage x rows t0-3 .. t0+63 of `nch16` 16-byte channel groups starting at channel
+    // ch0 (row stride `rowb` bytes): rows before the sequence come from its conv state
+    // (or are zero), rows past its end are not read
+    auto stage_rows = [&](unsigned char* dst, int ch0, int nch16, int rowb, int f0, int nf) {
+        for (int f = f0 + tid; f < nf; f += P_THREADS) {
+            const int r = f / nch16, c16i = f % nch16;
+            const int64_t tau = t0 - 3 + r;
+            unsigned char* d = dst + r * rowb + c16i * 16;
+            const int ch = ch0 + c16i * 8;
+            if (tau >= start && tau < end) {
+                cp_async16(d, x + (size_t)tau * Cch + ch);
+            } else if (tau < start && cin && tau - start >= -(K - 1)) {
+                cp_async16(d, cin + (size_t)((K - 1) + (tau - start)) * Cch + ch);
+            } else {
+                *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
+            }
+        }
+    };
+    // the q/k rows: channel group c16i < 16 is q, >= 16 is k (contiguous in shared memory)
+    for (int f = tid; f < kXRows * 32; f += P_THREADS) {
+        const int r = f >> 5, c16i = f & 31;
+        const int64_t tau = t0 - 3 + r;
+        unsigned char* d = sXQK + r * 512 + c16i * 16;
+        const int ch = (c16i < 16 ? h : Hk + h) * D + (c16i & 15) * 8;
+        if (tau >= start && tau < end) cp_async16(d, x + (size_t)tau * Cch + ch);
+        else if (tau < start && cin && tau - start >= -(K - 1))
+            cp_async16(d, cin + (size_t)((K - 1) + (tau - start)) * Cch + ch);
+        else *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
+    }
+    // the v rows of the first (up to) 2 v-heads
+    for (int u = 0; u < 2 && u < G; ++u) stage_rows(sXV + u * kXRows * 256, 2 * Hk * D + (h * G + u) * D, 16, 256, 0, kXRows * 16);
+    cp_async_commit();
 
     if (warp == 0) tc::alloc(tslot, P_TMEM_COLS);
     if (tid == 0) {
         mbar_init(mbar, 1);
         fence_mbar_init();
     }
+    const int ch_qk = (lane < 16 ? h : Hk + h) * D + (lane & 15) * 8;
+    float wqk[4][8], bqk[8];
+    conv_weights8(A.p, K, raw, ch_qk, wqk, bqk);
+    cp_async_wait_all();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tm = *tslot;
 
     // ---- conv + SiLU + L2 norm of q and k: thread = 8 channels (lanes 0..15 q,
     // 16..31 k) x 8 tokens (one warp's) -> rows 0..63 K^, 64..127 Q^ -------------
     {
         const bool is_q = lane < 16;
         const int d0 = (lane & 15) * 8;
-        const int ch = (is_q ? h : Hk + h) * D + d0;
-        float w[4][8], bias[8];
-        conv_weights8(A.p, K, raw, ch, w, bias);
         const int tt0 = warp * 8;
         uint4 rows[11];
-        load_window<8>(J, Cch, K, ch, t0 + tt0, start, end, cin, rows);
+#pragma unroll
+        for (int k = 0; k < 11; ++k) rows[k] = *reinterpret_cast<const uint4*>(sXQK + (tt0 + k) * 512 + lane * 16);
         unsigned char* atom = sKQ + (d0 >> 6) * 16384;
         const int cc = (d0 & 63) >> 3;
         const float qs = is_q ? g.q_scale : 1.f;
         const bool l2 = !(g.flags & kFlagNoL2);
-        conv_tokens<8>(rows, w, bias, K, raw, [&](int i, float u[8]) {
+        conv_tokens<8>(rows, wqk, bqk, K, raw, [&](int i, float u[8]) {
             const int t = tt0 + i;
             float ss = 0.f;
 #pragma unroll
@@ -196,7 +243,6 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
-    const uint32_t tm = *tslot;
     if (tid == 0) {
         // K^ for the chain: the first 64 rows of each atom
         unsigned char* dst = A.kk + ((size_t)cs * Hk + h) * kK;
@@ -223,24 +269,61 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
         ok = __syncthreads_and(ok && w);
         tc::fence_after();
     };
-    wait_mma();
 
-    const bool direct = g.flags & kFlagGatesDirect;
     for (int jj = 0; jj < G; ++jj) {
         const int j = h * G + jj;
-        if (tid == 0) bulk_wait_read_all();  // the previous record's stores have read shared memory
-        __syncthreads();
+        unsigned char* rec = A.rec + ((size_t)cs * Hv + j) * kRec;
+        if (jj >= 2 && jj % 2 == 0) {  // the v rows of the next 2 v-heads (A and T are free again)
+            for (int u = 0; u < 2 && jj + u < G; ++u)
+                stage_rows(sXV + u * kXRows * 256, 2 * Hk * D + (j + u) * D, 16, 256, 0, kXRows * 16);
+            cp_async_commit();
+            cp_async_wait_all();
+            __syncthreads();
+        }
+        // gate inputs of token t = tid, requested before the V conv
+        float ga = 0.f, gb = 0.f;
+        if (tid < n) {
+            const size_t tok = (size_t)(t0 + tid);
+            ga = L::ld(J.a, tok * Hv + j);
+            gb = L::ld(J.b, tok * Hv + j);
+        }
+        // V = silu(conv(x)) of the group's 2 v-heads from the staged rows (thread = 8
+        // channels x 4 tokens), straight to the records (MN-major [64 tokens][128] fp16),
+        // before A and T overwrite the staging
+        if (jj % 2 == 0) {
+            const int cgp = tid & 15, tg = tid >> 4;
+            for (int u = 0; u < 2 && jj + u < G; ++u) {
+                float w[4][8], bias[8];
+                conv_weights8(A.p, K, raw, 2 * Hk * D + (j + u) * D + cgp * 8, w, bias);
+                const unsigned char* xv = sXV + u * kXRows * 256;
+                uint4 rows[7];
+#pragma unroll
+                for (int k = 0; k < 7; ++k) rows[k] = *reinterpret_cast<const uint4*>(xv + (4 * tg + k) * 256 + cgp * 16);
+                unsigned char* vat = A.rec + ((size_t)cs * Hv + j + u) * kRec + kRecV + (cgp >> 3) * 8192;
+                conv_tokens<4>(rows, w, bias, K, raw, [&](int i, float uu[8]) {
+                    const int t = 4 * tg + i;
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) v[e] = t < n ? uu[e] : 0.f;  // zero past the sequence end
+                    *reinterpret_cast<uint4*>(vat + tc::h_off(t, cgp & 7)) = pack8(v);
+                });
+            }
+        }
+        if (jj == 0) {
+            wait_mma();  // the Gram
+        } else {
+            if (tid == 0) bulk_wait_read_all();  // the previous [T'; PT'] store has read sOUT
+            __syncthreads();
+        }
         if (tid < C) {  // gates of token t = tid (zero past the sequence end)
             float gl = 0.f, be = 0.f;
-            if (tid < n) {
-                const size_t tok = (size_t)(t0 + tid);
-                gates(L::ld(J.a, tok * Hv + j), L::ld(J.b, tok * Hv + j), direct ? 0.f : A.p.A_log[j],
-                      (!direct && A.p.dt_bias) ? A.p.dt_bias[j] : 0.f, direct, gl, be);
-            }
+            if (tid < n)
+                gates(ga, gb, direct ? 0.f : A.p.A_log[j], (!direct && A.p.dt_bias) ? A.p.dt_bias[j] : 0.f, direct,
+                      gl, be);
             gam[tid] = gl;
             bet[tid] = be;
         }
-        // identity rows of [I; P] (the region served as e^gamma K^ and V before)
+        // identity rows of [I; P] (the region held e^gamma K^ or the q/k rows before)
         for (int f = tid; f < C * 8; f += P_THREADS) {
             const int r = f >> 3, cc = f & 7;
             uint32_t wd[4] = {0u, 0u, 0u, 0u};
@@ -344,6 +427,9 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
         __syncthreads();
         if (tid == 0) {
             tc::fence_after();
+            bulk_s2g(rec + kRecTP, sOUT, kTP);  // [T'; PT'] and the gates
+            bulk_s2g(rec + kRecG, sOUT + kTP, kGates);
+            bulk_commit();
             if (ok) {  // [W; PW] = [T'; PT'] (e^gamma K^) (M = 128, N = 128, K = 64)
                 const uint32_t a0 = tc::smem_addr(sOUT), b0 = tc::smem_addr(sIP);
                 for (int s = 0; s < C / 16; ++s)
@@ -353,28 +439,11 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
             }
             tc::commit(mbar);
         }
-        // V = silu(conv(x)) of the v-head's channels (thread = 8 channels x 4 tokens), into
-        // registers while the product runs
-        uint4 vpk[4];
-        const int cgp = tid & 15, tg = tid >> 4;
-        {
-            const int ch = 2 * Hk * D + j * D + cgp * 8;
-            float w[4][8], bias[8];
-            conv_weights8(A.p, K, raw, ch, w, bias);
-            uint4 rows[7];
-            load_window<4>(J, Cch, K, ch, t0 + 4 * tg, start, end, cin, rows);
-            conv_tokens<4>(rows, w, bias, K, raw, [&](int i, float u[8]) {
-                const int t = 4 * tg + i;
-                float v[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = t < n ? u[e] : 0.f;  // zero past the sequence end
-                vpk[i] = pack8(v);
-            });
-        }
         wait_mma();
-        {  // [-W; Q'] -> staging over A and T (K-major [128][128], atoms of 128 rows)
+        {  // [-W; Q'] -> the record (K-major [128][128], atoms of 128 rows), from registers
             const int r = 32 * q4 + lane;
             const float e = r < C ? 0.f : eg[r - C];
+            unsigned char* aop = rec + hf * 16384;
 #pragma unroll 1
             for (int b = 0; b < 2; ++b) {
                 float v[32];
@@ -391,26 +460,11 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
 #pragma unroll
                         for (int i = 0; i < 8; ++i) v[8 * k + i] = fmaf(e, qv[i], -v[8 * k + i]);
                     }
-                    *reinterpret_cast<uint4*>(sAop + hf * 16384 + tc::h_off(r, cc)) = pack8(v + 8 * k);
+                    *reinterpret_cast<uint4*>(aop + tc::h_off(r, cc)) = pack8(v + 8 * k);
                 }
             }
         }
-        {  // V -> MN-major [64 tokens][128] over e^gamma K^ (read by the finished product)
-            unsigned char* vat = sIP + (cgp >> 3) * 8192;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(vat + tc::h_off(4 * tg + i, cgp & 7)) = vpk[i];
-        }
-        fence_proxy_async_smem();
         tc::fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            unsigned char* rec = A.rec + ((size_t)cs * Hv + j) * kRec;
-            bulk_s2g(rec, sAop, kAop);
-            bulk_s2g(rec + kRecTP, sOUT, kTP);
-            bulk_s2g(rec + kRecV, sIP, kV);
-            bulk_s2g(rec + kRecG, sOUT + kTP, kGates);
-            bulk_commit();
-        }
     }
     if (tid == 0) bulk_wait_read_all();
     if (!ok && tid == 0) report_device_status(kDevWaitTimeout);

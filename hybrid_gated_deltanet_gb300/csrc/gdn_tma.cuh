@@ -74,6 +74,14 @@ __device__ __forceinline__ void tma_tile_2d(void* dst, const void* tmap, int x, 
         : "memory");
 }
 
+// 16-byte global -> shared copy through L2 (cp.async); complete with
+// cp_async_commit / cp_async_wait_all
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src_gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst_smem)), "l"(src_gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // global -> shared (this CTA), completion counted on `bar` in bytes
 __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes, uint64_t* bar) {
     asm volatile(
