@@ -165,14 +165,14 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
     const __nv_bfloat16* cin = static_cast<const __nv_bfloat16*>(seq_conv_in(J, g, sq, slot_ok));
     const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(J.x);
 
-    // stage x rows t0-3 .. t0+63 of `nch16` 16-byte channel groups starting at channel
-    // ch0 (row stride `rowb` bytes): rows before the sequence come from its conv state
-    // (or are zero), rows past its end are not read
-    auto stage_rows = [&](unsigned char* dst, int ch0, int nch16, int rowb, int f0, int nf) {
-        for (int f = f0 + tid; f < nf; f += P_THREADS) {
-            const int r = f / nch16, c16i = f % nch16;
+    // stage x rows t0-3 .. t0+63 of 16 channel groups of 8 (one v-head's 128 channels,
+    // from channel ch0) into rows of 256 bytes: rows before the sequence come from its
+    // conv state (or are zero), rows past its end are not read
+    auto stage_v = [&](unsigned char* dst, int ch0) {
+        for (int f = tid; f < kXRows * 16; f += P_THREADS) {
+            const int r = f >> 4, c16i = f & 15;
             const int64_t tau = t0 - 3 + r;
-            unsigned char* d = dst + r * rowb + c16i * 16;
+            unsigned char* d = dst + r * 256 + c16i * 16;
             const int ch = ch0 + c16i * 8;
             if (tau >= start && tau < end) {
                 cp_async16(d, x + (size_t)tau * Cch + ch);
@@ -195,7 +195,7 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
         else *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
     }
     // the v rows of the first (up to) 2 v-heads
-    for (int u = 0; u < 2 && u < G; ++u) stage_rows(sXV + u * kXRows * 256, 2 * Hk * D + (h * G + u) * D, 16, 256, 0, kXRows * 16);
+    for (int u = 0; u < 2 && u < G; ++u) stage_v(sXV + u * kXRows * 256, 2 * Hk * D + (h * G + u) * D);
     cp_async_commit();
 
     if (warp == 0) tc::alloc(tslot, P_TMEM_COLS);
@@ -274,8 +274,7 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
         const int j = h * G + jj;
         unsigned char* rec = A.rec + ((size_t)cs * Hv + j) * kRec;
         if (jj >= 2 && jj % 2 == 0) {  // the v rows of the next 2 v-heads (A and T are free again)
-            for (int u = 0; u < 2 && jj + u < G; ++u)
-                stage_rows(sXV + u * kXRows * 256, 2 * Hk * D + (j + u) * D, 16, 256, 0, kXRows * 16);
+            for (int u = 0; u < 2 && jj + u < G; ++u) stage_v(sXV + u * kXRows * 256, 2 * Hk * D + (j + u) * D);
             cp_async_commit();
             cp_async_wait_all();
             __syncthreads();
