@@ -11,17 +11,22 @@
 // their inputs, outputs and states; only the scratch moves here.
 //
 // Contract:
-// - The scratch is kNoAllocScratchBytes (64 MiB).  Every GPU that loads this
-//   library holds that much device memory until the process exits.
-// - The first call on a device looks up the array's device address with
-//   cudaGetSymbolAddress (with that device current) and caches it; make that
-//   first call before any stream capture.  Later calls only read the cache.
+// - The scratch is kNoAllocScratchBytes (64 MiB).  A device holds it from the
+//   moment the library's module is loaded there (at the first use of the library
+//   on that device under CUDA's lazy loading) until the process exits.
+// - Each call looks up the array's device address for the current device and
+//   context with cudaGetSymbolAddress the first time that context is seen, and
+//   caches it under the context's unique id; a device reset or a new primary
+//   context makes the next call look it up again.  Make the first call in a
+//   context before any stream capture.
 // - All calls share the one array, which keeps the previous call's contents.
-//   Nothing in it needs to start at zero: the prologue kernel writes every
-//   workspace entry the chunk kernel reads.  Calls that overlap on the GPU
-//   (different streams, or different host threads without ordering) race on
-//   the array and give undefined results.
+//   Nothing in it needs to start at zero: the prefill writes every workspace
+//   entry it reads.  Calls that overlap on the GPU (different streams, or
+//   different host threads without ordering) race on the array and give
+//   undefined results.
 // - This file calls no cudaMalloc, cudaFree or allocating library routine.
+#include <cuda.h>
+
 #include <cstdio>
 #include <mutex>
 
@@ -42,7 +47,33 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_prefill_scratch[kNoAllocScratchBytes];
 
 std::mutex g_mu;
+// per device: the context id the address was looked up in, and the address
+unsigned long long g_ctx_id[kMaxDevices] = {};
 void* g_scratch_ptr[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name, unsigned version) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(p);
+}
+
+// unique id of the current context (0 if it cannot be read: the address is then
+// looked up on every call)
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_ctx = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent", 4000);
+    static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId", 12000);
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_ctx || !get_id || get_ctx(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 gdn_status scratch_for_current_device(void** out) {
     int dev = -1;
@@ -57,8 +88,11 @@ gdn_status scratch_for_current_device(void** out) {
         snprintf(msg, sizeof msg, "device: found ordinal %d, required 0..%d", dev, kMaxDevices - 1);
         return (gdn_status)gdn::report_error(GDN_ERR_UNSUPPORTED, msg);
     }
+    // id 0: no current context yet (cudaGetSymbolAddress below makes the primary one
+    // current) or the driver entry points are missing: look the address up this time
+    const unsigned long long id = current_context_id();
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_scratch_ptr[dev] || id == 0 || g_ctx_id[dev] != id) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_prefill_scratch);
         if (e != cudaSuccess || !p) {
@@ -68,6 +102,7 @@ gdn_status scratch_for_current_device(void** out) {
             return (gdn_status)gdn::report_error(GDN_ERR_CUDA, msg);
         }
         g_scratch_ptr[dev] = p;
+        g_ctx_id[dev] = id;
     }
     *out = g_scratch_ptr[dev];
     return GDN_OK;

@@ -257,16 +257,19 @@ gdn_status gdn_varlen_prefill_ckpt(const gdn_config* cfg, const gdn_params* prm,
  * allowed there), or a latency-critical path that cannot pay for the
  * device-wide synchronisation of cudaFree.
  * Same arguments and results as gdn_chunk_prefill, minus the workspace: the
- * workspace is a static device array of 64 MiB inside libgdn, which every GPU
- * that loads the library holds until the process exits.  T is limited to
- * what fits: gdn_workspace_size(cfg, GDN_OP_CHUNK_PREFILL, T, 1) <= 64 MiB
- * (about 440 tokens at the Qwen3.5-4B geometry); larger T returns
- * GDN_ERR_WORKSPACE with both sizes in gdn_last_error().
- * The first call on a device looks up the array's address (cudaGetSymbolAddress,
- * with that device current) and caches it: make that first call before any
- * stream capture.  All calls share the array and it keeps the previous call's
- * contents (nothing in it needs to start at zero); calls that overlap on the
- * GPU race on it.  Nothing here allocates. */
+ * workspace is a static device array of 64 MiB inside libgdn, held on each
+ * device where the library has been used (its module loaded there) until the
+ * process exits.  T is limited to what fits:
+ * gdn_workspace_size(cfg, GDN_OP_CHUNK_PREFILL, T, 1) <= 64 MiB (1727 tokens
+ * at the Qwen3.5-4B geometry); larger T returns GDN_ERR_WORKSPACE with
+ * both sizes in gdn_last_error().
+ * A call looks up the array's device address (cudaGetSymbolAddress, with the
+ * device current) the first time it runs in a CUDA context and caches it under
+ * that context's unique id, so a device reset or a new primary context makes the
+ * next call look it up again: make the first call in a context before any stream
+ * capture.  All calls share the array and it keeps the previous call's contents
+ * (nothing in it needs to start at zero); calls that overlap on the GPU race on
+ * it.  Nothing here allocates. */
 gdn_status gdn_chunk_prefill_noalloc(const gdn_config* cfg, const gdn_params* prm, const void* x,
                                      const void* z, const void* a, const void* b, int64_t T,
                                      const float* s0, const void* conv0, float* s_final,
