@@ -6,6 +6,7 @@
 // 6.5): name the argument, the value found and the value required.
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <string>
 
 #include "../../include/gdn.h"
@@ -252,6 +253,37 @@ gdn_status gdn_conv_state_update(const gdn_config* cfg, const gdn_params* prm, c
     return cuda_status(gdn::launch_conv_update(g, p, job, (cudaStream_t)stream), "gdn_conv_state_update");
 }
 
+// GDN_DEBUG set (and not "0"): slot indices are checked on the device before the
+// call's kernels; unless the stream is being captured, the call then waits for the
+// check and refuses bad indices with GDN_ERR_RANGE (the capture case only sets the
+// status bit GDN_DEV_BAD_SLOT for gdn_device_status)
+static bool debug_on() {
+    const char* e = std::getenv("GDN_DEBUG");
+    return e && e[0] && !(e[0] == '0' && e[1] == 0);
+}
+
+static gdn_status debug_check_slots(const char* name_a, const int32_t* idx_a, int na, const char* name_b,
+                                    const int32_t* idx_b, int nb, int n_slots, void* stream) {
+    if (!debug_on() || na + nb == 0) return GDN_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cap);
+    if (e != cudaSuccess) return cuda_status(e, "GDN_DEBUG slot check");
+    long long bad = -1, di = -1, dj = -1;
+    int32_t v = 0;
+    e = gdn::check_slots(idx_a, na, idx_b, nb, n_slots, st, cap == cudaStreamCaptureStatusNone, &bad, &di, &dj, &v);
+    if (e != cudaSuccess) return cuda_status(e, "GDN_DEBUG slot check");
+    auto name = [&](long long k) { return k < na ? name_a : name_b; };
+    auto pos = [&](long long k) { return k < na ? k : k - na; };
+    if (bad >= 0)
+        return fail(GDN_ERR_RANGE, "%s[%lld]: found slot %d, required 0..%d (GDN_DEBUG)", name(bad), pos(bad), v,
+                    n_slots - 1);
+    if (di >= 0)
+        return fail(GDN_ERR_RANGE, "%s[%lld] and %s[%lld]: found slot %d twice, required distinct slots (GDN_DEBUG)",
+                    name(di), pos(di), name(dj), pos(dj), v);
+    return GDN_OK;
+}
+
 static gdn_status rows_check(const gdn_config* cfg, const gdn_params* prm, const void* x, const void* z,
                              const void* a, const void* b, void* conv_pool, float* state_pool,
                              const int32_t* slot_idx, int32_t B, int32_t r, int32_t n_slots, void* y, int mode,
@@ -286,6 +318,9 @@ static gdn_status rows_common(const gdn_config* cfg, const gdn_params* prm, cons
                                accepted, &g, &p);
     if (st) return st;
     if (B == 0) return ok();
+    if ((st = debug_check_slots("slot_idx", slot_idx, B, "snap_idx", snap_idx, snap_idx ? B * r : 0, n_slots,
+                                stream)))
+        return st;
     gdn::RowsJob job{x, z, a, b, conv_pool, state_pool, slot_idx, snap_idx, y, B, r, n_slots};
     job.mode = mode;
     job.accepted = accepted;
@@ -337,6 +372,7 @@ gdn_status gdn_commit_rows(const gdn_config* cfg, void* conv_pool, float* state_
     GDN_REQUIRE_PTR_A(slot_idx, "slot_idx", 4u);
     GDN_REQUIRE_PTR_A(snap_idx, "snap_idx", 4u);
     GDN_REQUIRE_PTR_A(accepted, "accepted", 4u);
+    if ((st = debug_check_slots("slot_idx", slot_idx, B, "snap_idx", snap_idx, B * r, n_slots, stream))) return st;
     gdn::CommitJob job{conv_pool, state_pool, slot_idx, snap_idx, accepted, B, r, n_slots};
     return cuda_status(gdn::launch_commit(g, job, (cudaStream_t)stream), "gdn_commit_rows");
 }
@@ -368,6 +404,9 @@ static gdn_status prefill_common(const gdn_config* cfg, const gdn_params* prm, g
     gdn::LayerParams p;
     gdn_status st = prefill_check(cfg, prm, job, &g, &p);
     if (st) return st;
+    if (job.slot_idx &&
+        (st = debug_check_slots("slot_idx", job.slot_idx, (int)job.n_seq, "", nullptr, 0, job.n_slots, stream)))
+        return st;
     return cuda_status(gdn::launch_prefill(g, p, job, (cudaStream_t)stream), who);
 }
 

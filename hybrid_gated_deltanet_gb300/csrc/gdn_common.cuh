@@ -59,6 +59,7 @@ constexpr uint32_t kFlagRawQKV = 1u, kFlagNoL2 = 2u, kFlagGatesDirect = 4u, kFla
 // compiled without relocatable device code, so every translation unit that
 // includes this header has its own word and its own reader below.
 constexpr unsigned kDevWaitTimeout = 1u;
+constexpr unsigned kDevBadSlot = 2u;  // GDN_DEBUG: a slot index out of range or repeated
 
 static __device__ unsigned int g_device_status = 0;
 

@@ -974,6 +974,67 @@ cudaError_t launch_conv_update(const Geom& g, const LayerParams& p, const ConvJo
     return cudaGetLastError();
 }
 
+// ---- debug check of slot indices (GDN_DEBUG) -------------------------------
+// result: [0] first position holding an index outside [0, n_slots) (INT32_MAX: none),
+// [1..2] first pair (i, j), i < j, holding the same index (packed i * 2^32 + j;
+// ~0: none).  Positions run over the concatenation of idx_a [na] and idx_b [nb].
+namespace {
+__device__ unsigned long long g_slot_check[2];
+
+__global__ void k_check_slots(const int32_t* idx_a, int na, const int32_t* idx_b, int nb, int n_slots) {
+    // one thread per position i compares it with every later position: quadratic,
+    // which is fine for a debugging aid at the batch sizes the calls take
+    const int n = na + nb;
+    auto at = [&](int k) { return k < na ? __ldg(idx_a + k) : __ldg(idx_b + (k - na)); };
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int v = at(i);
+    bool bad = false;
+    if (v < 0 || v >= n_slots) {
+        atomicMin(&g_slot_check[0], (unsigned long long)i);
+        bad = true;
+    }
+    for (int j = i + 1; j < n; ++j) {
+        if (at(j) == v) {
+            atomicMin(&g_slot_check[1], ((unsigned long long)i << 32) | (unsigned long long)j);
+            bad = true;
+            break;
+        }
+    }
+    if (bad) report_device_status(kDevBadSlot);
+}
+
+__global__ void k_check_reset() { g_slot_check[0] = g_slot_check[1] = ~0ull; }
+}  // namespace
+
+cudaError_t check_slots(const int32_t* idx_a, int na, const int32_t* idx_b, int nb, int n_slots, cudaStream_t st,
+                        bool wait, long long* bad_range, long long* dup_i, long long* dup_j, int32_t* value) {
+    // a reset kernel rather than a host copy keeps the check capturable
+    k_check_reset<<<1, 1, 0, st>>>();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int n = na + nb;
+    k_check_slots<<<(n + 255) / 256, 256, 0, st>>>(idx_a, na, idx_b, nb, n_slots);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || !wait) return e;
+    unsigned long long got[2];
+    e = cudaMemcpyFromSymbolAsync(got, g_slot_check, sizeof got, 0, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return e;
+    *bad_range = got[0] == ~0ull ? -1 : (long long)got[0];
+    *dup_i = got[1] == ~0ull ? -1 : (long long)(got[1] >> 32);
+    *dup_j = got[1] == ~0ull ? -1 : (long long)(got[1] & 0xffffffffull);
+    // the offending value, read back for the message
+    *value = 0;
+    const long long k = *bad_range >= 0 ? *bad_range : *dup_i;
+    if (k >= 0) {
+        const int32_t* src = k < na ? idx_a + k : idx_b + (k - na);
+        e = cudaMemcpyAsync(value, src, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
+    return e;
+}
+
 cudaError_t take_device_status_decode(unsigned* out) { return take_device_status_tu(out); }
 
 cudaError_t launch_commit(const Geom& g, const CommitJob& job, cudaStream_t st) {

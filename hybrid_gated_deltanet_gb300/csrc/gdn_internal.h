@@ -195,6 +195,14 @@ struct AttnPfJob {
 };
 cudaError_t launch_attn_prefill(const AttnPfJob& job, cudaStream_t st);
 
+// GDN_DEBUG: device-side check that the na + nb indices of idx_a then idx_b lie in
+// [0, n_slots) and are distinct.  A violation ORs kDevBadSlot into the device status
+// word.  With wait, the stream is synchronised and the first bad position (or -1)
+// and the first repeated pair (or -1, -1) are returned, with the value found at
+// the first of them.
+cudaError_t check_slots(const int32_t* idx_a, int na, const int32_t* idx_b, int nb, int n_slots, cudaStream_t st,
+                        bool wait, long long* bad_range, long long* dup_i, long long* dup_j, int32_t* value);
+
 // read and clear the device status word of each kernel file (synchronous)
 cudaError_t take_device_status_decode(unsigned* out);
 cudaError_t take_device_status_prefill(unsigned* out);

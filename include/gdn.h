@@ -48,6 +48,16 @@
  *   skipped by the kernels (nothing is read or written for that entry; its y
  *   rows are left as they were).  Duplicate slots within one call race and
  *   give undefined results.
+ * - Debug mode: with the environment variable GDN_DEBUG set (and not "0"),
+ *   gdn_decode_step, gdn_verify_rows(_nosnap), gdn_commit_rows(_recompute) and
+ *   gdn_varlen_prefill(_ckpt) first check their slot indices on the device
+ *   (slot_idx, and snap_idx where the call takes one, together): every index
+ *   in [0, n_slots) and no index twice.  Unless the stream is being captured,
+ *   the call waits for the check and returns GDN_ERR_RANGE naming the first
+ *   offending position and value.  Under stream capture it cannot wait: the
+ *   check then only sets GDN_DEV_BAD_SLOT in the device status.  The check
+ *   never traps.  The pages describe no such mode; it is a debugging aid of
+ *   this library (one extra small launch and a host wait per call).
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -422,9 +432,10 @@ const char* gdn_last_error(void);
  * second); a kernel whose wait gives up skips its remaining work, leaves its
  * outputs incomplete and ORs a code into a status word on the device instead
  * of hanging.  This call reads and clears that word for the current device
- * (*status = 0: nothing reported; bit GDN_DEV_WAIT_TIMEOUT: a wait gave up).
+ * (*status = 0: nothing reported; bit GDN_DEV_WAIT_TIMEOUT: a wait gave up;
+ * bit GDN_DEV_BAD_SLOT: a GDN_DEBUG slot check found a bad or repeated index).
  * It synchronises the current device. */
-enum { GDN_DEV_WAIT_TIMEOUT = 1u };
+enum { GDN_DEV_WAIT_TIMEOUT = 1u, GDN_DEV_BAD_SLOT = 2u };
 gdn_status gdn_device_status(uint32_t* status);
 
 /* Library version string. */
