@@ -15,7 +15,13 @@ write 98,304; x 16,384; z 8,192; a, b 128; y 8,192) and each layer call reads
 65,920 B of parameters.  The chunked prefill (1 sequence, T = 8192, chunk 64)
 is timed too and reported under "prefill" in tokens/s per layer and as a
 fraction of the bf16 tensor peak (5.29 MFLOP per token and layer, counted on
-the chunk form at C = 64).
+the chunk form at C = 64), with its end-to-end figure (inputs copied in from
+pinned host memory, y and the final states copied back).  Two more workloads
+follow: the wide-GVA one (16/48 heads, 10240 conv channels: a 4 x 32768-token
+varlen prefill and verify of r = 4 rows at 4 and 64 slots) under "wide_gva",
+and the serving mix (20 sequences of log-uniform length in [500, 30000] packed
+into one varlen prefill, then decode of 256 random slots of a 1024-slot pool)
+under "serving".
 
 --impl reference times the CPU fp64 oracle (test infrastructure) on a bounded
 sample of the same workload; it is a deliberately slow reported baseline.
@@ -43,6 +49,9 @@ GEOM_ARGS = (16, 32, 128, 128, 4)
 # algorithmic bytes of one decode slot-layer and one layer call's parameters
 SLOT_BYTES = (2 * 32 * 128 * 128 * 4) + (2 * 3 * 8192 * 2) + 8192 * 2 + 32 * 128 * 2 + 2 * 32 * 2 + 32 * 128 * 2
 PARAM_BYTES = 8192 * 4 * 2 + 32 * 4 + 128 * 2
+# algorithmic bytes of one prefill token (x, z, y, a, b) and of one sequence's final state and conv state
+TOKEN_BYTES = 8192 * 2 + 4096 * 2 + 4096 * 2 + 2 * 32 * 2
+STATE_BYTES = 32 * 128 * 128 * 4 + 3 * 8192 * 2
 # algorithmic flops per token and layer of the chunk form at C = 64 (16 k-heads, 32 v-heads, d = 128)
 C_REF = 64
 FLOP_KHEAD = 4 * C_REF * 128                                  # K K^T and Q K^T per k-head
@@ -335,7 +344,7 @@ def time_decode_e2e(torch, cfg, layers, steps, warmup):
     return ev0.elapsed_time(ev1) / 1e3, h2d, d2h
 
 
-def prefill_measure(torch, device, steps, warmup, seed, check=True):
+def prefill_measure(torch, device, steps, warmup, seed, check=True, e2e=True):
     """Chunked prefill of one 8192-token sequence: parity on sampled heads, then timing."""
     import oracle
     from hybrid_gated_deltanet_gb300 import binding as gb
@@ -382,7 +391,52 @@ def prefill_measure(torch, device, steps, warmup, seed, check=True):
         ev1.record(stream)
     ev1.synchronize()
     t = ev0.elapsed_time(ev1) / 1e3 / steps
-    return t, errs
+    e2e_line = prefill_e2e(torch, cfg, prm, (x, z, a, b), s_fin, c_fin, y, ws, steps, warmup) if e2e else None
+    return t, errs, e2e_line
+
+
+def prefill_e2e(torch, cfg, prm, inputs, s_fin, c_fin, y, ws, steps, warmup):
+    """The same prefill through the public API with its inputs copied in from
+    pinned host memory (x, z, a, b packed in one buffer: one copy) and y, the
+    final state and the final conv state copied back, all inside the timed
+    region, one call after another on one stream."""
+    from hybrid_gated_deltanet_gb300 import binding as gb
+    stream = _side_stream(torch)
+    sizes = [t.numel() for t in inputs]
+    dbuf = torch.empty(sum(sizes), dtype=inputs[0].dtype, device=inputs[0].device)
+    views, o = [], 0
+    for t, n_el in zip(inputs, sizes):
+        views.append(dbuf[o:o + n_el].view(t.shape))
+        views[-1].copy_(t)
+        o += n_el
+    hin = dbuf.cpu().pin_memory()
+    outs = (y, s_fin, c_fin)
+    hout = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = hin.numel() * hin.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in hout)
+    x, z, a, b = views
+
+    def step():
+        dbuf.copy_(hin, non_blocking=True)
+        gb.gdn_chunk_prefill(cfg, prm, x, z, a, b, None, None, s_fin, c_fin, y, ws, stream=stream)
+        for ho, t in zip(hout, outs):
+            ho.copy_(t, non_blocking=True)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+    ev1.synchronize()
+    t = ev0.elapsed_time(ev1) / 1e3 / steps
+    return {"value": round(PREFILL_T / t, 1), "unit": "tokens/s/layer", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * t, 4)}
 
 
 # -----------------------------------------------------------------------------
@@ -399,12 +453,12 @@ def _oracle_decode_inputs(n_slots: int, seed: int):
     return geom, p, tok, S, CS
 
 
-def oracle_decode_rate(n_slots: int, min_seconds: float = 0.0, seed: int = 7, inputs=None):
+def oracle_decode_rate(n_slots: int, min_seconds: float = 0.0, seed: int = 7, inputs=None, threads=None):
     """Oracle decode of n_slots slots of one layer (repeated from the same initial
     states until min_seconds have passed): GB/s of the same algorithmic bytes."""
     import oracle
     geom, p, tok, S, CS = inputs or _oracle_decode_inputs(n_slots, seed)
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     kw = dict(conv_w=p["conv_w"].f64, A_log=p["A_log"].f64, norm_w=p["norm_w"].f64, threads=threads)
     done, t0 = 0, time.perf_counter()
     while True:
@@ -442,15 +496,20 @@ def oracle_prefill_rate(T: int, n_heads: int, min_seconds: float = 0.0, seed: in
     return reps * T / (dt * 32 / n_heads), dt, threads
 
 
-def _src_hash(name: str) -> str:
+def _src_hash(names: str) -> str:
+    """First 16 hex digits of the sha256 of the named csrc files, concatenated
+    in the order given (names separated by '+')."""
     import hashlib
-    with open(os.path.join(ROOT, "hybrid_gated_deltanet_gb300", "csrc", name), "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for name in names.split("+"):
+        with open(os.path.join(ROOT, "hybrid_gated_deltanet_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def measured_traffic(kernel: str, source: str):
     """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel's source changed since the counters were taken (hash recorded there)."""
+    kernel's sources changed since the counters were taken (hash recorded there)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -508,7 +567,7 @@ def profile_case(args):
         for nb in (4, 64):
             print(json.dumps(verify_measure(torch, device, args.steps, args.warmup, batch=nb)))
     else:
-        t, _ = prefill_measure(torch, device, args.steps, args.warmup, seed=0, check=False)
+        t, _, _ = prefill_measure(torch, device, args.steps, args.warmup, seed=0, check=False, e2e=False)
         print(json.dumps({"case": args.case, "ms_per_call": round(1e3 * t, 4)}))
     return 0
 
@@ -995,7 +1054,7 @@ def verify_measure(torch, device, steps, warmup, batch=4, r=4):
                                   "snapshot_verify_plus_commit_us": round(1e6 * (t_v + t_c), 2)}}
 
 
-def serving_measure(torch, device, steps, warmup, n_seq=20, pool=512, batch=256):
+def serving_measure(torch, device, steps, warmup, n_seq=20, pool=1024, batch=256):
     """The serving mix: one varlen prefill of n_seq sequences with lengths
     log-uniform in [500, 30000] into a pool of fp32 states, then decode steps of
     `batch` slots drawn at random from the same pool.  Timing only: inputs are
@@ -1113,8 +1172,16 @@ def gpu_arm(args):
                             per_step=step_s)
         torch.cuda.synchronize()
         barrier(world)
-        t_pf, pf_err = prefill_measure(torch, device, pf_steps, max(3, args.warmup // 4), seed=rank,
-                                       check=(rank == 0))
+        t_pf, pf_err, pf_e2e = prefill_measure(torch, device, pf_steps, max(3, args.warmup // 4), seed=rank,
+                                               check=(rank == 0))
+        extra = {}
+        if not args.no_workloads:
+            # the wide-GVA workload (4 x 32768-token prefill, then verify at 4 and 64
+            # slots) and the serving mix (20-sequence prefill, 256-of-1024 decode)
+            wide_pf = wide_prefill_measure(torch, device, pf_steps, 3)
+            wide_v = [verify_measure(torch, device, max(20, args.steps // 8), 3, batch=nb) for nb in (4, 64)]
+            extra["wide_gva"] = {"prefill": wide_pf, "verify": wide_v}
+            extra["serving"] = serving_measure(torch, device, max(3, pf_steps // 2), 3)
     t_dec = max_over_ranks(t_dec, world)
     e2e_t, h2d, d2h = time_decode_e2e(torch, cfg, layers, max(3, args.steps // 4), 3)
     e2e_t = max_over_ranks(e2e_t, world)
@@ -1138,7 +1205,12 @@ def gpu_arm(args):
         pf_cpu = {"value": round(pf_cpu_rate, 3), "unit": "tokens/s/layer", "cores": cpu_thr, "kind": "oracle",
                   "sample": f"{args.cpu_prefill_tokens} tokens x {pf_heads} of 32 v-heads ({pf_cpu_dt:.1f} s), "
                             "scaled to 32 heads"}
+        one_rate, one_dt, _, one_done = oracle_decode_rate(16, min_seconds=args.cpu_seconds / 2, threads=1)
+        cpu_base["single_core"] = {"value": round(one_rate, 4), "unit": "GB/s", "cores": 1,
+                                   "sample": f"{one_done} slot-steps of one layer, one thread ({one_dt:.1f} s)"}
     traffic = measured_traffic("k_decode_persist", "gdn_decode.cu")
+    pf_traffic = measured_traffic("gdn_chunk_prefill", "gdn_chunk16.cu+gdn_prefill.cu")
+    pf_bytes = PREFILL_T * TOKEN_BYTES + STATE_BYTES
     clocks = clk.summary()
     line = {
         "metric": METRIC,
@@ -1158,11 +1230,20 @@ def gpu_arm(args):
                      "traffic": traffic, "call_us": round(launch_s * 1e6, 3),
                      "algorithmic_bytes_per_launch": B * SLOT_BYTES + PARAM_BYTES},
         "prefill": {"workload": "chunked prefill, 1 sequence, T = 8192, 16/32 heads, d = 128, bf16 in, fp32 state, "
-                                "chunk 64 (5 launches: tile prologue, conv state, two prep kernels, chain kernel)",
+                                "chunk 64 (3 launches: k_prep16, k_chain16, k_conv_final)",
                     "tokens_per_s_per_layer": round(PREFILL_T / t_pf, 1), "ms_per_call": round(t_pf * 1e3, 4),
                     "tflops": round(pf_tflops, 3), "flop_per_token": FLOP_PER_TOKEN,
                     "peak_tflops": peaks["bf16_tflops"], "frac_tc": round(pf_tflops / peaks["bf16_tflops"], 4),
-                    "cpu_baseline": pf_cpu},
+                    "roofline": {"bound": "tensor", "kernel": "one gdn_chunk_prefill call (its 3 launches)",
+                                 "achieved": round(pf_tflops, 3), "peak": peaks["bf16_tflops"],
+                                 "peak_src": peaks["src"], "unit": "TFLOP/s",
+                                 "frac": round(pf_tflops / peaks["bf16_tflops"], 4), "traffic": pf_traffic,
+                                 "algorithmic_flops_per_call": FLOP_PER_TOKEN * PREFILL_T,
+                                 "algorithmic_bytes_per_call": pf_bytes,
+                                 "hbm_view": {"achieved": round(pf_bytes / t_pf / 1e9, 1), "unit": "GB/s",
+                                              "frac": round(pf_bytes / t_pf / 1e9 / peaks["hbm_gbs"], 4)}},
+                    "e2e": pf_e2e, "cpu_baseline": pf_cpu},
+        **extra,
         "cpu_baseline": cpu_base,
         "e2e": {"value": round(world * step_bytes * e2e_steps / e2e_t / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -1187,6 +1268,8 @@ def main():
                     help="small cases for ncu captures")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-prefill-tokens", type=int, default=8192)
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="leave out the wide-GVA and serving-mix figures of the full run")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
