@@ -54,10 +54,11 @@
  *   (slot_idx, and snap_idx where the call takes one, together): every index
  *   in [0, n_slots) and no index twice.  Unless the stream is being captured,
  *   the call waits for the check and returns GDN_ERR_RANGE naming the first
- *   offending position and value.  Under stream capture it cannot wait: the
- *   check then only sets GDN_DEV_BAD_SLOT in the device status.  The check
- *   never traps.  The pages describe no such mode; it is a debugging aid of
- *   this library (one extra small launch and a host wait per call).
+ *   offending position and value (the refusal convention above, Strata
+ *   chapter 6, sections 6.2 and 6.5).  Under stream capture it cannot wait:
+ *   the check then only sets GDN_DEV_BAD_SLOT in the device status.  The
+ *   check never traps.  It costs one extra small launch and a host wait per
+ *   call, so it is off by default.
  */
 #ifndef GDN_H_
 #define GDN_H_
