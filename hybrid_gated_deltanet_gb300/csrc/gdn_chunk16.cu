@@ -106,32 +106,161 @@ __device__ __forceinline__ uint4 pack8(const float* v) {
                       tc::pack_h2(v[6], v[7]));
 }
 
-__device__ __forceinline__ void unpack_h8(const uint4& u, float* f) {
-    float2 a = tc::unpack_h2(u.x), b = tc::unpack_h2(u.y), c = tc::unpack_h2(u.z), d = tc::unpack_h2(u.w);
-    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
-}
-
 // ---------------------------------------------------------------------------
 // 1. per-chunk preparation
 // ---------------------------------------------------------------------------
+// Packed fp32 pairs: sm_100's paired FMA / multiply / add (__ffma2_rn and kin)
+// round each lane exactly like the scalar operation, at half the instructions.
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {  // two bf16 (element 0 in the low half)
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ void unpack8x2(const uint4& u, float2 f[4]) {
+    f[0] = bf2_to_f2(u.x);
+    f[1] = bf2_to_f2(u.y);
+    f[2] = bf2_to_f2(u.z);
+    f[3] = bf2_to_f2(u.w);
+}
+
+__device__ __forceinline__ float tanh_hw(float x) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
+    return t;
+}
+
+__device__ __forceinline__ float ex2_hw(float x) {  // 2^x; x <= 0 here
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
+}
+
+// silu of a pair through one hardware tanh each: x sigma(x) = h + h tanh(h), h = x / 2
+__device__ __forceinline__ float2 silu2(float2 x) {
+    const float2 hh = __fmul2_rn(x, make_float2(0.5f, 0.5f));
+    return __ffma2_rn(hh, make_float2(tanh_hw(hh.x), tanh_hw(hh.y)), hh);
+}
+
+__device__ __forceinline__ uint4 pack8x2(const float2 v[4]) {
+    return make_uint4(tc::pack_h2(v[0].x, v[0].y), tc::pack_h2(v[1].x, v[1].y), tc::pack_h2(v[2].x, v[2].y),
+                      tc::pack_h2(v[3].x, v[3].y));
+}
+
+// conv + SiLU of NT tokens for 8 channels held as 4 pairs; rows i .. i+3
+// (row(k) returns packed bf16 row k) are the window of token i.  Window rows that are not taps (d_conv < 4)
+// carry zero weights.  emit(i, u) receives token i's 4 pairs.
+template <int NT, typename Row, typename Emit>
+__device__ __forceinline__ void conv8x2(Row row, const float2 w[4][4], const float2 bias[4], bool raw, Emit emit) {
+    float2 win[4][4];
+#pragma unroll
+    for (int r = 1; r < 4; ++r) unpack8x2(row(r - 1), win[r]);
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+#pragma unroll
+        for (int r = 0; r < 3; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) win[r][c] = win[r + 1][c];
+        unpack8x2(row(i + 3), win[3]);
+        float2 u[4];
+        if (raw) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) u[c] = win[3][c];
+        } else {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float2 s = bias[c];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) s = __ffma2_rn(w[r][c], win[r][c], s);
+                u[c] = silu2(s);
+            }
+        }
+        emit(i, u);
+    }
+}
+
+// window-row weights of 8 channels (as pairs) from the [8][K] bf16 taps at `src`
+// (channel c's tap m at element c K + m; 16-byte aligned): w[4 - K + m] = tap m
+__device__ __forceinline__ void conv_weights8x2(const __nv_bfloat16* src, int K, float2 w[4][4]) {
+    float f[4][8];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) f[r][c] = 0.f;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    auto unpack_taps = [&](auto kk) {
+        constexpr int KK = decltype(kk)::value;
+        float t[8 * KK];
+#pragma unroll
+        for (int v = 0; v < KK; ++v) unpack8(s4[v], t + 8 * v);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+#pragma unroll
+            for (int m = 0; m < KK; ++m) f[4 - KK + m][c] = t[c * KK + m];
+    };
+    if (K == 4) unpack_taps(std::integral_constant<int, 4>{});
+    else if (K == 3) unpack_taps(std::integral_constant<int, 3>{});
+    else unpack_taps(std::integral_constant<int, 2>{});
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) w[r][c] = make_float2(f[r][2 * c], f[r][2 * c + 1]);
+}
+
+__device__ __forceinline__ void bias8x2(const LayerParams& p, int ch, float2 b[4]) {
+    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (p.conv_b) unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.conv_b) + ch), f);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) b[c] = make_float2(f[2 * c], f[2 * c + 1]);
+}
+
+// warp-level fp16 tensor-core pieces of the triangular merges (m16n8k16, fp32
+// accumulation): fragments straight from shared memory
+__device__ __forceinline__ void ldsm_x4(uint32_t r[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(tc::smem_addr(p)));
+}
+
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t r[2], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(tc::smem_addr(p)));
+}
+
+__device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], const uint32_t b[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
 constexpr int P_THREADS = 256;
-constexpr uint32_t P_KQ = 0;                          // [K^; Q^] fp16 [128][128] (atoms of 128 rows)
-constexpr uint32_t P_IP = 32768;                      // [I; P] (A of the T' product), then e^gamma K^
-constexpr uint32_t P_TB = 49152;                      // T' fp16 MN-major [64 (j)][64 (i)]
-constexpr uint32_t P_OUT = 57344;                     // [T'; PT'] tile, then the gates (512 B)
-constexpr uint32_t P_AM = P_OUT + kTP + kGates;       // A fp32 [64][kUtLd]
-constexpr uint32_t P_TM = P_AM + 64 * kUtLd * 4;      // T fp32 [64][kUtLd]
-constexpr uint32_t P_SMALL = P_TM + 64 * kUtLd * 4;   // gamma [64], beta [64], mbarrier, TMEM slot
-constexpr uint32_t P_SMEM = P_SMALL + 2 * C * 4 + 16;
+constexpr int kXRows = C + 3;                              // staged x rows: tokens t0-3 .. t0+63
+constexpr uint32_t kStage = kXRows * 512;                  // q/k rows, or the v rows of 2 v-heads
+constexpr uint32_t kStageV = kXRows * 256;                 // the v rows of one v-head
+constexpr uint32_t P_KQ = 0;                               // [K^; Q^] fp16 [128][128], atoms of 128 rows
+constexpr uint32_t P_STG = 32768;                          // staged raw x rows
+constexpr uint32_t P_SCR = (P_STG + kStage + 1023) & ~1023u;  // scratch of one v-head:
+constexpr uint32_t P_IP = P_SCR;                           //   [I; P] fp16 K-major [128][64]
+constexpr uint32_t P_TB = P_IP + 16384;                    //   T' fp16 MN-major [64 (k)][64]
+constexpr int kA16Ld = 72;                                 //   (halves)
+constexpr uint32_t P_A16 = P_TB + 8192;                    //   A fp16 [64][72] (its blocks below the diagonal)
+constexpr int kA32Ld = 17;                                 //   (floats)
+constexpr uint32_t P_A32 = P_A16 + 64 * kA16Ld * 2;        //   A's diagonal 16 x 16 blocks fp32 [4][16][17]
+constexpr int kX16Ld = 24;                                 //   (halves)
+constexpr uint32_t P_X16 = P_A32 + 4 * 16 * kA32Ld * 4;    //   (I + A)^-1's diagonal blocks fp16 [4][16][24]
+constexpr uint32_t P_Y = P_X16 + 4 * 16 * kX16Ld * 2;      //   a 16 x 8 fp16 tile per warp
+constexpr uint32_t P_WA = P_SCR;                           //   later [-T'e, 0; -PT'e, diag(e^gamma)] [128][128]
+constexpr uint32_t P_WV = P_Y + 8 * 256;                   // conv taps of the 2 staged v-heads (2 x 1 KB)
+constexpr uint32_t P_SMALL = P_WV + 2048;                  // gamma log2(e), beta, e^gamma, e^(gamma_C - gamma)
+constexpr uint32_t P_SMEM = P_SMALL + 4 * C * 4 + 16;      //   [64] each; mbarrier; TMEM slot
 constexpr uint32_t P_SMEM_ALLOC = P_SMEM + 1024;
-constexpr uint32_t P_TMEM_COLS = 256;                 // Gram (64) | [T'; PT'] (64) | [W; PW] (128)
-// staging of raw x rows (token t0-3+r in row r), requested before any arithmetic:
-// the k-head's q and k channels over [I; P] .. the gates (67 rows of 512 B), and the
-// channels of 2 v-heads over A and T (67 rows of 256 B each)
-constexpr uint32_t P_XQK = P_IP, P_XV = P_AM;
-constexpr int kXRows = C + 3;
-static_assert(P_XQK + kXRows * 512 <= P_AM, "q/k staging");
-static_assert(P_XV + 2 * kXRows * 256 <= P_SMALL, "v staging");
+constexpr uint32_t P_TMEM_COLS = 256;                      // Gram (64) | [T'; PT'] (64) | [-W; Q'] (128)
+static_assert(P_WA + 32768 <= P_WV, "WA overlay");
+static_assert((P_IP & 1023) == 0 && (P_TB & 1023) == 0 && (P_A16 & 15) == 0 && (P_X16 & 15) == 0 &&
+                  (P_Y & 15) == 0 && (P_WV & 15) == 0,
+              "operand alignment");
+static_assert(2 * (P_SMEM_ALLOC + 1024) <= 233472, "two CTAs per SM");
 
 __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__ Args A) {
     using L = Act<__nv_bfloat16>;
@@ -149,63 +278,87 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
-    unsigned char *sKQ = sm + P_KQ, *sIP = sm + P_IP, *sTB = sm + P_TB, *sOUT = sm + P_OUT;
-    unsigned char *sXQK = sm + P_XQK, *sXV = sm + P_XV;
-    float* eg = reinterpret_cast<float*>(sOUT + kTP);  // the record's gate block
+    unsigned char *sKQ = sm + P_KQ, *sSTG = sm + P_STG, *sIP = sm + P_IP, *sTB = sm + P_TB, *sWA = sm + P_WA;
+    unsigned char *sA16 = sm + P_A16, *sX16 = sm + P_X16, *sY = sm + P_Y, *sWV = sm + P_WV;
+    float* A32 = reinterpret_cast<float*>(sm + P_A32);
+    float* gam2 = reinterpret_cast<float*>(sm + P_SMALL);
+    float* bet = gam2 + C;
+    float* eg = bet + C;
     float* erev = eg + C;
-    float* Am = reinterpret_cast<float*>(sm + P_AM);
-    float* Tm = reinterpret_cast<float*>(sm + P_TM);
-    float* gam = reinterpret_cast<float*>(sm + P_SMALL);
-    float* bet = gam + C;
-    uint64_t* mbar = reinterpret_cast<uint64_t*>(bet + C);
+    uint64_t* mbar = reinterpret_cast<uint64_t*>(erev + C);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(mbar + 1);
     const bool raw = g.flags & kFlagRawQKV;
     const bool direct = g.flags & kFlagGatesDirect;
     int slot_ok;
     const __nv_bfloat16* cin = static_cast<const __nv_bfloat16*>(seq_conv_in(J, g, sq, slot_ok));
     const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(J.x);
+    const __nv_bfloat16* cw = static_cast<const __nv_bfloat16*>(A.p.conv_w);
 
-    // stage x rows t0-3 .. t0+63 of 16 channel groups of 8 (one v-head's 128 channels,
-    // from channel ch0) into rows of 256 bytes: rows before the sequence come from its
-    // conv state (or are zero), rows past its end are not read
-    auto stage_v = [&](unsigned char* dst, int ch0) {
-        for (int f = tid; f < kXRows * 16; f += P_THREADS) {
-            const int r = f >> 4, c16i = f & 15;
+    // stage x rows tau = t0-3+r (r < kXRows), 32 chunks of 16 bytes per row: chunk ci
+    // of row r goes to dst(r, ci) from channel ch(ci) (negative: not staged).  Rows
+    // before the sequence come from its conv state (or are zero), rows past its end
+    // are zero.
+    auto stage_rows = [&](auto dst, int ch) {
+        const int ci = tid & 31;
+        if (ch < 0) return;
+        for (int r = tid >> 5; r < kXRows; r += P_THREADS / 32) {
             const int64_t tau = t0 - 3 + r;
-            unsigned char* d = dst + r * 256 + c16i * 16;
-            const int ch = ch0 + c16i * 8;
-            if (tau >= start && tau < end) {
-                cp_async16(d, x + (size_t)tau * Cch + ch);
-            } else if (tau < start && cin && tau - start >= -(K - 1)) {
+            unsigned char* d = dst(r, ci);
+            if (tau >= start && tau < end) cp_async16(d, x + (size_t)tau * Cch + ch);
+            else if (tau < start && cin && tau - start >= -(K - 1))
                 cp_async16(d, cin + (size_t)((K - 1) + (tau - start)) * Cch + ch);
-            } else {
-                *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
-            }
+            else *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
         }
     };
-    // the q/k rows: channel group c16i < 16 is q, >= 16 is k (contiguous in shared memory)
-    for (int f = tid; f < kXRows * 32; f += P_THREADS) {
-        const int r = f >> 5, c16i = f & 31;
-        const int64_t tau = t0 - 3 + r;
-        unsigned char* d = sXQK + r * 512 + c16i * 16;
-        const int ch = (c16i < 16 ? h : Hk + h) * D + (c16i & 15) * 8;
-        if (tau >= start && tau < end) cp_async16(d, x + (size_t)tau * Cch + ch);
-        else if (tau < start && cin && tau - start >= -(K - 1))
-            cp_async16(d, cin + (size_t)((K - 1) + (tau - start)) * Cch + ch);
-        else *reinterpret_cast<uint4*>(d) = make_uint4(0, 0, 0, 0);
-    }
-    // the v rows of the first (up to) 2 v-heads
-    for (int u = 0; u < 2 && u < G; ++u) stage_v(sXV + u * kXRows * 256, 2 * Hk * D + (h * G + u) * D);
-    cp_async_commit();
+    // the v rows and conv taps of v-heads 2p and 2p + 1 of the group
+    auto stage_pair = [&](int p) {
+        const int u = (tid & 31) >> 4;
+        const int jh = h * G + 2 * p + u;
+        const bool live = 2 * p + u < G;
+        stage_rows([&](int r, int ci) { return sSTG + (ci >> 4) * kStageV + r * 256 + (ci & 15) * 16; },
+                   live ? 2 * Hk * D + jh * D + (tid & 15) * 8 : -1);
+        if (!raw && tid < 2 * 16 * K) {  // 128 channels x K taps of each v-head: 16 K chunks of 16 bytes
+            const int uu = tid / (16 * K), f = tid % (16 * K);
+            if (2 * p + uu < G)
+                cp_async16(sWV + uu * 1024 + f * 16, cw + (size_t)(2 * Hk * D + (h * G + 2 * p + uu) * D) * K + f * 8);
+        }
+        cp_async_commit();
+    };
 
+    // ---- prologue: stage the k-head's q and k rows (chunks 0..15 q, 16..31 k) -------------
+    stage_rows([&](int r, int ci) { return sSTG + r * 512 + ci * 16; },
+               ((tid & 31) < 16 ? h : Hk + h) * D + (tid & 15) * 8);
+    cp_async_commit();
     if (warp == 0) tc::alloc(tslot, P_TMEM_COLS);
     if (tid == 0) {
         mbar_init(mbar, 1);
         fence_mbar_init();
     }
+    // gate inputs of tokens lane and lane + 32 of the first v-head (warp 0)
+    float ga[2] = {0.f, 0.f}, gb[2] = {0.f, 0.f};
+    auto load_gates = [&](int j) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int t = lane + 32 * e;
+            if (t < n) {
+                const size_t tok = (size_t)(t0 + t);
+                ga[e] = L::ld(J.a, tok * Hv + j);
+                gb[e] = L::ld(J.b, tok * Hv + j);
+            }
+        }
+    };
+    if (warp == 0) load_gates(h * G);
     const int ch_qk = (lane < 16 ? h : Hk + h) * D + (lane & 15) * 8;
-    float wqk[4][8], bqk[8];
-    conv_weights8(A.p, K, raw, ch_qk, wqk, bqk);
+    float2 wqk[4][4], bqk[4];
+    if (raw) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) wqk[r][c] = make_float2(0.f, 0.f);
+    } else {
+        conv_weights8x2(cw + (size_t)ch_qk * K, K, wqk);
+    }
+    bias8x2(A.p, ch_qk, bqk);
     cp_async_wait_all();
     tc::fence_before();
     __syncthreads();
@@ -218,31 +371,33 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
         const bool is_q = lane < 16;
         const int d0 = (lane & 15) * 8;
         const int tt0 = warp * 8;
-        uint4 rows[11];
-#pragma unroll
-        for (int k = 0; k < 11; ++k) rows[k] = *reinterpret_cast<const uint4*>(sXQK + (tt0 + k) * 512 + lane * 16);
+        const unsigned char* xr = sSTG + tt0 * 512 + lane * 16;
         unsigned char* atom = sKQ + (d0 >> 6) * 16384;
         const int cc = (d0 & 63) >> 3;
         const float qs = is_q ? g.q_scale : 1.f;
         const bool l2 = !(g.flags & kFlagNoL2);
-        conv_tokens<8>(rows, wqk, bqk, K, raw, [&](int i, float u[8]) {
+        conv8x2<8>([&](int k) { return *reinterpret_cast<const uint4*>(xr + k * 512); }, wqk, bqk, raw,
+                   [&](int i, float2 u[4]) {
             const int t = tt0 + i;
-            float ss = 0.f;
+            float2 s2 = __fmul2_rn(u[0], u[0]);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) ss = fmaf(u[c], u[c], ss);
+            for (int c = 1; c < 4; ++c) s2 = __ffma2_rn(u[c], u[c], s2);
+            float ss = s2.x + s2.y;
 #pragma unroll
             for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            const float scale = l2 ? qs * rsqrtf(ss + g.l2_eps) : qs;
-            float v[8];
+            float scale = l2 ? qs * rsqrtf(ss + g.l2_eps) : qs;
+            if (t >= n) scale = 0.f;  // zero past the sequence end
+            float2 v[4];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) v[c] = t < n ? u[c] * scale : 0.f;  // zero past the sequence end
-            *reinterpret_cast<uint4*>(atom + tc::h_off(is_q ? C + t : t, cc)) = pack8(v);
+            for (int c = 0; c < 4; ++c) v[c] = __fmul2_rn(u[c], make_float2(scale, scale));
+            *reinterpret_cast<uint4*>(atom + tc::h_off(is_q ? C + t : t, cc)) = pack8x2(v);
         });
     }
     fence_proxy_async_smem();
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
+    stage_pair(0);  // over the q/k rows, which are consumed
     if (tid == 0) {
         // K^ for the chain: the first 64 rows of each atom
         unsigned char* dst = A.kk + ((size_t)cs * Hk + h) * kK;
@@ -270,129 +425,222 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
         tc::fence_after();
     };
 
+    // V = silu(conv(x)) of v-head slot u (0, 1) of the staged pair, head j: thread = 8
+    // channels x 4 tokens, straight to the record (MN-major [64 tokens][128] fp16)
+    auto v_conv = [&](int u, int j) {
+        const int cgp = tid & 15, tg = tid >> 4;
+        float2 w[4][4], bias[4];
+        if (raw) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) w[r][c] = make_float2(0.f, 0.f);
+        } else {
+            conv_weights8x2(reinterpret_cast<const __nv_bfloat16*>(sWV + u * 1024) + cgp * 8 * K, K, w);
+        }
+        bias8x2(A.p, 2 * Hk * D + j * D + cgp * 8, bias);
+        const unsigned char* xv = sSTG + u * kStageV;
+        const unsigned char* xr = xv + 4 * tg * 256 + cgp * 16;
+        unsigned char* vat = A.rec + ((size_t)cs * Hv + j) * kRec + kRecV + (cgp >> 3) * 8192;
+        conv8x2<4>([&](int k) { return *reinterpret_cast<const uint4*>(xr + k * 256); }, w, bias, raw,
+                   [&](int i, float2 uu[4]) {
+            const int t = 4 * tg + i;
+            if (t >= n) {  // zero past the sequence end
+#pragma unroll
+                for (int c = 0; c < 4; ++c) uu[c] = make_float2(0.f, 0.f);
+            }
+            *reinterpret_cast<uint4*>(vat + tc::h_off(t, cgp & 7)) = pack8x2(uu);
+        });
+    };
+
     for (int jj = 0; jj < G; ++jj) {
         const int j = h * G + jj;
         unsigned char* rec = A.rec + ((size_t)cs * Hv + j) * kRec;
-        if (jj >= 2 && jj % 2 == 0) {  // the v rows of the next 2 v-heads (A and T are free again)
-            for (int u = 0; u < 2 && jj + u < G; ++u) stage_v(sXV + u * kXRows * 256, 2 * Hk * D + (j + u) * D);
-            cp_async_commit();
-            cp_async_wait_all();
-            __syncthreads();
-        }
-        // gate inputs of token t = tid, requested before the V conv
-        float ga = 0.f, gb = 0.f;
-        if (tid < n) {
-            const size_t tok = (size_t)(t0 + tid);
-            ga = L::ld(J.a, tok * Hv + j);
-            gb = L::ld(J.b, tok * Hv + j);
-        }
-        // V = silu(conv(x)) of the group's 2 v-heads from the staged rows (thread = 8
-        // channels x 4 tokens), straight to the records (MN-major [64 tokens][128] fp16),
-        // before A and T overwrite the staging
-        if (jj % 2 == 0) {
-            const int cgp = tid & 15, tg = tid >> 4;
-            for (int u = 0; u < 2 && jj + u < G; ++u) {
-                float w[4][8], bias[8];
-                conv_weights8(A.p, K, raw, 2 * Hk * D + (j + u) * D + cgp * 8, w, bias);
-                const unsigned char* xv = sXV + u * kXRows * 256;
-                uint4 rows[7];
+        // ---- gates (warp 0): g, beta of tokens lane, lane + 32; gamma = cumsum(g) ----------
+        if (warp == 0) {
+            const float alog = direct ? 0.f : A.p.A_log[j];
+            const float dtb = (!direct && A.p.dt_bias) ? A.p.dt_bias[j] : 0.f;
+            float gl[2], be[2];
 #pragma unroll
-                for (int k = 0; k < 7; ++k) rows[k] = *reinterpret_cast<const uint4*>(xv + (4 * tg + k) * 256 + cgp * 16);
-                unsigned char* vat = A.rec + ((size_t)cs * Hv + j + u) * kRec + kRecV + (cgp >> 3) * 8192;
-                conv_tokens<4>(rows, w, bias, K, raw, [&](int i, float uu[8]) {
-                    const int t = 4 * tg + i;
-                    float v[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = t < n ? uu[e] : 0.f;  // zero past the sequence end
-                    *reinterpret_cast<uint4*>(vat + tc::h_off(t, cgp & 7)) = pack8(v);
-                });
+            for (int e = 0; e < 2; ++e) {
+                gl[e] = 0.f;
+                be[e] = 0.f;
+                if (lane + 32 * e < n) gates(ga[e], gb[e], alog, dtb, direct, gl[e], be[e]);
             }
-        }
-        if (jj == 0) {
-            wait_mma();  // the Gram
-        } else {
-            if (tid == 0) bulk_wait_read_all();  // the previous [T'; PT'] store has read sOUT
-            __syncthreads();
-        }
-        if (tid < C) {  // gates of token t = tid (zero past the sequence end)
-            float gl = 0.f, be = 0.f;
-            if (tid < n)
-                gates(ga, gb, direct ? 0.f : A.p.A_log[j], (!direct && A.p.dt_bias) ? A.p.dt_bias[j] : 0.f, direct,
-                      gl, be);
-            gam[tid] = gl;
-            bet[tid] = be;
-        }
-        // identity rows of [I; P] (the region held e^gamma K^ or the q/k rows before)
-        for (int f = tid; f < C * 8; f += P_THREADS) {
-            const int r = f >> 3, cc = f & 7;
-            uint32_t wd[4] = {0u, 0u, 0u, 0u};
-            if ((r >> 3) == cc) wd[(r & 7) >> 1] = (r & 1) ? 0x3C000000u : 0x00003C00u;  // fp16 1.0 at column r
-            *reinterpret_cast<uint4*>(sIP + tc::h_off(r, cc)) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-        }
-        __syncthreads();
-        if (warp == 0) {  // gamma = cumsum(g), e^gamma, e^(gamma_C - gamma)
+            if (jj + 1 < G) load_gates(j + 1);  // the next v-head's inputs, in flight meanwhile
             float run = 0.f;
-            for (int base = 0; base < C; base += 32) {
-                float v = gam[base + lane];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float v = gl[e];
 #pragma unroll
                 for (int off = 1; off < 32; off <<= 1) {
                     const float o = __shfl_up_sync(0xffffffffu, v, off);
                     if (lane >= off) v += o;
                 }
-                v += run;
-                gam[base + lane] = v;
-                eg[base + lane] = expf(v);
-                run = __shfl_sync(0xffffffffu, v, 31);
+                gl[e] = v + run;
+                run = __shfl_sync(0xffffffffu, gl[e], 31);
             }
-            __syncwarp();
-            for (int t = lane; t < C; t += 32) erev[t] = expf(gam[C - 1] - gam[t]);
+            const float gC = run;
+            float* rg = reinterpret_cast<float*>(rec + kRecG);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int t = lane + 32 * e;
+                const float ev = expf(gl[e]), er = expf(gC - gl[e]);
+                gam2[t] = gl[e] * 1.4426950408889634f;
+                bet[t] = be[e];
+                eg[t] = ev;
+                erev[t] = er;
+                rg[t] = ev;
+                rg[C + t] = er;
+            }
         }
-        __syncthreads();
-        // decay masks from the Gram: A (strictly lower, beta_t) from the K^K^T rows
-        // (lanes 0..63), P (lower incl.) from the Q^K^T rows (lanes 64..127)
+        if (jj == 0) wait_mma();  // the Gram (ends with a CTA barrier)
+        else __syncthreads();
+        // ---- masks from the Gram: A = strict-lower(beta_t Gamma o K^K^T) (TMEM lanes 0..63),
+        // P = lower-incl(Gamma o Q^K^T) (lanes 64..127); Gamma_ti = 2^(gamma2_t - gamma2_i) ------
+        for (int f = tid; f < C * 8; f += P_THREADS) {  // identity rows of [I; P]
+            const int r = f >> 3, cc = f & 7;
+            // fp16 1.0 at column r: word (r & 7) / 2 of chunk r / 8, high half for odd r
+            const uint32_t one = (r >> 3) == cc ? ((r & 1) ? 0x3C000000u : 0x00003C00u) : 0u;
+            const int wsel = (r & 7) >> 1;
+            *reinterpret_cast<uint4*>(sIP + tc::h_off(r, cc)) =
+                make_uint4(wsel == 0 ? one : 0u, wsel == 1 ? one : 0u, wsel == 2 ? one : 0u, wsel == 3 ? one : 0u);
+        }
         {
-            const int t = 32 * (q4 & 1) + lane;
-            const float gt = gam[t], bt = bet[t];
-            float v[32];
-            tc::ld32(tc::taddr(tm, 32 * q4, hf * 32), v);
-            if (q4 < 2) {
+            const bool isA = q4 < 2;
+            const int rb = q4 & 1;             // row half: rows 32 rb .. 32 rb + 31
+            const int t = 32 * rb + lane;
+            if (hf > rb) {                     // above the diagonal: A unused, P zero
+                if (!isA) {
 #pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    float o4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = hf * 32 + c + e;
-                        o4[e] = i < t ? bt * __expf(gt - gam[i]) * v[c + e] : 0.f;  // exponent <= 0 only
-                    }
-                    *reinterpret_cast<float4*>(Am + t * kUtLd + hf * 32 + c) = make_float4(o4[0], o4[1], o4[2], o4[3]);
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4*>(sIP + tc::h_off(C + t, 4 * hf + k)) = make_uint4(0, 0, 0, 0);
                 }
             } else {
+                float v[32];
+                tc::ld32(tc::taddr(tm, 32 * q4, 32 * hf), v);
+                const float gt = gam2[t];
+                const float bt = isA ? bet[t] : 1.f;
+                const bool diag = hf == rb;
+                const float2* g2 = reinterpret_cast<const float2*>(gam2 + 32 * hf);
+                const int tb = t >> 4;
+                // one 16-column block at a time: 8 pairs
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float p8[8];
+                for (int bq = 0; bq < 2; ++bq) {
+                    const int cb = 2 * hf + bq;
+                    if (isA && cb > tb) continue;  // above the diagonal: unused
+                    float2 m[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int i = hf * 32 + 8 * k + e;
-                        p8[e] = i <= t ? __expf(gt - gam[i]) * v[8 * k + e] : 0.f;
+                    for (int c = 0; c < 8; ++c) {
+                        const int cp = 8 * bq + c;
+                        const float2 d = __ffma2_rn(g2[cp], make_float2(-1.f, -1.f), make_float2(gt, gt));
+                        const float2 e = make_float2(ex2_hw(fminf(d.x, 0.f)), ex2_hw(fminf(d.y, 0.f)));
+                        m[c] = __fmul2_rn(__fmul2_rn(e, make_float2(v[2 * cp], v[2 * cp + 1])), make_float2(bt, bt));
+                        if (diag) {  // strictly below (A) or on / below (P) the diagonal
+                            const int i0 = 32 * hf + 2 * cp;
+                            if (isA ? i0 >= t : i0 > t) m[c].x = 0.f;
+                            if (isA ? i0 + 1 >= t : i0 + 1 > t) m[c].y = 0.f;
+                        }
                     }
-                    *reinterpret_cast<uint4*>(sIP + tc::h_off(C + t, hf * 4 + k)) = pack8(p8);
+                    if (!isA) {
+                        *reinterpret_cast<uint4*>(sIP + tc::h_off(C + t, 4 * hf + 2 * bq)) = pack8x2(m);
+                        *reinterpret_cast<uint4*>(sIP + tc::h_off(C + t, 4 * hf + 2 * bq + 1)) = pack8x2(m + 4);
+                    } else if (cb < tb) {  // below the diagonal -> fp16 A16
+                        uint4* dst = reinterpret_cast<uint4*>(sA16 + (t * kA16Ld + 16 * cb) * 2);
+                        dst[0] = pack8x2(m);
+                        dst[1] = pack8x2(m + 4);
+                    } else {  // the diagonal block -> fp32 A32
+                        float* dst = A32 + (tb * 16 + (t & 15)) * kA32Ld;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            dst[2 * c] = m[c].x;
+                            dst[2 * c + 1] = m[c].y;
+                        }
+                    }
                 }
             }
         }
         __syncthreads();
-        ut_inverse64(Am, Tm, tid, P_THREADS);
-        // T' = T diag(beta) as the B operand of [I; P] T': MN-major, row j holds T'[j][0..63]
-        for (int f = tid; f < C * 8; f += P_THREADS) {
-            const int r = f >> 3, cc = f & 7;
-            float v[8];
+        // ---- T' = (I + A)^-1 diag(beta) -> sTB (MN-major: row k holds T'[k][0..63]) --------
+        // diagonal 16 x 16 blocks by register-resident substitution (fp32): lane = column
+        // jc of block b; once x_k is final, every later row takes -A_ik x_k.  The blocks
+        // above the diagonal are zero.
+        if (warp < 2) {
+            const int b = 2 * warp + (lane >> 4), jc = lane & 15, lb = lane & 16;
+            const float* ab = A32 + b * 16 * kA32Ld;
+            float acol[16], xv[16];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = Tm[r * kUtLd + cc * 8 + e] * bet[cc * 8 + e];
-            *reinterpret_cast<uint4*>(sTB + tc::h_off(r, cc)) = pack8(v);
+            for (int i = 0; i < 16; ++i) {
+                acol[i] = ab[i * kA32Ld + jc];
+                xv[i] = i == jc ? 1.f : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < 15; ++k) {
+#pragma unroll
+                for (int i = k + 1; i < 16; ++i) xv[i] = fmaf(-__shfl_sync(0xffffffffu, acol[i], lb + k), xv[k], xv[i]);
+            }
+            const float bj = bet[16 * b + jc];
+            __half* xd = reinterpret_cast<__half*>(sX16) + b * 16 * kX16Ld + jc;
+            const int col = 16 * b + jc;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                xd[i * kX16Ld] = __float2half_rn(xv[i]);
+                *reinterpret_cast<__half*>(sTB + tc::h_off(16 * b + i, col >> 3) + (col & 7) * 2) =
+                    __float2half_rn(xv[i] * bj);
+            }
+        } else {
+            // zeros above the diagonal blocks: row r, 16-byte chunk cc with cc / 2 > r / 16
+            const int f = tid - 64;
+            int r, cc;
+            if (f < 96) {
+                r = f / 6;
+                cc = 2 + f % 6;
+            } else if (f < 160) {
+                r = 16 + (f - 96) / 4;
+                cc = 4 + (f - 96) % 4;
+            } else {
+                r = 32 + (f - 160) / 2;
+                cc = 6 + (f - 160) % 2;
+            }
+            *reinterpret_cast<uint4*>(sTB + tc::h_off(r, cc)) = make_uint4(0, 0, 0, 0);
+        }
+        __syncthreads();
+        // the blocks below the diagonal, row block a = 1..3 after the rows above it:
+        // T'_ab = -X_aa sum_{c=b}^{a-1} A_ac T'_cb, one 16 x 8 tile (b, column half nh)
+        // per warp, fp16 operands with fp32 accumulation
+#pragma unroll 1
+        for (int a = 1; a < 4; ++a) {
+            if (warp < 2 * a) {
+                const int b = warp >> 1, nh = warp & 1;
+                const int gq = lane >> 2, t4 = lane & 3;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int c = b; c < a; ++c) {
+                    uint32_t af[4], bfr[2];
+                    ldsm_x4(af, sA16 + ((16 * a + (lane & 15)) * kA16Ld + 16 * c + (lane >> 4) * 8) * 2);
+                    ldsm_x2_trans(bfr, sTB + tc::h_off(16 * c + (lane & 15), 2 * b + nh));
+                    mma16816(acc, af, bfr);
+                }
+                uint32_t* yw = reinterpret_cast<uint32_t*>(sY + warp * 256);
+                yw[gq * 4 + t4] = tc::pack_h2(acc[0], acc[1]);
+                yw[(gq + 8) * 4 + t4] = tc::pack_h2(acc[2], acc[3]);
+                __syncwarp();
+                uint32_t xf[4], yf[2];
+                ldsm_x4(xf, sX16 + ((a * 16 + (lane & 15)) * kX16Ld + (lane >> 4) * 8) * 2);
+                ldsm_x2_trans(yf, sY + warp * 256 + (lane & 15) * 16);
+                float o[4] = {0.f, 0.f, 0.f, 0.f};
+                mma16816(o, xf, yf);
+                *reinterpret_cast<uint32_t*>(sTB + tc::h_off(16 * a + gq, 2 * b + nh) + 4 * t4) =
+                    tc::pack_h2(-o[0], -o[1]);
+                *reinterpret_cast<uint32_t*>(sTB + tc::h_off(16 * a + gq + 8, 2 * b + nh) + 4 * t4) =
+                    tc::pack_h2(-o[2], -o[3]);
+                __syncwarp();  // the scratch tile is rewritten at the next row block
+            }
+            __syncthreads();
         }
         fence_proxy_async_smem();
         tc::fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0) {  // [T'; PT'] = [I; P] T' (M = 128, N = 64, K = 64)
             tc::fence_after();
             if (ok) {
                 const uint32_t a0 = tc::smem_addr(sIP), b0 = tc::smem_addr(sTB);
@@ -403,63 +651,80 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
             }
             tc::commit(mbar);
         }
+        // V of this v-head while the product runs (the pair's rows were staged earlier)
+        if ((jj & 1) == 0) {
+            cp_async_wait_all();
+            __syncthreads();
+            v_conv(0, j);
+        }
         wait_mma();
-        {  // [T'; PT'] -> the record tile, K-major [128][64]
+        {  // [T'; PT'] -> the record tile (K-major [128][64]); -[T'; PT'] diag(e^gamma) -> WA
             const int r = 32 * q4 + lane;
             float v[32];
             tc::ld32(tc::taddr(tm, 32 * q4, 64 + hf * 32), v);
+            unsigned char* rtp = rec + kRecTP;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(sOUT + tc::h_off(r, hf * 4 + k)) = pack8(v + 8 * k);
-        }
-        // e^gamma K^ -> B operand of [W; PW] (MN-major [64 tokens][128 d_k], over [I; P])
-        for (int f = tid; f < C * 16; f += P_THREADS) {
-            const int t = f >> 4, a = (f >> 3) & 1, cc = f & 7;
-            float v[8];
-            unpack_h8(*reinterpret_cast<const uint4*>(sKQ + a * 16384 + tc::h_off(t, cc)), v);
-            const float e = eg[t];
+            for (int k = 0; k < 4; ++k) {
+                const int cc = 4 * hf + k;
+                float2 p2[4], s2[4];
+                const float4 e0 = *reinterpret_cast<const float4*>(eg + 8 * cc);
+                const float4 e1 = *reinterpret_cast<const float4*>(eg + 8 * cc + 4);
+                const float2 en[4] = {make_float2(-e0.x, -e0.y), make_float2(-e0.z, -e0.w), make_float2(-e1.x, -e1.y),
+                                      make_float2(-e1.z, -e1.w)};
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] *= e;
-            *reinterpret_cast<uint4*>(sIP + a * 8192 + tc::h_off(t, cc)) = pack8(v);
+                for (int c = 0; c < 4; ++c) {
+                    p2[c] = make_float2(v[8 * k + 2 * c], v[8 * k + 2 * c + 1]);
+                    s2[c] = __fmul2_rn(p2[c], en[c]);
+                }
+                *reinterpret_cast<uint4*>(rtp + tc::h_off(r, cc)) = pack8x2(p2);
+                *reinterpret_cast<uint4*>(sWA + tc::h_off(r, cc)) = pack8x2(s2);
+                // the second atom (columns 64..127): zero, with e^gamma_t at column t of row 64 + t
+                uint32_t dw = 0u;
+                if (r >= C && ((r - C) >> 3) == cc) {
+                    const uint32_t hb = __half_as_ushort(__float2half_rn(eg[r - C]));
+                    dw = ((r - C) & 1) ? (hb << 16) : hb;
+                }
+                const int wsel = ((r - C) & 7) >> 1;
+                *reinterpret_cast<uint4*>(sWA + 16384 + tc::h_off(r, cc)) =
+                    make_uint4(wsel == 0 ? dw : 0u, wsel == 1 ? dw : 0u, wsel == 2 ? dw : 0u, wsel == 3 ? dw : 0u);
+            }
         }
         fence_proxy_async_smem();
         tc::fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == 0) {  // [-W; Q'] = WA [K^; Q^] (M = 128, N = 128, K = 128)
             tc::fence_after();
-            bulk_s2g(rec + kRecTP, sOUT, kTP);  // [T'; PT'] and the gates
-            bulk_s2g(rec + kRecG, sOUT + kTP, kGates);
-            bulk_commit();
-            if (ok) {  // [W; PW] = [T'; PT'] (e^gamma K^) (M = 128, N = 128, K = 64)
-                const uint32_t a0 = tc::smem_addr(sOUT), b0 = tc::smem_addr(sIP);
-                for (int s = 0; s < C / 16; ++s)
-                    tc::mma_f16(tm + 128, tc::sdesc_lbo(a0 + (uint32_t)(s * 32), 16),
-                                tc::sdesc_lbo(b0 + (uint32_t)(s * 2048), 8192), tc::idesc_f16(128, 128, false, true),
-                                s > 0 ? 1u : 0u);
+            if (ok) {
+                const uint32_t a0 = tc::smem_addr(sWA), b0 = tc::smem_addr(sKQ);
+                for (int s = 0; s < 2 * C / 16; ++s)
+                    tc::mma_f16(tm + 128, tc::sdesc_lbo(a0 + (uint32_t)((s >> 2) * 16384 + (s & 3) * 32), 16),
+                                tc::sdesc_lbo(b0 + (uint32_t)(s * 2048), 16384),
+                                tc::idesc_f16(128, 128, false, true), s > 0 ? 1u : 0u);
             }
             tc::commit(mbar);
+        }
+        // the pair's second V while this product runs; then the next pair's rows
+        if ((jj & 1) == 0) {
+            if (jj + 1 < G) v_conv(1, j + 1);
+            if (jj + 2 < G) {
+                __syncthreads();  // every thread is done with the staged rows
+                stage_pair(jj / 2 + 1);
+            }
         }
         wait_mma();
         {  // [-W; Q'] -> the record (K-major [128][128], atoms of 128 rows), from registers
             const int r = 32 * q4 + lane;
-            const float e = r < C ? 0.f : eg[r - C];
             unsigned char* aop = rec + hf * 16384;
-#pragma unroll 1
+#pragma unroll
             for (int b = 0; b < 2; ++b) {
                 float v[32];
                 tc::ld32(tc::taddr(tm, 32 * q4, 128 + hf * 64 + 32 * b), v);
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const int cc = 4 * b + k;
-                    if (r < C) {
+                    float2 p2[4];
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) v[8 * k + i] = -v[8 * k + i];
-                    } else {
-                        float qv[8];
-                        unpack_h8(*reinterpret_cast<const uint4*>(sKQ + hf * 16384 + tc::h_off(r, cc)), qv);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) v[8 * k + i] = fmaf(e, qv[i], -v[8 * k + i]);
-                    }
-                    *reinterpret_cast<uint4*>(aop + tc::h_off(r, cc)) = pack8(v + 8 * k);
+                    for (int c = 0; c < 4; ++c) p2[c] = make_float2(v[8 * k + 2 * c], v[8 * k + 2 * c + 1]);
+                    *reinterpret_cast<uint4*>(aop + tc::h_off(r, 4 * b + k)) = pack8x2(p2);
                 }
             }
         }
