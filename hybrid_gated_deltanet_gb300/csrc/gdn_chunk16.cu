@@ -30,11 +30,16 @@
 //  1. k_prep16, one CTA per (chunk slot, k-head), all chunks at once:
 //     conv + SiLU + L2 norm of the k-head's q and k -> [K^; Q^] (fp16) and the
 //     Gram [K^ K^T; Q^ K^T] (one M = 128 product); K^ is stored for the chain.
-//     Per v-head of the k-head's group: gates, gamma, the masks A and P,
-//     T = (I + A)^-1 (fp32), T' = T diag(beta), [T'; PT'] = [I; P] T' and
-//     [W; PW] = [T'; PT'] diag(e^gamma) K^ (M = 128 products), the A operand
-//     [-W; Q'] of the chain with Q' = e^gamma Q^ - PW, and V = silu(conv(x)) of
-//     the v-head's channels -> stored fp16 with e^gamma and e^(gamma_C - gamma).
+//     Per v-head of the k-head's group: gates, gamma, the masks A and P, and
+//     T' = (I + A)^-1 diag(beta): its diagonal 16 x 16 blocks by substitution
+//     in fp32, the blocks below by T'_ab = -X_aa sum_c A_ac T'_cb on warp-level
+//     fp16 MMAs (fp32 accumulation; a rounding emulation of the chain shows no
+//     loss against an exact inverse).  Then [T'; PT'] = [I; P] T' and, in one
+//     product over [K^; Q^] (K = 128), the chain's A operand
+//         [-W; Q'] = [-[T'; PT'] diag(e^gamma) | 0; diag(e^gamma)] [K^; Q^],
+//     and V = silu(conv(x)) of the v-head's channels (while the products run)
+//     -> stored fp16 with e^gamma and e^(gamma_C - gamma).  Elementwise work
+//     runs on paired fp32 instructions (two lanes per FFMA2 / FMUL2).
 //  2. k_chain16, one CTA per (sequence, v-head), chunks in order; the fp32
 //     state S^T lives in tensor memory for the whole sequence.  Per chunk:
 //       PRE  [U~; X] = [T'; PT'] V                                   (4 MMAs)
