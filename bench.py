@@ -187,17 +187,18 @@ def _rel(got, ref):
     return float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-300))
 
 
-def setup_decode(torch, device, seed: int):
+def setup_decode(torch, device, seed: int, n_layers=None, batch=None, pool=None):
     from hybrid_gated_deltanet_gb300 import binding as gb
     from hybrid_gated_deltanet_gb300 import synth
+    n_layers, batch, pool = n_layers or N_LAYERS, batch or B, pool or POOL
     geom = synth.QWEN35_4B
     r = synth.rng_for(1, seed)
     cfg = gb.Config(*GEOM_ARGS, chunk=64, act_dtype=gb.BF16)
     p = synth.make_params(geom, r, synth.BF16)
-    tok = synth.make_tokens(geom, B, r, synth.BF16)
-    S = synth.make_state(geom, POOL, r, std=0.1)
-    CS = synth.make_conv_state(geom, POOL, r, synth.BF16, std=0.1)
-    slots = r.permutation(POOL)[:B].astype(np.int32)
+    tok = synth.make_tokens(geom, batch, r, synth.BF16)
+    S = synth.make_state(geom, pool, r, std=0.1)
+    CS = synth.make_conv_state(geom, pool, r, synth.BF16, std=0.1)
+    slots = r.permutation(pool)[:batch].astype(np.int32)
     host = dict(geom=geom, p=p, tok=tok, S=S, CS=CS, slots=slots)
     # layer 0 from the generator; layers 1..23 are device copies (distinct buffers)
     prm0 = gb.Params(conv_w=_dev(p["conv_w"], torch, device), A_log=_dev(p["A_log"], torch, device),
@@ -206,13 +207,34 @@ def setup_decode(torch, device, seed: int):
     x0, z0, a0, b0 = (_dev(tok[k], torch, device) for k in ("x", "z", "a", "b"))
     sl = torch.from_numpy(slots).to(device)
     layers = []
-    for l in range(N_LAYERS):
+    for l in range(n_layers):
         clone = (lambda t: t) if l == 0 else (lambda t: t.clone())
         layers.append(dict(prm=gb.Params(conv_w=clone(prm0.conv_w), A_log=clone(prm0.A_log),
                                          norm_w=clone(prm0.norm_w)),
                            S=clone(s0), C=clone(c0), x=clone(x0), z=clone(z0), a=clone(a0), b=clone(b0),
-                           slots=clone(sl), y=torch.empty((B, geom.value_dim), dtype=torch.bfloat16, device=device)))
+                           slots=clone(sl), y=torch.empty((batch, geom.value_dim), dtype=torch.bfloat16, device=device)))
     return cfg, host, layers
+
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def small_batch_decode(torch, device, steps, warmup, batches=(1, 4, 16)):
+    """The decode step at small batches: per batch, enough layers (each with its own
+    pool of 4 B slots) that one step touches at least 4 x L2 of state, replayed from
+    a CUDA graph; GB/s of the same algorithmic bytes per slot and layer."""
+    out = []
+    for bt in batches:
+        layer_bytes = bt * SLOT_BYTES + PARAM_BYTES
+        n_layers = max(24, -(-4 * L2_BYTES // layer_bytes))
+        cfg, _, layers = setup_decode(torch, device, seed=100 + bt, n_layers=n_layers, batch=bt, pool=4 * bt)
+        t = time_decode(torch, cfg, layers, steps, warmup)
+        us = 1e6 * t / (steps * n_layers)
+        out.append({"batch": bt, "layers": n_layers, "working_set_bytes": n_layers * layer_bytes,
+                    "us_per_layer": round(us, 3), "gbs": round(layer_bytes / us / 1e3, 1)})
+        del layers
+        torch.cuda.empty_cache()
+    return out
 
 
 def decode_parity(torch, cfg, host, layers, n_check=8):
@@ -546,6 +568,10 @@ def profile_case(args):
                           "us_per_launch": round(us, 3),
                           "gbs": round((B * SLOT_BYTES + PARAM_BYTES) / us / 1e3, 1),
                           "slices": os.environ.get("GDN_DECODE_SLICES", "auto")}))
+    elif args.case == "decode-batches":
+        for rec in small_batch_decode(torch, device, args.steps, args.warmup):
+            print(json.dumps(dict(rec, slices=os.environ.get("GDN_DECODE_SLICES", "auto"),
+                                  clustered=os.environ.get("GDN_DECODE_CLUSTERED", "auto"))))
     elif args.case == "serving":
         print(json.dumps(serving_measure(torch, device, args.steps, args.warmup)))
     elif args.case == "ckpt":
@@ -1263,7 +1289,8 @@ def main():
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--batch", type=int, default=64, help="slots of the decode-small case")
-    ap.add_argument("--case", default="full", choices=["full", "decode-small", "prefill-small", "serving", "verify", "ckpt", "layer",
+    ap.add_argument("--case", default="full", choices=["full", "decode-small", "decode-batches", "prefill-small", "serving",
+                             "verify", "ckpt", "layer",
                              "proj-decode", "attn", "proj-prefill", "attn-small"],
                     help="small cases for ncu captures")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -145,6 +145,10 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
     float* obuf = reinterpret_cast<float*>(smem + lay.obuf);
     float* ssp = reinterpret_cast<float*>(smem + lay.ssp);
 
+    // programmatic dependent launch: this grid may be resident before the previous
+    // kernel of the stream ends; every read below waits for it (and its memory)
+    griddep_wait();
+    griddep_launch_dependents();
     const int slot = J.slot_idx[bb];
     if (slot < 0 || slot >= J.n_slots) return;  // the whole cluster shares bb
     // rows to run: all r, or for a commit by recompute the accepted ones
@@ -784,13 +788,17 @@ cudaError_t launch_rows_t(const Geom& g, const LayerParams& p, const RowsJob& jo
     cfg.blockDim = dim3(kRowsThreads);
     cfg.dynamicSmemBytes = (size_t)lay.total;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    // a cluster per k-head group; programmatic stream serialization lets the grid be
+    // scheduled while its predecessor finishes (it waits in griddep_wait)
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = g.G * NS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, k_rows<D, TA>, A);
 }
 
