@@ -1208,6 +1208,10 @@ def gpu_arm(args):
             wide_v = [verify_measure(torch, device, max(20, args.steps // 8), 3, batch=nb) for nb in (4, 64)]
             extra["wide_gva"] = {"prefill": wide_pf, "verify": wide_v}
             extra["serving"] = serving_measure(torch, device, max(3, pf_steps // 2), 3)
+            sb = small_batch_decode(torch, device, max(10, args.steps // 20), 3)
+            for rec in sb:
+                rec["frac"] = round(rec["gbs"] / peaks["hbm_gbs"], 4)
+            extra["decode_small_batch"] = sb
     t_dec = max_over_ranks(t_dec, world)
     e2e_t, h2d, d2h = time_decode_e2e(torch, cfg, layers, max(3, args.steps // 4), 3)
     e2e_t = max_over_ranks(e2e_t, world)
