@@ -87,6 +87,10 @@ struct Args {
     unsigned char* kk;   // [ncs][Hk] kK
     unsigned char* rec;  // [ncs][Hv] kRec
     int64_t ncs;         // chunk slots
+    int64_t cs_lo;       // k_prep16 covers chunk slots cs_lo .. cs_lo + grid - 1
+    int c_lo, c_hi;      // k_chain16 runs chunks c_lo .. c_hi - 1 of each sequence
+    int carry_in;        // k_chain16 starts from the state a previous segment left in s_final
+    int prep_wait_end;   // k_prep16 ends with a wait for the grid before it in the stream
 };
 
 size_t align1024(size_t x) { return (x + 1023) & ~(size_t)1023; }
@@ -273,7 +277,7 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
     const PrefillJob& J = A.J;
     const int Hk = g.Hk, Hv = g.Hv, G = g.G, K = g.K, Cch = g.C_ch;
     const int h = blockIdx.x;
-    const int64_t cs = (int64_t)blockIdx.z * gridDim.y + blockIdx.y;
+    const int64_t cs = A.cs_lo + (int64_t)blockIdx.z * gridDim.y + blockIdx.y;
     if (cs >= A.ncs) return;
     int sq, n;
     int64_t start, end, t0;
@@ -740,6 +744,9 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
     tc::fence_before();
     __syncthreads();
     if (warp == 0) tc::dealloc(tm, P_TMEM_COLS);
+    // a segment's prep launched beside the previous chain segment completes only after it,
+    // so that the next chain segment, launched after this grid, follows both
+    if (A.prep_wait_end && tid == 0) griddep_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -787,6 +794,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1) k_chain16(const __grid_constant
     const int Hk = g.Hk, Hv = g.Hv;
     const int j = blockIdx.x, seq = blockIdx.y, h = j / g.G;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    griddep_launch_dependents();  // a following prep segment may start beside this grid
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = smem_raw + ((1024 - (tc::smem_addr(smem_raw) & 1023)) & 1023);
@@ -802,13 +810,17 @@ __global__ void __launch_bounds__(CH_THREADS, 1) k_chain16(const __grid_constant
     int64_t start, end;
     seq_bounds(J, seq, start, end);
     const int64_t T = end - start;
-    const int nch = (int)((T + C - 1) / C);
+    // this launch's chunks of the sequence: c_lo .. c_hi - 1 (local index c = 0 .. nch - 1)
+    const int nch_all = (int)((T + C - 1) / C);
+    const int c_lo = A.c_lo, c_hi = A.c_hi < nch_all ? A.c_hi : nch_all;
+    const int nch = c_hi > c_lo ? c_hi - c_lo : 0;
     const bool outnorm = !(g.flags & kFlagNoOutNorm);
     const float* Sin = nullptr;
     float* Sout = nullptr;
     if (!J.cu_seqlens) {
-        Sin = J.s0 ? J.s0 + (size_t)j * D * D : nullptr;
         Sout = J.s_final + (size_t)j * D * D;
+        // a later segment continues from the state the previous one left in s_final
+        Sin = A.carry_in ? Sout : (J.s0 ? J.s0 + (size_t)j * D * D : nullptr);
     } else {
         const int slot = J.slot_idx[seq];
         if (slot >= 0 && slot < J.n_slots) {
@@ -843,12 +855,12 @@ __global__ void __launch_bounds__(CH_THREADS, 1) k_chain16(const __grid_constant
     tc::fence_after();
     const uint32_t tm = *tslot;
 
-    auto chunk_t0 = [&](int c) -> int64_t { return start + (int64_t)c * C; };
+    auto chunk_t0 = [&](int c) -> int64_t { return start + (int64_t)(c_lo + c) * C; };
     auto chunk_n = [&](int c) -> int {
         const int64_t left = end - chunk_t0(c);
         return (int)(left < C ? left : C);
     };
-    auto chunk_slot = [&](int c) -> size_t { return (size_t)(start / C + seq + c); };
+    auto chunk_slot = [&](int c) -> size_t { return (size_t)(start / C + seq + c_lo + c); };
     // bounded wait; after an abort every wait returns at once
     auto wait = [&](int b, int c) {
         if (*abortp) return;
@@ -1039,7 +1051,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1) k_chain16(const __grid_constant
                 wait(B_FULL_K, c + 1);
             }
             const float egC = more ? sG[((c + 1) & 1) * 128 + C - 1] : 0.f;
-            const int ck = ckpt_after(J, seq, (int64_t)(c + 1) * C, T);
+            const int ck = ckpt_after(J, seq, (int64_t)(c_lo + c + 1) * C, T);
             float* snap = ck >= 0 ? J.state_pool + ((size_t)ck * Hv + j) * D * D : nullptr;
 #pragma unroll 1
             for (int b = 0; b < 2; ++b) {
@@ -1193,6 +1205,35 @@ size_t chunk16_workspace_bytes(const Geom& g, int64_t n_tokens, int n_seq) {
     return n_tokens > 0 ? c16::ws_layout(g, n_tokens, n_seq).total : 0;
 }
 
+namespace {
+cudaError_t launch_prep(const c16::Args& A, int64_t cs_lo, int64_t n_cs, bool beside, cudaStream_t st) {
+    c16::Args B = A;
+    B.cs_lo = cs_lo;
+    B.prep_wait_end = beside ? 1 : 0;
+    const int64_t ny = n_cs < 32768 ? n_cs : 32768;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)A.g.Hk, (unsigned)ny, (unsigned)((n_cs + ny - 1) / ny));
+    cfg.blockDim = dim3(c16::P_THREADS);
+    cfg.dynamicSmemBytes = c16::P_SMEM_ALLOC;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = beside ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, c16::k_prep16, B);
+}
+
+cudaError_t launch_chain(const c16::Args& A, int c_lo, int c_hi, bool carry_in, cudaStream_t st) {
+    c16::Args B = A;
+    B.c_lo = c_lo;
+    B.c_hi = c_hi;
+    B.carry_in = carry_in ? 1 : 0;
+    k_chain16<<<dim3((unsigned)A.g.Hv, (unsigned)A.J.n_seq), c16::CH_THREADS, c16::S_SMEM_ALLOC, st>>>(B);
+    return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t chunk16_launch(const Geom& g, const LayerParams& p, const PrefillJob& J, cudaStream_t st) {
     using namespace c16;
     static std::atomic<uint64_t> smem_prep{0}, smem_chain{0};
@@ -1209,15 +1250,42 @@ cudaError_t chunk16_launch(const Geom& g, const LayerParams& p, const PrefillJob
     A.kk = ws + L.kk;
     A.rec = ws + L.rec;
     A.ncs = L.ncs;
+    A.cs_lo = 0;
+    A.c_lo = 0;
+    A.c_hi = 1 << 30;
+    A.carry_in = 0;
+    A.prep_wait_end = 0;
+    // One long sequence: its chain occupies one SM per v-head and leaves the rest of the
+    // GPU idle while it walks the chunks.  The sequence is then cut into segments, all on
+    // the caller's stream:  prep(0), chain(0), prep(1), chain(1), ...  Each chain segment
+    // lets the next grid start once its CTAs are resident (programmatic dependent launch),
+    // so the prep of segment k + 1 runs on the other SMs beside the chain of segment k and
+    // waits for it only at its very end; the chain of segment k + 1, launched normally,
+    // therefore follows both.  No kernel waits on another's data.  Each chain segment
+    // leaves its state in s_final for the next, so the result is bit for bit that of one
+    // chain launch.  A prep segment is sized to about one wave on the SMs the chain
+    // leaves (2 CTAs per SM); it is faster per chunk than the chain.
+    const int64_t nch = J.n_tokens / C + (J.n_tokens % C ? 1 : 0);
+    const int sms = sm_count();
+    const int64_t per = std::max<int64_t>(4, (int64_t)(2 * (sms - g.Hv)) / g.Hk);
+    const bool segmented = !J.cu_seqlens && 2 * g.Hv <= sms && nch >= 2 * per;
+    if (J.n_tokens > 0 && segmented) {
+        const int64_t nseg = std::min<int64_t>(32, (nch + per - 1) / per);
+        const int64_t len = (nch + nseg - 1) / nseg;
+        for (int64_t k = 0; k < nseg; ++k) {
+            const int64_t c0 = k * len, c1 = std::min(nch, c0 + len);
+            if (k == 0 && (e = launch_prep(A, c0, c1 - c0, false, st)) != cudaSuccess) return e;
+            if ((e = launch_chain(A, (int)c0, (int)c1, k > 0, st)) != cudaSuccess) return e;
+            const int64_t n0 = c1, n1 = std::min(nch, n0 + len);
+            if (n0 < nch && (e = launch_prep(A, n0, n1 - n0, true, st)) != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     if (J.n_tokens > 0) {
-        const int64_t ny = L.ncs < 32768 ? L.ncs : 32768;
-        const dim3 grid((unsigned)g.Hk, (unsigned)ny, (unsigned)((L.ncs + ny - 1) / ny));
-        k_prep16<<<grid, P_THREADS, P_SMEM_ALLOC, st>>>(A);
-        e = cudaGetLastError();
+        e = launch_prep(A, 0, L.ncs, false, st);
         if (e != cudaSuccess) return e;
     }
-    k_chain16<<<dim3((unsigned)g.Hv, (unsigned)J.n_seq), CH_THREADS, S_SMEM_ALLOC, st>>>(A);
-    return cudaGetLastError();
+    return launch_chain(A, 0, 1 << 30, false, st);
 }
 
 cudaError_t take_device_status_chunk16(unsigned* out) { return take_device_status_tu(out); }

@@ -187,3 +187,38 @@ def test_prefill_empty_sequence_keeps_state():
     torch.cuda.synchronize()
     np.testing.assert_array_equal(host(s_fin), S0.f64[0])
     np.testing.assert_array_equal(host(c_fin), C0.f64[0])
+
+
+@pytest.mark.parametrize("T", [2048, 4096 + 37])
+def test_segmented_single_sequence_is_bitwise_one_chain(T):
+    """A long single sequence runs as segments (the prep of the next segment beside the
+    chain of this one, the state handed over in s_final); a one-sequence varlen call of
+    the same tokens runs one chain.  Both must agree bit for bit, with and without an
+    initial state."""
+    geom, act, r, p, tok = make_case("prefill4b", 300 + T, T)
+    cfg = config(geom, act)
+    H = cfg.n_v_heads
+    prm = params_dev(p)
+    x, z, a, b = (dev(tok[k]) for k in ("x", "z", "a", "b"))
+    S0 = synth.make_state(geom, 1, r, std=0.1)
+    C0 = synth.make_conv_state(geom, 1, r, act, std=0.1)
+    for init in (False, True):
+        s_fin = torch.empty((H, cfg.d_v, cfg.d_k), device="cuda")
+        c_fin = torch.empty((cfg.d_conv - 1, cfg.conv_channels), dtype=cfg.torch_dtype, device="cuda")
+        y1 = torch.empty((T, H * cfg.d_v), dtype=cfg.torch_dtype, device="cuda")
+        ws = torch.empty(gb.gdn_workspace_size(cfg, gb.OP_CHUNK_PREFILL, T), dtype=torch.uint8, device="cuda")
+        s0 = dev(S0)[0].contiguous() if init else None
+        c0 = dev(C0)[0].contiguous() if init else None
+        gb.gdn_chunk_prefill(cfg, prm, x, z, a, b, s0, c0, s_fin, c_fin, y1, ws)
+        sp, cp = dev(S0), dev(C0)
+        y2 = torch.empty_like(y1)
+        ws2 = torch.empty(gb.gdn_workspace_size(cfg, gb.OP_VARLEN_PREFILL, T, 1), dtype=torch.uint8, device="cuda")
+        cu = torch.tensor([0, T], dtype=torch.int32, device="cuda")
+        sl = torch.zeros(1, dtype=torch.int32, device="cuda")
+        hi = torch.tensor([1 if init else 0], dtype=torch.uint8, device="cuda")
+        gb.gdn_varlen_prefill(cfg, prm, x, z, a, b, cu, sl, hi, cp, sp, y2, ws2)
+        torch.cuda.synchronize()
+        assert torch.equal(y1, y2), f"y differs (init={init})"
+        assert torch.equal(s_fin, sp[0]), f"S differs (init={init})"
+        assert torch.equal(c_fin, cp[0]), f"conv differs (init={init})"
+    assert gb.gdn_device_status() == 0
