@@ -124,13 +124,6 @@ __device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {  // two bf16 (element 
     return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-__device__ __forceinline__ void unpack8x2(const uint4& u, float2 f[4]) {
-    f[0] = bf2_to_f2(u.x);
-    f[1] = bf2_to_f2(u.y);
-    f[2] = bf2_to_f2(u.z);
-    f[3] = bf2_to_f2(u.w);
-}
-
 __device__ __forceinline__ float tanh_hw(float x) {
     float t;
     asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
@@ -152,73 +145,6 @@ __device__ __forceinline__ float2 silu2(float2 x) {
 __device__ __forceinline__ uint4 pack8x2(const float2 v[4]) {
     return make_uint4(tc::pack_h2(v[0].x, v[0].y), tc::pack_h2(v[1].x, v[1].y), tc::pack_h2(v[2].x, v[2].y),
                       tc::pack_h2(v[3].x, v[3].y));
-}
-
-// conv + SiLU of NT tokens for 8 channels held as 4 pairs; rows i .. i+3
-// (row(k) returns packed bf16 row k) are the window of token i.  Window rows that are not taps (d_conv < 4)
-// carry zero weights.  emit(i, u) receives token i's 4 pairs.
-template <int NT, typename Row, typename Emit>
-__device__ __forceinline__ void conv8x2(Row row, const float2 w[4][4], const float2 bias[4], bool raw, Emit emit) {
-    float2 win[4][4];
-#pragma unroll
-    for (int r = 1; r < 4; ++r) unpack8x2(row(r - 1), win[r]);
-#pragma unroll
-    for (int i = 0; i < NT; ++i) {
-#pragma unroll
-        for (int r = 0; r < 3; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) win[r][c] = win[r + 1][c];
-        unpack8x2(row(i + 3), win[3]);
-        float2 u[4];
-        if (raw) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) u[c] = win[3][c];
-        } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float2 s = bias[c];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) s = __ffma2_rn(w[r][c], win[r][c], s);
-                u[c] = silu2(s);
-            }
-        }
-        emit(i, u);
-    }
-}
-
-// window-row weights of 8 channels (as pairs) from the [8][K] bf16 taps at `src`
-// (channel c's tap m at element c K + m; 16-byte aligned): w[4 - K + m] = tap m
-__device__ __forceinline__ void conv_weights8x2(const __nv_bfloat16* src, int K, float2 w[4][4]) {
-    float f[4][8];
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) f[r][c] = 0.f;
-    const uint4* s4 = reinterpret_cast<const uint4*>(src);
-    auto unpack_taps = [&](auto kk) {
-        constexpr int KK = decltype(kk)::value;
-        float t[8 * KK];
-#pragma unroll
-        for (int v = 0; v < KK; ++v) unpack8(s4[v], t + 8 * v);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-#pragma unroll
-            for (int m = 0; m < KK; ++m) f[4 - KK + m][c] = t[c * KK + m];
-    };
-    if (K == 4) unpack_taps(std::integral_constant<int, 4>{});
-    else if (K == 3) unpack_taps(std::integral_constant<int, 3>{});
-    else unpack_taps(std::integral_constant<int, 2>{});
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) w[r][c] = make_float2(f[r][2 * c], f[r][2 * c + 1]);
-}
-
-__device__ __forceinline__ void bias8x2(const LayerParams& p, int ch, float2 b[4]) {
-    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (p.conv_b) unpack8(*reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.conv_b) + ch), f);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) b[c] = make_float2(f[2 * c], f[2 * c + 1]);
 }
 
 // warp-level fp16 tensor-core pieces of the triangular merges (m16n8k16, fp32
@@ -243,35 +169,127 @@ __device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], const 
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
 
+// 4-channel forms of the conv helpers (a thread owns 4 channels: two pairs)
+__device__ __forceinline__ void unpack4x2(const uint2& u, float2 f[2]) {
+    f[0] = bf2_to_f2(u.x);
+    f[1] = bf2_to_f2(u.y);
+}
+
+__device__ __forceinline__ uint2 pack4x2(const float2 v[2]) {
+    return make_uint2(tc::pack_h2(v[0].x, v[0].y), tc::pack_h2(v[1].x, v[1].y));
+}
+
+// conv + SiLU of NT tokens for 4 channels (two pairs); row(k) returns packed bf16 row k,
+// rows i .. i+3 are the window of token i
+template <int NT, typename Row, typename Emit>
+__device__ __forceinline__ void conv4x2(Row row, const float2 w[4][2], const float2 bias[2], bool raw, Emit emit) {
+    float2 win[4][2];
+#pragma unroll
+    for (int r = 1; r < 4; ++r) unpack4x2(row(r - 1), win[r]);
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+#pragma unroll
+        for (int r = 0; r < 3; ++r)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) win[r][c] = win[r + 1][c];
+        unpack4x2(row(i + 3), win[3]);
+        float2 u[2];
+        if (raw) {
+            u[0] = win[3][0];
+            u[1] = win[3][1];
+        } else {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                float2 s = bias[c];
+#pragma unroll
+                for (int r = 0; r < 4; ++r) s = __ffma2_rn(w[r][c], win[r][c], s);
+                u[c] = silu2(s);
+            }
+        }
+        emit(i, u);
+    }
+}
+
+// window-row weights of 4 channels from the [4][K] bf16 taps at `src` (8-byte aligned)
+__device__ __forceinline__ void conv_weights4x2(const __nv_bfloat16* src, int K, float2 w[4][2]) {
+    float f[4][4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) f[r][c] = 0.f;
+    const uint2* s2 = reinterpret_cast<const uint2*>(src);
+    auto unpack_taps = [&](auto kk) {
+        constexpr int KK = decltype(kk)::value;
+        float t[4 * KK];
+#pragma unroll
+        for (int v = 0; v < KK; ++v) {
+            const uint2 u = s2[v];
+            const float2 a = bf2_to_f2(u.x), b = bf2_to_f2(u.y);
+            t[4 * v] = a.x;
+            t[4 * v + 1] = a.y;
+            t[4 * v + 2] = b.x;
+            t[4 * v + 3] = b.y;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int m = 0; m < KK; ++m) f[4 - KK + m][c] = t[c * KK + m];
+    };
+    if (K == 4) unpack_taps(std::integral_constant<int, 4>{});
+    else if (K == 3) unpack_taps(std::integral_constant<int, 3>{});
+    else unpack_taps(std::integral_constant<int, 2>{});
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        w[r][0] = make_float2(f[r][0], f[r][1]);
+        w[r][1] = make_float2(f[r][2], f[r][3]);
+    }
+}
+
+__device__ __forceinline__ void bias4x2(const LayerParams& p, int ch, float2 b[2]) {
+    b[0] = b[1] = make_float2(0.f, 0.f);
+    if (p.conv_b) {
+        const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.conv_b) + ch);
+        b[0] = bf2_to_f2(u.x);
+        b[1] = bf2_to_f2(u.y);
+    }
+}
+
 constexpr int P_THREADS = 256;
 constexpr int kXRows = C + 3;                              // staged x rows: tokens t0-3 .. t0+63
 constexpr uint32_t kStage = kXRows * 512;                  // q/k rows, or the v rows of 2 v-heads
 constexpr uint32_t kStageV = kXRows * 256;                 // the v rows of one v-head
 constexpr uint32_t P_KQ = 0;                               // [K^; Q^] fp16 [128][128], atoms of 128 rows
-constexpr uint32_t P_STG = 32768;                          // staged raw x rows
-constexpr uint32_t P_SCR = (P_STG + kStage + 1023) & ~1023u;  // scratch of one v-head:
+constexpr uint32_t P_SCR = 32768;                          // scratch of one v-head (staging before it):
 constexpr uint32_t P_IP = P_SCR;                           //   [I; P] fp16 K-major [128][64]
 constexpr uint32_t P_TB = P_IP + 16384;                    //   T' fp16 MN-major [64 (k)][64]
-constexpr int kA16Ld = 72;                                 //   (halves)
-constexpr uint32_t P_A16 = P_TB + 8192;                    //   A fp16 [64][72] (its blocks below the diagonal)
+constexpr int kBLd = 24;                                   //   row stride (halves) of the 16 x 16 blocks
+constexpr uint32_t kBlk = 16 * kBLd * 2;                   //   768 B per block
+constexpr uint32_t P_A16 = P_TB + 8192;                    //   A's 6 blocks below the diagonal, fp16
 constexpr int kA32Ld = 17;                                 //   (floats)
-constexpr uint32_t P_A32 = P_A16 + 64 * kA16Ld * 2;        //   A's diagonal 16 x 16 blocks fp32 [4][16][17]
-constexpr int kX16Ld = 24;                                 //   (halves)
-constexpr uint32_t P_X16 = P_A32 + 4 * 16 * kA32Ld * 4;    //   (I + A)^-1's diagonal blocks fp16 [4][16][24]
-constexpr uint32_t P_Y = P_X16 + 4 * 16 * kX16Ld * 2;      //   a 16 x 8 fp16 tile per warp
+constexpr uint32_t P_A32 = P_A16 + 6 * kBlk;               //   A's diagonal 16 x 16 blocks fp32 [4][16][17]
+constexpr uint32_t P_X16 = P_A32 + 4 * 16 * kA32Ld * 4;    //   (I + A)^-1's diagonal blocks fp16 [4] blocks
+constexpr uint32_t P_Y = P_X16 + 4 * kBlk;                 //   a 16 x 8 fp16 tile per warp
+constexpr uint32_t P_SCR_END = P_Y + 8 * 256;
 constexpr uint32_t P_WA = P_SCR;                           //   later [-T'e, 0; -PT'e, diag(e^gamma)] [128][128]
-constexpr uint32_t P_WV = P_Y + 8 * 256;                   // conv taps of the 2 staged v-heads (2 x 1 KB)
+constexpr uint32_t P_STG = P_SCR;                          //   before: the staged raw x rows
+constexpr uint32_t P_WV = P_SCR_END;                       // conv taps of the 2 staged v-heads (2 x 1 KB)
 constexpr uint32_t P_SMALL = P_WV + 2048;                  // gamma log2(e), beta, e^gamma, e^(gamma_C - gamma)
 constexpr uint32_t P_SMEM = P_SMALL + 4 * C * 4 + 16;      //   [64] each; mbarrier; TMEM slot
 constexpr uint32_t P_SMEM_ALLOC = P_SMEM + 1024;
-constexpr uint32_t P_TMEM_COLS = 256;                      // Gram (64) | [T'; PT'] (64) | [-W; Q'] (128)
-static_assert(P_WA + 32768 <= P_WV, "WA overlay");
+constexpr uint32_t P_TMEM_COLS = 128;                      // Gram (0..63) | [T'; PT'] (64..127), then [-W; Q']
+constexpr int P_CTAS_PER_SM = 3;
+static_assert(P_WA + 32768 <= P_SCR_END && P_STG + kStage <= P_SCR_END, "overlays of the scratch");
 static_assert((P_IP & 1023) == 0 && (P_TB & 1023) == 0 && (P_A16 & 15) == 0 && (P_X16 & 15) == 0 &&
                   (P_Y & 15) == 0 && (P_WV & 15) == 0,
               "operand alignment");
-static_assert(2 * (P_SMEM_ALLOC + 1024) <= 233472, "two CTAs per SM");
+static_assert(P_CTAS_PER_SM * (P_SMEM_ALLOC + 1024) <= 233472, "three CTAs per SM");
 
-__global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__ Args A) {
+// byte offset of row r, column c (fp16) of block b of the packed 16 x 16 blocks
+__device__ __forceinline__ uint32_t blk_off(int b, int r, int c) { return (uint32_t)(b * kBlk + (r * kBLd + c) * 2); }
+// packed index of A's block (a, c) below the diagonal (a > c)
+__device__ __forceinline__ int low_blk(int a, int c) { return a * (a - 1) / 2 + c; }
+
+__global__ void __launch_bounds__(P_THREADS, P_CTAS_PER_SM) k_prep16(const __grid_constant__ Args A) {
     using L = Act<__nv_bfloat16>;
     const Geom& g = A.g;
     const PrefillJob& J = A.J;
@@ -304,9 +322,8 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
     const __nv_bfloat16* cw = static_cast<const __nv_bfloat16*>(A.p.conv_w);
 
     // stage x rows tau = t0-3+r (r < kXRows), 32 chunks of 16 bytes per row: chunk ci
-    // of row r goes to dst(r, ci) from channel ch(ci) (negative: not staged).  Rows
-    // before the sequence come from its conv state (or are zero), rows past its end
-    // are zero.
+    // of row r goes to dst(r, ci) from channel ch (negative: not staged).  Rows before
+    // the sequence come from its conv state (or are zero), rows past its end are zero.
     auto stage_rows = [&](auto dst, int ch) {
         const int ci = tid & 31;
         if (ch < 0) return;
@@ -357,69 +374,56 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
         }
     };
     if (warp == 0) load_gates(h * G);
-    const int ch_qk = (lane < 16 ? h : Hk + h) * D + (lane & 15) * 8;
-    float2 wqk[4][4], bqk[4];
+    // q/k thread: warps 0..3 q, 4..7 k; lane = 4 channels; warp & 3 = a block of 16 tokens
+    const bool is_q = warp < 4;
+    const int ch_qk = (is_q ? h : Hk + h) * D + lane * 4;
+    float2 wqk[4][2], bqk[2];
     if (raw) {
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) wqk[r][c] = make_float2(0.f, 0.f);
+        for (int r = 0; r < 4; ++r) wqk[r][0] = wqk[r][1] = make_float2(0.f, 0.f);
     } else {
-        conv_weights8x2(cw + (size_t)ch_qk * K, K, wqk);
+        conv_weights4x2(cw + (size_t)ch_qk * K, K, wqk);
     }
-    bias8x2(A.p, ch_qk, bqk);
+    bias4x2(A.p, ch_qk, bqk);
     cp_async_wait_all();
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tm = *tslot;
 
-    // ---- conv + SiLU + L2 norm of q and k: thread = 8 channels (lanes 0..15 q,
-    // 16..31 k) x 8 tokens (one warp's) -> rows 0..63 K^, 64..127 Q^ -------------
+    // ---- conv + SiLU + L2 norm of q and k -> rows 0..63 K^, 64..127 Q^ -------------------
     {
-        const bool is_q = lane < 16;
-        const int d0 = (lane & 15) * 8;
-        const int tt0 = warp * 8;
-        const unsigned char* xr = sSTG + tt0 * 512 + lane * 16;
+        const int tt0 = (warp & 3) * 16;
+        const unsigned char* xr = sSTG + tt0 * 512 + (is_q ? 0 : 256) + lane * 8;
+        const int d0 = lane * 4;
         unsigned char* atom = sKQ + (d0 >> 6) * 16384;
-        const int cc = (d0 & 63) >> 3;
+        const int cc = (d0 & 63) >> 3, sub = (d0 & 7) * 2;
         const float qs = is_q ? g.q_scale : 1.f;
         const bool l2 = !(g.flags & kFlagNoL2);
-        conv8x2<8>([&](int k) { return *reinterpret_cast<const uint4*>(xr + k * 512); }, wqk, bqk, raw,
-                   [&](int i, float2 u[4]) {
-            const int t = tt0 + i;
-            float2 s2 = __fmul2_rn(u[0], u[0]);
+        conv4x2<16>([&](int k) { return *reinterpret_cast<const uint2*>(xr + k * 512); }, wqk, bqk, raw,
+                    [&](int i, float2 u[2]) {
+                        const int t = tt0 + i;
+                        const float2 s2 = __ffma2_rn(u[1], u[1], __fmul2_rn(u[0], u[0]));
+                        float ss = s2.x + s2.y;
 #pragma unroll
-            for (int c = 1; c < 4; ++c) s2 = __ffma2_rn(u[c], u[c], s2);
-            float ss = s2.x + s2.y;
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-            float scale = l2 ? qs * rsqrtf(ss + g.l2_eps) : qs;
-            if (t >= n) scale = 0.f;  // zero past the sequence end
-            float2 v[4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) v[c] = __fmul2_rn(u[c], make_float2(scale, scale));
-            *reinterpret_cast<uint4*>(atom + tc::h_off(is_q ? C + t : t, cc)) = pack8x2(v);
-        });
+                        for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+                        float scale = l2 ? qs * rsqrtf(ss + g.l2_eps) : qs;
+                        if (t >= n) scale = 0.f;  // zero past the sequence end
+                        float2 v[2] = {__fmul2_rn(u[0], make_float2(scale, scale)),
+                                       __fmul2_rn(u[1], make_float2(scale, scale))};
+                        *reinterpret_cast<uint2*>(atom + tc::h_off(is_q ? C + t : t, cc) + sub) = pack4x2(v);
+                    });
     }
     fence_proxy_async_smem();
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     stage_pair(0);  // over the q/k rows, which are consumed
-    if (tid == 0) {
-        // K^ for the chain: the first 64 rows of each atom
+    if (tid == 0) {  // K^ for the chain: the first 64 rows of each atom
         unsigned char* dst = A.kk + ((size_t)cs * Hk + h) * kK;
         bulk_s2g(dst, sKQ, 8192);
         bulk_s2g(dst + 8192, sKQ + 16384, 8192);
         bulk_commit();
-        // [K^ K^T; Q^ K^T] = [K^; Q^] K^T: B = the K^ rows of the same tile (N = 64)
-        const uint32_t a0 = tc::smem_addr(sKQ);
-        for (int s = 0; s < D / 16; ++s) {
-            const uint64_t d = tc::sdesc_lbo(a0 + (uint32_t)((s >> 2) * 16384 + (s & 3) * 32), 16);
-            tc::mma_f16(tm, d, d, tc::idesc_f16(128, 64, false, false), s > 0 ? 1u : 0u);
-        }
-        tc::commit(mbar);
     }
     uint32_t phase = 0;
     bool ok = true;
@@ -433,38 +437,59 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
         ok = __syncthreads_and(ok && w);
         tc::fence_after();
     };
+    // [K^ K^T; Q^ K^T] = [K^; Q^] K^T into columns 0..63 (B = the K^ rows of the same tile)
+    auto issue_gram = [&]() {
+        if (tid == 0) {
+            tc::fence_after();
+            if (ok) {
+                const uint32_t a0 = tc::smem_addr(sKQ);
+                for (int s = 0; s < D / 16; ++s) {
+                    const uint64_t d = tc::sdesc_lbo(a0 + (uint32_t)((s >> 2) * 16384 + (s & 3) * 32), 16);
+                    tc::mma_f16(tm, d, d, tc::idesc_f16(128, 64, false, false), s > 0 ? 1u : 0u);
+                }
+            }
+            tc::commit(mbar);
+        }
+    };
+    issue_gram();
 
-    // V = silu(conv(x)) of v-head slot u (0, 1) of the staged pair, head j: thread = 8
-    // channels x 4 tokens, straight to the record (MN-major [64 tokens][128] fp16)
+    // V = silu(conv(x)) of v-head slot u (0, 1) of the staged pair, head j: thread = 4
+    // channels x 8 tokens, straight to the record (MN-major [64 tokens][128] fp16)
     auto v_conv = [&](int u, int j) {
-        const int cgp = tid & 15, tg = tid >> 4;
-        float2 w[4][4], bias[4];
+        const int cgp = tid & 31, tg = tid >> 5;
+        float2 w[4][2], bias[2];
         if (raw) {
 #pragma unroll
-            for (int r = 0; r < 4; ++r)
-#pragma unroll
-                for (int c = 0; c < 4; ++c) w[r][c] = make_float2(0.f, 0.f);
+            for (int r = 0; r < 4; ++r) w[r][0] = w[r][1] = make_float2(0.f, 0.f);
         } else {
-            conv_weights8x2(reinterpret_cast<const __nv_bfloat16*>(sWV + u * 1024) + cgp * 8 * K, K, w);
+            conv_weights4x2(reinterpret_cast<const __nv_bfloat16*>(sWV + u * 1024) + cgp * 4 * K, K, w);
         }
-        bias8x2(A.p, 2 * Hk * D + j * D + cgp * 8, bias);
-        const unsigned char* xv = sSTG + u * kStageV;
-        const unsigned char* xr = xv + 4 * tg * 256 + cgp * 16;
-        unsigned char* vat = A.rec + ((size_t)cs * Hv + j) * kRec + kRecV + (cgp >> 3) * 8192;
-        conv8x2<4>([&](int k) { return *reinterpret_cast<const uint4*>(xr + k * 256); }, w, bias, raw,
-                   [&](int i, float2 uu[4]) {
-            const int t = 4 * tg + i;
-            if (t >= n) {  // zero past the sequence end
-#pragma unroll
-                for (int c = 0; c < 4; ++c) uu[c] = make_float2(0.f, 0.f);
-            }
-            *reinterpret_cast<uint4*>(vat + tc::h_off(t, cgp & 7)) = pack8x2(uu);
-        });
+        bias4x2(A.p, 2 * Hk * D + j * D + cgp * 4, bias);
+        const unsigned char* xr = sSTG + u * kStageV + 8 * tg * 256 + cgp * 8;
+        const int d0 = cgp * 4;
+        unsigned char* vat = A.rec + ((size_t)cs * Hv + j) * kRec + kRecV + (d0 >> 6) * 8192;
+        const int cc = (d0 & 63) >> 3, sub = (d0 & 7) * 2;
+        conv4x2<8>([&](int k) { return *reinterpret_cast<const uint2*>(xr + k * 256); }, w, bias, raw,
+                   [&](int i, float2 uu[2]) {
+                       const int t = 8 * tg + i;
+                       if (t >= n) uu[0] = uu[1] = make_float2(0.f, 0.f);  // zero past the sequence end
+                       *reinterpret_cast<uint2*>(vat + tc::h_off(t, cc) + sub) = pack4x2(uu);
+                   });
     };
 
     for (int jj = 0; jj < G; ++jj) {
         const int j = h * G + jj;
         unsigned char* rec = A.rec + ((size_t)cs * Hv + j) * kRec;
+        // ---- V of the pair at its first v-head (the staged rows use the scratch) ----------
+        if ((jj & 1) == 0) {
+            if (jj > 0) {
+                stage_pair(jj / 2);  // the scratch is free: the previous [-W; Q'] product is done
+            }
+            cp_async_wait_all();
+            __syncthreads();
+            v_conv(0, j);
+            if (jj + 1 < G) v_conv(1, j + 1);
+        }
         // ---- gates (warp 0): g, beta of tokens lane, lane + 32; gamma = cumsum(g) ----------
         if (warp == 0) {
             const float alog = direct ? 0.f : A.p.A_log[j];
@@ -503,8 +528,7 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
                 rg[C + t] = er;
             }
         }
-        if (jj == 0) wait_mma();  // the Gram (ends with a CTA barrier)
-        else __syncthreads();
+        wait_mma();  // the Gram of this v-head (ends with a CTA barrier)
         // ---- masks from the Gram: A = strict-lower(beta_t Gamma o K^K^T) (TMEM lanes 0..63),
         // P = lower-incl(Gamma o Q^K^T) (lanes 64..127); Gamma_ti = 2^(gamma2_t - gamma2_i) ------
         for (int f = tid; f < C * 8; f += P_THREADS) {  // identity rows of [I; P]
@@ -526,36 +550,35 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
                         *reinterpret_cast<uint4*>(sIP + tc::h_off(C + t, 4 * hf + k)) = make_uint4(0, 0, 0, 0);
                 }
             } else {
-                float v[32];
-                tc::ld32(tc::taddr(tm, 32 * q4, 32 * hf), v);
                 const float gt = gam2[t];
                 const float bt = isA ? bet[t] : 1.f;
                 const bool diag = hf == rb;
-                const float2* g2 = reinterpret_cast<const float2*>(gam2 + 32 * hf);
                 const int tb = t >> 4;
                 // one 16-column block at a time: 8 pairs
-#pragma unroll
+#pragma unroll 1
                 for (int bq = 0; bq < 2; ++bq) {
                     const int cb = 2 * hf + bq;
+                    float v[16];
+                    tc::ld16(tc::taddr(tm, 32 * q4, 16 * cb), v);  // warp-collective: every lane loads
                     if (isA && cb > tb) continue;  // above the diagonal: unused
+                    const float2* g2 = reinterpret_cast<const float2*>(gam2 + 16 * cb);
                     float2 m[8];
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
-                        const int cp = 8 * bq + c;
-                        const float2 d = __ffma2_rn(g2[cp], make_float2(-1.f, -1.f), make_float2(gt, gt));
+                        const float2 d = __ffma2_rn(g2[c], make_float2(-1.f, -1.f), make_float2(gt, gt));
                         const float2 e = make_float2(ex2_hw(fminf(d.x, 0.f)), ex2_hw(fminf(d.y, 0.f)));
-                        m[c] = __fmul2_rn(__fmul2_rn(e, make_float2(v[2 * cp], v[2 * cp + 1])), make_float2(bt, bt));
+                        m[c] = __fmul2_rn(__fmul2_rn(e, make_float2(v[2 * c], v[2 * c + 1])), make_float2(bt, bt));
                         if (diag) {  // strictly below (A) or on / below (P) the diagonal
-                            const int i0 = 32 * hf + 2 * cp;
+                            const int i0 = 16 * cb + 2 * c;
                             if (isA ? i0 >= t : i0 > t) m[c].x = 0.f;
                             if (isA ? i0 + 1 >= t : i0 + 1 > t) m[c].y = 0.f;
                         }
                     }
                     if (!isA) {
-                        *reinterpret_cast<uint4*>(sIP + tc::h_off(C + t, 4 * hf + 2 * bq)) = pack8x2(m);
-                        *reinterpret_cast<uint4*>(sIP + tc::h_off(C + t, 4 * hf + 2 * bq + 1)) = pack8x2(m + 4);
-                    } else if (cb < tb) {  // below the diagonal -> fp16 A16
-                        uint4* dst = reinterpret_cast<uint4*>(sA16 + (t * kA16Ld + 16 * cb) * 2);
+                        *reinterpret_cast<uint4*>(sIP + tc::h_off(C + t, 2 * cb)) = pack8x2(m);
+                        *reinterpret_cast<uint4*>(sIP + tc::h_off(C + t, 2 * cb + 1)) = pack8x2(m + 4);
+                    } else if (cb < tb) {  // below the diagonal -> fp16 block (tb, cb)
+                        uint4* dst = reinterpret_cast<uint4*>(sA16 + blk_off(low_blk(tb, cb), t & 15, 0));
                         dst[0] = pack8x2(m);
                         dst[1] = pack8x2(m + 4);
                     } else {  // the diagonal block -> fp32 A32
@@ -569,6 +592,7 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
                 }
             }
         }
+        tc::fence_before();
         __syncthreads();
         // ---- T' = (I + A)^-1 diag(beta) -> sTB (MN-major: row k holds T'[k][0..63]) --------
         // diagonal 16 x 16 blocks by register-resident substitution (fp32): lane = column
@@ -589,11 +613,10 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
                 for (int i = k + 1; i < 16; ++i) xv[i] = fmaf(-__shfl_sync(0xffffffffu, acol[i], lb + k), xv[k], xv[i]);
             }
             const float bj = bet[16 * b + jc];
-            __half* xd = reinterpret_cast<__half*>(sX16) + b * 16 * kX16Ld + jc;
             const int col = 16 * b + jc;
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                xd[i * kX16Ld] = __float2half_rn(xv[i]);
+                *reinterpret_cast<__half*>(sX16 + blk_off(b, i, jc)) = __float2half_rn(xv[i]);
                 *reinterpret_cast<__half*>(sTB + tc::h_off(16 * b + i, col >> 3) + (col & 7) * 2) =
                     __float2half_rn(xv[i] * bj);
             }
@@ -625,7 +648,7 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int c = b; c < a; ++c) {
                     uint32_t af[4], bfr[2];
-                    ldsm_x4(af, sA16 + ((16 * a + (lane & 15)) * kA16Ld + 16 * c + (lane >> 4) * 8) * 2);
+                    ldsm_x4(af, sA16 + blk_off(low_blk(a, c), lane & 15, (lane >> 4) * 8));
                     ldsm_x2_trans(bfr, sTB + tc::h_off(16 * c + (lane & 15), 2 * b + nh));
                     mma16816(acc, af, bfr);
                 }
@@ -634,7 +657,7 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
                 yw[(gq + 8) * 4 + t4] = tc::pack_h2(acc[2], acc[3]);
                 __syncwarp();
                 uint32_t xf[4], yf[2];
-                ldsm_x4(xf, sX16 + ((a * 16 + (lane & 15)) * kX16Ld + (lane >> 4) * 8) * 2);
+                ldsm_x4(xf, sX16 + blk_off(a, lane & 15, (lane >> 4) * 8));
                 ldsm_x2_trans(yf, sY + warp * 256 + (lane & 15) * 16);
                 float o[4] = {0.f, 0.f, 0.f, 0.f};
                 mma16816(o, xf, yf);
@@ -649,7 +672,7 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
         fence_proxy_async_smem();
         tc::fence_before();
         __syncthreads();
-        if (tid == 0) {  // [T'; PT'] = [I; P] T' (M = 128, N = 64, K = 64)
+        if (tid == 0) {  // [T'; PT'] = [I; P] T' (M = 128, N = 64, K = 64) into columns 64..127
             tc::fence_after();
             if (ok) {
                 const uint32_t a0 = tc::smem_addr(sIP), b0 = tc::smem_addr(sTB);
@@ -660,84 +683,75 @@ __global__ void __launch_bounds__(P_THREADS, 2) k_prep16(const __grid_constant__
             }
             tc::commit(mbar);
         }
-        // V of this v-head while the product runs (the pair's rows were staged earlier)
-        if ((jj & 1) == 0) {
-            cp_async_wait_all();
-            __syncthreads();
-            v_conv(0, j);
-        }
         wait_mma();
         {  // [T'; PT'] -> the record tile (K-major [128][64]); -[T'; PT'] diag(e^gamma) -> WA
             const int r = 32 * q4 + lane;
-            float v[32];
-            tc::ld32(tc::taddr(tm, 32 * q4, 64 + hf * 32), v);
             unsigned char* rtp = rec + kRecTP;
+#pragma unroll 1
+            for (int hh = 0; hh < 2; ++hh) {
+                float v[16];
+                tc::ld16(tc::taddr(tm, 32 * q4, 64 + hf * 32 + 16 * hh), v);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int cc = 4 * hf + k;
-                float2 p2[4], s2[4];
-                const float4 e0 = *reinterpret_cast<const float4*>(eg + 8 * cc);
-                const float4 e1 = *reinterpret_cast<const float4*>(eg + 8 * cc + 4);
-                const float2 en[4] = {make_float2(-e0.x, -e0.y), make_float2(-e0.z, -e0.w), make_float2(-e1.x, -e1.y),
-                                      make_float2(-e1.z, -e1.w)};
+                for (int k = 0; k < 2; ++k) {
+                    const int cc = 4 * hf + 2 * hh + k;
+                    float2 p2[4], s2[4];
+                    const float4 e0 = *reinterpret_cast<const float4*>(eg + 8 * cc);
+                    const float4 e1 = *reinterpret_cast<const float4*>(eg + 8 * cc + 4);
+                    const float2 en[4] = {make_float2(-e0.x, -e0.y), make_float2(-e0.z, -e0.w),
+                                          make_float2(-e1.x, -e1.y), make_float2(-e1.z, -e1.w)};
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    p2[c] = make_float2(v[8 * k + 2 * c], v[8 * k + 2 * c + 1]);
-                    s2[c] = __fmul2_rn(p2[c], en[c]);
+                    for (int c = 0; c < 4; ++c) {
+                        p2[c] = make_float2(v[8 * k + 2 * c], v[8 * k + 2 * c + 1]);
+                        s2[c] = __fmul2_rn(p2[c], en[c]);
+                    }
+                    *reinterpret_cast<uint4*>(rtp + tc::h_off(r, cc)) = pack8x2(p2);
+                    *reinterpret_cast<uint4*>(sWA + tc::h_off(r, cc)) = pack8x2(s2);
+                    // the second atom (columns 64..127): zero, with e^gamma_t at column t of row 64 + t
+                    uint32_t dw = 0u;
+                    if (r >= C && ((r - C) >> 3) == cc) {
+                        const uint32_t hb = __half_as_ushort(__float2half_rn(eg[r - C]));
+                        dw = ((r - C) & 1) ? (hb << 16) : hb;
+                    }
+                    const int wsel = ((r - C) & 7) >> 1;
+                    *reinterpret_cast<uint4*>(sWA + 16384 + tc::h_off(r, cc)) =
+                        make_uint4(wsel == 0 ? dw : 0u, wsel == 1 ? dw : 0u, wsel == 2 ? dw : 0u, wsel == 3 ? dw : 0u);
                 }
-                *reinterpret_cast<uint4*>(rtp + tc::h_off(r, cc)) = pack8x2(p2);
-                *reinterpret_cast<uint4*>(sWA + tc::h_off(r, cc)) = pack8x2(s2);
-                // the second atom (columns 64..127): zero, with e^gamma_t at column t of row 64 + t
-                uint32_t dw = 0u;
-                if (r >= C && ((r - C) >> 3) == cc) {
-                    const uint32_t hb = __half_as_ushort(__float2half_rn(eg[r - C]));
-                    dw = ((r - C) & 1) ? (hb << 16) : hb;
-                }
-                const int wsel = ((r - C) & 7) >> 1;
-                *reinterpret_cast<uint4*>(sWA + 16384 + tc::h_off(r, cc)) =
-                    make_uint4(wsel == 0 ? dw : 0u, wsel == 1 ? dw : 0u, wsel == 2 ? dw : 0u, wsel == 3 ? dw : 0u);
             }
         }
         fence_proxy_async_smem();
         tc::fence_before();
         __syncthreads();
-        if (tid == 0) {  // [-W; Q'] = WA [K^; Q^] (M = 128, N = 128, K = 128)
+        if (tid == 0) {  // [-W; Q'] = WA [K^; Q^] (M = 128, N = 128, K = 128) into columns 0..127
             tc::fence_after();
             if (ok) {
                 const uint32_t a0 = tc::smem_addr(sWA), b0 = tc::smem_addr(sKQ);
                 for (int s = 0; s < 2 * C / 16; ++s)
-                    tc::mma_f16(tm + 128, tc::sdesc_lbo(a0 + (uint32_t)((s >> 2) * 16384 + (s & 3) * 32), 16),
+                    tc::mma_f16(tm, tc::sdesc_lbo(a0 + (uint32_t)((s >> 2) * 16384 + (s & 3) * 32), 16),
                                 tc::sdesc_lbo(b0 + (uint32_t)(s * 2048), 16384),
                                 tc::idesc_f16(128, 128, false, true), s > 0 ? 1u : 0u);
             }
             tc::commit(mbar);
         }
-        // the pair's second V while this product runs; then the next pair's rows
-        if ((jj & 1) == 0) {
-            if (jj + 1 < G) v_conv(1, j + 1);
-            if (jj + 2 < G) {
-                __syncthreads();  // every thread is done with the staged rows
-                stage_pair(jj / 2 + 1);
-            }
-        }
         wait_mma();
         {  // [-W; Q'] -> the record (K-major [128][128], atoms of 128 rows), from registers
             const int r = 32 * q4 + lane;
             unsigned char* aop = rec + hf * 16384;
+#pragma unroll 1
+            for (int b = 0; b < 4; ++b) {
+                float v[16];
+                tc::ld16(tc::taddr(tm, 32 * q4, hf * 64 + 16 * b), v);
 #pragma unroll
-            for (int b = 0; b < 2; ++b) {
-                float v[32];
-                tc::ld32(tc::taddr(tm, 32 * q4, 128 + hf * 64 + 32 * b), v);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
+                for (int k = 0; k < 2; ++k) {
                     float2 p2[4];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) p2[c] = make_float2(v[8 * k + 2 * c], v[8 * k + 2 * c + 1]);
-                    *reinterpret_cast<uint4*>(aop + tc::h_off(r, 4 * b + k)) = pack8x2(p2);
+                    *reinterpret_cast<uint4*>(aop + tc::h_off(r, 2 * b + k)) = pack8x2(p2);
                 }
             }
         }
         tc::fence_before();
+        __syncthreads();  // the columns are read before the next Gram, the scratch before the next staging
+        if (jj + 1 < G) issue_gram();
     }
     if (tid == 0) bulk_wait_read_all();
     if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
