@@ -574,6 +574,8 @@ def profile_case(args):
                                   clustered=os.environ.get("GDN_DECODE_CLUSTERED", "auto"))))
     elif args.case == "serving":
         print(json.dumps(serving_measure(torch, device, args.steps, args.warmup)))
+    elif args.case == "prefill-varlen":
+        print(json.dumps(varlen_prefill_case(torch, device, args.steps, args.warmup)))
     elif args.case == "ckpt":
         print(json.dumps(ckpt_measure(torch, device, args.steps, args.warmup)))
     elif args.case == "proj-prefill":
@@ -596,6 +598,38 @@ def profile_case(args):
         t, _, _ = prefill_measure(torch, device, args.steps, args.warmup, seed=0, check=False, e2e=False)
         print(json.dumps({"case": args.case, "ms_per_call": round(1e3 * t, 4)}))
     return 0
+
+
+def varlen_prefill_case(torch, device, steps, warmup, n_seq=4, T=2048):
+    """One varlen prefill of n_seq x T tokens (16/32 heads, d = 128): the prep kernel
+    runs as one launch over all chunks (no segments), for ncu captures."""
+    from hybrid_gated_deltanet_gb300 import binding as gb
+    from hybrid_gated_deltanet_gb300 import synth
+    r = synth.rng_for(5, 0)
+    cfg = gb.Config(*GEOM_ARGS, chunk=64, act_dtype=gb.BF16)
+    p = synth.make_params(synth.QWEN35_4B, r, synth.BF16)
+    prm = gb.Params(conv_w=_dev(p["conv_w"], torch, device), A_log=_dev(p["A_log"], torch, device),
+                    norm_w=_dev(p["norm_w"], torch, device))
+    g = torch.Generator(device=device)
+    g.manual_seed(5)
+    bf = torch.bfloat16
+    N = n_seq * T
+    x = torch.randn((N, 8192), generator=g, device=device).to(bf)
+    z = torch.randn((N, 4096), generator=g, device=device).to(bf)
+    a = torch.randn((N, 32), generator=g, device=device).to(bf)
+    b = torch.randn((N, 32), generator=g, device=device).to(bf)
+    y = torch.empty((N, 4096), dtype=bf, device=device)
+    S = torch.zeros((n_seq, 32, 128, 128), device=device)
+    Cp = torch.zeros((n_seq, 3, 8192), dtype=bf, device=device)
+    cu = torch.arange(0, N + 1, T, dtype=torch.int32, device=device)
+    sl = torch.arange(n_seq, dtype=torch.int32, device=device)
+    ws = torch.empty(gb.gdn_workspace_size(cfg, gb.OP_VARLEN_PREFILL, N, n_seq), dtype=torch.uint8, device=device)
+    stream = _side_stream(torch)
+    with torch.cuda.stream(stream):
+        for _ in range(warmup + steps):
+            gb.gdn_varlen_prefill(cfg, prm, x, z, a, b, cu, sl, None, Cp, S, y, ws, stream=stream)
+    torch.cuda.synchronize()
+    return {"case": "prefill-varlen", "n_seq": n_seq, "tokens_each": T, "launches": warmup + steps}
 
 
 def proj_prefill_case(torch, device, steps, warmup, T=8192):
@@ -1293,7 +1327,8 @@ def main():
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--batch", type=int, default=64, help="slots of the decode-small case")
-    ap.add_argument("--case", default="full", choices=["full", "decode-small", "decode-batches", "prefill-small", "serving",
+    ap.add_argument("--case", default="full", choices=["full", "decode-small", "decode-batches", "prefill-small",
+                             "prefill-varlen", "serving",
                              "verify", "ckpt", "layer",
                              "proj-decode", "attn", "proj-prefill", "attn-small"],
                     help="small cases for ncu captures")
