@@ -88,7 +88,9 @@ struct ProjArgs {
     int32_t n_out, k;
     int64_t n_tok;
     int32_t tiles_n;  // 128-row weight blocks
-    int64_t n_tiles;  // tiles_n x token blocks
+    int32_t tiles_t;  // token blocks
+    int32_t token_fast;  // tile order: token blocks fastest (1) or weight blocks fastest (0)
+    int64_t n_tiles;  // tiles_n x tiles_t
     int32_t kb;       // 64-wide K blocks
     int32_t ks;       // K split over ks CTAs per tile (1: persistent grid, no split)
     float* part;      // split: fp32 partial blocks [tile][rank][bt columns][128 rows]
@@ -96,6 +98,21 @@ struct ProjArgs {
     int32_t nseg;
     ProjSeg seg[4];
 };
+
+// tile -> (weight block, token block).  The tiles in flight on the grid sweep the
+// fastest index while sharing a few blocks of the other, so the operand of the
+// fastest index is re-read once per sweep and must stay in L2: the smaller operand
+// goes fastest.  Measured on the 8192-token in-projection (weights 63 MB, tokens
+// 42 MB): weight-fastest order read 477 MB from DRAM, token-fastest 121 MB.
+__device__ __forceinline__ void tile_coords(const ProjArgs& P, int64_t tile, int& wn, int& tt) {
+    if (P.token_fast) {
+        wn = (int)(tile / P.tiles_t);
+        tt = (int)(tile % P.tiles_t);
+    } else {
+        wn = (int)(tile % P.tiles_n);
+        tt = (int)(tile / P.tiles_n);
+    }
+}
 
 template <int BT, int STAGES, int KBOX>
 __global__ void __launch_bounds__(kPjThreads, 2)
@@ -145,8 +162,8 @@ __global__ void __launch_bounds__(kPjThreads, 2)
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&ta)) : "memory");
             uint32_t it = 0;
             for (int64_t tile = tile0; tile < P.n_tiles && ok; tile += tstep) {
-                const int wn = (int)(tile % P.tiles_n);
-                const int tt = (int)(tile / P.tiles_n);
+                int wn, tt;
+                tile_coords(P, tile, wn, tt);
                 for (int kb = kb0; kb < kb1; kb += KBOX, ++it) {
                     const int s = (int)(it % STAGES);
                     if (!mbar_wait(empty + s, ((it / STAGES) & 1u) ^ 1u)) {
@@ -205,8 +222,8 @@ __global__ void __launch_bounds__(kPjThreads, 2)
         uint32_t use = 0;
         for (int64_t tile = tile0; tile < P.n_tiles; tile += tstep, ++use) {
             const uint32_t buf = use & 1u;
-            const int wn = (int)(tile % P.tiles_n);
-            const int tt = (int)(tile / P.tiles_n);
+            int wn, tt;
+            tile_coords(P, tile, wn, tt);
             const bool w = mbar_wait(acc_full + buf, (use >> 1) & 1u);
             ok = ok && w;
             if (!__all_sync(0xffffffffu, w)) break;
@@ -252,7 +269,9 @@ __global__ void __launch_bounds__(kPjThreads, 2)
         // last token are skipped
         const int q4 = warp & 3;
         const int row = 32 * q4 + lane;
-        const int tt = (int)(tile0 / P.tiles_n);
+        int wn0, tt;
+        tile_coords(P, tile0, wn0, tt);
+        (void)wn0;
         const int64_t t0 = (int64_t)tt * BT;
         const int ncol = (int)((P.n_tok - t0) < BT ? (P.n_tok - t0) : BT);
         float* dst = P.part + ((size_t)tile0 * P.ks + rank) * BT * kBM + row;
@@ -315,8 +334,9 @@ __global__ void __launch_bounds__(32 * kRedWarps) k_proj_reduce(const __grid_con
     const int64_t tile = item / BT;
     const int c = (int)(item % BT);
     if (tile >= P.n_tiles) return;
-    const int wn = (int)(tile % P.tiles_n);
-    const int64_t t = (tile / P.tiles_n) * BT + c;
+    int wn, tt;
+    tile_coords(P, tile, wn, tt);
+    const int64_t t = (int64_t)tt * BT + c;
     if (t >= P.n_tok) return;
     const float4* src = reinterpret_cast<const float4*>(P.part + ((size_t)tile * P.ks * BT + c) * kBM) + lane;
     const size_t rstride = (size_t)BT * kBM / 4;  // float4s between ranks
@@ -419,6 +439,8 @@ cudaError_t launch_proj(const ProjJob& job, cudaStream_t st) {
     P.k = job.k;
     P.n_tok = job.n_tok;
     P.tiles_n = (job.n_out + kBM - 1) / kBM;
+    P.tiles_t = (int32_t)((job.n_tok + plan.bt - 1) / plan.bt);
+    P.token_fast = job.n_tok < job.n_out ? 1 : 0;  // the token operand is the smaller one
     P.kb = (job.k + kBK - 1) / kBK;
     P.n_tiles = plan.n_tiles;
     P.ks = plan.ks;
