@@ -582,6 +582,8 @@ def profile_case(args):
         print(json.dumps(proj_prefill_case(torch, device, args.steps, args.warmup)))
     elif args.case == "attn-small":
         print(json.dumps(attn_small_case(torch, device, args.steps, args.warmup)))
+    elif args.case == "attn-wide":
+        print(json.dumps(attn_wide_case(torch, device, args.steps, args.warmup)))
     elif args.case == "attn":
         for rec in attn_measure(torch, device, args.steps, args.warmup):
             print(json.dumps(rec))
@@ -646,6 +648,32 @@ def proj_prefill_case(torch, device, steps, warmup, T=8192):
         gb.gdn_proj_gemm(h, w, u)
     torch.cuda.synchronize()
     return {"case": "proj-prefill", "tokens": T, "launches": warmup + steps}
+
+
+def attn_wide_case(torch, device, steps, warmup):
+    """Wide-GQA decode attention alone (24 query / 2 kv-heads of 256, pages of 528,
+    4 sequences x 32768 cached tokens: 268 MB of K and V); warmup + steps calls, for
+    ncu captures."""
+    from hybrid_gated_deltanet_gb300 import binding as gb
+    g = torch.Generator(device=device)
+    g.manual_seed(14)
+    bf = torch.bfloat16
+    cfg = gb.AttnConfig(24, 2, 256, 528)
+    B, L = 4, 32768
+    per = (L + 1 + 527) // 528
+    kp = torch.randn((B * per, 2, 528, 256), generator=g, device=device).to(bf)
+    vp = torch.randn((B * per, 2, 528, 256), generator=g, device=device).to(bf)
+    table = torch.randperm(B * per, generator=g, device=device).to(torch.int32).view(B, per)
+    lens = torch.full((B,), L, dtype=torch.int32, device=device)
+    q = torch.randn((B, 24, 256), generator=g, device=device).to(bf)
+    kn = torch.randn((B, 2, 256), generator=g, device=device).to(bf)
+    o = torch.empty((B, 24, 256), dtype=bf, device=device)
+    ws = torch.empty(max(16, gb.gdn_attn_workspace_size(cfg, B, L + 1)), dtype=torch.uint8, device=device)
+    torch.cuda.synchronize()
+    for _ in range(warmup + steps):
+        gb.gdn_attn_decode(cfg, q, kn, kn, kp, vp, table, lens, L + 1, o, ws)
+    torch.cuda.synchronize()
+    return {"case": "attn-wide", "launches": warmup + steps}
 
 
 def attn_small_case(torch, device, steps, warmup):
@@ -1330,7 +1358,7 @@ def main():
     ap.add_argument("--case", default="full", choices=["full", "decode-small", "decode-batches", "prefill-small",
                              "prefill-varlen", "serving",
                              "verify", "ckpt", "layer",
-                             "proj-decode", "attn", "proj-prefill", "attn-small"],
+                             "proj-decode", "attn", "proj-prefill", "attn-small", "attn-wide"],
                     help="small cases for ncu captures")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--cpu-prefill-tokens", type=int, default=8192)

@@ -46,7 +46,8 @@ struct AttnArgs {
     const int32_t* seq_lens;     // [B] tokens in the cache before this step
     __nv_bfloat16* o;            // [B][Hq][D]
     float* part;                 // [B][Hq][n_split][D + 2]: unnormalised o, max, sum
-    int B, Hq, Hkv, page, max_pages, n_pages, n_split, span;  // span: tokens per split (multiple of kTJ)
+    int B, Hq, Hkv, page, max_pages, n_pages, n_split, span;  // span: tokens per split (multiple of 16)
+    int box_rows;  // tensor-core kernel: page rows per K/V box, gcd(page, 16)
     float scale;
 };
 
@@ -363,15 +364,433 @@ cudaError_t launch_decode(const AttnArgs& A, cudaStream_t st) {
     return launch_pdl(k_attn_combine<D>, dim3((unsigned)A.Hq, (unsigned)A.B), dim3(D), 0, st, A);
 }
 
-// query heads per kv-head G: 1 or 2 in one CTA, multiples of 4 in CTAs of 4
-// heads (the kv-head's K and V are then read by G/4 CTAs side by side, the
-// later reads mostly from L2)
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn();
+
+// ---- tensor-core decode for wide groups (8 to 16 query heads per kv-head) ---------
+// One CTA per (context split, kv-head, sequence) scores all G heads of the kv-head at
+// once, so K and V are read once: the heads are the 16 rows (zero past G) of warp-level
+// bf16 MMAs (m16n8k16, fp32 accumulation).  The split's tokens come in groups of 16
+// and warp w takes groups w, w + 4, ... whole: S = Q K^T, an online softmax per row in
+// registers, O += P V over all d columns with P as the A operand straight from the
+// score accumulators.  Each warp fills its own ring of NSW stages (16 K rows, then 16
+// V rows): a group is one or two runs of rows of a page (splits start on multiples of
+// 16 tokens, pages hold a multiple of 8), each run loaded by tensor TMA in boxes of
+// 64 columns with the 128-byte swizzle, so the 8-row fragment loads are free of bank
+// conflicts; the page of a run is fetched one group before its copy.  The four warps'
+// (maximum, sum, O) are merged once at the end through shared memory.  The new token L
+// (its row in the pool is written by this launch) is added from k_new / v_new by
+// warp 0 of the split that holds it.
+__device__ __forceinline__ void ldsm_x4_b16(uint32_t r[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(tc::smem_addr(p)));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans_b16(uint32_t r[4], const void* p) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(tc::smem_addr(p)));
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};\n"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf2(float a, float b) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);  // a in the low half
+    uint32_t u;
+    memcpy(&u, &h, 4);
+    return u;
+}
+
+template <int D>
+struct AtTcLay {
+    static constexpr int NCH = D / 64;         // 128-byte column chunks of a row
+    static constexpr int TILE = NCH * 2048;    // 16 rows of K (or V): chunk-major, 128-byte swizzled
+    static constexpr int STAGE = 2 * TILE;     // K tile, then V tile
+    static constexpr int NSW = 3;              // stages per warp
+    static constexpr int NST = 4 * NSW;
+    static constexpr int QS = D * 2 + 16;      // padded row stride of Q (bytes)
+    static constexpr int Q_OFF = NST * STAGE;  // Q of the 16 rows, scaled, bf16
+    static constexpr int BAR_OFF = Q_OFF + 16 * QS;
+    static constexpr int SMEM = BAR_OFF + NST * 8 + NST * 4;  // + mbarriers, token masks
+    static constexpr int SMEM_ALLOC = SMEM + 1024;             // base rounded up to a swizzle atom
+    // the merge overlays the rings: per warp 16 rows of O (OS floats) and (m, l) per row
+    static constexpr int OS = D + 4;
+    static_assert(4 * 16 * OS * 4 + 4 * 16 * 2 * 4 <= NST * STAGE, "merge area");
+    static_assert(SMEM_ALLOC <= 227 * 1024, "shared memory");
+};
+
+template <int D>
+__global__ void __launch_bounds__(128, 1)
+    k_attn_decode_tc(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                     const __grid_constant__ AttnArgs A) {
+    using Lay = AtTcLay<D>;
+    constexpr int KS = D / 16;  // k-steps of Q K^T
+    constexpr int NT = D / 8;   // n8 tiles of O
+    constexpr int NSW = Lay::NSW;
+    static_assert(KS % 2 == 0, "k-steps in pairs");
+    griddep_wait();  // launched with programmatic serialization
+    griddep_launch_dependents();
+    const int G = A.Hq / A.Hkv;
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int h0 = kvh * G;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gq = lane >> 2, t4 = lane & 3;
+    const int L = A.seq_lens[b];  // cached tokens; the new one is token L
+    if (L < 0 || L >= A.max_pages * A.page) return;  // nothing to read or write for b
+    const int n_tok = L + 1;
+    const int t_begin = split * A.span;
+    const int t_end = min(n_tok, t_begin + A.span);
+    const int lim = min(t_end, L);  // tokens from the pool: t_begin .. lim - 1
+    const int n_groups = lim > t_begin ? (lim - t_begin + 15) / 16 : 0;
+    const int my_groups = n_groups > warp ? (n_groups - warp + 3) / 4 : 0;  // groups warp, warp + 4, ...
+
+    extern __shared__ __align__(128) unsigned char at_dyn[];
+    unsigned char* at_smem = at_dyn + ((1024u - (smem_u32(at_dyn) & 1023u)) & 1023u);
+    unsigned char* ring = at_smem + warp * NSW * Lay::STAGE;
+    unsigned char* q_s = at_smem + Lay::Q_OFF;
+    uint64_t* full = reinterpret_cast<uint64_t*>(at_smem + Lay::BAR_OFF) + warp * NSW;
+    volatile uint32_t* smask = reinterpret_cast<uint32_t*>(at_smem + Lay::BAR_OFF + Lay::NST * 8) + warp * NSW;
+    const int R = A.box_rows, n_seg = 16 / R;  // runs of page rows per group
+
+    // the new token's K and V go to the pool (every reader takes token L from k_new / v_new)
+    if (split == A.n_split - 1 && tid < D / 8) {
+        const int pg = L / A.page;
+        const int page_id = (pg < A.max_pages) ? A.block_table[(size_t)b * A.max_pages + pg] : -1;
+        if (page_id >= 0 && page_id < A.n_pages) {
+            const size_t dst = (((size_t)page_id * A.Hkv + kvh) * A.page + L % A.page) * D + tid * 8;
+            const size_t src = ((size_t)b * A.Hkv + kvh) * D + tid * 8;
+            *reinterpret_cast<uint4*>(A.k_pool + dst) = *reinterpret_cast<const uint4*>(A.k_new + src);
+            *reinterpret_cast<uint4*>(A.v_pool + dst) = *reinterpret_cast<const uint4*>(A.v_new + src);
+        }
+    }
+    // Q of the G heads, scaled in fp32 and rounded to bf16; rows past G are zero
+    for (int i = tid; i < 16 * (D / 8); i += 128) {
+        const int r = i / (D / 8), c = i % (D / 8);
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (r < G) {
+            const uint4 raw = *reinterpret_cast<const uint4*>(A.q + ((size_t)b * A.Hq + h0 + r) * D + 8 * c);
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+            float2 f = __bfloat1622float2(h[0]);
+            u.x = pack_bf2(f.x * A.scale, f.y * A.scale);
+            f = __bfloat1622float2(h[1]);
+            u.y = pack_bf2(f.x * A.scale, f.y * A.scale);
+            f = __bfloat1622float2(h[2]);
+            u.z = pack_bf2(f.x * A.scale, f.y * A.scale);
+            f = __bfloat1622float2(h[3]);
+            u.w = pack_bf2(f.x * A.scale, f.y * A.scale);
+        }
+        *reinterpret_cast<uint4*>(q_s + r * Lay::QS + 16 * c) = u;
+    }
+    if (lane == 0) {
+        for (int s = 0; s < NSW; ++s) mbar_init(full + s, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    // token t of the pool: its page, or -1 (outside the cache or the pool)
+    auto page_of = [&](int t) -> int {
+        if (t < t_begin || t >= lim) return -1;
+        const int pg = t / A.page;
+        const int pid = (pg < A.max_pages) ? __ldg(A.block_table + (size_t)b * A.max_pages + pg) : -1;
+        return (pid >= 0 && pid < A.n_pages) ? pid : -1;
+    };
+    // lane l < n_seg: run l (rows l R .. l R + R - 1) of this warp's j-th group; a run
+    // whose first token is in the pool is loaded whole (its rows past lim lie on the
+    // same page and are masked)
+    auto row_page = [&](int j) -> int {
+        return lane < n_seg ? page_of(t_begin + 16 * (warp + 4 * j) + lane * R) : -1;
+    };
+    auto issue = [&](int j, int pid) {
+        const int s = j % NSW, t0 = t_begin + 16 * (warp + 4 * j);
+        const unsigned live = __ballot_sync(0xffffffffu, pid >= 0);
+        if (lane == 0) {
+            const unsigned runs = (R == 16) ? ((live & 1u) ? 0xffffu : 0u)
+                                            : (((live & 1u) ? 0x00ffu : 0u) | ((live & 2u) ? 0xff00u : 0u));
+            const int nv = lim - t0;  // tokens of the group before lim (at least 1)
+            smask[s] = nv >= 16 ? runs : (runs & ((1u << nv) - 1u));  // tokens of the group to score
+            const uint32_t bytes = (uint32_t)__popc(live) * (uint32_t)(2 * Lay::NCH * R * 128);
+            if (bytes) mbar_arrive_expect_tx(full + s, bytes);
+            else asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(full + s)) : "memory");
+        }
+        __syncwarp();
+        if (pid >= 0) {
+            const int y = (t0 + lane * R) % A.page;
+            unsigned char* kt = ring + s * Lay::STAGE + lane * R * 128;
+#pragma unroll
+            for (int ch = 0; ch < Lay::NCH; ++ch) {
+                tma_load_4d(kt + ch * 2048, &tk, 64 * ch, y, kvh, pid, full + s);
+                tma_load_4d(kt + Lay::TILE + ch * 2048, &tv, 64 * ch, y, kvh, pid, full + s);
+            }
+        }
+    };
+    {
+        int pid0[NSW];
+#pragma unroll
+        for (int j = 0; j < NSW; ++j) pid0[j] = j < my_groups ? row_page(j) : -1;
+#pragma unroll
+        for (int j = 0; j < NSW; ++j)
+            if (j < my_groups) issue(j, pid0[j]);
+    }
+    int pf = NSW < my_groups ? row_page(NSW) : -1;  // the page of the next copy, one group ahead
+
+    float o[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows gq, gq + 8
+    bool ok = true;
+    const unsigned char* qb = q_s + (lane & 15) * Lay::QS + (lane >> 4) * 16;
+    // A tile as TMA writes it with the 128-byte swizzle: 16-byte unit u of row r sits in
+    // chunk u / 8 (2 KB each), row r (128 bytes), at unit (u % 8) ^ (r % 8).  Per-lane
+    // parts of the fragment addresses: K row (lane & 7) + 8 (lane >> 4) at unit
+    // 2 ks + ((lane >> 3) & 1); V row lane & 15 at unit n + (lane >> 4) for even n.
+    const int k_row = (lane & 7) + ((lane >> 4) << 3), k_x = ((lane >> 3) & 1) ^ (lane & 7);
+    const int v_row = lane & 15, v_x = (lane >> 4) ^ (lane & 7);
+
+    for (int j = 0; j < my_groups; ++j) {
+        const int s = j % NSW;
+        unsigned char* st = ring + s * Lay::STAGE;
+        ok = mbar_wait(full + s, (uint32_t)((j / NSW) & 1)) && ok;
+        // rows never loaded hold anything: their scores are masked, their V rows zeroed
+        const unsigned valid = smask[s];
+        if (valid != 0xffffu) {
+            for (int i = lane; i < 16 * (D / 8); i += 32) {  // whole rows: the swizzle does not matter
+                const int r = i / (D / 8), c = i % (D / 8);
+                if (!((valid >> r) & 1u))
+                    *reinterpret_cast<uint4*>(st + Lay::TILE + (c >> 3) * 2048 + r * 128 + (c & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+        // S = Q K^T: tokens 0..7 and 8..15, even and odd k-steps apart (shorter chains)
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+        float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const unsigned char* kb = st + k_row * 128;
+#pragma unroll
+            for (int ks = 0; ks < KS; ks += 2) {
+                uint32_t qa[4], qc[4], bk[4], bl[4];
+                ldsm_x4_b16(qa, qb + ks * 32);
+                ldsm_x4_b16(bk, kb + (ks >> 2) * 2048 + (((2 * ks) & 7) ^ k_x) * 16);
+                ldsm_x4_b16(qc, qb + ks * 32 + 32);
+                ldsm_x4_b16(bl, kb + ((ks + 1) >> 2) * 2048 + (((2 * ks + 2) & 7) ^ k_x) * 16);
+                mma_bf16_16816(sa, qa, bk[0], bk[1]);
+                mma_bf16_16816(sb, qa, bk[2], bk[3]);
+                mma_bf16_16816(sc, qc, bl[0], bl[1]);
+                mma_bf16_16816(sd, qc, bl[2], bl[3]);
+            }
+        }
+        // online softmax per row (a quad holds a row's 16 scores)
+        const int j0 = 2 * t4, j1 = 8 + 2 * t4;
+        auto pick = [&](int t, float x) { return ((valid >> t) & 1u) ? x : -INFINITY; };
+        const float v00 = pick(j0, sa[0] + sc[0]), v01 = pick(j0 + 1, sa[1] + sc[1]);
+        const float v02 = pick(j1, sb[0] + sd[0]), v03 = pick(j1 + 1, sb[1] + sd[1]);
+        const float v10 = pick(j0, sa[2] + sc[2]), v11 = pick(j0 + 1, sa[3] + sc[3]);
+        const float v12 = pick(j1, sb[2] + sd[2]), v13 = pick(j1 + 1, sb[3] + sd[3]);
+        float mx0 = fmaxf(fmaxf(v00, v01), fmaxf(v02, v03)), mx1 = fmaxf(fmaxf(v10, v11), fmaxf(v12, v13));
+#pragma unroll
+        for (int off = 1; off < 4; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const bool moved = __any_sync(0xffffffffu, mn0 != m0 || mn1 != m1);
+        const float a0 = (m0 == -INFINITY) ? 0.f : __expf(m0 - mn0), a1 = (m1 == -INFINITY) ? 0.f : __expf(m1 - mn1);
+        auto ex = [](float v, float m) { return v == -INFINITY ? 0.f : __expf(v - m); };
+        const float p00 = ex(v00, mn0), p01 = ex(v01, mn0), p02 = ex(v02, mn0), p03 = ex(v03, mn0);
+        const float p10 = ex(v10, mn1), p11 = ex(v11, mn1), p12 = ex(v12, mn1), p13 = ex(v13, mn1);
+        float ps0 = p00 + p01 + p02 + p03, ps1 = p10 + p11 + p12 + p13;
+#pragma unroll
+        for (int off = 1; off < 4; off <<= 1) {
+            ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
+            ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
+        }
+        l0 = l0 * a0 + ps0;
+        l1 = l1 * a1 + ps1;
+        m0 = mn0;
+        m1 = mn1;
+        if (moved) {  // a row's maximum grew somewhere in the warp: rescale O
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                o[n][0] *= a0;
+                o[n][1] *= a0;
+                o[n][2] *= a1;
+                o[n][3] *= a1;
+            }
+        }
+        // O += P V, P as the A operand (rows gq, gq + 8; k = the 16 tokens)
+        const uint32_t pa[4] = {pack_bf2(p00, p01), pack_bf2(p10, p11), pack_bf2(p02, p03), pack_bf2(p12, p13)};
+        {
+            const unsigned char* vb = st + Lay::TILE + v_row * 128;
+#pragma unroll
+            for (int n = 0; n < NT; n += 2) {
+                uint32_t bv[4];
+                ldsm_x4_trans_b16(bv, vb + (n >> 3) * 2048 + ((n & 7) ^ v_x) * 16);
+                mma_bf16_16816(o[n], pa, bv[0], bv[1]);
+                mma_bf16_16816(o[n + 1], pa, bv[2], bv[3]);
+            }
+        }
+        // the stage is read (and its V rows written) by this warp: refill it
+        __syncwarp();
+        if (j + NSW < my_groups) {
+            fence_proxy_async_smem();
+            issue(j + NSW, pf);
+            pf = j + NSW + 1 < my_groups ? row_page(j + NSW + 1) : -1;
+        }
+    }
+
+    // the new token L, from k_new / v_new, by warp 0 of the split that holds it
+    if (warp == 0 && L >= t_begin && L < t_end) {
+        const __nv_bfloat16* kn = A.k_new + ((size_t)b * A.Hkv + kvh) * D;
+        const __nv_bfloat16* vn = A.v_new + ((size_t)b * A.Hkv + kvh) * D;
+        float d0 = 0.f, d1 = 0.f;  // q . k_new for rows gq, gq + 8 over this lane's dims
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+            const int d = 8 * i + 2 * t4;
+            const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(kn + d));
+            const float2 f0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q_s + gq * Lay::QS + 2 * d));
+            const float2 f1 =
+                __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(q_s + (gq + 8) * Lay::QS + 2 * d));
+            d0 = fmaf(f0.x, kf.x, fmaf(f0.y, kf.y, d0));
+            d1 = fmaf(f1.x, kf.x, fmaf(f1.y, kf.y, d1));
+        }
+#pragma unroll
+        for (int off = 1; off < 4; off <<= 1) {
+            d0 += __shfl_xor_sync(0xffffffffu, d0, off);
+            d1 += __shfl_xor_sync(0xffffffffu, d1, off);
+        }
+        const float mn0 = fmaxf(m0, d0), mn1 = fmaxf(m1, d1);
+        const float a0 = (m0 == -INFINITY) ? 0.f : __expf(m0 - mn0), a1 = (m1 == -INFINITY) ? 0.f : __expf(m1 - mn1);
+        const float pn0 = __expf(d0 - mn0), pn1 = __expf(d1 - mn1);
+        l0 = l0 * a0 + pn0;
+        l1 = l1 * a1 + pn1;
+        m0 = mn0;
+        m1 = mn1;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const float2 vf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vn + 8 * n + 2 * t4));
+            o[n][0] = fmaf(pn0, vf.x, o[n][0] * a0);
+            o[n][1] = fmaf(pn0, vf.y, o[n][1] * a0);
+            o[n][2] = fmaf(pn1, vf.x, o[n][2] * a1);
+            o[n][3] = fmaf(pn1, vf.y, o[n][3] * a1);
+        }
+    }
+
+    // ---- merge of the four warps (over the rings, all copies landed) and out --------
+    if (__syncthreads_or(!ok)) {  // a wait gave up: copies may still land in the rings
+        if (tid == 0) report_device_status(kDevWaitTimeout);
+        return;
+    }
+    float* ob = reinterpret_cast<float*>(at_smem);          // [warp][16][OS]
+    float* ml = ob + 4 * 16 * Lay::OS;                      // [warp][16][2]: maximum, sum
+    {
+        float* w0 = ob + (warp * 16 + gq) * Lay::OS + 2 * t4;
+        float* w1 = w0 + 8 * Lay::OS;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            *reinterpret_cast<float2*>(w0 + 8 * n) = make_float2(o[n][0], o[n][1]);
+            *reinterpret_cast<float2*>(w1 + 8 * n) = make_float2(o[n][2], o[n][3]);
+        }
+        if (t4 == 0) {
+            ml[(warp * 16 + gq) * 2] = m0;
+            ml[(warp * 16 + gq) * 2 + 1] = l0;
+            ml[(warp * 16 + gq + 8) * 2] = m1;
+            ml[(warp * 16 + gq + 8) * 2 + 1] = l1;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < G * (D / 2); i += 128) {
+        const int r = i / (D / 2), c = 2 * (i % (D / 2));
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, ml[(w * 16 + r) * 2]);
+        float l = 0.f, ox = 0.f, oy = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float mw = ml[(w * 16 + r) * 2];
+            const float sw = (mw == -INFINITY) ? 0.f : __expf(mw - M);
+            const float2 v = *reinterpret_cast<const float2*>(ob + (w * 16 + r) * Lay::OS + c);
+            l = fmaf(sw, ml[(w * 16 + r) * 2 + 1], l);
+            ox = fmaf(sw, v.x, ox);
+            oy = fmaf(sw, v.y, oy);
+        }
+        const int h = h0 + r;
+        if (A.n_split == 1) {
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            *reinterpret_cast<__nv_bfloat162*>(A.o + ((size_t)b * A.Hq + h) * D + c) =
+                __floats2bfloat162_rn(ox * inv, oy * inv);
+        } else {
+            float* pr = A.part + (((size_t)b * A.Hq + h) * A.n_split + split) * (D + 2);
+            pr[c] = ox;
+            pr[c + 1] = oy;
+            if (c == 0) {
+                pr[D] = M;
+                pr[D + 1] = l;
+            }
+        }
+    }
+}
+
+template <int D>
+cudaError_t launch_decode_tc(const AttnArgs& A0, cudaStream_t st) {
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = raise_smem_limit(k_attn_decode_tc<D>, AtTcLay<D>::SMEM_ALLOC, smem_set);
+    if (e != cudaSuccess) return e;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = at_encode_fn();
+    if (!enc) return cudaErrorInvalidValue;
+    AttnArgs A = A0;
+    A.box_rows = (A.page % 16 == 0) ? 16 : 8;  // the page size is a multiple of 8
+    CUtensorMap mk, mv;
+    for (int w = 0; w < 2; ++w) {  // [n_pages][Hkv][page][D] bf16, boxes of box_rows x 64
+        const cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)A.page, (cuuint64_t)A.Hkv, (cuuint64_t)A.n_pages};
+        const cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)A.page * D * 2,
+                                       (cuuint64_t)A.Hkv * A.page * D * 2};
+        const cuuint32_t box[4] = {64, (cuuint32_t)A.box_rows, 1, 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(w == 0 ? &mk : &mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, w == 0 ? A.k_pool : A.v_pool, dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const dim3 grid((unsigned)A.n_split, (unsigned)A.Hkv, (unsigned)A.B);
+    e = launch_pdl(k_attn_decode_tc<D>, grid, dim3(128), AtTcLay<D>::SMEM_ALLOC, st, mk, mv, A);
+    if (e != cudaSuccess || A.n_split == 1) return e;
+    return launch_pdl(k_attn_combine<D>, dim3((unsigned)A.Hq, (unsigned)A.B), dim3(D), 0, st, A);
+}
+
+// query heads per kv-head G: 1 or 2 in one CTA of the CUDA-core kernel, 4 in one CTA
+// of 4 heads; 8, 12 or 16 on the tensor-core kernel (one CTA per kv-head, the heads
+// as MMA rows); more in CTAs of 4 heads of the CUDA-core kernel (the kv-head's K and V
+// are then read by G/4 CTAs side by side, the later reads mostly from L2)
 template <int D>
 cudaError_t launch_decode_d(const AttnArgs& A, int G, cudaStream_t st) {
     if (G == 1) return launch_decode<D, 1>(A, st);
     if (G == 2) return launch_decode<D, 2>(A, st);
-    if (G % 4 == 0) return launch_decode<D, 4>(A, st);
-    return cudaErrorInvalidValue;
+    if (G % 4 != 0) return cudaErrorInvalidValue;
+    if (G > 4 && G <= 16) return launch_decode_tc<D>(A, st);
+    return launch_decode<D, 4>(A, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -401,23 +820,6 @@ struct AttnPfArgs {
     int64_t n_slots;  // q tiles: N / TQ + n_seq + 1 slots (slot of tile c of sequence s: cu[s] / TQ + s + c)
     float scale_log2;  // scale * log2(e)
 };
-
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-        "[%5];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z, int w,
-                                            uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
-        "%5}], [%6];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
-        : "memory");
-}
 
 // all `count` threads of named barrier `id` agree on `pred` (logical and)
 __device__ __forceinline__ bool named_bar_and(int id, int count, bool pred) {
@@ -892,16 +1294,21 @@ cudaError_t launch_prefill_attn(const AttnPfJob& j, cudaStream_t st) {
 }  // namespace
 
 // Splits of the context: about kAttnCtas CTAs over all (sequence, kv-head,
-// head group) triples, each split at least 128 tokens (a multiple of 8);
-// shapes only, so the workspace is known without a device.
-constexpr int kAttnCtas = 1216;  // 8 waves of 152: short CTAs balance the load (fewer, longer ones measured slower)
+// head group) triples, each split at least 128 tokens (a multiple of 16);
+// shapes only, so the workspace is known without a device.  A head group is the
+// kv-head's G query heads, except for G > 16 (CTAs of 4 heads).  The tensor-core
+// kernel (G = 8, 12, 16) holds one CTA per SM and aims at kAttnCtasTc CTAs: its
+// fixed cost per CTA (Q, first copies, merge) made more, shorter CTAs slower.
+constexpr int kAttnCtas = 1216;   // 8 waves of 152: short CTAs balance the load (fewer, longer ones measured slower)
+constexpr int kAttnCtasTc = 152;  // one wave at one CTA per SM
 
 AttnPlan attn_plan(int B, int Hq, int Hkv, int max_seq_len) {
     AttnPlan p;
     const int G = Hq / Hkv;
-    const int64_t pairs = (int64_t)B * Hkv * (G >= 4 ? G / 4 : 1);
+    const int64_t pairs = (int64_t)B * Hkv * (G > 16 ? G / 4 : 1);
     const int max_tok = max_seq_len > 1 ? max_seq_len : 1;
-    int target = kAttnCtas;
+    const bool tc = G > 4 && G <= 16 && G % 4 == 0;
+    int target = tc ? kAttnCtasTc : kAttnCtas;
     if (const char* e = std::getenv("GDN_ATTN_CTAS")) {  // tuning override
         const int v = std::atoi(e);
         if (v >= 1 && v <= 1 << 20) target = v;
@@ -911,7 +1318,7 @@ AttnPlan attn_plan(int B, int Hq, int Hkv, int max_seq_len) {
     if (ns > max_ns) ns = max_ns;
     if (ns < 1) ns = 1;
     int span = (max_tok + ns - 1) / ns;
-    span = (span + kTJ - 1) / kTJ * kTJ;
+    span = (span + 15) / 16 * 16;
     ns = (max_tok + span - 1) / span;
     p.n_split = ns;
     p.span = span;

@@ -276,20 +276,24 @@ def test_attention_validation(lib):
 
 
 def test_attention_workspace_sizes(lib):
-    """Context splits of gdn_attn_decode: about 1216 CTAs over (sequence, kv-head, group of
-    up to 4 query heads), each split at least 128 tokens, a multiple of 8; the workspace
-    holds B x Hq x splits x (d + 2) fp32 (unnormalised o, maximum, sum) when splitting."""
+    """Context splits of gdn_attn_decode: about 1216 CTAs over (sequence, kv-head, head
+    group), each split at least 128 tokens, a multiple of 16; a head group is all G query
+    heads of the kv-head up to G = 16, groups of 4 beyond; G = 8, 12, 16 (the tensor-core
+    kernel, one CTA per SM) aim at 152 CTAs.  The workspace holds B x Hq x splits x
+    (d + 2) fp32 (unnormalised o, maximum, sum) when splitting."""
     def want(Hq, Hkv, D, B, max_seq):
         G = Hq // Hkv
-        pairs = B * Hkv * (G // 4 if G >= 4 else 1)
-        ns = min(-(-1216 // pairs), -(-max_seq // 128))
+        pairs = B * Hkv * (G // 4 if G > 16 else 1)
+        target = 152 if G in (8, 12, 16) else 1216
+        ns = min(-(-target // pairs), -(-max_seq // 128))
         ns = max(ns, 1)
         span = -(-max_seq // ns)
-        span = -(-span // 8) * 8
+        span = -(-span // 16) * 16
         ns = -(-max_seq // span)
         return B * Hq * ns * (D + 2) * 4 if ns > 1 else 0
 
     for Hq, Hkv, D, B, L in [(16, 4, 256, 1, 8193), (16, 4, 256, 64, 8193), (24, 2, 256, 4, 32769),
-                             (8, 8, 128, 200, 60), (4, 2, 128, 3, 129), (32, 4, 128, 16, 4000)]:
+                             (8, 8, 128, 200, 60), (4, 2, 128, 3, 129), (32, 4, 128, 16, 4000),
+                             (32, 2, 128, 1, 5000), (64, 8, 256, 3, 70000)]:
         c = gb.AttnConfig(Hq, Hkv, D, 16).c()
         assert lib.gdn_attn_workspace_size(ctypes.byref(c), B, L) == want(Hq, Hkv, D, B, L), (Hq, Hkv, D, B, L)

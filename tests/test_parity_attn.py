@@ -87,14 +87,22 @@ def test_attn_qwen35_4b_mixed_lengths_split():
 
 
 def test_attn_wide_gqa_large_pages():
-    """24 query heads over 2 kv-heads (G = 12, three CTAs of 4 heads per kv-head),
-    pages of 528 tokens."""
+    """24 query heads over 2 kv-heads (G = 12: the tensor-core kernel, all 12 heads of a
+    kv-head as MMA rows of one CTA), pages of 528 tokens."""
     run_case(24, 2, 256, 528, [5, 600, 1056, 2000], 2)
 
 
 @pytest.mark.parametrize("Hq,Hkv,D,page", [(8, 8, 128, 8), (4, 2, 128, 32), (32, 4, 128, 16)])
 def test_attn_small_groups_and_d128(Hq, Hkv, D, page):
     run_case(Hq, Hkv, D, page, [3, 64, 65, 0, 200], 3)
+
+
+@pytest.mark.parametrize("Hq,Hkv,D,page", [(16, 2, 128, 8), (32, 2, 256, 24), (24, 3, 128, 40)])
+def test_attn_wide_gqa_pages_of_8_rows(Hq, Hkv, D, page):
+    """The tensor-core kernel (G = 8, 16) on pages that are not a multiple of 16 tokens:
+    a group of 16 tokens is then two runs of 8 page rows, each loaded on its own, and
+    the runs of a group can sit on different pages."""
+    run_case(Hq, Hkv, D, page, [1, 8, 15, 16, 17, 100, 333, 1000], 6)
 
 
 def test_attn_many_sequences_no_split():
