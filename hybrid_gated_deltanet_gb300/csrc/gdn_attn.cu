@@ -388,8 +388,8 @@ PFN_cuTensorMapEncodeTiled_v12000 at_encode_fn();
 // once, so K and V are read once: the heads are the 16 rows (zero past G) of warp-level
 // bf16 MMAs (m16n8k16, fp32 accumulation).  The split's tokens come in groups of 16
 // and warp w takes groups w, w + 4, ... whole: S = Q K^T, an online softmax per row in
-// registers, O += P V over all d columns with P as the A operand straight from the
-// score accumulators.  Each warp fills its own ring of NSW stages (16 K rows, then 16
+// registers (its reference maximum moves in steps of at least 8), O += P V over all d
+// columns with P as the A operand straight from the score accumulators.  Each warp fills its own ring of NSW stages (16 K rows, then 16
 // V rows): a group is one or two runs of rows of a page (splits start on multiples of
 // 16 tokens, pages hold a multiple of 8), each run loaded by tensor TMA in boxes of
 // 64 columns with the 128-byte swizzle, so the 8-row fragment loads are free of bank
@@ -615,9 +615,14 @@ __global__ void __launch_bounds__(128, 1)
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
             mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
         }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const bool moved = __any_sync(0xffffffffu, mn0 != m0 || mn1 != m1);
-        const float a0 = (m0 == -INFINITY) ? 0.f : __expf(m0 - mn0), a1 = (m1 == -INFINITY) ? 0.f : __expf(m1 - mn1);
+        // the reference maximum of a row moves only when the row's maximum passes it by
+        // more than 8 (p then stays below e^8, well inside bf16 and fp32), so O is
+        // rescaled in few groups
+        const bool up0 = mx0 > m0 + 8.f, up1 = mx1 > m1 + 8.f;
+        const float mn0 = up0 ? mx0 : m0, mn1 = up1 ? mx1 : m1;
+        const bool moved = __any_sync(0xffffffffu, up0 || up1);
+        const float a0 = !up0 ? 1.f : (m0 == -INFINITY) ? 0.f : __expf(m0 - mn0);
+        const float a1 = !up1 ? 1.f : (m1 == -INFINITY) ? 0.f : __expf(m1 - mn1);
         auto ex = [](float v, float m) { return v == -INFINITY ? 0.f : __expf(v - m); };
         const float p00 = ex(v00, mn0), p01 = ex(v01, mn0), p02 = ex(v02, mn0), p03 = ex(v03, mn0);
         const float p10 = ex(v10, mn1), p11 = ex(v11, mn1), p12 = ex(v12, mn1), p13 = ex(v13, mn1);
@@ -631,7 +636,7 @@ __global__ void __launch_bounds__(128, 1)
         l1 = l1 * a1 + ps1;
         m0 = mn0;
         m1 = mn1;
-        if (moved) {  // a row's maximum grew somewhere in the warp: rescale O
+        if (moved) {  // a reference maximum moved somewhere in the warp: rescale O
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 o[n][0] *= a0;

@@ -91,12 +91,17 @@ struct Args {
     int c_lo, c_hi;      // k_chain16 runs chunks c_lo .. c_hi - 1 of each sequence
     int carry_in;        // k_chain16 starts from the state a previous segment left in s_final
     int prep_wait_end;   // k_prep16 ends with a wait for the grid before it in the stream
+    int32_t* ord;        // [n_seq] or null: chain row y runs sequence ord[y] (longest first)
 };
 
 size_t align1024(size_t x) { return (x + 1023) & ~(size_t)1023; }
 
+// Sequences a varlen call orders longest first for the chain (more are left in
+// their given order: the ranking is one CTA's O(n_seq^2) loop).
+constexpr int kOrdMax = 1024;
+
 struct Ws {
-    size_t kk, rec, total;
+    size_t kk, rec, ord, total;  // ord: 0 when there is no order region
     int64_t ncs;
 };
 
@@ -106,6 +111,11 @@ Ws ws_layout(const Geom& g, int64_t N, int n_seq) {
     L.kk = 0;
     L.rec = align1024((size_t)L.ncs * g.Hk * kK);
     L.total = align1024(L.rec + (size_t)L.ncs * g.Hv * kRec);
+    L.ord = 0;
+    if (n_seq > 1 && n_seq <= kOrdMax) {
+        L.ord = L.total;
+        L.total = align1024(L.ord + (size_t)n_seq * 4);
+    }
     return L;
 }
 
@@ -297,6 +307,20 @@ __global__ void __launch_bounds__(P_THREADS, P_CTAS_PER_SM) k_prep16(const __gri
     const int h = blockIdx.x;
     const int64_t cs = A.cs_lo + (int64_t)blockIdx.z * gridDim.y + blockIdx.y;
     if (cs >= A.ncs) return;
+    // Sequences longest first for the chain (one CTA per sequence and v-head, one
+    // per SM, so the longest should start first): rank by length, ties by index.
+    if (A.ord && cs == 0 && h == 0) {
+        const int ns = J.n_seq;
+        for (int i = threadIdx.x; i < ns; i += P_THREADS) {
+            const int li = J.cu_seqlens[i + 1] - J.cu_seqlens[i];
+            int rk = 0;
+            for (int k = 0; k < ns; ++k) {
+                const int lk = __ldg(J.cu_seqlens + k + 1) - __ldg(J.cu_seqlens + k);
+                rk += (lk > li || (lk == li && k < i)) ? 1 : 0;
+            }
+            A.ord[rk] = i;
+        }
+    }
     int sq, n;
     int64_t start, end, t0;
     if (!slot_chunk(J, cs, sq, start, end, t0, n)) return;  // a slot between two sequences' chunks
@@ -806,7 +830,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1) k_chain16(const __grid_constant
     const Geom& g = A.g;
     const PrefillJob& J = A.J;
     const int Hk = g.Hk, Hv = g.Hv;
-    const int j = blockIdx.x, seq = blockIdx.y, h = j / g.G;
+    const int j = blockIdx.x, seq = A.ord ? A.ord[blockIdx.y] : (int)blockIdx.y, h = j / g.G;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     griddep_launch_dependents();  // a following prep segment may start beside this grid
 
@@ -1269,6 +1293,7 @@ cudaError_t chunk16_launch(const Geom& g, const LayerParams& p, const PrefillJob
     A.c_hi = 1 << 30;
     A.carry_in = 0;
     A.prep_wait_end = 0;
+    A.ord = (L.ord && J.cu_seqlens) ? reinterpret_cast<int32_t*>(ws + L.ord) : nullptr;
     // One long sequence: its chain occupies one SM per v-head and leaves the rest of the
     // GPU idle while it walks the chunks.  The sequence is then cut into segments, all on
     // the caller's stream:  prep(0), chain(0), prep(1), chain(1), ...  Each chain segment
