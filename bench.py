@@ -21,7 +21,10 @@ follow: the wide-GVA one (16/48 heads, 10240 conv channels: a 4 x 32768-token
 varlen prefill and verify of r = 4 rows at 4 and 64 slots) under "wide_gva",
 and the serving mix (20 sequences of log-uniform length in [500, 30000] packed
 into one varlen prefill, then decode of 256 random slots of a 1024-slot pool)
-under "serving".
+under "serving", the decode step at B = 1, 4, 16 under "decode_small_batch",
+and the hybrid's attention layer (decode over paged K/V at 16/4 and 24/2 heads
+of 256, prefill at T = 8192, each with its fraction of the measured peak)
+under "attention".
 
 --impl reference times the CPU fp64 oracle (test infrastructure) on a bounded
 sample of the same workload; it is a deliberately slow reported baseline.
@@ -710,19 +713,25 @@ def attn_small_case(torch, device, steps, warmup):
     return {"case": "attn-small", "launches": 4 * (warmup + steps)}
 
 
-def attn_measure(torch, device, steps, warmup):
+ATTN_DECODE_CASES = ((16, 4, 256, 16, 1, 8192), (16, 4, 256, 16, 16, 8192), (16, 4, 256, 16, 64, 8192),
+                     (24, 2, 256, 528, 4, 32768))
+ATTN_PREFILL_CASES = ((16, 4, 256, 16, [(0, 8192)]), (16, 4, 256, 128, [(0, 8192)]),
+                      (16, 4, 256, 16, [(8192, 512)] * 4), (24, 2, 256, 528, [(0, 32768)]))
+
+
+def attn_measure(torch, device, steps, warmup, decode_cases=ATTN_DECODE_CASES, prefill_cases=ATTN_PREFILL_CASES):
     """Decode attention over a paged KV cache (timing only, N(0, 1) bf16 q, K, V
     drawn on the device): 16 query / 4 kv-heads of 256 with pages of 16 tokens at
     B = 1, 16, 64 sequences of 8192 cached tokens, and 24 / 2 heads with pages of
     528 tokens at B = 4 sequences of 32768.  Bytes: K and V of every cached
-    token read once, the new token's K and V written, q and o."""
+    token read once, the new token's K and V written, q and o.  Then prefill
+    attention (flops: 4 d Hq per (query, visible key) pair)."""
     from hybrid_gated_deltanet_gb300 import binding as gb
     out = []
     g = torch.Generator(device=device)
     g.manual_seed(11)
     bf = torch.bfloat16
-    for Hq, Hkv, D, page, B, L in ((16, 4, 256, 16, 1, 8192), (16, 4, 256, 16, 16, 8192), (16, 4, 256, 16, 64, 8192),
-                                   (24, 2, 256, 528, 4, 32768)):
+    for Hq, Hkv, D, page, B, L in decode_cases:
         cfg = gb.AttnConfig(Hq, Hkv, D, page)
         per = (L + 1 + page - 1) // page
         n_pages = B * per
@@ -760,8 +769,7 @@ def attn_measure(torch, device, steps, warmup):
                     "us": round(1e6 * t, 2), "gbs": round(nbytes / t / 1e9, 1)})
         del kp, vp
     # prefill: (cached, new) tokens per sequence; flops 4 d Hq per (query, visible key) pair
-    for Hq, Hkv, D, page, seqs in ((16, 4, 256, 16, [(0, 8192)]), (16, 4, 256, 128, [(0, 8192)]),
-                                   (16, 4, 256, 16, [(8192, 512)] * 4), (24, 2, 256, 528, [(0, 32768)])):
+    for Hq, Hkv, D, page, seqs in prefill_cases:
         cfg = gb.AttnConfig(Hq, Hkv, D, page)
         per = [(c + n + page - 1) // page for c, n in seqs]
         n_pages, max_pages = sum(per), max(per)
@@ -1274,6 +1282,17 @@ def gpu_arm(args):
             for rec in sb:
                 rec["frac"] = round(rec["gbs"] / peaks["hbm_gbs"], 4)
             extra["decode_small_batch"] = sb
+            # the hybrid's attention layer: decode at 16/4 heads (B = 64) and the wide
+            # 24/2 heads (B = 4 x 32768, the tensor-core kernel), prefill at T = 8192
+            att = attn_measure(torch, device, args.steps, 3,
+                               decode_cases=(ATTN_DECODE_CASES[2], ATTN_DECODE_CASES[3]),
+                               prefill_cases=(ATTN_PREFILL_CASES[0],))
+            for rec in att:
+                if rec["case"] == "attn":
+                    rec["frac_hbm"] = round(rec["gbs"] / peaks["hbm_gbs"], 4)
+                else:
+                    rec["frac_bf16"] = round(rec["tflops"] / peaks["bf16_tflops"], 4)
+            extra["attention"] = att
     t_dec = max_over_ranks(t_dec, world)
     e2e_t, h2d, d2h = time_decode_e2e(torch, cfg, layers, max(3, args.steps // 4), 3)
     e2e_t = max_over_ranks(e2e_t, world)
