@@ -46,13 +46,14 @@ struct RowsArgs {
     int NS;
 };
 
-// barrier over the 256 consumer threads only (named barrier 1), AND of a predicate
-__device__ __forceinline__ bool __syncthreads_and_consumers(bool pred) {
+// barrier over the 256 threads of one consumer group only (named barrier 1 + group),
+// AND of a predicate
+__device__ __forceinline__ bool __syncthreads_and_consumers(bool pred, int group) {
     uint32_t r;
     asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.and.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.and.pred q, %2, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
         : "=r"(r)
-        : "r"((uint32_t)pred)
+        : "r"((uint32_t)pred), "r"(1 + group)
         : "memory");
     return r != 0;
 }
@@ -469,17 +470,24 @@ __global__ void __launch_bounds__(kRowsThreads) k_rows(const __grid_constant__ R
 }
 
 // ---- persistent, pipelined decode (d = 128, one token per slot) ---------------
-// One CTA per SM walks a strided list of (slot, v-head) items.  Warp 8 is the
-// producer: it reads the item's slot index and gates, issues the bulk copies
-// of the item's 64 KB state tile and small inputs into one of 3 shared-memory
-// stages (up to 3 items ahead), and once the consumers are done with an item
-// writes its state back with one bulk store.  Warps 0..7 consume: conv +
-// SiLU + L2 norm + gates from shared memory, the row update with the
-// transposing butterfly, the gated RMSNorm and y.  The conv state is rolled
-// by a second, tiny launch after this one (stream order keeps every read of
-// it before the write), so CTAs never wait on each other.
+// One CTA per SM walks a strided list of (slot, k-head) units, each the G
+// (slot, v-head) items of that k-head.  Warp 16 is the producer: it reads an
+// item's slot index and gates, issues the bulk copies of its 64 KB state tile
+// and small inputs into one of 3 shared-memory stages (up to 3 items ahead),
+// and once the consumers are done with an item writes its state back with one
+// bulk store, and the rolled conv rows of its v channels (and, after the
+// unit's last item, of the k-head's q and k channels) from the stage.  Only
+// this CTA reads those conv rows, and it retires items in order, so every
+// read of the old rows has landed before they are overwritten: no second
+// launch and no wait between CTAs.  Two consumer groups of 8 warps (warps
+// 0..7, 8..15) take the CTA's items in turn, so that one group's serial
+// phases (conv + SiLU + L2 norm + gates from shared memory, the row update
+// with the transposing butterfly, the gated RMSNorm and y, with a group
+// barrier between them) overlap the other's.
 namespace pd {
-constexpr int D = 128, NCH = 3 * D, STAGES = 3, CONSUMERS = 256, THREADS = CONSUMERS + 32;
+constexpr int D = 128, NCH = 3 * D, STAGES = 3, GROUPS = 2, CONSUMERS = 256;
+constexpr int THREADS = GROUPS * CONSUMERS + 32;
+constexpr int SCRATCH = 3 * D + 64 + D + 16;  // floats per consumer group: q, k, v, partial sums, o, sum of o^2
 template <typename TA>
 struct Stage {
     static constexpr int E = sizeof(TA);
@@ -494,7 +502,7 @@ struct Stage {
 };
 template <typename TA>
 constexpr int smem_bytes() {
-    return STAGES * Stage<TA>::BYTES + 4 * STAGES * 8 /*mbarriers*/ + (3 * D + 64 + D + 16) * 4 + 128;
+    return STAGES * Stage<TA>::BYTES + 4 * STAGES * 8 /*mbarriers*/ + GROUPS * SCRATCH * 4 + 128;
 }
 }  // namespace pd
 
@@ -511,7 +519,17 @@ __global__ void __launch_bounds__(pd::THREADS, 1) k_decode_persist(const __grid_
     const bool raw = g.flags & kFlagRawQKV;
     const bool outnorm = !(g.flags & kFlagNoOutNorm);
     const bool direct = g.flags & kFlagGatesDirect;
-    const int n_items = J.B * Hv;
+    // Work units (sequence b, k-head h), strided over the CTAs; a unit is the G items
+    // (b, v-head h G + g), taken in turn.  A CTA owns every reader of the unit's q and k
+    // conv rows, so it rolls them itself once the unit's last item is done.
+    const int n_units = J.B * Hk;
+    const int my_units = (int)blockIdx.x < n_units ? (n_units - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    const int n_local = my_units * G;  // this CTA's items, k = 0 .. n_local - 1
+    auto item_of = [&](int kk, int& bb, int& jj) {
+        const int unit = (int)blockIdx.x + (kk / G) * (int)gridDim.x;
+        bb = unit / Hk;
+        jj = (unit % Hk) * G + kk % G;
+    };
 
     // programmatic dependent launch: this grid may be resident before the previous
     // kernel of the stream ends; every read below waits for it (and its memory)
@@ -522,7 +540,8 @@ __global__ void __launch_bounds__(pd::THREADS, 1) k_decode_persist(const __grid_
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * St::BYTES);
     uint64_t* fullS = full + STAGES;     // the state tile of the stage
     uint64_t* done = fullS + STAGES;     // consumers finished the stage's item
-    float* qs = reinterpret_cast<float*>(done + STAGES + STAGES);
+    const int group = warp / (CONSUMERS / 32) < GROUPS ? warp / (CONSUMERS / 32) : 0;
+    float* qs = reinterpret_cast<float*>(done + STAGES + STAGES) + group * SCRATCH;  // this group's scratch
     float* ks = qs + D;
     float* vs = ks + D;
     float* red = vs + D;
@@ -539,27 +558,45 @@ __global__ void __launch_bounds__(pd::THREADS, 1) k_decode_persist(const __grid_
     }
     __syncthreads();
 
-    if (warp == CONSUMERS / 32) {
+    if (warp == GROUPS * CONSUMERS / 32) {
         // ---------------- producer ----------------
         if (lane == 0) {
-            int k = 0;
-            for (int item = blockIdx.x; item < n_items + (int)gridDim.x * STAGES; item += gridDim.x, ++k) {
+            // the conv state: rows m = 0 .. K-2 become rows 1 .. K-2 and the new x (from the stage)
+            char* cpool = static_cast<char*>(J.conv_pool);
+            auto roll_part = [&](const unsigned char* sb, int slot, int part, int ch0) {
+                for (int m = 0; m < Km1; ++m) {
+                    const int src_row = m + 1;  // row of the window that becomes row m
+                    const unsigned char* src = src_row < Km1 ? sb + St::CV + (size_t)(src_row * NCH + part * D) * E
+                                                             : sb + St::X + (size_t)(part * D) * E;
+                    bulk_s2g(cpool + (((size_t)slot * Km1 + m) * C + ch0) * E, src, D * E);
+                }
+            };
+            for (int k = 0; k < n_local + STAGES; ++k) {
                 const int st = k % STAGES;
-                const int pitem = item - (int)gridDim.x * STAGES;  // the item that used this stage before
-                if (k >= STAGES && pitem < n_items) {               // retire it
+                const int pk = k - STAGES;  // the item that used this stage before
+                if (pk >= 0 && pk < n_local) {  // retire it
                     if (!mbar_wait(&done[st], ((k / STAGES) - 1) & 1)) report_device_status(kDevWaitTimeout);
                     unsigned char* sb = smem + st * St::BYTES;
                     const int* hdr = reinterpret_cast<const int*>(sb + St::HDR);
-                    if (hdr[2] >= 0) {  // state back in place
-                        const int pj = pitem % Hv;
+                    if (hdr[2] >= 0) {  // state back in place, conv rows rolled
+                        int pb, pj;
+                        item_of(pk, pb, pj);
+                        const int ph = pj / G;
                         bulk_s2g(J.state_pool + ((size_t)hdr[2] * Hv + pj) * D * D, sb + St::S, D * D * 4);
+                        roll_part(sb, hdr[2], 2, 2 * Hk * D + pj * D);  // the item's own v channels
+                        if (pk % G == G - 1) {  // the unit's last item: every reader of its q, k rows is done
+                            roll_part(sb, hdr[2], 0, ph * D);
+                            roll_part(sb, hdr[2], 1, Hk * D + ph * D);
+                        }
                         bulk_commit();
                     }
                     bulk_wait_read_all();  // the stage may be refilled
                 }
-                if (item >= n_items) continue;
+                if (k >= n_local) continue;
                 unsigned char* sb = smem + st * St::BYTES;
-                const int bb = item / Hv, j = item % Hv, h = j / G;
+                int bb, j;
+                item_of(k, bb, j);
+                const int h = j / G;
                 const int slot = J.slot_idx[bb];
                 const bool valid = slot >= 0 && slot < J.n_slots;
                 int* hdr = reinterpret_cast<int*>(sb + St::HDR);
@@ -607,10 +644,10 @@ __global__ void __launch_bounds__(pd::THREADS, 1) k_decode_persist(const __grid_
         return;
     }
 
-    // ---------------- consumers (warps 0..7) ----------------
+    // ---------------- consumers (group g: warps 8g .. 8g + 7, items k = g, g + 2, ...) ----------------
     const int col4 = lane;  // D = 128: a warp covers one row, 4 floats per lane
-    int k = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
+    const int gtid = tid - group * CONSUMERS, gwarp = gtid >> 5;
+    for (int k = group; k < n_local; k += GROUPS) {
         const int st = k % STAGES;
         const uint32_t par = (k / STAGES) & 1;
         unsigned char* sb = smem + st * St::BYTES;
@@ -620,13 +657,15 @@ __global__ void __launch_bounds__(pd::THREADS, 1) k_decode_persist(const __grid_
         const TA* zs = reinterpret_cast<const TA*>(sb + St::Z);
         const TA* nw = reinterpret_cast<const TA*>(sb + St::NW);
         float* Sb = reinterpret_cast<float*>(sb + St::S);
-        const int bb = item / Hv, j = item % Hv, h = j / G;
+        int bb, j;
+        item_of(k, bb, j);
+        const int h = j / G;
         bool ok = true;
-        if (warp == 0) {
+        if (gwarp == 0) {
             ok = mbar_wait(&full[st], par);
             if (!ok) mbar_wait(&full[st], par);
         }
-        ok = __syncthreads_and_consumers(ok);
+        ok = __syncthreads_and_consumers(ok, group);
         const int* hdr = reinterpret_cast<const int*>(sb + St::HDR);
         const float* hfl = reinterpret_cast<const float*>(sb + St::HDR);
         const bool valid = hdr[2] >= 0;
@@ -643,31 +682,33 @@ __global__ void __launch_bounds__(pd::THREADS, 1) k_decode_persist(const __grid_
             return siluf_(c);
         };
         float sq = 0.f, sk = 0.f, sqk = 0.f;
-        if (ok && valid) {
-            for (int c = tid; c < D; c += CONSUMERS) {
+        if (ok && valid) {  // threads 0..127: channel c of q and k; 128..255: channel c of v
+            const int c = gtid & (D - 1);
+            if (gtid < D) {
                 const float qv = conv(c), kv = conv(D + c);
                 qs[c] = qv;
                 ks[c] = kv;
                 sq = fmaf(qv, qv, sq);
                 sk = fmaf(kv, kv, sk);
                 sqk = fmaf(qv, kv, sqk);
+            } else {
+                vs[c] = conv(2 * D + c);
             }
-            for (int c = tid; c < D; c += CONSUMERS) vs[c] = conv(2 * D + c);
         }
         sq = warp_sum(sq);
         sk = warp_sum(sk);
         sqk = warp_sum(sqk);
         if (lane == 0) {
-            red[warp * 4 + 0] = sq;
-            red[warp * 4 + 1] = sk;
-            red[warp * 4 + 2] = sqk;
+            red[gwarp * 4 + 0] = sq;
+            red[gwarp * 4 + 1] = sk;
+            red[gwarp * 4 + 2] = sqk;
         }
         bool s_ok = true;
-        if (warp == 0 && ok) {
+        if (gwarp == 0 && ok) {
             s_ok = mbar_wait(&fullS[st], par);
             if (!s_ok) mbar_wait(&fullS[st], par);
         }
-        ok = __syncthreads_and_consumers(ok && s_ok);
+        ok = __syncthreads_and_consumers(ok && s_ok, group);
         if (ok && valid) {
             sq = sk = sqk = 0.f;
             for (int w = 0; w < CONSUMERS / 32; ++w) {
@@ -694,7 +735,7 @@ __global__ void __launch_bounds__(pd::THREADS, 1) k_decode_persist(const __grid_
                 kr[e] = ks[col4 * 4 + e] * rk;
                 qr[e] = qs[col4 * 4 + e] * rq;
             }
-            for (int rb = warp * 8; rb < D; rb += 8 * (CONSUMERS / 32)) {
+            for (int rb = gwarp * 8; rb < D; rb += 8 * (CONSUMERS / 32)) {
                 float4 sv[8];
                 float v[16];
 #pragma unroll
@@ -739,25 +780,25 @@ __global__ void __launch_bounds__(pd::THREADS, 1) k_decode_persist(const __grid_
             }
         }
         fence_proxy_async_smem();  // the state tile goes out through the async proxy
-        __syncthreads_and_consumers(true);
+        __syncthreads_and_consumers(true, group);
         if (ok && valid) {
             // output gated RMSNorm over the whole v-head
-            if (warp == 0) {
+            if (gwarp == 0) {
                 float ss = 0.f;
                 for (int rr = lane; rr < D; rr += 32) ss = fmaf(obuf[rr], obuf[rr], ss);
                 ss = warp_sum(ss);
                 if (lane == 0) ssp[0] = ss;
             }
-            __syncthreads_and_consumers(true);
-            for (int rr = tid; rr < D; rr += CONSUMERS) {
+            __syncthreads_and_consumers(true, group);
+            for (int rr = gtid; rr < D; rr += CONSUMERS) {
                 float yv = obuf[rr];
                 if (outnorm) yv = yv * rsqrtf(ssp[0] / (float)D + g.norm_eps) * L::ld(nw, rr) * siluf_(L::ld(zs, rr));
                 L::st(J.y, ((size_t)bb * Hv + j) * D + rr, yv);
             }
         }
-        if (!ok && tid == 0) report_device_status(kDevWaitTimeout);
-        __syncthreads_and_consumers(true);  // qs/ks/vs/obuf/red reused by the next item; stage fully read
-        if (tid == 0) mbar_arrive(&done[st]);  // the producer may store and refill the stage
+        if (!ok && gtid == 0) report_device_status(kDevWaitTimeout);
+        __syncthreads_and_consumers(true, group);  // qs/ks/vs/obuf/red reused by the next item; stage fully read
+        if (gtid == 0) mbar_arrive(&done[st]);  // the producer may store and refill the stage
     }
 }
 
@@ -847,36 +888,6 @@ __global__ void k_conv_roll(const Geom g, const ConvJob J) {
     }
 }
 
-// The same roll 16 bytes of channels per thread (x and the conv pool 16-byte
-// aligned, as the decode step requires): raw inputs move bit for bit.
-template <typename TA>
-__global__ void k_conv_roll_v(const Geom g, const ConvJob J) {
-    griddep_wait();  // the decode kernel before it has read every old conv row
-    griddep_launch_dependents();
-    constexpr int VEC = 16 / (int)sizeof(TA);
-    const int C = g.C_ch, Km1 = g.K - 1, CV = C / VEC;
-    const size_t total = (size_t)J.n_seq * CV;
-    const TA* x = static_cast<const TA*>(J.x);
-    TA* cp = static_cast<TA*>(J.conv_pool);
-    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < total;
-         idx += (size_t)gridDim.x * blockDim.x) {
-        const int ch = (int)(idx % CV) * VEC, sq = (int)(idx / CV);
-        const int slot = J.slot_idx[sq];
-        if (slot < 0 || slot >= J.n_slots) continue;
-        uint4 old[3];
-#pragma unroll
-        for (int m = 0; m < 3; ++m)
-            if (m < Km1) old[m] = *reinterpret_cast<const uint4*>(cp + ((size_t)slot * Km1 + m) * C + ch);
-#pragma unroll
-        for (int m = 0; m < 3; ++m) {
-            if (m >= Km1) break;
-            const int pidx = J.n_tok + m;
-            const uint4 v = pidx < Km1 ? old[pidx < 3 ? pidx : 0]
-                                       : *reinterpret_cast<const uint4*>(x + ((size_t)sq * J.n_tok + (pidx - Km1)) * C + ch);
-            *reinterpret_cast<uint4*>(cp + ((size_t)slot * Km1 + m) * C + ch) = v;
-        }
-    }
-}
 
 // ---- commit by copy -----------------------------------------------------------
 __global__ void k_commit(const Geom g, const CommitJob J, int elt_bytes) {
@@ -902,49 +913,40 @@ __global__ void k_commit(const Geom g, const CommitJob J, int elt_bytes) {
 template <typename TA>
 cudaError_t launch_decode_persist(const Geom& g, const LayerParams& p, const RowsJob& job, cudaStream_t st) {
     constexpr int smem = pd::smem_bytes<TA>();
+    static_assert(smem <= 227 * 1024, "persistent decode: shared memory");
     static std::atomic<uint64_t> smem_set{0};
     {
         const cudaError_t e = raise_smem_limit(k_decode_persist<TA>, smem, smem_set);
         if (e != cudaSuccess) return e;
     }
     const int sms = sm_count();
-    const int items = job.B * g.Hv;
+    const int units = job.B * g.Hk;
     RowsArgs A{g, p, job, 1};
-    // both kernels go out with programmatic stream serialization: each may be
-    // scheduled while its predecessor finishes and waits for it (griddep_wait)
-    // before its first access to memory, which hides the launch gaps
+    // programmatic stream serialization: the grid may be scheduled while its
+    // predecessor finishes and waits for it (griddep_wait) before its first access
+    // to memory, which hides the launch gap
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)std::min(items, sms));
+    cfg.gridDim = dim3((unsigned)std::min(units, sms));
     cfg.blockDim = dim3(pd::THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_decode_persist<TA>, A);
-    if (e != cudaSuccess) return e;
-    // roll the conv state (raw inputs) after every read of it above
-    ConvJob cj{job.x, job.conv_pool, job.slot_idx, nullptr, job.B, 1, job.n_slots};
-    const size_t total = (size_t)job.B * g.C_ch / (16 / sizeof(TA));
-    const int blocks = (int)std::min<size_t>((total + 255) / 256, (size_t)sms * 8);
-    cfg.gridDim = dim3((unsigned)blocks);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
-    return cudaLaunchKernelEx(&cfg, k_conv_roll_v<TA>, g, cj);
+    return cudaLaunchKernelEx(&cfg, k_decode_persist<TA>, A);
 }
 
 cudaError_t launch_rows(const Geom& g, const LayerParams& p, const RowsJob& job, cudaStream_t st) {
     if (job.B == 0) return cudaSuccess;
     // the persistent pipelined kernel pays off once every SM has several
     // (slot, v-head) items to overlap (measured: B = 64 and 256 at the 4B
-    // geometry gain 18% / 26%; B <= 16 is faster with one CTA per item)
-    if (g.D == 128 && job.r == 1 && !job.snap_idx && job.mode == 0 && std::getenv("GDN_DECODE_CLUSTERED") == nullptr &&
-        std::getenv("GDN_DECODE_SLICES") == nullptr) {
-        if ((long)job.B * g.Hv >= 4L * sm_count())
-            return g.act_bf16 ? launch_decode_persist<__nv_bfloat16>(g, p, job, st)
-                              : launch_decode_persist<float>(g, p, job, st);
+    // geometry gain 18% / 26%; B <= 16 is faster with one CTA per item).  Its
+    // three stages fit in shared memory with bf16 inputs only.
+    if (g.D == 128 && g.act_bf16 && job.r == 1 && !job.snap_idx && job.mode == 0 &&
+        std::getenv("GDN_DECODE_CLUSTERED") == nullptr && std::getenv("GDN_DECODE_SLICES") == nullptr) {
+        if ((long)job.B * g.Hv >= 4L * sm_count()) return launch_decode_persist<__nv_bfloat16>(g, p, job, st);
     }
     if (g.act_bf16) {
         switch (g.D) {

@@ -31,9 +31,8 @@ def _oracle_slot(geom, p, tok, S, CS, slot, rows, heads=None, **kw):
                                s0=S.f64[slot], conv0=CS.f64[slot], heads=heads, **oracle_kwargs(p), **kw)
 
 
-@pytest.mark.parametrize("B", [1, 4, 16, 64])
-def test_decode_step_qwen35_4b(B):
-    geom, act, p, tok, S, CS, slots = _pool_case("decode4b", B, stream=B)
+def _check_decode_step(B, stream, act=None):
+    geom, act, p, tok, S, CS, slots = _pool_case("decode4b", B, stream=stream, act=act)
     cfg = config(geom, act)
     sp = dev(S)
     cp = dev(CS)
@@ -54,6 +53,17 @@ def test_decode_step_qwen35_4b(B):
     np.testing.assert_array_equal(s_got[untouched], S.f64[untouched])
     np.testing.assert_array_equal(c_got[untouched], CS.f64[untouched])
     assert gb.gdn_device_status() == 0  # no bounded wait gave up
+
+
+@pytest.mark.parametrize("B", [1, 4, 16, 64])
+def test_decode_step_qwen35_4b(B):
+    _check_decode_step(B, stream=B)
+
+
+def test_decode_step_fp32_activations_at_a_persistent_batch():
+    """fp32 activations at B = 24 (768 slot-heads: a batch that bf16 activations run on the
+    persistent kernel, whose three stages of fp32 inputs would not fit in shared memory)."""
+    _check_decode_step(24, stream=24, act=synth.F32)
 
 
 @pytest.mark.parametrize("slices", ["1", "2", "4"])
