@@ -938,15 +938,45 @@ cudaError_t launch_decode_persist(const Geom& g, const LayerParams& p, const Row
     return cudaLaunchKernelEx(&cfg, k_decode_persist<TA>, A);
 }
 
+// CTAs of k_rows<128, TA> resident per SM in a decode step (cached per device)
+template <typename TA>
+int rows_ctas_per_sm(const Geom& g) {
+    static std::atomic<int> cache[64];  // static storage: zero, i.e. not yet queried
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::atomic<int>& c = cache[dev & 63];
+    int n = c.load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    static std::atomic<uint64_t> smem_set{0};
+    if (raise_smem_limit(k_rows<128, TA>, 200 * 1024, smem_set) != cudaSuccess) return 1;
+    const RowsSmem lay = rows_smem(128, 128, 1, g.K, (int)sizeof(TA));
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_rows<128, TA>, kRowsThreads, (size_t)lay.total) !=
+            cudaSuccess ||
+        n <= 0)
+        n = 1;
+    c.store(n, std::memory_order_relaxed);
+    return n;
+}
+
 cudaError_t launch_rows(const Geom& g, const LayerParams& p, const RowsJob& job, cudaStream_t st) {
     if (job.B == 0) return cudaSuccess;
-    // the persistent pipelined kernel pays off once every SM has several
-    // (slot, v-head) items to overlap (measured: B = 64 and 256 at the 4B
-    // geometry gain 18% / 26%; B <= 16 is faster with one CTA per item).  Its
-    // three stages fit in shared memory with bf16 inputs only.
+    // A decode step runs on the persistent kernel (three stages in shared memory: bf16
+    // inputs only) or on k_rows (one CTA per item).  Measured at the 4B geometry,
+    // us per layer call, k_rows / persistent: B = 1: 7.4 / 9.3; 4: 8.9 / 10.6;
+    // 6: 11.3 / 11.0; 8: 13.9 / 11.9; 10: 14.9 / 16.1; 12: 15.5 / 16.5;
+    // 16: 22.4 / 17.2; 64: - / 47.7.  The persistent kernel costs about one item's
+    // chain per (slot, k-head) unit a CTA holds; k_rows about one chain per wave.  So:
+    // k_rows for about one item per SM or fewer, the persistent kernel while a CTA
+    // holds one unit, k_rows while its CTAs fit in one wave, the persistent kernel
+    // beyond.
     if (g.D == 128 && g.act_bf16 && job.r == 1 && !job.snap_idx && job.mode == 0 &&
         std::getenv("GDN_DECODE_CLUSTERED") == nullptr && std::getenv("GDN_DECODE_SLICES") == nullptr) {
-        if ((long)job.B * g.Hv >= 4L * sm_count()) return launch_decode_persist<__nv_bfloat16>(g, p, job, st);
+        const long items = (long)job.B * g.Hv, units = (long)job.B * g.Hk, sms = sm_count();
+        bool persist;
+        if (items * 4 <= sms * 5) persist = false;
+        else if (units <= sms) persist = true;
+        else persist = items > (long)rows_ctas_per_sm<__nv_bfloat16>(g) * sms;
+        if (persist) return launch_decode_persist<__nv_bfloat16>(g, p, job, st);
     }
     if (g.act_bf16) {
         switch (g.D) {
