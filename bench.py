@@ -302,14 +302,17 @@ def time_decode(torch, cfg, layers, steps, warmup, use_graph=True, per_step=None
     return evs[0].elapsed_time(evs[-1]) / 1e3  # seconds
 
 
-def time_decode_e2e(torch, cfg, layers, steps, warmup):
+def time_decode_e2e(torch, cfg, layers, steps, warmup, graph=False):
     """Same step through the public API, with each step's inputs copied in from
     pinned host memory and its outputs copied back, inside the timed region.
     Three streams pipeline it: layer l's inputs are copied in on a copy stream
     once the previous step's kernel for layer l has read its buffers, layer l
     runs on the compute stream once its inputs have landed and its previous y
     has been read out, and y goes back on a third stream.  The timed region
-    ends after the last read-back."""
+    ends after the last read-back.  With graph=True one step (its 24 copies in,
+    24 API calls and 24 read-backs, on the same three streams) is captured as a
+    CUDA graph, as the device-timed step is, and replayed once per step: the
+    host-side cost of the eager calls leaves the timed region, the copies stay."""
     from hybrid_gated_deltanet_gb300 import binding as gb
     stream = _side_stream(torch)
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
@@ -356,14 +359,53 @@ def time_decode_e2e(torch, cfg, layers, steps, warmup):
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
+    if graph:
+        # Replays are serialized, so inside one step no buffer is reused: the kernels
+        # wait only for their inputs.  The copies in run ahead on their own stream, in
+        # layer order (about 10 us per layer's 1.6 MB here, against about 48 us per
+        # layer's kernel), so a wait for copy i covers every layer up to i: layer 0
+        # waits for its own, layer 1 for the copies up to layer 4, layer 5 for the
+        # last one.  Every other kernel follows its predecessor without a wait, which
+        # keeps the programmatic launch (a wait in front of a kernel costs about 4 us).
+        ev_fork = torch.cuda.Event()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            ev_fork.record(stream)  # the side streams join the capture here
+            s_in.wait_event(ev_fork)
+            s_out.wait_event(ev_fork)
+            with torch.cuda.stream(s_in):
+                for l, (dbuf, v, hbuf) in enumerate(packs):
+                    dbuf.copy_(hbuf, non_blocking=True)
+                    e_in[l].record(s_in)
+            waits = {0: 0, 1: min(4, n - 1), 5: n - 1}  # kernel of layer l: wait for copies up to layer i
+            for l, (L, (dbuf, v, hbuf), ho) in enumerate(zip(layers, packs, hout)):
+                if l in waits:
+                    stream.wait_event(e_in[waits[l]])
+                gb.gdn_decode_step(cfg, L["prm"], v["x"], v["z"], v["a"], v["b"], L["C"], L["S"], L["slots"],
+                                   L["y"], stream=stream)
+                e_k[l].record(stream)
+                s_out.wait_event(e_k[l])
+                with torch.cuda.stream(s_out):
+                    ho.copy_(L["y"], non_blocking=True)
+            e_out[n - 1].record(s_out)
+            stream.wait_event(e_in[n - 1])  # rejoin: every copy of the step is in the graph
+            stream.wait_event(e_out[n - 1])
+        with torch.cuda.stream(stream):  # a graph replays on the current stream
+            for _ in range(warmup):
+                g.replay()
+        torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     s_in.wait_event(ev0)
     for _ in range(steps):
-        step()
-    stream.wait_event(e_out[n - 1])  # every read-back of the last step precedes the end mark
-    for l in range(n):
-        stream.wait_event(e_out[l])
+        if graph:
+            with torch.cuda.stream(stream):  # a graph replays on the current stream
+                g.replay()
+        else:
+            step()
+    if not graph:  # (a replayed graph ends with its streams joined: the read-backs are in it)
+        for l in range(n):  # every read-back of the last step precedes the end mark
+            stream.wait_event(e_out[l])
     ev1.record(stream)
     ev1.synchronize()
     return ev0.elapsed_time(ev1) / 1e3, h2d, d2h
@@ -1294,9 +1336,11 @@ def gpu_arm(args):
                     rec["frac_bf16"] = round(rec["tflops"] / peaks["bf16_tflops"], 4)
             extra["attention"] = att
     t_dec = max_over_ranks(t_dec, world)
-    e2e_t, h2d, d2h = time_decode_e2e(torch, cfg, layers, max(3, args.steps // 4), 3)
-    e2e_t = max_over_ranks(e2e_t, world)
     e2e_steps = max(3, args.steps // 4)
+    e2e_t, h2d, d2h = time_decode_e2e(torch, cfg, layers, e2e_steps, 3, graph=not args.no_graph)
+    e2e_t = max_over_ranks(e2e_t, world)
+    e2e_eager_t, _, _ = time_decode_e2e(torch, cfg, layers, e2e_steps, 3, graph=False)
+    e2e_eager_t = max_over_ranks(e2e_eager_t, world)
 
     step_bytes = N_LAYERS * (B * SLOT_BYTES + PARAM_BYTES)
     value = world * step_bytes * args.steps / t_dec / 1e9
@@ -1358,7 +1402,9 @@ def gpu_arm(args):
         "cpu_baseline": cpu_base,
         "e2e": {"value": round(world * step_bytes * e2e_steps / e2e_t / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(1e3 * e2e_t / e2e_steps, 4)},
+                "ms_per_step": round(1e3 * e2e_t / e2e_steps, 4), "graph": not args.no_graph,
+                "eager": {"value": round(world * step_bytes * e2e_steps / e2e_eager_t / 1e9, 2),
+                          "ms_per_step": round(1e3 * e2e_eager_t / e2e_steps, 4)}},
         "gpu_launches": args.steps * N_LAYERS,  # per layer: the persistent decode kernel
         "clocks": clocks,
     }
