@@ -387,7 +387,9 @@ typedef struct gdn_attn_config {
  *   workspace: gdn_attn_workspace_size(cfg, B, max_seq_len) bytes (the
  *   partial results of the context splits; NULL when 0).
  *   All pointers 16-byte aligned.  bf16 in, fp32 softmax and accumulation,
- *   bf16 out. */
+ *   bf16 out.  With G = 8, 12 or 16 the two products run on the tensor cores:
+ *   q scale is rounded to bf16 before Q K^T and the softmax weights to bf16
+ *   before P V (fp32 accumulation in both). */
 gdn_status gdn_attn_decode(const gdn_attn_config* cfg, const void* q, const void* k_new,
                            const void* v_new, void* k_pool, void* v_pool,
                            const int32_t* block_table, const int32_t* seq_lens, int32_t B,

@@ -4,7 +4,10 @@ pages.  Tolerance: q, K, V are bf16 and exact in both; the kernel scores and
 accumulates in fp32 (errors near 1e-6 relative) and rounds o to bf16 (at most
 2^-8 relative per element, 2^-8/sqrt(3) in the root mean square), so the
 relative Frobenius error of o is held to 4e-3, and each element to
-2^-8 |ref| + 1e-3 max|V|."""
+2^-8 |ref| + 1e-3 max|V|.  The tensor-core path (G = 8, 12, 16) also rounds
+q scale and the softmax weights to bf16 (2^-9 relative each, unbiased): a score
+then moves by at most 2^-9 of sum |q_i k_i|, and a weight by 2^-9 of itself,
+both well inside the same bounds at these value ranges."""
 import math
 
 import numpy as np
