@@ -230,6 +230,24 @@ def test_projection_workspace_sizes(lib):
     assert lib.gdn_proj_workspace_size(256, 2560, 4096) == 20 * 7 * 256 * 128 * 4
 
 
+def test_varlen_prefill_workspace_holds_the_sequence_order(lib):
+    """A varlen prefill of 2 to 1024 sequences adds one int32 per sequence (the chain's
+    longest-first order) after the chunk records, in its own 1024-byte-aligned region;
+    one sequence, or more than 1024, adds nothing."""
+    cfg = _cfg()
+    up = lambda v: (v + 1023) // 1024 * 1024
+
+    def records(n, n_seq):
+        slots = n // 64 + n_seq + 1
+        return up(up(slots * 16 * 16384) + slots * 32 * (32768 + 16384 + 16384 + 512))
+
+    for n, n_seq in [(8192, 1), (8192, 2), (5000, 20), (70000, 1024), (70000, 1025), (300, 3)]:
+        want = records(n, n_seq)
+        if 1 < n_seq <= 1024:
+            want = up(want + 4 * n_seq)
+        assert lib.gdn_workspace_size(ctypes.byref(cfg), gb.OP_VARLEN_PREFILL, n, n_seq) == want, (n, n_seq)
+
+
 def test_layer_workspace_sizes(lib):
     """x [n][8192], z [n][4096], a, b [n][32], y [n][4096] in bf16, then the larger of
     the two projections' partial sums, each region rounded up to 256 bytes; a layer
