@@ -189,7 +189,7 @@ def test_prefill_empty_sequence_keeps_state():
     np.testing.assert_array_equal(host(c_fin), C0.f64[0])
 
 
-@pytest.mark.parametrize("T", [45 * 64, 4096 + 37])  # 3 and 4 segments of at most 22 chunks
+@pytest.mark.parametrize("T", [45 * 64, 4096 + 37])  # 45 and 65 chunks: 3 segments each
 def test_segmented_single_sequence_is_bitwise_one_chain(T):
     """A long single sequence runs as segments (the prep of the next segment beside the
     chain of this one, the state handed over in s_final); a one-sequence varlen call of
