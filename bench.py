@@ -639,7 +639,8 @@ def profile_case(args):
                           "gbs": round((B * SLOT_BYTES + PARAM_BYTES) / us / 1e3, 1),
                           "slices": os.environ.get("GDN_DECODE_SLICES", "auto")}))
     elif args.case == "decode-batches":
-        for rec in small_batch_decode(torch, device, args.steps, args.warmup):
+        batches = tuple(int(v) for v in args.batches.split(","))
+        for rec in small_batch_decode(torch, device, args.steps, args.warmup, batches=batches):
             print(json.dumps(dict(rec, slices=os.environ.get("GDN_DECODE_SLICES", "auto"),
                                   clustered=os.environ.get("GDN_DECODE_CLUSTERED", "auto"))))
     elif args.case == "serving":
@@ -1445,6 +1446,7 @@ def main():
     ap.add_argument("--impl", default="gdn", choices=["gdn", "reference"])
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--batch", type=int, default=64, help="slots of the decode-small case")
+    ap.add_argument("--batches", default="1,4,16", help="slot counts of the decode-batches case")
     ap.add_argument("--case", default="full", choices=["full", "decode-small", "decode-batches", "prefill-small",
                              "prefill-varlen", "serving",
                              "verify", "ckpt", "layer",
