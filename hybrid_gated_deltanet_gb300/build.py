@@ -7,6 +7,7 @@ CUDA runtime linked statically.  Usage: ``python -m hybrid_gated_deltanet_gb300.
 from __future__ import annotations
 
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -41,8 +42,26 @@ def _newest_input() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
+# ELF e_machine of the host, so that a library built on another architecture is never taken as current.
+_ELF_MACHINE = {"x86_64": 62, "amd64": 62, "aarch64": 183, "arm64": 183}
+
+
+def _built_here(path: str) -> bool:
+    want = _ELF_MACHINE.get(platform.machine().lower())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    if len(head) < 20 or head[:4] != b"\x7fELF":
+        return False
+    return want is None or int.from_bytes(head[18:20], "little") == want
+
+
 def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
+    """Compile and link libgdn.so; skipped when the library exists, was built for this
+    host's architecture and is newer than every source, header and this script."""
+    if not force and os.path.exists(LIB) and _built_here(LIB) and os.path.getmtime(LIB) >= _newest_input():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()

@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 from concurrent.futures import ThreadPoolExecutor
@@ -49,9 +50,24 @@ class OracleGeom(ctypes.Structure):
     ]
 
 
+def _native(path: str) -> bool:
+    """True if the shared object at `path` is an ELF file for this host's machine type."""
+    machine = {"x86_64": 62, "amd64": 62, "aarch64": 183, "arm64": 183}.get(platform.machine().lower())
+    try:
+        with open(path, "rb") as f:
+            head = f.read(20)
+    except OSError:
+        return False
+    if len(head) < 20 or head[:4] != b"\x7fELF":
+        return False
+    return machine is None or int.from_bytes(head[18:20], "little") == machine
+
+
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (plain -O2, no fast-math)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    """Compile the oracle with gcc (plain -O2, no fast-math), unless a library for this
+    host's architecture, newer than the source, is already there."""
+    if (force or not os.path.exists(_LIB) or not _native(_LIB)
+            or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.run(["gcc", "-O2", "-std=c11", "-Wall", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"],
                        check=True)

@@ -315,3 +315,36 @@ def test_attention_workspace_sizes(lib):
                              (32, 2, 128, 1, 5000), (64, 8, 256, 3, 70000)]:
         c = gb.AttnConfig(Hq, Hkv, D, 16).c()
         assert lib.gdn_attn_workspace_size(ctypes.byref(c), B, L) == want(Hq, Hkv, D, B, L), (Hq, Hkv, D, B, L)
+
+
+def _oracle_check(path):
+    import oracle
+    return oracle._native(path)
+
+
+@pytest.mark.parametrize("check, built", [(gbuild._built_here, gbuild.LIB), (_oracle_check, None)],
+                         ids=["libgdn", "oracle"])
+def test_build_rejects_a_library_of_another_architecture(tmp_path, check, built):
+    """A shared library carried over from a machine of another architecture is rebuilt, not
+    loaded: each up-to-date check reads the ELF machine field as well as the times."""
+    import platform
+    here = {"x86_64": 62, "amd64": 62, "aarch64": 183, "arm64": 183}.get(platform.machine().lower())
+    if here is None:
+        pytest.skip("host architecture without a known ELF machine number")
+    other = 183 if here == 62 else 62
+
+    def elf(machine):
+        head = bytearray(64)
+        head[:4] = b"\x7fELF"
+        head[4], head[5] = 2, 1  # 64-bit, little-endian
+        head[18:20] = machine.to_bytes(2, "little")
+        return bytes(head)
+
+    for name, data, want in (("native.so", elf(here), True), ("foreign.so", elf(other), False),
+                             ("text.so", b"not an ELF file at all....", False), ("short.so", b"\x7fELF", False)):
+        path = tmp_path / name
+        path.write_bytes(data)
+        assert check(str(path)) is want, name
+    assert check(str(tmp_path / "missing.so")) is False
+    if built is not None:
+        assert check(built)
